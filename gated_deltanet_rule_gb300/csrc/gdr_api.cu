@@ -1,0 +1,275 @@
+// C ABI of libgdr: host-side argument checks, dispatch to the kernels, the sticky device error
+// word, and the stage timer. Every check runs before any CUDA call, so a rejected call never
+// touches the GPU.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "gdr.h"
+#include "gdr_internal.h"
+
+namespace gdr {
+
+__device__ int g_error_word;   // first device-side error wins (atomicCAS from 0)
+
+namespace {
+
+thread_local std::string t_msg;
+
+gdr_status fail(gdr_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_msg = buf;
+  return st;
+}
+
+gdr_status ok() {
+  t_msg.clear();
+  return GDR_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+std::mutex g_err_mu;
+int* g_err_ptr[128] = {};
+
+// Stage timer: one (start, end) event pair per recorded launch.
+struct StageTimer {
+  std::mutex mu;
+  bool on = false;
+  int cap = 0;
+  int used = 0;
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> id;
+} g_timer;
+
+int timer_begin(cudaStream_t s, int kid) {
+  std::lock_guard<std::mutex> lk(g_timer.mu);
+  if (!g_timer.on || g_timer.used >= g_timer.cap) return -1;
+  const int slot = g_timer.used++;
+  g_timer.id[slot] = kid;
+  cudaEventRecord(g_timer.ev[2 * slot], s);
+  return slot;
+}
+
+void timer_end(int slot, cudaStream_t s) {
+  if (slot < 0) return;
+  cudaEventRecord(g_timer.ev[2 * slot + 1], s);
+}
+
+// Checks shared by every entry point.
+gdr_status check_common(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, const void* o, int B, int L, int Hk, int Hv, int D,
+                        gdr_dtype dt, const char* who) {
+  if (!q || !k || !v || !g || !beta || !o)
+    return fail(GDR_ERR_INVALID_ARG, "%s: q, k, v, g, beta and o must be non-NULL", who);
+  if (B < 1 || L < 1 || Hk < 1 || Hv < 1)
+    return fail(GDR_ERR_INVALID_ARG, "%s: sizes must be >= 1 (B=%d L=%d Hk=%d Hv=%d)", who, B, L, Hk, Hv);
+  if (Hv % Hk != 0)
+    return fail(GDR_ERR_INVALID_ARG, "%s: Hv=%d is not a multiple of Hk=%d", who, Hv, Hk);
+  if (dt != GDR_F32 && dt != GDR_BF16)
+    return fail(GDR_ERR_INVALID_ARG, "%s: unknown dtype %d", who, (int)dt);
+  if (D != kD)
+    return fail(GDR_ERR_UNSUPPORTED, "%s: head dimension D=%d is not implemented (only 128)", who, D);
+  if ((long long)Hv > 65535)
+    return fail(GDR_ERR_UNSUPPORTED, "%s: Hv=%d exceeds 65535", who, Hv);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(g) || !aligned16(beta))
+    return fail(GDR_ERR_INVALID_ARG, "%s: q, k, v, o, g and beta must be 16-byte aligned", who);
+  return GDR_OK;
+}
+
+gdr_status launch_status(cudaError_t e, const char* who) {
+  if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+}  // namespace gdr
+
+using namespace gdr;
+
+extern "C" {
+
+size_t gdr_chunk_workspace_bytes(int B, int L, int Hk, int Hv, int D, gdr_dtype dt) {
+  if (B < 1 || L < 1 || Hk < 1 || Hv < 1 || D != kD || Hv % Hk != 0) return 0;
+  (void)dt;
+  return 0;
+}
+
+gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* S0, void* o, float* S_T, int B, int L,
+                         int Hk, int Hv, int D, gdr_dtype dt, void* ws, size_t ws_bytes,
+                         gdr_stream_t stream) {
+  const char* who = "gdr_chunk_fwd";
+  gdr_status st = check_common(q, k, v, g, beta, o, B, L, Hk, Hv, D, dt, who);
+  if (st != GDR_OK) return st;
+  if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T)))
+    return fail(GDR_ERR_INVALID_ARG, "%s: S0 and S_T must be 16-byte aligned", who);
+  const size_t need = gdr_chunk_workspace_bytes(B, L, Hk, Hv, D, dt);
+  if (need > 0 && (ws == nullptr || ws_bytes < need))
+    return fail(GDR_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", who, need,
+                ws == nullptr ? (size_t)0 : ws_bytes);
+  int* err = device_error_word();
+  if (!err) return fail(GDR_ERR_CUDA, "%s: no CUDA device available", who);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  RecurrentArgs a{q, k, v, g, beta, S0, nullptr, B, o, S_T, B, L, Hk, Hv, dt == GDR_BF16, err};
+  const int slot = timer_begin(s, kKernRecurrent);
+  cudaError_t e = launch_recurrent(a, s);
+  timer_end(slot, s);
+  return launch_status(e, who);
+}
+
+gdr_status gdr_fork_fwd(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, const float* trunk, const int64_t* trunk_idx, int N,
+                        void* o, float* states_out, int F, int L_pad, int Hk, int Hv, int D,
+                        gdr_dtype dt, gdr_stream_t stream) {
+  const char* who = "gdr_fork_fwd";
+  gdr_status st = check_common(q, k, v, g, beta, o, F, L_pad, Hk, Hv, D, dt, who);
+  if (st != GDR_OK) return st;
+  if (!trunk || !trunk_idx || N < 1)
+    return fail(GDR_ERR_INVALID_ARG, "%s: trunk and trunk_idx must be non-NULL and N >= 1", who);
+  if (!aligned16(trunk) || (states_out && !aligned16(states_out)) || (reinterpret_cast<uintptr_t>(trunk_idx) & 7u))
+    return fail(GDR_ERR_INVALID_ARG, "%s: trunk/states_out must be 16-byte and trunk_idx 8-byte aligned", who);
+  if (states_out) {
+    const size_t per = (size_t)Hv * kD * kD * sizeof(float);
+    const char* t0 = reinterpret_cast<const char*>(trunk);
+    const char* t1 = t0 + (size_t)N * per;
+    const char* s0 = reinterpret_cast<const char*>(states_out);
+    const char* s1 = s0 + (size_t)F * per;
+    if (s0 < t1 && t0 < s1)
+      return fail(GDR_ERR_INVALID_ARG, "%s: states_out overlaps trunk", who);
+  }
+  int* err = device_error_word();
+  if (!err) return fail(GDR_ERR_CUDA, "%s: no CUDA device available", who);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  RecurrentArgs a{q, k, v, g, beta, trunk, trunk_idx, N, o, states_out, F, L_pad, Hk, Hv, dt == GDR_BF16, err};
+  const int slot = timer_begin(s, kKernRecurrent);
+  cudaError_t e = launch_recurrent(a, s);
+  timer_end(slot, s);
+  return launch_status(e, who);
+}
+
+gdr_status gdr_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, float* states, void* o, int F, int Hk, int Hv,
+                           int D, gdr_dtype dt, gdr_stream_t stream) {
+  const char* who = "gdr_decode_step";
+  gdr_status st = check_common(q, k, v, g, beta, o, F, 1, Hk, Hv, D, dt, who);
+  if (st != GDR_OK) return st;
+  if (!states || !aligned16(states))
+    return fail(GDR_ERR_INVALID_ARG, "%s: states must be non-NULL and 16-byte aligned", who);
+  int* err = device_error_word();
+  if (!err) return fail(GDR_ERR_CUDA, "%s: no CUDA device available", who);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  RecurrentArgs a{q, k, v, g, beta, states, nullptr, F, o, states, F, 1, Hk, Hv, dt == GDR_BF16, err};
+  const int slot = timer_begin(s, kKernRecurrent);
+  cudaError_t e = launch_recurrent(a, s);
+  timer_end(slot, s);
+  return launch_status(e, who);
+}
+
+gdr_status gdr_sync_status(gdr_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "gdr_sync_status: %s", cudaGetErrorString(e));
+  int* p = device_error_word();
+  if (!p) return fail(GDR_ERR_CUDA, "gdr_sync_status: no CUDA device available");
+  int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int));
+  if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "gdr_sync_status: %s", cudaGetErrorString(e));
+  if (word != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+    if (word == kErrDeviceIndex) return fail(GDR_ERR_DEVICE_INDEX, "a fork's trunk index was out of range");
+    if (word == kErrTimeout) return fail(GDR_ERR_TIMEOUT, "a kernel wait ran past its limit");
+    return fail(GDR_ERR_CUDA, "device error word %d", word);
+  }
+  return ok();
+}
+
+const char* gdr_status_string(gdr_status s) {
+  switch (s) {
+    case GDR_OK: return "GDR_OK";
+    case GDR_ERR_INVALID_ARG: return "GDR_ERR_INVALID_ARG";
+    case GDR_ERR_UNSUPPORTED: return "GDR_ERR_UNSUPPORTED";
+    case GDR_ERR_CUDA: return "GDR_ERR_CUDA";
+    case GDR_ERR_DEVICE_INDEX: return "GDR_ERR_DEVICE_INDEX";
+    case GDR_ERR_TIMEOUT: return "GDR_ERR_TIMEOUT";
+  }
+  return "GDR_ERR_UNKNOWN";
+}
+
+const char* gdr_last_error_message(void) { return t_msg.c_str(); }
+
+gdr_status gdr_stage_timer_enable(int on, int capacity) {
+  std::lock_guard<std::mutex> lk(g_timer.mu);
+  for (cudaEvent_t e : g_timer.ev) cudaEventDestroy(e);
+  g_timer.ev.clear();
+  g_timer.id.clear();
+  g_timer.used = 0;
+  g_timer.cap = 0;
+  g_timer.on = false;
+  if (!on) return ok();
+  if (capacity < 1 || capacity > (1 << 20))
+    return fail(GDR_ERR_INVALID_ARG, "gdr_stage_timer_enable: capacity %d out of range", capacity);
+  g_timer.ev.resize(2 * (size_t)capacity);
+  g_timer.id.resize(capacity);
+  for (auto& e : g_timer.ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      g_timer.ev.clear();
+      return fail(GDR_ERR_CUDA, "gdr_stage_timer_enable: cudaEventCreate failed");
+    }
+  }
+  g_timer.cap = capacity;
+  g_timer.on = true;
+  return ok();
+}
+
+gdr_status gdr_stage_timer_collect(double* total_ms, int* launches, int max_ids) {
+  if (!total_ms || !launches || max_ids < 1)
+    return fail(GDR_ERR_INVALID_ARG, "gdr_stage_timer_collect: bad output arrays");
+  std::lock_guard<std::mutex> lk(g_timer.mu);
+  for (int i = 0; i < max_ids; ++i) { total_ms[i] = 0.0; launches[i] = 0; }
+  for (int s = 0; s < g_timer.used; ++s) {
+    if (cudaEventSynchronize(g_timer.ev[2 * s + 1]) != cudaSuccess)
+      return fail(GDR_ERR_CUDA, "gdr_stage_timer_collect: event sync failed");
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_timer.ev[2 * s], g_timer.ev[2 * s + 1]) != cudaSuccess)
+      return fail(GDR_ERR_CUDA, "gdr_stage_timer_collect: elapsed time failed");
+    const int id = g_timer.id[s];
+    if (id >= 0 && id < max_ids) { total_ms[id] += ms; launches[id] += 1; }
+  }
+  g_timer.used = 0;
+  return ok();
+}
+
+const char* gdr_kernel_name(int id) {
+  switch (id) {
+    case kKernRecurrent: return "gdr_recurrent";
+    case kKernChunkPrep: return "gdr_chunk_prep";
+    case kKernChunkState: return "gdr_chunk_state";
+  }
+  return nullptr;
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gdr {
+
+constexpr int kD = 128;      // head dimension (Dk = Dv) the kernels implement
+constexpr int kChunk = 64;   // tokens per chunk of the tensor-core path
+
+// Device error codes written into the sticky error word (same values as gdr_status).
+constexpr int kErrDeviceIndex = 4;
+constexpr int kErrTimeout = 5;
+
+// Kernel ids for the stage timer.
+enum KernelId : int {
+  kKernRecurrent = 0,
+  kKernChunkPrep = 1,
+  kKernChunkState = 2,
+  kNumKernelIds = 3
+};
+
+// Token-by-token recurrence on CUDA cores (float32 state in registers).
+// Row b reads its initial state from S_in[(idx ? idx[b] : b)] (NULL S_in = zeros) and writes its
+// final state to S_out[b] (NULL = not written). Used for the float32 path, forks and decode.
+struct RecurrentArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const float* S_in;
+  const int64_t* idx;
+  int n_in;            // number of states S_in holds (bounds for idx)
+  void* o;
+  float* S_out;
+  int B, L, Hk, Hv;
+  bool bf16;
+  int* err;            // device error word
+};
+cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t s);
+
+// Device error word of the current device (address of a __device__ int).
+int* device_error_word();
+
+}  // namespace gdr

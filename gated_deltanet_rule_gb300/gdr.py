@@ -1,0 +1,199 @@
+"""Python binding of libgdr (the C ABI in include/gdr.h): argument marshalling only.
+
+Each function checks tensor devices, dtypes, shapes and contiguity, allocates outputs the
+caller did not pass (torch.empty: memory plumbing, no arithmetic), hands raw device pointers
+and the current CUDA stream to the library and raises ``GdrError`` on a non-OK status. Every
+step of the computation runs in the library's kernels; there is no CPU fallback: if
+``libgdr.so`` is missing this module raises instead of computing anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdr.so")
+
+GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_CUDA, GDR_ERR_DEVICE_INDEX, GDR_ERR_TIMEOUT = range(6)
+GDR_F32, GDR_BF16 = 0, 1
+D = 128
+
+EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_fork_fwd", "gdr_decode_step",
+           "gdr_sync_status", "gdr_status_string", "gdr_last_error_message",
+           "gdr_stage_timer_enable", "gdr_stage_timer_collect", "gdr_kernel_name"]
+
+
+class GdrError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgdr.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "or python -m gated_deltanet_rule_gb300.build")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, fp, i, sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.gdr_chunk_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    L.gdr_chunk_workspace_bytes.restype = sz
+    L.gdr_chunk_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, vp, sz, vp]
+    L.gdr_chunk_fwd.restype = i
+    L.gdr_fork_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, vp, fp, i, i, i, i, i, i, vp]
+    L.gdr_fork_fwd.restype = i
+    L.gdr_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, vp]
+    L.gdr_decode_step.restype = i
+    L.gdr_sync_status.argtypes = [vp]
+    L.gdr_sync_status.restype = i
+    L.gdr_status_string.argtypes = [i]
+    L.gdr_status_string.restype = ctypes.c_char_p
+    L.gdr_last_error_message.argtypes = []
+    L.gdr_last_error_message.restype = ctypes.c_char_p
+    L.gdr_stage_timer_enable.argtypes = [i, i]
+    L.gdr_stage_timer_enable.restype = i
+    L.gdr_stage_timer_collect.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int), i]
+    L.gdr_stage_timer_collect.restype = i
+    L.gdr_kernel_name.argtypes = [i]
+    L.gdr_kernel_name.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(status: int) -> None:
+    if status != GDR_OK:
+        L = lib()
+        name = L.gdr_status_string(status).decode()
+        msg = L.gdr_last_error_message().decode()
+        raise GdrError(status, f"{name}: {msg}")
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GDR_F32
+    if t.dtype == torch.bfloat16:
+        return GDR_BF16
+    raise TypeError(f"q/k/v must be float32 or bfloat16, got {t.dtype}")
+
+
+def _need(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _check_inputs(q, k, v, g, beta, device_check=True):
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        _need(isinstance(t, torch.Tensor), f"{name} must be a tensor")
+        if device_check:
+            _need(t.is_cuda, f"{name} must be a CUDA tensor")
+        _need(t.is_contiguous(), f"{name} must be contiguous")
+    _need(q.dtype == k.dtype == v.dtype, "q, k, v must share one dtype")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g and beta must be float32")
+    _need(q.dim() == 4 and k.shape == q.shape and v.dim() == 4, "q, k [B,L,Hk,D] and v [B,L,Hv,D]")
+    B, L, Hk, Dk = q.shape
+    _need(v.shape[0] == B and v.shape[1] == L, "v must be [B, L, Hv, D]")
+    Hv = v.shape[2]
+    _need(g.shape == (B, L, Hv) and beta.shape == (B, L, Hv), "g and beta must be [B, L, Hv]")
+    return B, L, Hk, Hv, Dk
+
+
+def workspace_bytes(B: int, L: int, Hk: int, Hv: int, D: int = D, dtype=torch.bfloat16) -> int:
+    code = GDR_BF16 if dtype == torch.bfloat16 else GDR_F32
+    return int(lib().gdr_chunk_workspace_bytes(B, L, Hk, Hv, D, code))
+
+
+def gdr_chunk_fwd(q, k, v, g, beta, S0=None, o=None, S_T=None, ws=None, stream=None,
+                  final_state: bool = True):
+    """Prefill of B rows: returns (o [B,L,Hv,D] in v's dtype, S_T [B,Hv,D,D] float32 or None)."""
+    B, L, Hk, Hv, Dk = _check_inputs(q, k, v, g, beta)
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty_like(v)
+    if S_T is None and final_state:
+        S_T = torch.empty(B, Hv, Dk, v.shape[3], device=v.device, dtype=torch.float32)
+    for name, t in (("S0", S0), ("S_T", S_T)):
+        if t is not None:
+            _need(t.dtype == torch.float32 and t.is_contiguous() and t.is_cuda, f"{name} must be contiguous CUDA float32")
+    need = workspace_bytes(B, L, Hk, Hv, Dk, q.dtype)
+    if need and ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().gdr_chunk_fwd(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o), _p(S_T),
+                               B, L, Hk, Hv, Dk, dt, _p(ws), ws_bytes, _stream(stream)))
+    return o, S_T
+
+
+def gdr_fork_fwd(q, k, v, g, beta, trunk, trunk_idx, o=None, states_out=None, stream=None,
+                 keep: bool = True):
+    """Fork batch: returns (o [F,L_pad,Hv,D], states_out [F,Hv,D,D] or None)."""
+    F, L, Hk, Hv, Dk = _check_inputs(q, k, v, g, beta)
+    dt = _dtype_code(q)
+    _need(trunk.is_cuda and trunk.dtype == torch.float32 and trunk.is_contiguous(), "trunk: CUDA float32")
+    _need(trunk_idx.is_cuda and trunk_idx.dtype == torch.int64 and trunk_idx.shape == (F,), "trunk_idx: CUDA int64 [F]")
+    if o is None:
+        o = torch.empty_like(v)
+    if states_out is None and keep:
+        states_out = torch.empty(F, Hv, Dk, v.shape[3], device=v.device, dtype=torch.float32)
+    _check(lib().gdr_fork_fwd(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(trunk), _p(trunk_idx),
+                              trunk.shape[0], _p(o), _p(states_out), F, L, Hk, Hv, Dk, dt,
+                              _stream(stream)))
+    return o, states_out
+
+
+def gdr_decode_step(q, k, v, g, beta, states, o=None, stream=None):
+    """One token per row; ``states`` [F,Hv,D,D] float32 is updated in place. Returns o [F,1,Hv,D]."""
+    F, L, Hk, Hv, Dk = _check_inputs(q, k, v, g, beta)
+    _need(L == 1, "decode takes one token per row")
+    dt = _dtype_code(q)
+    _need(states.is_cuda and states.dtype == torch.float32 and states.is_contiguous(), "states: CUDA float32")
+    if o is None:
+        o = torch.empty_like(v)
+    _check(lib().gdr_decode_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(states), _p(o),
+                                 F, Hk, Hv, Dk, dt, _stream(stream)))
+    return o
+
+
+def gdr_sync_status(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel recorded a device-side error."""
+    _check(lib().gdr_sync_status(_stream(stream)))
+
+
+def kernel_names() -> list[str]:
+    names, i = [], 0
+    while True:
+        n = lib().gdr_kernel_name(i)
+        if n is None:
+            return names
+        names.append(n.decode())
+        i += 1
+
+
+def stage_timer_enable(on: bool = True, capacity: int = 8192) -> None:
+    _check(lib().gdr_stage_timer_enable(int(on), int(capacity)))
+
+
+def stage_timer_collect() -> dict:
+    """{kernel name: (total ms, launches)} for the launches recorded since the last collect."""
+    names = kernel_names()
+    n = len(names)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int * n)()
+    _check(lib().gdr_stage_timer_collect(ms, cnt, n))
+    return {names[i]: (ms[i], cnt[i]) for i in range(n)}

@@ -1,0 +1,130 @@
+/*
+ * gdr.h -- C ABI of libgdr, the gated delta rule forward on GB300 (sm_103a).
+ *
+ * The operation (Kev-4B-LiteRT page "r15_kernel_test.py", function truth_f64; DEG page
+ * "model.py", function delta_rule_reference): per row and value head h, with key head
+ * hk = h / (Hv/Hk) (adjacent value heads share a key head, repeat_interleave order),
+ *
+ *   k^ = k / sqrt(sum k^2 + 1e-6),  q~ = q / sqrt(sum q^2 + 1e-6) * D^-0.5
+ *   S = S0 (zeros if absent); for each token t:
+ *     S = exp(g_t) S;  delta = beta_t (v_t - S^T k^);  S = S + k^ delta^T;  o_t = S^T q~
+ *
+ * Pads are data: a position with beta = g = 0 neither decays nor writes the state.
+ *
+ * Conventions shared by every call:
+ *  - All array pointers are DEVICE pointers owned by the caller, row-major and contiguous,
+ *    16-byte aligned. The library never allocates device memory; scratch memory, where a path
+ *    needs it, is a caller-provided workspace.
+ *  - D = Dk = Dv must be 128 (GDR_ERR_UNSUPPORTED otherwise). Hv must be a multiple of Hk.
+ *  - q, k, v and o share one element type (gdr_dtype); g, beta and every state are float32.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream). Host-side argument
+ *    checks happen before anything is launched and return an error without touching the GPU.
+ *    Errors found on the device (a fork index out of range, a wait that ran out) are recorded
+ *    in a sticky device error word that gdr_sync_status() reads and clears.
+ *  - No exception crosses the ABI; every call returns a gdr_status. gdr_last_error_message()
+ *    gives a one-line reason for the last non-OK status returned on the calling host thread.
+ */
+#ifndef GDR_H
+#define GDR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDR_OK = 0,
+  GDR_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, workspace too small  */
+  GDR_ERR_UNSUPPORTED = 2,   /* a size the kernels do not implement (D != 128)            */
+  GDR_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, sync, encode)          */
+  GDR_ERR_DEVICE_INDEX = 4,  /* a fork's trunk index was outside [0, N)                    */
+  GDR_ERR_TIMEOUT = 5        /* a kernel wait ran past its limit; the kernel stopped early */
+} gdr_status;
+
+typedef enum { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
+
+/* Same type as cudaStream_t, declared here so that C callers need no CUDA header. */
+typedef struct CUstream_st* gdr_stream_t;
+
+/*
+ * Workspace bytes gdr_chunk_fwd needs for these sizes (0 when the path needs none: float32).
+ * The bfloat16 tensor-core path keeps per-chunk intermediates there (the WY factors of each
+ * 64-token chunk). Returns 0 for invalid sizes.
+ */
+size_t gdr_chunk_workspace_bytes(int B, int L, int Hk, int Hv, int D, gdr_dtype dt);
+
+/*
+ * Prefill: B rows of L tokens each, every row continuing its own initial state.
+ * (Kev-4B-LiteRT "r15_kernel_test.py": kernel(q, k, v, g, beta, initial_state,
+ *  output_final_state=True, use_qk_l2norm_in_kernel=True) -> (o, S_T);
+ *  DEG "model.py", _delta_rule.)
+ *   q, k   [B, L, Hk, D]  dt          raw (not yet normalised) queries and keys
+ *   v      [B, L, Hv, D]  dt
+ *   g      [B, L, Hv]     float32     natural-log decay per token and value head (<= 0)
+ *   beta   [B, L, Hv]     float32     write strength
+ *   S0     [B, Hv, D, D]  float32     initial state, S[i][j] = key i, value j; NULL = zeros
+ *   o      [B, L, Hv, D]  dt          output, every position (pads included)
+ *   S_T    [B, Hv, D, D]  float32     final state; NULL = not written. May alias S0.
+ *   ws     workspace of at least gdr_chunk_workspace_bytes(...) bytes (may be NULL if that is 0)
+ * L need not be a multiple of 64; nothing is written beyond position L-1.
+ */
+gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* S0, void* o, float* S_T, int B, int L,
+                         int Hk, int Hv, int D, gdr_dtype dt, void* ws, size_t ws_bytes,
+                         gdr_stream_t stream);
+
+/*
+ * Fork batch: F forks, fork f continuing its own copy of trunk[trunk_idx[f]] over its L_pad
+ * tokens (right-padded with beta = g = 0). The trunk states are read in place, never copied.
+ * (DEG "model.py": fork_delta_rule(q, k, v, g, beta, h0, h0_idx, store) in _fork_linear_layer;
+ *  Backbone.fork reads the prefixes by reference through the row index prow.)
+ *   q, k        [F, L_pad, Hk, D] dt;  v [F, L_pad, Hv, D] dt;  g, beta [F, L_pad, Hv] float32
+ *   trunk       [N, Hv, D, D] float32   shared prefix states
+ *   trunk_idx   [F] int64 (device)      fork f starts from trunk[trunk_idx[f]]
+ *   o           [F, L_pad, Hv, D] dt
+ *   states_out  [F, Hv, D, D] float32   each fork's final state (the `store` of the pages);
+ *                                       NULL = not kept. Must not overlap trunk.
+ * An index outside [0, N) leaves that fork's outputs untouched and records
+ * GDR_ERR_DEVICE_INDEX in the device error word.
+ */
+gdr_status gdr_fork_fwd(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, const float* trunk, const int64_t* trunk_idx, int N,
+                        void* o, float* states_out, int F, int L_pad, int Hk, int Hv, int D,
+                        gdr_dtype dt, gdr_stream_t stream);
+
+/*
+ * One decode step (L = 1) for F rows, each row's state updated in place.
+ * (DEG "model.py": DecodeGraph.step -> fork_forward(keep=True, decode=True); an idle row has
+ *  lens 0, hence beta = g = 0, and its state stays bit-identical.)
+ *   q, k [F, 1, Hk, D] dt;  v [F, 1, Hv, D] dt;  g, beta [F, 1, Hv] float32
+ *   states [F, Hv, D, D] float32, read and written in place;  o [F, 1, Hv, D] dt
+ */
+gdr_status gdr_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, float* states, void* o, int F, int Hk, int Hv,
+                           int D, gdr_dtype dt, gdr_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the sticky device error word of the current device. */
+gdr_status gdr_sync_status(gdr_stream_t stream);
+
+/* Static strings; never NULL. */
+const char* gdr_status_string(gdr_status status);
+const char* gdr_last_error_message(void);
+
+/*
+ * Stage timer (measurement aid). When enabled, every kernel the library launches is bracketed
+ * by a pair of CUDA events recorded on its launch stream (up to `capacity` launches).
+ * gdr_stage_timer_collect() synchronises those events and, for each kernel id k < max_ids,
+ * writes the summed milliseconds to total_ms[k] and the launch count to launches[k], then
+ * clears the record. gdr_kernel_name(k) names kernel id k (NULL past the last id).
+ */
+gdr_status gdr_stage_timer_enable(int on, int capacity);
+gdr_status gdr_stage_timer_collect(double* total_ms, int* launches, int max_ids);
+const char* gdr_kernel_name(int id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H */

@@ -1,0 +1,103 @@
+"""The C ABI without a GPU: the library loads, exports every function include/gdr.h declares, and
+rejects bad arguments on the host (status codes and messages) before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_deltanet_rule_gb300 import build as gbuild
+from gated_deltanet_rule_gb300 import gdr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return gdr.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "gdr.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdr_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared()
+    assert "gdr_chunk_fwd" in declared and "gdr_fork_fwd" in declared and "gdr_decode_step" in declared
+    for name in declared:
+        assert hasattr(L, name), name
+    assert sorted(gdr.EXPORTS) == declared
+
+
+def test_status_strings(L):
+    for code, name in enumerate(["GDR_OK", "GDR_ERR_INVALID_ARG", "GDR_ERR_UNSUPPORTED", "GDR_ERR_CUDA",
+                                 "GDR_ERR_DEVICE_INDEX", "GDR_ERR_TIMEOUT"]):
+        assert L.gdr_status_string(code).decode() == name
+    assert gdr.kernel_names()[0] == "gdr_recurrent"
+
+
+P = ctypes.c_void_p(1 << 20)       # a 16-byte aligned address; never dereferenced on the host
+BAD = ctypes.c_void_p((1 << 20) + 4)
+
+
+def _chunk(L, q=P, g=P, o=P, S0=None, B=1, Lt=64, Hk=16, Hv=32, D=128, dt=1, ws=None, ws_bytes=0):
+    return L.gdr_chunk_fwd(q, P, P, g, P, S0, o, None, B, Lt, Hk, Hv, D, dt, ws, ws_bytes, None)
+
+
+def test_chunk_rejects_bad_arguments(L):
+    assert _chunk(L, q=None) == gdr.GDR_ERR_INVALID_ARG
+    assert b"non-NULL" in L.gdr_last_error_message()
+    assert _chunk(L, Lt=0) == gdr.GDR_ERR_INVALID_ARG
+    assert _chunk(L, B=0) == gdr.GDR_ERR_INVALID_ARG
+    assert _chunk(L, Hk=3, Hv=32) == gdr.GDR_ERR_INVALID_ARG
+    assert b"multiple" in L.gdr_last_error_message()
+    assert _chunk(L, D=64) == gdr.GDR_ERR_UNSUPPORTED
+    assert _chunk(L, dt=7) == gdr.GDR_ERR_INVALID_ARG
+    assert _chunk(L, q=BAD) == gdr.GDR_ERR_INVALID_ARG
+    assert b"aligned" in L.gdr_last_error_message()
+    assert _chunk(L, S0=BAD) == gdr.GDR_ERR_INVALID_ARG
+
+
+def test_chunk_rejects_small_workspace(L):
+    need = L.gdr_chunk_workspace_bytes(1, 4096, 16, 32, 128, 1)
+    if need == 0:
+        pytest.skip("this path needs no workspace")
+    assert _chunk(L, Lt=4096, ws=P, ws_bytes=need - 1) == gdr.GDR_ERR_INVALID_ARG
+    assert b"workspace" in L.gdr_last_error_message()
+    assert _chunk(L, Lt=4096, ws=None, ws_bytes=need) == gdr.GDR_ERR_INVALID_ARG
+
+
+def test_workspace_query(L):
+    assert L.gdr_chunk_workspace_bytes(1, 64, 16, 32, 64, 1) == 0      # unsupported D
+    assert L.gdr_chunk_workspace_bytes(1, 64, 3, 32, 128, 1) == 0      # bad head ratio
+    assert L.gdr_chunk_workspace_bytes(1, 64, 16, 32, 128, 0) == 0     # float32 path needs none
+    a = L.gdr_chunk_workspace_bytes(1, 4096, 16, 32, 128, 1)
+    b = L.gdr_chunk_workspace_bytes(2, 4096, 16, 32, 128, 1)
+    assert b >= a
+
+
+def test_fork_rejects_bad_arguments(L):
+    def fork(trunk=P, idx=P, N=1, states=None, F=4):
+        return L.gdr_fork_fwd(P, P, P, P, P, trunk, idx, N, P, states, F, 64, 16, 32, 128, 1, None)
+    assert fork(trunk=None) == gdr.GDR_ERR_INVALID_ARG
+    assert fork(idx=None) == gdr.GDR_ERR_INVALID_ARG
+    assert fork(N=0) == gdr.GDR_ERR_INVALID_ARG
+    assert fork(idx=ctypes.c_void_p((1 << 20) + 4)) == gdr.GDR_ERR_INVALID_ARG
+    # states_out overlapping the trunk is rejected
+    assert fork(trunk=P, states=ctypes.c_void_p((1 << 20) + 1024)) == gdr.GDR_ERR_INVALID_ARG
+    assert b"overlaps" in L.gdr_last_error_message()
+
+
+def test_decode_rejects_bad_arguments(L):
+    assert L.gdr_decode_step(P, P, P, P, P, None, P, 4, 16, 32, 128, 1, None) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_decode_step(P, P, P, P, P, P, P, 4, 16, 32, 100, 1, None) == gdr.GDR_ERR_UNSUPPORTED
+    assert L.gdr_decode_step(P, P, P, P, P, BAD, P, 4, 16, 32, 128, 1, None) == gdr.GDR_ERR_INVALID_ARG
+
+
+def test_stage_timer_argument_checks(L):
+    assert L.gdr_stage_timer_enable(1, 0) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_stage_timer_enable(0, 0) == gdr.GDR_OK
+    assert L.gdr_stage_timer_collect(None, None, 0) == gdr.GDR_ERR_INVALID_ARG
