@@ -51,7 +51,9 @@ struct StageTimer {
   std::vector<int> id;
 } g_timer;
 
-int timer_begin(cudaStream_t s, int kid) {
+}  // namespace
+
+int stage_timer_begin(cudaStream_t s, int kid) {
   std::lock_guard<std::mutex> lk(g_timer.mu);
   if (!g_timer.on || g_timer.used >= g_timer.cap) return -1;
   const int slot = g_timer.used++;
@@ -60,10 +62,12 @@ int timer_begin(cudaStream_t s, int kid) {
   return slot;
 }
 
-void timer_end(int slot, cudaStream_t s) {
+void stage_timer_end(int slot, cudaStream_t s) {
   if (slot < 0) return;
   cudaEventRecord(g_timer.ev[2 * slot + 1], s);
 }
+
+namespace {
 
 // Checks shared by every entry point.
 gdr_status check_common(const void* q, const void* k, const void* v, const float* g,
@@ -113,8 +117,8 @@ extern "C" {
 
 size_t gdr_chunk_workspace_bytes(int B, int L, int Hk, int Hv, int D, gdr_dtype dt) {
   if (B < 1 || L < 1 || Hk < 1 || Hv < 1 || D != kD || Hv % Hk != 0) return 0;
-  (void)dt;
-  return 0;
+  if (dt != GDR_BF16) return 0;   // the float32 path keeps everything in registers
+  return chunk_workspace_bytes(B, L, Hv);
 }
 
 gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
@@ -134,10 +138,16 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
   if (!err) return fail(GDR_ERR_CUDA, "%s: no CUDA device available", who);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  RecurrentArgs a{q, k, v, g, beta, S0, nullptr, B, o, S_T, B, L, Hk, Hv, dt == GDR_BF16, err};
-  const int slot = timer_begin(s, kKernRecurrent);
+  if (dt == GDR_BF16) {
+    if (B > 65535 || Hk > 65535)
+      return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d or Hk=%d exceeds 65535", who, B, Hk);
+    ChunkLaunch c{q, k, v, g, beta, S0, o, S_T, ws, B, L, Hk, Hv, err};
+    return launch_status(launch_chunk_bf16(c, s), who);
+  }
+  RecurrentArgs a{q, k, v, g, beta, S0, nullptr, B, o, S_T, B, L, Hk, Hv, false, err};
+  const int slot = stage_timer_begin(s, kKernRecurrent);
   cudaError_t e = launch_recurrent(a, s);
-  timer_end(slot, s);
+  stage_timer_end(slot, s);
   return launch_status(e, who);
 }
 
@@ -165,9 +175,9 @@ gdr_status gdr_fork_fwd(const void* q, const void* k, const void* v, const float
   if (!err) return fail(GDR_ERR_CUDA, "%s: no CUDA device available", who);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   RecurrentArgs a{q, k, v, g, beta, trunk, trunk_idx, N, o, states_out, F, L_pad, Hk, Hv, dt == GDR_BF16, err};
-  const int slot = timer_begin(s, kKernRecurrent);
+  const int slot = stage_timer_begin(s, kKernRecurrent);
   cudaError_t e = launch_recurrent(a, s);
-  timer_end(slot, s);
+  stage_timer_end(slot, s);
   return launch_status(e, who);
 }
 
@@ -183,9 +193,9 @@ gdr_status gdr_decode_step(const void* q, const void* k, const void* v, const fl
   if (!err) return fail(GDR_ERR_CUDA, "%s: no CUDA device available", who);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   RecurrentArgs a{q, k, v, g, beta, states, nullptr, F, o, states, F, 1, Hk, Hv, dt == GDR_BF16, err};
-  const int slot = timer_begin(s, kKernRecurrent);
+  const int slot = stage_timer_begin(s, kKernRecurrent);
   cudaError_t e = launch_recurrent(a, s);
-  timer_end(slot, s);
+  stage_timer_end(slot, s);
   return launch_status(e, who);
 }
 

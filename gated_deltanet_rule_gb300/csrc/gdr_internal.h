@@ -42,7 +42,29 @@ struct RecurrentArgs {
 };
 cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t s);
 
+// Chunked tensor-core path for bf16 q/k/v (two kernels: per-chunk WY factors, then the state
+// recurrence). ws must hold chunk_workspace_bytes(B, L, Hv) bytes.
+struct ChunkLaunch {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const float* S0;
+  void* o;
+  float* S_T;
+  void* ws;
+  int B, L, Hk, Hv;
+  int* err;
+};
+size_t chunk_workspace_bytes(int B, int L, int Hv);
+cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s);
+
 // Device error word of the current device (address of a __device__ int).
 int* device_error_word();
+
+// Stage timer hooks (no-ops unless enabled): bracket one kernel launch on stream s.
+int stage_timer_begin(cudaStream_t s, int kernel_id);
+void stage_timer_end(int slot, cudaStream_t s);
 
 }  // namespace gdr

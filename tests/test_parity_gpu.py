@@ -56,6 +56,14 @@ def test_config2_joint_scale_2_pow_8_bit_exact():
     assert torch.equal(o8, o * 256.0) and torch.equal(S8, S * 256.0)
 
 
+def test_bf16_joint_scale_2_pow_8_bit_exact():
+    x = inputs.regime("R2", 130, 22, Hk=4, Hv=8, init_state=True, n_valid=100, dtype=torch.bfloat16)
+    o, S = run_chunk(x)
+    x.v, x.S0 = x.v * 256.0, x.S0 * 256.0
+    o8, S8 = run_chunk(x)
+    assert torch.equal(o8, o * 256.0) and torch.equal(S8, S * 256.0)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("L", [1, 2, 63, 64, 65, 130, 200])
 def test_lengths_and_ragged_tails(dtype, L):
@@ -182,3 +190,40 @@ def test_decode_steps_match_oracle_and_idle_rows_are_unchanged():
         assert_close(o, ro, TOL_BF16, "decode o")
         assert torch.equal(st_dev[3], before_idle)
     assert_close(st_dev, ref, TOL_BF16, "decode states")
+
+
+# ------------------------------------------------------------------------------------------------
+# the full-size workloads, in the launch configuration the benchmark times
+# ------------------------------------------------------------------------------------------------
+
+def test_config3_prefill_4096_full_size():
+    x = inputs.config3()
+    o, S = run_chunk(x)
+    ro, rS = ref_chunk(x)
+    assert_close(o, ro, TOL_BF16, "o")
+    assert_close(S, rS, TOL_BF16, "S_T")
+
+
+def test_config4_long_prefill_8192_full_size():
+    x = inputs.config4()
+    o, S = run_chunk(x, S0=False)
+    ro, rS = ref_chunk(x, S0=False)
+    assert_close(o, ro, TOL_BF16, "o")
+    assert_close(S, rS, TOL_BF16, "S_T")
+
+
+def test_config5_forks_and_decode_full_size_sampled():
+    c = inputs.config5()
+    x = c.fork
+    o, S = gdr.gdr_fork_fwd(dev(x.q), dev(x.k), dev(x.v), dev(x.g), dev(x.beta), dev(c.trunk), dev(c.trunk_idx))
+    for step in c.decode:
+        gdr.gdr_decode_step(dev(step.q), dev(step.k), dev(step.v), dev(step.g), dev(step.beta), S)
+    gdr.gdr_sync_status()
+    # oracle on a sample of 24 forks (each fork is independent of the others)
+    pick = torch.arange(0, 256, 11)
+    sub = lambda t: t[pick].contiguous()
+    ro, rS = oracle.fork(sub(x.q), sub(x.k), sub(x.v), sub(x.g), sub(x.beta), c.trunk, c.trunk_idx[pick])
+    assert_close(o[pick.cuda()], ro, TOL_BF16, "fork o")
+    for step in c.decode:
+        _, rS = oracle.decode_step(sub(step.q), sub(step.k), sub(step.v), sub(step.g), sub(step.beta), rS)
+    assert_close(S[pick.cuda()], rS, TOL_BF16, "states after 32 decode steps")
