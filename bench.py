@@ -1,0 +1,412 @@
+"""Benchmark of the gated delta rule prefill on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference] [--workload NAME]
+
+One step = one gdr_chunk_fwd over one row of the workload (default: L = 4096 tokens, 16 key heads
+-> 32 value heads, D = 128, bf16 q/k/v, float32 gates and states, initial state in, final state
+out): the whole hot path (normalisation, chunk decay, WY factors, state recurrence, outputs).
+Under torchrun each rank runs its own row on its own GPU (independent problems: weak scaling, no
+collective on the data path); rank 0 prints one JSON line with the max time over ranks.
+
+Timing: W untimed warm-up steps, then exactly K steps between CUDA events on the launch stream
+(barrier + synchronize on both sides). Inputs rotate over several resident copies whose total
+exceeds the 129 MB L2, so every step reads its inputs from HBM. Per-kernel times come from the
+library's stage timer (CUDA events recorded around each of its launches on the same stream).
+The e2e figure is the same step through the same call with host buffers: pinned host -> device
+copies of the inputs, the call, and device -> host copies of o and S_T, all inside its timed
+region.
+
+--impl reference times the float64 CPU oracle (the checker the tests use) on a bounded sample of
+the same workload on the host cores, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "gated-delta-rule prefill tokens/s (Hv=32,D=128,L=4096), % of roofline"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+D = 128
+
+WORKLOADS = {
+    # name: (L, Hk, Hv, with S0, input regime)
+    "prefill4096": (4096, 16, 32, True, "R1"),
+    "prefill8192": (8192, 16, 16, False, "R2"),
+}
+
+
+def algorithmic(L: int, Hk: int, Hv: int, s0: bool) -> tuple[int, float]:
+    """(bytes, flops) the path must move / compute for one row.
+
+    Bytes: q, k read once at the key heads, v, g, beta, o (bf16 o), S0 in (if any), S_T out.
+    FLOPs: per (value head, 64-token chunk) 5 * 2 C^2 D (A, W, U, Q K^T, P Vnew)
+           + 3 * 2 C D^2 (W S, Q S, K^T Vnew) + C^3 / 3 (triangular inverse), C = 64.
+    """
+    b = 2 * L * Hk * D * 2 + L * Hv * D * 2 + 2 * L * Hv * 4 + L * Hv * D * 2
+    b += Hv * D * D * 4 * (2 if s0 else 1)
+    C = 64
+    nc = -(-L // C)
+    f = Hv * nc * (5 * 2 * C * C * D + 3 * 2 * C * D * D + C ** 3 / 3)
+    return b, f
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_rule_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per step from the committed ncu summary, if it was taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.md")
+    if not os.path.exists(path):
+        return None, None
+    text = open(path).read()
+    m = re.search(r"sources:\s*([0-9a-f]{16})", text)
+    t = re.search(r"dram bytes per step:\s*([0-9]+)", text)
+    if not m or not t or m.group(1) != source_digest():
+        return None, None
+    per_kernel = {k: int(v) for k, v in re.findall(r"^\|\s*(gdr_[a-z_0-9]+)\s*\|\s*([0-9]+)\s*\|", text, re.M)}
+    return int(t.group(1)), per_kernel
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing (also exercised by the CPU tests with gloo)
+# ------------------------------------------------------------------------------------------------
+
+def dist_env() -> tuple[int, int, int]:
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def reduce_max(x: float) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, seconds_this_rank: float) -> tuple[float, float]:
+    """(whole-job units/s, max seconds over ranks): every rank processed units_per_rank."""
+    import torch.distributed as dist
+    n = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    tmax = reduce_max(seconds_this_rank)
+    return n * units_per_rank / tmax, tmax
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    pass
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 0.3 * max(x[2] for x in rows)] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(loaded), "power_w_max": max(r[2] for r in rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------------------------------------
+# GB300 arm
+# ------------------------------------------------------------------------------------------------
+
+def make_row(workload: str, seed: int):
+    from gated_deltanet_rule_gb300 import inputs
+    if workload == "prefill4096":
+        return inputs.config3(seed=seed)
+    if workload == "prefill8192":
+        return inputs.config4(seed=seed)
+    import torch
+    L, Hk, Hv, s0, regime = WORKLOADS[workload]
+    x = inputs.regime(regime, L, seed, Hk, Hv, D, init_state=s0, dtype=torch.bfloat16)
+    x.meta["workload"] = f"{workload} bf16 L={L} Hk={Hk} Hv={Hv} D={D}"
+    return x
+
+
+def run_gb300(args) -> dict | None:
+    import torch
+    import torch.distributed as dist
+    from gated_deltanet_rule_gb300 import gdr
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    L, Hk, Hv, s0, _ = WORKLOADS[args.workload]
+
+    x = make_row(args.workload, seed=3 + rank)
+    host = [x.q, x.k, x.v, x.g, x.beta] + ([x.S0] if s0 else [])
+    set_bytes = sum(t.numel() * t.element_size() for t in host)
+    n_sets = max(2, -(-2 * L2_BYTES // set_bytes))       # resident copies, > 2x L2 in total
+    sets = []
+    for _ in range(n_sets):
+        sets.append([t.to(dev, non_blocking=False).contiguous() for t in host])
+    o = torch.empty_like(sets[0][2])
+    S_T = torch.empty(1, Hv, D, D, device=dev, dtype=torch.float32)
+    ws = torch.empty(max(1, gdr.workspace_bytes(1, L, Hk, Hv)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        s = sets[i % n_sets]
+        gdr.gdr_chunk_fwd(s[0], s[1], s[2], s[3], s[4], s[5] if s0 else None, o=o, S_T=S_T, ws=ws, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    gdr.gdr_sync_status()
+
+    # clocks: sample through a short untimed soak of the same step and through the timed steps
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    t_end = time.time() + args.soak
+    i = 0
+    while time.time() < t_end:
+        step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    gdr.stage_timer_enable(True, 4 * args.steps + 16)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    stages = gdr.stage_timer_collect()
+    gdr.stage_timer_enable(False, 0)
+    gdr.gdr_sync_status()
+    assert torch.isfinite(o.float()).all() and torch.isfinite(S_T).all()
+
+    ms = e0.elapsed_time(e1) / args.steps
+    value, tmax = aggregate(L * args.steps, ms * args.steps / 1e3)
+    ms_max = tmax * 1e3 / args.steps
+    launches = sum(c for _, c in stages.values())
+
+    # e2e: host buffers through the same call, copies inside the timed region
+    pinned = [t.pin_memory() for t in host]
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    S_h = torch.empty(S_T.shape, dtype=S_T.dtype).pin_memory()
+    dbuf = sets[0]
+    h2d = sum(t.numel() * t.element_size() for t in pinned)
+    d2h = o_h.numel() * o_h.element_size() + S_h.numel() * S_h.element_size()
+
+    def e2e_step():
+        for d_, h_ in zip(dbuf, pinned):
+            d_.copy_(h_, non_blocking=True)
+        gdr.gdr_chunk_fwd(dbuf[0], dbuf[1], dbuf[2], dbuf[3], dbuf[4], dbuf[5] if s0 else None, o=o, S_T=S_T,
+                          ws=ws, stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S_T, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_value, _ = aggregate(L * args.steps, f0.elapsed_time(f1) / 1e3)
+    barrier()
+
+    peaks = measured_peaks()
+    alg_bytes, alg_flops = algorithmic(L, Hk, Hv, s0)
+    t_s = ms_max / 1e3
+    hbm_time = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    tc_time = alg_flops / (peaks["bf16_tflops"] * 1e12)
+    bound = "hbm" if hbm_time >= tc_time else "tensor"
+    achieved = alg_bytes / t_s / 1e9 if bound == "hbm" else alg_flops / t_s / 1e12
+    peak = peaks["hbm_gbs"] if bound == "hbm" else peaks["bf16_tflops"]
+    traffic, traffic_k = profiled_traffic(args.workload)
+    kern = {}
+    total_stage = sum(v[0] for v in stages.values()) or 1.0
+    for name, (tot, cnt) in stages.items():
+        if cnt:
+            kern[name] = {"launches": cnt, "avg_us": round(tot / cnt * 1e3, 2), "share": round(tot / total_stage, 4)}
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": x.meta.get("workload"), "L": L, "Hk": Hk, "Hv": Hv, "D": D, "rows_per_gpu": 1,
+                   "S0": s0, "parallelism": f"replicas x{world}" if world > 1 else "single gpu",
+                   "l2": f"{n_sets} resident input sets of {set_bytes / 2**20:.0f} MiB rotated (> L2)"},
+        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "scope": "whole step (all kernels of the path)",
+                     "algorithmic_bytes": alg_bytes, "algorithmic_flops": alg_flops,
+                     "peak_source": f"MEASURED_PEAKS.json ({peaks['source']})"},
+        "kernels": kern,
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+    }
+    if traffic_k:
+        line["roofline"]["traffic_per_kernel"] = traffic_k
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+    return line
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ------------------------------------------------------------------------------------------------
+
+def oracle_sample(workload: str, tokens: int):
+    """The workload's row (seed 3) restricted to its first `tokens` positions (all heads)."""
+    x = make_row(workload, seed=3)
+    L = x.q.shape[1]
+    t = min(L, tokens)
+    args = tuple(None if a is None else a[:, :t].contiguous() for a in (x.q, x.k, x.v, x.g, x.beta))
+    return args + (x.S0,), t, x.meta.get("workload")
+
+
+def cpu_baseline(workload: str, budget_s: float = 20.0) -> dict:
+    import oracle
+    L, Hk, Hv, s0, _ = WORKLOADS[workload]
+    args, tokens, _ = oracle_sample(workload, L)
+    t0 = time.perf_counter()
+    oracle.forward(*args)
+    dt = time.perf_counter() - t0
+    reps = [dt]
+    while sum(reps) < budget_s / 2 and len(reps) < 3:
+        t0 = time.perf_counter()
+        oracle.forward(*args)
+        reps.append(time.perf_counter() - t0)
+    t = statistics.median(reps)
+    return {"value": round(tokens / t, 1), "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"the full row (L={L}, {Hk}->{Hv} heads) once per run, float64 oracle, median of {len(reps)} runs"}
+
+
+def run_reference(args) -> dict | None:
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    L, Hk, Hv, s0, _ = WORKLOADS[args.workload]
+    sample, tokens, wname = oracle_sample(args.workload, max(64, L // 4))   # bounded sample per step
+    for _ in range(args.warmup):
+        oracle.forward(*sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward(*sample)
+    dt = time.perf_counter() - t0
+    value = tokens * args.steps / dt
+    desc = f"the first {tokens} of the row's {L} tokens, all {Hk}->{Hv} heads, per step (float64 oracle)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wname, "L": L, "Hk": Hk, "Hv": Hv, "D": D},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="prefill4096")
+    ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed steps while clocks are sampled")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_gb300(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    try:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+
+
+if __name__ == "__main__":
+    main()
