@@ -97,6 +97,11 @@ gdr_status launch_status(cudaError_t e, const char* who) {
 
 }  // namespace
 
+int record_error(int status, const char* message) {
+  t_msg = message;
+  return status;
+}
+
 int* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;

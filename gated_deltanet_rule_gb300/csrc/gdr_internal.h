@@ -60,6 +60,9 @@ struct ChunkLaunch {
 size_t chunk_workspace_bytes(int B, int L, int Hv);
 cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s);
 
+// Record a one-line message for gdr_last_error_message() on this host thread; returns status.
+int record_error(int status, const char* message);
+
 // Device error word of the current device (address of a __device__ int).
 int* device_error_word();
 

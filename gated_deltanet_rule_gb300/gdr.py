@@ -20,7 +20,7 @@ GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_CUDA, GDR_ERR_DEVICE_I
 GDR_F32, GDR_BF16 = 0, 1
 D = 128
 
-EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_fork_fwd", "gdr_decode_step",
+EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_noalloc", "gdr_fork_fwd", "gdr_decode_step",
            "gdr_sync_status", "gdr_status_string", "gdr_last_error_message",
            "gdr_stage_timer_enable", "gdr_stage_timer_collect", "gdr_kernel_name"]
 
@@ -48,6 +48,8 @@ def lib() -> ctypes.CDLL:
     L.gdr_chunk_workspace_bytes.restype = sz
     L.gdr_chunk_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, vp, sz, vp]
     L.gdr_chunk_fwd.restype = i
+    L.gdr_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, vp]
+    L.gdr_chunk_fwd_noalloc.restype = i
     L.gdr_fork_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, vp, fp, i, i, i, i, i, i, vp]
     L.gdr_fork_fwd.restype = i
     L.gdr_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, vp]

@@ -105,6 +105,29 @@ gdr_status gdr_decode_step(const void* q, const void* k, const void* v, const fl
                            const float* beta, float* states, void* o, int F, int Hk, int Hv,
                            int D, gdr_dtype dt, gdr_stream_t stream);
 
+/*
+ * Prefill without a caller workspace and without any device allocation. The pages have no
+ * counterpart to this call; it is for callers that cannot allocate GPU memory: a host program
+ * that owns the whole device memory budget (a serving process or engine that reserves the GPU at
+ * start-up, or a plugin loaded into one), or a latency-critical loop where a cudaMalloc, which may
+ * synchronise the device and can fail under memory pressure, is not allowed once running.
+ *
+ * Same arguments (minus ws and ws_bytes), computation, results and errors as gdr_chunk_fwd. The
+ * scratch is a fixed array of GDR_NOALLOC_SCRATCH_BYTES in device memory, held by every GPU on which
+ * the library's code is loaded until the process exits. Sizes whose workspace
+ * (gdr_chunk_workspace_bytes) exceeds it are rejected with GDR_ERR_UNSUPPORTED and a message, before
+ * any CUDA call; float32 q/k/v need no scratch.
+ * The first call on a device looks up the scratch's device address (with that device current);
+ * make that first call before any stream capture.
+ * Every call uses the same scratch, which keeps the previous call's contents (nothing in it needs
+ * to start at zero: each call writes all the scratch it reads). Calls whose GPU work overlaps
+ * (other streams, other host threads) race on the scratch: serialise them.
+ */
+#define GDR_NOALLOC_SCRATCH_BYTES ((size_t)64 * 1024 * 1024)
+gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, const float* S0, void* o, float* S_T, int B,
+                                 int L, int Hk, int Hv, int D, gdr_dtype dt, gdr_stream_t stream);
+
 /* Synchronise `stream`, then read and clear the sticky device error word of the current device. */
 gdr_status gdr_sync_status(gdr_stream_t stream);
 
