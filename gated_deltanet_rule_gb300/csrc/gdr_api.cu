@@ -123,7 +123,7 @@ extern "C" {
 size_t gdr_chunk_workspace_bytes(int B, int L, int Hk, int Hv, int D, gdr_dtype dt) {
   if (B < 1 || L < 1 || Hk < 1 || Hv < 1 || D != kD || Hv % Hk != 0) return 0;
   if (dt != GDR_BF16) return 0;   // the float32 path keeps everything in registers
-  return chunk_workspace_bytes(B, L, Hv);
+  return chunk_workspace_bytes(B, Hk, L, Hv);
 }
 
 gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g,

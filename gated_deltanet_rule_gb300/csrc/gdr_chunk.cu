@@ -1,31 +1,38 @@
-// Chunked gated delta rule on tcgen05 tensor cores (bf16 operands, float32 accumulation).
+// Chunked gated delta rule on tcgen05 tensor cores (fp16 / bf16 operands, float32 accumulation).
 //
 // Chunk algebra (64-token chunks; the "R64" form named in Kev-4B-LiteRT "r15_kernel_test.py",
 // with the pair decay computed directly, never as a ratio of cumulative decays). For a chunk with
 // entering state S, gamma_i = sum_{j<=i} g_j, Gamma_i = exp(gamma_i), raw q/k rows and their
-// inverse norms qi_i = (|q_i|^2 + 1e-6)^-1/2, ki_i likewise:
+// inverse norms qi_i = (|q_i|^2 + 1e-6)^-1/2, ki_i likewise, sq_i = Gamma_i qi_i D^-1/2:
 //
 //   A_ij  = beta_i ki_i ki_j (k_i . k_j) exp(gamma_i - gamma_j),  j < i         (strictly lower)
 //   T     = (I + A)^-1                                                          (unit lower)
 //   W     = T diag(beta Gamma ki) K,     U = T diag(beta) V                     (WY factors)
 //   P_ij  = qi_i ki_j D^-1/2 (q_i . k_j) exp(gamma_i - gamma_j),  j <= i
 //   Vnew  = U - W S
-//   O     = diag(Gamma qi D^-1/2) Q S + P Vnew
+//   O     = diag(sq) Q S + P Vnew  =  Q' S + P U,      Q' = diag(sq) Q - P W
 //   S'    = Gamma_C S + K^T diag(exp(gamma_C - gamma) ki) Vnew
 //
-// Kernel 1 (gdr_chunk_prep, one CTA per (row, key head, chunk), all chunks in parallel):
-//   TMA loads the raw q, k tiles once per key head and the v tile of each of its r value heads;
-//   one MMA gives [Q; K] K^T (both Gram matrices); CUDA cores build A and P, invert I + A by
-//   16x16 blocks in fp32, and scale T's columns; one MMA pair gives W and U. W and P are written
-//   to the workspace as 128B-swizzled shared-memory images (bulk-copied as they are by kernel 2),
-//   U in 64-column slices, plus the per-position scales.
-// Kernel 2 (gdr_chunk_state, one CTA per (row, value head, 64 value columns), sequential over
-//   chunks): the float32 state slice stays in registers (one key row per thread); per chunk
-//   MMA_A = [W; Q] S (both products in one M = 128 MMA), Vnew on CUDA cores, then MMA2 = K^T Vs
-//   (state increment) and MMA3 = P Vnew (intra-chunk output), S update and the output stores.
-//   The next chunk's tiles are loaded by TMA while the current chunk computes.
+// Every product whose operands are computed values runs on fp16 operands: one fp16 rounding
+// (11-bit significand) costs about an eighth of a bf16 one, and an emulation of every rounding
+// point against the float64 oracle puts the outputs at the floor set by rounding o to bf16.
+// Operands are assumed inside fp16's range (|x| < 65504), which holds for l2-normalised keys.
+//
+// Kernel 1 (gdr_chunk_prep, one CTA per (row, value head, chunk), all chunks in parallel):
+//   TMA loads raw q, k, v; a bf16 MMA gives [Q; K] K^T (both Gram matrices, exact products); CUDA
+//   cores build A and P; a 16/32-blocked fp32 inverse keeps T^T in A's unused upper triangle; T's
+//   scaled columns form the operand [A1; A2]; MMAs give W = A1 K and U = A2 V, then P [W | U].
+//   Kernel 1 writes, per unit, W and Q' as the 128B-swizzled images kernel 2 uses as its MMA
+//   operand, U and P U as four 32-column fp16 slices, the scales, and once per key head k in fp16.
+// Kernel 2 (gdr_chunk_state, a cluster of 4 CTAs per (row, value head), CTA r owning value columns
+//   [32 r, 32 r + 32), sequential over chunks): the float32 state slice stays in registers. Per
+//   chunk: MMA_A = [W; Q'] S (one M = 128 MMA gives W S and Q' S), then CUDA cores form
+//   Vnew = U - W S, Vs = diag(sk) Vnew and the output rows o = Q' S + P U, then MMA2 = K^T Vs, then
+//   S = Gamma_C S + K^T Vs. The tiles every CTA of the cluster needs (W, Q', K) are TMA-multicast,
+//   each CTA loading a quarter, by a producer warp that runs up to three chunks ahead.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include "gdr_internal.h"
@@ -38,20 +45,23 @@ using namespace ptx;
 namespace {
 
 constexpr float kScale = 0.08838834764831845f;   // 128^-0.5
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitBudget = 2000000000ll;   // cycles (~1 s) before a wait gives up
+constexpr int kSlices = 4;                        // value-column slices per value head = cluster size
+constexpr int kN = kD / kSlices;                  // 32 value columns per state CTA
 
-// Workspace image sizes per (row, value head, chunk) unit.
-// Precision: the operands an MMA takes from computed values are split into bf16 hi + lo pairs
-// where a single bf16 rounding would cost accuracy (T's scaled columns, U, P, and the two Vnew
-// operands); W and the state operand S stay single bf16. Measured against the float64 oracle, this
-// keeps outputs at the floor set by rounding o itself to bf16.
-constexpr uint32_t kWBytes = 16384;     // W: 64 x 128 bf16, two 64-column swizzled atoms
-constexpr uint32_t kPBytes = 16384;     // P: hi and lo bf16 images, 64 x 64 each, swizzled
-constexpr uint32_t kUBytes = 32768;     // U: two slices of 64 x 64 float32, 16-byte chunks swizzled
-constexpr uint32_t kSBytes = 1024;      // scales: sq[64], sk[64], Gamma_C (129 floats used)
-constexpr uint32_t kSCopy = 528;        // bytes of the scale block kernel 2 copies (16-byte multiple)
-constexpr uint32_t kUnitP = kWBytes, kUnitU = kUnitP + kPBytes, kUnitS = kUnitU + kUBytes;
+// Workspace. Per (row, value head, chunk) unit:
+constexpr uint32_t kWBytes = 16384;     // W: 64 x 128 fp16, two 64-column 128B-swizzled atoms
+constexpr uint32_t kQBytes = 16384;     // Q': same layout
+constexpr uint32_t kUBytes = 16384;     // U: four 64 x 32 fp16 slices, rows of 64 B, 64B-swizzled
+constexpr uint32_t kPUBytes = 16384;    // P U: same layout as U
+constexpr uint32_t kSBytes = 512;       // scales: sk[64], Gamma_C
+constexpr uint32_t kSCopy = 272;        // bytes of the scale block kernel 2 copies (16-byte multiple)
+constexpr uint32_t kUnitQ = kWBytes, kUnitU = kUnitQ + kQBytes, kUnitPU = kUnitU + kUBytes;
+constexpr uint32_t kUnitS = kUnitPU + kPUBytes;
 constexpr uint32_t kUnitBytes = kUnitS + kSBytes;
+// ... and per (row, key head, chunk): k in fp16, the same image layout as W.
+constexpr uint32_t kKBytes = 16384;
 
 struct ChunkArgs {
   const float* g;
@@ -60,6 +70,7 @@ struct ChunkArgs {
   __nv_bfloat16* o;
   float* S_T;
   uint8_t* ws;       // 1024-aligned
+  uint8_t* wsk;      // fp16 k images, after the units
   int B, L, Hk, Hv, NC;
   int* err;
 };
@@ -67,44 +78,175 @@ struct ChunkArgs {
 __device__ __forceinline__ uint8_t* unit_base(const ChunkArgs& a, int b, int h, int c) {
   return a.ws + ((size_t)((size_t)b * a.Hv + h) * a.NC + c) * kUnitBytes;
 }
+__device__ __forceinline__ uint8_t* kimg_base(const ChunkArgs& a, int b, int hk, int c) {
+  return a.wsk + ((size_t)((size_t)b * a.Hk + hk) * a.NC + c) * kKBytes;
+}
 
 __device__ __forceinline__ void set_error(int* err, int code) { atomicCAS(err, 0, code); }
 
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+__device__ __forceinline__ uint4 pack8_f16(const float* v) {
+  return make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]),
+                    pack_f16x2(v[6], v[7]));
+}
+__device__ __forceinline__ void unpack8_f16(uint4 w, float* v) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[e]));
+    v[2 * e] = f.x;
+    v[2 * e + 1] = f.y;
+  }
+}
+
 // -------------------------------------------------------------------------------------------
-// Kernel 1: per-chunk WY factors
+// Kernel 1: per-chunk factors
 // -------------------------------------------------------------------------------------------
 constexpr int kPrepThreads = 128;
-constexpr uint32_t kOffQK0 = 0, kOffQK1 = 16384, kOffV = 32768, kOffAop = 49152;
-constexpr uint32_t kOffAm = 65536, kOffTm = kOffAm + 64 * 65 * 4, kOffXs = kOffTm + 64 * 65 * 4;
-constexpr uint32_t kOffVec = kOffXs + 3 * 16 * 17 * 4;
-constexpr uint32_t kPrepSmem = kOffVec + 5 * 64 * 4 + 1024;   // + alignment slack
+constexpr uint32_t kPQ0 = 0, kPK0 = 8192, kPQ1 = 16384, kPK1 = 24576;   // [q|k] K-atoms (Gram operand)
+constexpr uint32_t kPV = 32768;       // v atoms; later the MN-major operand [W0 | W1 | U0 | U1]
+constexpr uint32_t kPAop = 65536;     // MN-major operand [A1 | A2], fp16
+constexpr uint32_t kPP = 81920;       // P, K-major fp16 rows 0-63 (rows 64-127 of the operand unused)
+constexpr uint32_t kPAm = 90112;      // A (strict lower) and T^T (strict upper), float32 [64][68]
+constexpr uint32_t kPVec = kPAm + 64 * 68 * 4;   // gam2, Gam, bet, qinv, kinv, tmp: 6 x 64 floats
+constexpr uint32_t kPXs = kPVec + 6 * 64 * 4;    // block-inverse scratch, 32 x 33 floats
+constexpr uint32_t kPrepSmem = kPXs + 32 * 33 * 4 + 1024;
+
+// T = (I + A)^-1 for the strictly lower 64 x 64 A held in Am (row stride 68). T's strictly lower
+// part is stored transposed in Am's strictly upper part: T(i, j) = Am[j * 68 + i] for i > j.
+// 16 x 16 diagonal blocks by forward substitution, then T_IJ = -T_II (A_IJ T_JJ) for the
+// 16-blocks (1,0), (3,2) and finally for the 32-block (1,0).
+__device__ __forceinline__ float tval(const float* Am, int i, int j) {   // T(i, j)
+  return (i == j) ? 1.f : ((i > j) ? Am[j * 68 + i] : 0.f);
+}
+
+__device__ void block_inverse(float* Am, float* Xs, int tid) {
+  // 1. diagonal 16 x 16 blocks, one column per thread (threads 0-63)
+  if (tid < 64) {
+    const int r0 = (tid >> 4) * 16, col = tid & 15;
+    float x[16];
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) {
+      float acc = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < ii; ++jj) acc = fmaf(Am[(r0 + ii) * 68 + r0 + jj], x[jj], acc);
+      x[ii] = (ii == col) ? 1.f : ((ii < col) ? 0.f : -acc);
+    }
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii)
+      if (ii > col) Am[(r0 + col) * 68 + r0 + ii] = x[ii];
+  }
+  __syncthreads();
+  // 2. 16-blocks (1,0) and (3,2): X = A_IJ T_JJ, then T_IJ = -T_II X. Thread: block, row, 4 columns.
+  {
+    const int blk = tid >> 6, e = tid & 63, rr = e >> 2, c0 = (e & 3) * 4;
+    const int I = 1 + 2 * blk, J = 2 * blk;
+    float xv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float av = Am[(16 * I + rr) * 68 + 16 * J + m];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xv[q] = fmaf(av, tval(Am, 16 * J + m, 16 * J + c0 + q), xv[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) Xs[(blk * 16 + rr) * 17 + c0 + q] = xv[q];
+    __syncthreads();
+    float tv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tv[q] = Xs[(blk * 16 + rr) * 17 + c0 + q];
+    for (int m = 0; m < rr; ++m) {
+      const float t = Am[(16 * I + m) * 68 + 16 * I + rr];   // T(16I + rr, 16I + m)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tv[q] = fmaf(t, Xs[(blk * 16 + m) * 17 + c0 + q], tv[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) Am[(16 * J + c0 + q) * 68 + 16 * I + rr] = -tv[q];
+  }
+  __syncthreads();
+  // 3. 32-block (1,0): X = A(32:64, 0:32) T(0:32, 0:32), then T(32:64, 0:32) = -T(32:64, 32:64) X.
+  //    Thread: row rr, 8 columns.
+  {
+    const int rr = tid >> 2, c0 = (tid & 3) * 8;
+    float ar[32];
+    const float4* arow = reinterpret_cast<const float4*>(Am + (32 + rr) * 68);
+#pragma unroll
+    for (int m4 = 0; m4 < 8; ++m4) {
+      const float4 v = arow[m4];
+      ar[4 * m4] = v.x; ar[4 * m4 + 1] = v.y; ar[4 * m4 + 2] = v.z; ar[4 * m4 + 3] = v.w;
+    }
+    float xv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int cc = c0 + q;
+      const float4* trow = reinterpret_cast<const float4*>(Am + cc * 68);   // T(m, cc) = Am[cc*68+m], m > cc
+      float acc = 0.f;
+#pragma unroll
+      for (int m4 = 0; m4 < 8; ++m4) {
+        const float4 v = trow[m4];
+        const float tv4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int m = 4 * m4 + u;
+          const float t = (m > cc) ? tv4[u] : ((m == cc) ? 1.f : 0.f);
+          acc = fmaf(ar[m], t, acc);
+        }
+      }
+      xv[q] = acc;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) Xs[rr * 33 + c0 + q] = xv[q];
+    __syncthreads();
+    float tv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) tv[q] = Xs[rr * 33 + c0 + q];
+    for (int m = 0; m < rr; ++m) {
+      const float t = Am[(32 + m) * 68 + 32 + rr];   // T(32 + rr, 32 + m)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) tv[q] = fmaf(t, Xs[m * 33 + c0 + q], tv[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) Am[(c0 + q) * 68 + 32 + rr] = -tv[q];
+  }
+  __syncthreads();
+}
 
 __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_qk, bar_v, bar_mma;
+  __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_base;
 
-  const int c = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int r = a.Hv / a.Hk;
-  float* Am = reinterpret_cast<float*>(sm + kOffAm);      // [64][65]
-  float* Tm = reinterpret_cast<float*>(sm + kOffTm);      // [64][65]
-  float* Xs = reinterpret_cast<float*>(sm + kOffXs);      // [3][16][17]
-  float* gam = reinterpret_cast<float*>(sm + kOffVec);
-  float* Gam = gam + 64;
-  float* bet = gam + 128;
-  float* qinv = gam + 192;
-  float* kinv = gam + 256;
+  const int r = a.Hv / a.Hk, hk = h / r;
+  float* Am = reinterpret_cast<float*>(sm + kPAm);
+  float* gam2 = reinterpret_cast<float*>(sm + kPVec);     // cumulative log-decay times log2(e)
+  float* Gam = gam2 + 64;
+  float* bet = gam2 + 128;
+  float* qinv = gam2 + 192;
+  float* kinv = gam2 + 256;
+  float* tmp = gam2 + 320;
+  float* Xs = reinterpret_cast<float*>(sm + kPXs);
 
+  // gates of this chunk; positions past L read as beta = g = 0
+  float gg = 0.f, bb = 0.f;
+  if (tid < 64) {
+    const int p = c * 64 + tid;
+    if (p < a.L) {
+      gg = __ldg(a.g + ((size_t)b * a.L + p) * a.Hv + h);
+      bb = __ldg(a.beta + ((size_t)b * a.L + p) * a.Hv + h);
+    }
+  }
   if (tid == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
-    mbar_init(&bar_qk, 1);
-    mbar_init(&bar_v, 1);
+    mbar_init(&bar_ld, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
   }
@@ -114,45 +256,61 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_after();
   const uint32_t tb = tmem_base;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const int i = tid & 63;
   bool ok = true;
 
   if (tid == 0) {
-    mbar_arrive_expect_tx(&bar_qk, 32768);
-    tma_load_4d(sm + kOffQK0, &tm_q, &bar_qk, 0, hk, c * 64, b);
-    tma_load_4d(sm + kOffQK1, &tm_q, &bar_qk, 64, hk, c * 64, b);
-    tma_load_4d(sm + kOffQK0 + 8192, &tm_k, &bar_qk, 0, hk, c * 64, b);
-    tma_load_4d(sm + kOffQK1 + 8192, &tm_k, &bar_qk, 64, hk, c * 64, b);
-    mbar_arrive_expect_tx(&bar_v, 16384);
-    tma_load_4d(sm + kOffV, &tm_v, &bar_v, 0, hk * r, c * 64, b);
-    tma_load_4d(sm + kOffV + 8192, &tm_v, &bar_v, 64, hk * r, c * 64, b);
+    mbar_arrive_expect_tx(&bar_ld, 49152);
+    tma_load_4d(sm + kPQ0, &tm_q, &bar_ld, 0, hk, c * 64, b);
+    tma_load_4d(sm + kPQ1, &tm_q, &bar_ld, 64, hk, c * 64, b);
+    tma_load_4d(sm + kPK0, &tm_k, &bar_ld, 0, hk, c * 64, b);
+    tma_load_4d(sm + kPK1, &tm_k, &bar_ld, 64, hk, c * 64, b);
+    tma_load_4d(sm + kPV, &tm_v, &bar_ld, 0, h, c * 64, b);
+    tma_load_4d(sm + kPV + 8192, &tm_v, &bar_ld, 64, h, c * 64, b);
+  }
+  // inclusive scan of g over the chunk (warps 0 and 1, then warp 1 adds warp 0's total)
+  if (tid < 64) {
+    float x = gg;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, off);
+      if ((tid & 31) >= off) x += y;
+    }
+    tmp[tid] = x;
+    bet[tid] = bb;
+  }
+  __syncthreads();
+  if (tid < 64) {
+    const float gam = tmp[tid] + (tid >= 32 ? tmp[31] : 0.f);
+    gam2[tid] = gam * kLog2e;
+    Gam[tid] = exp2f(gam * kLog2e);
   }
 
-  ok = mbar_wait(&bar_qk, 0, kWaitBudget);
+  ok = mbar_wait(&bar_ld, 0, kWaitBudget);
   if (!__syncthreads_and(ok)) goto fail;
 
-  // Inverse norms: thread t < 64 reads q row t, t >= 64 reads k row t - 64 (order-free sum).
+  // inverse norms: thread t < 64 reads q row t, t >= 64 reads k row t - 64 (order-free sum)
   {
-    const int row = tid & 63;
-    const uint8_t* base = sm + (tid < 64 ? 0 : 8192) + row * 128;
+    const uint8_t* base = sm + (tid < 64 ? kPQ0 : kPK0) + i * 128;
     float s = 0.f;
 #pragma unroll
     for (int atom = 0; atom < 2; ++atom) {
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         const uint4 w = *reinterpret_cast<const uint4*>(base + atom * 16384 + ch * 16);
-        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float lo = __uint_as_float(ws4[e] << 16), hi = __uint_as_float(ws4[e] & 0xFFFF0000u);
+          const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xFFFF0000u);
           s = fmaf(lo, lo, s);
           s = fmaf(hi, hi, s);
         }
       }
     }
-    (tid < 64 ? qinv : kinv)[row] = rsqrtf(s + 1e-6f);
+    (tid < 64 ? qinv : kinv)[i] = rsqrtf(s + 1e-6f);
   }
 
-  // Gram MMA: D[0:128, 0:64] = [Q; K] K^T  (A rows 0-63 = q, 64-127 = k; B = k rows)
+  // Gram MMA (bf16, exact products): D[0:128, 0:64] = [Q; K] K^T
   if (tid == 0) {
     tc_fence_after();
     const uint32_t idesc = idesc_bf16(128, 64, false, false);
@@ -168,209 +326,205 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_after();
 
   {
-    // This thread's Gram row: rows 0-63 = (Q K^T)_i,:, rows 64-127 = (K K^T)_i,:
+    // this thread's Gram row: rows 0-63 = (Q K^T)_i,:, rows 64-127 = (K K^T)_i,:
     float G[64];
     tmem_ld32(tb + lane_base + 0, G);
     tmem_ld32(tb + lane_base + 32, G + 32);
     tc_fence_before();
-    const int i = tid & 63;
-
-    for (int j = 0; j < r; ++j) {
-      const int h = hk * r + j;
-      // gates of this value head; positions past L read as beta = g = 0
-      if (tid < 64) {
-        const int p = c * 64 + tid;
-        const bool in = p < a.L;
-        const float gg = in ? __ldg(a.g + ((size_t)b * a.L + p) * a.Hv + h) : 0.f;
-        bet[tid] = in ? __ldg(a.beta + ((size_t)b * a.L + p) * a.Hv + h) : 0.f;
-        // inclusive scan of g over the chunk (two warps)
-        float x = gg;
+    const float gi = gam2[i];
+    if (tid >= 64) {
+      // row i of A (strict lower) into shared memory; the upper part is written by the inverse
+      const float si = bet[i] * kinv[i];
+      float4* arow = reinterpret_cast<float4*>(Am + i * 68);
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, x, off);
-          if ((tid & 31) >= off) x += y;
+      for (int j4 = 0; j4 < 16; ++j4) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 4 * j4 + e;
+          v[e] = (j < i) ? si * kinv[j] * G[j] * ex2_approx(gi - gam2[j]) : 0.f;
         }
-        gam[tid] = x;
+        arow[j4] = make_float4(v[0], v[1], v[2], v[3]);
       }
-      __syncthreads();
-      if (tid >= 32 && tid < 64) gam[tid] += gam[31];
-      __syncthreads();
-      if (tid < 64) Gam[tid] = expf(gam[tid]);
+    } else {
+      // row i of P (lower, diagonal included) as fp16 K-major operand row
+      const float si = qinv[i] * kScale;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = 8 * ch + e;
+          v[e] = (j <= i) ? si * kinv[j] * G[j] * ex2_approx(gi - gam2[j]) : 0.f;
+        }
+        *reinterpret_cast<uint4*>(sm + kPP + i * 128 + ((ch ^ (i & 7)) << 4)) = pack8_f16(v);
+      }
+    }
+    // k and v tiles to fp16 in place (the Gram MMA that read k as bf16 has completed)
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      const int chunk16 = tid * 16 + n;                 // 2048 chunks of 16 B: k atoms then v atoms
+      const int which = chunk16 >> 9, off = (chunk16 & 511) * 16;
+      const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPV + (which - 2) * 8192);
+      uint4* p = reinterpret_cast<uint4*>(sm + base + off);
+      uint4 w = *p;
+      w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+      *p = w;
+    }
+  }
+  __syncthreads();
 
-      // A (threads 64..127, row i) and P (threads 0..63, row i)
-      const float gi = gam[i];
-      if (tid >= 64) {
-        const float si = bet[i] * kinv[i];
+  block_inverse(Am, Xs, tid);
+
+  // operand [A1; A2] = [T diag(beta Gamma ki); T diag(beta)], MN-major: K-row j holds column j of T
+  {
+    const int j = i, blk = tid >> 6;
+    const float s = blk ? bet[j] : bet[j] * Gam[j] * kinv[j];
+    const float4* trow = reinterpret_cast<const float4*>(Am + j * 68);
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj)
-          Am[i * 65 + jj] = (jj < i) ? si * kinv[jj] * G[jj] * expf(gi - gam[jj]) : 0.f;
-      } else {
-        const float si = qinv[i] * kScale;
-        uint8_t* prow = unit_base(a, b, h, c) + kUnitP + i * 128;
+    for (int ch = 0; ch < 8; ++ch) {
+      const float4 t0 = trow[2 * ch], t1 = trow[2 * ch + 1];
+      const float tt[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+      float v[8];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t hv[4], lv[4];
+      for (int e = 0; e < 8; ++e) {
+        const int ii = 8 * ch + e;
+        v[e] = ((ii > j) ? tt[e] : (ii == j ? 1.f : 0.f)) * s;
+      }
+      *reinterpret_cast<uint4*>(sm + kPAop + blk * 8192 + j * 128 + ((ch ^ (j & 7)) << 4)) = pack8_f16(v);
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+
+  // W = [A1; A2] K (rows 0-63) into columns 0-127, U = [A1; A2] V (rows 64-127) into 128-255
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t idesc = idesc_f16(128, 128, true, true);
+    const uint32_t aop = smem_u32(sm + kPAop);
+    const uint32_t kt = smem_u32(sm + kPK0);   // k atoms at +8192 and +24576: stride 16384
+    const uint32_t vt = smem_u32(sm + kPV);    // v atoms at +32768 and +40960: stride 8192
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16(tb, smem_desc(aop + kk * 2048, 8192, 1024), smem_desc(kt + kk * 2048, 16384, 1024), idesc, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16(tb + 128, smem_desc(aop + kk * 2048, 8192, 1024), smem_desc(vt + kk * 2048, 8192, 1024), idesc,
+               kk > 0);
+    mma_commit(&bar_mma);
+  }
+  ok = mbar_wait(&bar_mma, 1, kWaitBudget);
+  if (!__syncthreads_and(ok)) goto fail;
+  tc_fence_after();
+
+  {
+    uint8_t* ub = unit_base(a, b, h, c);
+    if (tid < 64) {
+      // W row i (lanes 0-63, columns 0-127) -> fp16 into the operand blocks W0/W1 (over v, now
+      // consumed) and the workspace image (same bytes)
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        float w[32];
+        tmem_ld32(tb + lane_base + part * 32, w);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int col = part * 32 + q4 * 8;
+          const int atom = col >> 6, ch = (col & 63) >> 3;
+          const uint32_t off = atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4);
+          const uint4 pk = pack8_f16(w + q4 * 8);
+          *reinterpret_cast<uint4*>(sm + kPV + off) = pk;
+          *reinterpret_cast<uint4*>(ub + off) = pk;
+        }
+      }
+    } else {
+      // U row i (lanes 64-127, columns 128-255) -> fp16 into operand blocks U0/U1 and the slices
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        float u[32];
+        tmem_ld32(tb + lane_base + 128 + part * 32, u);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int col = part * 32 + q4 * 8;
+          const int atom = col >> 6, ch = (col & 63) >> 3;
+          const uint4 pk = pack8_f16(u + q4 * 8);
+          *reinterpret_cast<uint4*>(sm + kPV + 16384 + atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4)) = pk;
+          *reinterpret_cast<uint4*>(ub + kUnitU + part * 4096 + swz64(i * 64 + q4 * 16)) = pk;
+        }
+      }
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+
+  // [P; .] [W | U]: rows 0-63 = P W (columns 0-127) and P U (columns 128-255)
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t idesc = idesc_f16(128, 256, false, true);
+    const uint32_t pa = smem_u32(sm + kPP), wu = smem_u32(sm + kPV);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16(tb, smem_desc(pa + kk * 32, 16, 1024), smem_desc(wu + kk * 2048, 8192, 1024), idesc, kk > 0);
+    mma_commit(&bar_mma);
+  }
+  ok = mbar_wait(&bar_mma, 0, kWaitBudget);
+  if (!__syncthreads_and(ok)) goto fail;
+  tc_fence_after();
+
+  {
+    uint8_t* ub = unit_base(a, b, h, c);
+    if (tid < 64) {
+      // Q'_i = sq_i q_i - (P W)_i (fp16 image), (P U)_i (fp16 slices), scales
+      const float sq = Gam[i] * qinv[i] * kScale;
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        float w[32];
+        tmem_ld32(tb + lane_base + part * 32, w);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int col = part * 32 + q4 * 8;
+          const int atom = col >> 6, ch = (col & 63) >> 3;
+          const uint32_t off = atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4);
+          const uint4 qr = *reinterpret_cast<const uint4*>(sm + (atom ? kPQ1 : kPQ0) + i * 128 + ((ch ^ (i & 7)) << 4));
+          const uint32_t q4w[4] = {qr.x, qr.y, qr.z, qr.w};
+          float v[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
-            const float p0 = (j0 <= i) ? si * kinv[j0] * G[j0] * expf(gi - gam[j0]) : 0.f;
-            const float p1 = (j1 <= i) ? si * kinv[j1] * G[j1] * expf(gi - gam[j1]) : 0.f;
-            split_bf16x2(p0, p1, hv[e], lv[e]);
+            v[2 * e] = sq * __uint_as_float(q4w[e] << 16) - w[q4 * 8 + 2 * e];
+            v[2 * e + 1] = sq * __uint_as_float(q4w[e] & 0xFFFF0000u) - w[q4 * 8 + 2 * e + 1];
           }
-          const uint32_t off = (ch ^ (i & 7)) << 4;
-          *reinterpret_cast<uint4*>(prow + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-          *reinterpret_cast<uint4*>(prow + 8192 + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+          *reinterpret_cast<uint4*>(ub + kUnitQ + off) = pack8_f16(v);
         }
       }
-      __syncthreads();
-
-      // T = (I + A)^-1 by 16x16 blocks. Diagonal blocks: forward substitution per column.
-      if (tid < 64) {
-        const int blk = tid >> 4, col = tid & 15, r0 = blk * 16;
-        float x[16];
 #pragma unroll
-        for (int ii = 0; ii < 16; ++ii) {
-          float acc = 0.f;
+      for (int part = 0; part < 4; ++part) {
+        float u[32];
+        tmem_ld32(tb + lane_base + 128 + part * 32, u);
 #pragma unroll
-          for (int jj = 0; jj < ii; ++jj) acc = fmaf(Am[(r0 + ii) * 65 + r0 + jj], x[jj], acc);
-          x[ii] = (ii == col) ? 1.f : ((ii < col) ? 0.f : -acc);
-          Tm[(r0 + ii) * 65 + r0 + col] = x[ii];
-        }
-      } else {
-        // zero the blocks above the diagonal
-        for (int e = tid - 64; e < 64 * 64; e += 64) {
-          const int rr = e >> 6, cc = e & 63;
-          if ((cc >> 4) > (rr >> 4)) Tm[rr * 65 + cc] = 0.f;
-        }
+        for (int q4 = 0; q4 < 4; ++q4)
+          *reinterpret_cast<uint4*>(ub + kUnitPU + part * 4096 + swz64(i * 64 + q4 * 16)) = pack8_f16(u + q4 * 8);
       }
-      __syncthreads();
-      for (int I = 1; I < 4; ++I) {
-        // X_IJ = sum_{M=J}^{I-1} A_IM T_MJ for J < I
-        for (int e = tid; e < I * 256; e += kPrepThreads) {
-          const int J = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-          float acc = 0.f;
-          for (int M = J; M < I; ++M) {
+      float* sc = reinterpret_cast<float*>(ub + kUnitS);
+      sc[i] = exp2f(gam2[63] - gam2[i]) * kinv[i];
+      if (i == 0) sc[64] = Gam[63];
+    } else if (h % r == 0) {
+      // the fp16 k image, once per key head
+      uint8_t* kb = kimg_base(a, b, hk, c);
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-              acc = fmaf(Am[(16 * I + rr) * 65 + 16 * M + m], Tm[(16 * M + m) * 65 + 16 * J + cc], acc);
-          }
-          Xs[(J * 16 + rr) * 17 + cc] = acc;
-        }
-        __syncthreads();
-        // T_IJ = -T_II X_IJ  (T_II unit lower triangular)
-        for (int e = tid; e < I * 256; e += kPrepThreads) {
-          const int J = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-          float acc = Xs[(J * 16 + rr) * 17 + cc];
-          for (int m = 0; m < rr; ++m)
-            acc = fmaf(Tm[(16 * I + rr) * 65 + 16 * I + m], Xs[(J * 16 + m) * 17 + cc], acc);
-          Tm[(16 * I + rr) * 65 + 16 * J + cc] = -acc;
-        }
-        __syncthreads();
+      for (int n = 0; n < 16; ++n) {
+        const int chunk16 = (tid - 64) * 16 + n;    // 1024 chunks of 16 B over the two k atoms
+        const int atom = chunk16 >> 9, off = (chunk16 & 511) * 16;
+        *reinterpret_cast<uint4*>(kb + atom * 8192 + off) =
+            *reinterpret_cast<const uint4*>(sm + (atom ? kPK1 : kPK0) + off);
       }
-
-      // A operand [T diag(beta Gamma ki); T diag(beta)], K-major swizzled (K = 64 positions), as
-      // a bf16 hi image and a bf16 lo image (the lo image reuses A's storage, dead by now)
-      {
-        const bool wrow = tid < 64;
-        uint8_t* arow = sm + kOffAop + tid * 128;
-        uint8_t* lrow = sm + kOffAm + tid * 128;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t hv[4], lv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j0 = ch * 8 + 2 * e, j1 = j0 + 1;
-            const float s0 = wrow ? bet[j0] * Gam[j0] * kinv[j0] : bet[j0];
-            const float s1 = wrow ? bet[j1] * Gam[j1] * kinv[j1] : bet[j1];
-            split_bf16x2(Tm[i * 65 + j0] * s0, Tm[i * 65 + j1] * s1, hv[e], lv[e]);
-          }
-          const uint32_t off = (ch ^ (tid & 7)) << 4;
-          *reinterpret_cast<uint4*>(arow + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-          *reinterpret_cast<uint4*>(lrow + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-        }
-      }
-      fence_async_smem();
-      tc_fence_before();
-      __syncthreads();
-
-      ok = mbar_wait(&bar_v, j & 1, kWaitBudget);
-      if (!__syncthreads_and(ok)) goto fail;
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t idesc = idesc_bf16(128, 128, false, true);
-        const uint32_t aop[2] = {smem_u32(sm + kOffAop), smem_u32(sm + kOffAm)};   // hi, lo
-        const uint32_t kt = smem_u32(sm + kOffQK0 + 8192);   // k atoms at +8192 and +24576
-        const uint32_t vt = smem_u32(sm + kOffV);            // v atoms at +0 and +8192
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tb, smem_desc(aop[part] + kk * 32, 16, 1024), smem_desc(kt + kk * 2048, 16384, 1024), idesc,
-                     part | kk);
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tb + 128, smem_desc(aop[part] + kk * 32, 16, 1024), smem_desc(vt + kk * 2048, 8192, 1024),
-                     idesc, part | kk);
-        mma_commit(&bar_mma);
-      }
-      ok = mbar_wait(&bar_mma, (j + 1) & 1, kWaitBudget);
-      if (!__syncthreads_and(ok)) goto fail;
-      tc_fence_after();
-
-      // next value head's v tile (the U MMA has consumed this one)
-      if (tid == 0 && j + 1 < r) {
-        mbar_arrive_expect_tx(&bar_v, 16384);
-        tma_load_4d(sm + kOffV, &tm_v, &bar_v, 0, h + 1, c * 64, b);
-        tma_load_4d(sm + kOffV + 8192, &tm_v, &bar_v, 64, h + 1, c * 64, b);
-      }
-
-      uint8_t* ub = unit_base(a, b, h, c);
-      if (tid < 64) {
-        // W row i (TMEM lanes 0-63, columns 0-127) -> swizzled image
-#pragma unroll
-        for (int part = 0; part < 4; ++part) {
-          float w[32];
-          tmem_ld32(tb + lane_base + part * 32, w);
-#pragma unroll
-          for (int ch4 = 0; ch4 < 4; ++ch4) {
-            const int col = part * 32 + ch4 * 8;
-            const int atom = col >> 6, ch = (col & 63) >> 3;
-            uint4 pk = make_uint4(pack_bf16x2(w[ch4 * 8 + 0], w[ch4 * 8 + 1]), pack_bf16x2(w[ch4 * 8 + 2], w[ch4 * 8 + 3]),
-                                  pack_bf16x2(w[ch4 * 8 + 4], w[ch4 * 8 + 5]), pack_bf16x2(w[ch4 * 8 + 6], w[ch4 * 8 + 7]));
-            *reinterpret_cast<uint4*>(ub + atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4)) = pk;
-          }
-        }
-        // per-position scales for kernel 2
-        float* sc = reinterpret_cast<float*>(ub + kUnitS);
-        sc[i] = Gam[i] * qinv[i] * kScale;
-        sc[64 + i] = expf(gam[63] - gam[i]) * kinv[i];
-        if (i == 0) sc[128] = Gam[63];
-      } else {
-        // U row i (TMEM lanes 64-127, columns 128-255) -> two 64-column float32 slices; the
-        // 16-byte chunk c of row i is stored at chunk c ^ (i % 8) so that row reads do not collide
-#pragma unroll
-        for (int part = 0; part < 4; ++part) {
-          float u[32];
-          tmem_ld32(tb + lane_base + 128 + part * 32, u);
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const int col = part * 32 + c4 * 4;
-            const int sl = col >> 6, ch = (col & 63) >> 2;
-            *reinterpret_cast<float4*>(ub + kUnitU + sl * 16384 + i * 256 + ((ch ^ (i & 7)) << 4)) =
-                make_float4(u[c4 * 4 + 0], u[c4 * 4 + 1], u[c4 * 4 + 2], u[c4 * 4 + 3]);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncthreads();
     }
   }
   goto done;
 fail:
   if (tid == 0) set_error(a.err, kErrTimeout);
 done:
+  tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
@@ -379,237 +533,230 @@ done:
 }
 
 // -------------------------------------------------------------------------------------------
-// Kernel 2: sequential state recurrence over chunks, 64 value columns per CTA
+// Kernel 2: sequential state recurrence over chunks; cluster of 4 CTAs per (row, value head)
 // -------------------------------------------------------------------------------------------
-constexpr int kStateThreads = 128;
-// Stage (one chunk's tiles, 1024-aligned). [W0|Q0] and [W1|Q1] form the two K-atoms of the
-// M = 128 operand [W; Q]; the 8 KB before P_hi (Q1) and before P_lo (P_hi) are the unused top
-// halves of the operands [. ; P_hi] and [. ; P_lo].
-constexpr uint32_t kStW0 = 0, kStQ0 = 8192, kStW1 = 16384, kStQ1 = 24576, kStPh = 32768, kStPl = 40960;
-constexpr uint32_t kStK0 = 49152, kStK1 = 57344, kStU = 65536, kStS = 81920;
-constexpr uint32_t kStage = 82944;
-constexpr uint32_t kStageTx = kWBytes + 16384 + kPBytes + 16384 + 16384 + kSCopy;
-constexpr uint32_t kOffSb = 2 * kStage, kOffVsh = kOffSb + 16384, kOffVsl = kOffVsh + 8192;
-constexpr uint32_t kOffVuh = kOffVsl + 8192, kOffVul = kOffVuh + 8192;
-constexpr uint32_t kStateSmem = kOffVul + 8192 + 1024;
+// Warp roles (warp w reads TMEM lanes 32 (w % 4) .. + 31):
+//   warps 0-3: own the state rows (key row = tid, 32 value columns, float32 registers);
+//   warps 0, 1, 4, 5: Vnew for positions 0-63 (warps 0, 1: value columns 0-15; 4, 5: 16-31);
+//   warps 2, 3: output rows o = Q' S + P U for positions 0-63 (TMEM lanes 64-127);
+//   thread 0 issues the MMAs. Warps 0-5 synchronise on named barrier 1.
+//   warp 6: producer, loading the early tiles up to three chunks ahead.
+constexpr int kStateThreads = 224;
+constexpr uint32_t kChainBar = 1, kChainCount = 192;
+constexpr int kEStages = 3;
+// stage: [W0|Q'0] and [W1|Q'1] are the two K-atoms of the M = 128 operand [W; Q']
+constexpr uint32_t kEW0 = 0, kEQ0 = 8192, kEW1 = 16384, kEQ1 = 24576, kEK0 = 32768, kEK1 = 40960;
+constexpr uint32_t kEU = 49152, kEPU = 53248, kES = 57344;
+constexpr uint32_t kEStage = 58368;
+constexpr uint32_t kOffSb = kEStages * kEStage;   // state operand, fp16 MN-major, 128 rows of 64 B
+constexpr uint32_t kOffVs = kOffSb + 8192;        // Vs operand, fp16 MN-major, 64 rows of 64 B
+constexpr uint32_t kStateSmem = kOffVs + 4096 + 1024;
+constexpr uint32_t kETx = 12 * 4096 + 4096 + 4096 + kSCopy;   // bytes landing in one stage of each CTA
+constexpr uint32_t kTmemState = 64;                            // D_A [0, 32), D_X [32, 64)
 
-__global__ void __launch_bounds__(kStateThreads, 1)
-chunk_state_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const ChunkArgs a) {
+__global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads, 1)
+chunk_state_kernel(const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full[2], bar_mma;
+  __shared__ uint64_t fullE[kEStages], freeE[kEStages], bar_a, bar_x;
   __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
 
-  const int sl = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int sl = (int)rank, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hk = h / (a.Hv / a.Hk);
   const int NC = a.NC;
 
-  auto issue_loads = [&](int c) {
-    uint8_t* st = sm + (c & 1) * kStage;
+  // tiles of chunk c: this CTA multicasts 3 of the 12 shared 4 KB pieces (W, Q', k) and loads its
+  // own U and P U slices and the scales
+  auto issue_early = [&](int c) {
+    uint8_t* st = sm + (c % kEStages) * kEStage;
+    uint64_t* bar = &fullE[c % kEStages];
     const uint8_t* ub = unit_base(a, b, h, c);
-    uint64_t* bar = &full[c & 1];
-    mbar_arrive_expect_tx(bar, kStageTx);
-    bulk_load(st + kStW0, ub, 8192, bar);
-    bulk_load(st + kStW1, ub + 8192, 8192, bar);
-    bulk_load(st + kStPh, ub + kUnitP, kPBytes, bar);
-    bulk_load(st + kStU, ub + kUnitU + sl * 16384, 16384, bar);
-    bulk_load(st + kStS, ub + kUnitS, kSCopy, bar);
-    tma_load_4d(st + kStQ0, &tm_q, bar, 0, hk, c * 64, b);
-    tma_load_4d(st + kStQ1, &tm_q, bar, 64, hk, c * 64, b);
-    tma_load_4d(st + kStK0, &tm_k, bar, 0, hk, c * 64, b);
-    tma_load_4d(st + kStK1, &tm_k, bar, 64, hk, c * 64, b);
+    const uint8_t* kb = kimg_base(a, b, hk, c);
+    mbar_arrive_expect_tx(bar, kETx);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int p = 3 * sl + k, half = p & 1, atom = (p >> 1) & 1;
+      const uint8_t* src;
+      uint32_t dst;
+      if (p < 4) {            // W
+        src = ub + atom * 8192 + half * 4096;
+        dst = (atom ? kEW1 : kEW0) + half * 4096;
+      } else if (p < 8) {     // Q'
+        src = ub + kUnitQ + atom * 8192 + half * 4096;
+        dst = (atom ? kEQ1 : kEQ0) + half * 4096;
+      } else {                // k (fp16)
+        src = kb + atom * 8192 + half * 4096;
+        dst = (atom ? kEK1 : kEK0) + half * 4096;
+      }
+      bulk_load_mc(st + dst, src, 4096, bar, 0xF);
+    }
+    bulk_load(st + kEU, ub + kUnitU + sl * 4096, 4096, bar);
+    bulk_load(st + kEPU, ub + kUnitPU + sl * 4096, 4096, bar);
+    bulk_load(st + kES, ub + kUnitS, kSCopy, bar);
   };
 
   if (tid == 0) {
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_k);
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
-    mbar_init(&bar_mma, 1);
+    for (int s = 0; s < kEStages; ++s) {
+      mbar_init(&fullE[s], 1);
+      mbar_init(&freeE[s], kSlices);
+    }
+    mbar_init(&bar_a, 1);
+    mbar_init(&bar_x, 1);
+    abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(&tmem_base, 256);
+  if (warp == 0) tmem_alloc(&tmem_base, kTmemState);
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();   // every CTA's barriers exist before anyone multicasts into them
   tc_fence_after();
   const uint32_t tb = tmem_base;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  if (tid == 0) issue_loads(0);
-
-  // State slice: thread kr owns key row kr, value columns [64 sl, 64 sl + 64), float32.
-  const int kr = tid;
-  float Sm[64];
-  {
-    const float* s0 = a.S0 ? a.S0 + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * 64 : nullptr;
-#pragma unroll
-    for (int n = 0; n < 64; n += 4) {
-      float4 x = s0 ? __ldg(reinterpret_cast<const float4*>(s0 + n)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      Sm[n] = x.x; Sm[n + 1] = x.y; Sm[n + 2] = x.z; Sm[n + 3] = x.w;
-    }
-  }
-  // bf16 state operand: MN-major (rows = key index, 64 value columns per 128-byte row)
-  auto write_state_operand = [&]() {
-    uint8_t* row = sm + kOffSb + kr * 128;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      uint4 pk = make_uint4(pack_bf16x2(Sm[ch * 8 + 0], Sm[ch * 8 + 1]), pack_bf16x2(Sm[ch * 8 + 2], Sm[ch * 8 + 3]),
-                            pack_bf16x2(Sm[ch * 8 + 4], Sm[ch * 8 + 5]), pack_bf16x2(Sm[ch * 8 + 6], Sm[ch * 8 + 7]));
-      *reinterpret_cast<uint4*>(row + ((ch ^ (kr & 7)) << 4)) = pk;
-    }
-  };
-  write_state_operand();
-  fence_async_smem();
-  __syncthreads();
-
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   bool ok = true;
-  const int i = tid & 63;   // chunk position for the row-per-position phases
-  for (int c = 0; c < NC; ++c) {
-    uint8_t* st = sm + (c & 1) * kStage;
-    if (tid == 0 && c + 1 < NC) issue_loads(c + 1);
-    ok = mbar_wait(&full[c & 1], (c >> 1) & 1, kWaitBudget);
-    if (!__syncthreads_and(ok)) goto fail;
 
-    // MMA_A: D[:, 0:64] = [W; Q] S   (rows 0-63 W S, rows 64-127 Q S)
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, 64, false, true);
-      const uint32_t sb = smem_u32(sm + kOffSb);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t aa = smem_u32(st) + (kk >> 2) * 16384 + (kk & 3) * 32;
-        mma_bf16(tb, smem_desc(aa, 16, 1024), smem_desc(sb + kk * 2048, 8192, 1024), idesc, kk > 0);
+  if (warp == 6) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      for (int c = 0; c < NC; ++c) {
+        if (c >= kEStages) ok = mbar_wait(&freeE[c % kEStages], ((c - kEStages) / kEStages) & 1, kWaitBudget);
+        if (!ok || *(volatile int*)&abort_flag) break;
+        issue_early(c);
       }
-      mma_commit(&bar_mma);
     }
-    ok = mbar_wait(&bar_mma, 0, kWaitBudget);
-    if (!__syncthreads_and(ok)) goto fail;
-    tc_fence_after();
-
-    const float* sc = reinterpret_cast<const float*>(st + kStS);
-    float qs[64];
-    if (tid < 64) {
-      // Vnew row i = U_i - (W S)_i ; Vs = sk_i Vnew (state operand), Vu = Vnew (output operand),
-      // each as bf16 hi + lo rows of the MN-major B operands
-      float ws_[64];
-      tmem_ld32(tb + lane_base, ws_);
-      tmem_ld32(tb + lane_base + 32, ws_ + 32);
-      const float sk = sc[64 + i];
-      const uint8_t* urow = st + kStU + i * 256;
+  } else {
+    // ---------------- chain and output (warps 0-5) ----------------
+    const bool owner = warp < 4;                         // owns state row kr = tid
+    const int kr = tid & 127;
+    const bool vrow = (warp < 2) || (warp >= 4);         // forms Vnew rows
+    const bool orow = (warp == 2) || (warp == 3);        // forms output rows
+    const int i = tid & 63, ch0 = (warp >= 4) ? 16 : 0;
+    float Sm[kN];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const float4 u0 = *reinterpret_cast<const float4*>(urow + (((2 * ch) ^ (i & 7)) << 4));
-        const float4 u1 = *reinterpret_cast<const float4*>(urow + (((2 * ch + 1) ^ (i & 7)) << 4));
-        const float un[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        uint32_t vsh[4], vsl[4], vuh[4], vul[4];
+    for (int n = 0; n < kN; ++n) Sm[n] = 0.f;
+    if (owner && a.S0) {
+      const float* s0 = a.S0 + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float v0 = un[2 * e] - ws_[ch * 8 + 2 * e];
-          const float v1 = un[2 * e + 1] - ws_[ch * 8 + 2 * e + 1];
-          split_bf16x2(sk * v0, sk * v1, vsh[e], vsl[e]);
-          split_bf16x2(v0, v1, vuh[e], vul[e]);
-        }
-        const uint32_t off = i * 128 + ((ch ^ (i & 7)) << 4);
-        *reinterpret_cast<uint4*>(sm + kOffVsh + off) = make_uint4(vsh[0], vsh[1], vsh[2], vsh[3]);
-        *reinterpret_cast<uint4*>(sm + kOffVsl + off) = make_uint4(vsl[0], vsl[1], vsl[2], vsl[3]);
-        *reinterpret_cast<uint4*>(sm + kOffVuh + off) = make_uint4(vuh[0], vuh[1], vuh[2], vuh[3]);
-        *reinterpret_cast<uint4*>(sm + kOffVul + off) = make_uint4(vul[0], vul[1], vul[2], vul[3]);
+      for (int n = 0; n < kN; n += 4) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(s0 + n));
+        Sm[n] = x.x; Sm[n + 1] = x.y; Sm[n + 2] = x.z; Sm[n + 3] = x.w;
       }
-    } else {
-      tmem_ld32(tb + lane_base, qs);
-      tmem_ld32(tb + lane_base + 32, qs + 32);
-      const float sq = sc[i];
-#pragma unroll
-      for (int n = 0; n < 64; ++n) qs[n] *= sq;
     }
+    // fp16 state operand: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle
+    auto write_state_operand = [&]() {
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+        *reinterpret_cast<uint4*>(sm + kOffSb + swz64(kr * 64 + ch * 16)) = pack8_f16(Sm + 8 * ch);
+    };
+    if (owner) write_state_operand();
     fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
+    named_bar_and(kChainBar, kChainCount, true);
 
-    // MMA2: D[:, 64:128] = K^T (Vs_hi + Vs_lo)  (state increment)
-    // MMA3: D[64:128, 128:192] = P_hi Vu_hi + P_hi Vu_lo + P_lo Vu_hi  (intra-chunk output)
-    if (tid == 0) {
+    for (int c = 0; c < NC; ++c) {
+      const int es = c % kEStages;
+      uint8_t* st = sm + es * kEStage;
+      ok = mbar_wait(&fullE[es], (c / kEStages) & 1, kWaitBudget) && !*(volatile int*)&abort_flag;
+      if (tid == 0 && ok) {
+        // MMA_A: D[:, 0:32] = [W; Q'] S  (rows 0-63 W S, rows 64-127 Q' S)
+        tc_fence_after();
+        const uint32_t idesc = idesc_f16(128, kN, false, true);
+        const uint32_t sb = smem_u32(sm + kOffSb);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t aa = smem_u32(st) + (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16(tb, smem_desc(aa, 16, 1024), smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
+        }
+        mma_commit(&bar_a);
+      }
+      if (!named_bar_and(kChainBar, kChainCount, ok)) break;
+
+      ok = mbar_wait(&bar_a, c & 1, kWaitBudget);
       tc_fence_after();
-      const uint32_t id2 = idesc_bf16(128, 64, true, true);
-      const uint32_t id3 = idesc_bf16(128, 64, false, true);
-      const uint32_t kt = smem_u32(st + kStK0);
-      const uint32_t vsh = smem_u32(sm + kOffVsh), vsl = smem_u32(sm + kOffVsl);
-      const uint32_t vuh = smem_u32(sm + kOffVuh), vul = smem_u32(sm + kOffVul);
-      const uint32_t ph = smem_u32(st + kStQ1), pl = smem_u32(st + kStPh);   // rows 64-127 = P_hi / P_lo
+      if (vrow) {
+        // Vnew row i = U_i - (W S)_i on 16 value columns; Vs = sk_i Vnew as fp16 MN-major rows
+        float ws_[16], un[16];
+        tmem_ld16(tb + lane_base + ch0, ws_);
+        const float sk = reinterpret_cast<const float*>(st + kES)[i];
+        const uint8_t* urow = st + kEU;
+        unpack8_f16(*reinterpret_cast<const uint4*>(urow + swz64(i * 64 + (ch0 / 8) * 16)), un);
+        unpack8_f16(*reinterpret_cast<const uint4*>(urow + swz64(i * 64 + (ch0 / 8 + 1) * 16)), un + 8);
+        float vs[16];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(tb + 64, smem_desc(kt + kk * 2048, 8192, 1024), smem_desc(vsh + kk * 2048, 8192, 1024), id2, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(tb + 64, smem_desc(kt + kk * 2048, 8192, 1024), smem_desc(vsl + kk * 2048, 8192, 1024), id2, 1);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(tb + 128, smem_desc(ph + kk * 32, 16, 1024), smem_desc(vuh + kk * 2048, 8192, 1024), id3, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(tb + 128, smem_desc(ph + kk * 32, 16, 1024), smem_desc(vul + kk * 2048, 8192, 1024), id3, 1);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(tb + 128, smem_desc(pl + kk * 32, 16, 1024), smem_desc(vuh + kk * 2048, 8192, 1024), id3, 1);
-      mma_commit(&bar_mma);
-    }
-    ok = mbar_wait(&bar_mma, 1, kWaitBudget);
-    if (!__syncthreads_and(ok)) goto fail;
-    tc_fence_after();
-
-    {
-      // S = Gamma_C S + X (this thread's key row), then the bf16 operand for the next chunk
-      const float gc = sc[128];
-      float x[32];
-      tmem_ld32(tb + lane_base + 64, x);
-#pragma unroll
-      for (int n = 0; n < 32; ++n) Sm[n] = fmaf(gc, Sm[n], x[n]);
-      tmem_ld32(tb + lane_base + 96, x);
-#pragma unroll
-      for (int n = 0; n < 32; ++n) Sm[32 + n] = fmaf(gc, Sm[32 + n], x[n]);
-      write_state_operand();
-    }
-    if (tid >= 64) {
-      // o row i = sq_i (Q S)_i + (P Vnew)_i
-      const int p = c * 64 + i;
-      float pv[32];
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        tmem_ld32(tb + lane_base + 128 + part * 32, pv);
+        for (int e = 0; e < 16; ++e) vs[e] = sk * (un[e] - ws_[e]);
+        *reinterpret_cast<uint4*>(sm + kOffVs + swz64(i * 64 + (ch0 / 8) * 16)) = pack8_f16(vs);
+        *reinterpret_cast<uint4*>(sm + kOffVs + swz64(i * 64 + (ch0 / 8 + 1) * 16)) = pack8_f16(vs + 8);
+      } else if (orow) {
+        // o row i = (Q' S)_i + (P U)_i
+        float qs[kN], pu[kN];
+        tmem_ld32(tb + lane_base, qs);
+        const int p = c * 64 + i;
         if (p < a.L) {
-          __nv_bfloat16* orow = a.o + (((size_t)b * a.L + p) * a.Hv + h) * kD + sl * 64 + part * 32;
+          const uint8_t* purow = st + kEPU;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+            unpack8_f16(*reinterpret_cast<const uint4*>(purow + swz64(i * 64 + ch * 16)), pu + 8 * ch);
+          __nv_bfloat16* orow_p = a.o + (((size_t)b * a.L + p) * a.Hv + h) * kD + sl * kN;
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
-            const int n0 = part * 32 + ch * 8;
-            uint4 pk = make_uint4(pack_bf16x2(qs[n0 + 0] + pv[ch * 8 + 0], qs[n0 + 1] + pv[ch * 8 + 1]),
-                                  pack_bf16x2(qs[n0 + 2] + pv[ch * 8 + 2], qs[n0 + 3] + pv[ch * 8 + 3]),
-                                  pack_bf16x2(qs[n0 + 4] + pv[ch * 8 + 4], qs[n0 + 5] + pv[ch * 8 + 5]),
-                                  pack_bf16x2(qs[n0 + 6] + pv[ch * 8 + 6], qs[n0 + 7] + pv[ch * 8 + 7]));
-            *reinterpret_cast<uint4*>(orow + ch * 8) = pk;
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = qs[8 * ch + e] + pu[8 * ch + e];
+            *reinterpret_cast<uint4*>(orow_p + 8 * ch) = pack8_bf16(v);
           }
         }
       }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-  }
+      fence_async_smem();
+      tc_fence_before();
+      if (!named_bar_and(kChainBar, kChainCount, ok)) break;
 
-  if (a.S_T) {
-    float* dst = a.S_T + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * 64;
+      // MMA2: D[:, 32:64] = K^T Vs
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t id2 = idesc_f16(128, kN, true, true);
+        const uint32_t kt = smem_u32(st + kEK0), vs = smem_u32(sm + kOffVs);
 #pragma unroll
-    for (int n = 0; n < 64; n += 4)
-      *reinterpret_cast<float4*>(dst + n) = make_float4(Sm[n], Sm[n + 1], Sm[n + 2], Sm[n + 3]);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(tb + 32, smem_desc(kt + kk * 2048, 8192, 1024), smem_desc(vs + kk * 1024, 4096, 512, kSwizzle64B),
+                   id2, kk > 0);
+        mma_commit(&bar_x);
+      }
+      if (owner) {
+        // S = Gamma_C S + K^T Vs (this thread's key row), then the fp16 operand for the next chunk
+        ok = mbar_wait(&bar_x, c & 1, kWaitBudget);
+        tc_fence_after();
+        const float gc = reinterpret_cast<const float*>(st + kES)[64];
+        float x[kN];
+        tmem_ld32(tb + lane_base + 32, x);
+#pragma unroll
+        for (int n = 0; n < kN; ++n) Sm[n] = fmaf(gc, Sm[n], x[n]);
+        write_state_operand();
+      }
+      fence_async_smem();
+      tc_fence_before();
+      if (!named_bar_and(kChainBar, kChainCount, ok)) break;
+      // this CTA is done with stage es (MMA_A and MMA2 completed, U, P U and scales read)
+      if (tid >= 96 && tid < 96 + kSlices && c + kEStages < NC) remote_arrive(&freeE[es], tid - 96);
+    }
+    if (ok && owner && a.S_T) {
+      float* dst = a.S_T + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
+#pragma unroll
+      for (int n = 0; n < kN; n += 4)
+        *reinterpret_cast<float4*>(dst + n) = make_float4(Sm[n], Sm[n + 1], Sm[n + 2], Sm[n + 3]);
+    }
   }
-  goto done;
-fail:
-  if (tid == 0) set_error(a.err, kErrTimeout);
-done:
+  if (!ok) {
+    atomicExch(&abort_flag, 1);
+    set_error(a.err, kErrTimeout);
+  }
+  __syncwarp();         // the producer warp's lanes reconverge before the block barrier
+  tc_fence_before();
   __syncthreads();
+  cluster_sync_all();   // no CTA leaves while a peer may still multicast into it or arrive on it
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tb, 256);
+    tmem_dealloc(tb, kTmemState);
   }
 }
 
@@ -642,11 +789,15 @@ bool make_map(CUtensorMap* m, const void* base, int B, int L, int H) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+size_t units_bytes(int B, int L, int Hv) {
+  return (size_t)B * Hv * ((L + kChunk - 1) / kChunk) * kUnitBytes;
+}
+
 }  // namespace
 
-size_t chunk_workspace_bytes(int B, int L, int Hv) {
+size_t chunk_workspace_bytes(int B, int Hk, int L, int Hv) {
   const size_t NC = (size_t)(L + kChunk - 1) / kChunk;
-  return (size_t)B * Hv * NC * kUnitBytes + 1024;
+  return units_bytes(B, L, Hv) + (size_t)B * Hk * NC * kKBytes + 1024;
 }
 
 cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
@@ -661,6 +812,7 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   a.o = static_cast<__nv_bfloat16*>(p.o);
   a.S_T = p.S_T;
   a.ws = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p.ws) + 1023) & ~uintptr_t(1023));
+  a.wsk = a.ws + units_bytes(p.B, p.L, p.Hv);
   a.B = p.B;
   a.L = p.L;
   a.Hk = p.Hk;
@@ -668,19 +820,17 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   a.NC = (p.L + kChunk - 1) / kChunk;
   a.err = p.err;
 
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
-    cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
-    attr_set = true;
-  }
+  cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
+  if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkPrep);
-  chunk_prep_kernel<<<dim3(a.NC, p.Hk, p.B), kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
+  chunk_prep_kernel<<<dim3(a.NC, p.Hv, p.B), kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
   stage_timer_end(slot, s);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   slot = stage_timer_begin(s, kKernChunkState);
-  chunk_state_kernel<<<dim3(kD / 64, p.Hv, p.B), kStateThreads, kStateSmem, s>>>(mq, mk, a);
+  chunk_state_kernel<<<dim3(kSlices, p.Hv, p.B), kStateThreads, kStateSmem, s>>>(a);
   stage_timer_end(slot, s);
   return cudaGetLastError();
 }

@@ -43,7 +43,7 @@ struct RecurrentArgs {
 cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t s);
 
 // Chunked tensor-core path for bf16 q/k/v (two kernels: per-chunk WY factors, then the state
-// recurrence). ws must hold chunk_workspace_bytes(B, L, Hv) bytes.
+// recurrence). ws must hold chunk_workspace_bytes(B, Hk, L, Hv) bytes.
 struct ChunkLaunch {
   const void* q;
   const void* k;
@@ -57,7 +57,7 @@ struct ChunkLaunch {
   int B, L, Hk, Hv;
   int* err;
 };
-size_t chunk_workspace_bytes(int B, int L, int Hv);
+size_t chunk_workspace_bytes(int B, int Hk, int L, int Hv);
 cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s);
 
 // Record a one-line message for gdr_last_error_message() on this host thread; returns status.
