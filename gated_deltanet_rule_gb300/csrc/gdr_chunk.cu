@@ -105,110 +105,175 @@ __device__ __forceinline__ void unpack8_f16(uint4 w, float* v) {
 // -------------------------------------------------------------------------------------------
 // Kernel 1: per-chunk factors
 // -------------------------------------------------------------------------------------------
-constexpr int kPrepThreads = 128;
+constexpr int kPrepThreads = 256;
 constexpr uint32_t kPQ0 = 0, kPK0 = 8192, kPQ1 = 16384, kPK1 = 24576;   // [q|k] K-atoms (Gram operand)
-constexpr uint32_t kPV = 32768;       // v atoms; later the MN-major operand [W0 | W1 | U0 | U1]
-constexpr uint32_t kPAop = 65536;     // MN-major operand [A1 | A2], fp16
-constexpr uint32_t kPP = 81920;       // P, K-major fp16 rows 0-63 (rows 64-127 of the operand unused)
-constexpr uint32_t kPAm = 90112;      // A (strict lower) and T^T (strict upper), float32 [64][68]
-constexpr uint32_t kPVec = kPAm + 64 * 68 * 4;   // gam2, Gam, bet, qinv, kinv, tmp: 6 x 64 floats
-constexpr uint32_t kPXs = kPVec + 6 * 64 * 4;    // block-inverse scratch, 32 x 33 floats
-constexpr uint32_t kPrepSmem = kPXs + 32 * 33 * 4 + 1024;
+constexpr uint32_t kPV = 32768;       // v atoms; then the MN-major operand [W0 | W1 | U0 | U1]; W0 | W1
+                                      // is also the workspace image of W; then the staged P U slices
+constexpr uint32_t kPXs = 49152;      // inverse scratch (free until U is written there)
+// P: K-major fp16 rows 0-63. The P [W | U] MMA has M = 128 and also reads operand rows 64-127 (the
+// 8 KB after P, here the start of AT): their products land in TMEM lanes 64-127, which nobody reads.
+constexpr uint32_t kPP = 65536;
+constexpr uint32_t kPAT = kPP + 8192;           // fp32 [64][68]: A strictly lower, 1 on the diagonal, T^T strictly
+                                                // upper; then the staged U slices
+constexpr uint32_t kPTm = kPAT + 64 * 68 * 4;   // fp32 [64][68]: T row-major (zero above the diagonal)
+constexpr uint32_t kPAop = kPTm;                // after the inverse: MN-major operand [A1 | A2], fp16; then
+                                                // the staged Q' image
+constexpr uint32_t kPVec = kPTm + 64 * 68 * 4;  // gam2, Gam, bet, qinv, kinv, e1: 6 x 64 floats
+constexpr uint32_t kPE2 = kPVec + 6 * 64 * 4;   // E2[I][j] = ki_j exp(gamma_16I - gamma_j): [4][68] floats
+constexpr uint32_t kPrepSmem = kPE2 + 4 * 68 * 4 + 1024;
+static_assert(kPTm % 1024 == 0 && kPP % 1024 == 0, "operand tiles need 1024-byte alignment");
+static_assert(kPP + 16384 <= kPrepSmem - 1024 && kPAop + 16384 <= kPVec, "M = 128 operands stay inside the buffer");
 
-// T = (I + A)^-1 for the strictly lower 64 x 64 A held in Am (row stride 68). T's strictly lower
-// part is stored transposed in Am's strictly upper part: T(i, j) = Am[j * 68 + i] for i > j.
-// 16 x 16 diagonal blocks by forward substitution, then T_IJ = -T_II (A_IJ T_JJ) for the
-// 16-blocks (1,0), (3,2) and finally for the 32-block (1,0).
-__device__ __forceinline__ float tval(const float* Am, int i, int j) {   // T(i, j)
-  return (i == j) ? 1.f : ((i > j) ? Am[j * 68 + i] : 0.f);
-}
-
-__device__ void block_inverse(float* Am, float* Xs, int tid) {
-  // 1. diagonal 16 x 16 blocks, one column per thread (threads 0-63)
+// T = (I + A)^-1 for the strictly lower 64 x 64 A in AT (row stride 68, 1 on the diagonal), by
+// recursive doubling: 16 x 16 diagonal blocks by forward substitution, then the merges
+// T_BL = -T_BR (A_BL T_TL) for the 16-blocks (1,0), (3,2) and for the 32-block (1,0). T is written
+// twice: transposed into AT's strictly upper part (T(i, j) = AT[j][i], a column of T is a row of
+// AT) and row-major into Tm, whose diagonal is 1 and upper part 0 on entry. Entries of A are
+// zeroed once consumed, so that a row of AT restricted to a finished diagonal block is exactly a
+// column of T. Block products read rows of the left factor and columns of the right factor as
+// contiguous float4 runs, and skip the blocks that are zero by triangularity.
+__device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  // 1. diagonal 16-blocks: thread = (block, column), right-looking substitution; a block's 16
+  //    threads share a warp
   if (tid < 64) {
     const int r0 = (tid >> 4) * 16, col = tid & 15;
     float x[16];
 #pragma unroll
+    for (int ii = 0; ii < 16; ++ii) x[ii] = (ii == col) ? 1.f : 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 15; ++jj) {
+#pragma unroll
+      for (int ii = jj + 1; ii < 16; ++ii) x[ii] = fmaf(-AT[(r0 + ii) * 68 + r0 + jj], x[jj], x[ii]);
+    }
+    __syncwarp();
+#pragma unroll
     for (int ii = 0; ii < 16; ++ii) {
-      float acc = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < ii; ++jj) acc = fmaf(Am[(r0 + ii) * 68 + r0 + jj], x[jj], acc);
-      x[ii] = (ii == col) ? 1.f : ((ii < col) ? 0.f : -acc);
+      if (ii > col) {
+        Tm[(r0 + ii) * 68 + r0 + col] = x[ii];
+        AT[(r0 + col) * 68 + r0 + ii] = x[ii];
+      } else if (ii < col) {
+        AT[(r0 + col) * 68 + r0 + ii] = 0.f;
+      }
     }
-#pragma unroll
-    for (int ii = 0; ii < 16; ++ii)
-      if (ii > col) Am[(r0 + col) * 68 + r0 + ii] = x[ii];
   }
   __syncthreads();
-  // 2. 16-blocks (1,0) and (3,2): X = A_IJ T_JJ, then T_IJ = -T_II X. Thread: block, row, 4 columns.
+  // 2. 16-block merges p = 0, 1 (TL = [32p, 32p+16), BR = [32p+16, 32p+32)). Lane: (p, row i);
+  //    warp: columns 2w, 2w+1.
   {
-    const int blk = tid >> 6, e = tid & 63, rr = e >> 2, c0 = (e & 3) * 4;
-    const int I = 1 + 2 * blk, J = 2 * blk;
-    float xv[4] = {0.f, 0.f, 0.f, 0.f};
+    const int p = lane >> 4, i = lane & 15, base = 32 * p;
+    float ar[16];
+    const float4* arow = reinterpret_cast<const float4*>(AT + (base + 16 + i) * 68 + base);
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float av = Am[(16 * I + rr) * 68 + 16 * J + m];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) xv[q] = fmaf(av, tval(Am, 16 * J + m, 16 * J + c0 + q), xv[q]);
+    for (int m4 = 0; m4 < 4; ++m4) {
+      const float4 t = arow[m4];
+      ar[4 * m4] = t.x; ar[4 * m4 + 1] = t.y; ar[4 * m4 + 2] = t.z; ar[4 * m4 + 3] = t.w;
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) Xs[(blk * 16 + rr) * 17 + c0 + q] = xv[q];
+    for (int q = 0; q < 2; ++q) {
+      const int j = 2 * warp + q;
+      const float4* tcol = reinterpret_cast<const float4*>(AT + (base + j) * 68 + base);   // column j of T_TL
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 t = tcol[m4];
+        acc0 = fmaf(ar[4 * m4], t.x, acc0);
+        acc1 = fmaf(ar[4 * m4 + 1], t.y, acc1);
+        acc0 = fmaf(ar[4 * m4 + 2], t.z, acc0);
+        acc1 = fmaf(ar[4 * m4 + 3], t.w, acc1);
+      }
+      Xs[(p * 16 + j) * 20 + i] = acc0 + acc1;    // X column-major
+    }
     __syncthreads();
-    float tv[4];
+    if (warp < 4)   // A_BL consumed
+      reinterpret_cast<float4*>(AT + (base + 16 + i) * 68 + base)[warp] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float tr[16];
+    const float4* trow = reinterpret_cast<const float4*>(Tm + (base + 16 + i) * 68 + base + 16);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) tv[q] = Xs[(blk * 16 + rr) * 17 + c0 + q];
-    for (int m = 0; m < rr; ++m) {
-      const float t = Am[(16 * I + m) * 68 + 16 * I + rr];   // T(16I + rr, 16I + m)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tv[q] = fmaf(t, Xs[(blk * 16 + m) * 17 + c0 + q], tv[q]);
+    for (int m4 = 0; m4 < 4; ++m4) {
+      const float4 t = trow[m4];
+      tr[4 * m4] = t.x; tr[4 * m4 + 1] = t.y; tr[4 * m4 + 2] = t.z; tr[4 * m4 + 3] = t.w;
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) Am[(16 * J + c0 + q) * 68 + 16 * I + rr] = -tv[q];
+    for (int q = 0; q < 2; ++q) {
+      const int j = 2 * warp + q;
+      const float4* xcol = reinterpret_cast<const float4*>(Xs + (p * 16 + j) * 20);
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 t = xcol[m4];
+        acc0 = fmaf(tr[4 * m4], t.x, acc0);
+        acc1 = fmaf(tr[4 * m4 + 1], t.y, acc1);
+        acc0 = fmaf(tr[4 * m4 + 2], t.z, acc0);
+        acc1 = fmaf(tr[4 * m4 + 3], t.w, acc1);
+      }
+      Tm[(base + 16 + i) * 68 + base + j] = -(acc0 + acc1);
+      AT[(base + j) * 68 + base + 16 + i] = -(acc0 + acc1);
+    }
   }
   __syncthreads();
-  // 3. 32-block (1,0): X = A(32:64, 0:32) T(0:32, 0:32), then T(32:64, 0:32) = -T(32:64, 32:64) X.
-  //    Thread: row rr, 8 columns.
+  // 3. 32-block merge. X = A_BL T_TL: lane = row i, warp = columns 4w .. 4w + 3; columns >= 16
+  //    only meet rows >= 16 of T_TL.
   {
-    const int rr = tid >> 2, c0 = (tid & 3) * 8;
+    const int i = lane;
     float ar[32];
-    const float4* arow = reinterpret_cast<const float4*>(Am + (32 + rr) * 68);
+    const float4* arow = reinterpret_cast<const float4*>(AT + (32 + i) * 68);
 #pragma unroll
     for (int m4 = 0; m4 < 8; ++m4) {
-      const float4 v = arow[m4];
-      ar[4 * m4] = v.x; ar[4 * m4 + 1] = v.y; ar[4 * m4 + 2] = v.z; ar[4 * m4 + 3] = v.w;
+      const float4 t = arow[m4];
+      ar[4 * m4] = t.x; ar[4 * m4 + 1] = t.y; ar[4 * m4 + 2] = t.z; ar[4 * m4 + 3] = t.w;
     }
-    float xv[8];
+    auto prod1 = [&](const int m4lo) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int cc = c0 + q;
-      const float4* trow = reinterpret_cast<const float4*>(Am + cc * 68);   // T(m, cc) = Am[cc*68+m], m > cc
-      float acc = 0.f;
+      for (int q = 0; q < 4; ++q) {
+        const int j = 4 * warp + q;
+        const float4* tcol = reinterpret_cast<const float4*>(AT + j * 68);
+        float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-      for (int m4 = 0; m4 < 8; ++m4) {
-        const float4 v = trow[m4];
-        const float tv4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int m = 4 * m4 + u;
-          const float t = (m > cc) ? tv4[u] : ((m == cc) ? 1.f : 0.f);
-          acc = fmaf(ar[m], t, acc);
+        for (int m4 = m4lo; m4 < 8; ++m4) {
+          const float4 t = tcol[m4];
+          acc0 = fmaf(ar[4 * m4], t.x, acc0);
+          acc1 = fmaf(ar[4 * m4 + 1], t.y, acc1);
+          acc0 = fmaf(ar[4 * m4 + 2], t.z, acc0);
+          acc1 = fmaf(ar[4 * m4 + 3], t.w, acc1);
         }
+        Xs[j * 36 + i] = acc0 + acc1;
       }
-      xv[q] = acc;
-    }
+    };
+    if (warp >= 4) prod1(4);
+    else prod1(0);
+  }
+  __syncthreads();
+  // T_BL = -T_BR X: warp = rows 4w .. 4w + 3 of the bottom block, lane = column j; rows < 16 only
+  // meet columns < 16 of T_BR.
+  {
+    const int j = lane;
+    auto prod2 = [&](const int m4hi) {
+      float xc[32];
+      const float4* xcol = reinterpret_cast<const float4*>(Xs + j * 36);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) Xs[rr * 33 + c0 + q] = xv[q];
-    __syncthreads();
-    float tv[8];
+      for (int m4 = 0; m4 < m4hi; ++m4) {
+        const float4 t = xcol[m4];
+        xc[4 * m4] = t.x; xc[4 * m4 + 1] = t.y; xc[4 * m4 + 2] = t.z; xc[4 * m4 + 3] = t.w;
+      }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) tv[q] = Xs[rr * 33 + c0 + q];
-    for (int m = 0; m < rr; ++m) {
-      const float t = Am[(32 + m) * 68 + 32 + rr];   // T(32 + rr, 32 + m)
+      for (int q = 0; q < 4; ++q) {
+        const int i = 4 * warp + q;
+        const float4* trow = reinterpret_cast<const float4*>(Tm + (32 + i) * 68 + 32);
+        float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) tv[q] = fmaf(t, Xs[m * 33 + c0 + q], tv[q]);
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) Am[(c0 + q) * 68 + 32 + rr] = -tv[q];
+        for (int m4 = 0; m4 < m4hi; ++m4) {
+          const float4 t = trow[m4];
+          acc0 = fmaf(t.x, xc[4 * m4], acc0);
+          acc1 = fmaf(t.y, xc[4 * m4 + 1], acc1);
+          acc0 = fmaf(t.z, xc[4 * m4 + 2], acc0);
+          acc1 = fmaf(t.w, xc[4 * m4 + 3], acc1);
+        }
+        AT[j * 68 + 32 + i] = -(acc0 + acc1);
+      }
+    };
+    if (warp >= 4) prod2(8);
+    else prod2(4);
   }
   __syncthreads();
 }
@@ -222,16 +287,19 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __shared__ uint32_t tmem_base;
 
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = a.Hv / a.Hk, hk = h / r;
-  float* Am = reinterpret_cast<float*>(sm + kPAm);
+  float* AT = reinterpret_cast<float*>(sm + kPAT);
+  float* Tm = reinterpret_cast<float*>(sm + kPTm);
+  float* Xs = reinterpret_cast<float*>(sm + kPXs);
   float* gam2 = reinterpret_cast<float*>(sm + kPVec);     // cumulative log-decay times log2(e)
   float* Gam = gam2 + 64;
   float* bet = gam2 + 128;
   float* qinv = gam2 + 192;
   float* kinv = gam2 + 256;
-  float* tmp = gam2 + 320;
-  float* Xs = reinterpret_cast<float*>(sm + kPXs);
+  float* e1 = gam2 + 320;                                  // exp(gamma_i - gamma_16I); scan scratch first
+  float* E2 = reinterpret_cast<float*>(sm + kPE2);
+  uint8_t* ub = unit_base(a, b, h, c);
 
   // gates of this chunk; positions past L read as beta = g = 0
   float gg = 0.f, bb = 0.f;
@@ -243,23 +311,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   }
   if (tid == 0) {
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(&tmem_base, 256);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = tmem_base;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const int i = tid & 63;
-  bool ok = true;
-
-  if (tid == 0) {
     mbar_arrive_expect_tx(&bar_ld, 49152);
     tma_load_4d(sm + kPQ0, &tm_q, &bar_ld, 0, hk, c * 64, b);
     tma_load_4d(sm + kPQ1, &tm_q, &bar_ld, 64, hk, c * 64, b);
@@ -268,47 +322,39 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tma_load_4d(sm + kPV, &tm_v, &bar_ld, 0, h, c * 64, b);
     tma_load_4d(sm + kPV + 8192, &tm_v, &bar_ld, 64, h, c * 64, b);
   }
+  if (warp == 1) tmem_alloc(&tmem_base, 256);
+  // T's row-major copy starts as the identity (its upper part stays zero)
+  for (int e = tid; e < 64 * 17; e += kPrepThreads) {
+    const int rr = e / 17, c4 = e - rr * 17;
+    const int d = ((rr >> 2) == c4) ? (rr & 3) : -1;
+    reinterpret_cast<float4*>(Tm + rr * 68)[c4] =
+        make_float4(d == 0 ? 1.f : 0.f, d == 1 ? 1.f : 0.f, d == 2 ? 1.f : 0.f, d == 3 ? 1.f : 0.f);
+  }
   // inclusive scan of g over the chunk (warps 0 and 1, then warp 1 adds warp 0's total)
   if (tid < 64) {
     float x = gg;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const float y = __shfl_up_sync(0xffffffffu, x, off);
-      if ((tid & 31) >= off) x += y;
+      if (lane >= off) x += y;
     }
-    tmp[tid] = x;
+    e1[tid] = x;
     bet[tid] = bb;
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  bool ok = true;
   if (tid < 64) {
-    const float gam = tmp[tid] + (tid >= 32 ? tmp[31] : 0.f);
+    const float gam = e1[tid] + (tid >= 32 ? e1[31] : 0.f);
     gam2[tid] = gam * kLog2e;
     Gam[tid] = exp2f(gam * kLog2e);
   }
 
   ok = mbar_wait(&bar_ld, 0, kWaitBudget);
   if (!__syncthreads_and(ok)) goto fail;
-
-  // inverse norms: thread t < 64 reads q row t, t >= 64 reads k row t - 64 (order-free sum)
-  {
-    const uint8_t* base = sm + (tid < 64 ? kPQ0 : kPK0) + i * 128;
-    float s = 0.f;
-#pragma unroll
-    for (int atom = 0; atom < 2; ++atom) {
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 w = *reinterpret_cast<const uint4*>(base + atom * 16384 + ch * 16);
-        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xFFFF0000u);
-          s = fmaf(lo, lo, s);
-          s = fmaf(hi, hi, s);
-        }
-      }
-    }
-    (tid < 64 ? qinv : kinv)[i] = rsqrtf(s + 1e-6f);
-  }
 
   // Gram MMA (bf16, exact products): D[0:128, 0:64] = [Q; K] K^T
   if (tid == 0) {
@@ -321,49 +367,108 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     mma_commit(&bar_mma);
   }
+  // inverse norms: two threads per row (one 64-column atom each); rows 0-63 q, 64-127 k
+  {
+    const int row = tid >> 1, half = tid & 1, rr = row & 63;
+    const uint8_t* base = sm + (row < 64 ? kPQ0 : kPK0) + half * 16384 + rr * 128;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      const uint4 w = *reinterpret_cast<const uint4*>(base + ch * 16);
+      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xFFFF0000u);
+        s0 = fmaf(lo, lo, s0);
+        s1 = fmaf(hi, hi, s1);
+      }
+    }
+    float s = s0 + s1;
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    if (half == 0) (row < 64 ? qinv : kinv)[rr] = rsqrtf(s + 1e-6f);
+  }
+  __syncthreads();
+  // decay factors through the 16-block anchors: for j < 16 I <= i,
+  // exp(gamma_i - gamma_j) = exp(gamma_i - gamma_16I) * exp(gamma_16I - gamma_j), both factors <= 1
+  if (tid < 64) {
+    e1[tid] = ex2_approx(gam2[tid] - gam2[tid & ~15]);
+  } else {
+    const int I = 1 + ((tid - 64) >> 6), j = tid & 63;
+    E2[I * 68 + j] = (j < 16 * I) ? kinv[j] * ex2_approx(gam2[16 * I] - gam2[j]) : 0.f;
+  }
   ok = mbar_wait(&bar_mma, 0, kWaitBudget);
   if (!__syncthreads_and(ok)) goto fail;
   tc_fence_after();
 
   {
-    // this thread's Gram row: rows 0-63 = (Q K^T)_i,:, rows 64-127 = (K K^T)_i,:
-    float G[64];
-    tmem_ld32(tb + lane_base + 0, G);
-    tmem_ld32(tb + lane_base + 32, G + 32);
+    // this thread's half Gram row: TMEM lane 32 (warp % 4) + lane, columns jb .. jb + 31
+    // (rows 0-63: (Q K^T)_i,:, rows 64-127: (K K^T)_i,:), as two 16-column blocks J
+    const int row = 32 * (warp & 3) + lane, i = row & 63, jb = (warp >> 2) * 32, I = i >> 4;
+    const bool isK = row >= 64;
+    float G[32];
+    tmem_ld32(tb + lane_base + jb, G);
     tc_fence_before();
+    const float rowf = isK ? bet[i] * kinv[i] : qinv[i] * kScale;
+    const float rowe = rowf * e1[i];
     const float gi = gam2[i];
-    if (tid >= 64) {
-      // row i of A (strict lower) into shared memory; the upper part is written by the inverse
-      const float si = bet[i] * kinv[i];
-      float4* arow = reinterpret_cast<float4*>(Am + i * 68);
+    const int jlim = isK ? i : i + 1;     // A keeps j < i, P keeps j <= i
+    float v[32];
 #pragma unroll
-      for (int j4 = 0; j4 < 16; ++j4) {
-        float v[4];
+    for (int hb = 0; hb < 2; ++hb) {
+      const int J = (jb >> 4) + hb;
+      float* vv = v + 16 * hb;
+      const float* Gv = G + 16 * hb;
+      if (J < I) {
+        const float4* e4 = reinterpret_cast<const float4*>(E2 + I * 68 + 16 * J);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = 4 * j4 + e;
-          v[e] = (j < i) ? si * kinv[j] * G[j] * ex2_approx(gi - gam2[j]) : 0.f;
+        for (int q = 0; q < 4; ++q) {
+          const float4 t = e4[q];
+          vv[4 * q] = rowe * t.x * Gv[4 * q];
+          vv[4 * q + 1] = rowe * t.y * Gv[4 * q + 1];
+          vv[4 * q + 2] = rowe * t.z * Gv[4 * q + 2];
+          vv[4 * q + 3] = rowe * t.w * Gv[4 * q + 3];
         }
-        arow[j4] = make_float4(v[0], v[1], v[2], v[3]);
+      } else if (J == I) {
+        const float4* k4 = reinterpret_cast<const float4*>(kinv + 16 * J);
+        const float4* g4 = reinterpret_cast<const float4*>(gam2 + 16 * J);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 kq = k4[q], gq = g4[q];
+          const float kk[4] = {kq.x, kq.y, kq.z, kq.w}, gm[4] = {gq.x, gq.y, gq.z, gq.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = 16 * J + 4 * q + u;
+            const float d = rowf * kk[u] * ex2_approx(gi - gm[u]);
+            vv[4 * q + u] = (j < jlim) ? d * Gv[4 * q + u] : 0.f;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) vv[e] = 0.f;
+      }
+    }
+    if (isK) {
+      // row i of A into AT (1 on the diagonal; the upper part is overwritten by the inverse)
+      float4* arow = reinterpret_cast<float4*>(AT + i * 68 + jb);
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        float t[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) t[e] = (jb + 4 * j4 + e == i) ? 1.f : v[4 * j4 + e];
+        arow[j4] = make_float4(t[0], t[1], t[2], t[3]);
       }
     } else {
       // row i of P (lower, diagonal included) as fp16 K-major operand row
-      const float si = qinv[i] * kScale;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = 8 * ch + e;
-          v[e] = (j <= i) ? si * kinv[j] * G[j] * ex2_approx(gi - gam2[j]) : 0.f;
-        }
-        *reinterpret_cast<uint4*>(sm + kPP + i * 128 + ((ch ^ (i & 7)) << 4)) = pack8_f16(v);
+      for (int q = 0; q < 4; ++q) {
+        const int ch = (jb >> 3) + q;
+        *reinterpret_cast<uint4*>(sm + kPP + i * 128 + ((ch ^ (i & 7)) << 4)) = pack8_f16(v + 8 * q);
       }
     }
     // k and v tiles to fp16 in place (the Gram MMA that read k as bf16 has completed)
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int chunk16 = tid * 16 + n;                 // 2048 chunks of 16 B: k atoms then v atoms
+    for (int n = 0; n < 8; ++n) {
+      const int chunk16 = n * kPrepThreads + tid;       // 2048 chunks of 16 B: k atoms then v atoms
       const int which = chunk16 >> 9, off = (chunk16 & 511) * 16;
       const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPV + (which - 2) * 8192);
       uint4* p = reinterpret_cast<uint4*>(sm + base + off);
@@ -374,23 +479,21 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   __syncthreads();
 
-  block_inverse(Am, Xs, tid);
+  invert_unit_lower(AT, Tm, Xs, tid);
 
   // operand [A1; A2] = [T diag(beta Gamma ki); T diag(beta)], MN-major: K-row j holds column j of T
   {
-    const int j = i, blk = tid >> 6;
+    const int j = tid & 63, blk = (tid >> 6) & 1, hf = tid >> 7;
     const float s = blk ? bet[j] : bet[j] * Gam[j] * kinv[j];
-    const float4* trow = reinterpret_cast<const float4*>(Am + j * 68);
+    const float4* trow = reinterpret_cast<const float4*>(AT + j * 68);
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
+    for (int q = 0; q < 4; ++q) {
+      const int ch = 4 * hf + q;
       const float4 t0 = trow[2 * ch], t1 = trow[2 * ch + 1];
       const float tt[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
       float v[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int ii = 8 * ch + e;
-        v[e] = ((ii > j) ? tt[e] : (ii == j ? 1.f : 0.f)) * s;
-      }
+      for (int e = 0; e < 8; ++e) v[e] = (8 * ch + e >= j) ? tt[e] * s : 0.f;
       *reinterpret_cast<uint4*>(sm + kPAop + blk * 8192 + j * 128 + ((ch ^ (j & 7)) << 4)) = pack8_f16(v);
     }
   }
@@ -419,37 +522,27 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_after();
 
   {
-    uint8_t* ub = unit_base(a, b, h, c);
-    if (tid < 64) {
-      // W row i (lanes 0-63, columns 0-127) -> fp16 into the operand blocks W0/W1 (over v, now
-      // consumed) and the workspace image (same bytes)
+    // W rows (TMEM lanes 0-63, warps 0, 1, 4, 5) and U rows (lanes 64-127, warps 2, 3, 6, 7);
+    // warps 0-3 take columns 0-63, warps 4-7 columns 64-127. W goes to its operand block over v
+    // (consumed), which is also byte for byte the workspace image; U to its operand block and,
+    // as the four 32-column slices of the workspace, to a staging area over AT.
+    const int row = 32 * (warp & 3) + lane, i = row & 63, cb = (warp >> 2) * 64;
+    const bool isU = row >= 64;
 #pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        float w[32];
-        tmem_ld32(tb + lane_base + part * 32, w);
+    for (int part = 0; part < 2; ++part) {
+      float w[32];
+      tmem_ld32(tb + lane_base + (isU ? 128 : 0) + cb + part * 32, w);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int col = part * 32 + q4 * 8;
-          const int atom = col >> 6, ch = (col & 63) >> 3;
-          const uint32_t off = atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4);
-          const uint4 pk = pack8_f16(w + q4 * 8);
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int col = cb + part * 32 + q4 * 8;
+        const int atom = col >> 6, ch = (col & 63) >> 3;
+        const uint32_t off = atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4);
+        const uint4 pk = pack8_f16(w + q4 * 8);
+        if (!isU) {
           *reinterpret_cast<uint4*>(sm + kPV + off) = pk;
-          *reinterpret_cast<uint4*>(ub + off) = pk;
-        }
-      }
-    } else {
-      // U row i (lanes 64-127, columns 128-255) -> fp16 into operand blocks U0/U1 and the slices
-#pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        float u[32];
-        tmem_ld32(tb + lane_base + 128 + part * 32, u);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int col = part * 32 + q4 * 8;
-          const int atom = col >> 6, ch = (col & 63) >> 3;
-          const uint4 pk = pack8_f16(u + q4 * 8);
-          *reinterpret_cast<uint4*>(sm + kPV + 16384 + atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4)) = pk;
-          *reinterpret_cast<uint4*>(ub + kUnitU + part * 4096 + swz64(i * 64 + q4 * 16)) = pk;
+        } else {
+          *reinterpret_cast<uint4*>(sm + kPV + 16384 + off) = pk;
+          *reinterpret_cast<uint4*>(sm + kPAT + (col >> 5) * 4096 + swz64(i * 64 + ((col & 31) >> 3) * 16)) = pk;
         }
       }
     }
@@ -458,7 +551,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_before();
   __syncthreads();
 
-  // [P; .] [W | U]: rows 0-63 = P W (columns 0-127) and P U (columns 128-255)
+  // [P; .] [W | U]: rows 0-63 = P W (columns 0-127) and P U (columns 128-255); W and the U slices
+  // leave for the workspace meanwhile
   if (tid == 0) {
     tc_fence_after();
     const uint32_t idesc = idesc_f16(128, 256, false, true);
@@ -467,66 +561,77 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(tb, smem_desc(pa + kk * 32, 16, 1024), smem_desc(wu + kk * 2048, 8192, 1024), idesc, kk > 0);
     mma_commit(&bar_mma);
+    bulk_store(ub, sm + kPV, kWBytes);
+    bulk_store(ub + kUnitU, sm + kPAT, kUBytes);
+    bulk_commit();
   }
   ok = mbar_wait(&bar_mma, 0, kWaitBudget);
   if (!__syncthreads_and(ok)) goto fail;
   tc_fence_after();
 
-  {
-    uint8_t* ub = unit_base(a, b, h, c);
-    if (tid < 64) {
-      // Q'_i = sq_i q_i - (P W)_i (fp16 image), (P U)_i (fp16 slices), scales
-      const float sq = Gam[i] * qinv[i] * kScale;
+  if ((warp & 3) < 2) {
+    // warps 0, 1, 4, 5 (lanes 0-63): Q'_i = sq_i q_i - (P W)_i (fp16 image, staged over T) and
+    // (P U)_i (fp16 slices, staged over the consumed U operand) on columns cb .. cb + 63
+    const int i = 32 * (warp & 3) + lane, cb = (warp >> 2) * 64;
+    const float sq = Gam[i] * qinv[i] * kScale;
 #pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        float w[32];
-        tmem_ld32(tb + lane_base + part * 32, w);
+    for (int part = 0; part < 2; ++part) {
+      float w[32];
+      tmem_ld32(tb + lane_base + cb + part * 32, w);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int col = part * 32 + q4 * 8;
-          const int atom = col >> 6, ch = (col & 63) >> 3;
-          const uint32_t off = atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4);
-          const uint4 qr = *reinterpret_cast<const uint4*>(sm + (atom ? kPQ1 : kPQ0) + i * 128 + ((ch ^ (i & 7)) << 4));
-          const uint32_t q4w[4] = {qr.x, qr.y, qr.z, qr.w};
-          float v[8];
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int col = cb + part * 32 + q4 * 8;
+        const int atom = col >> 6, ch = (col & 63) >> 3;
+        const uint32_t off = atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4);
+        const uint4 qr = *reinterpret_cast<const uint4*>(sm + (atom ? kPQ1 : kPQ0) + i * 128 + ((ch ^ (i & 7)) << 4));
+        const uint32_t q4w[4] = {qr.x, qr.y, qr.z, qr.w};
+        float v[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            v[2 * e] = sq * __uint_as_float(q4w[e] << 16) - w[q4 * 8 + 2 * e];
-            v[2 * e + 1] = sq * __uint_as_float(q4w[e] & 0xFFFF0000u) - w[q4 * 8 + 2 * e + 1];
-          }
-          *reinterpret_cast<uint4*>(ub + kUnitQ + off) = pack8_f16(v);
+        for (int e = 0; e < 4; ++e) {
+          v[2 * e] = sq * __uint_as_float(q4w[e] << 16) - w[q4 * 8 + 2 * e];
+          v[2 * e + 1] = sq * __uint_as_float(q4w[e] & 0xFFFF0000u) - w[q4 * 8 + 2 * e + 1];
         }
-      }
-#pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        float u[32];
-        tmem_ld32(tb + lane_base + 128 + part * 32, u);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *reinterpret_cast<uint4*>(ub + kUnitPU + part * 4096 + swz64(i * 64 + q4 * 16)) = pack8_f16(u + q4 * 8);
-      }
-      float* sc = reinterpret_cast<float*>(ub + kUnitS);
-      sc[i] = exp2f(gam2[63] - gam2[i]) * kinv[i];
-      if (i == 0) sc[64] = Gam[63];
-    } else if (h % r == 0) {
-      // the fp16 k image, once per key head
-      uint8_t* kb = kimg_base(a, b, hk, c);
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const int chunk16 = (tid - 64) * 16 + n;    // 1024 chunks of 16 B over the two k atoms
-        const int atom = chunk16 >> 9, off = (chunk16 & 511) * 16;
-        *reinterpret_cast<uint4*>(kb + atom * 8192 + off) =
-            *reinterpret_cast<const uint4*>(sm + (atom ? kPK1 : kPK0) + off);
+        *reinterpret_cast<uint4*>(sm + kPTm + off) = pack8_f16(v);
       }
     }
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      float u[32];
+      tmem_ld32(tb + lane_base + 128 + cb + part * 32, u);
+      const int col = cb + part * 32;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        *reinterpret_cast<uint4*>(sm + kPV + 16384 + (col >> 5) * 4096 + swz64(i * 64 + q4 * 16)) =
+            pack8_f16(u + q4 * 8);
+    }
+  } else if (warp < 4) {
+    // warps 2, 3: the scales sk_i = exp(gamma_C - gamma_i) ki_i and Gamma_C, staged over P
+    const int i = tid - 64;
+    float* sc = reinterpret_cast<float*>(sm + kPP);
+    sc[i] = exp2f(gam2[63] - gam2[i]) * kinv[i];
+    if (i < 4) sc[64 + i] = (i == 0) ? Gam[63] : 0.f;
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    bulk_store(ub + kUnitQ, sm + kPTm, kQBytes);
+    bulk_store(ub + kUnitPU, sm + kPV + 16384, kPUBytes);
+    bulk_store(ub + kUnitS, sm + kPP, kSCopy);
+    if (h % r == 0) {   // the fp16 k image, once per key head
+      uint8_t* kb = kimg_base(a, b, hk, c);
+      bulk_store(kb, sm + kPK0, 8192);
+      bulk_store(kb + 8192, sm + kPK1, 8192);
+    }
+    bulk_commit();
   }
   goto done;
 fail:
   if (tid == 0) set_error(a.err, kErrTimeout);
 done:
+  if (tid == 0) bulk_wait_read();   // shared memory stays valid until every bulk store has read it
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tb, 256);
   }
