@@ -3,7 +3,8 @@
 // Chunk algebra (64-token chunks; the "R64" form named in Kev-4B-LiteRT "r15_kernel_test.py",
 // with the pair decay computed directly, never as a ratio of cumulative decays). For a chunk with
 // entering state S, gamma_i = sum_{j<=i} g_j, Gamma_i = exp(gamma_i), raw q/k rows and their
-// inverse norms qi_i = (|q_i|^2 + 1e-6)^-1/2, ki_i likewise, sq_i = Gamma_i qi_i D^-1/2:
+// inverse norms qi_i = (|q_i|^2 + 1e-6)^-1/2, ki_i likewise, sq_i = Gamma_i qi_i D^-1/2 and
+// sk_i = exp(gamma_C - gamma_i) ki_i:
 //
 //   A_ij  = beta_i ki_i ki_j (k_i . k_j) exp(gamma_i - gamma_j),  j < i         (strictly lower)
 //   T     = (I + A)^-1                                                          (unit lower)
@@ -11,25 +12,31 @@
 //   P_ij  = qi_i ki_j D^-1/2 (q_i . k_j) exp(gamma_i - gamma_j),  j <= i
 //   Vnew  = U - W S
 //   O     = diag(sq) Q S + P Vnew  =  Q' S + P U,      Q' = diag(sq) Q - P W
-//   S'    = Gamma_C S + K^T diag(exp(gamma_C - gamma) ki) Vnew
+//   S'    = Gamma_C S + K^T diag(sk) Vnew  =  Gamma_C S + M' S + N,
+//           M' = -K^T diag(sk) W,   N = K^T diag(sk) U
+//
+// Everything but S is chunk-local, so the sequential part of the recurrence is one product M' S
+// per chunk (plus Q' S for the output, which nothing later depends on).
 //
 // Every product whose operands are computed values runs on fp16 operands: one fp16 rounding
 // (11-bit significand) costs about an eighth of a bf16 one, and an emulation of every rounding
-// point against the float64 oracle puts the outputs at the floor set by rounding o to bf16.
+// point against the float64 oracle puts the outputs at the floor set by rounding o to bf16 (the
+// M' form's final states come out slightly closer to the oracle than the two-product form's).
 // Operands are assumed inside fp16's range (|x| < 65504), which holds for l2-normalised keys.
 //
 // Kernel 1 (gdr_chunk_prep, one CTA per (row, value head, chunk), all chunks in parallel):
 //   TMA loads raw q, k, v; a bf16 MMA gives [Q; K] K^T (both Gram matrices, exact products); CUDA
-//   cores build A and P; a 16/32-blocked fp32 inverse keeps T^T in A's unused upper triangle; T's
-//   scaled columns form the operand [A1; A2]; MMAs give W = A1 K and U = A2 V, then P [W | U].
-//   Kernel 1 writes, per unit, W and Q' as the 128B-swizzled images kernel 2 uses as its MMA
-//   operand, U and P U as four 32-column fp16 slices, the scales, and once per key head k in fp16.
+//   cores build A and P; a recursive-doubling fp32 inverse gives T; T's scaled columns form the
+//   operand [A1; A2]; MMAs give W = A1 K and U = A2 V, then P [W | U], then
+//   K^T [diag(sk) W | diag(sk) U] = [-M' | N]. Per unit it writes, with bulk copies, M' and Q' as
+//   the 128B-swizzled images kernel 2 uses as MMA operands, N and P U as four 32-column slices, and
+//   Gamma_C.
 // Kernel 2 (gdr_chunk_state, a cluster of 4 CTAs per (row, value head), CTA r owning value columns
 //   [32 r, 32 r + 32), sequential over chunks): the float32 state slice stays in registers. Per
-//   chunk: MMA_A = [W; Q'] S (one M = 128 MMA gives W S and Q' S), then CUDA cores form
-//   Vnew = U - W S, Vs = diag(sk) Vnew and the output rows o = Q' S + P U, then MMA2 = K^T Vs, then
-//   S = Gamma_C S + K^T Vs. The tiles every CTA of the cluster needs (W, Q', K) are TMA-multicast,
-//   each CTA loading a quarter, by a producer warp that runs up to three chunks ahead.
+//   chunk one thread issues D = M' S and O' = Q' S (fp16 copy of S as the B operand); the state
+//   warps form S = Gamma_C S + D + N and the next fp16 copy; two output warps form o = O' + P U
+//   off the critical path. M' and Q' are TMA-multicast across the cluster, each CTA loading a
+//   quarter, by a producer warp that runs up to three chunks ahead.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -51,17 +58,15 @@ constexpr int kSlices = 4;                        // value-column slices per val
 constexpr int kN = kD / kSlices;                  // 32 value columns per state CTA
 
 // Workspace. Per (row, value head, chunk) unit:
-constexpr uint32_t kWBytes = 16384;     // W: 64 x 128 fp16, two 64-column 128B-swizzled atoms
-constexpr uint32_t kQBytes = 16384;     // Q': same layout
-constexpr uint32_t kUBytes = 16384;     // U: four 64 x 32 fp16 slices, rows of 64 B, 64B-swizzled
-constexpr uint32_t kPUBytes = 16384;    // P U: same layout as U
-constexpr uint32_t kSBytes = 512;       // scales: sk[64], Gamma_C
-constexpr uint32_t kSCopy = 272;        // bytes of the scale block kernel 2 copies (16-byte multiple)
-constexpr uint32_t kUnitQ = kWBytes, kUnitU = kUnitQ + kQBytes, kUnitPU = kUnitU + kUBytes;
+constexpr uint32_t kMBytes = 32768;     // M': 128 x 128 fp16, two 64-column 128B-swizzled K-atoms
+constexpr uint32_t kQBytes = 16384;     // Q': 64 x 128 fp16, same layout
+constexpr uint32_t kNBytes = 32768;     // N: four 128 x 32 fp16 slices, rows of 64 B, 64B-swizzled
+constexpr uint32_t kPUBytes = 16384;    // P U: four 64 x 32 fp16 slices, same row layout
+constexpr uint32_t kSBytes = 512;       // Gamma_C (16 bytes used)
+constexpr uint32_t kSCopy = 16;         // bytes of the scale block kernel 2 copies
+constexpr uint32_t kUnitQ = kMBytes, kUnitN = kUnitQ + kQBytes, kUnitPU = kUnitN + kNBytes;
 constexpr uint32_t kUnitS = kUnitPU + kPUBytes;
 constexpr uint32_t kUnitBytes = kUnitS + kSBytes;
-// ... and per (row, key head, chunk): k in fp16, the same image layout as W.
-constexpr uint32_t kKBytes = 16384;
 
 struct ChunkArgs {
   const float* g;
@@ -70,16 +75,12 @@ struct ChunkArgs {
   __nv_bfloat16* o;
   float* S_T;
   uint8_t* ws;       // 1024-aligned
-  uint8_t* wsk;      // fp16 k images, after the units
   int B, L, Hk, Hv, NC;
   int* err;
 };
 
 __device__ __forceinline__ uint8_t* unit_base(const ChunkArgs& a, int b, int h, int c) {
   return a.ws + ((size_t)((size_t)b * a.Hv + h) * a.NC + c) * kUnitBytes;
-}
-__device__ __forceinline__ uint8_t* kimg_base(const ChunkArgs& a, int b, int hk, int c) {
-  return a.wsk + ((size_t)((size_t)b * a.Hk + hk) * a.NC + c) * kKBytes;
 }
 
 __device__ __forceinline__ void set_error(int* err, int code) { atomicCAS(err, 0, code); }
@@ -107,22 +108,24 @@ __device__ __forceinline__ void unpack8_f16(uint4 w, float* v) {
 // -------------------------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
 constexpr uint32_t kPQ0 = 0, kPK0 = 8192, kPQ1 = 16384, kPK1 = 24576;   // [q|k] K-atoms (Gram operand)
-constexpr uint32_t kPV = 32768;       // v atoms; then the MN-major operand [W0 | W1 | U0 | U1]; W0 | W1
-                                      // is also the workspace image of W; then the staged P U slices
+constexpr uint32_t kPV = 32768;       // v atoms; then the MN-major operand [W0 | W1 | U0 | U1]; then
+                                      // the staged Q' image and P U slices
 constexpr uint32_t kPXs = 49152;      // inverse scratch (free until U is written there)
 // P: K-major fp16 rows 0-63. The P [W | U] MMA has M = 128 and also reads operand rows 64-127 (the
 // 8 KB after P, here the start of AT): their products land in TMEM lanes 64-127, which nobody reads.
 constexpr uint32_t kPP = 65536;
-constexpr uint32_t kPAT = kPP + 8192;           // fp32 [64][68]: A strictly lower, 1 on the diagonal, T^T strictly
-                                                // upper; then the staged U slices
+constexpr uint32_t kPAT = kPP + 8192;           // fp32 [64][68]: A strictly lower, 1 on the diagonal, T^T strictly upper
 constexpr uint32_t kPTm = kPAT + 64 * 68 * 4;   // fp32 [64][68]: T row-major (zero above the diagonal)
-constexpr uint32_t kPAop = kPTm;                // after the inverse: MN-major operand [A1 | A2], fp16; then
-                                                // the staged Q' image
-constexpr uint32_t kPVec = kPTm + 64 * 68 * 4;  // gam2, Gam, bet, qinv, kinv, e1: 6 x 64 floats
-constexpr uint32_t kPE2 = kPVec + 6 * 64 * 4;   // E2[I][j] = ki_j exp(gamma_16I - gamma_j): [4][68] floats
+constexpr uint32_t kPAop = kPTm;                // after the inverse: MN-major operand [A1 | A2], fp16
+constexpr uint32_t kPWS = kPAT;                 // after [A1 | A2] is consumed: MN-major operand
+                                                // [sk W | sk U] (32 KB over AT and T); then the staged N
+constexpr uint32_t kPM = 0;                     // after the last products: the staged M' image (over q, k)
+constexpr uint32_t kPVec = kPTm + 64 * 68 * 4;  // gam2, Gam, bet, qinv, kinv, e1, sk: 7 x 64 floats
+constexpr uint32_t kPE2 = kPVec + 7 * 64 * 4;   // E2[I][j] = ki_j exp(gamma_16I - gamma_j): [4][68] floats
 constexpr uint32_t kPrepSmem = kPE2 + 4 * 68 * 4 + 1024;
 static_assert(kPTm % 1024 == 0 && kPP % 1024 == 0, "operand tiles need 1024-byte alignment");
 static_assert(kPP + 16384 <= kPrepSmem - 1024 && kPAop + 16384 <= kPVec, "M = 128 operands stay inside the buffer");
+static_assert(kPWS % 1024 == 0 && kPWS + 32768 <= kPVec, "the [sk W | sk U] operand fits over AT and T");
 
 // T = (I + A)^-1 for the strictly lower 64 x 64 A in AT (row stride 68, 1 on the diagonal), by
 // recursive doubling: 16 x 16 diagonal blocks by forward substitution, then the merges
@@ -298,6 +301,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   float* qinv = gam2 + 192;
   float* kinv = gam2 + 256;
   float* e1 = gam2 + 320;                                  // exp(gamma_i - gamma_16I); scan scratch first
+  float* skv = gam2 + 384;                                 // sk_i = exp(gamma_C - gamma_i) ki_i
   float* E2 = reinterpret_cast<float*>(sm + kPE2);
   uint8_t* ub = unit_base(a, b, h, c);
 
@@ -392,6 +396,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // exp(gamma_i - gamma_j) = exp(gamma_i - gamma_16I) * exp(gamma_16I - gamma_j), both factors <= 1
   if (tid < 64) {
     e1[tid] = ex2_approx(gam2[tid] - gam2[tid & ~15]);
+    skv[tid] = exp2f(gam2[63] - gam2[tid]) * kinv[tid];
   } else {
     const int I = 1 + ((tid - 64) >> 6), j = tid & 63;
     E2[I * 68 + j] = (j < 16 * I) ? kinv[j] * ex2_approx(gam2[16 * I] - gam2[j]) : 0.f;
@@ -523,11 +528,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   {
     // W rows (TMEM lanes 0-63, warps 0, 1, 4, 5) and U rows (lanes 64-127, warps 2, 3, 6, 7);
-    // warps 0-3 take columns 0-63, warps 4-7 columns 64-127. W goes to its operand block over v
-    // (consumed), which is also byte for byte the workspace image; U to its operand block and,
-    // as the four 32-column slices of the workspace, to a staging area over AT.
+    // warps 0-3 take columns 0-63, warps 4-7 columns 64-127. Each goes to its fp16 operand block
+    // over v (consumed) for P [W | U], and scaled by sk_i to the operand [sk W | sk U] for K^T.
     const int row = 32 * (warp & 3) + lane, i = row & 63, cb = (warp >> 2) * 64;
     const bool isU = row >= 64;
+    const float sk = skv[i];
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
       float w[32];
@@ -536,14 +541,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int q4 = 0; q4 < 4; ++q4) {
         const int col = cb + part * 32 + q4 * 8;
         const int atom = col >> 6, ch = (col & 63) >> 3;
-        const uint32_t off = atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4);
-        const uint4 pk = pack8_f16(w + q4 * 8);
-        if (!isU) {
-          *reinterpret_cast<uint4*>(sm + kPV + off) = pk;
-        } else {
-          *reinterpret_cast<uint4*>(sm + kPV + 16384 + off) = pk;
-          *reinterpret_cast<uint4*>(sm + kPAT + (col >> 5) * 4096 + swz64(i * 64 + ((col & 31) >> 3) * 16)) = pk;
-        }
+        const uint32_t off = (isU ? 16384 : 0) + atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4);
+        float ws[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ws[e] = sk * w[q4 * 8 + e];
+        *reinterpret_cast<uint4*>(sm + kPV + off) = pack8_f16(w + q4 * 8);
+        *reinterpret_cast<uint4*>(sm + kPWS + off) = pack8_f16(ws);
       }
     }
   }
@@ -551,8 +554,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_before();
   __syncthreads();
 
-  // [P; .] [W | U]: rows 0-63 = P W (columns 0-127) and P U (columns 128-255); W and the U slices
-  // leave for the workspace meanwhile
+  // [P; .] [W | U]: rows 0-63 = P W (columns 0-127) and P U (columns 128-255)
   if (tid == 0) {
     tc_fence_after();
     const uint32_t idesc = idesc_f16(128, 256, false, true);
@@ -561,17 +563,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(tb, smem_desc(pa + kk * 32, 16, 1024), smem_desc(wu + kk * 2048, 8192, 1024), idesc, kk > 0);
     mma_commit(&bar_mma);
-    bulk_store(ub, sm + kPV, kWBytes);
-    bulk_store(ub + kUnitU, sm + kPAT, kUBytes);
-    bulk_commit();
   }
   ok = mbar_wait(&bar_mma, 0, kWaitBudget);
   if (!__syncthreads_and(ok)) goto fail;
   tc_fence_after();
 
   if ((warp & 3) < 2) {
-    // warps 0, 1, 4, 5 (lanes 0-63): Q'_i = sq_i q_i - (P W)_i (fp16 image, staged over T) and
-    // (P U)_i (fp16 slices, staged over the consumed U operand) on columns cb .. cb + 63
+    // warps 0, 1, 4, 5 (lanes 0-63): Q'_i = sq_i q_i - (P W)_i (fp16 image) and (P U)_i (fp16
+    // slices) on columns cb .. cb + 63, staged over the consumed [W | U] operand
     const int i = 32 * (warp & 3) + lane, cb = (warp >> 2) * 64;
     const float sq = Gam[i] * qinv[i] * kScale;
 #pragma unroll
@@ -591,7 +590,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           v[2 * e] = sq * __uint_as_float(q4w[e] << 16) - w[q4 * 8 + 2 * e];
           v[2 * e + 1] = sq * __uint_as_float(q4w[e] & 0xFFFF0000u) - w[q4 * 8 + 2 * e + 1];
         }
-        *reinterpret_cast<uint4*>(sm + kPTm + off) = pack8_f16(v);
+        *reinterpret_cast<uint4*>(sm + kPV + off) = pack8_f16(v);
       }
     }
 #pragma unroll
@@ -604,24 +603,66 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         *reinterpret_cast<uint4*>(sm + kPV + 16384 + (col >> 5) * 4096 + swz64(i * 64 + q4 * 16)) =
             pack8_f16(u + q4 * 8);
     }
-  } else if (warp < 4) {
-    // warps 2, 3: the scales sk_i = exp(gamma_C - gamma_i) ki_i and Gamma_C, staged over P
-    const int i = tid - 64;
-    float* sc = reinterpret_cast<float*>(sm + kPP);
-    sc[i] = exp2f(gam2[63] - gam2[i]) * kinv[i];
-    if (i < 4) sc[64 + i] = (i == 0) ? Gam[63] : 0.f;
+  } else if (tid == 64) {
+    // Gamma_C, staged over P (consumed)
+    *reinterpret_cast<float4*>(sm + kPP) = make_float4(Gam[63], 0.f, 0.f, 0.f);
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+
+  // K^T [sk W | sk U] = [-M' | N] into columns 0-255 (the P [W | U] results have been read); Q',
+  // P U and Gamma_C leave for the workspace meanwhile
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t idesc = idesc_f16(128, 256, true, true);
+    const uint32_t kt = smem_u32(sm + kPK0);    // k atoms (M blocks) at +8192 and +24576: stride 16384
+    const uint32_t wsu = smem_u32(sm + kPWS);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16(tb, smem_desc(kt + kk * 2048, 16384, 1024), smem_desc(wsu + kk * 2048, 8192, 1024), idesc, kk > 0);
+    mma_commit(&bar_mma);
+    bulk_store(ub + kUnitQ, sm + kPV, kQBytes);
+    bulk_store(ub + kUnitPU, sm + kPV + 16384, kPUBytes);
+    bulk_store(ub + kUnitS, sm + kPP, kSCopy);
+    bulk_commit();
+  }
+  ok = mbar_wait(&bar_mma, 1, kWaitBudget);
+  if (!__syncthreads_and(ok)) goto fail;
+  tc_fence_after();
+
+  {
+    // every warp: key row i = TMEM lane, columns cb .. cb + 63 of M' = -D[:, 0:128] (fp16 K-major
+    // image over q and k, consumed) and of N = D[:, 128:256] (fp16 slices over [sk W | sk U])
+    const int i = 32 * (warp & 3) + lane, cb = (warp >> 2) * 64;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      float w[32];
+      tmem_ld32(tb + lane_base + cb + part * 32, w);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) w[e] = -w[e];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int col = cb + part * 32 + q4 * 8;
+        const int atom = col >> 6, ch = (col & 63) >> 3;
+        *reinterpret_cast<uint4*>(sm + kPM + atom * 16384 + i * 128 + ((ch ^ (i & 7)) << 4)) = pack8_f16(w + q4 * 8);
+      }
+    }
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      float n[32];
+      tmem_ld32(tb + lane_base + 128 + cb + part * 32, n);
+      const int col = cb + part * 32;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        *reinterpret_cast<uint4*>(sm + kPWS + (col >> 5) * 8192 + swz64(i * 64 + q4 * 16)) = pack8_f16(n + q4 * 8);
+    }
   }
   fence_async_smem();
   __syncthreads();
   if (tid == 0) {
-    bulk_store(ub + kUnitQ, sm + kPTm, kQBytes);
-    bulk_store(ub + kUnitPU, sm + kPV + 16384, kPUBytes);
-    bulk_store(ub + kUnitS, sm + kPP, kSCopy);
-    if (h % r == 0) {   // the fp16 k image, once per key head
-      uint8_t* kb = kimg_base(a, b, hk, c);
-      bulk_store(kb, sm + kPK0, 8192);
-      bulk_store(kb + 8192, sm + kPK1, 8192);
-    }
+    bulk_store(ub, sm + kPM, kMBytes);
+    bulk_store(ub + kUnitN, sm + kPWS, kNBytes);
     bulk_commit();
   }
   goto done;
@@ -641,64 +682,55 @@ done:
 // Kernel 2: sequential state recurrence over chunks; cluster of 4 CTAs per (row, value head)
 // -------------------------------------------------------------------------------------------
 // Warp roles (warp w reads TMEM lanes 32 (w % 4) .. + 31):
-//   warps 0-3: own the state rows (key row = tid, 32 value columns, float32 registers);
-//   warps 0, 1, 4, 5: Vnew for positions 0-63 (warps 0, 1: value columns 0-15; 4, 5: 16-31);
-//   warps 2, 3: output rows o = Q' S + P U for positions 0-63 (TMEM lanes 64-127);
-//   thread 0 issues the MMAs. Warps 0-5 synchronise on named barrier 1.
-//   warp 6: producer, loading the early tiles up to three chunks ahead.
-constexpr int kStateThreads = 224;
-constexpr uint32_t kChainBar = 1, kChainCount = 192;
+//   warps 0-3: own the state rows (key row = tid, 32 value columns, float32 registers) and form
+//              S = Gamma_C S + D + N; thread 0 issues the state product. Named barrier 1.
+//   warps 4, 5: output rows o = O' + P U for positions 0-63 (TMEM lanes 0-63); named barrier 2.
+//   warp 6: producer, loading the tiles of up to three chunks ahead.
+//   warp 7: issues the output product, so that its issue time stays off the state chain.
+// Per chunk c (stage c % 3, buffers p = c % 2): thread 0 issues D[p] = M' Sb[p] and then signals
+// sReady[p]; warp 7 issues O'[p] = Q' Sb[p] once the output warps are done with chunk c - 2
+// (oFree[p]) and commits it to bar_o[p]. The state warps write S_{c+1} into Sb[p ^ 1] after the
+// O' product of chunk c - 1 (which read it) has completed. sReady, oFree and bar_o come in pairs
+// indexed by p, so each completes every other chunk and none can run two phases ahead of the
+// threads that wait on it.
+constexpr int kStateThreads = 256;
+constexpr uint32_t kChainBar = 1, kChainCount = 128, kOutBar = 2, kOutCount = 64;
 constexpr int kEStages = 3;
-// stage: [W0|Q'0] and [W1|Q'1] are the two K-atoms of the M = 128 operand [W; Q']
-constexpr uint32_t kEW0 = 0, kEQ0 = 8192, kEW1 = 16384, kEQ1 = 24576, kEK0 = 32768, kEK1 = 40960;
-constexpr uint32_t kEU = 49152, kEPU = 53248, kES = 57344;
-constexpr uint32_t kEStage = 58368;
-constexpr uint32_t kOffSb = kEStages * kEStage;   // state operand, fp16 MN-major, 128 rows of 64 B
-constexpr uint32_t kOffVs = kOffSb + 8192;        // Vs operand, fp16 MN-major, 64 rows of 64 B
-constexpr uint32_t kStateSmem = kOffVs + 4096 + 1024;
-constexpr uint32_t kETx = 12 * 4096 + 4096 + 4096 + kSCopy;   // bytes landing in one stage of each CTA
-constexpr uint32_t kTmemState = 64;                            // D_A [0, 32), D_X [32, 64)
+// stage: M' (two 16 KB K-atoms), Q' (two 8 KB K-atoms), this CTA's N and P U slices, Gamma_C
+constexpr uint32_t kEM = 0, kEQ0 = 32768, kEN = 49152, kEPU = 57344, kES = 61440;
+constexpr uint32_t kEStage = 62464;
+constexpr uint32_t kOffSb = kEStages * kEStage;   // two fp16 state operands, MN-major, 128 rows of 64 B
+constexpr uint32_t kStateSmem = kOffSb + 2 * 8192 + 1024;
+constexpr uint32_t kETx = 12 * 4096 + 8192 + 4096 + kSCopy;   // bytes landing in one stage of each CTA
+constexpr uint32_t kTmemState = 128;                           // D[2] at 0, 32; O'[2] at 64, 96
+static_assert(kEQ0 == kMBytes && kES + kSCopy <= kEStage && kEStage % 1024 == 0, "stage layout");
 
 __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t fullE[kEStages], freeE[kEStages], bar_a, bar_x;
+  __shared__ uint64_t fullE[kEStages], freeE[kEStages], bar_d, bar_o[2], oFree[2], sReady[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
   const uint32_t rank = cluster_ctarank();
   const int sl = (int)rank, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hk = h / (a.Hv / a.Hk);
   const int NC = a.NC;
 
-  // tiles of chunk c: this CTA multicasts 3 of the 12 shared 4 KB pieces (W, Q', k) and loads its
-  // own U and P U slices and the scales
-  auto issue_early = [&](int c) {
+  // tiles of chunk c: this CTA multicasts 3 of the 12 shared 4 KB pieces (M', Q'; contiguous in
+  // the unit and in the stage) and loads its own N and P U slices and Gamma_C
+  auto issue = [&](int c) {
     uint8_t* st = sm + (c % kEStages) * kEStage;
     uint64_t* bar = &fullE[c % kEStages];
     const uint8_t* ub = unit_base(a, b, h, c);
-    const uint8_t* kb = kimg_base(a, b, hk, c);
     mbar_arrive_expect_tx(bar, kETx);
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
-      const int p = 3 * sl + k, half = p & 1, atom = (p >> 1) & 1;
-      const uint8_t* src;
-      uint32_t dst;
-      if (p < 4) {            // W
-        src = ub + atom * 8192 + half * 4096;
-        dst = (atom ? kEW1 : kEW0) + half * 4096;
-      } else if (p < 8) {     // Q'
-        src = ub + kUnitQ + atom * 8192 + half * 4096;
-        dst = (atom ? kEQ1 : kEQ0) + half * 4096;
-      } else {                // k (fp16)
-        src = kb + atom * 8192 + half * 4096;
-        dst = (atom ? kEK1 : kEK0) + half * 4096;
-      }
-      bulk_load_mc(st + dst, src, 4096, bar, 0xF);
+      const int p = 3 * sl + k;
+      bulk_load_mc(st + p * 4096, ub + p * 4096, 4096, bar, 0xF);
     }
-    bulk_load(st + kEU, ub + kUnitU + sl * 4096, 4096, bar);
+    bulk_load(st + kEN, ub + kUnitN + sl * 8192, 8192, bar);
     bulk_load(st + kEPU, ub + kUnitPU + sl * 4096, 4096, bar);
     bulk_load(st + kES, ub + kUnitS, kSCopy, bar);
   };
@@ -706,10 +738,14 @@ chunk_state_kernel(const ChunkArgs a) {
   if (tid == 0) {
     for (int s = 0; s < kEStages; ++s) {
       mbar_init(&fullE[s], 1);
-      mbar_init(&freeE[s], kSlices);
+      mbar_init(&freeE[s], 2 * kSlices);   // the state and output warps of every CTA
     }
-    mbar_init(&bar_a, 1);
-    mbar_init(&bar_x, 1);
+    mbar_init(&bar_d, 1);
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(&bar_o[p], 1);
+      mbar_init(&oFree[p], 1);
+      mbar_init(&sReady[p], 1);
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -728,20 +764,16 @@ chunk_state_kernel(const ChunkArgs a) {
       for (int c = 0; c < NC; ++c) {
         if (c >= kEStages) ok = mbar_wait(&freeE[c % kEStages], ((c - kEStages) / kEStages) & 1, kWaitBudget);
         if (!ok || *(volatile int*)&abort_flag) break;
-        issue_early(c);
+        issue(c);
       }
     }
-  } else {
-    // ---------------- chain and output (warps 0-5) ----------------
-    const bool owner = warp < 4;                         // owns state row kr = tid
-    const int kr = tid & 127;
-    const bool vrow = (warp < 2) || (warp >= 4);         // forms Vnew rows
-    const bool orow = (warp == 2) || (warp == 3);        // forms output rows
-    const int i = tid & 63, ch0 = (warp >= 4) ? 16 : 0;
+  } else if (warp < 4) {
+    // ---------------- state warps ----------------
+    const int kr = tid;
     float Sm[kN];
 #pragma unroll
     for (int n = 0; n < kN; ++n) Sm[n] = 0.f;
-    if (owner && a.S0) {
+    if (a.S0) {
       const float* s0 = a.S0 + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
 #pragma unroll
       for (int n = 0; n < kN; n += 4) {
@@ -749,60 +781,104 @@ chunk_state_kernel(const ChunkArgs a) {
         Sm[n] = x.x; Sm[n + 1] = x.y; Sm[n + 2] = x.z; Sm[n + 3] = x.w;
       }
     }
-    // fp16 state operand: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle
-    auto write_state_operand = [&]() {
+    // fp16 state operand p: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle
+    auto write_state_operand = [&](int p) {
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4*>(sm + kOffSb + swz64(kr * 64 + ch * 16)) = pack8_f16(Sm + 8 * ch);
+        *reinterpret_cast<uint4*>(sm + kOffSb + p * 8192 + swz64(kr * 64 + ch * 16)) = pack8_f16(Sm + 8 * ch);
     };
-    if (owner) write_state_operand();
+    write_state_operand(0);
     fence_async_smem();
     named_bar_and(kChainBar, kChainCount, true);
 
     for (int c = 0; c < NC; ++c) {
-      const int es = c % kEStages;
+      const int es = c % kEStages, p = c & 1;
       uint8_t* st = sm + es * kEStage;
       ok = mbar_wait(&fullE[es], (c / kEStages) & 1, kWaitBudget) && !*(volatile int*)&abort_flag;
       if (tid == 0 && ok) {
-        // MMA_A: D[:, 0:32] = [W; Q'] S  (rows 0-63 W S, rows 64-127 Q' S)
         tc_fence_after();
+        const uint32_t sb = smem_u32(sm + kOffSb + p * 8192);
         const uint32_t idesc = idesc_f16(128, kN, false, true);
-        const uint32_t sb = smem_u32(sm + kOffSb);
+        const uint32_t sm_m = smem_u32(st + kEM);
+        // D[p] = M' S   (the critical product)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aa = smem_u32(st) + (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16(tb, smem_desc(aa, 16, 1024), smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
-        }
-        mma_commit(&bar_a);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tb + 32 * p, smem_desc(sm_m + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                   smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
+        mma_commit(&bar_d);
+        mbar_arrive(&sReady[p]);   // Sb[p] holds S_c: warp 7 may issue the output product
       }
-      if (!named_bar_and(kChainBar, kChainCount, ok)) break;
-
-      ok = mbar_wait(&bar_a, c & 1, kWaitBudget);
-      tc_fence_after();
-      if (vrow) {
-        // Vnew row i = U_i - (W S)_i on 16 value columns; Vs = sk_i Vnew as fp16 MN-major rows
-        float ws_[16], un[16];
-        tmem_ld16(tb + lane_base + ch0, ws_);
-        const float sk = reinterpret_cast<const float*>(st + kES)[i];
-        const uint8_t* urow = st + kEU;
-        unpack8_f16(*reinterpret_cast<const uint4*>(urow + swz64(i * 64 + (ch0 / 8) * 16)), un);
-        unpack8_f16(*reinterpret_cast<const uint4*>(urow + swz64(i * 64 + (ch0 / 8 + 1) * 16)), un + 8);
-        float vs[16];
+      ok = ok && mbar_wait(&bar_d, c & 1, kWaitBudget);
+      // Sb[p ^ 1] is rewritten below: the output product of chunk c - 1 must have read it
+      if (c >= 1) ok = ok && mbar_wait(&bar_o[p ^ 1], ((c - 1) >> 1) & 1, kWaitBudget);
+      if (ok) {
+        tc_fence_after();
+        float d[kN];
+        tmem_ld32(tb + lane_base + 32 * p, d);
+        const float gc = *reinterpret_cast<const float*>(st + kES);
+        const uint8_t* nrow = st + kEN;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) vs[e] = sk * (un[e] - ws_[e]);
-        *reinterpret_cast<uint4*>(sm + kOffVs + swz64(i * 64 + (ch0 / 8) * 16)) = pack8_f16(vs);
-        *reinterpret_cast<uint4*>(sm + kOffVs + swz64(i * 64 + (ch0 / 8 + 1) * 16)) = pack8_f16(vs + 8);
-      } else if (orow) {
-        // o row i = (Q' S)_i + (P U)_i
-        float qs[kN], pu[kN];
-        tmem_ld32(tb + lane_base, qs);
-        const int p = c * 64 + i;
-        if (p < a.L) {
+        for (int ch = 0; ch < 4; ++ch) {
+          float nv[8];
+          unpack8_f16(*reinterpret_cast<const uint4*>(nrow + swz64(kr * 64 + ch * 16)), nv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], d[8 * ch + e] + nv[e]);
+        }
+        write_state_operand(p ^ 1);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      if (!named_bar_and(kChainBar, kChainCount, ok)) break;
+      // this CTA's state warps are done with stage es (D complete, N read)
+      if (tid < kSlices && c + kEStages < NC) remote_arrive(&freeE[es], tid);
+    }
+    if (ok && a.S_T) {
+      float* dst = a.S_T + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
+#pragma unroll
+      for (int n = 0; n < kN; n += 4)
+        *reinterpret_cast<float4*>(dst + n) = make_float4(Sm[n], Sm[n + 1], Sm[n + 2], Sm[n + 3]);
+    }
+  } else if (warp == 7) {
+    // ---------------- output-product issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(128, kN, false, true);
+      for (int c = 0; c < NC; ++c) {
+        const int es = c % kEStages, p = c & 1;
+        ok = mbar_wait(&fullE[es], (c / kEStages) & 1, kWaitBudget) &&
+             mbar_wait(&sReady[p], (c >> 1) & 1, kWaitBudget) &&
+             (c < 2 || mbar_wait(&oFree[p], ((c - 2) >> 1) & 1, kWaitBudget));
+        if (!ok || *(volatile int*)&abort_flag) break;
+        tc_fence_after();
+        const uint32_t sb = smem_u32(sm + kOffSb + p * 8192);
+        const uint32_t sm_q = smem_u32(sm + es * kEStage + kEQ0);
+        // O'[p] = Q' S  (M = 128; operand rows 64-127 run into the next tile and are not read)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tb + 64 + 32 * p, smem_desc(sm_q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                   smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
+        mma_commit(&bar_o[p]);
+      }
+    }
+  } else {
+    // ---------------- output warps 4, 5 ----------------
+    const int i = tid - 128;   // position in the chunk = TMEM lane
+    for (int c = 0; c < NC; ++c) {
+      const int es = c % kEStages, p = c & 1;
+      const uint8_t* st = sm + es * kEStage;
+      ok = mbar_wait(&fullE[es], (c / kEStages) & 1, kWaitBudget) &&
+           mbar_wait(&bar_o[p], (c >> 1) & 1, kWaitBudget) && !*(volatile int*)&abort_flag;
+      if (ok) {
+        tc_fence_after();
+        float qs[kN];
+        tmem_ld32(tb + lane_base + 64 + 32 * p, qs);
+        const int pos = c * 64 + i;
+        if (pos < a.L) {
+          float pu[kN];
           const uint8_t* purow = st + kEPU;
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch)
             unpack8_f16(*reinterpret_cast<const uint4*>(purow + swz64(i * 64 + ch * 16)), pu + 8 * ch);
-          __nv_bfloat16* orow_p = a.o + (((size_t)b * a.L + p) * a.Hv + h) * kD + sl * kN;
+          __nv_bfloat16* orow_p = a.o + (((size_t)b * a.L + pos) * a.Hv + h) * kD + sl * kN;
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             float v[8];
@@ -812,43 +888,11 @@ chunk_state_kernel(const ChunkArgs a) {
           }
         }
       }
-      fence_async_smem();
       tc_fence_before();
-      if (!named_bar_and(kChainBar, kChainCount, ok)) break;
-
-      // MMA2: D[:, 32:64] = K^T Vs
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t id2 = idesc_f16(128, kN, true, true);
-        const uint32_t kt = smem_u32(st + kEK0), vs = smem_u32(sm + kOffVs);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16(tb + 32, smem_desc(kt + kk * 2048, 8192, 1024), smem_desc(vs + kk * 1024, 4096, 512, kSwizzle64B),
-                   id2, kk > 0);
-        mma_commit(&bar_x);
-      }
-      if (owner) {
-        // S = Gamma_C S + K^T Vs (this thread's key row), then the fp16 operand for the next chunk
-        ok = mbar_wait(&bar_x, c & 1, kWaitBudget);
-        tc_fence_after();
-        const float gc = reinterpret_cast<const float*>(st + kES)[64];
-        float x[kN];
-        tmem_ld32(tb + lane_base + 32, x);
-#pragma unroll
-        for (int n = 0; n < kN; ++n) Sm[n] = fmaf(gc, Sm[n], x[n]);
-        write_state_operand();
-      }
-      fence_async_smem();
-      tc_fence_before();
-      if (!named_bar_and(kChainBar, kChainCount, ok)) break;
-      // this CTA is done with stage es (MMA_A and MMA2 completed, U, P U and scales read)
-      if (tid >= 96 && tid < 96 + kSlices && c + kEStages < NC) remote_arrive(&freeE[es], tid - 96);
-    }
-    if (ok && owner && a.S_T) {
-      float* dst = a.S_T + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
-#pragma unroll
-      for (int n = 0; n < kN; n += 4)
-        *reinterpret_cast<float4*>(dst + n) = make_float4(Sm[n], Sm[n + 1], Sm[n + 2], Sm[n + 3]);
+      if (!named_bar_and(kOutBar, kOutCount, ok)) break;
+      if (tid == 128) mbar_arrive(&oFree[p]);
+      // this CTA's output warps are done with stage es (the Q' product complete, P U read)
+      if (tid >= 128 && tid < 128 + kSlices && c + kEStages < NC) remote_arrive(&freeE[es], tid - 128);
     }
   }
   if (!ok) {
@@ -901,8 +945,8 @@ size_t units_bytes(int B, int L, int Hv) {
 }  // namespace
 
 size_t chunk_workspace_bytes(int B, int Hk, int L, int Hv) {
-  const size_t NC = (size_t)(L + kChunk - 1) / kChunk;
-  return units_bytes(B, L, Hv) + (size_t)B * Hk * NC * kKBytes + 1024;
+  (void)Hk;
+  return units_bytes(B, L, Hv) + 1024;
 }
 
 cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
@@ -917,7 +961,6 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   a.o = static_cast<__nv_bfloat16*>(p.o);
   a.S_T = p.S_T;
   a.ws = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p.ws) + 1023) & ~uintptr_t(1023));
-  a.wsk = a.ws + units_bytes(p.B, p.L, p.Hv);
   a.B = p.B;
   a.L = p.L;
   a.Hk = p.Hk;
