@@ -323,9 +323,86 @@ def run_gb300(args) -> dict | None:
     }
     if traffic_k:
         line["roofline"]["traffic_per_kernel"] = traffic_k
+    if world == 1 and not args.no_rows:
+        line["rows"] = run_fork_decode(reps=max(3, min(args.steps, 20)), warmup=args.warmup)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
     return line
+
+
+# ------------------------------------------------------------------------------------------------
+# the other rows of the path: the fork pass and the decode step (one trunk state, 256 forks)
+# ------------------------------------------------------------------------------------------------
+
+def fork_decode_bytes(F: int, L_pad: int, Hk: int, Hv: int, N: int) -> tuple[int, int]:
+    """Algorithmic bytes of one fork pass and of one decode step (bf16 q/k/v/o, fp32 gates/states).
+
+    Fork pass: q, k at the key heads, v, o, g, beta for every padded position, the trunk states read
+    once, every fork's final state written. Decode step: one token of q, k, v, o, g, beta per fork and
+    the fork states read and written in place.
+    """
+    st = Hv * D * D * 4
+    fork = F * L_pad * (2 * Hk * D * 2 + 2 * Hv * D * 2 + 2 * Hv * 4) + N * st + F * st
+    dec = F * (2 * Hk * D * 2 + 2 * Hv * D * 2 + 2 * Hv * 4) + 2 * F * st
+    return fork, dec
+
+
+def run_fork_decode(reps: int, warmup: int) -> dict:
+    """Times rows a6 (fork pass) and a7 (decode step) of the hot path on the fork workload."""
+    import torch
+    from gated_deltanet_rule_gb300 import gdr, inputs
+    x = inputs.config5()
+    f = x.fork
+    d = lambda t: t.cuda().contiguous()
+    q, k, v, g, beta = (d(t) for t in (f.q, f.k, f.v, f.g, f.beta))
+    trunk, idx = d(x.trunk), d(x.trunk_idx)
+    F, L_pad, Hk, _ = q.shape
+    Hv = v.shape[2]
+    o = torch.empty_like(v)
+    states = torch.empty(F, Hv, D, D, device="cuda", dtype=torch.float32)
+    dec = [[d(t) for t in (s.q, s.k, s.v, s.g, s.beta)] for s in x.decode]
+    od = torch.empty_like(dec[0][2])
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+    fb, db = fork_decode_bytes(F, L_pad, Hk, Hv, trunk.shape[0])
+
+    ws = torch.empty(max(1, gdr.fork_workspace_bytes(F, L_pad, Hk, Hv)), dtype=torch.uint8, device="cuda")
+
+    def fork_pass():
+        gdr.gdr_fork_fwd(q, k, v, g, beta, trunk, idx, o=o, states_out=states, stream=stream, ws=ws)
+
+    def decode_round():
+        for s in dec:
+            gdr.gdr_decode_step(s[0], s[1], s[2], s[3], s[4], states, o=od, stream=stream)
+
+    out = {}
+    for name, fn, per, nbytes, tok in (("a6_fork_pass", fork_pass, 1, fb, int(x.lengths.sum())),
+                                       ("a7_decode_step", decode_round, len(dec), db, F)):
+        for _ in range(warmup):
+            fn()
+        gdr.gdr_sync_status()
+        gdr.stage_timer_enable(True, 4 * reps * per + 16)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        stages = gdr.stage_timer_collect()
+        gdr.stage_timer_enable(False, 0)
+        gdr.gdr_sync_status()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * per)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {
+            "us_per_call": round(us, 2), "tokens_per_s": round(tok / (us * 1e-6), 1),
+            "tokens": "real tokens of the fork batch" if per == 1 else "one token per fork",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes},
+            "kernels": {kname: {"launches": c, "avg_us": round(t / c * 1e3, 2)} for kname, (t, c) in stages.items() if c},
+        }
+    assert torch.isfinite(states).all() and torch.isfinite(o.float()).all()
+    out["workload"] = x.meta["workload"] + f" (F={F}, Hk={Hk}, Hv={Hv}, D={D}, bf16 q/k/v)"
+    return out
 
 
 # ------------------------------------------------------------------------------------------------
@@ -394,6 +471,7 @@ def main(argv=None):
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed steps while clocks are sampled")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rows", action="store_true", help="skip the fork-pass and decode-step rows")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

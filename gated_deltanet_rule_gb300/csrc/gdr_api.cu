@@ -156,10 +156,14 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
   return launch_status(e, who);
 }
 
+size_t gdr_fork_workspace_bytes(int F, int L_pad, int Hk, int Hv, int D, gdr_dtype dt) {
+  return gdr_chunk_workspace_bytes(F, L_pad, Hk, Hv, D, dt);
+}
+
 gdr_status gdr_fork_fwd(const void* q, const void* k, const void* v, const float* g,
                         const float* beta, const float* trunk, const int64_t* trunk_idx, int N,
                         void* o, float* states_out, int F, int L_pad, int Hk, int Hv, int D,
-                        gdr_dtype dt, gdr_stream_t stream) {
+                        gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream) {
   const char* who = "gdr_fork_fwd";
   gdr_status st = check_common(q, k, v, g, beta, o, F, L_pad, Hk, Hv, D, dt, who);
   if (st != GDR_OK) return st;
@@ -176,10 +180,20 @@ gdr_status gdr_fork_fwd(const void* q, const void* k, const void* v, const float
     if (s0 < t1 && t0 < s1)
       return fail(GDR_ERR_INVALID_ARG, "%s: states_out overlaps trunk", who);
   }
+  const size_t need = gdr_fork_workspace_bytes(F, L_pad, Hk, Hv, D, dt);
+  if (need > 0 && (ws == nullptr || ws_bytes < need))
+    return fail(GDR_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", who, need,
+                ws == nullptr ? (size_t)0 : ws_bytes);
   int* err = device_error_word();
   if (!err) return fail(GDR_ERR_CUDA, "%s: no CUDA device available", who);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  RecurrentArgs a{q, k, v, g, beta, trunk, trunk_idx, N, o, states_out, F, L_pad, Hk, Hv, dt == GDR_BF16, err};
+  if (dt == GDR_BF16) {
+    if (F > 65535 || Hk > 65535)
+      return fail(GDR_ERR_UNSUPPORTED, "%s: F=%d or Hk=%d exceeds 65535", who, F, Hk);
+    ChunkLaunch c{q, k, v, g, beta, trunk, o, states_out, ws, F, L_pad, Hk, Hv, err, trunk_idx, N};
+    return launch_status(launch_chunk_bf16(c, s), who);
+  }
+  RecurrentArgs a{q, k, v, g, beta, trunk, trunk_idx, N, o, states_out, F, L_pad, Hk, Hv, false, err};
   const int slot = stage_timer_begin(s, kKernRecurrent);
   cudaError_t e = launch_recurrent(a, s);
   stage_timer_end(slot, s);

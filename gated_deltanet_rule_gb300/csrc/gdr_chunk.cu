@@ -72,6 +72,8 @@ struct ChunkArgs {
   const float* g;
   const float* beta;
   const float* S0;
+  const int64_t* S0_idx;   // row b starts from S0[S0_idx[b]] (forks); NULL = S0[b]
+  int n_S0;                // states S0 holds when S0_idx is set
   __nv_bfloat16* o;
   float* S_T;
   uint8_t* ws;       // 1024-aligned
@@ -135,29 +137,58 @@ static_assert(kPWS % 1024 == 0 && kPWS + 32768 <= kPVec, "the [sk W | sk U] oper
 // zeroed once consumed, so that a row of AT restricted to a finished diagonal block is exactly a
 // column of T. Block products read rows of the left factor and columns of the right factor as
 // contiguous float4 runs, and skip the blocks that are zero by triangularity.
-__device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, int tid) {
+__device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
-  // 1. diagonal 16-blocks: thread = (block, column), right-looking substitution; a block's 16
-  //    threads share a warp
-  if (tid < 64) {
-    const int r0 = (tid >> 4) * 16, col = tid & 15;
-    float x[16];
+  // 1. diagonal 16-blocks, one warp each (warps 0-3): lane = (row i, column half hf), holding
+  //    T(i, 8 hf .. 8 hf + 7) of its block in registers and row i of A in registers. Forward
+  //    substitution by rows: when row j is final its values are broadcast by shuffle and every
+  //    row i > j subtracts A_ij T_j (A_ij is taken as 0 for j >= i).
+  if (warp < 4) {
+    const int r0 = 16 * warp, i = lane & 15, hf = lane >> 4;
+    float av[16];
+    const float4* arow = reinterpret_cast<const float4*>(AT + (r0 + i) * 68 + r0);
 #pragma unroll
-    for (int ii = 0; ii < 16; ++ii) x[ii] = (ii == col) ? 1.f : 0.f;
+    for (int m4 = 0; m4 < 4; ++m4) {
+      const float4 t = arow[m4];
+      av[4 * m4] = t.x; av[4 * m4 + 1] = t.y; av[4 * m4 + 2] = t.z; av[4 * m4 + 3] = t.w;
+    }
 #pragma unroll
-    for (int jj = 0; jj < 15; ++jj) {
+    for (int j = 0; j < 16; ++j) av[j] = (j < i) ? av[j] : 0.f;
+    float t[8];
 #pragma unroll
-      for (int ii = jj + 1; ii < 16; ++ii) x[ii] = fmaf(-AT[(r0 + ii) * 68 + r0 + jj], x[jj], x[ii]);
+    for (int e = 0; e < 8; ++e) t[e] = (8 * hf + e == i) ? 1.f : 0.f;
+#pragma unroll
+    for (int j = 0; j < 15; ++j) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float tj = __shfl_sync(0xffffffffu, t[e], j + 16 * hf);
+        t[e] = fmaf(-av[j], tj, t[e]);
+      }
     }
     __syncwarp();
+    // Tm row i (its diagonal 1 and zero upper part included); AT row c (block columns) becomes
+    // column c of T: 0 above the diagonal of T (the consumed A entries), 1 on it, T(i, c) below
+    float4* trow = reinterpret_cast<float4*>(Tm + (r0 + i) * 68 + r0 + 8 * hf);
+    trow[0] = make_float4(t[0], t[1], t[2], t[3]);
+    trow[1] = make_float4(t[4], t[5], t[6], t[7]);
 #pragma unroll
-    for (int ii = 0; ii < 16; ++ii) {
-      if (ii > col) {
-        Tm[(r0 + ii) * 68 + r0 + col] = x[ii];
-        AT[(r0 + col) * 68 + r0 + ii] = x[ii];
-      } else if (ii < col) {
-        AT[(r0 + col) * 68 + r0 + ii] = 0.f;
-      }
+    for (int e = 0; e < 8; ++e) {
+      const int c = 8 * hf + e;
+      AT[(r0 + c) * 68 + r0 + i] = (i > c) ? t[e] : (i == c ? 1.f : 0.f);
+    }
+  } else {
+    // warps 4-7 meanwhile: the k and v tiles to fp16 in place, for the fp16 products (the Gram MMA
+    // that read k as bf16 has completed); 2048 chunks of 16 B, k atoms then v atoms
+    const int t = tid - 128;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      const int chunk16 = n * 128 + t;
+      const int which = chunk16 >> 9, off = (chunk16 & 511) * 16;
+      const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPV + (which - 2) * 8192);
+      uint4* p = reinterpret_cast<uint4*>(sm + base + off);
+      uint4 w = *p;
+      w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+      *p = w;
     }
   }
   __syncthreads();
@@ -371,14 +402,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     mma_commit(&bar_mma);
   }
-  // inverse norms: two threads per row (one 64-column atom each); rows 0-63 q, 64-127 k
+  // inverse norms: two threads per row (one 64-column atom each); rows 0-63 q, 64-127 k. The sum
+  // does not care about the order of the 16-byte chunks, so each thread starts at a different one
+  // (rotated by row and atom) and the eight lanes of a quarter-warp hit eight different banks.
   {
     const int row = tid >> 1, half = tid & 1, rr = row & 63;
     const uint8_t* base = sm + (row < 64 ? kPQ0 : kPK0) + half * 16384 + rr * 128;
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
-      const uint4 w = *reinterpret_cast<const uint4*>(base + ch * 16);
+      const uint4 w = *reinterpret_cast<const uint4*>(base + (((ch + rr + 4 * half) & 7) << 4));
       const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -470,21 +503,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         *reinterpret_cast<uint4*>(sm + kPP + i * 128 + ((ch ^ (i & 7)) << 4)) = pack8_f16(v + 8 * q);
       }
     }
-    // k and v tiles to fp16 in place (the Gram MMA that read k as bf16 has completed)
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const int chunk16 = n * kPrepThreads + tid;       // 2048 chunks of 16 B: k atoms then v atoms
-      const int which = chunk16 >> 9, off = (chunk16 & 511) * 16;
-      const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPV + (which - 2) * 8192);
-      uint4* p = reinterpret_cast<uint4*>(sm + base + off);
-      uint4 w = *p;
-      w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
-      *p = w;
-    }
   }
   __syncthreads();
 
-  invert_unit_lower(AT, Tm, Xs, tid);
+  invert_unit_lower(AT, Tm, Xs, sm, tid);
 
   // operand [A1; A2] = [T diag(beta Gamma ki); T diag(beta)], MN-major: K-row j holds column j of T
   {
@@ -685,7 +707,8 @@ done:
 //   warps 0-3: own the state rows (key row = tid, 32 value columns, float32 registers) and form
 //              S = Gamma_C S + D + N; thread 0 issues the state product. Named barrier 1.
 //   warps 4, 5: output rows o = O' + P U for positions 0-63 (TMEM lanes 0-63); named barrier 2.
-//   warp 6: producer, loading the tiles of up to three chunks ahead.
+//   warp 6: producer, loading the tiles of up to three chunks ahead; it also forwards this CTA's
+//           stage releases to the other CTAs of the cluster.
 //   warp 7: issues the output product, so that its issue time stays off the state chain.
 // Per chunk c (stage c % 3, buffers p = c % 2): thread 0 issues D[p] = M' Sb[p] and then signals
 // sReady[p]; warp 7 issues O'[p] = Q' Sb[p] once the output warps are done with chunk c - 2
@@ -709,7 +732,7 @@ __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads,
 chunk_state_kernel(const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t fullE[kEStages], freeE[kEStages], bar_d, bar_o[2], oFree[2], sReady[2];
+  __shared__ uint64_t fullE[kEStages], freeE[kEStages], localFree[kEStages], bar_d, bar_o[2], oFree[2], sReady[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -738,7 +761,8 @@ chunk_state_kernel(const ChunkArgs a) {
   if (tid == 0) {
     for (int s = 0; s < kEStages; ++s) {
       mbar_init(&fullE[s], 1);
-      mbar_init(&freeE[s], 2 * kSlices);   // the state and output warps of every CTA
+      mbar_init(&freeE[s], kSlices);      // one arrival from the producer of every CTA
+      mbar_init(&localFree[s], 2);        // this CTA's state and output warps
     }
     mbar_init(&bar_d, 1);
     for (int p = 0; p < 2; ++p) {
@@ -757,15 +781,37 @@ chunk_state_kernel(const ChunkArgs a) {
   const uint32_t tb = tmem_base;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   bool ok = true;
+  // the row's initial state: S0[b], or for forks the trunk state S0[S0_idx[b]]; an index out of
+  // range skips the row entirely (nothing of it is written) and records the error
+  size_t s0row = b;
+  bool skip = false;
+  if (a.S0_idx) {
+    const long long ix = a.S0_idx[b];
+    skip = ix < 0 || ix >= a.n_S0;
+    s0row = skip ? 0 : (size_t)ix;
+    if (skip && tid == 0) set_error(a.err, kErrDeviceIndex);
+  }
 
-  if (warp == 6) {
+  if (skip) {
+    // every CTA of the cluster reads the same index and skips together
+  } else if (warp == 6) {
     // ---------------- producer ----------------
-    if (lane == 0) {
-      for (int c = 0; c < NC; ++c) {
-        if (c >= kEStages) ok = mbar_wait(&freeE[c % kEStages], ((c - kEStages) / kEStages) & 1, kWaitBudget);
-        if (!ok || *(volatile int*)&abort_flag) break;
-        issue(c);
+    // Lane 0 issues the loads. Stage c % 3 last held chunk c - 3: once this CTA's consumers are
+    // done with it (localFree), lanes 0-3 tell the cluster's CTAs in parallel (a release at
+    // cluster scope takes long, so it stays off the chain), and lane 0 waits until every CTA is
+    // done (freeE) before multicasting into it.
+    for (int c = 0; c < NC; ++c) {
+      const int es = c % kEStages;
+      if (c >= kEStages) {
+        const uint32_t par = ((c - kEStages) / kEStages) & 1;
+        ok = mbar_wait(&localFree[es], par, kWaitBudget);
+        if (ok && lane < kSlices) remote_arrive(&freeE[es], lane);
+        ok = ok && (lane != 0 || mbar_wait(&freeE[es], par, kWaitBudget));
       }
+      ok = __all_sync(0xffffffffu, ok) && !*(volatile int*)&abort_flag;
+      if (!ok) break;
+      if (lane == 0) issue(c);
+      __syncwarp();
     }
   } else if (warp < 4) {
     // ---------------- state warps ----------------
@@ -774,7 +820,7 @@ chunk_state_kernel(const ChunkArgs a) {
 #pragma unroll
     for (int n = 0; n < kN; ++n) Sm[n] = 0.f;
     if (a.S0) {
-      const float* s0 = a.S0 + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
+      const float* s0 = a.S0 + ((s0row * a.Hv + h) * kD + kr) * kD + sl * kN;
 #pragma unroll
       for (int n = 0; n < kN; n += 4) {
         const float4 x = __ldg(reinterpret_cast<const float4*>(s0 + n));
@@ -830,7 +876,7 @@ chunk_state_kernel(const ChunkArgs a) {
       tc_fence_before();
       if (!named_bar_and(kChainBar, kChainCount, ok)) break;
       // this CTA's state warps are done with stage es (D complete, N read)
-      if (tid < kSlices && c + kEStages < NC) remote_arrive(&freeE[es], tid);
+      if (tid == 0 && c + kEStages < NC) mbar_arrive(&localFree[es]);
     }
     if (ok && a.S_T) {
       float* dst = a.S_T + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
@@ -892,7 +938,7 @@ chunk_state_kernel(const ChunkArgs a) {
       if (!named_bar_and(kOutBar, kOutCount, ok)) break;
       if (tid == 128) mbar_arrive(&oFree[p]);
       // this CTA's output warps are done with stage es (the Q' product complete, P U read)
-      if (tid >= 128 && tid < 128 + kSlices && c + kEStages < NC) remote_arrive(&freeE[es], tid - 128);
+      if (tid == 128 && c + kEStages < NC) mbar_arrive(&localFree[es]);
     }
   }
   if (!ok) {
@@ -958,6 +1004,8 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   a.g = p.g;
   a.beta = p.beta;
   a.S0 = p.S0;
+  a.S0_idx = p.S0_idx;
+  a.n_S0 = p.n_S0;
   a.o = static_cast<__nv_bfloat16*>(p.o);
   a.S_T = p.S_T;
   a.ws = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p.ws) + 1023) & ~uintptr_t(1023));

@@ -24,7 +24,7 @@ enum KernelId : int {
 
 // Token-by-token recurrence on CUDA cores (float32 state in registers).
 // Row b reads its initial state from S_in[(idx ? idx[b] : b)] (NULL S_in = zeros) and writes its
-// final state to S_out[b] (NULL = not written). Used for the float32 path, forks and decode.
+// final state to S_out[b] (NULL = not written). Used for the float32 path, float32 forks and decode.
 struct RecurrentArgs {
   const void* q;
   const void* k;
@@ -43,7 +43,9 @@ struct RecurrentArgs {
 cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t s);
 
 // Chunked tensor-core path for bf16 q/k/v (two kernels: per-chunk WY factors, then the state
-// recurrence). ws must hold chunk_workspace_bytes(B, Hk, L, Hv) bytes.
+// recurrence). ws must hold chunk_workspace_bytes(B, Hk, L, Hv) bytes. Row b starts from
+// S0[S0_idx ? S0_idx[b] : b] (NULL S0 = zeros); with S0_idx set, an index outside [0, n_S0) skips
+// the row (nothing written) and records kErrDeviceIndex. Used for prefill rows and bf16 forks.
 struct ChunkLaunch {
   const void* q;
   const void* k;
@@ -56,6 +58,8 @@ struct ChunkLaunch {
   void* ws;
   int B, L, Hk, Hv;
   int* err;
+  const int64_t* S0_idx = nullptr;
+  int n_S0 = 0;
 };
 size_t chunk_workspace_bytes(int B, int Hk, int L, int Hv);
 cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s);

@@ -20,7 +20,8 @@ GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_CUDA, GDR_ERR_DEVICE_I
 GDR_F32, GDR_BF16 = 0, 1
 D = 128
 
-EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_noalloc", "gdr_fork_fwd", "gdr_decode_step",
+EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_noalloc", "gdr_fork_workspace_bytes",
+           "gdr_fork_fwd", "gdr_decode_step",
            "gdr_sync_status", "gdr_status_string", "gdr_last_error_message",
            "gdr_stage_timer_enable", "gdr_stage_timer_collect", "gdr_kernel_name"]
 
@@ -50,7 +51,9 @@ def lib() -> ctypes.CDLL:
     L.gdr_chunk_fwd.restype = i
     L.gdr_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, vp]
     L.gdr_chunk_fwd_noalloc.restype = i
-    L.gdr_fork_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, vp, fp, i, i, i, i, i, i, vp]
+    L.gdr_fork_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    L.gdr_fork_workspace_bytes.restype = sz
+    L.gdr_fork_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, vp, fp, i, i, i, i, i, i, vp, sz, vp]
     L.gdr_fork_fwd.restype = i
     L.gdr_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, vp]
     L.gdr_decode_step.restype = i
@@ -142,8 +145,13 @@ def gdr_chunk_fwd(q, k, v, g, beta, S0=None, o=None, S_T=None, ws=None, stream=N
     return o, S_T
 
 
+def fork_workspace_bytes(F: int, L_pad: int, Hk: int, Hv: int, D: int = D, dtype=torch.bfloat16) -> int:
+    code = GDR_BF16 if dtype == torch.bfloat16 else GDR_F32
+    return int(lib().gdr_fork_workspace_bytes(F, L_pad, Hk, Hv, D, code))
+
+
 def gdr_fork_fwd(q, k, v, g, beta, trunk, trunk_idx, o=None, states_out=None, stream=None,
-                 keep: bool = True):
+                 keep: bool = True, ws=None):
     """Fork batch: returns (o [F,L_pad,Hv,D], states_out [F,Hv,D,D] or None)."""
     F, L, Hk, Hv, Dk = _check_inputs(q, k, v, g, beta)
     dt = _dtype_code(q)
@@ -153,9 +161,13 @@ def gdr_fork_fwd(q, k, v, g, beta, trunk, trunk_idx, o=None, states_out=None, st
         o = torch.empty_like(v)
     if states_out is None and keep:
         states_out = torch.empty(F, Hv, Dk, v.shape[3], device=v.device, dtype=torch.float32)
+    need = fork_workspace_bytes(F, L, Hk, Hv, Dk, q.dtype)
+    if need and ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().gdr_fork_fwd(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(trunk), _p(trunk_idx),
                               trunk.shape[0], _p(o), _p(states_out), F, L, Hk, Hv, Dk, dt,
-                              _stream(stream)))
+                              _p(ws), ws_bytes, _stream(stream)))
     return o, states_out
 
 

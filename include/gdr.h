@@ -75,9 +75,15 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
                          int Hk, int Hv, int D, gdr_dtype dt, void* ws, size_t ws_bytes,
                          gdr_stream_t stream);
 
+/* Bytes of caller workspace gdr_fork_fwd needs for these sizes (0 for float32: no workspace). */
+size_t gdr_fork_workspace_bytes(int F, int L_pad, int Hk, int Hv, int D, gdr_dtype dt);
+
 /*
  * Fork batch: F forks, fork f continuing its own copy of trunk[trunk_idx[f]] over its L_pad
  * tokens (right-padded with beta = g = 0). The trunk states are read in place, never copied.
+ * bf16 forks run on the same tensor-core kernels as gdr_chunk_fwd (one row per fork, the row's
+ * initial state taken from the trunk by index), so fork f equals gdr_chunk_fwd on that row from
+ * trunk[trunk_idx[f]] bit for bit; float32 forks run the token loop.
  * (DEG "model.py": fork_delta_rule(q, k, v, g, beta, h0, h0_idx, store) in _fork_linear_layer;
  *  Backbone.fork reads the prefixes by reference through the row index prow.)
  *   q, k        [F, L_pad, Hk, D] dt;  v [F, L_pad, Hv, D] dt;  g, beta [F, L_pad, Hv] float32
@@ -86,13 +92,15 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
  *   o           [F, L_pad, Hv, D] dt
  *   states_out  [F, Hv, D, D] float32   each fork's final state (the `store` of the pages);
  *                                       NULL = not kept. Must not overlap trunk.
+ *   ws          workspace of at least gdr_fork_workspace_bytes(...) bytes (NULL if that is 0),
+ *               owned by the caller and free for reuse once the call's stream work is done
  * An index outside [0, N) leaves that fork's outputs untouched and records
  * GDR_ERR_DEVICE_INDEX in the device error word.
  */
 gdr_status gdr_fork_fwd(const void* q, const void* k, const void* v, const float* g,
                         const float* beta, const float* trunk, const int64_t* trunk_idx, int N,
                         void* o, float* states_out, int F, int L_pad, int Hk, int Hv, int D,
-                        gdr_dtype dt, gdr_stream_t stream);
+                        gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream);
 
 /*
  * One decode step (L = 1) for F rows, each row's state updated in place.

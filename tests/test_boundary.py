@@ -80,8 +80,8 @@ def test_workspace_query(L):
 
 
 def test_fork_rejects_bad_arguments(L):
-    def fork(trunk=P, idx=P, N=1, states=None, F=4):
-        return L.gdr_fork_fwd(P, P, P, P, P, trunk, idx, N, P, states, F, 64, 16, 32, 128, 1, None)
+    def fork(trunk=P, idx=P, N=1, states=None, F=4, ws=P, ws_bytes=1 << 40):
+        return L.gdr_fork_fwd(P, P, P, P, P, trunk, idx, N, P, states, F, 64, 16, 32, 128, 1, ws, ws_bytes, None)
     assert fork(trunk=None) == gdr.GDR_ERR_INVALID_ARG
     assert fork(idx=None) == gdr.GDR_ERR_INVALID_ARG
     assert fork(N=0) == gdr.GDR_ERR_INVALID_ARG
@@ -89,6 +89,13 @@ def test_fork_rejects_bad_arguments(L):
     # states_out overlapping the trunk is rejected
     assert fork(trunk=P, states=ctypes.c_void_p((1 << 20) + 1024)) == gdr.GDR_ERR_INVALID_ARG
     assert b"overlaps" in L.gdr_last_error_message()
+    # bf16 forks run on the tensor-core kernels and need the caller's workspace
+    need = L.gdr_fork_workspace_bytes(4, 64, 16, 32, 128, 1)
+    assert need == L.gdr_chunk_workspace_bytes(4, 64, 16, 32, 128, 1) > 0
+    assert L.gdr_fork_workspace_bytes(4, 64, 16, 32, 128, 0) == 0
+    assert fork(ws=None, ws_bytes=0) == gdr.GDR_ERR_INVALID_ARG
+    assert b"workspace" in L.gdr_last_error_message()
+    assert fork(ws_bytes=need - 1) == gdr.GDR_ERR_INVALID_ARG
 
 
 def test_decode_rejects_bad_arguments(L):
