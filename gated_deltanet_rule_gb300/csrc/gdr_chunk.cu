@@ -24,19 +24,20 @@
 // M' form's final states come out slightly closer to the oracle than the two-product form's).
 // Operands are assumed inside fp16's range (|x| < 65504), which holds for l2-normalised keys.
 //
-// Kernel 1 (gdr_chunk_prep, one CTA per (row, value head, chunk), all chunks in parallel):
-//   TMA loads raw q, k, v; a bf16 MMA gives [Q; K] K^T (both Gram matrices, exact products); CUDA
-//   cores build A and P; a recursive-doubling fp32 inverse gives T; T's scaled columns form the
-//   operand [A1; A2]; MMAs give W = A1 K and U = A2 V, then P [W | U], then
-//   K^T [diag(sk) W | diag(sk) U] = [-M' | N]. Per unit it writes, with bulk copies, M' and Q' as
-//   the 128B-swizzled images kernel 2 uses as MMA operands, N and P U as four 32-column slices, and
-//   Gamma_C.
+// Kernel 1 (gdr_chunk_prep, persistent, two CTAs per SM, each working through (row, value head,
+//   chunk) units; every unit is independent): TMA loads raw q, k, v; a bf16 MMA gives [Q; K] K^T
+//   (both Gram matrices, exact products); CUDA cores build A and P; a recursive-doubling fp32
+//   inverse gives T; T's scaled columns form the operand [A1; A2]; MMAs give W = A1 K and U = A2 V,
+//   then P [W | U], then K^T [diag(sk) W | diag(sk) U] = [-M' | N]. Per unit it writes, with bulk
+//   copies from shared memory, M' and Q' as the 128B-swizzled images kernel 2 uses as MMA
+//   operands, N and P U as four 32-column slices, and Gamma_C.
 // Kernel 2 (gdr_chunk_state, a cluster of 4 CTAs per (row, value head), CTA r owning value columns
 //   [32 r, 32 r + 32), sequential over chunks): the float32 state slice stays in registers. Per
 //   chunk one thread issues D = M' S and O' = Q' S (fp16 copy of S as the B operand); the state
 //   warps form S = Gamma_C S + D + N and the next fp16 copy; two output warps form o = O' + P U
 //   off the critical path. M' and Q' are TMA-multicast across the cluster, each CTA loading a
 //   quarter, by a producer warp that runs up to three chunks ahead.
+#include <algorithm>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -312,6 +313,10 @@ __device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, 
   __syncthreads();
 }
 
+// Persistent: CTA i takes units i, i + gridDim.x, ... in the order value head fastest, then chunks
+// from the last to the first (so the units the state kernel reads first were written last and are
+// the likeliest to still sit in L2), then rows. While one unit computes, the next unit's gates are
+// loaded into registers and its tiles prefetched into L2.
 __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const ChunkArgs a) {
@@ -319,10 +324,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_base;
+  __shared__ float gbuf[2][128];   // gates of the current and the next unit: g[64] | beta[64]
 
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r = a.Hv / a.Hk, hk = h / r;
+  const int r = a.Hv / a.Hk;
+  const int total = a.B * a.Hv * a.NC;
   float* AT = reinterpret_cast<float*>(sm + kPAT);
   float* Tm = reinterpret_cast<float*>(sm + kPTm);
   float* Xs = reinterpret_cast<float*>(sm + kPXs);
@@ -334,39 +340,83 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   float* e1 = gam2 + 320;                                  // exp(gamma_i - gamma_16I); scan scratch first
   float* skv = gam2 + 384;                                 // sk_i = exp(gamma_C - gamma_i) ki_i
   float* E2 = reinterpret_cast<float*>(sm + kPE2);
-  uint8_t* ub = unit_base(a, b, h, c);
 
-  // gates of this chunk; positions past L read as beta = g = 0
-  float gg = 0.f, bb = 0.f;
-  if (tid < 64) {
-    const int p = c * 64 + tid;
-    if (p < a.L) {
-      gg = __ldg(a.g + ((size_t)b * a.L + p) * a.Hv + h);
-      bb = __ldg(a.beta + ((size_t)b * a.L + p) * a.Hv + h);
+  // unit u -> (chunk c, value head h, row b)
+  auto unit_of = [&](int u, int& c, int& h, int& b) {
+    h = u % a.Hv;
+    const int rest = u / a.Hv;
+    c = a.NC - 1 - rest % a.NC;
+    b = rest / a.NC;
+  };
+  // gates of a unit into gbuf[buf] (threads 0-63, one position each, asynchronous copies);
+  // positions past L read as beta = g = 0. Every thread commits one group per call.
+  auto copy_gates = [&](int u, int buf) {
+    if (tid < 64) {
+      int c, h, b;
+      unit_of(u, c, h, b);
+      const int p = c * 64 + tid;
+      if (p < a.L) {
+        cp_async4(&gbuf[buf][tid], a.g + ((size_t)b * a.L + p) * a.Hv + h);
+        cp_async4(&gbuf[buf][64 + tid], a.beta + ((size_t)b * a.L + p) * a.Hv + h);
+      } else {
+        gbuf[buf][tid] = 0.f;
+        gbuf[buf][64 + tid] = 0.f;
+      }
     }
-  }
+    cp_async_commit();
+  };
+  // raw q, k, v tiles of a unit (six 64 x 64 boxes) into shared memory, or only into L2; called
+  // by a whole warp, lane t < 6 issuing box t (lane 0 also posts the byte count)
+  auto tiles = [&](int u, bool to_smem) {
+    int c, h, b;
+    unit_of(u, c, h, b);
+    const int hk = h / r;
+    const CUtensorMap* map = lane < 2 ? &tm_q : (lane < 4 ? &tm_k : &tm_v);
+    const uint32_t dst = lane < 4 ? (uint32_t)lane * 8192 : kPV + (uint32_t)(lane - 4) * 8192;
+    const int c0 = (lane & 1) * 64, c1 = lane < 4 ? hk : h;
+    // shared-memory order: q0 k0 q1 k1 (the Gram operand), then v0 v1
+    const uint32_t dst_qk = (uint32_t)((lane & 1) * 16384 + (lane >> 1) * 8192);
+    if (to_smem) {
+      if (lane == 0) mbar_arrive_expect_tx(&bar_ld, 49152);
+      __syncwarp();
+      if (lane < 6) tma_load_4d(sm + (lane < 4 ? dst_qk : dst), map, &bar_ld, c0, c1, c * 64, b);
+    } else if (lane < 6) {
+      tma_prefetch_4d(map, c0, c1, c * 64, b);
+    }
+  };
+
+  int u = blockIdx.x;
+  copy_gates(u, 0);
   if (tid == 0) {
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&bar_ld, 49152);
-    tma_load_4d(sm + kPQ0, &tm_q, &bar_ld, 0, hk, c * 64, b);
-    tma_load_4d(sm + kPQ1, &tm_q, &bar_ld, 64, hk, c * 64, b);
-    tma_load_4d(sm + kPK0, &tm_k, &bar_ld, 0, hk, c * 64, b);
-    tma_load_4d(sm + kPK1, &tm_k, &bar_ld, 64, hk, c * 64, b);
-    tma_load_4d(sm + kPV, &tm_v, &bar_ld, 0, h, c * 64, b);
-    tma_load_4d(sm + kPV + 8192, &tm_v, &bar_ld, 64, h, c * 64, b);
   }
+  __syncthreads();
+  if (warp == 7) tiles(u, true);
   if (warp == 1) tmem_alloc(&tmem_base, 256);
-  // T's row-major copy starts as the identity (its upper part stays zero)
-  for (int e = tid; e < 64 * 17; e += kPrepThreads) {
-    const int rr = e / 17, c4 = e - rr * 17;
-    const int d = ((rr >> 2) == c4) ? (rr & 3) : -1;
-    reinterpret_cast<float4*>(Tm + rr * 68)[c4] =
-        make_float4(d == 0 ? 1.f : 0.f, d == 1 ? 1.f : 0.f, d == 2 ? 1.f : 0.f, d == 3 ? 1.f : 0.f);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  bool ok = true;
+
+  for (int it = 0;; ++it) {
+  int c, h, b;
+  unit_of(u, c, h, b);
+  uint8_t* ub = unit_base(a, b, h, c);
+  const int un = u + (int)gridDim.x;
+  if (un < total) {
+    copy_gates(un, (it + 1) & 1);
+    if (warp == 7) tiles(un, false);
+  } else {
+    cp_async_commit();
   }
+  cp_async_wait<1>();   // this unit's gates have landed (the next unit's may still be in flight)
   // inclusive scan of g over the chunk (warps 0 and 1, then warp 1 adds warp 0's total)
   if (tid < 64) {
+    const float gg = gbuf[it & 1][tid], bb = gbuf[it & 1][64 + tid];
     float x = gg;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -376,20 +426,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     e1[tid] = x;
     bet[tid] = bb;
   }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = tmem_base;
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  bool ok = true;
   if (tid < 64) {
     const float gam = e1[tid] + (tid >= 32 ? e1[31] : 0.f);
     gam2[tid] = gam * kLog2e;
     Gam[tid] = exp2f(gam * kLog2e);
   }
 
-  ok = mbar_wait(&bar_ld, 0, kWaitBudget);
-  if (!__syncthreads_and(ok)) goto fail;
+  ok = mbar_wait(&bar_ld, it & 1, kWaitBudget);
+  if (!__syncthreads_and(ok)) break;
 
   // Gram MMA (bf16, exact products): D[0:128, 0:64] = [Q; K] K^T
   if (tid == 0) {
@@ -434,10 +479,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int I = 1 + ((tid - 64) >> 6), j = tid & 63;
     E2[I * 68 + j] = (j < 16 * I) ? kinv[j] * ex2_approx(gam2[16 * I] - gam2[j]) : 0.f;
   }
+  if (tid == 0) bulk_wait_read();   // the previous unit's N store has read the AT / Tm region
   ok = mbar_wait(&bar_mma, 0, kWaitBudget);
-  if (!__syncthreads_and(ok)) goto fail;
+  if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
+  // T's row-major copy starts as the identity (its upper part stays zero)
+  for (int e = tid; e < 64 * 17; e += kPrepThreads) {
+    const int rr = e / 17, c4 = e - rr * 17;
+    const int d = ((rr >> 2) == c4) ? (rr & 3) : -1;
+    reinterpret_cast<float4*>(Tm + rr * 68)[c4] =
+        make_float4(d == 0 ? 1.f : 0.f, d == 1 ? 1.f : 0.f, d == 2 ? 1.f : 0.f, d == 3 ? 1.f : 0.f);
+  }
   {
     // this thread's half Gram row: TMEM lane 32 (warp % 4) + lane, columns jb .. jb + 31
     // (rows 0-63: (Q K^T)_i,:, rows 64-127: (K K^T)_i,:), as two 16-column blocks J
@@ -545,7 +598,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mma_commit(&bar_mma);
   }
   ok = mbar_wait(&bar_mma, 1, kWaitBudget);
-  if (!__syncthreads_and(ok)) goto fail;
+  if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
   {
@@ -587,7 +640,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mma_commit(&bar_mma);
   }
   ok = mbar_wait(&bar_mma, 0, kWaitBudget);
-  if (!__syncthreads_and(ok)) goto fail;
+  if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
   if ((warp & 3) < 2) {
@@ -650,12 +703,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     bulk_commit();
   }
   ok = mbar_wait(&bar_mma, 1, kWaitBudget);
-  if (!__syncthreads_and(ok)) goto fail;
+  if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
   {
     // every warp: key row i = TMEM lane, columns cb .. cb + 63 of M' = -D[:, 0:128] (fp16 K-major
-    // image over q and k, consumed) and of N = D[:, 128:256] (fp16 slices over [sk W | sk U])
+    // image over q and k, consumed) and of N = D[:, 128:256] (fp16 slices over [sk W | sk U]),
+    // staged for bulk stores (per-thread 16-byte global stores of these row layouts are far slower)
     const int i = 32 * (warp & 3) + lane, cb = (warp >> 2) * 64;
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
@@ -684,14 +738,24 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __syncthreads();
   if (tid == 0) {
     bulk_store(ub, sm + kPM, kMBytes);
-    bulk_store(ub + kUnitN, sm + kPWS, kNBytes);
     bulk_commit();
+    bulk_store(ub + kUnitN, sm + kPWS, kNBytes);   // its own group: it may drain into the next unit
+    bulk_commit();
+    // the next unit's tile loads overwrite q, k, v once the stores staged there have read them
+    // (every group but the last, N, which is staged over AT and T)
+    bulk_wait_read_but_last();
   }
-  goto done;
-fail:
-  if (tid == 0) set_error(a.err, kErrTimeout);
-done:
-  if (tid == 0) bulk_wait_read();   // shared memory stays valid until every bulk store has read it
+  // the next unit's tile loads (async proxy) overwrite what this unit wrote to shared memory
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (un >= total) break;
+  u = un;
+  if (warp == 7) tiles(u, true);
+  }   // units
+
+  if (!ok && tid == 0) set_error(a.err, kErrTimeout);
+  if (tid == 0) bulk_wait_read();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -984,6 +1048,19 @@ bool make_map(CUtensorMap* m, const void* base, int B, int L, int H) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// SMs of the current device (cached per device ordinal)
+int num_sms() {
+  static int cache[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 size_t units_bytes(int B, int L, int Hv) {
   return (size_t)B * Hv * ((L + kChunk - 1) / kChunk) * kUnitBytes;
 }
@@ -1021,7 +1098,9 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
     e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
   if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkPrep);
-  chunk_prep_kernel<<<dim3(a.NC, p.Hv, p.B), kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
+  const long long units = (long long)a.B * a.Hv * a.NC;
+  const int grid = (int)std::min<long long>(units, 2ll * num_sms());
+  chunk_prep_kernel<<<grid, kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
   stage_timer_end(slot, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
