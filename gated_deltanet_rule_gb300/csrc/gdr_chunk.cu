@@ -782,18 +782,21 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // threads that wait on it.
 constexpr int kStateThreads = 256;
 constexpr uint32_t kChainBar = 1, kChainCount = 128, kOutBar = 2, kOutCount = 64;
-constexpr int kEStages = 3;
+// Stage count: 3 for rows of several chunks; 1 for single-chunk rows (forks), whose smaller
+// footprint lets two CTAs share an SM.
 // stage: M' (two 16 KB K-atoms), Q' (two 8 KB K-atoms), this CTA's N and P U slices, Gamma_C
 constexpr uint32_t kEM = 0, kEQ0 = 32768, kEN = 49152, kEPU = 57344, kES = 61440;
 constexpr uint32_t kEStage = 62464;
-constexpr uint32_t kOffSb = kEStages * kEStage;   // two fp16 state operands, MN-major, 128 rows of 64 B
-constexpr uint32_t kStateSmem = kOffSb + 2 * 8192 + 1024;
+// after the stages: two fp16 state operands, MN-major, 128 rows of 64 B
+constexpr uint32_t state_smem(int stages) { return stages * kEStage + 2 * 8192 + 1024; }
 constexpr uint32_t kETx = 12 * 4096 + 8192 + 4096 + kSCopy;   // bytes landing in one stage of each CTA
 constexpr uint32_t kTmemState = 128;                           // D[2] at 0, 32; O'[2] at 64, 96
 static_assert(kEQ0 == kMBytes && kES + kSCopy <= kEStage && kEStage % 1024 == 0, "stage layout");
 
+template <int kEStages>
 __global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const ChunkArgs a) {
+  constexpr uint32_t kOffSb = kEStages * kEStage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t fullE[kEStages], freeE[kEStages], localFree[kEStages], bar_d, bar_o[2], oFree[2], sReady[2];
@@ -1095,7 +1098,9 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
 
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
+    e = cudaFuncSetAttribute(chunk_state_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(3));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(chunk_state_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(1));
   if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkPrep);
   const long long units = (long long)a.B * a.Hv * a.NC;
@@ -1105,7 +1110,10 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   slot = stage_timer_begin(s, kKernChunkState);
-  chunk_state_kernel<<<dim3(kSlices, p.Hv, p.B), kStateThreads, kStateSmem, s>>>(a);
+  if (a.NC == 1)
+    chunk_state_kernel<1><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(1), s>>>(a);
+  else
+    chunk_state_kernel<3><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(3), s>>>(a);
   stage_timer_end(slot, s);
   return cudaGetLastError();
 }
