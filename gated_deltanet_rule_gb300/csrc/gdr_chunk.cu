@@ -31,12 +31,12 @@
 //   then P [W | U], then K^T [diag(sk) W | diag(sk) U] = [-M' | N]. Per unit it writes, with bulk
 //   copies from shared memory, M' and Q' as the 128B-swizzled images kernel 2 uses as MMA
 //   operands, N and P U as four 32-column slices, and Gamma_C.
-// Kernel 2 (gdr_chunk_state, a cluster of 4 CTAs per (row, value head), CTA r owning value columns
-//   [32 r, 32 r + 32), sequential over chunks): the float32 state slice stays in registers. Per
-//   chunk one thread issues D = M' S and O' = Q' S (fp16 copy of S as the B operand); the state
-//   warps form S = Gamma_C S + D + N and the next fp16 copy; two output warps form o = O' + P U
-//   off the critical path. M' and Q' are TMA-multicast across the cluster, each CTA loading a
-//   quarter, by a producer warp that runs up to three chunks ahead.
+// Kernel 2 (gdr_chunk_state, four independent CTAs per (row, value head), CTA s owning value
+//   columns [32 s, 32 s + 32), sequential over chunks): the float32 state slice stays in registers.
+//   Per chunk one thread issues D = M' S (fp16 copy of S as the B operand); the state warps form
+//   S = Gamma_C S + D + N and the next fp16 copy; a second thread issues O' = Q' S and two output
+//   warps form o = O' + P U, off the critical path. Two producer warps keep a ring of chain tiles
+//   (M', N, Gamma_C) and a ring of output tiles (Q', P U) filled ahead of the chain.
 #include <algorithm>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -55,7 +55,7 @@ namespace {
 constexpr float kScale = 0.08838834764831845f;   // 128^-0.5
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitBudget = 2000000000ll;   // cycles (~1 s) before a wait gives up
-constexpr int kSlices = 4;                        // value-column slices per value head = cluster size
+constexpr int kSlices = 4;                        // value-column slices (state CTAs) per value head
 constexpr int kN = kD / kSlices;                  // 32 value columns per state CTA
 
 // Workspace. Per (row, value head, chunk) unit:
@@ -765,77 +765,72 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 }
 
 // -------------------------------------------------------------------------------------------
-// Kernel 2: sequential state recurrence over chunks; cluster of 4 CTAs per (row, value head)
+// Kernel 2: sequential state recurrence over chunks; four CTAs per (row, value head)
 // -------------------------------------------------------------------------------------------
+// CTA s (blockIdx.x) owns value columns [32 s, 32 s + 32) of one value head. The four CTAs of a
+// head are independent: each reads the head's M' and Q' tiles itself (the other three read the
+// same lines, so they come from L2) and its own slices of N and P U. No CTA waits on another.
 // Warp roles (warp w reads TMEM lanes 32 (w % 4) .. + 31):
 //   warps 0-3: own the state rows (key row = tid, 32 value columns, float32 registers) and form
-//              S = Gamma_C S + D + N; thread 0 issues the state product. Named barrier 1.
+//              S = Gamma_C S + D + N; thread 0 issues the state product D = M' S. Named barrier 1.
 //   warps 4, 5: output rows o = O' + P U for positions 0-63 (TMEM lanes 0-63); named barrier 2.
-//   warp 6: producer, loading the tiles of up to three chunks ahead; it also forwards this CTA's
-//           stage releases to the other CTAs of the cluster.
-//   warp 7: issues the output product, so that its issue time stays off the state chain.
-// Per chunk c (stage c % 3, buffers p = c % 2): thread 0 issues D[p] = M' Sb[p] and then signals
-// sReady[p]; warp 7 issues O'[p] = Q' Sb[p] once the output warps are done with chunk c - 2
-// (oFree[p]) and commits it to bar_o[p]. The state warps write S_{c+1} into Sb[p ^ 1] after the
-// O' product of chunk c - 1 (which read it) has completed. sReady, oFree and bar_o come in pairs
-// indexed by p, so each completes every other chunk and none can run two phases ahead of the
-// threads that wait on it.
-constexpr int kStateThreads = 256;
+//   warp 6: loads the chain ring (M', this CTA's N slice, Gamma_C) up to CS chunks ahead.
+//   warp 7: issues the output product O' = Q' S, so that its issue time stays off the chain.
+//   warp 8: loads the output ring (Q', this CTA's P U slice) up to OS chunks ahead.
+// Per chunk c: chain stage c % CS (chFull / chFree: the state warps release it right after their
+// update), output stage c % OS (outFull / outFree: released by the output warps), state operand
+// q = c % 3 (sReady: S_c written; sFree: the output product has read it), TMEM buffers p = c % 2
+// (D[p]; O'[p] with bar_o: product done, oFree: the output warps have read it). Every barrier
+// completes once per CS, OS, 3 or 2 chunks and none can run two phases ahead of its waiters.
+constexpr int kStateThreads = 288;
 constexpr uint32_t kChainBar = 1, kChainCount = 128, kOutBar = 2, kOutCount = 64;
-// Stage count: 3 for rows of several chunks; 1 for single-chunk rows (forks), whose smaller
-// footprint lets two CTAs share an SM.
-// stage: M' (two 16 KB K-atoms), Q' (two 8 KB K-atoms), this CTA's N and P U slices, Gamma_C
-constexpr uint32_t kEM = 0, kEQ0 = 32768, kEN = 49152, kEPU = 57344, kES = 61440;
-constexpr uint32_t kEStage = 62464;
-// after the stages: two fp16 state operands, MN-major, 128 rows of 64 B
-constexpr uint32_t state_smem(int stages) { return stages * kEStage + 2 * 8192 + 1024; }
-constexpr uint32_t kETx = 12 * 4096 + 8192 + 4096 + kSCopy;   // bytes landing in one stage of each CTA
-constexpr uint32_t kTmemState = 128;                           // D[2] at 0, 32; O'[2] at 64, 96
-static_assert(kEQ0 == kMBytes && kES + kSCopy <= kEStage && kEStage % 1024 == 0, "stage layout");
+constexpr uint32_t kCStage = 40960;    // M' (two 16 KB K-atoms), then this CTA's N slice (8 KB)
+constexpr uint32_t kCN = 32768;
+constexpr uint32_t kOStage = 20480;    // Q' (two 8 KB K-atoms), then this CTA's P U slice (4 KB)
+constexpr uint32_t kOPU = 16384;
+constexpr uint32_t kTmemState = 128;   // D[2] at 0, 32; O'[2] at 64, 96
+// Rings: 4 chain and 2 output stages for rows of several chunks; 1 and 1 for single-chunk rows
+// (forks), whose smaller footprint lets two CTAs share an SM. After the rings: three fp16 state
+// operands (MN-major, 128 rows of 64 B). The M = 128 output product reads 8 KB past each Q' tile
+// (operand rows 64-127, whose products land in TMEM lanes nobody reads), which stays inside the
+// buffer because the state operands follow the output ring.
+constexpr uint32_t state_smem(int cs, int os) { return cs * kCStage + os * kOStage + 3 * 8192 + 1024; }
+static_assert(kCN == kMBytes && kOPU == kQBytes, "stage layout");
 
-template <int kEStages>
-__global__ void __cluster_dims__(kSlices, 1, 1) __launch_bounds__(kStateThreads, 1)
+template <int CS, int OS>
+__global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const ChunkArgs a) {
-  constexpr uint32_t kOffSb = kEStages * kEStage;
+  constexpr uint32_t kOffO = CS * kCStage;
+  constexpr uint32_t kOffSb = kOffO + OS * kOStage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t fullE[kEStages], freeE[kEStages], localFree[kEStages], bar_d, bar_o[2], oFree[2], sReady[2];
+  __shared__ uint64_t chFull[CS], chFree[CS], outFull[OS], outFree[OS], bar_d, bar_o[2], oFree[2], sReady[3],
+      sFree[3];
+  __shared__ __align__(16) float4 gam_ring[CS];   // Gamma_C of the chunk in each chain stage
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
-  const uint32_t rank = cluster_ctarank();
-  const int sl = (int)rank, h = blockIdx.y, b = blockIdx.z;
+  const int sl = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NC = a.NC;
 
-  // tiles of chunk c: this CTA multicasts 3 of the 12 shared 4 KB pieces (M', Q'; contiguous in
-  // the unit and in the stage) and loads its own N and P U slices and Gamma_C
-  auto issue = [&](int c) {
-    uint8_t* st = sm + (c % kEStages) * kEStage;
-    uint64_t* bar = &fullE[c % kEStages];
-    const uint8_t* ub = unit_base(a, b, h, c);
-    mbar_arrive_expect_tx(bar, kETx);
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      const int p = 3 * sl + k;
-      bulk_load_mc(st + p * 4096, ub + p * 4096, 4096, bar, 0xF);
-    }
-    bulk_load(st + kEN, ub + kUnitN + sl * 8192, 8192, bar);
-    bulk_load(st + kEPU, ub + kUnitPU + sl * 4096, 4096, bar);
-    bulk_load(st + kES, ub + kUnitS, kSCopy, bar);
-  };
-
   if (tid == 0) {
-    for (int s = 0; s < kEStages; ++s) {
-      mbar_init(&fullE[s], 1);
-      mbar_init(&freeE[s], kSlices);      // one arrival from the producer of every CTA
-      mbar_init(&localFree[s], 2);        // this CTA's state and output warps
+    for (int s = 0; s < CS; ++s) {
+      mbar_init(&chFull[s], 1);
+      mbar_init(&chFree[s], 1);
+    }
+    for (int s = 0; s < OS; ++s) {
+      mbar_init(&outFull[s], 1);
+      mbar_init(&outFree[s], 1);
     }
     mbar_init(&bar_d, 1);
     for (int p = 0; p < 2; ++p) {
       mbar_init(&bar_o[p], 1);
       mbar_init(&oFree[p], 1);
-      mbar_init(&sReady[p], 1);
+    }
+    for (int q = 0; q < 3; ++q) {
+      mbar_init(&sReady[q], 1);
+      mbar_init(&sFree[q], 1);
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -843,7 +838,6 @@ chunk_state_kernel(const ChunkArgs a) {
   if (warp == 0) tmem_alloc(&tmem_base, kTmemState);
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();   // every CTA's barriers exist before anyone multicasts into them
   tc_fence_after();
   const uint32_t tb = tmem_base;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -860,25 +854,31 @@ chunk_state_kernel(const ChunkArgs a) {
   }
 
   if (skip) {
-    // every CTA of the cluster reads the same index and skips together
-  } else if (warp == 6) {
-    // ---------------- producer ----------------
-    // Lane 0 issues the loads. Stage c % 3 last held chunk c - 3: once this CTA's consumers are
-    // done with it (localFree), lanes 0-3 tell the cluster's CTAs in parallel (a release at
-    // cluster scope takes long, so it stays off the chain), and lane 0 waits until every CTA is
-    // done (freeE) before multicasting into it.
-    for (int c = 0; c < NC; ++c) {
-      const int es = c % kEStages;
-      if (c >= kEStages) {
-        const uint32_t par = ((c - kEStages) / kEStages) & 1;
-        ok = mbar_wait(&localFree[es], par, kWaitBudget);
-        if (ok && lane < kSlices) remote_arrive(&freeE[es], lane);
-        ok = ok && (lane != 0 || mbar_wait(&freeE[es], par, kWaitBudget));
+    // every CTA of the row reads the same index and skips
+  } else if (warp == 6 || warp == 8) {
+    // ---------------- producers (lane 0): the chain ring (warp 6) and the output ring (warp 8) ----
+    if (lane == 0) {
+      const bool chain = warp == 6;
+      const int S = chain ? CS : OS;
+      for (int c = 0; c < NC; ++c) {
+        const int s = c % S;
+        if (c >= S) ok = mbar_wait(chain ? &chFree[s] : &outFree[s], ((c - S) / S) & 1, kWaitBudget);
+        if (!ok || *(volatile int*)&abort_flag) break;
+        const uint8_t* ub = unit_base(a, b, h, c);
+        if (chain) {
+          uint8_t* st = sm + s * kCStage;
+          mbar_arrive_expect_tx(&chFull[s], kMBytes + 8192 + kSCopy);
+          bulk_load(st, ub, 16384, &chFull[s]);
+          bulk_load(st + 16384, ub + 16384, 16384, &chFull[s]);
+          bulk_load(st + kCN, ub + kUnitN + sl * 8192, 8192, &chFull[s]);
+          bulk_load(&gam_ring[s], ub + kUnitS, kSCopy, &chFull[s]);
+        } else {
+          uint8_t* st = sm + kOffO + s * kOStage;
+          mbar_arrive_expect_tx(&outFull[s], kQBytes + 4096);
+          bulk_load(st, ub + kUnitQ, kQBytes, &outFull[s]);
+          bulk_load(st + kOPU, ub + kUnitPU + sl * 4096, 4096, &outFull[s]);
+        }
       }
-      ok = __all_sync(0xffffffffu, ok) && !*(volatile int*)&abort_flag;
-      if (!ok) break;
-      if (lane == 0) issue(c);
-      __syncwarp();
     }
   } else if (warp < 4) {
     // ---------------- state warps ----------------
@@ -894,42 +894,42 @@ chunk_state_kernel(const ChunkArgs a) {
         Sm[n] = x.x; Sm[n + 1] = x.y; Sm[n + 2] = x.z; Sm[n + 3] = x.w;
       }
     }
-    // fp16 state operand p: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle
-    auto write_state_operand = [&](int p) {
+    // fp16 state operand q: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle
+    auto write_state_operand = [&](int q) {
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4*>(sm + kOffSb + p * 8192 + swz64(kr * 64 + ch * 16)) = pack8_f16(Sm + 8 * ch);
+        *reinterpret_cast<uint4*>(sm + kOffSb + q * 8192 + swz64(kr * 64 + ch * 16)) = pack8_f16(Sm + 8 * ch);
     };
     write_state_operand(0);
     fence_async_smem();
     named_bar_and(kChainBar, kChainCount, true);
 
     for (int c = 0; c < NC; ++c) {
-      const int es = c % kEStages, p = c & 1;
-      uint8_t* st = sm + es * kEStage;
-      ok = mbar_wait(&fullE[es], (c / kEStages) & 1, kWaitBudget) && !*(volatile int*)&abort_flag;
+      const int cs = c % CS, p = c & 1, q = c % 3, qn = (c + 1) % 3;
+      uint8_t* st = sm + cs * kCStage;
+      ok = mbar_wait(&chFull[cs], (c / CS) & 1, kWaitBudget) && !*(volatile int*)&abort_flag;
       if (tid == 0 && ok) {
         tc_fence_after();
-        const uint32_t sb = smem_u32(sm + kOffSb + p * 8192);
+        const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
         const uint32_t idesc = idesc_f16(128, kN, false, true);
-        const uint32_t sm_m = smem_u32(st + kEM);
+        const uint32_t sm_m = smem_u32(st);
         // D[p] = M' S   (the critical product)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16(tb + 32 * p, smem_desc(sm_m + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                    smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
         mma_commit(&bar_d);
-        mbar_arrive(&sReady[p]);   // Sb[p] holds S_c: warp 7 may issue the output product
+        mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
       }
       ok = ok && mbar_wait(&bar_d, c & 1, kWaitBudget);
-      // Sb[p ^ 1] is rewritten below: the output product of chunk c - 1 must have read it
-      if (c >= 1) ok = ok && mbar_wait(&bar_o[p ^ 1], ((c - 1) >> 1) & 1, kWaitBudget);
+      // Sb[qn] is rewritten below: the output product of chunk c - 2 must have read it
+      if (c >= 2) ok = ok && mbar_wait(&sFree[qn], ((c - 2) / 3) & 1, kWaitBudget);
       if (ok) {
         tc_fence_after();
         float d[kN];
         tmem_ld32(tb + lane_base + 32 * p, d);
-        const float gc = *reinterpret_cast<const float*>(st + kES);
-        const uint8_t* nrow = st + kEN;
+        const float gc = gam_ring[cs].x;
+        const uint8_t* nrow = st + kCN;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           float nv[8];
@@ -937,13 +937,13 @@ chunk_state_kernel(const ChunkArgs a) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], d[8 * ch + e] + nv[e]);
         }
-        write_state_operand(p ^ 1);
+        write_state_operand(qn);
       }
       fence_async_smem();
       tc_fence_before();
       if (!named_bar_and(kChainBar, kChainCount, ok)) break;
-      // this CTA's state warps are done with stage es (D complete, N read)
-      if (tid == 0 && c + kEStages < NC) mbar_arrive(&localFree[es]);
+      // the chain stage is free (D complete, N and Gamma_C read)
+      if (tid == 0 && c + CS < NC) mbar_arrive(&chFree[cs]);
     }
     if (ok && a.S_T) {
       float* dst = a.S_T + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
@@ -956,29 +956,30 @@ chunk_state_kernel(const ChunkArgs a) {
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, kN, false, true);
       for (int c = 0; c < NC; ++c) {
-        const int es = c % kEStages, p = c & 1;
-        ok = mbar_wait(&fullE[es], (c / kEStages) & 1, kWaitBudget) &&
-             mbar_wait(&sReady[p], (c >> 1) & 1, kWaitBudget) &&
+        const int os = c % OS, p = c & 1, q = c % 3;
+        ok = mbar_wait(&outFull[os], (c / OS) & 1, kWaitBudget) &&
+             mbar_wait(&sReady[q], (c / 3) & 1, kWaitBudget) &&
              (c < 2 || mbar_wait(&oFree[p], ((c - 2) >> 1) & 1, kWaitBudget));
         if (!ok || *(volatile int*)&abort_flag) break;
         tc_fence_after();
-        const uint32_t sb = smem_u32(sm + kOffSb + p * 8192);
-        const uint32_t sm_q = smem_u32(sm + es * kEStage + kEQ0);
-        // O'[p] = Q' S  (M = 128; operand rows 64-127 run into the next tile and are not read)
+        const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
+        const uint32_t sm_q = smem_u32(sm + kOffO + os * kOStage);
+        // O'[p] = Q' S  (M = 128; operand rows 64-127 run past the tile and are not read)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16(tb + 64 + 32 * p, smem_desc(sm_q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
                    smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
         mma_commit(&bar_o[p]);
+        mma_commit(&sFree[q]);
       }
     }
   } else {
     // ---------------- output warps 4, 5 ----------------
     const int i = tid - 128;   // position in the chunk = TMEM lane
     for (int c = 0; c < NC; ++c) {
-      const int es = c % kEStages, p = c & 1;
-      const uint8_t* st = sm + es * kEStage;
-      ok = mbar_wait(&fullE[es], (c / kEStages) & 1, kWaitBudget) &&
+      const int os = c % OS, p = c & 1;
+      const uint8_t* st = sm + kOffO + os * kOStage;
+      ok = mbar_wait(&outFull[os], (c / OS) & 1, kWaitBudget) &&
            mbar_wait(&bar_o[p], (c >> 1) & 1, kWaitBudget) && !*(volatile int*)&abort_flag;
       if (ok) {
         tc_fence_after();
@@ -987,7 +988,7 @@ chunk_state_kernel(const ChunkArgs a) {
         const int pos = c * 64 + i;
         if (pos < a.L) {
           float pu[kN];
-          const uint8_t* purow = st + kEPU;
+          const uint8_t* purow = st + kOPU;
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch)
             unpack8_f16(*reinterpret_cast<const uint4*>(purow + swz64(i * 64 + ch * 16)), pu + 8 * ch);
@@ -1003,19 +1004,19 @@ chunk_state_kernel(const ChunkArgs a) {
       }
       tc_fence_before();
       if (!named_bar_and(kOutBar, kOutCount, ok)) break;
-      if (tid == 128) mbar_arrive(&oFree[p]);
-      // this CTA's output warps are done with stage es (the Q' product complete, P U read)
-      if (tid == 128 && c + kEStages < NC) mbar_arrive(&localFree[es]);
+      if (tid == 128) {
+        mbar_arrive(&oFree[p]);
+        if (c + OS < NC) mbar_arrive(&outFree[os]);   // the Q' product complete, P U read
+      }
     }
   }
   if (!ok) {
     atomicExch(&abort_flag, 1);
     set_error(a.err, kErrTimeout);
   }
-  __syncwarp();         // the producer warp's lanes reconverge before the block barrier
+  __syncwarp();         // the producer and issuer warps' lanes reconverge before the block barrier
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();   // no CTA leaves while a peer may still multicast into it or arrive on it
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tb, kTmemState);
@@ -1098,9 +1099,9 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
 
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(chunk_state_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(3));
+    e = cudaFuncSetAttribute(chunk_state_kernel<4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(4, 2));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(chunk_state_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(1));
+    e = cudaFuncSetAttribute(chunk_state_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(1, 1));
   if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkPrep);
   const long long units = (long long)a.B * a.Hv * a.NC;
@@ -1111,9 +1112,9 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   slot = stage_timer_begin(s, kKernChunkState);
   if (a.NC == 1)
-    chunk_state_kernel<1><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(1), s>>>(a);
+    chunk_state_kernel<1, 1><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(1, 1), s>>>(a);
   else
-    chunk_state_kernel<3><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(3), s>>>(a);
+    chunk_state_kernel<4, 2><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(4, 2), s>>>(a);
   stage_timer_end(slot, s);
   return cudaGetLastError();
 }
