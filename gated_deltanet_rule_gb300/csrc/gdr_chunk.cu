@@ -366,21 +366,22 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     cp_async_commit();
   };
   // raw q, k, v tiles of a unit (six 64 x 64 boxes) into shared memory, or only into L2; called
-  // by a whole warp, lane t < 6 issuing box t (lane 0 also posts the byte count)
+  // by every thread: lane 0 of warp t < 6 issues box t, so the six issues proceed in parallel
+  // (warp 0 also posts the byte count; the order of count and bytes does not matter)
   auto tiles = [&](int u, bool to_smem) {
+    if (warp >= 6 || lane != 0) return;
+    const int t = warp;
     int c, h, b;
     unit_of(u, c, h, b);
     const int hk = h / r;
-    const CUtensorMap* map = lane < 2 ? &tm_q : (lane < 4 ? &tm_k : &tm_v);
-    const uint32_t dst = lane < 4 ? (uint32_t)lane * 8192 : kPV + (uint32_t)(lane - 4) * 8192;
-    const int c0 = (lane & 1) * 64, c1 = lane < 4 ? hk : h;
+    const CUtensorMap* map = t < 2 ? &tm_q : (t < 4 ? &tm_k : &tm_v);
+    const int c0 = (t & 1) * 64, c1 = t < 4 ? hk : h;
     // shared-memory order: q0 k0 q1 k1 (the Gram operand), then v0 v1
-    const uint32_t dst_qk = (uint32_t)((lane & 1) * 16384 + (lane >> 1) * 8192);
+    const uint32_t dst = t < 4 ? (uint32_t)((t & 1) * 16384 + (t >> 1) * 8192) : kPV + (uint32_t)(t - 4) * 8192;
     if (to_smem) {
-      if (lane == 0) mbar_arrive_expect_tx(&bar_ld, 49152);
-      __syncwarp();
-      if (lane < 6) tma_load_4d(sm + (lane < 4 ? dst_qk : dst), map, &bar_ld, c0, c1, c * 64, b);
-    } else if (lane < 6) {
+      if (t == 0) mbar_arrive_expect_tx(&bar_ld, 49152);
+      tma_load_4d(sm + dst, map, &bar_ld, c0, c1, c * 64, b);
+    } else {
       tma_prefetch_4d(map, c0, c1, c * 64, b);
     }
   };
@@ -393,7 +394,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     fence_mbar_init();
   }
   __syncthreads();
-  if (warp == 7) tiles(u, true);
+  tiles(u, true);
   if (warp == 1) tmem_alloc(&tmem_base, 256);
   tc_fence_before();
   __syncthreads();
@@ -409,7 +410,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int un = u + (int)gridDim.x;
   if (un < total) {
     copy_gates(un, (it + 1) & 1);
-    if (warp == 7) tiles(un, false);
   } else {
     cp_async_commit();
   }
@@ -436,48 +436,62 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   ok = mbar_wait(&bar_ld, it & 1, kWaitBudget);
   if (!__syncthreads_and(ok)) break;
 
-  // Gram MMA (bf16, exact products): D[0:128, 0:64] = [Q; K] K^T
-  if (tid == 0) {
-    tc_fence_after();
-    const uint32_t idesc = idesc_bf16(128, 64, false, false);
+  // Gram MMA (bf16, exact products): D[0:128, 0:64] = [Q; K] K^T, issued by warp 7 while warps
+  // 0-3 form the inverse norms and warps 4-6 the decay factors
+  if (warp == 7) {
+    if (lane == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16(128, 64, false, false);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t atom = smem_u32(sm) + (kk >> 2) * 16384 + (kk & 3) * 32;
-      mma_bf16(tb, smem_desc(atom, 16, 1024), smem_desc(atom + 8192, 16, 1024), idesc, kk > 0);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t atom = smem_u32(sm) + (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_bf16(tb, smem_desc(atom, 16, 1024), smem_desc(atom + 8192, 16, 1024), idesc, kk > 0);
+      }
+      mma_commit(&bar_mma);
     }
-    mma_commit(&bar_mma);
-  }
-  // inverse norms: two threads per row (one 64-column atom each); rows 0-63 q, 64-127 k. The sum
-  // does not care about the order of the 16-byte chunks, so each thread starts at a different one
-  // (rotated by row and atom) and the eight lanes of a quarter-warp hit eight different banks.
-  {
-    const int row = tid >> 1, half = tid & 1, rr = row & 63;
-    const uint8_t* base = sm + (row < 64 ? kPQ0 : kPK0) + half * 16384 + rr * 128;
+  } else if (warp < 4) {
+    // inverse norms, one thread per row (rows 0-63 q, 64-127 k), both 64-column atoms. The sum
+    // does not care about the order of the 16-byte chunks, so each row starts at a different one
+    // and the eight lanes of a quarter-warp hit eight different banks.
+    const int rr = tid & 63;
+    const uint8_t* base = sm + (tid < 64 ? kPQ0 : kPK0) + rr * 128;
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      const uint4 w = *reinterpret_cast<const uint4*>(base + (((ch + rr + 4 * half) & 7) << 4));
-      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+    for (int half = 0; half < 2; ++half) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xFFFF0000u);
-        s0 = fmaf(lo, lo, s0);
-        s1 = fmaf(hi, hi, s1);
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 w = *reinterpret_cast<const uint4*>(base + half * 16384 + (((ch + rr) & 7) << 4));
+        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xFFFF0000u);
+          s0 = fmaf(lo, lo, s0);
+          s1 = fmaf(hi, hi, s1);
+        }
       }
     }
-    float s = s0 + s1;
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    if (half == 0) (row < 64 ? qinv : kinv)[rr] = rsqrtf(s + 1e-6f);
+    (tid < 64 ? qinv : kinv)[rr] = rsqrtf(s0 + s1 + 1e-6f);
+  } else {
+    // decay factors through the 16-block anchors: for j < 16 I <= i,
+    // exp(gamma_i - gamma_j) = exp(gamma_i - gamma_16I) * exp(gamma_16I - gamma_j), both factors
+    // <= 1; the k scales ki_j of E2 and ki_i of sk are applied once the norms are known
+    for (int e = tid - 128; e < 320; e += 96) {
+      if (e < 64) {
+        e1[e] = ex2_approx(gam2[e] - gam2[e & ~15]);
+      } else if (e < 128) {
+        skv[e - 64] = exp2f(gam2[63] - gam2[e - 64]);
+      } else {
+        const int I = 1 + ((e - 128) >> 6), j = e & 63;
+        E2[I * 68 + j] = (j < 16 * I) ? ex2_approx(gam2[16 * I] - gam2[j]) : 0.f;
+      }
+    }
   }
   __syncthreads();
-  // decay factors through the 16-block anchors: for j < 16 I <= i,
-  // exp(gamma_i - gamma_j) = exp(gamma_i - gamma_16I) * exp(gamma_16I - gamma_j), both factors <= 1
   if (tid < 64) {
-    e1[tid] = ex2_approx(gam2[tid] - gam2[tid & ~15]);
-    skv[tid] = exp2f(gam2[63] - gam2[tid]) * kinv[tid];
+    skv[tid] *= kinv[tid];
   } else {
     const int I = 1 + ((tid - 64) >> 6), j = tid & 63;
-    E2[I * 68 + j] = (j < 16 * I) ? kinv[j] * ex2_approx(gam2[16 * I] - gam2[j]) : 0.f;
+    E2[I * 68 + j] *= kinv[j];
   }
   if (tid == 0) bulk_wait_read();   // the previous unit's N store has read the AT / Tm region
   ok = mbar_wait(&bar_mma, 0, kWaitBudget);
@@ -597,6 +611,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                kk > 0);
     mma_commit(&bar_mma);
   }
+  if (un < total) tiles(un, false);   // the next unit's tiles into L2, while W and U are formed
   ok = mbar_wait(&bar_mma, 1, kWaitBudget);
   if (!__syncthreads_and(ok)) break;
   tc_fence_after();
@@ -751,7 +766,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __syncthreads();
   if (un >= total) break;
   u = un;
-  if (warp == 7) tiles(u, true);
+  tiles(u, true);
   }   // units
 
   if (!ok && tid == 0) set_error(a.err, kErrTimeout);
