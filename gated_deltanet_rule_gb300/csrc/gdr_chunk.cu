@@ -75,6 +75,7 @@ struct ChunkArgs {
   const float* S0;
   const int64_t* S0_idx;   // row b starts from S0[S0_idx[b]] (forks); NULL = S0[b]
   int n_S0;                // states S0 holds when S0_idx is set
+  int fused;               // single-chunk rows: kernel 1 applies the chunk to S0 itself
   __nv_bfloat16* o;
   float* S_T;
   uint8_t* ws;       // 1024-aligned
@@ -402,6 +403,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t tb = tmem_base;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   bool ok = true;
+  uint32_t mma_phase = 0;   // completions of bar_mma so far (4 per unit, 5 with the fused apply)
 
   for (int it = 0;; ++it) {
   int c, h, b;
@@ -494,7 +496,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     E2[I * 68 + j] *= kinv[j];
   }
   if (tid == 0) bulk_wait_read();   // the previous unit's N store has read the AT / Tm region
-  ok = mbar_wait(&bar_mma, 0, kWaitBudget);
+  ok = mbar_wait(&bar_mma, mma_phase++ & 1, kWaitBudget);
   if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
@@ -612,7 +614,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mma_commit(&bar_mma);
   }
   if (un < total) tiles(un, false);   // the next unit's tiles into L2, while W and U are formed
-  ok = mbar_wait(&bar_mma, 1, kWaitBudget);
+  ok = mbar_wait(&bar_mma, mma_phase++ & 1, kWaitBudget);
   if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
@@ -654,7 +656,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mma_bf16(tb, smem_desc(pa + kk * 32, 16, 1024), smem_desc(wu + kk * 2048, 8192, 1024), idesc, kk > 0);
     mma_commit(&bar_mma);
   }
-  ok = mbar_wait(&bar_mma, 0, kWaitBudget);
+  ok = mbar_wait(&bar_mma, mma_phase++ & 1, kWaitBudget);
   if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
@@ -712,12 +714,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(tb, smem_desc(kt + kk * 2048, 16384, 1024), smem_desc(wsu + kk * 2048, 8192, 1024), idesc, kk > 0);
     mma_commit(&bar_mma);
-    bulk_store(ub + kUnitQ, sm + kPV, kQBytes);
-    bulk_store(ub + kUnitPU, sm + kPV + 16384, kPUBytes);
-    bulk_store(ub + kUnitS, sm + kPP, kSCopy);
-    bulk_commit();
+    if (!a.fused) {
+      bulk_store(ub + kUnitQ, sm + kPV, kQBytes);
+      bulk_store(ub + kUnitPU, sm + kPV + 16384, kPUBytes);
+      bulk_store(ub + kUnitS, sm + kPP, kSCopy);
+      bulk_commit();
+    }
   }
-  ok = mbar_wait(&bar_mma, 1, kWaitBudget);
+  ok = mbar_wait(&bar_mma, mma_phase++ & 1, kWaitBudget);
   if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
@@ -750,8 +754,95 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   }
   fence_async_smem();
+  tc_fence_before();
   __syncthreads();
-  if (tid == 0) {
+  if (a.fused) {
+    // Single-chunk row: apply the chunk to the initial state here (no workspace, no kernel 2).
+    //   S_T = Gamma_C S0 + M' S0 + N,   o = Q' S0 + P U
+    // computed transposed, with S0^T (fp16) as the A operand in TMEM: D^T = S0^T M'^T (values x
+    // keys, columns 64-191), O^T = S0^T Q'^T (values x positions, columns 192-255). Thread
+    // (warp w, lane l) owns value v = 32 (w % 4) + l and keys / positions of half w / 4.
+    tc_fence_after();
+    const int v = 32 * (warp & 3) + lane, hb = warp >> 2;
+    const float* s0 = nullptr;
+    bool write = true;
+    if (a.S0) {
+      size_t row = b;
+      if (a.S0_idx) {
+        const long long ix = a.S0_idx[b];
+        write = ix >= 0 && ix < a.n_S0;
+        row = write ? (size_t)ix : 0;
+        if (!write && tid == 0) set_error(a.err, kErrDeviceIndex);
+      }
+      s0 = a.S0 + (row * a.Hv + h) * kD * kD;
+    } else if (a.S0_idx) {
+      const long long ix = a.S0_idx[b];
+      write = ix >= 0 && ix < a.n_S0;
+      if (!write && tid == 0) set_error(a.err, kErrDeviceIndex);
+    }
+    {
+      uint32_t r32[32];
+#pragma unroll
+      for (int c2 = 0; c2 < 32; ++c2) {
+        const int j = 64 * hb + 2 * c2;
+        const float x0 = s0 ? __ldg(s0 + (size_t)j * kD + v) : 0.f;
+        const float x1 = s0 ? __ldg(s0 + (size_t)(j + 1) * kD + v) : 0.f;
+        r32[c2] = pack_f16x2(x0, x1);
+      }
+      tmem_st32(tb + lane_base + 32 * hb, r32);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t id_d = idesc_f16(128, 128, false, false), id_o = idesc_f16(128, 64, false, false);
+      const uint32_t mp = smem_u32(sm + kPM), qp = smem_u32(sm + kPV);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_f16_tmem_a(tb + 64, tb + kk * 8, smem_desc(mp + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024), id_d,
+                       kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_f16_tmem_a(tb + 192, tb + kk * 8, smem_desc(qp + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), id_o,
+                       kk > 0);
+      mma_commit(&bar_mma);
+    }
+    ok = mbar_wait(&bar_mma, mma_phase++ & 1, kWaitBudget);
+    if (!__syncthreads_and(ok)) break;
+    tc_fence_after();
+    if (write && a.S_T) {
+      // S_T[i][v] for keys i = 64 hb .. + 63; N[i][v] from its staged fp16 slice
+      float* so = a.S_T + (((size_t)b * a.Hv + h) * kD) * kD;
+      const float gc = Gam[63];
+      const uint8_t* nsl = sm + kPWS + (v >> 5) * 8192;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        float d[32];
+        tmem_ld32(tb + lane_base + 64 + 64 * hb + 32 * part, d);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int i = 64 * hb + 32 * part + e;
+          const float n = __half2float(*reinterpret_cast<const __half*>(nsl + swz64(i * 64 + (v & 31) * 2)));
+          const float x = s0 ? __ldg(s0 + (size_t)i * kD + v) : 0.f;
+          so[(size_t)i * kD + v] = fmaf(gc, x, d[e] + n);
+        }
+      }
+    }
+    if (write) {
+      // o at positions 32 hb .. + 31 of this chunk; (P U)[pos][v] from its staged fp16 slice
+      float ov[32];
+      tmem_ld32(tb + lane_base + 192 + 32 * hb, ov);
+      const uint8_t* psl = sm + kPV + 16384 + (v >> 5) * 4096;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int pos = 32 * hb + e, pt = c * 64 + pos;
+        if (pt < a.L) {
+          const float pu = __half2float(*reinterpret_cast<const __half*>(psl + swz64(pos * 64 + (v & 31) * 2)));
+          a.o[(((size_t)b * a.L + pt) * a.Hv + h) * kD + v] = __float2bfloat16_rn(ov[e] + pu);
+        }
+      }
+    }
+  } else if (tid == 0) {
     bulk_store(ub, sm + kPM, kMBytes);
     bulk_commit();
     bulk_store(ub + kUnitN, sm + kPWS, kNBytes);   // its own group: it may drain into the next unit
@@ -1088,6 +1179,7 @@ size_t units_bytes(int B, int L, int Hv) {
 
 size_t chunk_workspace_bytes(int B, int Hk, int L, int Hv) {
   (void)Hk;
+  if (L <= kChunk) return 0;   // single-chunk rows are finished by kernel 1 without a workspace
   return units_bytes(B, L, Hv) + 1024;
 }
 
@@ -1102,6 +1194,7 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   a.S0 = p.S0;
   a.S0_idx = p.S0_idx;
   a.n_S0 = p.n_S0;
+  a.fused = (p.L <= kChunk) ? 1 : 0;
   a.o = static_cast<__nv_bfloat16*>(p.o);
   a.S_T = p.S_T;
   a.ws = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p.ws) + 1023) & ~uintptr_t(1023));
@@ -1115,8 +1208,6 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(chunk_state_kernel<4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(4, 2));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(chunk_state_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(1, 1));
   if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkPrep);
   const long long units = (long long)a.B * a.Hv * a.NC;
@@ -1125,11 +1216,9 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   stage_timer_end(slot, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (a.fused) return cudaSuccess;   // single-chunk rows are complete after kernel 1
   slot = stage_timer_begin(s, kKernChunkState);
-  if (a.NC == 1)
-    chunk_state_kernel<1, 1><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(1, 1), s>>>(a);
-  else
-    chunk_state_kernel<4, 2><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(4, 2), s>>>(a);
+  chunk_state_kernel<4, 2><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(4, 2), s>>>(a);
   stage_timer_end(slot, s);
   return cudaGetLastError();
 }

@@ -49,9 +49,10 @@ typedef enum { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
 typedef struct CUstream_st* gdr_stream_t;
 
 /*
- * Workspace bytes gdr_chunk_fwd needs for these sizes (0 when the path needs none: float32).
- * The bfloat16 tensor-core path keeps per-chunk intermediates there (the WY factors of each
- * 64-token chunk). Returns 0 for invalid sizes.
+ * Workspace bytes gdr_chunk_fwd needs for these sizes (0 when the path needs none: float32, and
+ * rows of one chunk, L <= 64, which the bfloat16 path finishes in a single kernel). For longer
+ * rows the bfloat16 tensor-core path keeps per-chunk intermediates there (the factors M', N, Q',
+ * P U of each 64-token chunk). Returns 0 for invalid sizes.
  */
 size_t gdr_chunk_workspace_bytes(int B, int L, int Hk, int Hv, int D, gdr_dtype dt);
 
@@ -75,7 +76,8 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
                          int Hk, int Hv, int D, gdr_dtype dt, void* ws, size_t ws_bytes,
                          gdr_stream_t stream);
 
-/* Bytes of caller workspace gdr_fork_fwd needs for these sizes (0 for float32: no workspace). */
+/* Bytes of caller workspace gdr_fork_fwd needs for these sizes (0 for float32, and 0 for
+ * single-chunk forks, L_pad <= 64, which the tensor-core path finishes in one kernel). */
 size_t gdr_fork_workspace_bytes(int F, int L_pad, int Hk, int Hv, int D, gdr_dtype dt);
 
 /*

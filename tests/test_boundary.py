@@ -89,13 +89,18 @@ def test_fork_rejects_bad_arguments(L):
     # states_out overlapping the trunk is rejected
     assert fork(trunk=P, states=ctypes.c_void_p((1 << 20) + 1024)) == gdr.GDR_ERR_INVALID_ARG
     assert b"overlaps" in L.gdr_last_error_message()
-    # bf16 forks run on the tensor-core kernels and need the caller's workspace
-    need = L.gdr_fork_workspace_bytes(4, 64, 16, 32, 128, 1)
-    assert need == L.gdr_chunk_workspace_bytes(4, 64, 16, 32, 128, 1) > 0
-    assert L.gdr_fork_workspace_bytes(4, 64, 16, 32, 128, 0) == 0
-    assert fork(ws=None, ws_bytes=0) == gdr.GDR_ERR_INVALID_ARG
+    # bf16 forks run on the tensor-core kernels: single-chunk forks need no workspace, longer ones
+    # need the caller's
+    assert L.gdr_fork_workspace_bytes(4, 64, 16, 32, 128, 1) == 0
+    need = L.gdr_fork_workspace_bytes(4, 128, 16, 32, 128, 1)
+    assert need == L.gdr_chunk_workspace_bytes(4, 128, 16, 32, 128, 1) > 0
+    assert L.gdr_fork_workspace_bytes(4, 128, 16, 32, 128, 0) == 0
+
+    def fork128(ws, ws_bytes):
+        return L.gdr_fork_fwd(P, P, P, P, P, P, P, 1, P, None, 4, 128, 16, 32, 128, 1, ws, ws_bytes, None)
+    assert fork128(None, 0) == gdr.GDR_ERR_INVALID_ARG
     assert b"workspace" in L.gdr_last_error_message()
-    assert fork(ws_bytes=need - 1) == gdr.GDR_ERR_INVALID_ARG
+    assert fork128(P, need - 1) == gdr.GDR_ERR_INVALID_ARG
 
 
 def test_decode_rejects_bad_arguments(L):
