@@ -885,7 +885,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 //   warp 8: loads the output ring (Q', this CTA's P U slice) up to OS chunks ahead.
 // Per chunk c: chain stage c % CS (chFull / chFree: the state warps release it right after their
 // update), output stage c % OS (outFull / outFree: released by the output warps), state operand
-// q = c % 3 (sReady: S_c written; sFree: the output product has read it), TMEM buffers p = c % 2
+// q = c % kSb (sReady: S_c written; sFree: the output product has read it), TMEM buffers p = c % 2
 // (D[p]; O'[p] with bar_o: product done, oFree: the output warps have read it). Every barrier
 // completes once per CS, OS, 3 or 2 chunks and none can run two phases ahead of its waiters.
 constexpr int kStateThreads = 288;
@@ -895,12 +895,12 @@ constexpr uint32_t kCN = 32768;
 constexpr uint32_t kOStage = 20480;    // Q' (two 8 KB K-atoms), then this CTA's P U slice (4 KB)
 constexpr uint32_t kOPU = 16384;
 constexpr uint32_t kTmemState = 128;   // D[2] at 0, 32; O'[2] at 64, 96
-// Rings: 4 chain and 2 output stages for rows of several chunks; 1 and 1 for single-chunk rows
-// (forks), whose smaller footprint lets two CTAs share an SM. After the rings: three fp16 state
-// operands (MN-major, 128 rows of 64 B). The M = 128 output product reads 8 KB past each Q' tile
+// Rings: 3 chain and 3 output stages. After the rings: kSb fp16 state operands (MN-major, 128 rows
+// of 64 B). The M = 128 output product reads 8 KB past each Q' tile
 // (operand rows 64-127, whose products land in TMEM lanes nobody reads), which stays inside the
 // buffer because the state operands follow the output ring.
-constexpr uint32_t state_smem(int cs, int os) { return cs * kCStage + os * kOStage + 3 * 8192 + 1024; }
+constexpr int kSb = 5;                 // fp16 state operands: the output path may trail the chain by 4 chunks
+constexpr uint32_t state_smem(int cs, int os) { return cs * kCStage + os * kOStage + kSb * 8192 + 1024; }
 static_assert(kCN == kMBytes && kOPU == kQBytes, "stage layout");
 
 template <int CS, int OS>
@@ -910,8 +910,8 @@ chunk_state_kernel(const ChunkArgs a) {
   constexpr uint32_t kOffSb = kOffO + OS * kOStage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t chFull[CS], chFree[CS], outFull[OS], outFree[OS], bar_d, bar_o[2], oFree[2], sReady[3],
-      sFree[3];
+  __shared__ uint64_t chFull[CS], chFree[CS], outFull[OS], outFree[OS], bar_d, bar_o[2], oFree[2], sReady[kSb],
+      sFree[kSb];
   __shared__ __align__(16) float4 gam_ring[CS];   // Gamma_C of the chunk in each chain stage
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -934,7 +934,7 @@ chunk_state_kernel(const ChunkArgs a) {
       mbar_init(&bar_o[p], 1);
       mbar_init(&oFree[p], 1);
     }
-    for (int q = 0; q < 3; ++q) {
+    for (int q = 0; q < kSb; ++q) {
       mbar_init(&sReady[q], 1);
       mbar_init(&sFree[q], 1);
     }
@@ -1011,7 +1011,7 @@ chunk_state_kernel(const ChunkArgs a) {
     named_bar_and(kChainBar, kChainCount, true);
 
     for (int c = 0; c < NC; ++c) {
-      const int cs = c % CS, p = c & 1, q = c % 3, qn = (c + 1) % 3;
+      const int cs = c % CS, p = c & 1, q = c % kSb, qn = (c + 1) % kSb;
       uint8_t* st = sm + cs * kCStage;
       ok = mbar_wait(&chFull[cs], (c / CS) & 1, kWaitBudget) && !*(volatile int*)&abort_flag;
       if (tid == 0 && ok) {
@@ -1028,8 +1028,8 @@ chunk_state_kernel(const ChunkArgs a) {
         mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
       }
       ok = ok && mbar_wait(&bar_d, c & 1, kWaitBudget);
-      // Sb[qn] is rewritten below: the output product of chunk c - 2 must have read it
-      if (c >= 2) ok = ok && mbar_wait(&sFree[qn], ((c - 2) / 3) & 1, kWaitBudget);
+      // Sb[qn] is rewritten below: the output product of chunk c + 1 - kSb must have read it
+      if (c + 1 >= kSb) ok = ok && mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, kWaitBudget);
       if (ok) {
         tc_fence_after();
         float d[kN];
@@ -1062,9 +1062,9 @@ chunk_state_kernel(const ChunkArgs a) {
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, kN, false, true);
       for (int c = 0; c < NC; ++c) {
-        const int os = c % OS, p = c & 1, q = c % 3;
+        const int os = c % OS, p = c & 1, q = c % kSb;
         ok = mbar_wait(&outFull[os], (c / OS) & 1, kWaitBudget) &&
-             mbar_wait(&sReady[q], (c / 3) & 1, kWaitBudget) &&
+             mbar_wait(&sReady[q], (c / kSb) & 1, kWaitBudget) &&
              (c < 2 || mbar_wait(&oFree[p], ((c - 2) >> 1) & 1, kWaitBudget));
         if (!ok || *(volatile int*)&abort_flag) break;
         tc_fence_after();
@@ -1207,7 +1207,7 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
 
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(chunk_state_kernel<4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(4, 2));
+    e = cudaFuncSetAttribute(chunk_state_kernel<3, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(3, 3));
   if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkPrep);
   const long long units = (long long)a.B * a.Hv * a.NC;
@@ -1218,7 +1218,7 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (a.fused) return cudaSuccess;   // single-chunk rows are complete after kernel 1
   slot = stage_timer_begin(s, kKernChunkState);
-  chunk_state_kernel<4, 2><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(4, 2), s>>>(a);
+  chunk_state_kernel<3, 3><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(3, 3), s>>>(a);
   stage_timer_end(slot, s);
   return cudaGetLastError();
 }
