@@ -864,6 +864,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (tid == 0) bulk_wait_read();
   tc_fence_before();
   __syncthreads();
+  launch_dependents();   // the state kernel may start its set-up; it waits for this grid before reading
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tb, 256);
@@ -964,6 +965,7 @@ chunk_state_kernel(const ChunkArgs a) {
   } else if (warp == 6 || warp == 8) {
     // ---------------- producers (lane 0): the chain ring (warp 6) and the output ring (warp 8) ----
     if (lane == 0) {
+      wait_prerequisite();   // the workspace is complete once the prep kernel has finished
       const bool chain = warp == 6;
       const int S = chain ? CS : OS;
       for (int c = 0; c < NC; ++c) {
@@ -1218,8 +1220,21 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (a.fused) return cudaSuccess;   // single-chunk rows are complete after kernel 1
   slot = stage_timer_begin(s, kKernChunkState);
-  chunk_state_kernel<3, 3><<<dim3(kSlices, p.Hv, p.B), kStateThreads, state_smem(3, 3), s>>>(a);
+  // launched as a programmatic dependent of the prep kernel: its set-up (barriers, tensor memory,
+  // the initial state) overlaps the prep kernel's tail; its loads of the workspace wait for it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kSlices, p.Hv, p.B);
+  cfg.blockDim = dim3(kStateThreads, 1, 1);
+  cfg.dynamicSmemBytes = state_smem(3, 3);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3>, a);
   stage_timer_end(slot, s);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -128,6 +128,12 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch: the next kernel on the stream may start once every CTA of this
+// grid has called launch_dependents (or exited); that kernel's wait_prerequisite blocks until this
+// grid has completed and its memory writes are visible.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier `id` over `count` threads (a multiple of 32); returns the AND of `pred` over them.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool pred) {
   uint32_t r;
