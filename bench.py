@@ -9,12 +9,15 @@ Under torchrun each rank runs its own row on its own GPU (independent problems: 
 collective on the data path); rank 0 prints one JSON line with the max time over ranks.
 
 Timing: W untimed warm-up steps, then exactly K steps between CUDA events on the launch stream
-(barrier + synchronize on both sides). Inputs rotate over several resident copies whose total
-exceeds the 129 MB L2, so every step reads its inputs from HBM. Per-kernel times come from the
-library's stage timer (CUDA events recorded around each of its launches on the same stream).
+(barrier + synchronize on both sides), with nothing recorded between the launches. Inputs rotate
+over several resident copies whose total exceeds the 129 MB L2, so every step reads its inputs
+from HBM. Per-kernel times come from a second pass of the same K steps with the library's stage
+timer (CUDA events recorded around each of its launches on the same stream); those events keep the
+state kernel from starting before the prep kernel ends, so that pass is not the headline value.
 The e2e figure is the same step through the same call with host buffers: pinned host -> device
 copies of the inputs, the call, and device -> host copies of o and S_T, all inside its timed
-region.
+region. The "rows" object adds the fork pass and the decode step of the fork workload (256 forks
+of one trunk state), each with its own HBM roofline.
 
 --impl reference times the float64 CPU oracle (the checker the tests use) on a bounded sample of
 the same workload on the host cores, as the reference arm.
