@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -40,6 +41,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 std::mutex g_err_mu;
 int* g_err_ptr[128] = {};
+
+constexpr long long kDefaultWaitBudget = 2000000000ll;   // cycles, about 1 s
+std::atomic<long long> g_wait_budget{kDefaultWaitBudget};
 
 // Stage timer: one (start, end) event pair per recorded launch.
 struct StageTimer {
@@ -96,6 +100,8 @@ gdr_status launch_status(cudaError_t e, const char* who) {
 }
 
 }  // namespace
+
+long long wait_budget_cycles() { return g_wait_budget.load(); }
 
 int record_error(int status, const char* message) {
   t_msg = message;
@@ -249,6 +255,11 @@ const char* gdr_status_string(gdr_status s) {
 }
 
 const char* gdr_last_error_message(void) { return t_msg.c_str(); }
+
+gdr_status gdr_debug_set_wait_budget(long long cycles) {
+  g_wait_budget.store(cycles > 0 ? cycles : (cycles == 0 ? 0 : kDefaultWaitBudget));
+  return ok();
+}
 
 gdr_status gdr_stage_timer_enable(int on, int capacity) {
   std::lock_guard<std::mutex> lk(g_timer.mu);

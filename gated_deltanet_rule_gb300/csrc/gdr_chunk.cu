@@ -54,7 +54,7 @@ namespace {
 
 constexpr float kScale = 0.08838834764831845f;   // 128^-0.5
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr long long kWaitBudget = 2000000000ll;   // cycles (~1 s) before a wait gives up
+constexpr long long kDrainBudget = 2000000000ll;  // cycles (~1 s) an aborting CTA waits for its own copies
 constexpr int kSlices = 4;                        // value-column slices (state CTAs) per value head
 constexpr int kN = kD / kSlices;                  // 32 value columns per state CTA
 
@@ -76,6 +76,7 @@ struct ChunkArgs {
   const int64_t* S0_idx;   // row b starts from S0[S0_idx[b]] (forks); NULL = S0[b]
   int n_S0;                // states S0 holds when S0_idx is set
   int fused;               // single-chunk rows: kernel 1 applies the chunk to S0 itself
+  long long wait_budget;   // cycles before a wait gives up (GDR_ERR_TIMEOUT)
   __nv_bfloat16* o;
   float* S_T;
   uint8_t* ws;       // 1024-aligned
@@ -404,6 +405,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   bool ok = true;
   uint32_t mma_phase = 0;   // completions of bar_mma so far (4 per unit, 5 with the fused apply)
+  // a wait that gives up leaves its copy or product in flight: the parity it waited for is kept so
+  // that the CTA can drain it before exiting
+  int ld_fail = -1, mma_fail = -1;
+  auto wait_mma = [&]() -> bool {
+    const uint32_t par = mma_phase++ & 1;
+    const bool r = mbar_wait(&bar_mma, par, a.wait_budget);
+    if (!r) mma_fail = (int)par;
+    return r;
+  };
 
   for (int it = 0;; ++it) {
   int c, h, b;
@@ -435,7 +445,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     Gam[tid] = exp2f(gam * kLog2e);
   }
 
-  ok = mbar_wait(&bar_ld, it & 1, kWaitBudget);
+  ok = mbar_wait(&bar_ld, it & 1, a.wait_budget);
+  if (!ok) ld_fail = it & 1;
   if (!__syncthreads_and(ok)) break;
 
   // Gram MMA (bf16, exact products): D[0:128, 0:64] = [Q; K] K^T, issued by warp 7 while warps
@@ -496,7 +507,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     E2[I * 68 + j] *= kinv[j];
   }
   if (tid == 0) bulk_wait_read();   // the previous unit's N store has read the AT / Tm region
-  ok = mbar_wait(&bar_mma, mma_phase++ & 1, kWaitBudget);
+  ok = wait_mma();
   if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
@@ -614,7 +625,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mma_commit(&bar_mma);
   }
   if (un < total) tiles(un, false);   // the next unit's tiles into L2, while W and U are formed
-  ok = mbar_wait(&bar_mma, mma_phase++ & 1, kWaitBudget);
+  ok = wait_mma();
   if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
@@ -656,7 +667,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mma_bf16(tb, smem_desc(pa + kk * 32, 16, 1024), smem_desc(wu + kk * 2048, 8192, 1024), idesc, kk > 0);
     mma_commit(&bar_mma);
   }
-  ok = mbar_wait(&bar_mma, mma_phase++ & 1, kWaitBudget);
+  ok = wait_mma();
   if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
@@ -721,7 +732,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       bulk_commit();
     }
   }
-  ok = mbar_wait(&bar_mma, mma_phase++ & 1, kWaitBudget);
+  ok = wait_mma();
   if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
@@ -807,7 +818,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                        kk > 0);
       mma_commit(&bar_mma);
     }
-    ok = mbar_wait(&bar_mma, mma_phase++ & 1, kWaitBudget);
+    ok = wait_mma();
     if (!__syncthreads_and(ok)) break;
     tc_fence_after();
     if (write && a.S_T) {
@@ -860,7 +871,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tiles(u, true);
   }   // units
 
-  if (!ok && tid == 0) set_error(a.err, kErrTimeout);
+  if (!ok && tid == 0) {
+    set_error(a.err, kErrTimeout);
+    // drain what this CTA still has in flight before its shared and tensor memory are released
+    if (ld_fail >= 0) mbar_wait(&bar_ld, (uint32_t)ld_fail, kDrainBudget);
+    if (mma_fail >= 0) mbar_wait(&bar_mma, (uint32_t)mma_fail, kDrainBudget);
+  }
+  cp_async_wait<0>();
   if (tid == 0) bulk_wait_read();
   tc_fence_before();
   __syncthreads();
@@ -968,9 +985,10 @@ chunk_state_kernel(const ChunkArgs a) {
       wait_prerequisite();   // the workspace is complete once the prep kernel has finished
       const bool chain = warp == 6;
       const int S = chain ? CS : OS;
+      int last = -1;   // last chunk whose tiles were issued
       for (int c = 0; c < NC; ++c) {
         const int s = c % S;
-        if (c >= S) ok = mbar_wait(chain ? &chFree[s] : &outFree[s], ((c - S) / S) & 1, kWaitBudget);
+        if (c >= S) ok = mbar_wait(chain ? &chFree[s] : &outFree[s], ((c - S) / S) & 1, a.wait_budget);
         if (!ok || *(volatile int*)&abort_flag) break;
         const uint8_t* ub = unit_base(a, b, h, c);
         if (chain) {
@@ -986,6 +1004,12 @@ chunk_state_kernel(const ChunkArgs a) {
           bulk_load(st, ub + kUnitQ, kQBytes, &outFull[s]);
           bulk_load(st + kOPU, ub + kUnitPU + sl * 4096, 4096, &outFull[s]);
         }
+        last = c;
+      }
+      if (!ok) {
+        // drain: the tiles of the last S issued chunks land before the CTA's memory is released
+        for (int c = (last - S + 1 > 0 ? last - S + 1 : 0); c <= last; ++c)
+          mbar_wait(chain ? &chFull[c % S] : &outFull[c % S], (c / S) & 1, kDrainBudget);
       }
     }
   } else if (warp < 4) {
@@ -1012,10 +1036,11 @@ chunk_state_kernel(const ChunkArgs a) {
     fence_async_smem();
     named_bar_and(kChainBar, kChainCount, true);
 
+    int d_pend = -1;   // chunk whose state product thread 0 issued and has not seen complete
     for (int c = 0; c < NC; ++c) {
       const int cs = c % CS, p = c & 1, q = c % kSb, qn = (c + 1) % kSb;
       uint8_t* st = sm + cs * kCStage;
-      ok = mbar_wait(&chFull[cs], (c / CS) & 1, kWaitBudget) && !*(volatile int*)&abort_flag;
+      ok = mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
       if (tid == 0 && ok) {
         tc_fence_after();
         const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
@@ -1028,10 +1053,14 @@ chunk_state_kernel(const ChunkArgs a) {
                    smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
         mma_commit(&bar_d);
         mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
+        d_pend = c;
       }
-      ok = ok && mbar_wait(&bar_d, c & 1, kWaitBudget);
+      if (ok) {
+        ok = mbar_wait(&bar_d, c & 1, a.wait_budget);
+        if (ok) d_pend = -1;
+      }
       // Sb[qn] is rewritten below: the output product of chunk c + 1 - kSb must have read it
-      if (c + 1 >= kSb) ok = ok && mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, kWaitBudget);
+      if (c + 1 >= kSb) ok = ok && mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget);
       if (ok) {
         tc_fence_after();
         float d[kN];
@@ -1053,6 +1082,7 @@ chunk_state_kernel(const ChunkArgs a) {
       // the chain stage is free (D complete, N and Gamma_C read)
       if (tid == 0 && c + CS < NC) mbar_arrive(&chFree[cs]);
     }
+    if (!ok && d_pend >= 0) mbar_wait(&bar_d, d_pend & 1, kDrainBudget);   // drain the last product
     if (ok && a.S_T) {
       float* dst = a.S_T + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
 #pragma unroll
@@ -1063,11 +1093,12 @@ chunk_state_kernel(const ChunkArgs a) {
     // ---------------- output-product issuer ----------------
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, kN, false, true);
+      int last = -1;   // last chunk whose output product was issued
       for (int c = 0; c < NC; ++c) {
         const int os = c % OS, p = c & 1, q = c % kSb;
-        ok = mbar_wait(&outFull[os], (c / OS) & 1, kWaitBudget) &&
-             mbar_wait(&sReady[q], (c / kSb) & 1, kWaitBudget) &&
-             (c < 2 || mbar_wait(&oFree[p], ((c - 2) >> 1) & 1, kWaitBudget));
+        ok = mbar_wait(&outFull[os], (c / OS) & 1, a.wait_budget) &&
+             mbar_wait(&sReady[q], (c / kSb) & 1, a.wait_budget) &&
+             (c < 2 || mbar_wait(&oFree[p], ((c - 2) >> 1) & 1, a.wait_budget));
         if (!ok || *(volatile int*)&abort_flag) break;
         tc_fence_after();
         const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
@@ -1079,7 +1110,9 @@ chunk_state_kernel(const ChunkArgs a) {
                    smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
         mma_commit(&bar_o[p]);
         mma_commit(&sFree[q]);
+        last = c;
       }
+      if (!ok && last >= 0) mbar_wait(&bar_o[last & 1], (last >> 1) & 1, kDrainBudget);   // drain
     }
   } else {
     // ---------------- output warps 4, 5 ----------------
@@ -1087,8 +1120,8 @@ chunk_state_kernel(const ChunkArgs a) {
     for (int c = 0; c < NC; ++c) {
       const int os = c % OS, p = c & 1;
       const uint8_t* st = sm + kOffO + os * kOStage;
-      ok = mbar_wait(&outFull[os], (c / OS) & 1, kWaitBudget) &&
-           mbar_wait(&bar_o[p], (c >> 1) & 1, kWaitBudget) && !*(volatile int*)&abort_flag;
+      ok = mbar_wait(&outFull[os], (c / OS) & 1, a.wait_budget) &&
+           mbar_wait(&bar_o[p], (c >> 1) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
       if (ok) {
         tc_fence_after();
         float qs[kN];
@@ -1197,6 +1230,7 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   a.S0_idx = p.S0_idx;
   a.n_S0 = p.n_S0;
   a.fused = (p.L <= kChunk) ? 1 : 0;
+  a.wait_budget = wait_budget_cycles();
   a.o = static_cast<__nv_bfloat16*>(p.o);
   a.S_T = p.S_T;
   a.ws = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p.ws) + 1023) & ~uintptr_t(1023));

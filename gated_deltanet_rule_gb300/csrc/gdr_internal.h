@@ -64,6 +64,10 @@ struct ChunkLaunch {
 size_t chunk_workspace_bytes(int B, int Hk, int L, int Hv);
 cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s);
 
+// Cycles a kernel wait may take before it gives up with GDR_ERR_TIMEOUT (about 1 s by default;
+// gdr_debug_set_wait_budget changes it for later launches).
+long long wait_budget_cycles();
+
 // Record a one-line message for gdr_last_error_message() on this host thread; returns status.
 int record_error(int status, const char* message);
 

@@ -23,7 +23,7 @@ D = 128
 EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_noalloc", "gdr_fork_workspace_bytes",
            "gdr_fork_fwd", "gdr_decode_step",
            "gdr_sync_status", "gdr_status_string", "gdr_last_error_message",
-           "gdr_stage_timer_enable", "gdr_stage_timer_collect", "gdr_kernel_name"]
+           "gdr_stage_timer_enable", "gdr_stage_timer_collect", "gdr_kernel_name", "gdr_debug_set_wait_budget"]
 
 
 class GdrError(RuntimeError):
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
     L.gdr_stage_timer_enable.restype = i
     L.gdr_stage_timer_collect.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int), i]
     L.gdr_stage_timer_collect.restype = i
+    L.gdr_debug_set_wait_budget.argtypes = [ctypes.c_longlong]
+    L.gdr_debug_set_wait_budget.restype = i
     L.gdr_kernel_name.argtypes = [i]
     L.gdr_kernel_name.restype = ctypes.c_char_p
     _lib = L
@@ -197,6 +199,11 @@ def kernel_names() -> list[str]:
             return names
         names.append(n.decode())
         i += 1
+
+
+def debug_set_wait_budget(cycles: int) -> None:
+    """Testing aid: cycles a kernel wait may take before it gives up (0: at once; < 0: default)."""
+    _check(lib().gdr_debug_set_wait_budget(int(cycles)))
 
 
 def stage_timer_enable(on: bool = True, capacity: int = 8192) -> None:

@@ -141,6 +141,16 @@ gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
 /* Synchronise `stream`, then read and clear the sticky device error word of the current device. */
 gdr_status gdr_sync_status(gdr_stream_t stream);
 
+/*
+ * Testing aid (failure detection): the SM clock cycles a kernel wait may take before the kernel
+ * gives up, records GDR_ERR_TIMEOUT in the device error word, waits (again bounded) for its own
+ * copies and products still in flight, frees its tensor memory and exits. Default about 2e9
+ * cycles (roughly 1 s); 0 makes every wait that is not already satisfied give up at once; a
+ * negative value restores the default. Applies to launches made after the call; results of a call
+ * that timed out are undefined, and the next call runs normally.
+ */
+gdr_status gdr_debug_set_wait_budget(long long cycles);
+
 /* Static strings; never NULL. */
 const char* gdr_status_string(gdr_status status);
 const char* gdr_last_error_message(void);

@@ -196,6 +196,27 @@ def test_decode_steps_match_oracle_and_idle_rows_are_unchanged():
     assert_close(st_dev, ref, TOL_BF16, "decode states")
 
 
+def test_forced_wait_timeout_reports_and_the_next_call_recovers():
+    """Failure detection without a fault: with a wait budget of 0 the kernels give up at their
+    first unsatisfied wait, drain their own copies in flight and report GDR_ERR_TIMEOUT through the
+    device error word; with the budget restored the same call is correct again."""
+    x = inputs.regime("R1", 256, 61, Hk=2, Hv=4, init_state=True, dtype=torch.bfloat16)
+    args = [dev(t) for t in (x.q, x.k, x.v, x.g, x.beta, x.S0)]
+    gdr.debug_set_wait_budget(0)
+    try:
+        gdr.gdr_chunk_fwd(*args)
+        with pytest.raises(gdr.GdrError) as ei:
+            gdr.gdr_sync_status()
+        assert ei.value.status == gdr.GDR_ERR_TIMEOUT
+    finally:
+        gdr.debug_set_wait_budget(-1)
+    o, S = gdr.gdr_chunk_fwd(*args)
+    gdr.gdr_sync_status()
+    ro, rS = ref_chunk(x)
+    assert_close(o, ro, TOL_BF16, "o after recovery")
+    assert_close(S, rS, TOL_BF16, "S_T after recovery")
+
+
 # ------------------------------------------------------------------------------------------------
 # the full-size workloads, in the launch configuration the benchmark times
 # ------------------------------------------------------------------------------------------------
