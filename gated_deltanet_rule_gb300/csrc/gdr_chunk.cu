@@ -636,21 +636,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int row = 32 * (warp & 3) + lane, i = row & 63, cb = (warp >> 2) * 64;
     const bool isU = row >= 64;
     const float sk = skv[i];
+    float w[64];
+    tmem_ld64(tb + lane_base + (isU ? 128 : 0) + cb, w);
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      float w[32];
-      tmem_ld32(tb + lane_base + (isU ? 128 : 0) + cb + part * 32, w);
+    for (int q8 = 0; q8 < 8; ++q8) {
+      const int col = cb + q8 * 8;
+      const int atom = col >> 6, ch = (col & 63) >> 3;
+      const uint32_t off = (isU ? 16384 : 0) + atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4);
+      float ws[8];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int col = cb + part * 32 + q4 * 8;
-        const int atom = col >> 6, ch = (col & 63) >> 3;
-        const uint32_t off = (isU ? 16384 : 0) + atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4);
-        float ws[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ws[e] = sk * w[q4 * 8 + e];
-        *reinterpret_cast<uint4*>(sm + kPV + off) = pack8_f16(w + q4 * 8);
-        *reinterpret_cast<uint4*>(sm + kPWS + off) = pack8_f16(ws);
-      }
+      for (int e = 0; e < 8; ++e) ws[e] = sk * w[q8 * 8 + e];
+      *reinterpret_cast<uint4*>(sm + kPV + off) = pack8_f16(w + q8 * 8);
+      *reinterpret_cast<uint4*>(sm + kPWS + off) = pack8_f16(ws);
     }
   }
   fence_async_smem();
@@ -676,13 +673,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // slices) on columns cb .. cb + 63, staged over the consumed [W | U] operand
     const int i = 32 * (warp & 3) + lane, cb = (warp >> 2) * 64;
     const float sq = Gam[i] * qinv[i] * kScale;
+    {
+      float w[64];
+      tmem_ld64(tb + lane_base + cb, w);
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      float w[32];
-      tmem_ld32(tb + lane_base + cb + part * 32, w);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int col = cb + part * 32 + q4 * 8;
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const int col = cb + q8 * 8;
         const int atom = col >> 6, ch = (col & 63) >> 3;
         const uint32_t off = atom * 8192 + i * 128 + ((ch ^ (i & 7)) << 4);
         const uint4 qr = *reinterpret_cast<const uint4*>(sm + (atom ? kPQ1 : kPQ0) + i * 128 + ((ch ^ (i & 7)) << 4));
@@ -690,21 +686,21 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float v[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          v[2 * e] = sq * __uint_as_float(q4w[e] << 16) - w[q4 * 8 + 2 * e];
-          v[2 * e + 1] = sq * __uint_as_float(q4w[e] & 0xFFFF0000u) - w[q4 * 8 + 2 * e + 1];
+          v[2 * e] = sq * __uint_as_float(q4w[e] << 16) - w[q8 * 8 + 2 * e];
+          v[2 * e + 1] = sq * __uint_as_float(q4w[e] & 0xFFFF0000u) - w[q8 * 8 + 2 * e + 1];
         }
         *reinterpret_cast<uint4*>(sm + kPV + off) = pack8_f16(v);
       }
     }
+    {
+      float u[64];
+      tmem_ld64(tb + lane_base + 128 + cb, u);
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      float u[32];
-      tmem_ld32(tb + lane_base + 128 + cb + part * 32, u);
-      const int col = cb + part * 32;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
-        *reinterpret_cast<uint4*>(sm + kPV + 16384 + (col >> 5) * 4096 + swz64(i * 64 + q4 * 16)) =
-            pack8_f16(u + q4 * 8);
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const int col = cb + q8 * 8;
+        *reinterpret_cast<uint4*>(sm + kPV + 16384 + (col >> 5) * 4096 + swz64(i * 64 + (q8 & 3) * 16)) =
+            pack8_f16(u + q8 * 8);
+      }
     }
   } else if (tid == 64) {
     // Gamma_C, staged over P (consumed)
@@ -741,27 +737,27 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // image over q and k, consumed) and of N = D[:, 128:256] (fp16 slices over [sk W | sk U]),
     // staged for bulk stores (per-thread 16-byte global stores of these row layouts are far slower)
     const int i = 32 * (warp & 3) + lane, cb = (warp >> 2) * 64;
+    {
+      float w[64];
+      tmem_ld64(tb + lane_base + cb, w);
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      float w[32];
-      tmem_ld32(tb + lane_base + cb + part * 32, w);
+      for (int e = 0; e < 64; ++e) w[e] = -w[e];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) w[e] = -w[e];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int col = cb + part * 32 + q4 * 8;
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const int col = cb + q8 * 8;
         const int atom = col >> 6, ch = (col & 63) >> 3;
-        *reinterpret_cast<uint4*>(sm + kPM + atom * 16384 + i * 128 + ((ch ^ (i & 7)) << 4)) = pack8_f16(w + q4 * 8);
+        *reinterpret_cast<uint4*>(sm + kPM + atom * 16384 + i * 128 + ((ch ^ (i & 7)) << 4)) = pack8_f16(w + q8 * 8);
       }
     }
+    {
+      float n[64];
+      tmem_ld64(tb + lane_base + 128 + cb, n);
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      float n[32];
-      tmem_ld32(tb + lane_base + 128 + cb + part * 32, n);
-      const int col = cb + part * 32;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
-        *reinterpret_cast<uint4*>(sm + kPWS + (col >> 5) * 8192 + swz64(i * 64 + q4 * 16)) = pack8_f16(n + q4 * 8);
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const int col = cb + q8 * 8;
+        *reinterpret_cast<uint4*>(sm + kPWS + (col >> 5) * 8192 + swz64(i * 64 + (q8 & 3) * 16)) =
+            pack8_f16(n + q8 * 8);
+      }
     }
   }
   fence_async_smem();
