@@ -142,44 +142,44 @@ static_assert(kPWS % 1024 == 0 && kPWS + 32768 <= kPVec, "the [sk W | sk U] oper
 // contiguous float4 runs, and skip the blocks that are zero by triangularity.
 __device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
-  // 1. diagonal 16-blocks, one warp each (warps 0-3): lane = (row i, column half hf), holding
-  //    T(i, 8 hf .. 8 hf + 7) of its block in registers and row i of A in registers. Forward
-  //    substitution by rows: when row j is final its values are broadcast by shuffle and every
-  //    row i > j subtracts A_ij T_j (A_ij is taken as 0 for j >= i).
-  if (warp < 4) {
-    const int r0 = 16 * warp, i = lane & 15, hf = lane >> 4;
-    float av[16];
-    const float4* arow = reinterpret_cast<const float4*>(AT + (r0 + i) * 68 + r0);
+  // 1. diagonal 16-blocks (warps 0, 1): thread = (block, column c), computing column c of the
+  //    block's inverse in registers, left-looking: x_i = -sum_{j < i} A_ij x_j for rows i > c (x_c = 1,
+  //    x_j = 0 above it). Each row of A is read as four float4 broadcasts; no shuffles.
+  if (warp < 2) {
+    const int r0 = (tid >> 4) * 16, c = tid & 15;
+    float x[16];
 #pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4) {
-      const float4 t = arow[m4];
-      av[4 * m4] = t.x; av[4 * m4 + 1] = t.y; av[4 * m4 + 2] = t.z; av[4 * m4 + 3] = t.w;
-    }
+    for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) av[j] = (j < i) ? av[j] : 0.f;
-    float t[8];
+    for (int i = 1; i < 16; ++i) {
+      const float4* arow = reinterpret_cast<const float4*>(AT + (r0 + i) * 68 + r0);
+      float av[16];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) t[e] = (8 * hf + e == i) ? 1.f : 0.f;
-#pragma unroll
-    for (int j = 0; j < 15; ++j) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float tj = __shfl_sync(0xffffffffu, t[e], j + 16 * hf);
-        t[e] = fmaf(-av[j], tj, t[e]);
+      for (int m4 = 0; m4 < 4; ++m4) {
+        if (4 * m4 < i) {
+          const float4 t = arow[m4];
+          av[4 * m4] = t.x; av[4 * m4 + 1] = t.y; av[4 * m4 + 2] = t.z; av[4 * m4 + 3] = t.w;
+        }
       }
-    }
-    __syncwarp();
-    // Tm row i (its diagonal 1 and zero upper part included); AT row c (block columns) becomes
-    // column c of T: 0 above the diagonal of T (the consumed A entries), 1 on it, T(i, c) below
-    float4* trow = reinterpret_cast<float4*>(Tm + (r0 + i) * 68 + r0 + 8 * hf);
-    trow[0] = make_float4(t[0], t[1], t[2], t[3]);
-    trow[1] = make_float4(t[4], t[5], t[6], t[7]);
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int c = 8 * hf + e;
-      AT[(r0 + c) * 68 + r0 + i] = (i > c) ? t[e] : (i == c ? 1.f : 0.f);
+      for (int j = 0; j < i; ++j) {
+        if (j & 1) s1 = fmaf(av[j], x[j], s1);
+        else s0 = fmaf(av[j], x[j], s0);
+      }
+      x[i] = (i > c) ? -(s0 + s1) : x[i];
     }
-  } else {
+    __syncwarp();   // every lane of the block has read A's rows before row c of AT is overwritten
+    // column c of T: Tm rows below the diagonal (its diagonal 1 and upper zeros are in place), and
+    // AT row c over the block's columns: 0 above the diagonal of T (the consumed A), 1 on it, T below
+#pragma unroll
+    for (int i = 1; i < 16; ++i)
+      if (i > c) Tm[(r0 + i) * 68 + r0 + c] = x[i];
+    float4* trow = reinterpret_cast<float4*>(AT + (r0 + c) * 68 + r0);
+#pragma unroll
+    for (int m4 = 0; m4 < 4; ++m4)
+      trow[m4] = make_float4(x[4 * m4], x[4 * m4 + 1], x[4 * m4 + 2], x[4 * m4 + 3]);
+  } else if (warp >= 4) {
     // warps 4-7 meanwhile: the k and v tiles to fp16 in place, for the fp16 products (the Gram MMA
     // that read k as bf16 has completed); 2048 chunks of 16 B, k atoms then v atoms
     const int t = tid - 128;
