@@ -1052,6 +1052,16 @@ chunk_state_kernel(const ChunkArgs a) {
         d_pend = c;
       }
       if (ok) {
+        // while the product runs: S <- Gamma_C S + N (S_c itself is already in the fp16 operand)
+        const float gc = gam_ring[cs].x;
+        const uint8_t* nrow = st + kCN;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          float nv[8];
+          unpack8_f16(*reinterpret_cast<const uint4*>(nrow + swz64(kr * 64 + ch * 16)), nv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], nv[e]);
+        }
         ok = mbar_wait(&bar_d, c & 1, a.wait_budget);
         if (ok) d_pend = -1;
       }
@@ -1061,15 +1071,8 @@ chunk_state_kernel(const ChunkArgs a) {
         tc_fence_after();
         float d[kN];
         tmem_ld32(tb + lane_base + 32 * p, d);
-        const float gc = gam_ring[cs].x;
-        const uint8_t* nrow = st + kCN;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float nv[8];
-          unpack8_f16(*reinterpret_cast<const uint4*>(nrow + swz64(kr * 64 + ch * 16)), nv);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], d[8 * ch + e] + nv[e]);
-        }
+        for (int n = 0; n < kN; ++n) Sm[n] += d[n];
         write_state_operand(qn);
       }
       fence_async_smem();
