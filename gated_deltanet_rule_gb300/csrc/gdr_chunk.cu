@@ -908,7 +908,7 @@ constexpr uint32_t kCStage = 40960;    // M' (two 16 KB K-atoms), then this CTA'
 constexpr uint32_t kCN = 32768;
 constexpr uint32_t kOStage = 20480;    // Q' (two 8 KB K-atoms), then this CTA's P U slice (4 KB)
 constexpr uint32_t kOPU = 16384;
-constexpr uint32_t kTmemState = 128;   // D[2] at 0, 32; O'[2] at 64, 96
+constexpr uint32_t kTmemState = 256;   // D[2] at 0, 64 (two 32-column K halves each); O'[2] at 128, 160
 // Rings: 3 chain and 3 output stages. After the rings: kSb fp16 state operands (MN-major, 128 rows
 // of 64 B). The M = 128 output product reads 8 KB past each Q' tile
 // (operand rows 64-127, whose products land in TMEM lanes nobody reads), which stays inside the
@@ -924,7 +924,7 @@ chunk_state_kernel(const ChunkArgs a) {
   constexpr uint32_t kOffSb = kOffO + OS * kOStage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t chFull[CS], chFree[CS], outFull[OS], outFree[OS], bar_d, bar_o[2], oFree[2], sReady[kSb],
+  __shared__ uint64_t chFull[CS], chFree[CS], outFull[OS], outFree[OS], bar_d[2], bar_o[2], oFree[2], sReady[kSb],
       sFree[kSb];
   __shared__ __align__(16) float4 gam_ring[CS];   // Gamma_C of the chunk in each chain stage
   __shared__ uint32_t tmem_base;
@@ -943,7 +943,8 @@ chunk_state_kernel(const ChunkArgs a) {
       mbar_init(&outFull[s], 1);
       mbar_init(&outFree[s], 1);
     }
-    mbar_init(&bar_d, 1);
+    mbar_init(&bar_d[0], 1);
+    mbar_init(&bar_d[1], 1);
     for (int p = 0; p < 2; ++p) {
       mbar_init(&bar_o[p], 1);
       mbar_init(&oFree[p], 1);
@@ -1032,23 +1033,28 @@ chunk_state_kernel(const ChunkArgs a) {
     fence_async_smem();
     named_bar_and(kChainBar, kChainCount, true);
 
-    int d_pend = -1;   // chunk whose state product thread 0 issued and has not seen complete
+    int d_pend = -1;   // chunk whose half product this thread issued and has not seen complete
+    const bool issuer = tid == 0 || tid == 32;
+    const int kh = tid >> 5;   // for the issuers: which K half of the product (key rows 64 kh ..)
     for (int c = 0; c < NC; ++c) {
       const int cs = c % CS, p = c & 1, q = c % kSb, qn = (c + 1) % kSb;
       uint8_t* st = sm + cs * kCStage;
       ok = mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
-      if (tid == 0 && ok) {
+      if (issuer && ok) {
         tc_fence_after();
         const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
         const uint32_t idesc = idesc_f16(128, kN, false, true);
         const uint32_t sm_m = smem_u32(st);
-        // D[p] = M' S   (the critical product)
+        // D[p] half kh = M'[:, 64 kh ..] S[64 kh .., :]: the critical product, its two K halves
+        // issued by two threads into two accumulators
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tb + 32 * p, smem_desc(sm_m + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                   smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
-        mma_commit(&bar_d);
-        mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = 4 * kh + k4;
+          mma_bf16(tb + 64 * p + 32 * kh, smem_desc(sm_m + kh * 16384 + k4 * 32, 16, 1024),
+                   smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, k4 > 0);
+        }
+        mma_commit(&bar_d[kh]);
+        if (kh == 0) mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
         d_pend = c;
       }
       if (ok) {
@@ -1062,17 +1068,17 @@ chunk_state_kernel(const ChunkArgs a) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], nv[e]);
         }
-        ok = mbar_wait(&bar_d, c & 1, a.wait_budget);
+        ok = mbar_wait(&bar_d[0], c & 1, a.wait_budget) && mbar_wait(&bar_d[1], c & 1, a.wait_budget);
         if (ok) d_pend = -1;
       }
       // Sb[qn] is rewritten below: the output product of chunk c + 1 - kSb must have read it
       if (c + 1 >= kSb) ok = ok && mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget);
       if (ok) {
         tc_fence_after();
-        float d[kN];
-        tmem_ld32(tb + lane_base + 32 * p, d);
+        float d[2 * kN];
+        tmem_ld64(tb + lane_base + 64 * p, d);
 #pragma unroll
-        for (int n = 0; n < kN; ++n) Sm[n] += d[n];
+        for (int n = 0; n < kN; ++n) Sm[n] += d[n] + d[kN + n];
         write_state_operand(qn);
       }
       fence_async_smem();
@@ -1081,7 +1087,7 @@ chunk_state_kernel(const ChunkArgs a) {
       // the chain stage is free (D complete, N and Gamma_C read)
       if (tid == 0 && c + CS < NC) mbar_arrive(&chFree[cs]);
     }
-    if (!ok && d_pend >= 0) mbar_wait(&bar_d, d_pend & 1, kDrainBudget);   // drain the last product
+    if (!ok && d_pend >= 0) mbar_wait(&bar_d[kh], d_pend & 1, kDrainBudget);   // drain the last product
     if (ok && a.S_T) {
       float* dst = a.S_T + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
 #pragma unroll
@@ -1105,7 +1111,7 @@ chunk_state_kernel(const ChunkArgs a) {
         // O'[p] = Q' S  (M = 128; operand rows 64-127 run past the tile and are not read)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tb + 64 + 32 * p, smem_desc(sm_q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+          mma_bf16(tb + 128 + 32 * p, smem_desc(sm_q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
                    smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
         mma_commit(&bar_o[p]);
         mma_commit(&sFree[q]);
@@ -1124,7 +1130,7 @@ chunk_state_kernel(const ChunkArgs a) {
       if (ok) {
         tc_fence_after();
         float qs[kN];
-        tmem_ld32(tb + lane_base + 64 + 32 * p, qs);
+        tmem_ld32(tb + lane_base + 128 + 32 * p, qs);
         const int pos = c * 64 + i;
         if (pos < a.L) {
           float pu[kN];
