@@ -116,8 +116,10 @@ constexpr uint32_t kPQ0 = 0, kPK0 = 8192, kPQ1 = 16384, kPK1 = 24576;   // [q|k]
 constexpr uint32_t kPV = 32768;       // v atoms; then the MN-major operand [W0 | W1 | U0 | U1]; then
                                       // the staged Q' image and P U slices
 constexpr uint32_t kPXs = 49152;      // inverse scratch (free until U is written there)
-// P: K-major fp16 rows 0-63. The P [W | U] MMA has M = 128 and also reads operand rows 64-127 (the
-// 8 KB after P, here the start of AT): their products land in TMEM lanes 64-127, which nobody reads.
+// P: K-major fp16 rows 0-63. The P [W | U] products have M = 128: P W reads operand rows from P on
+// (P in rows 0-63, lanes 0-63) and P U from 8 KB before P (P in rows 64-127, lanes 64-127), so that
+// the epilogue spreads over all eight warps; the other operand rows (the tail of the [W | U]
+// operand, the start of AT) yield products in lanes that nobody reads.
 constexpr uint32_t kPP = 65536;
 constexpr uint32_t kPAT = kPP + 8192;           // fp32 [64][68]: A strictly lower, 1 on the diagonal, T^T strictly upper
 constexpr uint32_t kPTm = kPAT + 64 * 68 * 4;   // fp32 [64][68]: T row-major (zero above the diagonal)
@@ -179,13 +181,10 @@ __device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, 
 #pragma unroll
     for (int m4 = 0; m4 < 4; ++m4)
       trow[m4] = make_float4(x[4 * m4], x[4 * m4 + 1], x[4 * m4 + 2], x[4 * m4 + 3]);
-  } else if (warp >= 4) {
-    // warps 4-7 meanwhile: the k and v tiles to fp16 in place, for the fp16 products (the Gram MMA
+  } else {
+    // warps 2-7 meanwhile: the k and v tiles to fp16 in place, for the fp16 products (the Gram MMA
     // that read k as bf16 has completed); 2048 chunks of 16 B, k atoms then v atoms
-    const int t = tid - 128;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int chunk16 = n * 128 + t;
+    for (int chunk16 = tid - 64; chunk16 < 2048; chunk16 += kPrepThreads - 64) {
       const int which = chunk16 >> 9, off = (chunk16 & 511) * 16;
       const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPV + (which - 2) * 8192);
       uint4* p = reinterpret_cast<uint4*>(sm + base + off);
@@ -195,122 +194,93 @@ __device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, 
     }
   }
   __syncthreads();
-  // 2. 16-block merges p = 0, 1 (TL = [32p, 32p+16), BR = [32p+16, 32p+32)). Lane: (p, row i);
-  //    warp: columns 2w, 2w+1.
-  {
-    const int p = lane >> 4, i = lane & 15, base = 32 * p;
-    float ar[16];
-    const float4* arow = reinterpret_cast<const float4*>(AT + (base + 16 + i) * 68 + base);
+  // 2. 16-block merges p = 0, 1 (TL = [32p, 32p+16), BR = [32p+16, 32p+32)) with the same warp-level
+  //    products: warp w < 4 forms the 16 x 8 tile (merge p = w >> 1, columns 8 (w & 1)) of
+  //    X = A_BL T_TL (stored transposed, Xs[p][j][i]) and then of T_BL = -T_BR X (into Tm and AT).
+  if (warp < 4) {
+    const int g = lane >> 2, t = lane & 3, p = warp >> 1, n = warp & 1, base = 32 * p;
+    float dh[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4) {
-      const float4 t = arow[m4];
-      ar[4 * m4] = t.x; ar[4 * m4 + 1] = t.y; ar[4 * m4 + 2] = t.z; ar[4 * m4 + 3] = t.w;
+    for (int kk = 0; kk < 2; ++kk) {
+      if (kk < n) continue;
+      const float* ar = AT + (base + 16 + g) * 68 + base + 8 * kk + t;   // A_BL(i, k)
+      const float* br = AT + (base + 8 * n + g) * 68 + base + 8 * kk + t;   // T_TL(k, j) = AT[j][k]
+      const float a4[4] = {ar[0], ar[8 * 68], ar[4], ar[8 * 68 + 4]};
+      const float b2[2] = {br[0], br[4]};
+      mma_3xtf32(dh, dc, a4, b2);
     }
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int j = 2 * warp + q;
-      const float4* tcol = reinterpret_cast<const float4*>(AT + (base + j) * 68 + base);   // column j of T_TL
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-      for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 t = tcol[m4];
-        acc0 = fmaf(ar[4 * m4], t.x, acc0);
-        acc1 = fmaf(ar[4 * m4 + 1], t.y, acc1);
-        acc0 = fmaf(ar[4 * m4 + 2], t.z, acc0);
-        acc1 = fmaf(ar[4 * m4 + 3], t.w, acc1);
-      }
-      Xs[(p * 16 + j) * 20 + i] = acc0 + acc1;    // X column-major
-    }
-    __syncthreads();
-    if (warp < 4)   // A_BL consumed
+    const int j0 = 8 * n + 2 * t;
+    Xs[(p * 16 + j0) * 20 + g] = dh[0] + dc[0];
+    Xs[(p * 16 + j0 + 1) * 20 + g] = dh[1] + dc[1];
+    Xs[(p * 16 + j0) * 20 + g + 8] = dh[2] + dc[2];
+    Xs[(p * 16 + j0 + 1) * 20 + g + 8] = dh[3] + dc[3];
+  }
+  __syncthreads();
+  if (warp < 4) {
+    {   // A_BL consumed: a row of AT restricted to a finished 32-block is then exactly a column of T
+      const int p = lane >> 4, i = lane & 15, base = 32 * p;
       reinterpret_cast<float4*>(AT + (base + 16 + i) * 68 + base)[warp] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float tr[16];
-    const float4* trow = reinterpret_cast<const float4*>(Tm + (base + 16 + i) * 68 + base + 16);
-#pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4) {
-      const float4 t = trow[m4];
-      tr[4 * m4] = t.x; tr[4 * m4 + 1] = t.y; tr[4 * m4 + 2] = t.z; tr[4 * m4 + 3] = t.w;
     }
+    const int g = lane >> 2, t = lane & 3, p = warp >> 1, n = warp & 1, base = 32 * p;
+    float dh[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int j = 2 * warp + q;
-      const float4* xcol = reinterpret_cast<const float4*>(Xs + (p * 16 + j) * 20);
-      float acc0 = 0.f, acc1 = 0.f;
+    for (int kk = 0; kk < 2; ++kk) {
+      const float* ar = Tm + (base + 16 + g) * 68 + base + 16 + 8 * kk + t;   // T_BR(i, k), row-major
+      const float* br = Xs + (p * 16 + 8 * n + g) * 20 + 8 * kk + t;         // X(k, j) = Xs[p][j][k]
+      const float a4[4] = {ar[0], ar[8 * 68], ar[4], ar[8 * 68 + 4]};
+      const float b2[2] = {br[0], br[4]};
+      mma_3xtf32(dh, dc, a4, b2);
+    }
+    const int j0 = 8 * n + 2 * t;
+    const float r[4] = {-(dh[0] + dc[0]), -(dh[1] + dc[1]), -(dh[2] + dc[2]), -(dh[3] + dc[3])};
 #pragma unroll
-      for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 t = xcol[m4];
-        acc0 = fmaf(tr[4 * m4], t.x, acc0);
-        acc1 = fmaf(tr[4 * m4 + 1], t.y, acc1);
-        acc0 = fmaf(tr[4 * m4 + 2], t.z, acc0);
-        acc1 = fmaf(tr[4 * m4 + 3], t.w, acc1);
-      }
-      Tm[(base + 16 + i) * 68 + base + j] = -(acc0 + acc1);
-      AT[(base + j) * 68 + base + 16 + i] = -(acc0 + acc1);
+    for (int e = 0; e < 4; ++e) {
+      const int i = base + 16 + g + 8 * (e >> 1), j = base + j0 + (e & 1);
+      Tm[i * 68 + j] = r[e];
+      AT[j * 68 + i] = r[e];
     }
   }
   __syncthreads();
-  // 3. 32-block merge. X = A_BL T_TL: lane = row i, warp = columns 4w .. 4w + 3; columns >= 16
-  //    only meet rows >= 16 of T_TL.
+  // 3. 32-block merge on the tensor cores with warp-level products at fp32 accuracy (3xTF32): warp w
+  //    forms the 16 x 8 tile (rows 16 (w & 1), columns 8 (w >> 1)) of X = A_BL T_TL, stored
+  //    transposed (Xs[j][i]), then of T_BL = -T_BR X into AT's upper part. Zero blocks of the
+  //    triangular factors are skipped (T_TL: k-blocks below the column block; T_BR: above the row block).
   {
-    const int i = lane;
-    float ar[32];
-    const float4* arow = reinterpret_cast<const float4*>(AT + (32 + i) * 68);
+    const int g = lane >> 2, t = lane & 3, m = warp & 1, n = warp >> 1;
+    float dh[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int m4 = 0; m4 < 8; ++m4) {
-      const float4 t = arow[m4];
-      ar[4 * m4] = t.x; ar[4 * m4 + 1] = t.y; ar[4 * m4 + 2] = t.z; ar[4 * m4 + 3] = t.w;
+    for (int kk = 0; kk < 4; ++kk) {
+      if (kk < n) continue;
+      const float* ar = AT + (32 + 16 * m + g) * 68 + 8 * kk + t;   // A_BL(i, k) = A(32 + i, k)
+      const float* br = AT + (8 * n + g) * 68 + 8 * kk + t;          // T_TL(k, j) = AT[j][k]
+      const float a4[4] = {ar[0], ar[8 * 68], ar[4], ar[8 * 68 + 4]};
+      const float b2[2] = {br[0], br[4]};
+      mma_3xtf32(dh, dc, a4, b2);
     }
-    auto prod1 = [&](const int m4lo) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int j = 4 * warp + q;
-        const float4* tcol = reinterpret_cast<const float4*>(AT + j * 68);
-        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-        for (int m4 = m4lo; m4 < 8; ++m4) {
-          const float4 t = tcol[m4];
-          acc0 = fmaf(ar[4 * m4], t.x, acc0);
-          acc1 = fmaf(ar[4 * m4 + 1], t.y, acc1);
-          acc0 = fmaf(ar[4 * m4 + 2], t.z, acc0);
-          acc1 = fmaf(ar[4 * m4 + 3], t.w, acc1);
-        }
-        Xs[j * 36 + i] = acc0 + acc1;
-      }
-    };
-    if (warp >= 4) prod1(4);
-    else prod1(0);
+    const int i0 = 16 * m + g, j0 = 8 * n + 2 * t;
+    Xs[j0 * 36 + i0] = dh[0] + dc[0];
+    Xs[(j0 + 1) * 36 + i0] = dh[1] + dc[1];
+    Xs[j0 * 36 + i0 + 8] = dh[2] + dc[2];
+    Xs[(j0 + 1) * 36 + i0 + 8] = dh[3] + dc[3];
   }
   __syncthreads();
-  // T_BL = -T_BR X: warp = rows 4w .. 4w + 3 of the bottom block, lane = column j; rows < 16 only
-  // meet columns < 16 of T_BR.
   {
-    const int j = lane;
-    auto prod2 = [&](const int m4hi) {
-      float xc[32];
-      const float4* xcol = reinterpret_cast<const float4*>(Xs + j * 36);
+    const int g = lane >> 2, t = lane & 3, m = warp & 1, n = warp >> 1;
+    float dh[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int m4 = 0; m4 < m4hi; ++m4) {
-        const float4 t = xcol[m4];
-        xc[4 * m4] = t.x; xc[4 * m4 + 1] = t.y; xc[4 * m4 + 2] = t.z; xc[4 * m4 + 3] = t.w;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = 4 * warp + q;
-        const float4* trow = reinterpret_cast<const float4*>(Tm + (32 + i) * 68 + 32);
-        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-        for (int m4 = 0; m4 < m4hi; ++m4) {
-          const float4 t = trow[m4];
-          acc0 = fmaf(t.x, xc[4 * m4], acc0);
-          acc1 = fmaf(t.y, xc[4 * m4 + 1], acc1);
-          acc0 = fmaf(t.z, xc[4 * m4 + 2], acc0);
-          acc1 = fmaf(t.w, xc[4 * m4 + 3], acc1);
-        }
-        AT[j * 68 + 32 + i] = -(acc0 + acc1);
-      }
-    };
-    if (warp >= 4) prod2(8);
-    else prod2(4);
+    for (int kk = 0; kk < 4; ++kk) {
+      if (kk > 2 * m + 1) continue;
+      const float* ar = Tm + (32 + 16 * m + g) * 68 + 32 + 8 * kk + t;   // T_BR(i, k), row-major
+      const float* br = Xs + (8 * n + g) * 36 + 8 * kk + t;              // X(k, j) = Xs[j][k]
+      const float a4[4] = {ar[0], ar[8 * 68], ar[4], ar[8 * 68 + 4]};
+      const float b2[2] = {br[0], br[4]};
+      mma_3xtf32(dh, dc, a4, b2);
+    }
+    const int i0 = 16 * m + g, j0 = 8 * n + 2 * t;   // T(32 + i, j) = AT[j][32 + i]
+    AT[j0 * 68 + 32 + i0] = -(dh[0] + dc[0]);
+    AT[(j0 + 1) * 68 + 32 + i0] = -(dh[1] + dc[1]);
+    AT[j0 * 68 + 32 + i0 + 8] = -(dh[2] + dc[2]);
+    AT[(j0 + 1) * 68 + 32 + i0 + 8] = -(dh[3] + dc[3]);
   }
   __syncthreads();
 }
@@ -654,27 +624,32 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_before();
   __syncthreads();
 
-  // [P; .] [W | U]: rows 0-63 = P W (columns 0-127) and P U (columns 128-255)
+  // P W into columns 0-127 of TMEM lanes 0-63 and P U into columns 128-255 of lanes 64-127
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t idesc = idesc_f16(128, 256, false, true);
+    const uint32_t idesc = idesc_f16(128, 128, false, true);
     const uint32_t pa = smem_u32(sm + kPP), wu = smem_u32(sm + kPV);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(tb, smem_desc(pa + kk * 32, 16, 1024), smem_desc(wu + kk * 2048, 8192, 1024), idesc, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16(tb + 128, smem_desc(pa - 8192 + kk * 32, 16, 1024), smem_desc(wu + 16384 + kk * 2048, 8192, 1024),
+               idesc, kk > 0);
     mma_commit(&bar_mma);
   }
   ok = wait_mma();
   if (!__syncthreads_and(ok)) break;
   tc_fence_after();
 
-  if ((warp & 3) < 2) {
-    // warps 0, 1, 4, 5 (lanes 0-63): Q'_i = sq_i q_i - (P W)_i (fp16 image) and (P U)_i (fp16
-    // slices) on columns cb .. cb + 63, staged over the consumed [W | U] operand
-    const int i = 32 * (warp & 3) + lane, cb = (warp >> 2) * 64;
-    const float sq = Gam[i] * qinv[i] * kScale;
-    {
-      float w[64];
+  {
+    // warps 0, 1, 4, 5 (lanes 0-63): Q'_i = sq_i q_i - (P W)_i, the fp16 image, on columns cb .. cb + 63;
+    // warps 2, 3, 6, 7 (lanes 64-127): (P U)_i, the fp16 slices, on columns cb .. cb + 63. Both are
+    // staged over the consumed [W | U] operand, Gamma_C over P.
+    const int row = 32 * (warp & 3) + lane, i = row & 63, cb = (warp >> 2) * 64;
+    float w[64];
+    if (row < 64) {
+      const float sq = Gam[i] * qinv[i] * kScale;
       tmem_ld64(tb + lane_base + cb, w);
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
@@ -691,20 +666,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         *reinterpret_cast<uint4*>(sm + kPV + off) = pack8_f16(v);
       }
-    }
-    {
-      float u[64];
-      tmem_ld64(tb + lane_base + 128 + cb, u);
+    } else {
+      tmem_ld64(tb + lane_base + 128 + cb, w);
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
         const int col = cb + q8 * 8;
         *reinterpret_cast<uint4*>(sm + kPV + 16384 + (col >> 5) * 4096 + swz64(i * 64 + (q8 & 3) * 16)) =
-            pack8_f16(u + q8 * 8);
+            pack8_f16(w + q8 * 8);
       }
     }
-  } else if (tid == 64) {
-    // Gamma_C, staged over P (consumed)
-    *reinterpret_cast<float4*>(sm + kPP) = make_float4(Gam[63], 0.f, 0.f, 0.f);
+    if (tid == 0) *reinterpret_cast<float4*>(sm + kPP) = make_float4(Gam[63], 0.f, 0.f, 0.f);
   }
   fence_async_smem();
   tc_fence_before();

@@ -344,6 +344,41 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
+// Warp-level tensor-core product for small fp32 tiles kept at fp32 accuracy: each operand x is split
+// into tf32 parts hi = tf32(x), lo = tf32(x - hi), and D += A B is formed as lo*hi + hi*lo + hi*hi
+// (the lo*lo term is below fp32 rounding). m16n8k8 fragments (lane = 4 g + t): A holds (g, t),
+// (g + 8, t), (g, t + 4), (g + 8, t + 4); B holds (t, g), (t + 4, g); C holds (g, 2t), (g, 2t + 1),
+// (g + 8, 2t), (g + 8, 2t + 1).
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32_16x8x8(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// dh += hi(A) hi(B), dc += lo(A) hi(B) + hi(A) lo(B): two accumulators, so the two chains overlap
+__device__ __forceinline__ void mma_3xtf32(float* dh, float* dc, const float* a, const float* b) {
+  uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    ah[e] = tf32_rna(a[e]);
+    al[e] = tf32_rna(a[e] - __uint_as_float(ah[e]));
+  }
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    bh[e] = tf32_rna(b[e]);
+    bl[e] = tf32_rna(b[e] - __uint_as_float(bh[e]));
+  }
+  mma_tf32_16x8x8(dc, al, bh);
+  mma_tf32_16x8x8(dh, ah, bh);
+  mma_tf32_16x8x8(dc, ah, bl);
+}
+
 // 2^x on the special-function unit (flushes results below 2^-126 to zero).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
