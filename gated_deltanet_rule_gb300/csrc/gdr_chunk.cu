@@ -862,24 +862,28 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // head are independent: each reads the head's M' and Q' tiles itself (the other three read the
 // same lines, so they come from L2) and its own slices of N and P U. No CTA waits on another.
 // Warp roles (warp w reads TMEM lanes 32 (w % 4) .. + 31):
-//   warps 0-3: own the state rows (key row = tid, 32 value columns, float32 registers) and form
-//              S = Gamma_C S + D + N; thread 0 issues the state product D = M' S. Named barrier 1.
+//   warps 0-3: own the state rows (key row = tid, 32 value columns, float32 registers), form
+//              S = Gamma_C S + D + N and write its fp16 copy, the operand of the next products.
 //   warps 4, 5: output rows o = O' + P U for positions 0-63 (TMEM lanes 0-63); named barrier 2.
 //   warp 6: loads the chain ring (M', this CTA's N slice, Gamma_C) up to CS chunks ahead.
 //   warp 7: issues the output product O' = Q' S, so that its issue time stays off the chain.
 //   warp 8: loads the output ring (Q', this CTA's P U slice) up to OS chunks ahead.
-// Per chunk c: chain stage c % CS (chFull / chFree: the state warps release it right after their
+//   warp 9: issues the state product D = M' S (in a warp of its own, so that its issue is not
+//           serialised with the state update of a diverged state warp).
+// Per chunk c: chain stage c % CS (chFull / chFree: each state warp releases it after its
 // update), output stage c % OS (outFull / outFree: released by the output warps), state operand
-// q = c % kSb (sReady: S_c written; sFree: the output product has read it), TMEM buffers p = c % 2
-// (D[p]; O'[p] with bar_o: product done, oFree: the output warps have read it). Every barrier
-// completes once per CS, OS, 3 or 2 chunks and none can run two phases ahead of its waiters.
-constexpr int kStateThreads = 288;
-constexpr uint32_t kChainBar = 1, kChainCount = 128, kOutBar = 2, kOutCount = 64;
+// q = c % kSb (opReady: the state warps have written S_c; sReady: the state product was issued, so
+// the output product may read it too; sFree: the output product has read it), TMEM buffers
+// p = c % 2 (D[p] with bar_d; O'[p] with bar_o: product done, oFree: the output warps have read
+// it). Every barrier completes once per CS, OS, kSb, 2 chunks or per chunk, and none can run two
+// phases ahead of its waiters.
+constexpr int kStateThreads = 320;
+constexpr uint32_t kOutBar = 2, kOutCount = 64;
 constexpr uint32_t kCStage = 40960;    // M' (two 16 KB K-atoms), then this CTA's N slice (8 KB)
 constexpr uint32_t kCN = 32768;
 constexpr uint32_t kOStage = 20480;    // Q' (two 8 KB K-atoms), then this CTA's P U slice (4 KB)
 constexpr uint32_t kOPU = 16384;
-constexpr uint32_t kTmemState = 256;   // D[2] at 0, 64 (two 32-column K halves each); O'[2] at 128, 160
+constexpr uint32_t kTmemState = 128;   // D[2] at 0, 32; O'[2] at 64, 96
 // Rings: 3 chain and 3 output stages. After the rings: kSb fp16 state operands (MN-major, 128 rows
 // of 64 B). The M = 128 output product reads 8 KB past each Q' tile
 // (operand rows 64-127, whose products land in TMEM lanes nobody reads), which stays inside the
@@ -895,7 +899,7 @@ chunk_state_kernel(const ChunkArgs a) {
   constexpr uint32_t kOffSb = kOffO + OS * kOStage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t chFull[CS], chFree[CS], outFull[OS], outFree[OS], bar_d[2], bar_o[2], oFree[2], sReady[kSb],
+  __shared__ uint64_t chFull[CS], chFree[CS], outFull[OS], outFree[OS], bar_d, opReady, bar_o[2], oFree[2], sReady[kSb],
       sFree[kSb];
   __shared__ __align__(16) float4 gam_ring[CS];   // Gamma_C of the chunk in each chain stage
   __shared__ uint32_t tmem_base;
@@ -908,14 +912,14 @@ chunk_state_kernel(const ChunkArgs a) {
   if (tid == 0) {
     for (int s = 0; s < CS; ++s) {
       mbar_init(&chFull[s], 1);
-      mbar_init(&chFree[s], 1);
+      mbar_init(&chFree[s], 4);
     }
     for (int s = 0; s < OS; ++s) {
       mbar_init(&outFull[s], 1);
       mbar_init(&outFree[s], 1);
     }
-    mbar_init(&bar_d[0], 1);
-    mbar_init(&bar_d[1], 1);
+    mbar_init(&bar_d, 1);
+    mbar_init(&opReady, 4);
     for (int p = 0; p < 2; ++p) {
       mbar_init(&bar_o[p], 1);
       mbar_init(&oFree[p], 1);
@@ -1002,68 +1006,69 @@ chunk_state_kernel(const ChunkArgs a) {
     };
     write_state_operand(0);
     fence_async_smem();
-    named_bar_and(kChainBar, kChainCount, true);
-
-    int d_pend = -1;   // chunk whose half product this thread issued and has not seen complete
-    const bool issuer = tid == 0 || tid == 32;
-    const int kh = tid >> 5;   // for the issuers: which K half of the product (key rows 64 kh ..)
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&opReady);   // S_0 is in Sb[0]
     for (int c = 0; c < NC; ++c) {
-      const int cs = c % CS, p = c & 1, q = c % kSb, qn = (c + 1) % kSb;
-      uint8_t* st = sm + cs * kCStage;
+      const int cs = c % CS, p = c & 1, qn = (c + 1) % kSb;
+      const uint8_t* st = sm + cs * kCStage;
       ok = mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
-      if (issuer && ok) {
-        tc_fence_after();
-        const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
-        const uint32_t idesc = idesc_f16(128, kN, false, true);
-        const uint32_t sm_m = smem_u32(st);
-        // D[p] half kh = M'[:, 64 kh ..] S[64 kh .., :]: the critical product, its two K halves
-        // issued by two threads into two accumulators
+      if (!ok) break;
+      // while the product D = M' S_c runs: S <- Gamma_C S + N (S_c is already in the fp16 operand)
+      const float gc = gam_ring[cs].x;
+      const uint8_t* nrow = st + kCN;
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const int kk = 4 * kh + k4;
-          mma_bf16(tb + 64 * p + 32 * kh, smem_desc(sm_m + kh * 16384 + k4 * 32, 16, 1024),
-                   smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, k4 > 0);
-        }
-        mma_commit(&bar_d[kh]);
-        if (kh == 0) mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
-        d_pend = c;
-      }
-      if (ok) {
-        // while the product runs: S <- Gamma_C S + N (S_c itself is already in the fp16 operand)
-        const float gc = gam_ring[cs].x;
-        const uint8_t* nrow = st + kCN;
+      for (int ch = 0; ch < 4; ++ch) {
+        float nv[8];
+        unpack8_f16(*reinterpret_cast<const uint4*>(nrow + swz64(kr * 64 + ch * 16)), nv);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float nv[8];
-          unpack8_f16(*reinterpret_cast<const uint4*>(nrow + swz64(kr * 64 + ch * 16)), nv);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], nv[e]);
-        }
-        ok = mbar_wait(&bar_d[0], c & 1, a.wait_budget) && mbar_wait(&bar_d[1], c & 1, a.wait_budget);
-        if (ok) d_pend = -1;
+        for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], nv[e]);
       }
       // Sb[qn] is rewritten below: the output product of chunk c + 1 - kSb must have read it
-      if (c + 1 >= kSb) ok = ok && mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget);
-      if (ok) {
-        tc_fence_after();
-        float d[2 * kN];
-        tmem_ld64(tb + lane_base + 64 * p, d);
+      ok = mbar_wait(&bar_d, c & 1, a.wait_budget) &&
+           (c + 1 < kSb || mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget));
+      if (!ok) break;
+      tc_fence_after();
+      float d[kN];
+      tmem_ld32(tb + lane_base + 32 * p, d);
 #pragma unroll
-        for (int n = 0; n < kN; ++n) Sm[n] += d[n] + d[kN + n];
-        write_state_operand(qn);
-      }
+      for (int n = 0; n < kN; ++n) Sm[n] += d[n];
+      write_state_operand(qn);
       fence_async_smem();
       tc_fence_before();
-      if (!named_bar_and(kChainBar, kChainCount, ok)) break;
-      // the chain stage is free (D complete, N and Gamma_C read)
-      if (tid == 0 && c + CS < NC) mbar_arrive(&chFree[cs]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&opReady);                        // S_{c+1} is in Sb[qn]
+        if (c + CS < NC) mbar_arrive(&chFree[cs]);   // this warp is done with N and Gamma_C
+      }
     }
-    if (!ok && d_pend >= 0) mbar_wait(&bar_d[kh], d_pend & 1, kDrainBudget);   // drain the last product
     if (ok && a.S_T) {
       float* dst = a.S_T + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
 #pragma unroll
       for (int n = 0; n < kN; n += 4)
         *reinterpret_cast<float4*>(dst + n) = make_float4(Sm[n], Sm[n + 1], Sm[n + 2], Sm[n + 3]);
+    }
+  } else if (warp == 9) {
+    // ---------------- state-product issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(128, kN, false, true);
+      int last = -1;   // last chunk whose state product was issued
+      for (int c = 0; c < NC; ++c) {
+        const int cs = c % CS, p = c & 1, q = c % kSb;
+        ok = mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && mbar_wait(&opReady, c & 1, a.wait_budget);
+        if (!ok || *(volatile int*)&abort_flag) break;
+        tc_fence_after();
+        const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
+        const uint32_t sm_m = smem_u32(sm + cs * kCStage);
+        // D[p] = M' S_c: the product on the chain
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tb + 32 * p, smem_desc(sm_m + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                   smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
+        mma_commit(&bar_d);
+        mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
+        last = c;
+      }
+      if (!ok && last >= 0) mbar_wait(&bar_d, last & 1, kDrainBudget);   // drain
     }
   } else if (warp == 7) {
     // ---------------- output-product issuer ----------------
@@ -1082,7 +1087,7 @@ chunk_state_kernel(const ChunkArgs a) {
         // O'[p] = Q' S  (M = 128; operand rows 64-127 run past the tile and are not read)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tb + 128 + 32 * p, smem_desc(sm_q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+          mma_bf16(tb + 64 + 32 * p, smem_desc(sm_q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
                    smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
         mma_commit(&bar_o[p]);
         mma_commit(&sFree[q]);
@@ -1101,7 +1106,7 @@ chunk_state_kernel(const ChunkArgs a) {
       if (ok) {
         tc_fence_after();
         float qs[kN];
-        tmem_ld32(tb + lane_base + 128 + 32 * p, qs);
+        tmem_ld32(tb + lane_base + 64 + 32 * p, qs);
         const int pos = c * 64 + i;
         if (pos < a.L) {
           float pu[kN];
