@@ -345,15 +345,11 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 // Warp-level tensor-core product for small fp32 tiles kept at fp32 accuracy: each operand x is split
-// into tf32 parts hi = tf32(x), lo = tf32(x - hi), and D += A B is formed as lo*hi + hi*lo + hi*hi
-// (the lo*lo term is below fp32 rounding). m16n8k8 fragments (lane = 4 g + t): A holds (g, t),
-// (g + 8, t), (g, t + 4), (g + 8, t + 4); B holds (t, g), (t + 4, g); C holds (g, 2t), (g, 2t + 1),
-// (g + 8, 2t), (g + 8, 2t + 1).
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
+// into hi = x with its 13 low mantissa bits cleared (a tf32 value) and lo = x - hi (exact in fp32;
+// the product reads its tf32 part), and D += A B is formed as lo*hi + hi*lo + hi*hi (the dropped
+// lo*lo term and the tf32 part of lo are below fp32 rounding of the result).
+// m16n8k8 fragments (lane = 4 g + t): A holds (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4);
+// B holds (t, g), (t + 4, g); C holds (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
 __device__ __forceinline__ void mma_tf32_16x8x8(float* d, const uint32_t* a, const uint32_t* b) {
   asm volatile(
       "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
@@ -366,13 +362,13 @@ __device__ __forceinline__ void mma_3xtf32(float* dh, float* dc, const float* a,
   uint32_t ah[4], al[4], bh[2], bl[2];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    ah[e] = tf32_rna(a[e]);
-    al[e] = tf32_rna(a[e] - __uint_as_float(ah[e]));
+    ah[e] = __float_as_uint(a[e]) & 0xFFFFE000u;
+    al[e] = __float_as_uint(a[e] - __uint_as_float(ah[e]));
   }
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    bh[e] = tf32_rna(b[e]);
-    bl[e] = tf32_rna(b[e] - __uint_as_float(bh[e]));
+    bh[e] = __float_as_uint(b[e]) & 0xFFFFE000u;
+    bl[e] = __float_as_uint(b[e] - __uint_as_float(bh[e]));
   }
   mma_tf32_16x8x8(dc, al, bh);
   mma_tf32_16x8x8(dh, ah, bh);
