@@ -113,9 +113,11 @@ __device__ __forceinline__ void unpack8_f16(uint4 w, float* v) {
 // -------------------------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
 constexpr uint32_t kPQ0 = 0, kPK0 = 8192, kPQ1 = 16384, kPK1 = 24576;   // [q|k] K-atoms (Gram operand)
-constexpr uint32_t kPV = 32768;       // v atoms; then the MN-major operand [W0 | W1 | U0 | U1]; then
-                                      // the staged Q' image and P U slices
-constexpr uint32_t kPXs = 49152;      // inverse scratch (free until U is written there)
+constexpr uint32_t kPV = 32768;       // the v atoms' region; then the MN-major operand [W0 | W1 | U0 | U1];
+                                      // then the staged Q' image and P U slices
+constexpr uint32_t kPVt = 40960;      // v atoms at +0 and +16384: with the k atoms (8192, 24576) they make
+                                      // [K | V] one MN-major operand of stride 16384
+constexpr uint32_t kPXs = 49152;      // inverse scratch, between the v atoms (free until U is written there)
 // P: K-major fp16 rows 0-63. The P [W | U] products have M = 128: P W reads operand rows from P on
 // (P in rows 0-63, lanes 0-63) and P U from 8 KB before P (P in rows 64-127, lanes 64-127), so that
 // the epilogue spreads over all eight warps; the other operand rows (the tail of the [W | U]
@@ -133,6 +135,8 @@ constexpr uint32_t kPrepSmem = kPE2 + 4 * 68 * 4 + 1024;
 static_assert(kPTm % 1024 == 0 && kPP % 1024 == 0, "operand tiles need 1024-byte alignment");
 static_assert(kPP + 16384 <= kPrepSmem - 1024 && kPAop + 16384 <= kPVec, "M = 128 operands stay inside the buffer");
 static_assert(kPWS % 1024 == 0 && kPWS + 32768 <= kPVec, "the [sk W | sk U] operand fits over AT and T");
+static_assert(kPVt == kPK1 + 16384 && kPXs + 36 * 32 * 4 <= kPVt + 16384 && kPVt + 16384 + 8192 <= kPP,
+              "v atoms continue the k atoms' stride; the inverse scratch fits between them");
 
 // T = (I + A)^-1 for the strictly lower 64 x 64 A in AT (row stride 68, 1 on the diagonal), by
 // recursive doubling: 16 x 16 diagonal blocks by forward substitution, then the merges
@@ -186,7 +190,7 @@ __device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, 
     // that read k as bf16 has completed); 2048 chunks of 16 B, k atoms then v atoms
     for (int chunk16 = tid - 64; chunk16 < 2048; chunk16 += kPrepThreads - 64) {
       const int which = chunk16 >> 9, off = (chunk16 & 511) * 16;
-      const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPV + (which - 2) * 8192);
+      const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPVt + (which - 2) * 16384);
       uint4* p = reinterpret_cast<uint4*>(sm + base + off);
       uint4 w = *p;
       w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
@@ -349,7 +353,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const CUtensorMap* map = t < 2 ? &tm_q : (t < 4 ? &tm_k : &tm_v);
     const int c0 = (t & 1) * 64, c1 = t < 4 ? hk : h;
     // shared-memory order: q0 k0 q1 k1 (the Gram operand), then v0 v1
-    const uint32_t dst = t < 4 ? (uint32_t)((t & 1) * 16384 + (t >> 1) * 8192) : kPV + (uint32_t)(t - 4) * 8192;
+    const uint32_t dst = t < 4 ? (uint32_t)((t & 1) * 16384 + (t >> 1) * 8192) : kPVt + (uint32_t)(t - 4) * 16384;
     if (to_smem) {
       if (t == 0) mbar_arrive_expect_tx(&bar_ld, 49152);
       tma_load_4d(sm + dst, map, &bar_ld, c0, c1, c * 64, b);
@@ -578,20 +582,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_before();
   __syncthreads();
 
-  // W = [A1; A2] K (rows 0-63) into columns 0-127, U = [A1; A2] V (rows 64-127) into 128-255
+  // [A1; A2] [K | V]: W = A1 K in rows 0-63 of columns 0-127, U = A2 V in rows 64-127 of columns
+  // 128-255 (the other two blocks are not read)
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t idesc = idesc_f16(128, 128, true, true);
+    const uint32_t idesc = idesc_f16(128, 256, true, true);
     const uint32_t aop = smem_u32(sm + kPAop);
-    const uint32_t kt = smem_u32(sm + kPK0);   // k atoms at +8192 and +24576: stride 16384
-    const uint32_t vt = smem_u32(sm + kPV);    // v atoms at +32768 and +40960: stride 8192
+    const uint32_t kv = smem_u32(sm + kPK0);   // k atoms at +8192, +24576, v atoms at +40960, +57344
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_bf16(tb, smem_desc(aop + kk * 2048, 8192, 1024), smem_desc(kt + kk * 2048, 16384, 1024), idesc, kk > 0);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      mma_bf16(tb + 128, smem_desc(aop + kk * 2048, 8192, 1024), smem_desc(vt + kk * 2048, 8192, 1024), idesc,
-               kk > 0);
+      mma_bf16(tb, smem_desc(aop + kk * 2048, 8192, 1024), smem_desc(kv + kk * 2048, 16384, 1024), idesc, kk > 0);
     mma_commit(&bar_mma);
   }
   if (un < total) tiles(un, false);   // the next unit's tiles into L2, while W and U are formed
