@@ -865,9 +865,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 //   warps 0-3: own the state rows (key row = tid, 32 value columns, float32 registers), form
 //              S = Gamma_C S + D + N and write its fp16 copy, the operand of the next products.
 //   warps 4, 5: output rows o = O' + P U for positions 0-63 (TMEM lanes 0-63); named barrier 2.
-//   warp 6: loads the chain ring (M', this CTA's N slice, Gamma_C) up to CS chunks ahead.
+//   warp 6: loads the chain ring (M', this CTA's N slice, Gamma_C) up to CS chunks ahead, and
+//           prefetches the chunk kPrefetchAhead beyond each load into L2.
 //   warp 7: issues the output product O' = Q' S, so that its issue time stays off the chain.
-//   warp 8: loads the output ring (Q', this CTA's P U slice) up to OS chunks ahead.
+//   warp 8: loads the output ring (Q', this CTA's P U slice) up to OS chunks ahead (with the
+//           same L2 prefetch).
 //   warp 9: issues the state product D = M' S (in a warp of its own, so that its issue is not
 //           serialised with the state update of a diverged state warp).
 // Per chunk c: chain stage c % CS (chFull / chFree: each state warp releases it after its
@@ -888,6 +890,7 @@ constexpr uint32_t kTmemState = 128;   // D[2] at 0, 32; O'[2] at 64, 96
 // of 64 B). The M = 128 output product reads 8 KB past each Q' tile
 // (operand rows 64-127, whose products land in TMEM lanes nobody reads), which stays inside the
 // buffer because the state operands follow the output ring.
+constexpr int kPrefetchAhead = 3;      // ring loads also prefetch the chunk this far beyond them into L2
 constexpr int kSb = 5;                 // fp16 state operands: the output path may trail the chain by 4 chunks
 constexpr uint32_t state_smem(int cs, int os) { return cs * kCStage + os * kOStage + kSb * 8192 + 1024; }
 static_assert(kCN == kMBytes && kOPU == kQBytes, "stage layout");
@@ -970,11 +973,21 @@ chunk_state_kernel(const ChunkArgs a) {
           bulk_load(st + 16384, ub + 16384, 16384, &chFull[s]);
           bulk_load(st + kCN, ub + kUnitN + sl * 8192, 8192, &chFull[s]);
           bulk_load(&gam_ring[s], ub + kUnitS, kSCopy, &chFull[s]);
+          if (c + kPrefetchAhead < NC) {   // the chunk kPrefetchAhead further on into L2
+            const uint8_t* uf = unit_base(a, b, h, c + kPrefetchAhead);
+            bulk_prefetch_l2(uf, kMBytes);
+            bulk_prefetch_l2(uf + kUnitN + sl * 8192, 8192);
+          }
         } else {
           uint8_t* st = sm + kOffO + s * kOStage;
           mbar_arrive_expect_tx(&outFull[s], kQBytes + 4096);
           bulk_load(st, ub + kUnitQ, kQBytes, &outFull[s]);
           bulk_load(st + kOPU, ub + kUnitPU + sl * 4096, 4096, &outFull[s]);
+          if (c + kPrefetchAhead < NC) {
+            const uint8_t* uf = unit_base(a, b, h, c + kPrefetchAhead);
+            bulk_prefetch_l2(uf + kUnitQ, kQBytes);
+            bulk_prefetch_l2(uf + kUnitPU + sl * 4096, 4096);
+          }
         }
         last = c;
       }
