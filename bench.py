@@ -17,7 +17,8 @@ state kernel from starting before the prep kernel ends, so that pass is not the 
 The e2e figure is the same step through the same call with host buffers: pinned host -> device
 copies of the inputs, the call, and device -> host copies of o and S_T, all inside its timed
 region. The "rows" object adds the fork pass and the decode step of the fork workload (256 forks
-of one trunk state), each with its own HBM roofline.
+of one trunk state) and the GDN prologue (conv + SiLU, gates and carry at the prefill row's
+shapes), each with its own HBM roofline.
 
 --impl reference times the float64 CPU oracle (the checker the tests use) on a bounded sample of
 the same workload on the host cores, as the reference arm.
@@ -351,6 +352,7 @@ def run_gb300(args) -> dict | None:
         line["roofline"]["traffic_per_kernel"] = traffic_k
     if world == 1 and not args.no_rows:
         line["rows"] = run_fork_decode(reps=max(3, min(args.steps, 20)), warmup=args.warmup)
+        line["rows"]["next_f1_prologue"] = run_prologue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
     return line
@@ -429,6 +431,50 @@ def run_fork_decode(reps: int, warmup: int) -> dict:
     assert torch.isfinite(states).all() and torch.isfinite(o.float()).all()
     out["workload"] = x.meta["workload"] + f" (F={F}, Hk={Hk}, Hv={Hv}, D={D}, bf16 q/k/v)"
     return out
+
+
+def run_prologue(reps: int, warmup: int) -> dict:
+    """Times the GDN prologue (the first adjacent row: conv + SiLU, gates, carry) on the prefill
+    row's shapes, L = 4096, 16 -> 32 heads, K = 4, with its HBM roofline."""
+    import torch
+    from gated_deltanet_rule_gb300 import gdr, inputs
+    K, L, Hk, Hv = 4, 4096, 16, 32
+    x = inputs.prologue_inputs(1, L, 3, Hk=Hk, Hv=Hv, K=K)
+    d = lambda t: t.cuda().contiguous()
+    mixed, w, a, b, A_log, dt_bias, tail = (d(t) for t in (x.mixed, x.conv_w, x.a, x.b, x.A_log, x.dt_bias, x.tail))
+    C = mixed.shape[2]
+    outs = gdr.gdr_prologue(mixed, w, a, b, A_log, dt_bias, Hk, Hv, tail=tail)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        gdr.gdr_prologue(mixed, w, a, b, A_log, dt_bias, Hk, Hv, tail=tail, q=outs[0], k=outs[1], v=outs[2],
+                         g=outs[3], beta=outs[4], new_tail=outs[5], stream=stream)
+
+    # algorithmic bytes: mixed and tail read, q, k, v and the carry written (bf16); a, b read and
+    # g, beta written (float32); the weights
+    nbytes = (L + K - 1) * C * 2 + L * C * 2 + (K - 1) * C * 2 + 4 * L * Hv * 4 + C * K * 4 + 2 * Hv * 4
+    for _ in range(warmup):
+        call()
+    gdr.gdr_sync_status()
+    gdr.stage_timer_enable(True, 4 * reps + 16)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    stages = gdr.stage_timer_collect()
+    gdr.stage_timer_enable(False, 0)
+    gdr.gdr_sync_status()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    gbs = nbytes / (us * 1e-6) / 1e9
+    peaks = measured_peaks()
+    assert torch.isfinite(outs[3]).all() and torch.isfinite(outs[0].float()).all()
+    return {"us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1),
+            "workload": f"GDN prologue L={L} Hk={Hk} Hv={Hv} D={D} K={K} (conv + SiLU, gates, carry), bf16",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes},
+            "kernels": {kname: {"launches": c, "avg_us": round(t / c * 1e3, 2)} for kname, (t, c) in stages.items() if c}}
 
 
 # ------------------------------------------------------------------------------------------------

@@ -224,6 +224,45 @@ gdr_status gdr_decode_step(const void* q, const void* k, const void* v, const fl
   return launch_status(e, who);
 }
 
+gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w, const float* a,
+                        const float* b, const float* A_log, const float* dt_bias, const int32_t* lengths,
+                        void* q, void* k, void* v, float* g, float* beta, void* new_tail, int B, int L,
+                        int Hk, int Hv, int D, int K, gdr_stream_t stream) {
+  const char* who = "gdr_prologue";
+  if (!mixed || !conv_w || !a || !b || !A_log || !dt_bias || !q || !k || !v || !g || !beta)
+    return fail(GDR_ERR_INVALID_ARG, "%s: mixed, conv_w, a, b, A_log, dt_bias, q, k, v, g and beta must be non-NULL", who);
+  if (B < 1 || L < 1 || Hk < 1 || Hv < 1)
+    return fail(GDR_ERR_INVALID_ARG, "%s: sizes must be >= 1 (B=%d L=%d Hk=%d Hv=%d)", who, B, L, Hk, Hv);
+  if (Hv % Hk != 0) return fail(GDR_ERR_INVALID_ARG, "%s: Hv=%d is not a multiple of Hk=%d", who, Hv, Hk);
+  if (K < 1 || K > 8) return fail(GDR_ERR_INVALID_ARG, "%s: conv width K=%d is outside [1, 8]", who, K);
+  if (D != kD) return fail(GDR_ERR_UNSUPPORTED, "%s: head dimension D=%d is not implemented (only 128)", who, D);
+  if ((long long)B > 65535 || (long long)L * Hv > ((long long)1 << 40))
+    return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d or L*Hv too large", who, B);
+  const void* ptrs16[] = {mixed, q, k, v, tail, new_tail};
+  for (const void* p : ptrs16)
+    if (p && !aligned16(p)) return fail(GDR_ERR_INVALID_ARG, "%s: mixed, tail, q, k, v and new_tail must be 16-byte aligned", who);
+  const void* ptrs4[] = {conv_w, a, b, A_log, dt_bias, g, beta, lengths};
+  for (const void* p : ptrs4)
+    if (p && (reinterpret_cast<uintptr_t>(p) & 3u))
+      return fail(GDR_ERR_INVALID_ARG, "%s: conv_w, a, b, A_log, dt_bias, g, beta and lengths must be 4-byte aligned", who);
+  const long long C = (2LL * Hk + Hv) * kD;
+  if (new_tail && K > 1) {
+    // the carry is gathered from tail and mixed: it must not overlap either
+    const uintptr_t nt0 = reinterpret_cast<uintptr_t>(new_tail), nt1 = nt0 + (uintptr_t)B * (K - 1) * C * 2;
+    auto overlaps = [&](const void* p, uintptr_t bytes) {
+      const uintptr_t p0 = reinterpret_cast<uintptr_t>(p);
+      return p && p0 < nt1 && nt0 < p0 + bytes;
+    };
+    if (overlaps(tail, (uintptr_t)B * (K - 1) * C * 2) || overlaps(mixed, (uintptr_t)B * L * C * 2))
+      return fail(GDR_ERR_INVALID_ARG, "%s: new_tail must not overlap tail or mixed", who);
+  }
+  int* err = device_error_word();
+  if (!err) return fail(GDR_ERR_CUDA, "%s: no CUDA device available", who);
+  PrologueArgs pa{mixed, tail, conv_w, a, b, A_log, dt_bias, lengths, q, k, v, g, beta, new_tail,
+                  B, L, Hk, Hv, (int)C, K, err};
+  return launch_status(launch_prologue(pa, reinterpret_cast<cudaStream_t>(stream)), who);
+}
+
 gdr_status gdr_sync_status(gdr_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "gdr_sync_status: %s", cudaGetErrorString(e));
@@ -308,6 +347,7 @@ const char* gdr_kernel_name(int id) {
     case kKernRecurrent: return "gdr_recurrent";
     case kKernChunkPrep: return "gdr_chunk_prep";
     case kKernChunkState: return "gdr_chunk_state";
+    case kKernPrologue: return "gdr_prologue";
   }
   return nullptr;
 }

@@ -19,7 +19,8 @@ enum KernelId : int {
   kKernRecurrent = 0,
   kKernChunkPrep = 1,
   kKernChunkState = 2,
-  kNumKernelIds = 3
+  kKernPrologue = 3,
+  kNumKernelIds = 4
 };
 
 // Token-by-token recurrence on CUDA cores (float32 state in registers).
@@ -63,6 +64,29 @@ struct ChunkLaunch {
 };
 size_t chunk_workspace_bytes(int B, int Hk, int L, int Hv);
 cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s);
+
+// GDN prologue (causal depthwise conv + SiLU over [tail, mixed], the gates, the conv carry).
+// mixed [B, L, C] bf16 with C = (2 Hk + Hv) kD; tail / new_tail [B, K-1, C] bf16; conv_w [C, K];
+// proj_a, proj_b [B, L, Hv]; A_log, dt_bias [Hv]; lengths [B] (NULL = all L); q, k, v bf16.
+struct PrologueArgs {
+  const void* mixed;
+  const void* tail;
+  const float* conv_w;
+  const float* proj_a;
+  const float* proj_b;
+  const float* A_log;
+  const float* dt_bias;
+  const int32_t* lengths;
+  void* q;
+  void* k;
+  void* v;
+  float* g;
+  float* beta;
+  void* new_tail;
+  int B, L, Hk, Hv, C, K;
+  int* err;
+};
+cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);
 
 // Cycles a kernel wait may take before it gives up with GDR_ERR_TIMEOUT (about 1 s by default;
 // gdr_debug_set_wait_budget changes it for later launches).

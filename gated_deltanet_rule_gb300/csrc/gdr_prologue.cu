@@ -1,0 +1,183 @@
+// GDN prologue: the causal depthwise convolution + SiLU that turns the q|k|v projection into the
+// path's q, k, v, the gates beta and g, and the convolution carry for the next call.
+// (DEG "model.py": _linear_layer, with _conv_silu over ext = [tail, mixed] and _dn_gates.)
+//
+// Streaming kernels, bound by HBM: every input element is read once and every output written once.
+//  - conv: thread = 8 consecutive channels (one 16-byte vector) of one row, walking a run of
+//    positions with the last K inputs in registers (a sliding window), so a warp reads and writes
+//    512 contiguous bytes per position; fp32 arithmetic, one rounding to bf16 at the end.
+//  - gates: thread = one (row, position, value head).
+//  - carry: thread = 8 channels of one of the K-1 carried positions.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gdr_internal.h"
+
+namespace gdr {
+namespace {
+
+constexpr int kConvThreads = 128;   // threads per block (8 channels each)
+constexpr int kConvRun = 32;        // positions one thread walks
+
+__device__ __forceinline__ void set_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 w, float* x) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(u[e] << 16);
+    x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 f32x8_to_bf16(const float* x) {
+  uint32_t u[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    u[e] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(u[0], u[1], u[2], u[3]);
+}
+
+// ext position e of row b: the carried input tail[b][e] for e < K-1, else mixed[b][e - (K-1)]
+__device__ __forceinline__ uint4 ext_load(const PrologueArgs& a, int b, int e, int c8, int K) {
+  const size_t C = a.C;
+  if (e < K - 1) {
+    if (!a.tail) return make_uint4(0, 0, 0, 0);
+    return __ldg(reinterpret_cast<const uint4*>(a.tail) + ((size_t)b * (K - 1) + e) * (C / 8) + c8);
+  }
+  return __ldg(reinterpret_cast<const uint4*>(a.mixed) + ((size_t)b * a.L + (e - (K - 1))) * (C / 8) + c8);
+}
+
+// out[t] = sum_{j < K} w[c][j] ext[t + j]; y = out sigmoid(out), written to q, k or v by channel
+template <int K>
+__global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(const PrologueArgs a) {
+  const int c8 = blockIdx.x * kConvThreads + threadIdx.x;   // 8-channel vector index
+  const int b = blockIdx.z;
+  const int t0 = blockIdx.y * kConvRun;
+  if (c8 * 8 >= a.C) return;
+  float w[K][8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+#pragma unroll
+    for (int j = 0; j < K; ++j) w[j][e] = __ldg(a.conv_w + (size_t)(c8 * 8 + e) * K + j);
+  // destination: channels [0, HkD) -> q, [HkD, 2 HkD) -> k, the rest -> v (8-channel vectors never
+  // straddle a boundary, since the boundaries are multiples of 128)
+  const int HkD = a.Hk * kD, c0 = c8 * 8;
+  uint4* dst;
+  size_t stride8;   // vectors per position in the destination
+  if (c0 < HkD) {
+    dst = reinterpret_cast<uint4*>(a.q) + c0 / 8;
+    stride8 = HkD / 8;
+  } else if (c0 < 2 * HkD) {
+    dst = reinterpret_cast<uint4*>(a.k) + (c0 - HkD) / 8;
+    stride8 = HkD / 8;
+  } else {
+    dst = reinterpret_cast<uint4*>(a.v) + (c0 - 2 * HkD) / 8;
+    stride8 = (size_t)a.Hv * kD / 8;
+  }
+  float win[K][8];   // ext positions t .. t + K - 1 (the last one is loaded in the loop)
+#pragma unroll
+  for (int j = 0; j < K - 1; ++j) bf16x8_to_f32(ext_load(a, b, t0 + j, c8, K), win[j]);
+  const int tend = min(t0 + kConvRun, a.L);
+#pragma unroll 4
+  for (int t = t0; t < tend; ++t) {
+    bf16x8_to_f32(ext_load(a, b, t + K - 1, c8, K), win[K - 1]);
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < K; ++j) s = fmaf(w[j][e], win[j][e], s);
+      y[e] = s / (1.f + __expf(-s));
+    }
+    dst[((size_t)b * a.L + t) * stride8] = f32x8_to_bf16(y);
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) win[j][e] = win[j + 1][e];
+  }
+}
+
+// beta = sigmoid(b), g = -exp(A_log) softplus(a + dt_bias) at valid positions, 0 at pads
+__global__ void gates_kernel(const PrologueArgs a) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long n = (long long)a.B * a.L * a.Hv;
+  if (i >= n) return;
+  const int h = (int)(i % a.Hv);
+  const long long bt = i / a.Hv;
+  const int t = (int)(bt % a.L), b = (int)(bt / a.L);
+  int len = a.L;
+  if (a.lengths) {
+    len = a.lengths[b];
+    if (len < 0 || len > a.L) {
+      if (t == 0 && h == 0) set_error(a.err, kErrDeviceIndex);
+      return;   // the row's gates are left untouched
+    }
+  }
+  float beta = 0.f, g = 0.f;
+  if (t < len) {
+    beta = 1.f / (1.f + expf(-a.proj_b[i]));
+    const float x = a.proj_a[i] + a.dt_bias[h];
+    const float sp = x > 20.f ? x : log1pf(expf(x));
+    g = -expf(a.A_log[h]) * sp;
+  }
+  a.beta[i] = beta;
+  a.g[i] = g;
+}
+
+// new_tail[b][j] = ext[b][len_b + j], j < K-1: the K-1 inputs ending at the row's last valid token
+__global__ void carry_kernel(const PrologueArgs a, int K) {
+  const int c8 = blockIdx.x * blockDim.x + threadIdx.x;
+  const int j = blockIdx.y, b = blockIdx.z;
+  if (c8 * 8 >= a.C) return;
+  int len = a.L;
+  if (a.lengths) {
+    len = a.lengths[b];
+    if (len < 0 || len > a.L) return;   // recorded by the gates kernel; the row's carry is untouched
+  }
+  reinterpret_cast<uint4*>(a.new_tail)[((size_t)b * (K - 1) + j) * (a.C / 8) + c8] = ext_load(a, b, len + j, c8, K);
+}
+
+template <int K>
+cudaError_t launch_conv(const PrologueArgs& a, cudaStream_t s) {
+  const dim3 grid((unsigned)((a.C / 8 + kConvThreads - 1) / kConvThreads), (unsigned)((a.L + kConvRun - 1) / kConvRun),
+                  (unsigned)a.B);
+  conv_silu_kernel<K><<<grid, kConvThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s) {
+  int slot = stage_timer_begin(s, kKernPrologue);
+  cudaError_t e;
+  switch (a.K) {
+    case 1: e = launch_conv<1>(a, s); break;
+    case 2: e = launch_conv<2>(a, s); break;
+    case 3: e = launch_conv<3>(a, s); break;
+    case 4: e = launch_conv<4>(a, s); break;
+    case 5: e = launch_conv<5>(a, s); break;
+    case 6: e = launch_conv<6>(a, s); break;
+    case 7: e = launch_conv<7>(a, s); break;
+    default: e = launch_conv<8>(a, s); break;
+  }
+  if (e == cudaSuccess) {
+    const long long n = (long long)a.B * a.L * a.Hv;
+    gates_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess && a.new_tail && a.K > 1) {
+    carry_kernel<<<dim3((unsigned)((a.C / 8 + 127) / 128), (unsigned)(a.K - 1), (unsigned)a.B), 128, 0, s>>>(a, a.K);
+    e = cudaGetLastError();
+  }
+  stage_timer_end(slot, s);
+  return e;
+}
+
+}  // namespace gdr

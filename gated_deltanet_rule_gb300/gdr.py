@@ -21,7 +21,7 @@ GDR_F32, GDR_BF16 = 0, 1
 D = 128
 
 EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_noalloc", "gdr_fork_workspace_bytes",
-           "gdr_fork_fwd", "gdr_decode_step",
+           "gdr_fork_fwd", "gdr_decode_step", "gdr_prologue",
            "gdr_sync_status", "gdr_status_string", "gdr_last_error_message",
            "gdr_stage_timer_enable", "gdr_stage_timer_collect", "gdr_kernel_name", "gdr_debug_set_wait_budget"]
 
@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
     L.gdr_fork_fwd.restype = i
     L.gdr_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i, i, vp]
     L.gdr_decode_step.restype = i
+    L.gdr_prologue.argtypes = [vp, vp, fp, fp, fp, fp, fp, vp, vp, vp, vp, fp, fp, vp, i, i, i, i, i, i, vp]
+    L.gdr_prologue.restype = i
     L.gdr_sync_status.argtypes = [vp]
     L.gdr_sync_status.restype = i
     L.gdr_status_string.argtypes = [i]
@@ -184,6 +186,46 @@ def gdr_decode_step(q, k, v, g, beta, states, o=None, stream=None):
     _check(lib().gdr_decode_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(states), _p(o),
                                  F, Hk, Hv, Dk, dt, _stream(stream)))
     return o
+
+
+def gdr_prologue(mixed, conv_w, a, b, A_log, dt_bias, Hk: int, Hv: int, tail=None, lengths=None,
+                 q=None, k=None, v=None, g=None, beta=None, new_tail=None, stream=None,
+                 keep_tail: bool = True):
+    """GDN prologue: conv + SiLU of ``mixed`` [B,L,C] bf16 (with the carry ``tail`` [B,K-1,C]),
+    gates from ``a``, ``b`` [B,L,Hv]. Returns (q, k, v, g, beta, new_tail or None)."""
+    for name, t in (("mixed", mixed), ("conv_w", conv_w), ("a", a), ("b", b), ("A_log", A_log), ("dt_bias", dt_bias)):
+        _need(isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _need(mixed.dtype == torch.bfloat16 and mixed.dim() == 3, "mixed must be bfloat16 [B, L, C]")
+    B, L, C = mixed.shape
+    _need(C == (2 * Hk + Hv) * D, f"mixed has {C} channels, expected (2 Hk + Hv) D = {(2 * Hk + Hv) * D}")
+    _need(conv_w.dtype == torch.float32 and conv_w.dim() == 2 and conv_w.shape[0] == C, "conv_w must be float32 [C, K]")
+    K = conv_w.shape[1]
+    for name, t in (("a", a), ("b", b)):
+        _need(t.dtype == torch.float32 and t.shape == (B, L, Hv), f"{name} must be float32 [B, L, Hv]")
+    for name, t in (("A_log", A_log), ("dt_bias", dt_bias)):
+        _need(t.dtype == torch.float32 and t.shape == (Hv,), f"{name} must be float32 [Hv]")
+    if tail is not None:
+        _need(tail.is_cuda and tail.is_contiguous() and tail.dtype == torch.bfloat16 and tail.shape == (B, K - 1, C),
+              "tail must be contiguous CUDA bfloat16 [B, K-1, C]")
+    if lengths is not None:
+        _need(lengths.is_cuda and lengths.dtype == torch.int32 and lengths.shape == (B,), "lengths must be CUDA int32 [B]")
+    dev = mixed.device
+    if q is None:
+        q = torch.empty(B, L, Hk, D, device=dev, dtype=torch.bfloat16)
+    if k is None:
+        k = torch.empty(B, L, Hk, D, device=dev, dtype=torch.bfloat16)
+    if v is None:
+        v = torch.empty(B, L, Hv, D, device=dev, dtype=torch.bfloat16)
+    if g is None:
+        g = torch.empty(B, L, Hv, device=dev, dtype=torch.float32)
+    if beta is None:
+        beta = torch.empty(B, L, Hv, device=dev, dtype=torch.float32)
+    if new_tail is None and keep_tail and K > 1:
+        new_tail = torch.empty(B, K - 1, C, device=dev, dtype=torch.bfloat16)
+    _check(lib().gdr_prologue(_p(mixed), _p(tail), _p(conv_w), _p(a), _p(b), _p(A_log), _p(dt_bias), _p(lengths),
+                              _p(q), _p(k), _p(v), _p(g), _p(beta), _p(new_tail), B, L, Hk, Hv, D, K,
+                              _stream(stream)))
+    return q, k, v, g, beta, new_tail
 
 
 def gdr_sync_status(stream=None) -> None:

@@ -159,3 +159,35 @@ def config5(seed: int = 5, F: int = 256, steps: int = 32, Hk: int = 16, Hv: int 
     return ForkInputs(trunk, trunk_idx, lengths, fork, dec,
                       {"workload": f"fork batch F={F} L_pad={L_pad} + {steps} decode steps",
                        "L_pad": L_pad})
+
+
+@dataclass
+class PrologueInputs:
+    mixed: torch.Tensor            # [B, L, C] bfloat16, C = (2 Hk + Hv) D: the q|k|v projection
+    conv_w: torch.Tensor           # [C, K] float32 depthwise causal weights
+    a: torch.Tensor                # [B, L, Hv] float32 decay projection
+    b: torch.Tensor                # [B, L, Hv] float32 write-strength projection
+    A_log: torch.Tensor            # [Hv] float32
+    dt_bias: torch.Tensor          # [Hv] float32
+    tail: torch.Tensor | None      # [B, K-1, C] bfloat16 carried inputs, or None (zeros)
+    lengths: torch.Tensor | None   # [B] int32 valid tokens per row, or None (all L)
+    Hk: int = 16
+    Hv: int = 32
+
+
+def prologue_inputs(B: int, L: int, seed: int, Hk: int = 16, Hv: int = 32, K: int = 4,
+                    with_tail: bool = True, lengths=None) -> PrologueInputs:
+    """Synthetic GDN-prologue inputs (the pages print no initialisation): mixed, tail, a, b ~ N(0, 1)
+    (mixed and tail rounded to bf16), conv_w ~ U(-1, 1) / sqrt(K), A_log = log U(1, 16),
+    dt_bias ~ U(-5, 0); ``lengths`` a list of valid token counts per row (None = all L)."""
+    gen = torch.Generator().manual_seed(seed)
+    C = (2 * Hk + Hv) * D
+    mixed = torch.randn(B, L, C, generator=gen).bfloat16()
+    tail = torch.randn(B, K - 1, C, generator=gen).bfloat16() if with_tail else None
+    conv_w = (2 * torch.rand(C, K, generator=gen) - 1) / math.sqrt(K)
+    a = torch.randn(B, L, Hv, generator=gen)
+    b = torch.randn(B, L, Hv, generator=gen)
+    A_log = torch.log(1 + 15 * torch.rand(Hv, generator=gen))
+    dt_bias = -5 * torch.rand(Hv, generator=gen)
+    lens = None if lengths is None else torch.tensor(lengths, dtype=torch.int32)
+    return PrologueInputs(mixed, conv_w, a, b, A_log, dt_bias, tail, lens, Hk, Hv)

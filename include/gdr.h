@@ -138,6 +138,36 @@ gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
                                  const float* beta, const float* S0, void* o, float* S_T, int B,
                                  int L, int Hk, int Hv, int D, gdr_dtype dt, gdr_stream_t stream);
 
+/*
+ * GDN prologue: from the layer's q|k|v projection to the path's inputs.
+ * (DEG "model.py": _linear_layer with _conv_silu and _dn_gates.) Per row b, with
+ * ext = [tail; mixed] along positions (K-1 carried inputs, then the L new ones) and
+ * C = (2 Hk + Hv) D channels,
+ *   y[t][c] = silu( sum_{j < K} conv_w[c][j] ext[t + j][c] ),  silu(x) = x / (1 + exp(-x))
+ * split by channel into q (channels [0, Hk D)), k ([Hk D, 2 Hk D)) and v (the rest), and
+ *   beta = sigmoid(b),  g = -exp(A_log[h]) softplus(a + dt_bias[h])   at valid positions t < len_b,
+ *   beta = g = 0 at pads (positions >= len_b), so that pads are exact no-ops of the recurrence;
+ *   new_tail[b][j] = ext[len_b + j] for j < K-1 (the inputs ending at the last valid token).
+ * q, k and v are computed at every position, pads included (their values there do not matter).
+ *   mixed    [B, L, C] bfloat16           the projection
+ *   tail     [B, K-1, C] bfloat16         the previous call's carry; NULL = zeros (a new sequence)
+ *   conv_w   [C, K] float32               depthwise causal weights; tap K-1 meets the current token
+ *   a, b     [B, L, Hv] float32           decay and write-strength projections
+ *   A_log, dt_bias [Hv] float32
+ *   lengths  [B] int32 (device)           valid tokens per row, in [0, L]; NULL = L for every row.
+ *                                         A length outside [0, L] leaves that row's g, beta and
+ *                                         new_tail untouched and records GDR_ERR_DEVICE_INDEX.
+ *   q, k     [B, L, Hk, D] bfloat16;  v [B, L, Hv, D] bfloat16
+ *   g, beta  [B, L, Hv] float32
+ *   new_tail [B, K-1, C] bfloat16         NULL = not written; must not overlap tail or mixed
+ * K is the convolution width, 1 <= K <= 8 (the pages use 4). Arithmetic is float32 from the
+ * bfloat16 inputs, with one rounding of q, k, v to bfloat16.
+ */
+gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w, const float* a,
+                        const float* b, const float* A_log, const float* dt_bias, const int32_t* lengths,
+                        void* q, void* k, void* v, float* g, float* beta, void* new_tail, int B, int L,
+                        int Hk, int Hv, int D, int K, gdr_stream_t stream);
+
 /* Synchronise `stream`, then read and clear the sticky device error word of the current device. */
 gdr_status gdr_sync_status(gdr_stream_t stream);
 

@@ -113,3 +113,27 @@ def test_stage_timer_argument_checks(L):
     assert L.gdr_stage_timer_enable(1, 0) == gdr.GDR_ERR_INVALID_ARG
     assert L.gdr_stage_timer_enable(0, 0) == gdr.GDR_OK
     assert L.gdr_stage_timer_collect(None, None, 0) == gdr.GDR_ERR_INVALID_ARG
+
+
+def _prologue(L, mixed=P, tail=None, w=P, a=P, lengths=None, q=P, new_tail=None, B=1, Lt=64, Hk=16, Hv=32,
+              D=128, K=4):
+    return L.gdr_prologue(mixed, tail, w, a, P, P, P, lengths, q, P, P, P, P, new_tail, B, Lt, Hk, Hv, D, K, None)
+
+
+def test_prologue_rejects_bad_arguments(L):
+    assert _prologue(L, mixed=None) == gdr.GDR_ERR_INVALID_ARG
+    assert b"non-NULL" in L.gdr_last_error_message()
+    assert _prologue(L, q=None) == gdr.GDR_ERR_INVALID_ARG
+    assert _prologue(L, Lt=0) == gdr.GDR_ERR_INVALID_ARG
+    assert _prologue(L, Hk=3) == gdr.GDR_ERR_INVALID_ARG
+    assert _prologue(L, K=0) == gdr.GDR_ERR_INVALID_ARG
+    assert _prologue(L, K=9) == gdr.GDR_ERR_INVALID_ARG
+    assert b"conv width" in L.gdr_last_error_message()
+    assert _prologue(L, D=64) == gdr.GDR_ERR_UNSUPPORTED
+    assert _prologue(L, mixed=BAD) == gdr.GDR_ERR_INVALID_ARG
+    assert b"aligned" in L.gdr_last_error_message()
+    assert _prologue(L, w=ctypes.c_void_p((1 << 20) + 2)) == gdr.GDR_ERR_INVALID_ARG
+    # the carry is gathered from tail and mixed, so it may overlap neither
+    assert _prologue(L, tail=P, new_tail=P) == gdr.GDR_ERR_INVALID_ARG
+    assert b"overlap" in L.gdr_last_error_message()
+    assert _prologue(L, new_tail=ctypes.c_void_p((1 << 20) + 4096)) == gdr.GDR_ERR_INVALID_ARG
