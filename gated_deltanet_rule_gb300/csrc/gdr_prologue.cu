@@ -85,22 +85,32 @@ __global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(const PrologueA
 #pragma unroll
   for (int j = 0; j < K - 1; ++j) bf16x8_to_f32(ext_load(a, b, t0 + j, c8, K), win[j]);
   const int tend = min(t0 + kConvRun, a.L);
-#pragma unroll 4
-  for (int t = t0; t < tend; ++t) {
-    bf16x8_to_f32(ext_load(a, b, t + K - 1, c8, K), win[K - 1]);
-    float y[8];
+  // ext position t + K - 1 is the new input t: eight of them are loaded before any is used
+  const uint4* src = reinterpret_cast<const uint4*>(a.mixed) + (size_t)b * a.L * (a.C / 8) + c8;
+  for (int tg = t0; tg < tend; tg += 8) {
+    uint4 xr[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float s = 0.f;
+    for (int u = 0; u < 8; ++u)
+      xr[u] = tg + u < tend ? __ldg(src + (size_t)(tg + u) * (a.C / 8)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int j = 0; j < K; ++j) s = fmaf(w[j][e], win[j][e], s);
-      y[e] = s / (1.f + __expf(-s));
+    for (int u = 0; u < 8; ++u) {
+      if (tg + u < tend) {
+        bf16x8_to_f32(xr[u], win[K - 1]);
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float s = 0.f;
+#pragma unroll
+          for (int j = 0; j < K; ++j) s = fmaf(w[j][e], win[j][e], s);
+          y[e] = __fdividef(s, 1.f + __expf(-s));   // one rounding to bf16 follows
+        }
+        dst[((size_t)b * a.L + tg + u) * stride8] = f32x8_to_bf16(y);
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) win[j][e] = win[j + 1][e];
+      }
     }
-    dst[((size_t)b * a.L + t) * stride8] = f32x8_to_bf16(y);
-#pragma unroll
-    for (int j = 0; j < K - 1; ++j)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) win[j][e] = win[j + 1][e];
   }
 }
 
