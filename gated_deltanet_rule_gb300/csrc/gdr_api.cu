@@ -241,10 +241,11 @@ gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w
   const void* ptrs16[] = {mixed, q, k, v, tail, new_tail};
   for (const void* p : ptrs16)
     if (p && !aligned16(p)) return fail(GDR_ERR_INVALID_ARG, "%s: mixed, tail, q, k, v and new_tail must be 16-byte aligned", who);
-  const void* ptrs4[] = {conv_w, a, b, A_log, dt_bias, g, beta, lengths};
+  if (!aligned16(conv_w)) return fail(GDR_ERR_INVALID_ARG, "%s: conv_w must be 16-byte aligned", who);
+  const void* ptrs4[] = {a, b, A_log, dt_bias, g, beta, lengths};
   for (const void* p : ptrs4)
     if (p && (reinterpret_cast<uintptr_t>(p) & 3u))
-      return fail(GDR_ERR_INVALID_ARG, "%s: conv_w, a, b, A_log, dt_bias, g, beta and lengths must be 4-byte aligned", who);
+      return fail(GDR_ERR_INVALID_ARG, "%s: a, b, A_log, dt_bias, g, beta and lengths must be 4-byte aligned", who);
   const long long C = (2LL * Hk + Hv) * kD;
   if (new_tail && K > 1) {
     // the carry is gathered from tail and mixed: it must not overlap either

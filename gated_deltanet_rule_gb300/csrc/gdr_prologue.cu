@@ -61,11 +61,17 @@ __global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(const PrologueA
   const int b = blockIdx.z;
   const int t0 = blockIdx.y * kConvRun;
   if (c8 * 8 >= a.C) return;
-  float w[K][8];
+  float w[K][8];   // this thread's 8 x K weights are 8 K contiguous floats (16-byte aligned: 32 K bytes)
+  {
+    const float4* w4 = reinterpret_cast<const float4*>(a.conv_w + (size_t)c8 * 8 * K);
 #pragma unroll
-  for (int e = 0; e < 8; ++e)
+    for (int i = 0; i < 2 * K; ++i) {
+      const float4 f = __ldg(w4 + i);
+      const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-    for (int j = 0; j < K; ++j) w[j][e] = __ldg(a.conv_w + (size_t)(c8 * 8 + e) * K + j);
+      for (int u = 0; u < 4; ++u) w[(4 * i + u) % K][(4 * i + u) / K] = fv[u];
+    }
+  }
   // destination: channels [0, HkD) -> q, [HkD, 2 HkD) -> k, the rest -> v (8-channel vectors never
   // straddle a boundary, since the boundaries are multiples of 128)
   const int HkD = a.Hk * kD, c0 = c8 * 8;

@@ -152,6 +152,7 @@ gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
  *   mixed    [B, L, C] bfloat16           the projection
  *   tail     [B, K-1, C] bfloat16         the previous call's carry; NULL = zeros (a new sequence)
  *   conv_w   [C, K] float32               depthwise causal weights; tap K-1 meets the current token
+ *                                         (16-byte aligned, like mixed, tail, q, k, v and new_tail)
  *   a, b     [B, L, Hv] float32           decay and write-strength projections
  *   A_log, dt_bias [Hv] float32
  *   lengths  [B] int32 (device)           valid tokens per row, in [0, L]; NULL = L for every row.
