@@ -84,10 +84,11 @@ def measured_peaks() -> dict:
 
 
 def source_digest() -> str:
+    """Digest of the sources of the prefill kernels (the tensor-core chunk path and its helpers)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_deltanet_rule_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in ("gdr_chunk.cu", "gdr_internal.h", "ptx.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
