@@ -2,12 +2,14 @@
 // path's q, k, v, the gates beta and g, and the convolution carry for the next call.
 // (DEG "model.py": _linear_layer, with _conv_silu over ext = [tail, mixed] and _dn_gates.)
 //
-// Streaming kernels, bound by HBM: every input element is read once and every output written once.
-//  - conv: thread = 8 consecutive channels (one 16-byte vector) of one row, walking a run of
-//    positions with the last K inputs in registers (a sliding window), so a warp reads and writes
-//    512 contiguous bytes per position; fp32 arithmetic, one rounding to bf16 at the end.
-//  - gates: thread = one (row, position, value head).
-//  - carry: thread = 8 channels of one of the K-1 carried positions.
+// One streaming kernel, bound by HBM: every input element is read once and every output written
+// once. Each thread first takes a grid-stride share of
+//  - the gates: one (row, position, value head) per element, and
+//  - the carry: 8 channels of one of the K-1 carried positions per element,
+// then its run of the convolution: 8 consecutive channels (one 16-byte vector) of one row over a
+// run of positions, with the last K inputs in registers (a sliding window) and eight loads in
+// flight, so a warp reads and writes 512 contiguous bytes per position; fp32 arithmetic, one
+// rounding to bf16 at the end.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -56,7 +58,7 @@ __device__ __forceinline__ uint4 ext_load(const PrologueArgs& a, int b, int e, i
 
 // out[t] = sum_{j < K} w[c][j] ext[t + j]; y = out sigmoid(out), written to q, k or v by channel
 template <int K>
-__global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(const PrologueArgs a) {
+__device__ __forceinline__ void conv_run(const PrologueArgs& a) {
   const int c8 = blockIdx.x * kConvThreads + threadIdx.x;   // 8-channel vector index
   const int b = blockIdx.z;
   const int t0 = blockIdx.y * kConvRun;
@@ -121,10 +123,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(const PrologueA
 }
 
 // beta = sigmoid(b), g = -exp(A_log) softplus(a + dt_bias) at valid positions, 0 at pads
-__global__ void gates_kernel(const PrologueArgs a) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long n = (long long)a.B * a.L * a.Hv;
-  if (i >= n) return;
+__device__ __forceinline__ void gate_element(const PrologueArgs& a, long long i) {
   const int h = (int)(i % a.Hv);
   const long long bt = i / a.Hv;
   const int t = (int)(bt % a.L), b = (int)(bt / a.L);
@@ -148,23 +147,38 @@ __global__ void gates_kernel(const PrologueArgs a) {
 }
 
 // new_tail[b][j] = ext[b][len_b + j], j < K-1: the K-1 inputs ending at the row's last valid token
-__global__ void carry_kernel(const PrologueArgs a, int K) {
-  const int c8 = blockIdx.x * blockDim.x + threadIdx.x;
-  const int j = blockIdx.y, b = blockIdx.z;
-  if (c8 * 8 >= a.C) return;
+__device__ __forceinline__ void carry_element(const PrologueArgs& a, long long i, int K) {
+  const int c8 = (int)(i % (a.C / 8));
+  const int j = (int)((i / (a.C / 8)) % (K - 1)), b = (int)(i / ((long long)(a.C / 8) * (K - 1)));
   int len = a.L;
   if (a.lengths) {
     len = a.lengths[b];
-    if (len < 0 || len > a.L) return;   // recorded by the gates kernel; the row's carry is untouched
+    if (len < 0 || len > a.L) return;   // recorded with the gates; the row's carry is untouched
   }
   reinterpret_cast<uint4*>(a.new_tail)[((size_t)b * (K - 1) + j) * (a.C / 8) + c8] = ext_load(a, b, len + j, c8, K);
+}
+
+// One launch for the whole prologue: every thread first takes its share of the gates and of the
+// carry (grid-stride over their elements), then its run of the convolution.
+template <int K>
+__global__ void __launch_bounds__(kConvThreads) prologue_kernel(const PrologueArgs a) {
+  const long long nthreads = (long long)gridDim.x * gridDim.y * gridDim.z * kConvThreads;
+  const long long gtid =
+      (((long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * kConvThreads + threadIdx.x;
+  const long long ngates = (long long)a.B * a.L * a.Hv;
+  for (long long i = gtid; i < ngates; i += nthreads) gate_element(a, i);
+  if (K > 1 && a.new_tail) {
+    const long long ncarry = (long long)a.B * (K - 1) * (a.C / 8);
+    for (long long i = gtid; i < ncarry; i += nthreads) carry_element(a, i, K);
+  }
+  conv_run<K>(a);
 }
 
 template <int K>
 cudaError_t launch_conv(const PrologueArgs& a, cudaStream_t s) {
   const dim3 grid((unsigned)((a.C / 8 + kConvThreads - 1) / kConvThreads), (unsigned)((a.L + kConvRun - 1) / kConvRun),
                   (unsigned)a.B);
-  conv_silu_kernel<K><<<grid, kConvThreads, 0, s>>>(a);
+  prologue_kernel<K><<<grid, kConvThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -182,15 +196,6 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s) {
     case 6: e = launch_conv<6>(a, s); break;
     case 7: e = launch_conv<7>(a, s); break;
     default: e = launch_conv<8>(a, s); break;
-  }
-  if (e == cudaSuccess) {
-    const long long n = (long long)a.B * a.L * a.Hv;
-    gates_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a);
-    e = cudaGetLastError();
-  }
-  if (e == cudaSuccess && a.new_tail && a.K > 1) {
-    carry_kernel<<<dim3((unsigned)((a.C / 8 + 127) / 128), (unsigned)(a.K - 1), (unsigned)a.B), 128, 0, s>>>(a, a.K);
-    e = cudaGetLastError();
   }
   stage_timer_end(slot, s);
   return e;
