@@ -17,8 +17,8 @@ state kernel from starting before the prep kernel ends, so that pass is not the 
 The e2e figure is the same step through the same call with host buffers: pinned host -> device
 copies of the inputs, the call, and device -> host copies of o and S_T, all inside its timed
 region. The "rows" object adds the fork pass and the decode step of the fork workload (256 forks
-of one trunk state) and the GDN prologue (conv + SiLU, gates and carry at the prefill row's
-shapes), each with its own HBM roofline.
+of one trunk state), the GDN prologue (conv + SiLU, gates and carry at the prefill row's shapes)
+and the gated RMSNorm epilogue on the prefill row's output, each with its own HBM roofline.
 
 --impl reference times the float64 CPU oracle (the checker the tests use) on a bounded sample of
 the same workload on the host cores, as the reference arm.
@@ -354,6 +354,7 @@ def run_gb300(args) -> dict | None:
     if world == 1 and not args.no_rows:
         line["rows"] = run_fork_decode(reps=max(3, min(args.steps, 20)), warmup=args.warmup)
         line["rows"]["next_f1_prologue"] = run_prologue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
+        line["rows"]["next_f2_gated_rmsnorm"] = run_epilogue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
     return line
@@ -477,6 +478,50 @@ def run_prologue(reps: int, warmup: int) -> dict:
     assert torch.isfinite(outs[3]).all() and torch.isfinite(outs[0].float()).all()
     return {"us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1),
             "workload": f"GDN prologue L={L} Hk={Hk} Hv={Hv} D={D} K={K} (conv + SiLU, gates, carry), bf16",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes},
+            "kernels": {kname: {"launches": c, "avg_us": round(t / c * 1e3, 2)} for kname, (t, c) in stages.items() if c}}
+
+
+def run_epilogue(reps: int, warmup: int) -> dict:
+    """Times the gated RMSNorm epilogue (the second adjacent row) on the prefill row's output,
+    o [1, 4096, 32, 128] bf16 with its gate z, with its HBM roofline."""
+    import torch
+    from gated_deltanet_rule_gb300 import gdr
+    L, Hv = 4096, 32
+    gen = torch.Generator().manual_seed(3)
+    x = torch.randn(1, L, Hv, D, generator=gen).bfloat16().cuda()
+    z = torch.randn(1, L, Hv, D, generator=gen).bfloat16().cuda()
+    w = (0.5 + torch.rand(D, generator=gen)).cuda()
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    nbytes = 3 * x.numel() * 2 + D * 4   # x and z read, out written (bf16), the weight
+
+    def call():
+        gdr.gdr_gated_rmsnorm(x, z, w, 1e-6, out=out, stream=stream)
+
+    for _ in range(warmup):
+        call()
+    gdr.gdr_sync_status()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    gdr.stage_timer_enable(True, 4 * reps + 16)
+    for _ in range(reps):
+        call()
+    torch.cuda.synchronize()
+    stages = gdr.stage_timer_collect()
+    gdr.stage_timer_enable(False, 0)
+    gdr.gdr_sync_status()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    peaks = measured_peaks()
+    assert torch.isfinite(out.float()).all()
+    return {"us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1),
+            "workload": f"gated RMSNorm over o [1, {L}, {Hv}, {D}] bf16 with gate z",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes},
             "kernels": {kname: {"launches": c, "avg_us": round(t / c * 1e3, 2)} for kname, (t, c) in stages.items() if c}}

@@ -13,6 +13,7 @@
 
 #include "gdr.h"
 #include "gdr_internal.h"
+#include "gdr_epilogue.h"
 
 namespace gdr {
 
@@ -264,6 +265,29 @@ gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w
   return launch_status(launch_prologue(pa, reinterpret_cast<cudaStream_t>(stream)), who);
 }
 
+gdr_status gdr_gated_rmsnorm(const void* x, const void* z, const float* w, float eps, void* out,
+                             long long rows, int D, gdr_stream_t stream) {
+  const char* who = "gdr_gated_rmsnorm";
+  if (!x || !z || !w || !out) return fail(GDR_ERR_INVALID_ARG, "%s: x, z, w and out must be non-NULL", who);
+  if (rows < 1) return fail(GDR_ERR_INVALID_ARG, "%s: rows=%lld must be >= 1", who, rows);
+  if (D != kD) return fail(GDR_ERR_UNSUPPORTED, "%s: row length D=%d is not implemented (only 128)", who, D);
+  if (!(eps >= 0.f)) return fail(GDR_ERR_INVALID_ARG, "%s: eps must be >= 0", who);
+  if (rows > ((long long)1 << 36)) return fail(GDR_ERR_UNSUPPORTED, "%s: rows=%lld too large", who, rows);
+  if (!aligned16(x) || !aligned16(z) || !aligned16(w) || !aligned16(out))
+    return fail(GDR_ERR_INVALID_ARG, "%s: x, z, w and out must be 16-byte aligned", who);
+  if (out != x && out != z) {
+    // out may be x or z exactly (each row is read before it is written) but must not partly overlap
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(out), o1 = o0 + (uintptr_t)rows * kD * 2;
+    for (const void* p : {x, z}) {
+      const uintptr_t p0 = reinterpret_cast<uintptr_t>(p);
+      if (p0 < o1 && o0 < p0 + (uintptr_t)rows * kD * 2)
+        return fail(GDR_ERR_INVALID_ARG, "%s: out overlaps x or z without being one of them", who);
+    }
+  }
+  EpilogueArgs ea{x, z, w, eps, out, rows};
+  return launch_status(launch_gated_rmsnorm(ea, reinterpret_cast<cudaStream_t>(stream)), who);
+}
+
 gdr_status gdr_sync_status(gdr_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "gdr_sync_status: %s", cudaGetErrorString(e));
@@ -349,6 +373,7 @@ const char* gdr_kernel_name(int id) {
     case kKernChunkPrep: return "gdr_chunk_prep";
     case kKernChunkState: return "gdr_chunk_state";
     case kKernPrologue: return "gdr_prologue";
+    case kKernEpilogue: return "gdr_gated_rmsnorm";
   }
   return nullptr;
 }

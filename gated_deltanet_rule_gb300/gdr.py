@@ -21,7 +21,7 @@ GDR_F32, GDR_BF16 = 0, 1
 D = 128
 
 EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_noalloc", "gdr_fork_workspace_bytes",
-           "gdr_fork_fwd", "gdr_decode_step", "gdr_prologue",
+           "gdr_fork_fwd", "gdr_decode_step", "gdr_prologue", "gdr_gated_rmsnorm",
            "gdr_sync_status", "gdr_status_string", "gdr_last_error_message",
            "gdr_stage_timer_enable", "gdr_stage_timer_collect", "gdr_kernel_name", "gdr_debug_set_wait_budget"]
 
@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
     L.gdr_decode_step.restype = i
     L.gdr_prologue.argtypes = [vp, vp, fp, fp, fp, fp, fp, vp, vp, vp, vp, fp, fp, vp, i, i, i, i, i, i, vp]
     L.gdr_prologue.restype = i
+    L.gdr_gated_rmsnorm.argtypes = [vp, vp, fp, ctypes.c_float, vp, ctypes.c_longlong, i, vp]
+    L.gdr_gated_rmsnorm.restype = i
     L.gdr_sync_status.argtypes = [vp]
     L.gdr_sync_status.restype = i
     L.gdr_status_string.argtypes = [i]
@@ -226,6 +228,20 @@ def gdr_prologue(mixed, conv_w, a, b, A_log, dt_bias, Hk: int, Hv: int, tail=Non
                               _p(q), _p(k), _p(v), _p(g), _p(beta), _p(new_tail), B, L, Hk, Hv, D, K,
                               _stream(stream)))
     return q, k, v, g, beta, new_tail
+
+
+def gdr_gated_rmsnorm(x, z, w, eps: float = 1e-6, out=None, stream=None):
+    """Gated RMSNorm over the last dimension (D = 128) of ``x`` with gate ``z`` (both bf16, same
+    shape, e.g. o [B, L, Hv, D]) and weight ``w`` [D] float32; returns ``out`` (x's shape, bf16)."""
+    for name, t in (("x", x), ("z", z), ("w", w)):
+        _need(isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _need(x.dtype == torch.bfloat16 and z.dtype == torch.bfloat16 and z.shape == x.shape, "x and z: bfloat16, same shape")
+    _need(w.dtype == torch.float32 and w.shape == (x.shape[-1],), "w must be float32 [D]")
+    if out is None:
+        out = torch.empty_like(x)
+    rows = x.numel() // x.shape[-1]
+    _check(lib().gdr_gated_rmsnorm(_p(x), _p(z), _p(w), float(eps), _p(out), rows, x.shape[-1], _stream(stream)))
+    return out
 
 
 def gdr_sync_status(stream=None) -> None:

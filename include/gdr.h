@@ -169,6 +169,18 @@ gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w
                         void* q, void* k, void* v, float* g, float* beta, void* new_tail, int B, int L,
                         int Hk, int Hv, int D, int K, gdr_stream_t stream);
 
+/*
+ * Gated RMSNorm epilogue: per row of D values (a position and value head of the recurrence
+ * output o [B, L, Hv, D], so rows = B L Hv), with the gate z of the same shape,
+ *   out = w * (x / sqrt(mean(x^2) + eps)) * silu(z),   silu(z) = z / (1 + exp(-z))
+ * (DEG "model.py": _gated_rms, applied to the output of _delta_rule with the in_proj_z gate.)
+ *   x, z, out  [rows, D] bfloat16   out may be x or z itself, but may not partly overlap them
+ *   w          [D] float32          the norm weight (16-byte aligned, like x, z and out)
+ * D must be 128; eps >= 0. Arithmetic is float32 from the bfloat16 inputs, one rounding of out.
+ */
+gdr_status gdr_gated_rmsnorm(const void* x, const void* z, const float* w, float eps, void* out,
+                             long long rows, int D, gdr_stream_t stream);
+
 /* Synchronise `stream`, then read and clear the sticky device error word of the current device. */
 gdr_status gdr_sync_status(gdr_stream_t stream);
 

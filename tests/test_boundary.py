@@ -137,3 +137,17 @@ def test_prologue_rejects_bad_arguments(L):
     assert _prologue(L, tail=P, new_tail=P) == gdr.GDR_ERR_INVALID_ARG
     assert b"overlap" in L.gdr_last_error_message()
     assert _prologue(L, new_tail=ctypes.c_void_p((1 << 20) + 4096)) == gdr.GDR_ERR_INVALID_ARG
+
+
+def test_gated_rmsnorm_rejects_bad_arguments(L):
+    f = L.gdr_gated_rmsnorm
+    Q = ctypes.c_void_p((1 << 24))   # a second, distant aligned address
+    assert f(None, P, P, 1e-6, Q, 4, 128, None) == gdr.GDR_ERR_INVALID_ARG
+    assert f(P, P, P, 1e-6, Q, 0, 128, None) == gdr.GDR_ERR_INVALID_ARG
+    assert f(P, P, P, 1e-6, Q, 4, 64, None) == gdr.GDR_ERR_UNSUPPORTED
+    assert f(P, P, P, -1.0, Q, 4, 128, None) == gdr.GDR_ERR_INVALID_ARG
+    assert f(BAD, P, P, 1e-6, Q, 4, 128, None) == gdr.GDR_ERR_INVALID_ARG
+    assert b"aligned" in L.gdr_last_error_message()
+    # out may be x itself, but not a shifted view of it
+    assert f(P, Q, P, 1e-6, ctypes.c_void_p((1 << 20) + 256), 4, 128, None) == gdr.GDR_ERR_INVALID_ARG
+    assert b"overlaps" in L.gdr_last_error_message()
