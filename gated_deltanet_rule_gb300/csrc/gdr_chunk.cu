@@ -795,30 +795,39 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const uint8_t* nsl = sm + kPWS + (v >> 5) * 8192;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
-        float d[32];
+        float d[32], x[32];
         tmem_ld32(tb + lane_base + 64 + 64 * hb + 32 * part, d);
+        // all of this part's S0 entries before any S_T store (S_T may alias S0, and each entry is
+        // read and written by this thread only), so that the loads overlap
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = s0 ? __ldg(s0 + (size_t)(64 * hb + 32 * part + e) * kD + v) : 0.f;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int i = 64 * hb + 32 * part + e;
           const float n = __half2float(*reinterpret_cast<const __half*>(nsl + swz64(i * 64 + (v & 31) * 2)));
-          const float x = s0 ? __ldg(s0 + (size_t)i * kD + v) : 0.f;
-          so[(size_t)i * kD + v] = fmaf(gc, x, d[e] + n);
+          so[(size_t)i * kD + v] = fmaf(gc, x[e], d[e] + n);
         }
       }
     }
     if (write) {
-      // o at positions 32 hb .. + 31 of this chunk; (P U)[pos][v] from its staged fp16 slice
+      // o at positions 32 hb .. + 31 of this chunk; (P U)[pos][v] from its staged fp16 slice. The
+      // bf16 rows are staged over the consumed Q' image and leave by one bulk store per position.
       float ov[32];
       tmem_ld32(tb + lane_base + 192 + 32 * hb, ov);
       const uint8_t* psl = sm + kPV + 16384 + (v >> 5) * 4096;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const int pos = 32 * hb + e, pt = c * 64 + pos;
-        if (pt < a.L) {
-          const float pu = __half2float(*reinterpret_cast<const __half*>(psl + swz64(pos * 64 + (v & 31) * 2)));
-          a.o[(((size_t)b * a.L + pt) * a.Hv + h) * kD + v] = __float2bfloat16_rn(ov[e] + pu);
-        }
+        const int pos = 32 * hb + e;
+        const float pu = __half2float(*reinterpret_cast<const __half*>(psl + swz64(pos * 64 + (v & 31) * 2)));
+        *reinterpret_cast<__nv_bfloat16*>(sm + kPV + pos * 256 + v * 2) = __float2bfloat16_rn(ov[e] + pu);
       }
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (write && tid < 64 && c * 64 + tid < a.L) {
+      bulk_store(a.o + (((size_t)b * a.L + c * 64 + tid) * a.Hv + h) * kD, sm + kPV + tid * 256, 256);
+      bulk_commit();
+      bulk_wait_read();   // the next unit's tiles overwrite the staging
     }
   } else if (tid == 0) {
     bulk_store(ub, sm + kPM, kMBytes);
