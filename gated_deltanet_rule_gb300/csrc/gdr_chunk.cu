@@ -292,7 +292,9 @@ __device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, 
 // Persistent: CTA i takes units i, i + gridDim.x, ... in the order value head fastest, then chunks
 // from the last to the first (so the units the state kernel reads first were written last and are
 // the likeliest to still sit in L2), then rows. While one unit computes, the next unit's gates are
-// loaded into registers and its tiles prefetched into L2.
+// loaded into registers and its tiles prefetched into L2. kFused (rows of one chunk, a.fused) is a
+// template parameter, so that the multi-chunk kernel carries none of the in-place apply's code.
+template <bool kFused>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const ChunkArgs a) {
@@ -692,7 +694,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(tb, smem_desc(kt + kk * 2048, 16384, 1024), smem_desc(wsu + kk * 2048, 8192, 1024), idesc, kk > 0);
     mma_commit(&bar_mma);
-    if (!a.fused) {
+    if (!kFused) {
       bulk_store(ub + kUnitQ, sm + kPV, kQBytes);
       bulk_store(ub + kUnitPU, sm + kPV + 16384, kPUBytes);
       bulk_store(ub + kUnitS, sm + kPP, kSCopy);
@@ -734,7 +736,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
-  if (a.fused) {
+  if constexpr (kFused) {
     // Single-chunk row: apply the chunk to the initial state here (no workspace, no kernel 2).
     //   S_T = Gamma_C S0 + M' S0 + N,   o = Q' S0 + P U
     // computed transposed, with S0^T (fp16) as the A operand in TMEM: D^T = S0^T M'^T (values x
@@ -785,6 +787,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                        kk > 0);
       mma_commit(&bar_mma);
     }
+    // while the products run: this thread's 64 S0 entries for the Gamma_C S0 term of S_T (read
+    // before any S_T store, since S_T may alias S0; each entry is read and written by this thread)
+    float x0[64];
+#pragma unroll
+    for (int e = 0; e < 64; ++e) x0[e] = (write && a.S_T && s0) ? __ldg(s0 + (size_t)(64 * hb + e) * kD + v) : 0.f;
     ok = wait_mma();
     if (!__syncthreads_and(ok)) break;
     tc_fence_after();
@@ -795,17 +802,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const uint8_t* nsl = sm + kPWS + (v >> 5) * 8192;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
-        float d[32], x[32];
+        float d[32];
         tmem_ld32(tb + lane_base + 64 + 64 * hb + 32 * part, d);
-        // all of this part's S0 entries before any S_T store (S_T may alias S0, and each entry is
-        // read and written by this thread only), so that the loads overlap
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = s0 ? __ldg(s0 + (size_t)(64 * hb + 32 * part + e) * kD + v) : 0.f;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int i = 64 * hb + 32 * part + e;
           const float n = __half2float(*reinterpret_cast<const __half*>(nsl + swz64(i * 64 + (v & 31) * 2)));
-          so[(size_t)i * kD + v] = fmaf(gc, x[e], d[e] + n);
+          so[(size_t)i * kD + v] = fmaf(gc, x0[32 * part + e], d[e] + n);
         }
       }
     }
@@ -1244,14 +1247,19 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   a.NC = (p.L + kChunk - 1) / kChunk;
   a.err = p.err;
 
-  cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+  cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(chunk_state_kernel<3, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(3, 3));
   if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkPrep);
   const long long units = (long long)a.B * a.Hv * a.NC;
   const int grid = (int)std::min<long long>(units, 2ll * num_sms());
-  chunk_prep_kernel<<<grid, kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
+  if (a.fused)
+    chunk_prep_kernel<true><<<grid, kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
+  else
+    chunk_prep_kernel<false><<<grid, kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
   stage_timer_end(slot, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
