@@ -760,15 +760,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       write = ix >= 0 && ix < a.n_S0;
       if (!write && tid == 0) set_error(a.err, kErrDeviceIndex);
     }
+    // this thread's 64 S0 entries (keys 64 hb .., value v), kept in registers for the Gamma_C S0
+    // term of S_T (S_T may alias S0: each entry is read here, before any store, by the one thread
+    // that later writes it)
+    float x0[64];
+#pragma unroll
+    for (int e = 0; e < 64; ++e) x0[e] = s0 ? __ldg(s0 + (size_t)(64 * hb + e) * kD + v) : 0.f;
     {
       uint32_t r32[32];
 #pragma unroll
-      for (int c2 = 0; c2 < 32; ++c2) {
-        const int j = 64 * hb + 2 * c2;
-        const float x0 = s0 ? __ldg(s0 + (size_t)j * kD + v) : 0.f;
-        const float x1 = s0 ? __ldg(s0 + (size_t)(j + 1) * kD + v) : 0.f;
-        r32[c2] = pack_f16x2(x0, x1);
-      }
+      for (int c2 = 0; c2 < 32; ++c2) r32[c2] = pack_f16x2(x0[2 * c2], x0[2 * c2 + 1]);
       tmem_st32(tb + lane_base + 32 * hb, r32);
     }
     tc_fence_before();
@@ -787,11 +788,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                        kk > 0);
       mma_commit(&bar_mma);
     }
-    // while the products run: this thread's 64 S0 entries for the Gamma_C S0 term of S_T (read
-    // before any S_T store, since S_T may alias S0; each entry is read and written by this thread)
-    float x0[64];
-#pragma unroll
-    for (int e = 0; e < 64; ++e) x0[e] = (write && a.S_T && s0) ? __ldg(s0 + (size_t)(64 * hb + e) * kD + v) : 0.f;
     ok = wait_mma();
     if (!__syncthreads_and(ok)) break;
     tc_fence_after();
