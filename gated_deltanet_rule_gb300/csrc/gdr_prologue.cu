@@ -6,9 +6,9 @@
 // once. Each thread first takes a grid-stride share of
 //  - the gates: one (row, position, value head) per element, and
 //  - the carry: 8 channels of one of the K-1 carried positions per element,
-// then its run of the convolution: 8 consecutive channels (one 16-byte vector) of one row over a
+// then its run of the convolution: 4 consecutive channels (one 8-byte vector) of one row over a
 // run of positions, with the last K inputs in registers (a sliding window) and eight loads in
-// flight, so a warp reads and writes 512 contiguous bytes per position; fp32 arithmetic, one
+// flight, so a warp reads and writes 256 contiguous bytes per position; fp32 arithmetic, one
 // rounding to bf16 at the end.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -27,25 +27,6 @@ __device__ __forceinline__ void set_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(uint4 w, float* x) {
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    x[2 * e] = __uint_as_float(u[e] << 16);
-    x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ uint4 f32x8_to_bf16(const float* x) {
-  uint32_t u[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-    u[e] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  return make_uint4(u[0], u[1], u[2], u[3]);
-}
-
 // ext position e of row b: the carried input tail[b][e] for e < K-1, else mixed[b][e - (K-1)]
 __device__ __forceinline__ uint4 ext_load(const PrologueArgs& a, int b, int e, int c8, int K) {
   const size_t C = a.C;
@@ -56,67 +37,90 @@ __device__ __forceinline__ uint4 ext_load(const PrologueArgs& a, int b, int e, i
   return __ldg(reinterpret_cast<const uint4*>(a.mixed) + ((size_t)b * a.L + (e - (K - 1))) * (C / 8) + c8);
 }
 
+// 4-channel (8-byte) vectors for the convolution: half the registers of 8-channel vectors, so
+// twice the warps, and twice the loads in flight, per SM
+__device__ __forceinline__ uint2 ext_load4(const PrologueArgs& a, int b, int e, int c4, int K) {
+  const size_t C = a.C;
+  if (e < K - 1) {
+    if (!a.tail) return make_uint2(0, 0);
+    return __ldg(reinterpret_cast<const uint2*>(a.tail) + ((size_t)b * (K - 1) + e) * (C / 4) + c4);
+  }
+  return __ldg(reinterpret_cast<const uint2*>(a.mixed) + ((size_t)b * a.L + (e - (K - 1))) * (C / 4) + c4);
+}
+
+__device__ __forceinline__ void bf16x4_to_f32(uint2 w, float* x) {
+  x[0] = __uint_as_float(w.x << 16);
+  x[1] = __uint_as_float(w.x & 0xFFFF0000u);
+  x[2] = __uint_as_float(w.y << 16);
+  x[3] = __uint_as_float(w.y & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ uint2 f32x4_to_bf16(const float* x) {
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(x[0], x[1]), h1 = __floats2bfloat162_rn(x[2], x[3]);
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+}
+
 // out[t] = sum_{j < K} w[c][j] ext[t + j]; y = out sigmoid(out), written to q, k or v by channel
 template <int K>
 __device__ __forceinline__ void conv_run(const PrologueArgs& a) {
-  const int c8 = blockIdx.x * kConvThreads + threadIdx.x;   // 8-channel vector index
+  const int c4 = blockIdx.x * kConvThreads + threadIdx.x;   // 4-channel vector index
   const int b = blockIdx.z;
   const int t0 = blockIdx.y * kConvRun;
-  if (c8 * 8 >= a.C) return;
-  float w[K][8];   // this thread's 8 x K weights are 8 K contiguous floats (16-byte aligned: 32 K bytes)
+  if (c4 * 4 >= a.C) return;
+  float w[K][4];   // this thread's 4 x K weights are 4 K contiguous floats (16-byte aligned: 16 K bytes)
   {
-    const float4* w4 = reinterpret_cast<const float4*>(a.conv_w + (size_t)c8 * 8 * K);
+    const float4* w4 = reinterpret_cast<const float4*>(a.conv_w + (size_t)c4 * 4 * K);
 #pragma unroll
-    for (int i = 0; i < 2 * K; ++i) {
+    for (int i = 0; i < K; ++i) {
       const float4 f = __ldg(w4 + i);
       const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
       for (int u = 0; u < 4; ++u) w[(4 * i + u) % K][(4 * i + u) / K] = fv[u];
     }
   }
-  // destination: channels [0, HkD) -> q, [HkD, 2 HkD) -> k, the rest -> v (8-channel vectors never
+  // destination: channels [0, HkD) -> q, [HkD, 2 HkD) -> k, the rest -> v (4-channel vectors never
   // straddle a boundary, since the boundaries are multiples of 128)
-  const int HkD = a.Hk * kD, c0 = c8 * 8;
-  uint4* dst;
-  size_t stride8;   // vectors per position in the destination
+  const int HkD = a.Hk * kD, c0 = c4 * 4;
+  uint2* dst;
+  size_t stride4;   // vectors per position in the destination
   if (c0 < HkD) {
-    dst = reinterpret_cast<uint4*>(a.q) + c0 / 8;
-    stride8 = HkD / 8;
+    dst = reinterpret_cast<uint2*>(a.q) + c0 / 4;
+    stride4 = HkD / 4;
   } else if (c0 < 2 * HkD) {
-    dst = reinterpret_cast<uint4*>(a.k) + (c0 - HkD) / 8;
-    stride8 = HkD / 8;
+    dst = reinterpret_cast<uint2*>(a.k) + (c0 - HkD) / 4;
+    stride4 = HkD / 4;
   } else {
-    dst = reinterpret_cast<uint4*>(a.v) + (c0 - 2 * HkD) / 8;
-    stride8 = (size_t)a.Hv * kD / 8;
+    dst = reinterpret_cast<uint2*>(a.v) + (c0 - 2 * HkD) / 4;
+    stride4 = (size_t)a.Hv * kD / 4;
   }
-  float win[K][8];   // ext positions t .. t + K - 1 (the last one is loaded in the loop)
+  float win[K][4];   // ext positions t .. t + K - 1 (the last one is loaded in the loop)
 #pragma unroll
-  for (int j = 0; j < K - 1; ++j) bf16x8_to_f32(ext_load(a, b, t0 + j, c8, K), win[j]);
+  for (int j = 0; j < K - 1; ++j) bf16x4_to_f32(ext_load4(a, b, t0 + j, c4, K), win[j]);
   const int tend = min(t0 + kConvRun, a.L);
   // ext position t + K - 1 is the new input t: eight of them are loaded before any is used
-  const uint4* src = reinterpret_cast<const uint4*>(a.mixed) + (size_t)b * a.L * (a.C / 8) + c8;
+  const uint2* src = reinterpret_cast<const uint2*>(a.mixed) + (size_t)b * a.L * (a.C / 4) + c4;
   for (int tg = t0; tg < tend; tg += 8) {
-    uint4 xr[8];
+    uint2 xr[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u)
-      xr[u] = tg + u < tend ? __ldg(src + (size_t)(tg + u) * (a.C / 8)) : make_uint4(0, 0, 0, 0);
+      xr[u] = tg + u < tend ? __ldg(src + (size_t)(tg + u) * (a.C / 4)) : make_uint2(0, 0);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (tg + u < tend) {
-        bf16x8_to_f32(xr[u], win[K - 1]);
-        float y[8];
+        bf16x4_to_f32(xr[u], win[K - 1]);
+        float y[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 4; ++e) {
           float s = 0.f;
 #pragma unroll
           for (int j = 0; j < K; ++j) s = fmaf(w[j][e], win[j][e], s);
           y[e] = __fdividef(s, 1.f + __expf(-s));   // one rounding to bf16 follows
         }
-        dst[((size_t)b * a.L + tg + u) * stride8] = f32x8_to_bf16(y);
+        dst[((size_t)b * a.L + tg + u) * stride4] = f32x4_to_bf16(y);
 #pragma unroll
         for (int j = 0; j < K - 1; ++j)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) win[j][e] = win[j + 1][e];
+          for (int e = 0; e < 4; ++e) win[j][e] = win[j + 1][e];
       }
     }
   }
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(kConvThreads) prologue_kernel(const PrologueAr
 
 template <int K>
 cudaError_t launch_conv(const PrologueArgs& a, cudaStream_t s) {
-  const dim3 grid((unsigned)((a.C / 8 + kConvThreads - 1) / kConvThreads), (unsigned)((a.L + kConvRun - 1) / kConvRun),
+  const dim3 grid((unsigned)((a.C / 4 + kConvThreads - 1) / kConvThreads), (unsigned)((a.L + kConvRun - 1) / kConvRun),
                   (unsigned)a.B);
   prologue_kernel<K><<<grid, kConvThreads, 0, s>>>(a);
   return cudaGetLastError();
