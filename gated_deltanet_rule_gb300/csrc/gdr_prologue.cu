@@ -3,13 +3,12 @@
 // (DEG "model.py": _linear_layer, with _conv_silu over ext = [tail, mixed] and _dn_gates.)
 //
 // One streaming kernel, bound by HBM: every input element is read once and every output written
-// once. Each thread first takes a grid-stride share of
+// once. Each thread runs its part of the convolution: 4 consecutive channels (one 8-byte vector)
+// of one row over a run of positions, with the last K inputs in registers (a sliding window) and
+// eight loads in flight, so a warp reads and writes 256 contiguous bytes per position; fp32
+// arithmetic, one rounding to bf16 at the end. Then it takes a grid-stride share of
 //  - the gates: one (row, position, value head) per element, and
-//  - the carry: 8 channels of one of the K-1 carried positions per element,
-// then its run of the convolution: 4 consecutive channels (one 8-byte vector) of one row over a
-// run of positions, with the last K inputs in registers (a sliding window) and eight loads in
-// flight, so a warp reads and writes 256 contiguous bytes per position; fp32 arithmetic, one
-// rounding to bf16 at the end.
+//  - the carry: 8 channels of one of the K-1 carried positions per element.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -162,20 +161,20 @@ __device__ __forceinline__ void carry_element(const PrologueArgs& a, long long i
   reinterpret_cast<uint4*>(a.new_tail)[((size_t)b * (K - 1) + j) * (a.C / 8) + c8] = ext_load(a, b, len + j, c8, K);
 }
 
-// One launch for the whole prologue: every thread first takes its share of the gates and of the
-// carry (grid-stride over their elements), then its run of the convolution.
+// One launch for the whole prologue: every thread runs its part of the convolution, then takes its
+// share of the gates and of the carry (grid-stride over their elements).
 template <int K>
 __global__ void __launch_bounds__(kConvThreads) prologue_kernel(const PrologueArgs a) {
   const long long nthreads = (long long)gridDim.x * gridDim.y * gridDim.z * kConvThreads;
   const long long gtid =
       (((long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * kConvThreads + threadIdx.x;
+  conv_run<K>(a);
   const long long ngates = (long long)a.B * a.L * a.Hv;
   for (long long i = gtid; i < ngates; i += nthreads) gate_element(a, i);
   if (K > 1 && a.new_tail) {
     const long long ncarry = (long long)a.B * (K - 1) * (a.C / 8);
     for (long long i = gtid; i < ncarry; i += nthreads) carry_element(a, i, K);
   }
-  conv_run<K>(a);
 }
 
 template <int K>
