@@ -252,3 +252,20 @@ def test_config5_forks_and_decode_full_size_sampled():
     for step in c.decode:
         _, rS = oracle.decode_step(sub(step.q), sub(step.k), sub(step.v), sub(step.g), sub(step.beta), rS)
     assert_close(S[pick.cuda()], rS, TOL_BF16, "states after 32 decode steps")
+
+
+def test_variable_length_rows_match_their_truncated_rows():
+    """Rows of different real lengths in one call (right-padded with beta = g = 0): each row's final
+    state equals the oracle's state after that row's last real token alone, and its outputs at
+    real positions match the oracle on the truncated row."""
+    lens = [256, 130, 64, 1]
+    x = inputs.regime("R1", 256, 81, Hk=2, Hv=4, B=len(lens), init_state=True, dtype=torch.bfloat16)
+    for r, n in enumerate(lens):
+        x.beta[r, n:] = 0.0
+        x.g[r, n:] = 0.0
+    o, S = run_chunk(x)
+    for r, n in enumerate(lens):
+        sl = lambda t: t[r:r + 1, :n].contiguous()
+        ro, rS = oracle.forward(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.beta), x.S0[r:r + 1])
+        assert_close(o[r:r + 1, :n], ro, TOL_BF16, f"o of row {r} (length {n})")
+        assert_close(S[r:r + 1], rS, TOL_BF16, f"S_T of row {r} (length {n})")
