@@ -102,7 +102,7 @@ __device__ __forceinline__ void conv_run(const PrologueArgs& a) {
     uint2 xr[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u)
-      xr[u] = tg + u < tend ? __ldg(src + (size_t)(tg + u) * (a.C / 4)) : make_uint2(0, 0);
+      xr[u] = tg + u < tend ? __ldcs(src + (size_t)(tg + u) * (a.C / 4)) : make_uint2(0, 0);   // read once
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (tg + u < tend) {
