@@ -54,6 +54,15 @@ def test_prologue_matches_oracle_with_lengths_and_carry(K):
     assert torch.all(g[0, 100:] == 0) and torch.all(got[4].cpu()[0, 100:] == 0), "pads must be exact no-ops"
 
 
+def test_prologue_rows_of_length_zero_and_full():
+    """A row of length 0 is all pads: its gates are zero and its carry is the old carry."""
+    x = inputs.prologue_inputs(3, 66, 45, Hk=2, Hv=2, K=4, lengths=[0, 66, 2])
+    got = run(x)
+    check_all(got, ref(x), 4)
+    assert torch.all(got[3][0] == 0) and torch.all(got[4][0] == 0)
+    assert torch.equal(got[5][0].cpu(), x.tail[0])
+
+
 def test_prologue_without_carry_or_lengths():
     x = inputs.prologue_inputs(1, 77, 41, Hk=2, Hv=2, K=4, with_tail=False)
     check_all(run(x), ref(x), 4)

@@ -135,3 +135,12 @@ def test_carry_of_a_short_row_keeps_the_old_carry():
     m = x.mixed.double().numpy()
     assert np.array_equal(new_tail[0, 0], t[0, 1]) and np.array_equal(new_tail[0, 1], t[0, 2])
     assert np.array_equal(new_tail[0, 2], m[0, 0])
+
+
+def test_row_of_length_zero_keeps_the_carry_and_zeroes_the_gates():
+    x = inputs.prologue_inputs(2, 5, 13, Hk=1, Hv=2, K=4, lengths=[0, 5])
+    q, k, v, g, beta, new_tail = op.prologue(x.mixed, x.conv_w, x.a, x.b, x.A_log, x.dt_bias, 1, 2,
+                                              tail=x.tail, lengths=x.lengths)
+    assert np.array_equal(new_tail[0], x.tail[0].double().numpy())
+    assert np.all(g[0] == 0) and np.all(beta[0] == 0)
+    assert np.array_equal(new_tail[1], x.mixed[1, 2:5].double().numpy())
