@@ -237,8 +237,9 @@ gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w
   if (Hv % Hk != 0) return fail(GDR_ERR_INVALID_ARG, "%s: Hv=%d is not a multiple of Hk=%d", who, Hv, Hk);
   if (K < 1 || K > 8) return fail(GDR_ERR_INVALID_ARG, "%s: conv width K=%d is outside [1, 8]", who, K);
   if (D != kD) return fail(GDR_ERR_UNSUPPORTED, "%s: head dimension D=%d is not implemented (only 128)", who, D);
-  if ((long long)B > 65535 || (long long)L * Hv > ((long long)1 << 40))
-    return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d or L*Hv too large", who, B);
+  // launch limits: rows are the grid's z dimension, runs of 32 positions its y dimension
+  if ((long long)B > 65535 || (long long)L > 32LL * 65535)
+    return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d or L=%d too large (B <= 65535, L <= 2097120)", who, B, L);
   const void* ptrs16[] = {mixed, q, k, v, tail, new_tail};
   for (const void* p : ptrs16)
     if (p && !aligned16(p)) return fail(GDR_ERR_INVALID_ARG, "%s: mixed, tail, q, k, v and new_tail must be 16-byte aligned", who);
@@ -272,7 +273,7 @@ gdr_status gdr_gated_rmsnorm(const void* x, const void* z, const float* w, float
   if (rows < 1) return fail(GDR_ERR_INVALID_ARG, "%s: rows=%lld must be >= 1", who, rows);
   if (D != kD) return fail(GDR_ERR_UNSUPPORTED, "%s: row length D=%d is not implemented (only 128)", who, D);
   if (!(eps >= 0.f)) return fail(GDR_ERR_INVALID_ARG, "%s: eps must be >= 0", who);
-  if (rows > ((long long)1 << 36)) return fail(GDR_ERR_UNSUPPORTED, "%s: rows=%lld too large", who, rows);
+  if (rows > ((long long)1 << 34)) return fail(GDR_ERR_UNSUPPORTED, "%s: rows=%lld too large (<= 2^34)", who, rows);
   if (!aligned16(x) || !aligned16(z) || !aligned16(w) || !aligned16(out))
     return fail(GDR_ERR_INVALID_ARG, "%s: x, z, w and out must be 16-byte aligned", who);
   if (out != x && out != z) {

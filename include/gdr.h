@@ -161,7 +161,8 @@ gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
  *   q, k     [B, L, Hk, D] bfloat16;  v [B, L, Hv, D] bfloat16
  *   g, beta  [B, L, Hv] float32
  *   new_tail [B, K-1, C] bfloat16         NULL = not written; must not overlap tail or mixed
- * K is the convolution width, 1 <= K <= 8 (the pages use 4). Arithmetic is float32 from the
+ * K is the convolution width, 1 <= K <= 8 (the pages use 4); B <= 65535 and L <= 2097120
+ * (GDR_ERR_UNSUPPORTED otherwise). Arithmetic is float32 from the
  * bfloat16 inputs, with one rounding of q, k, v to bfloat16.
  */
 gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w, const float* a,
@@ -176,7 +177,8 @@ gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w
  * (DEG "model.py": _gated_rms, applied to the output of _delta_rule with the in_proj_z gate.)
  *   x, z, out  [rows, D] bfloat16   out may be x or z itself, but may not partly overlap them
  *   w          [D] float32          the norm weight (16-byte aligned, like x, z and out)
- * D must be 128; eps >= 0. Arithmetic is float32 from the bfloat16 inputs, one rounding of out.
+ * D must be 128; eps >= 0; rows <= 2^34. Arithmetic is float32 from the bfloat16 inputs, one
+ * rounding of out.
  */
 gdr_status gdr_gated_rmsnorm(const void* x, const void* z, const float* w, float eps, void* out,
                              long long rows, int D, gdr_stream_t stream);

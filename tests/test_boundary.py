@@ -137,6 +137,8 @@ def test_prologue_rejects_bad_arguments(L):
     assert _prologue(L, tail=P, new_tail=P) == gdr.GDR_ERR_INVALID_ARG
     assert b"overlap" in L.gdr_last_error_message()
     assert _prologue(L, new_tail=ctypes.c_void_p((1 << 20) + 4096)) == gdr.GDR_ERR_INVALID_ARG
+    assert _prologue(L, Lt=32 * 65535 + 1) == gdr.GDR_ERR_UNSUPPORTED
+    assert _prologue(L, B=65536) == gdr.GDR_ERR_UNSUPPORTED
 
 
 def test_gated_rmsnorm_rejects_bad_arguments(L):
@@ -145,6 +147,7 @@ def test_gated_rmsnorm_rejects_bad_arguments(L):
     assert f(None, P, P, 1e-6, Q, 4, 128, None) == gdr.GDR_ERR_INVALID_ARG
     assert f(P, P, P, 1e-6, Q, 0, 128, None) == gdr.GDR_ERR_INVALID_ARG
     assert f(P, P, P, 1e-6, Q, 4, 64, None) == gdr.GDR_ERR_UNSUPPORTED
+    assert f(P, Q, P, 1e-6, P, (1 << 34) + 1, 128, None) == gdr.GDR_ERR_UNSUPPORTED
     assert f(P, P, P, -1.0, Q, 4, 128, None) == gdr.GDR_ERR_INVALID_ARG
     assert f(BAD, P, P, 1e-6, Q, 4, 128, None) == gdr.GDR_ERR_INVALID_ARG
     assert b"aligned" in L.gdr_last_error_message()
