@@ -355,6 +355,7 @@ def run_gb300(args) -> dict | None:
         line["rows"] = run_fork_decode(reps=max(3, min(args.steps, 20)), warmup=args.warmup)
         line["rows"]["next_f1_prologue"] = run_prologue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
         line["rows"]["next_f2_gated_rmsnorm"] = run_epilogue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
+        line["rows"]["next_f4_backward"] = run_backward(reps=max(3, min(args.steps, 10)), warmup=args.warmup)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
     return line
@@ -524,6 +525,52 @@ def run_epilogue(reps: int, warmup: int) -> dict:
             "workload": f"gated RMSNorm over o [1, {L}, {Hv}, {D}] bf16 with gate z",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes},
+            "kernels": {kname: {"launches": c, "avg_us": round(t / c * 1e3, 2)} for kname, (t, c) in stages.items() if c}}
+
+
+def run_backward(reps: int, warmup: int) -> dict:
+    """Times the backward (gdr_backward: the checkpointed token-loop kernel and its reducer) on the
+    prefill workload, L = 4096, Hk = 16, Hv = 32, bf16 q, k, v, dO, with dS_T. Its HBM roofline
+    counts the algorithmic bytes: q, k, v, dO, g, beta, dS_T read once, every gradient written once."""
+    import torch
+    from gated_deltanet_rule_gb300 import gdr, inputs
+    L, Hk, Hv = 4096, 16, 32
+    x = inputs.regime("R1", L, 3, Hk=Hk, Hv=Hv, B=1, dtype=torch.bfloat16)
+    dO, dS_T = inputs.upstream_grads(1, L, Hv, 4, dtype=torch.bfloat16)
+    q, k, v, g, beta, dO, dS_T = (t.cuda() for t in (x.q, x.k, x.v, x.g, x.beta, dO, dS_T))
+    ws = torch.empty(gdr.backward_workspace_bytes(1, L, Hk, Hv), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    nbytes = (2 * L * Hk * D * 2 + 2 * L * Hv * D * 2 + 2 * L * Hv * 4 + Hv * D * D * 4       # inputs
+              + 2 * L * Hk * D * 4 + L * Hv * D * 4 + 2 * L * Hv * 4 + Hv * D * D * 4)       # gradients
+
+    def call():
+        return gdr.gdr_backward(q, k, v, g, beta, None, dO, dS_T, ws=ws, stream=stream)
+
+    for _ in range(warmup):
+        call()
+    gdr.gdr_sync_status()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        out = call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    gdr.stage_timer_enable(True, 4 * reps + 16)
+    for _ in range(reps):
+        call()
+    torch.cuda.synchronize()
+    stages = gdr.stage_timer_collect()
+    gdr.stage_timer_enable(False, 0)
+    gdr.gdr_sync_status()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    peaks = measured_peaks()
+    assert all(torch.isfinite(t).all() for t in out if t is not None)
+    return {"us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1),
+            "workload": f"backward of the prefill row [1, {L}], Hk={Hk}, Hv={Hv}, D={D}, bf16 q/k/v/dO, float32 gradients",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes,
+                         "note": "a sequential token loop on CUDA cores: latency-bound, far from this roofline"},
             "kernels": {kname: {"launches": c, "avg_us": round(t / c * 1e3, 2)} for kname, (t, c) in stages.items() if c}}
 
 

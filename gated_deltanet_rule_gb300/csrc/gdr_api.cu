@@ -13,6 +13,7 @@
 
 #include "gdr.h"
 #include "gdr_internal.h"
+#include "gdr_backward.h"
 #include "gdr_epilogue.h"
 
 namespace gdr {
@@ -289,6 +290,37 @@ gdr_status gdr_gated_rmsnorm(const void* x, const void* z, const float* w, float
   return launch_status(launch_gated_rmsnorm(ea, reinterpret_cast<cudaStream_t>(stream)), who);
 }
 
+size_t gdr_backward_workspace_bytes(int B, int L, int Hk, int Hv, int D) {
+  if (B < 1 || L < 1 || Hk < 1 || Hv < 1 || D != kD || Hv % Hk != 0) return 0;
+  return backward_workspace_bytes(B, L, Hk, Hv);
+}
+
+gdr_status gdr_backward(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                        const float* S0, const void* dO, const float* dS_T, float* dq, float* dk,
+                        float* dv, float* dg, float* dbeta, float* dS0, int B, int L, int Hk, int Hv,
+                        int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream) {
+  const char* who = "gdr_backward";
+  if (!dO) return fail(GDR_ERR_INVALID_ARG, "%s: dO must be non-NULL", who);
+  gdr_status st = check_common(q, k, v, g, beta, dO, B, L, Hk, Hv, D, dt, who);
+  if (st != GDR_OK) return st;
+  if (!dq || !dk || !dv || !dg || !dbeta)
+    return fail(GDR_ERR_INVALID_ARG, "%s: dq, dk, dv, dg and dbeta must be non-NULL", who);
+  const void* ptrs16[] = {dq, dk, dv, dg, dbeta, S0, dS_T, dS0, ws};
+  for (const void* p : ptrs16)
+    if (p && !aligned16(p))
+      return fail(GDR_ERR_INVALID_ARG, "%s: every array and the workspace must be 16-byte aligned", who);
+  // launch limits: 4 B column-block CTAs on the grid's x dimension, B L tokens on the reducer's
+  if ((long long)B > 65535 || (long long)B * L > 0x7fffffffLL || Hk > 65535)
+    return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d, B*L=%lld or Hk=%d too large (B <= 65535, B*L < 2^31)", who, B,
+                (long long)B * L, Hk);
+  const size_t need = backward_workspace_bytes(B, L, Hk, Hv);
+  if (ws == nullptr || ws_bytes < need)
+    return fail(GDR_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", who, need,
+                ws == nullptr ? (size_t)0 : ws_bytes);
+  BackwardArgs a{q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, ws, B, L, Hk, Hv, dt == GDR_BF16};
+  return launch_status(launch_backward(a, reinterpret_cast<cudaStream_t>(stream)), who);
+}
+
 gdr_status gdr_sync_status(gdr_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(GDR_ERR_CUDA, "gdr_sync_status: %s", cudaGetErrorString(e));
@@ -375,6 +407,8 @@ const char* gdr_kernel_name(int id) {
     case kKernChunkState: return "gdr_chunk_state";
     case kKernPrologue: return "gdr_prologue";
     case kKernEpilogue: return "gdr_gated_rmsnorm";
+    case kKernBackward: return "gdr_backward";
+    case kKernBackwardReduce: return "gdr_backward_reduce";
   }
   return nullptr;
 }

@@ -1,0 +1,397 @@
+// Backward of the gated delta rule, token by token on CUDA cores with a float32 state.
+//
+// Reverse mode through the recurrence of the forward (Kev-4B-LiteRT "r15_kernel_test.py",
+// truth_f64; DEG "model.py", delta_rule_reference; the pages train through it but print no
+// backward). Per (row, value head), with S_{t-1} the state before token t, e = exp(g_t),
+// S_a = e S_{t-1}, kv = S_a^T k^, vm = v - kv, delta = beta vm, S_t = S_a + k^ delta^T and
+// o_t = S_t^T q~, the adjoint dS of S_t runs from the last token to the first:
+//   dq~ = S_t dO_t;     dS += q~ dO_t^T
+//   dk^ = dS delta;     ddelta = dS^T k^;   dbeta = ddelta . vm;   dv = beta ddelta
+//   dkv = -beta ddelta; dS_a = dS + k^ dkv^T;  dk^ += S_a dkv;  dg = <S_a, dS_a>
+//   dS = e dS_a                                   (the adjoint of S_{t-1})
+// and dS0 is the dS left after the first token.
+//
+// The states S_{t-1} are recomputed, not kept by the forward: a first pass stores the state at
+// the start of every 32-token segment (a checkpoint); then each segment, last first, runs forward
+// again from its checkpoint keeping its 32 states, and then in reverse. Both stores are private to
+// the thread that reads them back, so they need no synchronisation.
+//
+// A CTA owns 32 value columns of one (row, value head), the layout of the forward token loop:
+// thread t holds key rows (t/8) + 16m, m = 0..7, and columns 4(t%8)..+3 of both S and dS. The
+// per-column results (dv, dS0) are the CTA's own. The per-key-row ones (dq~, dk^) and the sums
+// over columns (dbeta, dg) are partial over the CTA's 32 columns: they go to the workspace, and a
+// second kernel sums them over the 4 column blocks and the value heads of each key head in a
+// fixed order (the result does not depend on scheduling), then takes dq~ and dk^ back through the
+// normalisations, dx = s dx^ - s^3 (x . dx^) x with s = (|x|^2 + 1e-6)^-1/2 (and D^-1/2 for q).
+#include <cuda_bf16.h>
+
+#include "gdr_backward.h"
+#include "gdr_internal.h"
+
+namespace gdr {
+namespace {
+
+constexpr int kCols = 32;                 // value columns per CTA
+constexpr int kThreads = 128;
+constexpr int kSlice = kD * kCols;        // floats of one CTA's state slice
+constexpr float kScale = 0.08838834764831845f;   // 128^-0.5
+
+__device__ __forceinline__ float ld_in(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float ld_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+// Workspace carve-up (floats): checkpoints [cta][segment][slice], segment states
+// [cta][kBwdSeg][slice], then the partials dq~, dk^ [B L Hv][4][kD] and dg, dbeta [B L Hv][4].
+// A slice is stored as [m][thread] float4, so slot s of thread t's m-th float4 is
+// (s * 8 + m) * kThreads + t.
+struct Workspace {
+  float* ckpt;
+  float* tok;
+  float* pq;
+  float* pk;
+  float* pg;
+  float* pb;
+};
+
+Workspace carve(void* ws, int B, int L, int Hv) {
+  const size_t nCta = 4 * (size_t)B * Hv;
+  const size_t nSeg = ((size_t)L + kBwdSeg - 1) / kBwdSeg;
+  const size_t tokens = (size_t)B * L * Hv;
+  float* p = static_cast<float*>(ws);
+  Workspace w;
+  w.ckpt = p; p += nCta * nSeg * kSlice;
+  w.tok = p;  p += nCta * kBwdSeg * kSlice;
+  w.pq = p;   p += tokens * 4 * kD;
+  w.pk = p;   p += tokens * 4 * kD;
+  w.pg = p;   p += tokens * 4;
+  w.pb = p;
+  return w;
+}
+
+struct BwdSmem {
+  float qs[2][kD], ks[2][kD], vs[2][kCols];
+  float nred[2][4][2];          // per-warp partials of q.q, k.k
+  float red[2][4][8][4];        // per-warp column partials of S^T k
+  float qt[kBwdSeg][kD];        // q~ of the segment's tokens
+  float kh[kBwdSeg][kD];        // k^
+  float vm[kBwdSeg][kCols];     // v - kv
+  float es[kBwdSeg], bs[kBwdSeg];
+  float cred[2][4][8][4];       // per-warp column partials of dS^T k^
+  float gred[2][4];             // per-warp partials of <S_{t-1}, dS_a>
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Workspace w) {
+  __shared__ BwdSmem sm;
+  const int cb = blockIdx.x & 3;
+  const int b = blockIdx.x >> 2;
+  const int h = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int cg = tid & 7, rg = tid >> 3;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int hk = h / (a.Hv / a.Hk);
+  const int L = a.L;
+  const int nSeg = (L + kBwdSeg - 1) / kBwdSeg;
+  const size_t cta = ((size_t)b * a.Hv + h) * 4 + cb;
+  float4* ck = reinterpret_cast<float4*>(w.ckpt + cta * nSeg * kSlice);
+  float4* tk = reinterpret_cast<float4*>(w.tok + cta * kBwdSeg * kSlice);
+  const T* q = static_cast<const T*>(a.q);
+  const T* k = static_cast<const T*>(a.k);
+  const T* v = static_cast<const T*>(a.v);
+  const T* dO = static_cast<const T*>(a.dO);
+  const size_t row_tok = (size_t)b * L;
+  const int col0 = cb * kCols + 4 * cg;
+  const size_t state_off = ((size_t)b * a.Hv + h) * kD * kD;
+
+  float S[8][4];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a.S0) x = __ldg(reinterpret_cast<const float4*>(a.S0 + state_off + (size_t)(rg + 16 * m) * kD + col0));
+    S[m][0] = x.x; S[m][1] = x.y; S[m][2] = x.z; S[m][3] = x.w;
+  }
+
+  // One forward token, S_{t-1} -> S_t. With rec, keeps what the reverse needs of token t in
+  // slot i: S_{t-1} (thread-private, workspace), q~, k^, v - kv, e and beta (shared memory).
+  auto forward_token = [&](int t, int buf, bool rec, int i) {
+    const size_t qk_off = ((row_tok + t) * a.Hk + hk) * kD + tid;
+    const float qv = ld_in(q + qk_off), kv = ld_in(k + qk_off);
+    const float gt = __ldg(a.g + (row_tok + t) * a.Hv + h);
+    const float bt = __ldg(a.beta + (row_tok + t) * a.Hv + h);
+    sm.qs[buf][tid] = qv;
+    sm.ks[buf][tid] = kv;
+    if (tid < kCols) sm.vs[buf][tid] = ld_in(v + ((row_tok + t) * a.Hv + h) * kD + cb * kCols + tid);
+    float s0 = qv * qv, s1 = kv * kv;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+    }
+    if (lane == 0) { sm.nred[buf][warp][0] = s0; sm.nred[buf][warp][1] = s1; }
+    __syncthreads();
+
+    float pk[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float kk = sm.ks[buf][rg + 16 * m];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) pk[c] = fmaf(S[m][c], kk, pk[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], 8);
+      pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], 16);
+    }
+    if (lane < 8) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sm.red[buf][warp][lane][c] = pk[c];
+    }
+    __syncthreads();
+
+    const float sqq = sm.nred[buf][0][0] + sm.nred[buf][1][0] + sm.nred[buf][2][0] + sm.nred[buf][3][0];
+    const float skk = sm.nred[buf][0][1] + sm.nred[buf][1][1] + sm.nred[buf][2][1] + sm.nred[buf][3][1];
+    const float qinv = rsqrtf(sqq + 1e-6f), kinv = rsqrtf(skk + 1e-6f);
+    const float e = expf(gt);
+    const float ekinv = e * kinv;
+    float delta[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float fk = sm.red[buf][0][cg][c] + sm.red[buf][1][cg][c] + sm.red[buf][2][cg][c] + sm.red[buf][3][cg][c];
+      const float vmc = sm.vs[buf][4 * cg + c] - ekinv * fk;
+      delta[c] = bt * vmc;
+      if (rec && rg == 0) sm.vm[i][4 * cg + c] = vmc;
+    }
+    if (rec) {
+      sm.qt[i][tid] = qv * (qinv * kScale);
+      sm.kh[i][tid] = kinv * kv;
+      if (tid == 0) { sm.es[i] = e; sm.bs[i] = bt; }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) tk[(size_t)(i * 8 + m) * kThreads + tid] = make_float4(S[m][0], S[m][1], S[m][2], S[m][3]);
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float kk = kinv * sm.ks[buf][rg + 16 * m];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) S[m][c] = fmaf(e, S[m][c], kk * delta[c]);
+    }
+  };
+
+  // Pass 1: checkpoints at every segment start (the last segment's tokens are not needed).
+  for (int seg = 0; seg < nSeg; ++seg) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) ck[(size_t)(seg * 8 + m) * kThreads + tid] = make_float4(S[m][0], S[m][1], S[m][2], S[m][3]);
+    if (seg == nSeg - 1) break;
+    for (int i = 0; i < kBwdSeg; ++i) forward_token(seg * kBwdSeg + i, i & 1, false, 0);
+  }
+
+  float dS[8][4];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a.dS_T) x = __ldg(reinterpret_cast<const float4*>(a.dS_T + state_off + (size_t)(rg + 16 * m) * kD + col0));
+    dS[m][0] = x.x; dS[m][1] = x.y; dS[m][2] = x.z; dS[m][3] = x.w;
+  }
+
+  // dg of a token is written by thread 0 once the next barrier has passed (pending until then).
+  bool pend = false;
+  size_t pend_tv = 0;
+  int pend_buf = 0;
+  float pend_e = 0.f;
+  auto flush_dg = [&]() {
+    if (pend && tid == 0)
+      w.pg[pend_tv * 4 + cb] = pend_e * (sm.gred[pend_buf][0] + sm.gred[pend_buf][1] + sm.gred[pend_buf][2] + sm.gred[pend_buf][3]);
+    pend = false;
+  };
+
+  // One reverse token: dS (adjoint of S_t) -> adjoint of S_{t-1}, from slot i.
+  auto backward_token = [&](int t, int buf, int i) {
+    const size_t tv = (row_tok + t) * a.Hv + h;
+    float dOc[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dOc[c] = ld_in(dO + tv * kD + col0 + c);
+    const float e = sm.es[i], bt = sm.bs[i];
+    float vmc[4], dl[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) { vmc[c] = sm.vm[i][4 * cg + c]; dl[c] = bt * vmc[c]; }
+    float Sp[8][4];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float4 x = tk[(size_t)(i * 8 + m) * kThreads + tid];
+      Sp[m][0] = x.x; Sp[m][1] = x.y; Sp[m][2] = x.z; Sp[m][3] = x.w;
+    }
+    float dqr[8], dkr[8];
+    float dcol[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float qr = sm.qt[i][rg + 16 * m], kr = sm.kh[i][rg + 16 * m];
+      float aq = 0.f, ak = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float st = fmaf(e, Sp[m][c], kr * dl[c]);     // S_t, as the forward formed it
+        aq = fmaf(st, dOc[c], aq);
+        dS[m][c] = fmaf(qr, dOc[c], dS[m][c]);
+        ak = fmaf(dS[m][c], dl[c], ak);
+        dcol[c] = fmaf(dS[m][c], kr, dcol[c]);
+      }
+      dqr[m] = aq;
+      dkr[m] = ak;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      dcol[c] += __shfl_xor_sync(0xffffffffu, dcol[c], 8);
+      dcol[c] += __shfl_xor_sync(0xffffffffu, dcol[c], 16);
+    }
+    if (lane < 8) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sm.cred[buf][warp][lane][c] = dcol[c];
+    }
+    __syncthreads();
+    flush_dg();
+
+    float ddl[4], dkv[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      ddl[c] = sm.cred[buf][0][cg][c] + sm.cred[buf][1][cg][c] + sm.cred[buf][2][cg][c] + sm.cred[buf][3][cg][c];
+      dkv[c] = -bt * ddl[c];
+    }
+    // dbeta: lanes 0..7 of warp 0 hold the 8 column groups
+    float xb = ddl[0] * vmc[0] + ddl[1] * vmc[1] + ddl[2] * vmc[2] + ddl[3] * vmc[3];
+    xb += __shfl_xor_sync(0xffffffffu, xb, 1);
+    xb += __shfl_xor_sync(0xffffffffu, xb, 2);
+    xb += __shfl_xor_sync(0xffffffffu, xb, 4);
+    if (tid == 0) w.pb[tv * 4 + cb] = xb;
+    if (rg == 0)
+      *reinterpret_cast<float4*>(a.dv + tv * kD + col0) = make_float4(bt * ddl[0], bt * ddl[1], bt * ddl[2], bt * ddl[3]);
+
+    float gp = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float kr = sm.kh[i][rg + 16 * m];
+      float a2 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        a2 = fmaf(Sp[m][c], dkv[c], a2);
+        dS[m][c] = fmaf(kr, dkv[c], dS[m][c]);               // dS_a
+        gp = fmaf(Sp[m][c], dS[m][c], gp);
+      }
+      dkr[m] = fmaf(e, a2, dkr[m]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) dS[m][c] *= e;
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1) {
+        dqr[m] += __shfl_xor_sync(0xffffffffu, dqr[m], off);
+        dkr[m] += __shfl_xor_sync(0xffffffffu, dkr[m], off);
+      }
+    }
+    if (cg == 0) {
+      float* pq = w.pq + (tv * 4 + cb) * kD;
+      float* pk = w.pk + (tv * 4 + cb) * kD;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) { pq[rg + 16 * m] = dqr[m]; pk[rg + 16 * m] = dkr[m]; }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) gp += __shfl_xor_sync(0xffffffffu, gp, off);
+    if (lane == 0) sm.gred[buf][warp] = gp;
+    pend = true;
+    pend_tv = tv;
+    pend_buf = buf;
+    pend_e = e;
+  };
+
+  // Pass 2: segments last to first, each recomputed forward, then reversed.
+  for (int seg = nSeg - 1; seg >= 0; --seg) {
+    const int t0 = seg * kBwdSeg;
+    const int n = min(kBwdSeg, L - t0);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float4 x = ck[(size_t)(seg * 8 + m) * kThreads + tid];
+      S[m][0] = x.x; S[m][1] = x.y; S[m][2] = x.z; S[m][3] = x.w;
+    }
+    __syncthreads();    // the previous segment's reverse is done with the shared arrays
+    for (int i = 0; i < n; ++i) forward_token(t0 + i, i & 1, true, i);
+    __syncthreads();    // the segment's records are complete
+    for (int i = n - 1; i >= 0; --i) backward_token(t0 + i, i & 1, i);
+    __syncthreads();
+    flush_dg();
+  }
+
+  if (a.dS0) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      *reinterpret_cast<float4*>(a.dS0 + state_off + (size_t)(rg + 16 * m) * kD + col0) =
+          make_float4(dS[m][0], dS[m][1], dS[m][2], dS[m][3]);
+  }
+}
+
+// One (row, token, key head) per CTA, one key row per thread: sums the partials over the value
+// heads of the key head and the 4 column blocks, then applies the normalisations' backward.
+template <typename T>
+__global__ void __launch_bounds__(kD) backward_reduce_kernel(BackwardArgs a, Workspace w) {
+  __shared__ float red[4][4];
+  const size_t bt = blockIdx.x;          // b L + t
+  const int hk = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = a.Hv / a.Hk;
+  float dqt = 0.f, dkh = 0.f;
+  for (int j = 0; j < r; ++j) {
+    const size_t base = (bt * a.Hv + (size_t)hk * r + j) * 4 * kD + tid;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) { dqt += w.pq[base + c * kD]; dkh += w.pk[base + c * kD]; }
+  }
+  const size_t off = (bt * a.Hk + hk) * kD + tid;
+  const float qv = ld_in(static_cast<const T*>(a.q) + off), kv = ld_in(static_cast<const T*>(a.k) + off);
+  float s[4] = {qv * qv, qv * dqt, kv * kv, kv * dkh};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s[j] += __shfl_xor_sync(0xffffffffu, s[j], o);
+    if (lane == 0) red[warp][j] = s[j];
+  }
+  __syncthreads();
+  float tot[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) tot[j] = red[0][j] + red[1][j] + red[2][j] + red[3][j];
+  const float sq = rsqrtf(tot[0] + 1e-6f), sk = rsqrtf(tot[2] + 1e-6f);
+  a.dq[off] = kScale * (sq * dqt - sq * sq * sq * tot[1] * qv);
+  a.dk[off] = sk * dkh - sk * sk * sk * tot[3] * kv;
+  for (int j = tid; j < r; j += kD) {
+    const size_t tv = bt * a.Hv + (size_t)hk * r + j;
+    a.dg[tv] = w.pg[tv * 4] + w.pg[tv * 4 + 1] + w.pg[tv * 4 + 2] + w.pg[tv * 4 + 3];
+    a.dbeta[tv] = w.pb[tv * 4] + w.pb[tv * 4 + 1] + w.pb[tv * 4 + 2] + w.pb[tv * 4 + 3];
+  }
+}
+
+}  // namespace
+
+size_t backward_workspace_bytes(int B, int L, int Hk, int Hv) {
+  (void)Hk;
+  const size_t nCta = 4 * (size_t)B * Hv;
+  const size_t nSeg = ((size_t)L + kBwdSeg - 1) / kBwdSeg;
+  const size_t tokens = (size_t)B * L * Hv;
+  return sizeof(float) * (nCta * (nSeg + kBwdSeg) * kSlice + tokens * 4 * (2 * kD + 2));
+}
+
+cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s) {
+  const Workspace w = carve(a.ws, a.B, a.L, a.Hv);
+  const dim3 grid((unsigned)(4 * a.B), (unsigned)a.Hv);
+  int slot = stage_timer_begin(s, kKernBackward);
+  if (a.bf16)
+    backward_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(a, w);
+  else
+    backward_kernel<float><<<grid, kThreads, 0, s>>>(a, w);
+  stage_timer_end(slot, s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const dim3 grid2((unsigned)((size_t)a.B * a.L), (unsigned)a.Hk);
+  slot = stage_timer_begin(s, kKernBackwardReduce);
+  if (a.bf16)
+    backward_reduce_kernel<__nv_bfloat16><<<grid2, kD, 0, s>>>(a, w);
+  else
+    backward_reduce_kernel<float><<<grid2, kD, 0, s>>>(a, w);
+  stage_timer_end(slot, s);
+  return cudaGetLastError();
+}
+
+}  // namespace gdr

@@ -83,6 +83,16 @@ def regime(name: str, L: int, seed: int, Hk: int = 16, Hv: int = 32, Dk: int = D
                      {"regime": name, "seed": seed})
 
 
+def upstream_grads(B: int, L: int, Hv: int, seed: int, dtype: torch.dtype = torch.float32, Dk: int = D,
+                   with_dS_T: bool = True):
+    """Seeded upstream gradients for the backward: dO ~ N(0, 1) [B, L, Hv, D] in ``dtype`` and
+    dS_T ~ 0.1 N(0, 1) [B, Hv, D, D] float32 (None when ``with_dS_T`` is False)."""
+    gen = torch.Generator().manual_seed(seed)
+    dO = torch.randn(B, L, Hv, Dk, generator=gen).to(dtype)
+    dS_T = 0.1 * torch.randn(B, Hv, Dk, Dk, generator=gen) if with_dS_T else None
+    return dO, dS_T
+
+
 # ---------------------------------------------------------------------------------------------
 # The five workloads (single row fp32, padded fp32 regimes, 4B prefill, 0.8B long prefill, forks)
 # ---------------------------------------------------------------------------------------------

@@ -183,6 +183,37 @@ gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w
 gdr_status gdr_gated_rmsnorm(const void* x, const void* z, const float* w, float eps, void* out,
                              long long rows, int D, gdr_stream_t stream);
 
+/*
+ * Backward of gdr_chunk_fwd: the gradients of a loss with respect to every input, given its
+ * gradients dO of the outputs o and dS_T of the final state. The pages train through the
+ * recurrence (DEG "model.py", delta_rule_reference inside the training loss; Kev-4B-LiteRT
+ * "r15_kernel_test.py", truth_f64) but print no backward; this is the plain reverse of the
+ * forward stated at the top of this header, token by token:
+ *   dq~ = S_t dO_t;  dS += q~ dO_t^T;  dk^ = dS delta;  ddelta = dS^T k^;  dbeta = ddelta . (v - kv);
+ *   dv = beta ddelta;  dkv = -beta ddelta;  dS_a = dS + k^ dkv^T;  dk^ += S_a dkv;
+ *   dg = <S_a, dS_a>;  dS = exp(g_t) dS_a
+ * (S_a = exp(g_t) S_{t-1}, kv = S_a^T k^), from dS = dS_T at the last token; dS0 is the last dS;
+ * dq and dk are taken back through the normalisations and summed over the value heads of a key
+ * head. Pads are tokens like any other (their dv is 0 because beta = 0).
+ *   q, k, v, g, beta, S0     as for gdr_chunk_fwd (S0 NULL = zeros)
+ *   dO     [B, L, Hv, D]  dt        gradient of o
+ *   dS_T   [B, Hv, D, D]  float32   gradient of the final state; NULL = zeros
+ *   dq, dk [B, L, Hk, D]  float32;  dv [B, L, Hv, D] float32;  dg, dbeta [B, L, Hv] float32
+ *   dS0    [B, Hv, D, D]  float32   gradient of S0; NULL = not written
+ *   ws     workspace of at least gdr_backward_workspace_bytes(...) bytes (never NULL), owned by
+ *          the caller: state checkpoints every 32 tokens, one 32-token segment of states per
+ *          (row, value head, 32-column block), and the per-column-block partial sums
+ * The outputs must not overlap the inputs or one another. Arithmetic is float32 throughout (the
+ * states are recomputed from checkpoints by the forward's own float32 recurrence), and the sums
+ * over column blocks and value heads run in a fixed order: the result is deterministic.
+ * B <= 65535 and B L < 2^31 (GDR_ERR_UNSUPPORTED otherwise).
+ */
+size_t gdr_backward_workspace_bytes(int B, int L, int Hk, int Hv, int D);
+gdr_status gdr_backward(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                        const float* S0, const void* dO, const float* dS_T, float* dq, float* dk,
+                        float* dv, float* dg, float* dbeta, float* dS0, int B, int L, int Hk, int Hv,
+                        int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream);
+
 /* Synchronise `stream`, then read and clear the sticky device error word of the current device. */
 gdr_status gdr_sync_status(gdr_stream_t stream);
 

@@ -154,3 +154,41 @@ def test_gated_rmsnorm_rejects_bad_arguments(L):
     # out may be x itself, but not a shifted view of it
     assert f(P, Q, P, 1e-6, ctypes.c_void_p((1 << 20) + 256), 4, 128, None) == gdr.GDR_ERR_INVALID_ARG
     assert b"overlaps" in L.gdr_last_error_message()
+
+
+def _bwd(L, q=P, dO=P, dq=P, dg=P, S0=None, dS0=None, B=1, Lt=64, Hk=2, Hv=4, D=128, dt=1, ws=P, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = L.gdr_backward_workspace_bytes(B, Lt, Hk, Hv, 128)
+    return L.gdr_backward(q, P, P, P, P, S0, dO, None, dq, P, P, dg, P, dS0, B, Lt, Hk, Hv, D, dt, ws, ws_bytes, None)
+
+
+def test_backward_rejects_bad_arguments(L):
+    assert _bwd(L, dO=None) == gdr.GDR_ERR_INVALID_ARG
+    assert b"dO" in L.gdr_last_error_message()
+    assert _bwd(L, q=None) == gdr.GDR_ERR_INVALID_ARG
+    assert _bwd(L, dq=None) == gdr.GDR_ERR_INVALID_ARG
+    assert b"dq" in L.gdr_last_error_message()
+    assert _bwd(L, Hk=3, Hv=4) == gdr.GDR_ERR_INVALID_ARG
+    assert _bwd(L, D=64) == gdr.GDR_ERR_UNSUPPORTED
+    assert _bwd(L, dt=5) == gdr.GDR_ERR_INVALID_ARG
+    assert _bwd(L, dg=BAD) == gdr.GDR_ERR_INVALID_ARG
+    assert b"aligned" in L.gdr_last_error_message()
+    assert _bwd(L, dS0=BAD) == gdr.GDR_ERR_INVALID_ARG
+    assert _bwd(L, B=65536, ws_bytes=1 << 62) == gdr.GDR_ERR_UNSUPPORTED
+    assert _bwd(L, B=2, Lt=1 << 30, ws_bytes=1 << 62) == gdr.GDR_ERR_UNSUPPORTED
+    need = L.gdr_backward_workspace_bytes(1, 64, 2, 4, 128)
+    assert _bwd(L, ws_bytes=need - 1) == gdr.GDR_ERR_INVALID_ARG
+    assert b"workspace" in L.gdr_last_error_message()
+    assert _bwd(L, ws=None) == gdr.GDR_ERR_INVALID_ARG
+
+
+def test_backward_workspace_query(L):
+    assert L.gdr_backward_workspace_bytes(1, 64, 2, 4, 64) == 0
+    assert L.gdr_backward_workspace_bytes(1, 64, 3, 4, 128) == 0
+    assert L.gdr_backward_workspace_bytes(0, 64, 2, 4, 128) == 0
+    # checkpoints (ceil(L/32) slices) + one segment (32 slices) per (row, value head, column block),
+    # a slice being 128 x 32 floats, then the partials: 4 column blocks x (2 D + 2) floats per token
+    for B, Lt, Hv in ((1, 64, 4), (2, 70, 8), (1, 4096, 32)):
+        n_seg = -(-Lt // 32)
+        want = 4 * (4 * B * Hv * (n_seg + 32) * 128 * 32 + B * Lt * Hv * 4 * (2 * 128 + 2))
+        assert L.gdr_backward_workspace_bytes(B, Lt, 2, Hv, 128) == want
