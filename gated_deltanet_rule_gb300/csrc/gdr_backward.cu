@@ -67,17 +67,23 @@ Workspace carve(void* ws, int B, int L, int Hv) {
   return w;
 }
 
+// One segment's inputs are staged here by a cooperative load (one memory latency per segment
+// instead of one per token); the forward over the segment then rewrites q and k in place (each
+// thread its own element) with q~ and k^ for the reverse.
 struct BwdSmem {
-  float qs[2][kD], ks[2][kD], vs[2][kCols];
+  float qt[kBwdSeg][kD];        // raw q, then q~
+  float kh[kBwdSeg][kD];        // raw k, then k^
+  float vseg[kBwdSeg][kCols];   // v (this CTA's columns)
+  float dOseg[kBwdSeg][kCols];  // dO (this CTA's columns)
+  float vm[kBwdSeg][kCols];     // v - kv
+  float gseg[kBwdSeg], bseg[kBwdSeg], es[kBwdSeg];
+  float ks[2][kD];              // raw k of the token in flight, read by every thread
   float nred[2][4][2];          // per-warp partials of q.q, k.k
   float red[2][4][8][4];        // per-warp column partials of S^T k
-  float qt[kBwdSeg][kD];        // q~ of the segment's tokens
-  float kh[kBwdSeg][kD];        // k^
-  float vm[kBwdSeg][kCols];     // v - kv
-  float es[kBwdSeg], bs[kBwdSeg];
   float cred[2][4][8][4];       // per-warp column partials of dS^T k^
   float gred[2][4];             // per-warp partials of <S_{t-1}, dS_a>
 };
+static_assert(sizeof(BwdSmem) <= 48 * 1024, "static shared memory limit");
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Workspace w) {
@@ -110,16 +116,33 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
     S[m][0] = x.x; S[m][1] = x.y; S[m][2] = x.z; S[m][3] = x.w;
   }
 
-  // One forward token, S_{t-1} -> S_t. With rec, keeps what the reverse needs of token t in
-  // slot i: S_{t-1} (thread-private, workspace), q~, k^, v - kv, e and beta (shared memory).
-  auto forward_token = [&](int t, int buf, bool rec, int i) {
-    const size_t qk_off = ((row_tok + t) * a.Hk + hk) * kD + tid;
-    const float qv = ld_in(q + qk_off), kv = ld_in(k + qk_off);
-    const float gt = __ldg(a.g + (row_tok + t) * a.Hv + h);
-    const float bt = __ldg(a.beta + (row_tok + t) * a.Hv + h);
-    sm.qs[buf][tid] = qv;
+  // Stages tokens [t0, t0 + n) of this CTA's inputs (dO too with with_dO) in shared memory.
+  auto load_segment = [&](int t0, int n, bool with_dO) {
+#pragma unroll 8
+    for (int i = 0; i < n; ++i) {
+      const size_t qk_off = ((row_tok + t0 + i) * a.Hk + hk) * kD + tid;
+      sm.qt[i][tid] = ld_in(q + qk_off);
+      sm.kh[i][tid] = ld_in(k + qk_off);
+    }
+    for (int j = tid; j < n * kCols; j += kThreads) {
+      const int i = j / kCols, c = j % kCols;
+      const size_t off = ((row_tok + t0 + i) * a.Hv + h) * kD + cb * kCols + c;
+      sm.vseg[i][c] = ld_in(v + off);
+      if (with_dO) sm.dOseg[i][c] = ld_in(dO + off);
+    }
+    if (tid < n) {
+      sm.gseg[tid] = __ldg(a.g + (row_tok + t0 + tid) * a.Hv + h);
+      sm.bseg[tid] = __ldg(a.beta + (row_tok + t0 + tid) * a.Hv + h);
+    }
+    __syncthreads();
+  };
+
+  // One forward token of the staged segment, S_{t-1} -> S_t. With rec, keeps what the reverse
+  // needs in slot i: S_{t-1} (thread-private, workspace), q~, k^, v - kv and e (shared memory).
+  auto forward_token = [&](int i, int buf, bool rec) {
+    const float qv = sm.qt[i][tid], kv = sm.kh[i][tid];
+    const float gt = sm.gseg[i], bt = sm.bseg[i];
     sm.ks[buf][tid] = kv;
-    if (tid < kCols) sm.vs[buf][tid] = ld_in(v + ((row_tok + t) * a.Hv + h) * kD + cb * kCols + tid);
     float s0 = qv * qv, s1 = kv * kv;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -156,14 +179,14 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const float fk = sm.red[buf][0][cg][c] + sm.red[buf][1][cg][c] + sm.red[buf][2][cg][c] + sm.red[buf][3][cg][c];
-      const float vmc = sm.vs[buf][4 * cg + c] - ekinv * fk;
+      const float vmc = sm.vseg[i][4 * cg + c] - ekinv * fk;
       delta[c] = bt * vmc;
       if (rec && rg == 0) sm.vm[i][4 * cg + c] = vmc;
     }
     if (rec) {
       sm.qt[i][tid] = qv * (qinv * kScale);
       sm.kh[i][tid] = kinv * kv;
-      if (tid == 0) { sm.es[i] = e; sm.bs[i] = bt; }
+      if (tid == 0) sm.es[i] = e;
 #pragma unroll
       for (int m = 0; m < 8; ++m) tk[(size_t)(i * 8 + m) * kThreads + tid] = make_float4(S[m][0], S[m][1], S[m][2], S[m][3]);
     }
@@ -180,7 +203,9 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
 #pragma unroll
     for (int m = 0; m < 8; ++m) ck[(size_t)(seg * 8 + m) * kThreads + tid] = make_float4(S[m][0], S[m][1], S[m][2], S[m][3]);
     if (seg == nSeg - 1) break;
-    for (int i = 0; i < kBwdSeg; ++i) forward_token(seg * kBwdSeg + i, i & 1, false, 0);
+    __syncthreads();    // the previous segment is done with the staged inputs
+    load_segment(seg * kBwdSeg, kBwdSeg, false);
+    for (int i = 0; i < kBwdSeg; ++i) forward_token(i, i & 1, false);
   }
 
   float dS[8][4];
@@ -203,21 +228,23 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
   };
 
   // One reverse token: dS (adjoint of S_t) -> adjoint of S_{t-1}, from slot i.
+  // Sp holds S_{t-1} of the token being reversed; the next one's is fetched while it runs.
+  float Sp[8][4];
+  auto load_sp = [&](int i, float4 (&x)[8]) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) x[m] = tk[(size_t)(i * 8 + m) * kThreads + tid];
+  };
   auto backward_token = [&](int t, int buf, int i) {
     const size_t tv = (row_tok + t) * a.Hv + h;
+    float4 nxt[8];
+    if (i > 0) load_sp(i - 1, nxt);
     float dOc[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) dOc[c] = ld_in(dO + tv * kD + col0 + c);
-    const float e = sm.es[i], bt = sm.bs[i];
+    for (int c = 0; c < 4; ++c) dOc[c] = sm.dOseg[i][4 * cg + c];
+    const float e = sm.es[i], bt = sm.bseg[i];
     float vmc[4], dl[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) { vmc[c] = sm.vm[i][4 * cg + c]; dl[c] = bt * vmc[c]; }
-    float Sp[8][4];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float4 x = tk[(size_t)(i * 8 + m) * kThreads + tid];
-      Sp[m][0] = x.x; Sp[m][1] = x.y; Sp[m][2] = x.z; Sp[m][3] = x.w;
-    }
     float dqr[8], dkr[8];
     float dcol[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -298,6 +325,10 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
     pend_tv = tv;
     pend_buf = buf;
     pend_e = e;
+    if (i > 0) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) { Sp[m][0] = nxt[m].x; Sp[m][1] = nxt[m].y; Sp[m][2] = nxt[m].z; Sp[m][3] = nxt[m].w; }
+    }
   };
 
   // Pass 2: segments last to first, each recomputed forward, then reversed.
@@ -310,8 +341,15 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
       S[m][0] = x.x; S[m][1] = x.y; S[m][2] = x.z; S[m][3] = x.w;
     }
     __syncthreads();    // the previous segment's reverse is done with the shared arrays
-    for (int i = 0; i < n; ++i) forward_token(t0 + i, i & 1, true, i);
+    load_segment(t0, n, true);
+    for (int i = 0; i < n; ++i) forward_token(i, i & 1, true);
     __syncthreads();    // the segment's records are complete
+    {
+      float4 x[8];
+      load_sp(n - 1, x);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) { Sp[m][0] = x[m].x; Sp[m][1] = x[m].y; Sp[m][2] = x[m].z; Sp[m][3] = x[m].w; }
+    }
     for (int i = n - 1; i >= 0; --i) backward_token(t0 + i, i & 1, i);
     __syncthreads();
     flush_dg();
