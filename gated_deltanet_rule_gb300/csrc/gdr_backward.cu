@@ -68,8 +68,8 @@ Workspace carve(void* ws, int B, int L, int Hv) {
 }
 
 // One segment's inputs are staged here by a cooperative load (one memory latency per segment
-// instead of one per token); the forward over the segment then rewrites q and k in place (each
-// thread its own element) with q~ and k^ for the reverse.
+// instead of one per token), and normalised there once (a warp per token), so the token steps
+// read q~, k^ and e ready-made.
 struct BwdSmem {
   float qt[kBwdSeg][kD];        // raw q, then q~
   float kh[kBwdSeg][kD];        // raw k, then k^
@@ -77,9 +77,7 @@ struct BwdSmem {
   float dOseg[kBwdSeg][kCols];  // dO (this CTA's columns)
   float vm[kBwdSeg][kCols];     // v - kv
   float gseg[kBwdSeg], bseg[kBwdSeg], es[kBwdSeg];
-  float ks[2][kD];              // raw k of the token in flight, read by every thread
-  float nred[2][4][2];          // per-warp partials of q.q, k.k
-  float red[2][4][8][4];        // per-warp column partials of S^T k
+  float red[2][4][8][4];        // per-warp column partials of S^T k^
   float cred[2][4][8][4];       // per-warp column partials of dS^T k^
   float gred[2][4];             // per-warp partials of <S_{t-1}, dS_a>
 };
@@ -135,27 +133,40 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
       sm.bseg[tid] = __ldg(a.beta + (row_tok + t0 + tid) * a.Hv + h);
     }
     __syncthreads();
+    // q~ = q (|q|^2 + 1e-6)^-1/2 D^-1/2, k^ = k (|k|^2 + 1e-6)^-1/2, e = exp(g): warp w takes
+    // tokens w, w + 4, ..., each lane four elements
+    for (int i = warp; i < n; i += 4) {
+      float x[4], y[4], sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[j] = sm.qt[i][lane + 32 * j];
+        y[j] = sm.kh[i][lane + 32 * j];
+        sq = fmaf(x[j], x[j], sq);
+        sk = fmaf(y[j], y[j], sk);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+      }
+      const float qs = rsqrtf(sq + 1e-6f) * kScale, kinv = rsqrtf(sk + 1e-6f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        sm.qt[i][lane + 32 * j] = x[j] * qs;
+        sm.kh[i][lane + 32 * j] = y[j] * kinv;
+      }
+      if (lane == 0) sm.es[i] = expf(sm.gseg[i]);
+    }
+    __syncthreads();
   };
 
-  // One forward token of the staged segment, S_{t-1} -> S_t. With rec, keeps what the reverse
-  // needs in slot i: S_{t-1} (thread-private, workspace), q~, k^, v - kv and e (shared memory).
+  // One forward token of the staged segment, S_{t-1} -> S_t (one barrier). With rec, keeps
+  // S_{t-1} (thread-private, workspace) and v - kv (shared memory) for the reverse in slot i.
   auto forward_token = [&](int i, int buf, bool rec) {
-    const float qv = sm.qt[i][tid], kv = sm.kh[i][tid];
-    const float gt = sm.gseg[i], bt = sm.bseg[i];
-    sm.ks[buf][tid] = kv;
-    float s0 = qv * qv, s1 = kv * kv;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      s0 += __shfl_xor_sync(0xffffffffu, s0, off);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, off);
-    }
-    if (lane == 0) { sm.nred[buf][warp][0] = s0; sm.nred[buf][warp][1] = s1; }
-    __syncthreads();
-
     float pk[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      const float kk = sm.ks[buf][rg + 16 * m];
+      const float kk = sm.kh[i][rg + 16 * m];
 #pragma unroll
       for (int c = 0; c < 4; ++c) pk[c] = fmaf(S[m][c], kk, pk[c]);
     }
@@ -170,29 +181,22 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
     }
     __syncthreads();
 
-    const float sqq = sm.nred[buf][0][0] + sm.nred[buf][1][0] + sm.nred[buf][2][0] + sm.nred[buf][3][0];
-    const float skk = sm.nred[buf][0][1] + sm.nred[buf][1][1] + sm.nred[buf][2][1] + sm.nred[buf][3][1];
-    const float qinv = rsqrtf(sqq + 1e-6f), kinv = rsqrtf(skk + 1e-6f);
-    const float e = expf(gt);
-    const float ekinv = e * kinv;
+    const float e = sm.es[i], bt = sm.bseg[i];
     float delta[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const float fk = sm.red[buf][0][cg][c] + sm.red[buf][1][cg][c] + sm.red[buf][2][cg][c] + sm.red[buf][3][cg][c];
-      const float vmc = sm.vseg[i][4 * cg + c] - ekinv * fk;
+      const float vmc = sm.vseg[i][4 * cg + c] - e * fk;
       delta[c] = bt * vmc;
       if (rec && rg == 0) sm.vm[i][4 * cg + c] = vmc;
     }
     if (rec) {
-      sm.qt[i][tid] = qv * (qinv * kScale);
-      sm.kh[i][tid] = kinv * kv;
-      if (tid == 0) sm.es[i] = e;
 #pragma unroll
       for (int m = 0; m < 8; ++m) tk[(size_t)(i * 8 + m) * kThreads + tid] = make_float4(S[m][0], S[m][1], S[m][2], S[m][3]);
     }
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      const float kk = kinv * sm.ks[buf][rg + 16 * m];
+      const float kk = sm.kh[i][rg + 16 * m];
 #pragma unroll
       for (int c = 0; c < 4; ++c) S[m][c] = fmaf(e, S[m][c], kk * delta[c]);
     }
