@@ -16,11 +16,12 @@
 // again from its checkpoint keeping its 32 states, and then in reverse. Both stores are private to
 // the thread that reads them back, so they need no synchronisation.
 //
-// A CTA owns 32 value columns of one (row, value head), the layout of the forward token loop:
-// thread t holds key rows (t/8) + 16m, m = 0..7, and columns 4(t%8)..+3 of both S and dS. The
+// A CTA owns 16 value columns (one of 8 column blocks) of one (row, value head): thread t holds
+// key rows (t/8) + 16m, m = 0..7, and columns 2(t%8), 2(t%8) + 1 of both S and dS. Eight chains
+// per head (two CTAs on most SMs) hide more of each token's latency than four wider ones. The
 // per-column results (dv, dS0) are the CTA's own. The per-key-row ones (dq~, dk^) and the sums
-// over columns (dbeta, dg) are partial over the CTA's 32 columns: they go to the workspace, and a
-// second kernel sums them over the 4 column blocks and the value heads of each key head in a
+// over columns (dbeta, dg) are partial over the CTA's columns: they go to the workspace, and a
+// second kernel sums them over the 8 column blocks and the value heads of each key head in a
 // fixed order (the result does not depend on scheduling), then takes dq~ and dk^ back through the
 // normalisations, dx = s dx^ - s^3 (x . dx^) x with s = (|x|^2 + 1e-6)^-1/2 (and D^-1/2 for q).
 #include <cuda_bf16.h>
@@ -31,18 +32,38 @@
 namespace gdr {
 namespace {
 
-constexpr int kCols = 32;                 // value columns per CTA
+constexpr int kNcb = kBwdColBlocks;       // CTAs per (row, value head)
+constexpr int kCols = kD / kNcb;          // value columns per CTA
+constexpr int kCpt = kCols / 8;           // value columns per thread
 constexpr int kThreads = 128;
 constexpr int kSlice = kD * kCols;        // floats of one CTA's state slice
 constexpr float kScale = 0.08838834764831845f;   // 128^-0.5
+static_assert(kCpt == 2 || kCpt == 4, "a thread holds 2 or 4 adjacent value columns");
 
 __device__ __forceinline__ float ld_in(const float* p) { return __ldg(p); }
 __device__ __forceinline__ float ld_in(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
+// kCpt adjacent floats as one vector access (p aligned to kCpt floats)
+__device__ __forceinline__ void ld_vec(const float* p, float (&x)[kCpt]) {
+  if constexpr (kCpt == 4) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+  } else {
+    const float2 u = *reinterpret_cast<const float2*>(p);
+    x[0] = u.x; x[1] = u.y;
+  }
+}
+__device__ __forceinline__ void st_vec(float* p, const float (&x)[kCpt]) {
+  if constexpr (kCpt == 4)
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  else
+    *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+}
+
 // Workspace carve-up (floats): checkpoints [cta][segment][slice], segment states
-// [cta][kBwdSeg][slice], then the partials dq~, dk^ [B L Hv][4][kD] and dg, dbeta [B L Hv][4].
-// A slice is stored as [m][thread] float4, so slot s of thread t's m-th float4 is
-// (s * 8 + m) * kThreads + t.
+// [cta][kBwdSeg][slice], then the partials dq~, dk^ [B L Hv][kNcb][kD] and dg, dbeta
+// [B L Hv][kNcb]. A slice is stored as [m][thread][kCpt], so thread t's m-th vector of slot s
+// starts at float ((s * 8 + m) * kThreads + t) * kCpt.
 struct Workspace {
   float* ckpt;
   float* tok;
@@ -53,16 +74,16 @@ struct Workspace {
 };
 
 Workspace carve(void* ws, int B, int L, int Hv) {
-  const size_t nCta = 4 * (size_t)B * Hv;
+  const size_t nCta = (size_t)kNcb * B * Hv;
   const size_t nSeg = ((size_t)L + kBwdSeg - 1) / kBwdSeg;
   const size_t tokens = (size_t)B * L * Hv;
   float* p = static_cast<float*>(ws);
   Workspace w;
   w.ckpt = p; p += nCta * nSeg * kSlice;
   w.tok = p;  p += nCta * kBwdSeg * kSlice;
-  w.pq = p;   p += tokens * 4 * kD;
-  w.pk = p;   p += tokens * 4 * kD;
-  w.pg = p;   p += tokens * 4;
+  w.pq = p;   p += tokens * kNcb * kD;
+  w.pk = p;   p += tokens * kNcb * kD;
+  w.pg = p;   p += tokens * kNcb;
   w.pb = p;
   return w;
 }
@@ -77,17 +98,18 @@ struct BwdSmem {
   float dOseg[kBwdSeg][kCols];  // dO (this CTA's columns)
   float vm[kBwdSeg][kCols];     // v - kv
   float gseg[kBwdSeg], bseg[kBwdSeg], es[kBwdSeg];
-  float red[2][4][8][4];        // per-warp column partials of S^T k^
-  float cred[2][4][8][4];       // per-warp column partials of dS^T k^
+  float red[2][4][8][kCpt];     // per-warp column partials of S^T k^
+  float cred[2][4][8][kCpt];    // per-warp column partials of dS^T k^
   float gred[2][4];             // per-warp partials of <S_{t-1}, dS_a>
 };
 static_assert(sizeof(BwdSmem) <= 48 * 1024, "static shared memory limit");
 
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Workspace w) {
   __shared__ BwdSmem sm;
-  const int cb = blockIdx.x & 3;
-  const int b = blockIdx.x >> 2;
+  const int cb = blockIdx.x % kNcb;
+  const int b = blockIdx.x / kNcb;
   const int h = blockIdx.y;
   const int tid = threadIdx.x;
   const int cg = tid & 7, rg = tid >> 3;
@@ -95,23 +117,28 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
   const int hk = h / (a.Hv / a.Hk);
   const int L = a.L;
   const int nSeg = (L + kBwdSeg - 1) / kBwdSeg;
-  const size_t cta = ((size_t)b * a.Hv + h) * 4 + cb;
-  float4* ck = reinterpret_cast<float4*>(w.ckpt + cta * nSeg * kSlice);
-  float4* tk = reinterpret_cast<float4*>(w.tok + cta * kBwdSeg * kSlice);
+  const size_t cta = ((size_t)b * a.Hv + h) * kNcb + cb;
+  float* ck = w.ckpt + cta * nSeg * kSlice;
+  float* tk = w.tok + cta * kBwdSeg * kSlice;
   const T* q = static_cast<const T*>(a.q);
   const T* k = static_cast<const T*>(a.k);
   const T* v = static_cast<const T*>(a.v);
   const T* dO = static_cast<const T*>(a.dO);
   const size_t row_tok = (size_t)b * L;
-  const int col0 = cb * kCols + 4 * cg;
+  const int col0 = cb * kCols + kCpt * cg;
   const size_t state_off = ((size_t)b * a.Hv + h) * kD * kD;
+  // thread-private vector m of slot s in a checkpoint or segment-state array
+  auto slot = [&](float* base, int s, int m) { return base + ((size_t)(s * 8 + m) * kThreads + tid) * kCpt; };
 
-  float S[8][4];
+  float S[8][kCpt];
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (a.S0) x = __ldg(reinterpret_cast<const float4*>(a.S0 + state_off + (size_t)(rg + 16 * m) * kD + col0));
-    S[m][0] = x.x; S[m][1] = x.y; S[m][2] = x.z; S[m][3] = x.w;
+    if (a.S0) {
+      ld_vec(a.S0 + state_off + (size_t)(rg + 16 * m) * kD + col0, S[m]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < kCpt; ++c) S[m][c] = 0.f;
+    }
   }
 
   // Stages tokens [t0, t0 + n) of this CTA's inputs (dO too with with_dO) in shared memory.
@@ -163,61 +190,66 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
   // One forward token of the staged segment, S_{t-1} -> S_t (one barrier). With rec, keeps
   // S_{t-1} (thread-private, workspace) and v - kv (shared memory) for the reverse in slot i.
   auto forward_token = [&](int i, int buf, bool rec) {
-    float pk[4] = {0.f, 0.f, 0.f, 0.f};
+    float pk[kCpt];
+#pragma unroll
+    for (int c = 0; c < kCpt; ++c) pk[c] = 0.f;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const float kk = sm.kh[i][rg + 16 * m];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) pk[c] = fmaf(S[m][c], kk, pk[c]);
+      for (int c = 0; c < kCpt; ++c) pk[c] = fmaf(S[m][c], kk, pk[c]);
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < kCpt; ++c) {
       pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], 8);
       pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], 16);
     }
     if (lane < 8) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) sm.red[buf][warp][lane][c] = pk[c];
+      for (int c = 0; c < kCpt; ++c) sm.red[buf][warp][lane][c] = pk[c];
     }
     __syncthreads();
 
     const float e = sm.es[i], bt = sm.bseg[i];
-    float delta[4];
+    float delta[kCpt];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < kCpt; ++c) {
       const float fk = sm.red[buf][0][cg][c] + sm.red[buf][1][cg][c] + sm.red[buf][2][cg][c] + sm.red[buf][3][cg][c];
-      const float vmc = sm.vseg[i][4 * cg + c] - e * fk;
+      const float vmc = sm.vseg[i][kCpt * cg + c] - e * fk;
       delta[c] = bt * vmc;
-      if (rec && rg == 0) sm.vm[i][4 * cg + c] = vmc;
+      if (rec && rg == 0) sm.vm[i][kCpt * cg + c] = vmc;
     }
     if (rec) {
 #pragma unroll
-      for (int m = 0; m < 8; ++m) tk[(size_t)(i * 8 + m) * kThreads + tid] = make_float4(S[m][0], S[m][1], S[m][2], S[m][3]);
+      for (int m = 0; m < 8; ++m) st_vec(slot(tk, i, m), S[m]);
     }
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const float kk = sm.kh[i][rg + 16 * m];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) S[m][c] = fmaf(e, S[m][c], kk * delta[c]);
+      for (int c = 0; c < kCpt; ++c) S[m][c] = fmaf(e, S[m][c], kk * delta[c]);
     }
   };
 
   // Pass 1: checkpoints at every segment start (the last segment's tokens are not needed).
   for (int seg = 0; seg < nSeg; ++seg) {
 #pragma unroll
-    for (int m = 0; m < 8; ++m) ck[(size_t)(seg * 8 + m) * kThreads + tid] = make_float4(S[m][0], S[m][1], S[m][2], S[m][3]);
+    for (int m = 0; m < 8; ++m) st_vec(slot(ck, seg, m), S[m]);
     if (seg == nSeg - 1) break;
     __syncthreads();    // the previous segment is done with the staged inputs
     load_segment(seg * kBwdSeg, kBwdSeg, false);
     for (int i = 0; i < kBwdSeg; ++i) forward_token(i, i & 1, false);
   }
 
-  float dS[8][4];
+  float dS[8][kCpt];
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (a.dS_T) x = __ldg(reinterpret_cast<const float4*>(a.dS_T + state_off + (size_t)(rg + 16 * m) * kD + col0));
-    dS[m][0] = x.x; dS[m][1] = x.y; dS[m][2] = x.z; dS[m][3] = x.w;
+    if (a.dS_T) {
+      ld_vec(a.dS_T + state_off + (size_t)(rg + 16 * m) * kD + col0, dS[m]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < kCpt; ++c) dS[m][c] = 0.f;
+    }
   }
 
   // dg of a token is written by thread 0 once the next barrier has passed (pending until then).
@@ -227,36 +259,36 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
   float pend_e = 0.f;
   auto flush_dg = [&]() {
     if (pend && tid == 0)
-      w.pg[pend_tv * 4 + cb] = pend_e * (sm.gred[pend_buf][0] + sm.gred[pend_buf][1] + sm.gred[pend_buf][2] + sm.gred[pend_buf][3]);
+      w.pg[pend_tv * kNcb + cb] = pend_e * (sm.gred[pend_buf][0] + sm.gred[pend_buf][1] + sm.gred[pend_buf][2] + sm.gred[pend_buf][3]);
     pend = false;
   };
 
   // One reverse token: dS (adjoint of S_t) -> adjoint of S_{t-1}, from slot i.
   // Sp holds S_{t-1} of the token being reversed; the next one's is fetched while it runs.
-  float Sp[8][4];
-  auto load_sp = [&](int i, float4 (&x)[8]) {
-#pragma unroll
-    for (int m = 0; m < 8; ++m) x[m] = tk[(size_t)(i * 8 + m) * kThreads + tid];
-  };
+  float Sp[8][kCpt];
   auto backward_token = [&](int t, int buf, int i) {
     const size_t tv = (row_tok + t) * a.Hv + h;
-    float4 nxt[8];
-    if (i > 0) load_sp(i - 1, nxt);
-    float dOc[4];
+    float nxt[8][kCpt];
+    if (i > 0) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) dOc[c] = sm.dOseg[i][4 * cg + c];
+      for (int m = 0; m < 8; ++m) ld_vec(slot(tk, i - 1, m), nxt[m]);
+    }
     const float e = sm.es[i], bt = sm.bseg[i];
-    float vmc[4], dl[4];
+    float dOc[kCpt], vmc[kCpt], dl[kCpt], dcol[kCpt];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) { vmc[c] = sm.vm[i][4 * cg + c]; dl[c] = bt * vmc[c]; }
+    for (int c = 0; c < kCpt; ++c) {
+      dOc[c] = sm.dOseg[i][kCpt * cg + c];
+      vmc[c] = sm.vm[i][kCpt * cg + c];
+      dl[c] = bt * vmc[c];
+      dcol[c] = 0.f;
+    }
     float dqr[8], dkr[8];
-    float dcol[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const float qr = sm.qt[i][rg + 16 * m], kr = sm.kh[i][rg + 16 * m];
       float aq = 0.f, ak = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kCpt; ++c) {
         const float st = fmaf(e, Sp[m][c], kr * dl[c]);     // S_t, as the forward formed it
         aq = fmaf(st, dOc[c], aq);
         dS[m][c] = fmaf(qr, dOc[c], dS[m][c]);
@@ -267,46 +299,46 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
       dkr[m] = ak;
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < kCpt; ++c) {
       dcol[c] += __shfl_xor_sync(0xffffffffu, dcol[c], 8);
       dcol[c] += __shfl_xor_sync(0xffffffffu, dcol[c], 16);
     }
     if (lane < 8) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) sm.cred[buf][warp][lane][c] = dcol[c];
+      for (int c = 0; c < kCpt; ++c) sm.cred[buf][warp][lane][c] = dcol[c];
     }
     __syncthreads();
     flush_dg();
 
-    float ddl[4], dkv[4];
+    float ddl[kCpt], dkv[kCpt], dvv[kCpt];
+    float xb = 0.f;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < kCpt; ++c) {
       ddl[c] = sm.cred[buf][0][cg][c] + sm.cred[buf][1][cg][c] + sm.cred[buf][2][cg][c] + sm.cred[buf][3][cg][c];
       dkv[c] = -bt * ddl[c];
+      dvv[c] = bt * ddl[c];
+      xb = fmaf(ddl[c], vmc[c], xb);
     }
     // dbeta: lanes 0..7 of warp 0 hold the 8 column groups
-    float xb = ddl[0] * vmc[0] + ddl[1] * vmc[1] + ddl[2] * vmc[2] + ddl[3] * vmc[3];
     xb += __shfl_xor_sync(0xffffffffu, xb, 1);
     xb += __shfl_xor_sync(0xffffffffu, xb, 2);
     xb += __shfl_xor_sync(0xffffffffu, xb, 4);
-    if (tid == 0) w.pb[tv * 4 + cb] = xb;
-    if (rg == 0)
-      *reinterpret_cast<float4*>(a.dv + tv * kD + col0) = make_float4(bt * ddl[0], bt * ddl[1], bt * ddl[2], bt * ddl[3]);
+    if (tid == 0) w.pb[tv * kNcb + cb] = xb;
+    if (rg == 0) st_vec(a.dv + tv * kD + col0, dvv);
 
-    float gp = 0.f;
+    float gp[2] = {0.f, 0.f};
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const float kr = sm.kh[i][rg + 16 * m];
       float a2 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kCpt; ++c) {
         a2 = fmaf(Sp[m][c], dkv[c], a2);
         dS[m][c] = fmaf(kr, dkv[c], dS[m][c]);               // dS_a
-        gp = fmaf(Sp[m][c], dS[m][c], gp);
+        gp[m & 1] = fmaf(Sp[m][c], dS[m][c], gp[m & 1]);
+        dS[m][c] *= e;
       }
       dkr[m] = fmaf(e, a2, dkr[m]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) dS[m][c] *= e;
     }
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
@@ -317,21 +349,25 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
       }
     }
     if (cg == 0) {
-      float* pq = w.pq + (tv * 4 + cb) * kD;
-      float* pk = w.pk + (tv * 4 + cb) * kD;
+      float* pq = w.pq + (tv * kNcb + cb) * kD;
+      float* pk = w.pk + (tv * kNcb + cb) * kD;
 #pragma unroll
       for (int m = 0; m < 8; ++m) { pq[rg + 16 * m] = dqr[m]; pk[rg + 16 * m] = dkr[m]; }
     }
+    float g2 = gp[0] + gp[1];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) gp += __shfl_xor_sync(0xffffffffu, gp, off);
-    if (lane == 0) sm.gred[buf][warp] = gp;
+    for (int off = 16; off > 0; off >>= 1) g2 += __shfl_xor_sync(0xffffffffu, g2, off);
+    if (lane == 0) sm.gred[buf][warp] = g2;
     pend = true;
     pend_tv = tv;
     pend_buf = buf;
     pend_e = e;
     if (i > 0) {
 #pragma unroll
-      for (int m = 0; m < 8; ++m) { Sp[m][0] = nxt[m].x; Sp[m][1] = nxt[m].y; Sp[m][2] = nxt[m].z; Sp[m][3] = nxt[m].w; }
+      for (int m = 0; m < 8; ++m) {
+#pragma unroll
+        for (int c = 0; c < kCpt; ++c) Sp[m][c] = nxt[m][c];
+      }
     }
   };
 
@@ -340,20 +376,13 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
     const int t0 = seg * kBwdSeg;
     const int n = min(kBwdSeg, L - t0);
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float4 x = ck[(size_t)(seg * 8 + m) * kThreads + tid];
-      S[m][0] = x.x; S[m][1] = x.y; S[m][2] = x.z; S[m][3] = x.w;
-    }
+    for (int m = 0; m < 8; ++m) ld_vec(slot(ck, seg, m), S[m]);
     __syncthreads();    // the previous segment's reverse is done with the shared arrays
     load_segment(t0, n, true);
     for (int i = 0; i < n; ++i) forward_token(i, i & 1, true);
     __syncthreads();    // the segment's records are complete
-    {
-      float4 x[8];
-      load_sp(n - 1, x);
 #pragma unroll
-      for (int m = 0; m < 8; ++m) { Sp[m][0] = x[m].x; Sp[m][1] = x[m].y; Sp[m][2] = x[m].z; Sp[m][3] = x[m].w; }
-    }
+    for (int m = 0; m < 8; ++m) ld_vec(slot(tk, n - 1, m), Sp[m]);
     for (int i = n - 1; i >= 0; --i) backward_token(t0 + i, i & 1, i);
     __syncthreads();
     flush_dg();
@@ -361,14 +390,12 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
 
   if (a.dS0) {
 #pragma unroll
-    for (int m = 0; m < 8; ++m)
-      *reinterpret_cast<float4*>(a.dS0 + state_off + (size_t)(rg + 16 * m) * kD + col0) =
-          make_float4(dS[m][0], dS[m][1], dS[m][2], dS[m][3]);
+    for (int m = 0; m < 8; ++m) st_vec(a.dS0 + state_off + (size_t)(rg + 16 * m) * kD + col0, dS[m]);
   }
 }
 
 // One (row, token, key head) per CTA, one key row per thread: sums the partials over the value
-// heads of the key head and the 4 column blocks, then applies the normalisations' backward.
+// heads of the key head and the column blocks, then applies the normalisations' backward.
 template <typename T>
 __global__ void __launch_bounds__(kD) backward_reduce_kernel(BackwardArgs a, Workspace w) {
   __shared__ float red[4][4];
@@ -378,9 +405,9 @@ __global__ void __launch_bounds__(kD) backward_reduce_kernel(BackwardArgs a, Wor
   const int r = a.Hv / a.Hk;
   float dqt = 0.f, dkh = 0.f;
   for (int j = 0; j < r; ++j) {
-    const size_t base = (bt * a.Hv + (size_t)hk * r + j) * 4 * kD + tid;
+    const size_t base = (bt * a.Hv + (size_t)hk * r + j) * kNcb * kD + tid;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) { dqt += w.pq[base + c * kD]; dkh += w.pk[base + c * kD]; }
+    for (int c = 0; c < kNcb; ++c) { dqt += w.pq[base + c * kD]; dkh += w.pk[base + c * kD]; }
   }
   const size_t off = (bt * a.Hk + hk) * kD + tid;
   const float qv = ld_in(static_cast<const T*>(a.q) + off), kv = ld_in(static_cast<const T*>(a.k) + off);
@@ -400,8 +427,11 @@ __global__ void __launch_bounds__(kD) backward_reduce_kernel(BackwardArgs a, Wor
   a.dk[off] = sk * dkh - sk * sk * sk * tot[3] * kv;
   for (int j = tid; j < r; j += kD) {
     const size_t tv = bt * a.Hv + (size_t)hk * r + j;
-    a.dg[tv] = w.pg[tv * 4] + w.pg[tv * 4 + 1] + w.pg[tv * 4 + 2] + w.pg[tv * 4 + 3];
-    a.dbeta[tv] = w.pb[tv * 4] + w.pb[tv * 4 + 1] + w.pb[tv * 4 + 2] + w.pb[tv * 4 + 3];
+    float sg = 0.f, sb = 0.f;
+#pragma unroll
+    for (int c = 0; c < kNcb; ++c) { sg += w.pg[tv * kNcb + c]; sb += w.pb[tv * kNcb + c]; }
+    a.dg[tv] = sg;
+    a.dbeta[tv] = sb;
   }
 }
 
@@ -409,15 +439,15 @@ __global__ void __launch_bounds__(kD) backward_reduce_kernel(BackwardArgs a, Wor
 
 size_t backward_workspace_bytes(int B, int L, int Hk, int Hv) {
   (void)Hk;
-  const size_t nCta = 4 * (size_t)B * Hv;
+  const size_t nCta = (size_t)kNcb * B * Hv;
   const size_t nSeg = ((size_t)L + kBwdSeg - 1) / kBwdSeg;
   const size_t tokens = (size_t)B * L * Hv;
-  return sizeof(float) * (nCta * (nSeg + kBwdSeg) * kSlice + tokens * 4 * (2 * kD + 2));
+  return sizeof(float) * (nCta * (nSeg + kBwdSeg) * kSlice + tokens * kNcb * (2 * kD + 2));
 }
 
 cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s) {
   const Workspace w = carve(a.ws, a.B, a.L, a.Hv);
-  const dim3 grid((unsigned)(4 * a.B), (unsigned)a.Hv);
+  const dim3 grid((unsigned)(kNcb * a.B), (unsigned)a.Hv);
   int slot = stage_timer_begin(s, kKernBackward);
   if (a.bf16)
     backward_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(a, w);

@@ -11,7 +11,8 @@ namespace gdr {
 constexpr int kKernBackward = kKernEpilogue + 1;
 constexpr int kKernBackwardReduce = kKernEpilogue + 2;
 
-constexpr int kBwdSeg = 32;   // tokens per recomputed segment
+constexpr int kBwdSeg = 32;        // tokens per recomputed segment
+constexpr int kBwdColBlocks = 8;   // CTAs per (row, value head), each owning D / 8 value columns
 
 // Reverse mode through the token recurrence. q, k, v, dO share one element type (bf16 or f32);
 // g, beta, S0, dS_T and every gradient are float32. S0 and dS_T may be NULL (zeros), dS0 may be

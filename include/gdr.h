@@ -202,7 +202,7 @@ gdr_status gdr_gated_rmsnorm(const void* x, const void* z, const float* w, float
  *   dS0    [B, Hv, D, D]  float32   gradient of S0; NULL = not written
  *   ws     workspace of at least gdr_backward_workspace_bytes(...) bytes (never NULL), owned by
  *          the caller: state checkpoints every 32 tokens, one 32-token segment of states per
- *          (row, value head, 32-column block), and the per-column-block partial sums
+ *          (row, value head, 16-column block), and the per-column-block partial sums
  * The outputs must not overlap the inputs or one another. Arithmetic is float32 throughout (the
  * states are recomputed from checkpoints by the forward's own float32 recurrence), and the sums
  * over column blocks and value heads run in a fixed order: the result is deterministic.

@@ -187,8 +187,9 @@ def test_backward_workspace_query(L):
     assert L.gdr_backward_workspace_bytes(1, 64, 3, 4, 128) == 0
     assert L.gdr_backward_workspace_bytes(0, 64, 2, 4, 128) == 0
     # checkpoints (ceil(L/32) slices) + one segment (32 slices) per (row, value head, column block),
-    # a slice being 128 x 32 floats, then the partials: 4 column blocks x (2 D + 2) floats per token
+    # 8 column blocks of 16 value columns, a slice being 128 x 16 floats; then the partials:
+    # 8 column blocks x (2 D + 2) floats per token and value head
     for B, Lt, Hv in ((1, 64, 4), (2, 70, 8), (1, 4096, 32)):
         n_seg = -(-Lt // 32)
-        want = 4 * (4 * B * Hv * (n_seg + 32) * 128 * 32 + B * Lt * Hv * 4 * (2 * 128 + 2))
+        want = 4 * (8 * B * Hv * (n_seg + 32) * 128 * 16 + B * Lt * Hv * 8 * (2 * 128 + 2))
         assert L.gdr_backward_workspace_bytes(B, Lt, 2, Hv, 128) == want
