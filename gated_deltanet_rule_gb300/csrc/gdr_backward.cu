@@ -340,19 +340,28 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BackwardArgs a, Work
       }
       dkr[m] = fmaf(e, a2, dkr[m]);
     }
+    // Row sums over the 8 lanes of a column group by recursive halving (xor 4, 2, 1; 14 shuffles
+    // instead of 48): values 0..7 are the dq~ rows rg + 16m, 8..15 the dk^ rows, and lane cg ends
+    // with the sums of values b and b + 1, b = 8 (cg >> 2 & 1) + 4 (cg >> 1 & 1) + 2 (cg & 1).
+    float r16[16];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
+    for (int m = 0; m < 8; ++m) { r16[m] = dqr[m]; r16[8 + m] = dkr[m]; }
 #pragma unroll
-      for (int off = 1; off < 8; off <<= 1) {
-        dqr[m] += __shfl_xor_sync(0xffffffffu, dqr[m], off);
-        dkr[m] += __shfl_xor_sync(0xffffffffu, dkr[m], off);
+    for (int half = 8, bit = 4; half >= 2; half >>= 1, bit >>= 1) {
+      const bool up = (cg & bit) != 0;
+#pragma unroll
+      for (int j = 0; j < half; ++j) {
+        const float send = up ? r16[j] : r16[j + half];
+        const float keep = up ? r16[j + half] : r16[j];
+        r16[j] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
       }
     }
-    if (cg == 0) {
-      float* pq = w.pq + (tv * kNcb + cb) * kD;
-      float* pk = w.pk + (tv * kNcb + cb) * kD;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) { pq[rg + 16 * m] = dqr[m]; pk[rg + 16 * m] = dkr[m]; }
+    {
+      const int b0 = 8 * ((cg >> 2) & 1) + 4 * ((cg >> 1) & 1) + 2 * (cg & 1);
+      float* dst = (b0 < 8 ? w.pq : w.pk) + (tv * kNcb + cb) * kD;
+      const int m0 = b0 & 7;
+      dst[rg + 16 * m0] = r16[0];
+      dst[rg + 16 * (m0 + 1)] = r16[1];
     }
     float g2 = gp[0] + gp[1];
 #pragma unroll
