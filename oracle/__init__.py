@@ -57,8 +57,8 @@ def _f64(x):
     """Widen any array-like (numpy, or a torch CPU tensor of any float dtype) to float64 exactly."""
     if x is None:
         return None
-    if hasattr(x, "detach"):  # torch tensor: bf16 -> float32 -> float64 is exact
-        x = x.detach().cpu().float().numpy()
+    if hasattr(x, "detach"):  # torch tensor of any float dtype: the conversion to float64 is exact
+        x = x.detach().cpu().double().numpy()
     return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
 
 
