@@ -42,7 +42,14 @@ gdr_status ok() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 std::mutex g_err_mu;
-int* g_err_ptr[128] = {};
+// device address of g_error_word per device ordinal, with the context it was looked up in: a
+// symbol's address belongs to the context that loaded the module, so a new context (after
+// cudaDeviceReset, say) needs a new lookup
+struct SymbolCache {
+  void* ctx = nullptr;
+  int* ptr = nullptr;
+};
+SymbolCache g_err_cache[128];
 
 constexpr long long kDefaultWaitBudget = 2000000000ll;   // cycles, about 1 s
 std::atomic<long long> g_wait_budget{kDefaultWaitBudget};
@@ -110,16 +117,34 @@ int record_error(int status, const char* message) {
   return status;
 }
 
+void* current_context() {
+  using CtxGetCurrent = int (*)(void**);   // CUresult cuCtxGetCurrent(CUcontext*)
+  static CtxGetCurrent fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuCtxGetCurrent", &p, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<CtxGetCurrent>(p);
+  }();
+  void* ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
 int* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  void* ctx = current_context();   // NULL before the runtime has made a context current
   std::lock_guard<std::mutex> lk(g_err_mu);
-  if (!g_err_ptr[dev]) {
+  SymbolCache& c = g_err_cache[dev];
+  if (!c.ptr || !ctx || c.ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<int*>(p);
+    c.ptr = static_cast<int*>(p);
+    c.ctx = current_context();     // the lookup has made the device's primary context current
   }
-  return g_err_ptr[dev];
+  return c.ptr;
 }
 
 }  // namespace gdr
@@ -309,7 +334,8 @@ gdr_status gdr_backward(const void* q, const void* k, const void* v, const float
   for (const void* p : ptrs16)
     if (p && !aligned16(p))
       return fail(GDR_ERR_INVALID_ARG, "%s: every array and the workspace must be 16-byte aligned", who);
-  // launch limits: 4 B column-block CTAs on the grid's x dimension, B L tokens on the reducer's
+  // launch limits: kBwdColBlocks * B column-block CTAs on the grid's x dimension (B <= 65535 keeps
+  // that within 2^31 - 1), B L tokens on the reducer's
   if ((long long)B > 65535 || (long long)B * L > 0x7fffffffLL || Hk > 65535)
     return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d, B*L=%lld or Hk=%d too large (B <= 65535, B*L < 2^31)", who, B,
                 (long long)B * L, Hk);
@@ -317,6 +343,37 @@ gdr_status gdr_backward(const void* q, const void* k, const void* v, const float
   if (ws == nullptr || ws_bytes < need)
     return fail(GDR_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", who, need,
                 ws == nullptr ? (size_t)0 : ws_bytes);
+  {
+    // the outputs (and the workspace) must not overlap one another or any input: half-open byte
+    // ranges, checked pairwise
+    const size_t es = dt == GDR_BF16 ? 2 : 4;
+    const size_t nq = (size_t)B * L * Hk * kD, nv = (size_t)B * L * Hv * kD, ng = (size_t)B * L * Hv;
+    const size_t ns = (size_t)B * Hv * kD * kD;
+    struct Range {
+      const void* p;
+      size_t bytes;
+      const char* name;
+    };
+    const Range outs[] = {{dq, nq * 4, "dq"},       {dk, nq * 4, "dk"},     {dv, nv * 4, "dv"},
+                          {dg, ng * 4, "dg"},       {dbeta, ng * 4, "dbeta"}, {dS0, ns * 4, "dS0"},
+                          {ws, need, "ws"}};
+    const Range ins[] = {{q, nq * es, "q"}, {k, nq * es, "k"},     {v, nv * es, "v"},   {g, ng * 4, "g"},
+                         {beta, ng * 4, "beta"}, {S0, ns * 4, "S0"}, {dO, nv * es, "dO"}, {dS_T, ns * 4, "dS_T"}};
+    auto overlap = [](const Range& a, const Range& b) {
+      if (!a.p || !b.p) return false;
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+      return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+    };
+    const int n_out = sizeof(outs) / sizeof(outs[0]);
+    for (int i = 0; i < n_out; ++i) {
+      for (int j = i + 1; j < n_out; ++j)
+        if (overlap(outs[i], outs[j]))
+          return fail(GDR_ERR_INVALID_ARG, "%s: %s overlaps %s", who, outs[i].name, outs[j].name);
+      for (const Range& in : ins)
+        if (overlap(outs[i], in))
+          return fail(GDR_ERR_INVALID_ARG, "%s: %s overlaps the input %s", who, outs[i].name, in.name);
+    }
+  }
   BackwardArgs a{q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, ws, B, L, Hk, Hv, dt == GDR_BF16};
   return launch_status(launch_backward(a, reinterpret_cast<cudaStream_t>(stream)), who);
 }

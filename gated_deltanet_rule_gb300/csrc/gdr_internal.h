@@ -95,8 +95,13 @@ long long wait_budget_cycles();
 // Record a one-line message for gdr_last_error_message() on this host thread; returns status.
 int record_error(int status, const char* message);
 
-// Device error word of the current device (address of a __device__ int).
+// Device error word of the current device (address of a __device__ int), looked up again when the
+// device's context has changed since the last lookup.
 int* device_error_word();
+
+// The calling thread's current CUDA context (a CUcontext, NULL if none or on failure); symbol
+// addresses cached per device are keyed on it.
+void* current_context();
 
 // Stage timer hooks (no-ops unless enabled): bracket one kernel launch on stream s.
 int stage_timer_begin(cudaStream_t s, int kernel_id);

@@ -24,7 +24,14 @@ constexpr size_t kScratchBytes = GDR_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_ptr[128] = {};   // device address of g_scratch, per device ordinal
+// Device address of g_scratch per device ordinal, with the CUDA context it was looked up in: the
+// address belongs to that context (a context created after cudaDeviceReset loads the module anew,
+// possibly elsewhere), so a change of context triggers a new lookup.
+struct ScratchAddr {
+  void* ctx = nullptr;
+  void* ptr = nullptr;
+};
+ScratchAddr g_scratch_addr[128];
 
 }  // namespace
 
@@ -42,14 +49,17 @@ extern "C" gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const 
     return static_cast<gdr_status>(gdr::record_error(GDR_ERR_UNSUPPORTED, msg));
   }
   // In host code g_scratch names a host-side stand-in, not device memory: the kernels must get the
-  // device address, looked up once per device with that device current.
+  // device address, looked up once per device (and again if the device's context changes) with that
+  // device current.
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128)
     return static_cast<gdr_status>(gdr::record_error(GDR_ERR_CUDA, "gdr_chunk_fwd_noalloc: no CUDA device"));
   void* scratch = nullptr;
   {
+    void* ctx = gdr::current_context();
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
+    ScratchAddr& a = g_scratch_addr[dev];
+    if (a.ptr == nullptr || ctx == nullptr || a.ctx != ctx) {
       void* p = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
       if (e != cudaSuccess || p == nullptr) {
@@ -58,9 +68,10 @@ extern "C" gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const 
                  cudaGetErrorString(e));
         return static_cast<gdr_status>(gdr::record_error(GDR_ERR_CUDA, msg));
       }
-      g_scratch_ptr[dev] = p;
+      a.ptr = p;
+      a.ctx = gdr::current_context();   // the lookup has made the device's primary context current
     }
-    scratch = g_scratch_ptr[dev];
+    scratch = a.ptr;
   }
   return gdr_chunk_fwd(q, k, v, g, beta, S0, o, S_T, B, L, Hk, Hv, D, dt, scratch, kScratchBytes, stream);
 }

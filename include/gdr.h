@@ -128,7 +128,9 @@ gdr_status gdr_decode_step(const void* q, const void* k, const void* v, const fl
  * (gdr_chunk_workspace_bytes) exceeds it are rejected with GDR_ERR_UNSUPPORTED and a message, before
  * any CUDA call; float32 q/k/v need no scratch.
  * The first call on a device looks up the scratch's device address (with that device current);
- * make that first call before any stream capture.
+ * make that first call before any stream capture. The address belongs to the device's CUDA
+ * context: after that context is destroyed (cudaDeviceReset) the next call looks it up again in
+ * the new one, so that call too belongs before any capture.
  * Every call uses the same scratch, which keeps the previous call's contents (nothing in it needs
  * to start at zero: each call writes all the scratch it reads). Calls whose GPU work overlaps
  * (other streams, other host threads) race on the scratch: serialise them.

@@ -15,7 +15,7 @@ import numpy as np
 
 def _f64(x):
     if hasattr(x, "detach"):
-        return x.detach().float().cpu().numpy().astype(np.float64)
+        return x.detach().cpu().double().numpy()
     return np.asarray(x, dtype=np.float64)
 
 

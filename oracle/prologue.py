@@ -22,7 +22,7 @@ def _f64(x):
     if x is None:
         return None
     if hasattr(x, "detach"):
-        return x.detach().float().cpu().numpy().astype(np.float64)
+        return x.detach().cpu().double().numpy()
     return np.asarray(x, dtype=np.float64)
 
 

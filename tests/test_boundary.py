@@ -193,3 +193,27 @@ def test_backward_workspace_query(L):
         n_seg = -(-Lt // 32)
         want = 4 * (8 * B * Hv * (n_seg + 32) * 128 * 16 + B * Lt * Hv * 8 * (2 * 128 + 2))
         assert L.gdr_backward_workspace_bytes(B, Lt, 2, Hv, 128) == want
+
+
+def test_backward_rejects_overlapping_outputs(L):
+    """Outputs that overlap each other, the workspace or an input are refused before any CUDA call
+    (each case below overlaps exactly one pair; every other pointer is far from the rest)."""
+    B, Lt, Hk, Hv = 1, 64, 2, 4
+    need = L.gdr_backward_workspace_bytes(B, Lt, Hk, Hv, 128)
+    base = {n: ctypes.c_void_p((i + 1) << 32) for i, n in enumerate(
+        ["q", "k", "v", "g", "beta", "S0", "dO", "dS_T", "dq", "dk", "dv", "dg", "dbeta", "dS0", "ws"])}
+
+    def call(**over):
+        p = dict(base, **{n: ctypes.c_void_p(v) for n, v in over.items()})
+        return L.gdr_backward(p["q"], p["k"], p["v"], p["g"], p["beta"], p["S0"], p["dO"], p["dS_T"], p["dq"],
+                              p["dk"], p["dv"], p["dg"], p["dbeta"], p["dS0"], B, Lt, Hk, Hv, 128, 1, p["ws"],
+                              need, None)
+
+    cases = [dict(dv=base["dq"].value + 256),          # two outputs
+             dict(ws=base["dg"].value + 16),           # an output and the workspace
+             dict(dq=base["q"].value + 4096),          # an output and an input
+             dict(dS0=base["S0"].value),               # the state gradient over the initial state
+             dict(dbeta=base["dO"].value + 1024)]
+    for over in cases:
+        assert call(**over) == gdr.GDR_ERR_INVALID_ARG, over
+        assert b"overlaps" in L.gdr_last_error_message(), over

@@ -3,10 +3,13 @@
 Hosts that own the whole device memory budget (a serving process that reserves the GPU at start-up,
 or a plugin inside one) and latency-critical loops cannot hand gdr_chunk_fwd a freshly allocated
 workspace; this entry point runs the same kernels on a fixed scratch array the library keeps in
-device memory. The test calls it through the C ABI twice in a row, on different sizes so that the
-second call starts from the first call's leftovers in the scratch, and compares each result with
-gdr_chunk_fwd given its own workspace, at the bf16 tolerance the other tests use. It also checks
-that a size beyond the scratch is refused with a clear message and no GPU work.
+device memory. The test calls it through the C ABI several times in a row, on different sizes so
+that each call starts from the previous call's leftovers in the scratch (a larger call, then
+smaller ones, then a single-chunk row, which needs no scratch at all), and compares each result
+with gdr_chunk_fwd given its own workspace. Both calls run the same kernels in the same order, so
+the results must be identical bit for bit (a leftover read from the scratch would show here even
+if it moved a result by less than the bf16 tolerance). It also checks that a size beyond the
+scratch is refused with a clear message and no GPU work.
 
 This file is named so that pytest collects it last.
 """
@@ -16,7 +19,6 @@ import pytest
 import torch
 
 from gated_deltanet_rule_gb300 import gdr, inputs
-from tests.gpu_util import TOL_BF16, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -36,9 +38,11 @@ def _noalloc(q, k, v, g, beta, S0, o, S_T):
                                            B, L, Hk, Hv, D, gdr.GDR_BF16, stream)
 
 
-def test_noalloc_matches_workspace_call_on_two_calls_in_a_row():
+def test_noalloc_matches_workspace_call_on_calls_in_a_row():
     cases = [inputs.regime("R1", 1000, 5, Hk=8, Hv=16, B=1, init_state=True, dtype=torch.bfloat16),
-             inputs.regime("R3", 700, 6, Hk=4, Hv=8, B=3, init_state=True, n_valid=650, dtype=torch.bfloat16)]
+             inputs.regime("R3", 700, 6, Hk=4, Hv=8, B=3, init_state=True, n_valid=650, dtype=torch.bfloat16),
+             inputs.regime("R2", 300, 7, Hk=2, Hv=4, B=2, init_state=True, dtype=torch.bfloat16),
+             inputs.regime("R1", 50, 8, Hk=4, Hv=8, B=2, init_state=True, dtype=torch.bfloat16)]
     for x in cases:
         q, k, v, g, b, S0 = (_dev(t) for t in (x.q, x.k, x.v, x.g, x.beta, x.S0))
         B, L, Hk, D = q.shape
@@ -49,8 +53,8 @@ def test_noalloc_matches_workspace_call_on_two_calls_in_a_row():
         st = _noalloc(q, k, v, g, b, S0, o, S_T)
         assert st == gdr.GDR_OK, gdr.lib().gdr_last_error_message().decode()
         gdr.gdr_sync_status()
-        assert_close(o, ref_o.double().cpu().numpy(), TOL_BF16, "o vs gdr_chunk_fwd")
-        assert_close(S_T, ref_S.double().cpu().numpy(), TOL_BF16, "S_T vs gdr_chunk_fwd")
+        assert torch.equal(o, ref_o), f"o differs from gdr_chunk_fwd (L={L}, Hv={v.shape[2]})"
+        assert torch.equal(S_T, ref_S), f"S_T differs from gdr_chunk_fwd (L={L}, Hv={v.shape[2]})"
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
