@@ -356,6 +356,7 @@ def run_gb300(args) -> dict | None:
         line["rows"]["next_f1_prologue"] = run_prologue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
         line["rows"]["next_f2_gated_rmsnorm"] = run_epilogue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
         line["rows"]["next_f4_backward"] = run_backward(reps=max(3, min(args.steps, 10)), warmup=args.warmup)
+        line["rows"]["configs"] = run_configs(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
     return line
@@ -572,6 +573,87 @@ def run_backward(reps: int, warmup: int) -> dict:
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes,
                          "note": "a sequential token loop on CUDA cores: latency-bound, far from this roofline"},
             "kernels": {kname: {"launches": c, "avg_us": round(t / c * 1e3, 2)} for kname, (t, c) in stages.items() if c}}
+
+
+def _time_calls(fn, reps: int, warmup: int, stream) -> tuple[float, dict]:
+    """Average microseconds per call of fn (CUDA events on `stream` around `reps` calls), then the
+    library's per-kernel stage times from a second pass."""
+    import torch
+    from gated_deltanet_rule_gb300 import gdr
+    for _ in range(warmup):
+        fn(0)
+    gdr.gdr_sync_status()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(reps):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    gdr.stage_timer_enable(True, 4 * reps + 16)
+    for i in range(reps):
+        fn(i)
+    torch.cuda.synchronize()
+    stages = gdr.stage_timer_collect()
+    gdr.stage_timer_enable(False, 0)
+    gdr.gdr_sync_status()
+    return us, {kname: {"launches": c, "avg_us": round(t / c * 1e3, 2)} for kname, (t, c) in stages.items() if c}
+
+
+def run_configs(reps: int, warmup: int) -> dict:
+    """Times the other workloads of the path: the long prefill (L = 8192, 16 = 16 heads, bf16, weak
+    decay, no initial state; its own HBM roofline) and the two float32 parity workloads (L = 64 and
+    the padded L = 130 row with an initial state; time only, no roofline: the float32 path is the
+    token loop on CUDA cores, whose FFMA peak is not measured)."""
+    import torch
+    from gated_deltanet_rule_gb300 import gdr, inputs
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+    out = {}
+    # long prefill: input sets rotated so that their total exceeds L2
+    x = inputs.config4()
+    L, Hk, Hv = x.q.shape[1], x.q.shape[2], x.v.shape[2]
+    host = [x.q, x.k, x.v, x.g, x.beta]
+    set_bytes = sum(t.numel() * t.element_size() for t in host)
+    n_sets = max(2, -(-2 * L2_BYTES // set_bytes))
+    sets = [[t.cuda().contiguous() for t in host] for _ in range(n_sets)]
+    o = torch.empty_like(sets[0][2])
+    S_T = torch.empty(1, Hv, D, D, device="cuda", dtype=torch.float32)
+    ws = torch.empty(max(1, gdr.workspace_bytes(1, L, Hk, Hv)), dtype=torch.uint8, device="cuda")
+
+    def long_row(i):
+        s = sets[i % n_sets]
+        gdr.gdr_chunk_fwd(s[0], s[1], s[2], s[3], s[4], None, o=o, S_T=S_T, ws=ws, stream=stream)
+
+    us, kern = _time_calls(long_row, reps, warmup, stream)
+    nbytes, nflops = algorithmic(L, Hk, Hv, False)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    assert torch.isfinite(o.float()).all() and torch.isfinite(S_T).all()
+    out["config4_prefill8192"] = {
+        "us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1),
+        "workload": f"{x.meta['workload']} ({n_sets} resident input sets rotated, > L2)",
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes,
+                     "algorithmic_flops": nflops},
+        "kernels": kern}
+    del sets, o, ws
+    # float32 parity workloads (tiny; they stay in L2)
+    for name, x in (("config1_fp32_L64", inputs.config1()), ("config2_fp32_L130_padded", inputs.config2("a"))):
+        q, k, v, g, beta = (t.cuda().contiguous() for t in (x.q, x.k, x.v, x.g, x.beta))
+        S0 = None if x.S0 is None else x.S0.cuda().contiguous()
+        o = torch.empty_like(v)
+        S_T = torch.empty(q.shape[0], v.shape[2], D, D, device="cuda", dtype=torch.float32)
+
+        def call(i):
+            gdr.gdr_chunk_fwd(q, k, v, g, beta, S0, o=o, S_T=S_T, stream=stream)
+
+        us, kern = _time_calls(call, reps, warmup, stream)
+        L = q.shape[1]
+        out[name] = {"us_per_call": round(us, 2), "tokens_per_s": round(q.shape[0] * L / (us * 1e-6), 1),
+                     "workload": f"{x.meta.get('workload', name)}: float32 q/k/v, L={L}, {q.shape[2]}->{v.shape[2]} heads "
+                                 "(time only; inputs L2-resident)",
+                     "kernels": kern}
+    return out
 
 
 # ------------------------------------------------------------------------------------------------
