@@ -55,8 +55,6 @@ namespace {
 constexpr float kScale = 0.08838834764831845f;   // 128^-0.5
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kDrainBudget = 2000000000ll;  // cycles (~1 s) an aborting CTA waits for its own copies
-constexpr int kSlices = 4;                        // value-column slices (state CTAs) per value head
-constexpr int kN = kD / kSlices;                  // 32 value columns per state CTA
 
 // Workspace. Per (row, value head, chunk) unit:
 constexpr uint32_t kMBytes = 32768;     // M': 128 x 128 fp16, two 64-column 128B-swizzled K-atoms
@@ -108,6 +106,30 @@ __device__ __forceinline__ void unpack8_f16(uint4 w, float* v) {
   }
 }
 
+// Power-of-two scale of a tile whose largest magnitude is m (>= 0): up = 2^e with m / up in
+// [0.5, 1) (up = 1 when m is zero or subnormal; e clamped to [-125, 125]), dn = 1 / up. Both are
+// exact powers of two, so scaling by them is exact, and scaling the tile by 2^k shifts e by k.
+__device__ __forceinline__ void pow2_scales(float m, float& up, float& dn) {
+  const int eb = (int)((__float_as_uint(m) >> 23) & 0xFFu);
+  int e = eb == 0 ? 0 : eb - 126;
+  e = e < -125 ? -125 : (e > 125 ? 125 : e);
+  up = __uint_as_float((uint32_t)(127 + e) << 23);
+  dn = __uint_as_float((uint32_t)(127 - e) << 23);
+}
+// Largest |x| over the 8 bf16 values of a 16-byte chunk, as bf16 magnitude bits (|x| orders like
+// its bits with the sign cleared).
+__device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 w) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) m = max(m, max(u[e] & 0x7FFFu, (u[e] >> 16) & 0x7FFFu));
+  return m;
+}
+// bf16x2 word -> fp16x2 word of the values times s (a power of two)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float s) {
+  return pack_f16x2(__uint_as_float(w << 16) * s, __uint_as_float(w & 0xFFFF0000u) * s);
+}
+
 // -------------------------------------------------------------------------------------------
 // Kernel 1: per-chunk factors
 // -------------------------------------------------------------------------------------------
@@ -146,7 +168,7 @@ static_assert(kPVt == kPK1 + 16384 && kPXs + 36 * 32 * 4 <= kPVt + 16384 && kPVt
 // zeroed once consumed, so that a row of AT restricted to a finished diagonal block is exactly a
 // column of T. Block products read rows of the left factor and columns of the right factor as
 // contiguous float4 runs, and skip the blocks that are zero by triangularity.
-__device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, int tid) {
+__device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, int tid, float dnK, float dnV) {
   const int warp = tid >> 5, lane = tid & 31;
   // 1. diagonal 16-blocks (warps 0, 1): thread = (block, column c), computing column c of the
   //    block's inverse in registers, left-looking: x_i = -sum_{j < i} A_ij x_j for rows i > c (x_c = 1,
@@ -187,13 +209,17 @@ __device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, 
       trow[m4] = make_float4(x[4 * m4], x[4 * m4 + 1], x[4 * m4 + 2], x[4 * m4 + 3]);
   } else {
     // warps 2-7 meanwhile: the k and v tiles to fp16 in place, for the fp16 products (the Gram MMA
-    // that read k as bf16 has completed); 2048 chunks of 16 B, k atoms then v atoms
+    // that read k as bf16 has completed); 2048 chunks of 16 B, k atoms then v atoms, each tile
+    // scaled by its power of two (dnK, dnV: the tile's largest magnitude lands in [0.5, 1), so
+    // every finite bf16 input fits fp16's range)
     for (int chunk16 = tid - 64; chunk16 < 2048; chunk16 += kPrepThreads - 64) {
       const int which = chunk16 >> 9, off = (chunk16 & 511) * 16;
       const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPVt + (which - 2) * 16384);
+      const float sc = which < 2 ? dnK : dnV;
       uint4* p = reinterpret_cast<uint4*>(sm + base + off);
       uint4 w = *p;
-      w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+      w = make_uint4(bf16x2_to_f16x2_scaled(w.x, sc), bf16x2_to_f16x2_scaled(w.y, sc),
+                     bf16x2_to_f16x2_scaled(w.z, sc), bf16x2_to_f16x2_scaled(w.w, sc));
       *p = w;
     }
   }
@@ -303,6 +329,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_base;
   __shared__ float gbuf[2][128];   // gates of the current and the next unit: g[64] | beta[64]
+  __shared__ uint32_t tile_max[3];   // largest |k| (two halves of the rows) and |v| of the unit, bf16 bits
+  __shared__ uint32_t s0max[kPrepThreads / 32];   // per-warp largest |S0| (float bits), fused apply
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = a.Hv / a.Hk;
@@ -438,6 +466,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       mma_commit(&bar_mma);
     }
+    __syncwarp();
+    // the largest |v| of the tile (two 8 KB atoms), for the v tile's power-of-two scale
+    uint32_t mv = 0;
+#pragma unroll 4
+    for (int c16 = lane; c16 < 1024; c16 += 32)
+      mv = max(mv, bf16x8_absmax_bits(*reinterpret_cast<const uint4*>(sm + kPVt + (c16 >> 9) * 16384 + (c16 & 511) * 16)));
+    mv = __reduce_max_sync(0xffffffffu, mv);
+    if (lane == 0) tile_max[2] = mv;
   } else if (warp < 4) {
     // inverse norms, one thread per row (rows 0-63 q, 64-127 k), both 64-column atoms. The sum
     // does not care about the order of the 16-byte chunks, so each row starts at a different one
@@ -445,11 +481,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int rr = tid & 63;
     const uint8_t* base = sm + (tid < 64 ? kPQ0 : kPK0) + rr * 128;
     float s0 = 0.f, s1 = 0.f;
+    uint32_t mk = 0;   // largest |k| of the row (bf16 bits), for the k tile's power-of-two scale
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         const uint4 w = *reinterpret_cast<const uint4*>(base + half * 16384 + (((ch + rr) & 7) << 4));
+        mk = max(mk, bf16x8_absmax_bits(w));
         const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -460,6 +498,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
     (tid < 64 ? qinv : kinv)[rr] = rsqrtf(s0 + s1 + 1e-6f);
+    mk = __reduce_max_sync(0xffffffffu, mk);
+    if (warp >= 2 && lane == 0) tile_max[warp - 2] = mk;
   } else {
     // decay factors through the 16-block anchors: for j < 16 I <= i,
     // exp(gamma_i - gamma_j) = exp(gamma_i - gamma_16I) * exp(gamma_16I - gamma_j), both factors
@@ -476,8 +516,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   }
   __syncthreads();
+  // the unit's power-of-two scales: k and v enter the fp16 products as k dnK and v dnV; 2^eK = upK
+  // is folded into the scalings that multiply K (A1 and sk), so W, M' and the rest come out as
+  // before, while U, N and P U stay in v's scale (upV is carried to the state kernel)
+  float upK, dnK, upV, dnV;
+  pow2_scales(__uint_as_float(max(tile_max[0], tile_max[1]) << 16), upK, dnK);
+  pow2_scales(__uint_as_float(tile_max[2] << 16), upV, dnV);
   if (tid < 64) {
-    skv[tid] *= kinv[tid];
+    skv[tid] *= kinv[tid] * upK;
   } else {
     const int I = 1 + ((tid - 64) >> 6), j = tid & 63;
     E2[I * 68 + j] *= kinv[j];
@@ -562,12 +608,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   __syncthreads();
 
-  invert_unit_lower(AT, Tm, Xs, sm, tid);
+  invert_unit_lower(AT, Tm, Xs, sm, tid, dnK, dnV);
 
   // operand [A1; A2] = [T diag(beta Gamma ki); T diag(beta)], MN-major: K-row j holds column j of T
   {
     const int j = tid & 63, blk = (tid >> 6) & 1, hf = tid >> 7;
-    const float s = blk ? bet[j] : bet[j] * Gam[j] * kinv[j];
+    const float s = blk ? bet[j] : bet[j] * Gam[j] * kinv[j] * upK;
     const float4* trow = reinterpret_cast<const float4*>(AT + j * 68);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -677,7 +723,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             pack8_f16(w + q8 * 8);
       }
     }
-    if (tid == 0) *reinterpret_cast<float4*>(sm + kPP) = make_float4(Gam[63], 0.f, 0.f, 0.f);
+    if (tid == 0) *reinterpret_cast<float4*>(sm + kPP) = make_float4(Gam[63], upV, 0.f, 0.f);
   }
   fence_async_smem();
   tc_fence_before();
@@ -766,10 +812,25 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     float x0[64];
 #pragma unroll
     for (int e = 0; e < 64; ++e) x0[e] = s0 ? __ldg(s0 + (size_t)(64 * hb + e) * kD + v) : 0.f;
+    // S0 enters the fp16 operand scaled by its power of two (dnS: the head's largest |S0| lands in
+    // [0.5, 1)); the products are scaled back by upS
+    float upS, dnS;
+    {
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) m = fmaxf(m, fabsf(x0[e]));
+      const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+      if (lane == 0) s0max[warp] = mw;
+      __syncthreads();
+      uint32_t mall = 0;
+#pragma unroll
+      for (int w8 = 0; w8 < kPrepThreads / 32; ++w8) mall = max(mall, s0max[w8]);
+      pow2_scales(__uint_as_float(mall), upS, dnS);
+    }
     {
       uint32_t r32[32];
 #pragma unroll
-      for (int c2 = 0; c2 < 32; ++c2) r32[c2] = pack_f16x2(x0[2 * c2], x0[2 * c2 + 1]);
+      for (int c2 = 0; c2 < 32; ++c2) r32[c2] = pack_f16x2(x0[2 * c2] * dnS, x0[2 * c2 + 1] * dnS);
       tmem_st32(tb + lane_base + 32 * hb, r32);
     }
     tc_fence_before();
@@ -804,7 +865,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int e = 0; e < 32; ++e) {
           const int i = 64 * hb + 32 * part + e;
           const float n = __half2float(*reinterpret_cast<const __half*>(nsl + swz64(i * 64 + (v & 31) * 2)));
-          so[(size_t)i * kD + v] = fmaf(gc, x0[32 * part + e], d[e] + n);
+          so[(size_t)i * kD + v] = fmaf(gc, x0[32 * part + e], fmaf(upS, d[e], upV * n));
         }
       }
     }
@@ -818,7 +879,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int e = 0; e < 32; ++e) {
         const int pos = 32 * hb + e;
         const float pu = __half2float(*reinterpret_cast<const __half*>(psl + swz64(pos * 64 + (v & 31) * 2)));
-        *reinterpret_cast<__nv_bfloat16*>(sm + kPV + pos * 256 + v * 2) = __float2bfloat16_rn(ov[e] + pu);
+        *reinterpret_cast<__nv_bfloat16*>(sm + kPV + pos * 256 + v * 2) =
+            __float2bfloat16_rn(fmaf(upS, ov[e], upV * pu));
       }
     }
     fence_async_smem();
@@ -864,85 +926,83 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 }
 
 // -------------------------------------------------------------------------------------------
-// Kernel 2: sequential state recurrence over chunks; four CTAs per (row, value head)
+// Kernel 2: sequential state recurrence over chunks; one CTA per (row, value head)
 // -------------------------------------------------------------------------------------------
-// CTA s (blockIdx.x) owns value columns [32 s, 32 s + 32) of one value head. The four CTAs of a
-// head are independent: each reads the head's M' and Q' tiles itself (the other three read the
-// same lines, so they come from L2) and its own slices of N and P U. No CTA waits on another.
-// Warp roles (warp w reads TMEM lanes 32 (w % 4) .. + 31):
-//   warps 0-3: own the state rows (key row = tid, 32 value columns, float32 registers), form
-//              S = Gamma_C S + D + N and write its fp16 copy, the operand of the next products.
-//   warps 4, 5: output rows o = O' + P U for positions 0-63 (TMEM lanes 0-63); named barrier 2.
-//   warp 6: loads the chain ring (M', this CTA's N slice, Gamma_C) up to CS chunks ahead, and
-//           prefetches the chunk kPrefetchAhead beyond each load into L2.
-//   warp 7: issues the output product O' = Q' S, so that its issue time stays off the chain.
-//   warp 8: loads the output ring (Q', this CTA's P U slice) up to OS chunks ahead (with the
-//           same L2 prefetch).
-//   warp 9: issues the state product D = M' S (in a warp of its own, so that its issue is not
-//           serialised with the state update of a diverged state warp).
-// Per chunk c: chain stage c % CS (chFull / chFree: each state warp releases it after its
-// update), output stage c % OS (outFull / outFree: released by the output warps), state operand
-// q = c % kSb (opReady: the state warps have written S_c; sReady: the state product was issued, so
-// the output product may read it too; sFree: the output product has read it), TMEM buffers
-// p = c % 2 (D[p] with bar_d; O'[p] with bar_o: product done, oFree: the output warps have read
-// it). Every barrier completes once per CS, OS, kSb, 2 chunks or per chunk, and none can run two
-// phases ahead of its waiters.
-constexpr int kStateThreads = 320;
-constexpr uint32_t kOutBar = 2, kOutCount = 64;
-constexpr uint32_t kCStage = 40960;    // M' (two 16 KB K-atoms), then this CTA's N slice (8 KB)
-constexpr uint32_t kCN = 32768;
-constexpr uint32_t kOStage = 20480;    // Q' (two 8 KB K-atoms), then this CTA's P U slice (4 KB)
-constexpr uint32_t kOPU = 16384;
-constexpr uint32_t kTmemState = 128;   // D[2] at 0, 32; O'[2] at 64, 96
-// Rings: 3 chain and 3 output stages. After the rings: kSb fp16 state operands (MN-major, 128 rows
-// of 64 B). The M = 128 output product reads 8 KB past each Q' tile
-// (operand rows 64-127, whose products land in TMEM lanes nobody reads), which stays inside the
-// buffer because the state operands follow the output ring.
-constexpr int kPrefetchAhead = 3;      // ring loads also prefetch the chunk this far beyond them into L2
-constexpr int kSb = 5;                 // fp16 state operands: the output path may trail the chain by 4 chunks
-constexpr uint32_t state_smem(int cs, int os) { return cs * kCStage + os * kOStage + kSb * 8192 + 1024; }
-static_assert(kCN == kMBytes && kOPU == kQBytes, "stage layout");
+// The chunk step S' = Gamma_C S + M' S + N and the chunk output o = Q' S + P U are formed
+// transposed: D = S_h^T [M'^T | Q'^T] with M = 128 (value columns), N = 192 (128 keys, then the
+// 64 positions of the chunk) and K = 128 (keys). The A operand is the fp16 copy S_h of the state,
+// kept in tensor memory (lane = value column, 32-bit column c = keys 2c and 2c + 1); the B operand
+// is the workspace's K-major images of M' (128 rows) and Q' (64 rows), loaded as one 192-row
+// operand. So the state product and the output product are one group of 8 MMAs per chunk, and a
+// thread's state update reads and writes only its own tensor-memory lane.
+//
+// Thread (warp w < 8, lane l) owns value column v = 32 (w % 4) + l: keys 64 (w / 4) .. + 63 of the
+// float32 state (registers) and positions 32 (w / 4) .. + 31 of every chunk's output.
+//   warps 0-7: per chunk c, read N (own column, own keys) and Gamma_C while the product runs, then
+//              S = Gamma_C S + upV N + sc D (D from tensor memory), write S_h = S / sc' into the A
+//              operand for the next product, then the output rows o = sc D_o + upV P U of chunk c,
+//              staged in shared memory and written by two TMA tensor stores (clipped at L).
+//   warp 8:   issues the 8 MMAs of each chunk into D[c % 2] (two accumulators, so that the output
+//              rows of chunk c are read while the product of chunk c + 1 runs).
+//   warp 9:   loads [M'; Q'], N and the chunk's scale block into a 2-stage ring.
+//   warp 10:  loads P U into the same ring stages.
+// Scales: N and P U arrive in their chunk's v scale (upV, a power of two, in the scale block); the
+// fp16 copy of S is S / sc with sc a running power of two: the initial state's own scale, raised to
+// upV of every chunk already applied. Power-of-two scales keep every fp16 operand in range and make
+// the whole path exactly linear under power-of-two scaling of (v, S0).
+// Barriers: fullB/fullN/fullP[s] (loads landed), emptyB[s] (the products of the stage's chunk are
+// done: an MMA commit), emptyN/emptyP[s] (each state warp has read N / P U), opReady (each state
+// warp has written S_h), bar_d[p] (the products into D[p] are done). Every wait is bounded; a wait
+// that runs out raises the CTA's abort flag and GDR_ERR_TIMEOUT, and the CTA drains and exits.
+constexpr int kChainThreads = 384;
+constexpr int kChainStages = 2;
+constexpr uint32_t kCBBytes = 49152;                      // [M' atom 0 | Q' atom 0 | M' atom 1 | Q' atom 1]
+constexpr uint32_t kCAtom = 24576;                        // one 192-row K atom of the B operand
+constexpr uint32_t kCNOff = kCBBytes;                     // N slices
+constexpr uint32_t kCPUOff = kCNOff + kNBytes;            // P U slices
+constexpr uint32_t kCStageBytes = kCPUOff + kPUBytes;     // 98304
+constexpr uint32_t kCOStage = kChainStages * kCStageBytes;   // o staging: two [64 pos][64 values] bf16 boxes
+constexpr uint32_t kChainSmem = kCOStage + 16384 + 1024;
+constexpr uint32_t kTmemChain = 512;                      // D[0] at 0, D[1] at 192 (192 columns each), S_h at 384
+constexpr uint32_t kTA = 384;
+constexpr uint32_t kStateBar = 1, kStateCount = 256;      // named barrier of the eight state warps
+static_assert(kCStageBytes % 1024 == 0 && kChainSmem <= 227 * 1024, "chain kernel shared memory");
 
-template <int CS, int OS>
-__global__ void __launch_bounds__(kStateThreads, 1)
-chunk_state_kernel(const ChunkArgs a) {
-  constexpr uint32_t kOffO = CS * kCStage;
-  constexpr uint32_t kOffSb = kOffO + OS * kOStage;
+// 1 / x for a power of two x (exact)
+__device__ __forceinline__ float pow2_inverse(float x) { return __uint_as_float((254u << 23) - __float_as_uint(x)); }
+
+__global__ void __launch_bounds__(kChainThreads, 1)
+chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t chFull[CS], chFree[CS], outFull[OS], outFree[OS], bar_d, opReady, bar_o[2], oFree[2], sReady[kSb],
-      sFree[kSb];
-  __shared__ __align__(16) float4 gam_ring[CS];   // Gamma_C of the chunk in each chain stage
+  __shared__ uint64_t fullB[kChainStages], fullN[kChainStages], fullP[kChainStages];
+  __shared__ uint64_t emptyB[kChainStages], emptyN[kChainStages], emptyP[kChainStages];
+  __shared__ uint64_t bar_d[2], opReady;
+  __shared__ __align__(16) float4 scl[kChainStages];   // Gamma_C, upV of the chunk in each stage
+  __shared__ uint32_t s0max[8];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
-  const int sl = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NC = a.NC;
 
   if (tid == 0) {
-    for (int s = 0; s < CS; ++s) {
-      mbar_init(&chFull[s], 1);
-      mbar_init(&chFree[s], 4);
+    for (int s = 0; s < kChainStages; ++s) {
+      mbar_init(&fullB[s], 1);
+      mbar_init(&fullN[s], 1);
+      mbar_init(&fullP[s], 1);
+      mbar_init(&emptyB[s], 1);
+      mbar_init(&emptyN[s], 8);
+      mbar_init(&emptyP[s], 8);
     }
-    for (int s = 0; s < OS; ++s) {
-      mbar_init(&outFull[s], 1);
-      mbar_init(&outFree[s], 1);
-    }
-    mbar_init(&bar_d, 1);
-    mbar_init(&opReady, 4);
-    for (int p = 0; p < 2; ++p) {
-      mbar_init(&bar_o[p], 1);
-      mbar_init(&oFree[p], 1);
-    }
-    for (int q = 0; q < kSb; ++q) {
-      mbar_init(&sReady[q], 1);
-      mbar_init(&sFree[q], 1);
-    }
+    mbar_init(&bar_d[0], 1);
+    mbar_init(&bar_d[1], 1);
+    mbar_init(&opReady, 8);
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(&tmem_base, kTmemState);
+  if (warp == 0) tmem_alloc(&tmem_base, kTmemChain);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -961,208 +1021,211 @@ chunk_state_kernel(const ChunkArgs a) {
   }
 
   if (skip) {
-    // every CTA of the row reads the same index and skips
-  } else if (warp == 6 || warp == 8) {
-    // ---------------- producers (lane 0): the chain ring (warp 6) and the output ring (warp 8) ----
+    // every thread of the CTA read the same index
+  } else if (warp == 9 || warp == 10) {
+    // ---------------- producers (lane 0): [M'; Q'] + N + scales (warp 9), P U (warp 10) ----------
     if (lane == 0) {
       wait_prerequisite();   // the workspace is complete once the prep kernel has finished
-      const bool chain = warp == 6;
-      const int S = chain ? CS : OS;
-      int last = -1;   // last chunk whose tiles were issued
+      const bool bn = warp == 9;
+      int last = -1;
       for (int c = 0; c < NC; ++c) {
-        const int s = c % S;
-        if (c >= S) ok = mbar_wait(chain ? &chFree[s] : &outFree[s], ((c - S) / S) & 1, a.wait_budget);
+        const int s = c % kChainStages;
+        if (c >= kChainStages) {
+          const uint32_t ph = (uint32_t)((c / kChainStages) - 1) & 1u;
+          ok = bn ? (mbar_wait(&emptyB[s], ph, a.wait_budget) && mbar_wait(&emptyN[s], ph, a.wait_budget))
+                  : mbar_wait(&emptyP[s], ph, a.wait_budget);
+        }
         if (!ok || *(volatile int*)&abort_flag) break;
         const uint8_t* ub = unit_base(a, b, h, c);
-        if (chain) {
-          uint8_t* st = sm + s * kCStage;
-          mbar_arrive_expect_tx(&chFull[s], kMBytes + 8192 + kSCopy);
-          bulk_load(st, ub, 16384, &chFull[s]);
-          bulk_load(st + 16384, ub + 16384, 16384, &chFull[s]);
-          bulk_load(st + kCN, ub + kUnitN + sl * 8192, 8192, &chFull[s]);
-          bulk_load(&gam_ring[s], ub + kUnitS, kSCopy, &chFull[s]);
-          if (c + kPrefetchAhead < NC) {   // the chunk kPrefetchAhead further on into L2
-            const uint8_t* uf = unit_base(a, b, h, c + kPrefetchAhead);
-            bulk_prefetch_l2(uf, kMBytes);
-            bulk_prefetch_l2(uf + kUnitN + sl * 8192, 8192);
-          }
+        uint8_t* st = sm + s * kCStageBytes;
+        if (bn) {
+          mbar_arrive_expect_tx(&fullB[s], kCBBytes);
+          bulk_load(st, ub, 16384, &fullB[s]);                               // M' atom 0
+          bulk_load(st + 16384, ub + kUnitQ, 8192, &fullB[s]);               // Q' atom 0
+          bulk_load(st + kCAtom, ub + 16384, 16384, &fullB[s]);              // M' atom 1
+          bulk_load(st + kCAtom + 16384, ub + kUnitQ + 8192, 8192, &fullB[s]);   // Q' atom 1
+          mbar_arrive_expect_tx(&fullN[s], kNBytes + kSCopy);
+          bulk_load(st + kCNOff, ub + kUnitN, kNBytes, &fullN[s]);
+          bulk_load(&scl[s], ub + kUnitS, kSCopy, &fullN[s]);
         } else {
-          uint8_t* st = sm + kOffO + s * kOStage;
-          mbar_arrive_expect_tx(&outFull[s], kQBytes + 4096);
-          bulk_load(st, ub + kUnitQ, kQBytes, &outFull[s]);
-          bulk_load(st + kOPU, ub + kUnitPU + sl * 4096, 4096, &outFull[s]);
-          if (c + kPrefetchAhead < NC) {
-            const uint8_t* uf = unit_base(a, b, h, c + kPrefetchAhead);
-            bulk_prefetch_l2(uf + kUnitQ, kQBytes);
-            bulk_prefetch_l2(uf + kUnitPU + sl * 4096, 4096);
-          }
+          mbar_arrive_expect_tx(&fullP[s], kPUBytes);
+          bulk_load(st + kCPUOff, ub + kUnitPU, kPUBytes, &fullP[s]);
         }
         last = c;
       }
       if (!ok) {
-        // drain: the tiles of the last S issued chunks land before the CTA's memory is released
-        for (int c = (last - S + 1 > 0 ? last - S + 1 : 0); c <= last; ++c)
-          mbar_wait(chain ? &chFull[c % S] : &outFull[c % S], (c / S) & 1, kDrainBudget);
-      }
-    }
-  } else if (warp < 4) {
-    // ---------------- state warps ----------------
-    const int kr = tid;
-    float Sm[kN];
-#pragma unroll
-    for (int n = 0; n < kN; ++n) Sm[n] = 0.f;
-    if (a.S0) {
-      const float* s0 = a.S0 + ((s0row * a.Hv + h) * kD + kr) * kD + sl * kN;
-#pragma unroll
-      for (int n = 0; n < kN; n += 4) {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(s0 + n));
-        Sm[n] = x.x; Sm[n + 1] = x.y; Sm[n + 2] = x.z; Sm[n + 3] = x.w;
-      }
-    }
-    // fp16 state operand q: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle
-    auto write_state_operand = [&](int q) {
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4*>(sm + kOffSb + q * 8192 + swz64(kr * 64 + ch * 16)) = pack8_f16(Sm + 8 * ch);
-    };
-    write_state_operand(0);
-    fence_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&opReady);   // S_0 is in Sb[0]
-    for (int c = 0; c < NC; ++c) {
-      const int cs = c % CS, p = c & 1, qn = (c + 1) % kSb;
-      const uint8_t* st = sm + cs * kCStage;
-      ok = mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
-      if (!ok) break;
-      // while the product D = M' S_c runs: S <- Gamma_C S + N (S_c is already in the fp16 operand)
-      const float gc = gam_ring[cs].x;
-      const uint8_t* nrow = st + kCN;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        float nv[8];
-        unpack8_f16(*reinterpret_cast<const uint4*>(nrow + swz64(kr * 64 + ch * 16)), nv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], nv[e]);
-      }
-      // Sb[qn] is rewritten below: the output product of chunk c + 1 - kSb must have read it
-      ok = mbar_wait(&bar_d, c & 1, a.wait_budget) &&
-           (c + 1 < kSb || mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget));
-      if (!ok) break;
-      tc_fence_after();
-      float d[kN];
-      tmem_ld32(tb + lane_base + 32 * p, d);
-#pragma unroll
-      for (int n = 0; n < kN; ++n) Sm[n] += d[n];
-      write_state_operand(qn);
-      fence_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&opReady);                        // S_{c+1} is in Sb[qn]
-        if (c + CS < NC) mbar_arrive(&chFree[cs]);   // this warp is done with N and Gamma_C
-      }
-    }
-    if (ok && a.S_T) {
-      float* dst = a.S_T + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
-#pragma unroll
-      for (int n = 0; n < kN; n += 4)
-        *reinterpret_cast<float4*>(dst + n) = make_float4(Sm[n], Sm[n + 1], Sm[n + 2], Sm[n + 3]);
-    }
-  } else if (warp == 9) {
-    // ---------------- state-product issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16(128, kN, false, true);
-      int last = -1;   // last chunk whose state product was issued
-      for (int c = 0; c < NC; ++c) {
-        const int cs = c % CS, p = c & 1, q = c % kSb;
-        ok = mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && mbar_wait(&opReady, c & 1, a.wait_budget);
-        if (!ok || *(volatile int*)&abort_flag) break;
-        tc_fence_after();
-        const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
-        const uint32_t sm_m = smem_u32(sm + cs * kCStage);
-        // D[p] = M' S_c: the product on the chain
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tb + 32 * p, smem_desc(sm_m + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                   smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
-        mma_commit(&bar_d);
-        mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
-        last = c;
-      }
-      if (!ok && last >= 0) mbar_wait(&bar_d, last & 1, kDrainBudget);   // drain
-    }
-  } else if (warp == 7) {
-    // ---------------- output-product issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16(128, kN, false, true);
-      int last = -1;   // last chunk whose output product was issued
-      for (int c = 0; c < NC; ++c) {
-        const int os = c % OS, p = c & 1, q = c % kSb;
-        ok = mbar_wait(&outFull[os], (c / OS) & 1, a.wait_budget) &&
-             mbar_wait(&sReady[q], (c / kSb) & 1, a.wait_budget) &&
-             (c < 2 || mbar_wait(&oFree[p], ((c - 2) >> 1) & 1, a.wait_budget));
-        if (!ok || *(volatile int*)&abort_flag) break;
-        tc_fence_after();
-        const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
-        const uint32_t sm_q = smem_u32(sm + kOffO + os * kOStage);
-        // O'[p] = Q' S  (M = 128; operand rows 64-127 run past the tile and are not read)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tb + 64 + 32 * p, smem_desc(sm_q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                   smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
-        mma_commit(&bar_o[p]);
-        mma_commit(&sFree[q]);
-        last = c;
-      }
-      if (!ok && last >= 0) mbar_wait(&bar_o[last & 1], (last >> 1) & 1, kDrainBudget);   // drain
-    }
-  } else {
-    // ---------------- output warps 4, 5 ----------------
-    const int i = tid - 128;   // position in the chunk = TMEM lane
-    for (int c = 0; c < NC; ++c) {
-      const int os = c % OS, p = c & 1;
-      const uint8_t* st = sm + kOffO + os * kOStage;
-      ok = mbar_wait(&outFull[os], (c / OS) & 1, a.wait_budget) &&
-           mbar_wait(&bar_o[p], (c >> 1) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
-      if (ok) {
-        tc_fence_after();
-        float qs[kN];
-        tmem_ld32(tb + lane_base + 64 + 32 * p, qs);
-        const int pos = c * 64 + i;
-        if (pos < a.L) {
-          float pu[kN];
-          const uint8_t* purow = st + kOPU;
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch)
-            unpack8_f16(*reinterpret_cast<const uint4*>(purow + swz64(i * 64 + ch * 16)), pu + 8 * ch);
-          __nv_bfloat16* orow_p = a.o + (((size_t)b * a.L + pos) * a.Hv + h) * kD + sl * kN;
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = qs[8 * ch + e] + pu[8 * ch + e];
-            *reinterpret_cast<uint4*>(orow_p + 8 * ch) = pack8_bf16(v);
+        // drain: the copies of the last issued chunks land before the CTA's memory is released
+        for (int c = (last - kChainStages + 1 > 0 ? last - kChainStages + 1 : 0); c <= last; ++c) {
+          const int s = c % kChainStages;
+          const uint32_t ph = (uint32_t)(c / kChainStages) & 1u;
+          if (bn) {
+            mbar_wait(&fullB[s], ph, kDrainBudget);
+            mbar_wait(&fullN[s], ph, kDrainBudget);
+          } else {
+            mbar_wait(&fullP[s], ph, kDrainBudget);
           }
         }
       }
-      tc_fence_before();
-      if (!named_bar_and(kOutBar, kOutCount, ok)) break;
-      if (tid == 128) {
-        mbar_arrive(&oFree[p]);
-        if (c + OS < NC) mbar_arrive(&outFree[os]);   // the Q' product complete, P U read
-      }
     }
+  } else if (warp == 8) {
+    // ---------------- MMA issuer (lane 0) ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(128, 192, false, false);
+      int last = -1;
+      for (int c = 0; c < NC; ++c) {
+        const int s = c % kChainStages, p = c & 1;
+        ok = mbar_wait(&fullB[s], (uint32_t)(c / kChainStages) & 1u, a.wait_budget) &&
+             mbar_wait(&opReady, (uint32_t)c & 1u, a.wait_budget);
+        if (!ok || *(volatile int*)&abort_flag) break;
+        tc_fence_after();
+        const uint32_t bb = smem_u32(sm + s * kCStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_tmem_a(tb + 192 * p, tb + kTA + kk * 8, smem_desc(bb + (kk >> 2) * kCAtom + (kk & 3) * 32, 16, 1024),
+                         idesc, kk > 0);
+        mma_commit(&bar_d[p]);
+        mma_commit(&emptyB[s]);
+        last = c;
+      }
+      if (!ok && last >= 0) mbar_wait(&bar_d[last & 1], (uint32_t)(last >> 1) & 1u, kDrainBudget);   // drain
+    }
+  } else if (warp < 8) {
+    // ---------------- state and output warps ----------------
+    const int v = 32 * (warp & 3) + lane, hf = warp >> 2;
+    float S[64];
+    {
+      const float* s0 = a.S0 ? a.S0 + (s0row * a.Hv + h) * kD * kD : nullptr;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) S[e] = s0 ? __ldg(s0 + (size_t)(64 * hf + e) * kD + v) : 0.f;
+    }
+    // sc: the power of two of the head's largest |S0|
+    float sc, inv;
+    {
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) m = fmaxf(m, fabsf(S[e]));
+      const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+      if (lane == 0) s0max[warp] = mw;
+      named_bar_and(kStateBar, kStateCount, true);
+      uint32_t mall = 0;
+#pragma unroll
+      for (int w8 = 0; w8 < 8; ++w8) mall = max(mall, s0max[w8]);
+      pow2_scales(__uint_as_float(mall), sc, inv);
+    }
+    // S_h = S / sc into this thread's 32 columns of the A operand, then signal the issuer
+    auto write_state_operand = [&](float iv) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t r16[16];
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) r16[c2] = pack_f16x2(S[32 * hh + 2 * c2] * iv, S[32 * hh + 2 * c2 + 1] * iv);
+        tmem_st16_nowait(tb + lane_base + kTA + 32 * hf + 16 * hh, r16);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&opReady);
+    };
+    write_state_operand(inv);
+    for (int c = 0; c < NC; ++c) {
+      const int s = c % kChainStages, p = c & 1;
+      const uint32_t ph = (uint32_t)(c / kChainStages) & 1u;
+      const uint8_t* st = sm + s * kCStageBytes;
+      float gc = 0.f, upV = 0.f;
+      __half2 nv[32];
+      ok = ok && mbar_wait(&fullN[s], ph, a.wait_budget) && !*(volatile int*)&abort_flag;
+      if (ok) {
+        // N[key][v] for this thread's keys (slice v / 32: 128 rows of 32 values, 64-byte swizzle),
+        // read while the product of this chunk runs
+        const float4 sv = scl[s];
+        gc = sv.x;
+        upV = sv.y;
+        const uint8_t* nsl = st + kCNOff + (v >> 5) * 8192;
+#pragma unroll
+        for (int e2 = 0; e2 < 32; ++e2) {
+          const int key = 64 * hf + 2 * e2;
+          const __half lo = *reinterpret_cast<const __half*>(nsl + swz64(key * 64 + (v & 31) * 2));
+          const __half hi = *reinterpret_cast<const __half*>(nsl + swz64((key + 1) * 64 + (v & 31) * 2));
+          nv[e2] = __halves2half2(lo, hi);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&emptyN[s]);
+      }
+      ok = ok && mbar_wait(&bar_d[p], (uint32_t)(c >> 1) & 1u, a.wait_budget);
+      float sc_next = sc;
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+          float d[16];
+          tmem_ld16(tb + lane_base + 192 * p + 64 * hf + 16 * part, d);
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const float2 n2 = __half22float2(nv[8 * part + e / 2]);
+            S[16 * part + e] = fmaf(gc, S[16 * part + e], fmaf(sc, d[e], upV * n2.x));
+            S[16 * part + e + 1] = fmaf(gc, S[16 * part + e + 1], fmaf(sc, d[e + 1], upV * n2.y));
+          }
+        }
+        sc_next = fmaxf(sc, upV);
+        if (c + 1 < NC) write_state_operand(pow2_inverse(sc_next));   // the next product may start
+      }
+      // the output rows of chunk c (overlapping the next product)
+      ok = ok && mbar_wait(&fullP[s], ph, a.wait_budget);
+      uint32_t ob[16];   // the 32 output values, bf16 pairs
+      const uint8_t* psl = st + kCPUOff + (v >> 5) * 4096;
+      if (ok) {
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          float ov[16];
+          tmem_ld16(tb + lane_base + 192 * p + 128 + 32 * hf + 16 * part, ov);
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const int pos = 32 * hf + 16 * part + e;
+            const float pu0 = __half2float(*reinterpret_cast<const __half*>(psl + swz64(pos * 64 + (v & 31) * 2)));
+            const float pu1 = __half2float(*reinterpret_cast<const __half*>(psl + swz64((pos + 1) * 64 + (v & 31) * 2)));
+            ob[8 * part + e / 2] = pack_bf16x2(fmaf(sc, ov[e], upV * pu0), fmaf(sc, ov[e + 1], upV * pu1));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&emptyP[s]);
+      }
+      if (tid == 0) bulk_wait_read();   // the previous chunk's o stores have read the staging
+      if (!named_bar_and(kStateBar, kStateCount, ok)) {
+        ok = false;
+        break;
+      }
+      uint8_t* ost = sm + kCOStage + (v >> 6) * 8192 + (v & 63) * 2;
+#pragma unroll
+      for (int e2 = 0; e2 < 16; ++e2) {
+        *reinterpret_cast<uint16_t*>(ost + (32 * hf + 2 * e2) * 128) = (uint16_t)(ob[e2] & 0xFFFFu);
+        *reinterpret_cast<uint16_t*>(ost + (32 * hf + 2 * e2 + 1) * 128) = (uint16_t)(ob[e2] >> 16);
+      }
+      fence_async_smem();
+      named_bar_and(kStateBar, kStateCount, true);
+      if (tid == 0) {
+        tma_store_4d(&tm_o, sm + kCOStage, 0, h, c * kChunk, b);
+        tma_store_4d(&tm_o, sm + kCOStage + 8192, 64, h, c * kChunk, b);
+        bulk_commit();
+      }
+      sc = sc_next;
+    }
+    if (ok && a.S_T) {
+      float* so = a.S_T + ((size_t)b * a.Hv + h) * kD * kD;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) so[(size_t)(64 * hf + e) * kD + v] = S[e];
+    }
+    if (tid == 0) bulk_wait_all();   // the o stores are complete before the CTA exits
   }
   if (!ok) {
     atomicExch(&abort_flag, 1);
     set_error(a.err, kErrTimeout);
   }
-  __syncwarp();         // the producer and issuer warps' lanes reconverge before the block barrier
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tb, kTmemState);
+    tmem_dealloc(tb, kTmemChain);
   }
 }
 
@@ -1182,8 +1245,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [B, L, H, 128] bf16 tensor, box {64 columns, 1 head, 64 positions, 1 row}, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int B, int L, int H) {
+// [B, L, H, 128] bf16 tensor, box {64 columns, 1 head, 64 positions, 1 row}, 128-byte swizzle
+// (the operand tiles of the prep kernel) or none (the o rows the state kernel stores).
+bool make_map(CUtensorMap* m, const void* base, int B, int L, int H, bool swizzle = true) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
@@ -1191,7 +1255,8 @@ bool make_map(CUtensorMap* m, const void* base, int B, int L, int H) {
   cuuint32_t box[4] = {64, 1, 64, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1247,7 +1312,7 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(chunk_state_kernel<3, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(3, 3));
+    e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem);
   if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkPrep);
   const long long units = (long long)a.B * a.Hv * a.NC;
@@ -1263,17 +1328,19 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   slot = stage_timer_begin(s, kKernChunkState);
   // launched as a programmatic dependent of the prep kernel: its set-up (barriers, tensor memory,
   // the initial state) overlaps the prep kernel's tail; its loads of the workspace wait for it
+  CUtensorMap mo;
+  if (!make_map(&mo, p.o, p.B, p.L, p.Hv, false)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kSlices, p.Hv, p.B);
-  cfg.blockDim = dim3(kStateThreads, 1, 1);
-  cfg.dynamicSmemBytes = state_smem(3, 3);
+  cfg.gridDim = dim3(p.Hv, p.B, 1);
+  cfg.blockDim = dim3(kChainThreads, 1, 1);
+  cfg.dynamicSmemBytes = kChainSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3>, a);
+  e = cudaLaunchKernelEx(&cfg, chunk_chain_kernel, mo, a);
   stage_timer_end(slot, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

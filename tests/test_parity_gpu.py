@@ -56,16 +56,38 @@ def test_config2_joint_scale_2_pow_8_bit_exact():
     assert torch.equal(o8, o * 256.0) and torch.equal(S8, S * 256.0)
 
 
-def test_bf16_joint_scale_2_pow_8_linear():
-    """The tensor-core path forms its products on fp16 operands, whose narrow exponent range
-    (subnormals below 6.1e-5) makes 2^8 scaling change which negligible contributions survive
-    rounding; joint linearity in (v, S0) then holds to the operand precision, not bit for bit."""
-    x = inputs.regime("R2", 130, 22, Hk=4, Hv=8, init_state=True, n_valid=100, dtype=torch.bfloat16)
+@pytest.mark.parametrize("L,B", [(50, 2), (130, 1), (300, 2)])
+def test_bf16_joint_scale_2_pow_8_bit_exact(L, B):
+    """The tensor-core path forms every fp16 operand that depends on v or the state from a tile
+    divided by its own power of two (v per chunk, the initial state per head, the running state by
+    the largest of those seen so far), so scaling (v, S0) by 2^8 leaves every operand bit-identical
+    and scales o and S_T by exactly 2^8: on single-chunk rows (one kernel) and multi-chunk rows."""
+    x = inputs.regime("R2", L, 22 + L, Hk=4, Hv=8, B=B, init_state=True, n_valid=L - 30, dtype=torch.bfloat16)
     o, S = run_chunk(x)
     x.v, x.S0 = x.v * 256.0, x.S0 * 256.0
     o8, S8 = run_chunk(x)
-    assert_close(o8 / 256.0, o.double().cpu().numpy(), 2e-3, "o")
-    assert_close(S8 / 256.0, S.double().cpu().numpy(), 1e-4, "S_T")
+    assert torch.equal(o8, o * 256.0) and torch.equal(S8, S * 256.0)
+    # negative control: v scaled alone is not a scaling of the result
+    x.S0 = x.S0 / 256.0
+    o9, _ = run_chunk(x)
+    assert not torch.equal(o9, o * 256.0)
+
+
+@pytest.mark.parametrize("L", [50, 300])
+def test_bf16_large_inputs_stay_in_range(L):
+    """q, k, v and S0 with entries in the thousands (well inside bf16's range, beyond what fp16
+    operands hold unscaled): the tensor-core path scales its operands by powers of two, so o and
+    S_T still match the oracle at the bf16 tolerance and nothing overflows to inf."""
+    x = inputs.regime("R1", L, 91 + L, Hk=2, Hv=4, B=2, init_state=True, dtype=torch.bfloat16)
+    x.q = (x.q.float() * 2000.0).bfloat16()
+    x.k = (x.k.float() * 4000.0).bfloat16()
+    x.v = (x.v.float() * 3000.0).bfloat16()
+    x.S0 = x.S0 * 30000.0
+    o, S = run_chunk(x)
+    ro, rS = ref_chunk(x)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(S).all()
+    assert_close(o, ro, TOL_BF16, "o")
+    assert_close(S, rS, TOL_BF16, "S_T")
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
