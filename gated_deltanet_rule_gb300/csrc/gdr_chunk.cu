@@ -218,8 +218,11 @@ __device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, 
       const float sc = which < 2 ? dnK : dnV;
       uint4* p = reinterpret_cast<uint4*>(sm + base + off);
       uint4 w = *p;
-      w = make_uint4(bf16x2_to_f16x2_scaled(w.x, sc), bf16x2_to_f16x2_scaled(w.y, sc),
-                     bf16x2_to_f16x2_scaled(w.z, sc), bf16x2_to_f16x2_scaled(w.w, sc));
+      if (sc == 1.f)
+        w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+      else
+        w = make_uint4(bf16x2_to_f16x2_scaled(w.x, sc), bf16x2_to_f16x2_scaled(w.y, sc),
+                       bf16x2_to_f16x2_scaled(w.z, sc), bf16x2_to_f16x2_scaled(w.w, sc));
       *p = w;
     }
   }
@@ -329,7 +332,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_base;
   __shared__ float gbuf[2][128];   // gates of the current and the next unit: g[64] | beta[64]
-  __shared__ uint32_t tile_max[3];   // largest |k| (two halves of the rows) and |v| of the unit, bf16 bits
+  __shared__ uint32_t tile_max[6];   // per warp 4-6: largest |k| (0-2) and |v| (3-5) of the unit, bf16 bits
   __shared__ uint32_t s0max[kPrepThreads / 32];   // per-warp largest |S0| (float bits), fused apply
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -466,14 +469,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       mma_commit(&bar_mma);
     }
-    __syncwarp();
-    // the largest |v| of the tile (two 8 KB atoms), for the v tile's power-of-two scale
-    uint32_t mv = 0;
-#pragma unroll 4
-    for (int c16 = lane; c16 < 1024; c16 += 32)
-      mv = max(mv, bf16x8_absmax_bits(*reinterpret_cast<const uint4*>(sm + kPVt + (c16 >> 9) * 16384 + (c16 & 511) * 16)));
-    mv = __reduce_max_sync(0xffffffffu, mv);
-    if (lane == 0) tile_max[2] = mv;
   } else if (warp < 4) {
     // inverse norms, one thread per row (rows 0-63 q, 64-127 k), both 64-column atoms. The sum
     // does not care about the order of the 16-byte chunks, so each row starts at a different one
@@ -481,13 +476,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int rr = tid & 63;
     const uint8_t* base = sm + (tid < 64 ? kPQ0 : kPK0) + rr * 128;
     float s0 = 0.f, s1 = 0.f;
-    uint32_t mk = 0;   // largest |k| of the row (bf16 bits), for the k tile's power-of-two scale
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         const uint4 w = *reinterpret_cast<const uint4*>(base + half * 16384 + (((ch + rr) & 7) << 4));
-        mk = max(mk, bf16x8_absmax_bits(w));
         const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -498,8 +491,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
     (tid < 64 ? qinv : kinv)[rr] = rsqrtf(s0 + s1 + 1e-6f);
-    mk = __reduce_max_sync(0xffffffffu, mk);
-    if (warp >= 2 && lane == 0) tile_max[warp - 2] = mk;
   } else {
     // decay factors through the 16-block anchors: for j < 16 I <= i,
     // exp(gamma_i - gamma_j) = exp(gamma_i - gamma_16I) * exp(gamma_16I - gamma_j), both factors
@@ -514,15 +505,41 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         E2[I * 68 + j] = (j < 16 * I) ? ex2_approx(gam2[16 * I] - gam2[j]) : 0.f;
       }
     }
+    // the largest |k| and |v| of the tiles (two 8 KB atoms each), for their power-of-two scales:
+    // warp 4 + t, t < 3, takes 16-byte chunks t, t + 3, ... of the 2048
+    uint32_t mk = 0, mv = 0;
+#pragma unroll 4
+    for (int c16 = tid - 128; c16 < 2048; c16 += 96) {
+      const int which = c16 >> 9;
+      const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPVt + (which - 2) * 16384);
+      const uint32_t m = bf16x8_absmax_bits(*reinterpret_cast<const uint4*>(sm + base + (c16 & 511) * 16));
+      if (which < 2) mk = max(mk, m);
+      else mv = max(mv, m);
+    }
+    mk = __reduce_max_sync(0xffffffffu, mk);
+    mv = __reduce_max_sync(0xffffffffu, mv);
+    if (lane == 0) {
+      tile_max[warp - 4] = mk;
+      tile_max[warp - 1] = mv;
+    }
   }
   __syncthreads();
   // the unit's power-of-two scales: k and v enter the fp16 products as k dnK and v dnV; 2^eK = upK
   // is folded into the scalings that multiply K (A1 and sk), so W, M' and the rest come out as
   // before, while U, N and P U stay in v's scale (upV is carried to the state kernel)
-  float upK, dnK, upV, dnV;
-  pow2_scales(__uint_as_float(max(tile_max[0], tile_max[1]) << 16), upK, dnK);
-  pow2_scales(__uint_as_float(tile_max[2] << 16), upV, dnV);
+  // (recomputed from tile_max where they are used, so that no register holds them across the unit)
+  auto unit_scales = [&](float& upK, float& dnK, float& upV, float& dnV) {
+    const uint32_t mk = max(tile_max[0], max(tile_max[1], tile_max[2]));
+    const uint32_t mv = max(tile_max[3], max(tile_max[4], tile_max[5]));
+    // k is scaled only when its tile would leave fp16's comfortable range (largest |k| >= 2^15 or
+    // below 2^-8); v always, so that U, N and P U are formed in v's own scale
+    upK = dnK = 1.f;
+    if (mk >= 0x4700u || mk < 0x3B80u) pow2_scales(__uint_as_float(mk << 16), upK, dnK);
+    pow2_scales(__uint_as_float(mv << 16), upV, dnV);
+  };
   if (tid < 64) {
+    float upK, dnK, upV, dnV;
+    unit_scales(upK, dnK, upV, dnV);
     skv[tid] *= kinv[tid] * upK;
   } else {
     const int I = 1 + ((tid - 64) >> 6), j = tid & 63;
@@ -608,11 +625,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   __syncthreads();
 
-  invert_unit_lower(AT, Tm, Xs, sm, tid, dnK, dnV);
+  {
+    float upK, dnK, upV, dnV;
+    unit_scales(upK, dnK, upV, dnV);
+    invert_unit_lower(AT, Tm, Xs, sm, tid, dnK, dnV);
+  }
 
   // operand [A1; A2] = [T diag(beta Gamma ki); T diag(beta)], MN-major: K-row j holds column j of T
   {
     const int j = tid & 63, blk = (tid >> 6) & 1, hf = tid >> 7;
+    float upK, dnK, upV, dnV;
+    unit_scales(upK, dnK, upV, dnV);
     const float s = blk ? bet[j] : bet[j] * Gam[j] * kinv[j] * upK;
     const float4* trow = reinterpret_cast<const float4*>(AT + j * 68);
 #pragma unroll
@@ -672,18 +695,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_before();
   __syncthreads();
 
-  // P W into columns 0-127 of TMEM lanes 0-63 and P U into columns 128-255 of lanes 64-127
+  // P W into columns 0-127 of TMEM lanes 0-63 (M = 128: operand rows 64-127 run past P into rows
+  // that nobody reads), and (P U)^T = U^T P^T into columns 128-191 of all 128 lanes (lane = value
+  // column: U as the MN-major A operand, P as the K-major B operand, N = 64 positions)
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t idesc = idesc_f16(128, 128, false, true);
+    const uint32_t id_pw = idesc_f16(128, 128, false, true), id_pu = idesc_f16(128, 64, true, false);
     const uint32_t pa = smem_u32(sm + kPP), wu = smem_u32(sm + kPV);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_bf16(tb, smem_desc(pa + kk * 32, 16, 1024), smem_desc(wu + kk * 2048, 8192, 1024), idesc, kk > 0);
+      mma_bf16(tb, smem_desc(pa + kk * 32, 16, 1024), smem_desc(wu + kk * 2048, 8192, 1024), id_pw, kk > 0);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_bf16(tb + 128, smem_desc(pa - 8192 + kk * 32, 16, 1024), smem_desc(wu + 16384 + kk * 2048, 8192, 1024),
-               idesc, kk > 0);
+      mma_bf16(tb + 128, smem_desc(wu + 16384 + kk * 2048, 8192, 1024), smem_desc(pa + kk * 32, 16, 1024), id_pu,
+               kk > 0);
     mma_commit(&bar_mma);
   }
   ok = wait_mma();
@@ -691,12 +716,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_after();
 
   {
-    // warps 0, 1, 4, 5 (lanes 0-63): Q'_i = sq_i q_i - (P W)_i, the fp16 image, on columns cb .. cb + 63;
-    // warps 2, 3, 6, 7 (lanes 64-127): (P U)_i, the fp16 slices, on columns cb .. cb + 63. Both are
-    // staged over the consumed [W | U] operand, Gamma_C over P.
+    // warps 0, 1, 4, 5 (lanes 0-63): Q'_i = sq_i q_i - (P W)_i, the fp16 image, on columns cb .. cb + 63,
+    // staged over the consumed W operand. Every warp: (P U)^T row v = TMEM lane (value column),
+    // positions 32 (w / 4) .. + 31, staged over the consumed U operand as [128 values][64 positions]
+    // fp16 rows of 128 bytes, 16-byte chunk j of row v at chunk j ^ (v % 8). Gamma_C over P.
     const int row = 32 * (warp & 3) + lane, i = row & 63, cb = (warp >> 2) * 64;
-    float w[64];
     if (row < 64) {
+      float w[64];
       const float sq = Gam[i] * qinv[i] * kScale;
       tmem_ld64(tb + lane_base + cb, w);
 #pragma unroll
@@ -714,31 +740,41 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         *reinterpret_cast<uint4*>(sm + kPV + off) = pack8_f16(v);
       }
-    } else {
-      tmem_ld64(tb + lane_base + 128 + cb, w);
-#pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        const int col = cb + q8 * 8;
-        *reinterpret_cast<uint4*>(sm + kPV + 16384 + (col >> 5) * 4096 + swz64(i * 64 + (q8 & 3) * 16)) =
-            pack8_f16(w + q8 * 8);
-      }
     }
-    if (tid == 0) *reinterpret_cast<float4*>(sm + kPP) = make_float4(Gam[63], upV, 0.f, 0.f);
+    {
+      float pu[32];
+      const int hp = warp >> 2;
+      tmem_ld32(tb + lane_base + 128 + 32 * hp, pu);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(sm + kPV + 16384 + row * 128 + (((4 * hp + q) ^ (row & 7)) << 4)) = pack8_f16(pu + 8 * q);
+    }
+    if (tid == 0) {
+      float upK, dnK, upV, dnV;
+      unit_scales(upK, dnK, upV, dnV);
+      *reinterpret_cast<float4*>(sm + kPP) = make_float4(Gam[63], upV, 0.f, 0.f);
+    }
   }
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
 
-  // K^T [sk W | sk U] = [-M' | N] into columns 0-255 (the P [W | U] results have been read); Q',
-  // P U and Gamma_C leave for the workspace meanwhile
+  // K^T (sk W) = -M' and (sk U)^T K = N^T into columns 0-255 (the P W and (P U)^T results have been
+  // read); Q', (P U)^T and Gamma_C leave for the workspace meanwhile
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t idesc = idesc_f16(128, 256, true, true);
-    const uint32_t kt = smem_u32(sm + kPK0);    // k atoms (M blocks) at +8192 and +24576: stride 16384
+    const uint32_t idesc = idesc_f16(128, 128, true, true);
+    const uint32_t kt = smem_u32(sm + kPK0);    // k atoms (M / N blocks) at +8192 and +24576: stride 16384
     const uint32_t wsu = smem_u32(sm + kPWS);
+    // -M' = K^T (sk W): lane = key (columns 0-127)
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(tb, smem_desc(kt + kk * 2048, 16384, 1024), smem_desc(wsu + kk * 2048, 8192, 1024), idesc, kk > 0);
+    // N^T = (sk U)^T K: lane = value column (columns 128-255)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16(tb + 128, smem_desc(wsu + 16384 + kk * 2048, 8192, 1024), smem_desc(kt + kk * 2048, 16384, 1024), idesc,
+               kk > 0);
     mma_commit(&bar_mma);
     if (!kFused) {
       bulk_store(ub + kUnitQ, sm + kPV, kQBytes);
@@ -752,9 +788,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_after();
 
   {
-    // every warp: key row i = TMEM lane, columns cb .. cb + 63 of M' = -D[:, 0:128] (fp16 K-major
-    // image over q and k, consumed) and of N = D[:, 128:256] (fp16 slices over [sk W | sk U]),
-    // staged for bulk stores (per-thread 16-byte global stores of these row layouts are far slower)
+    // every warp: lane i, columns cb .. cb + 63: of M' = -D[:, 0:128] (key row i; the fp16 K-major
+    // image over q and k, consumed) and of N^T = D[:, 128:256] (value row i), staged for bulk stores
+    // (per-thread 16-byte global stores of these row layouts are far slower)
     const int i = 32 * (warp & 3) + lane, cb = (warp >> 2) * 64;
     {
       float w[64];
@@ -769,13 +805,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
     {
+      // N^T row i (a value column), keys cb .. cb + 63, staged over the consumed [sk W | sk U] as
+      // [128 values][128 keys] fp16 rows of 256 bytes, 16-byte chunk j of row v at chunk
+      // (j & 8) | ((j & 7) ^ (v % 8))
       float n[64];
       tmem_ld64(tb + lane_base + 128 + cb, n);
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
-        const int col = cb + q8 * 8;
-        *reinterpret_cast<uint4*>(sm + kPWS + (col >> 5) * 8192 + swz64(i * 64 + (q8 & 3) * 16)) =
-            pack8_f16(n + q8 * 8);
+        const int j = (cb >> 3) + q8;
+        *reinterpret_cast<uint4*>(sm + kPWS + i * 256 + (((j & 8) | ((j & 7) ^ (i & 7))) << 4)) = pack8_f16(n + q8 * 8);
       }
     }
   }
@@ -790,6 +828,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // (warp w, lane l) owns value v = 32 (w % 4) + l and keys / positions of half w / 4.
     tc_fence_after();
     const int v = 32 * (warp & 3) + lane, hb = warp >> 2;
+    float upV;
+    {
+      float upK, dnK, dnV;
+      unit_scales(upK, dnK, upV, dnV);
+    }
     const float* s0 = nullptr;
     bool write = true;
     if (a.S0) {
@@ -856,31 +899,39 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       // S_T[i][v] for keys i = 64 hb .. + 63; N[i][v] from its staged fp16 slice
       float* so = a.S_T + (((size_t)b * a.Hv + h) * kD) * kD;
       const float gc = Gam[63];
-      const uint8_t* nsl = sm + kPWS + (v >> 5) * 8192;
+      const uint8_t* nrow = sm + kPWS + v * 256;   // N^T row v
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         float d[32];
         tmem_ld32(tb + lane_base + 64 + 64 * hb + 32 * part, d);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int i = 64 * hb + 32 * part + e;
-          const float n = __half2float(*reinterpret_cast<const __half*>(nsl + swz64(i * 64 + (v & 31) * 2)));
-          so[(size_t)i * kD + v] = fmaf(gc, x0[32 * part + e], fmaf(upS, d[e], upV * n));
+        for (int q = 0; q < 4; ++q) {
+          const int j = 8 * hb + 4 * part + q;
+          float n[8];
+          unpack8_f16(*reinterpret_cast<const uint4*>(nrow + (((j & 8) | ((j & 7) ^ (v & 7))) << 4)), n);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int i = 64 * hb + 32 * part + 8 * q + e;
+            so[(size_t)i * kD + v] = fmaf(gc, x0[32 * part + 8 * q + e], fmaf(upS, d[8 * q + e], upV * n[e]));
+          }
         }
       }
     }
     if (write) {
-      // o at positions 32 hb .. + 31 of this chunk; (P U)[pos][v] from its staged fp16 slice. The
-      // bf16 rows are staged over the consumed Q' image and leave by one bulk store per position.
+      // o at positions 32 hb .. + 31 of this chunk; (P U)^T[v][pos] from its staged row. The bf16
+      // rows are staged over the consumed Q' image and leave by one bulk store per position.
       float ov[32];
       tmem_ld32(tb + lane_base + 192 + 32 * hb, ov);
-      const uint8_t* psl = sm + kPV + 16384 + (v >> 5) * 4096;
+      const uint8_t* prow = sm + kPV + 16384 + v * 128;   // (P U)^T row v
+      float pu[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        unpack8_f16(*reinterpret_cast<const uint4*>(prow + (((4 * hb + q) ^ (v & 7)) << 4)), pu + 8 * q);
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int pos = 32 * hb + e;
-        const float pu = __half2float(*reinterpret_cast<const __half*>(psl + swz64(pos * 64 + (v & 31) * 2)));
         *reinterpret_cast<__nv_bfloat16*>(sm + kPV + pos * 256 + v * 2) =
-            __float2bfloat16_rn(fmaf(upS, ov[e], upV * pu));
+            __float2bfloat16_rn(fmaf(upS, ov[e], upV * pu[e]));
       }
     }
     fence_async_smem();
@@ -937,11 +988,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // thread's state update reads and writes only its own tensor-memory lane.
 //
 // Thread (warp w < 8, lane l) owns value column v = 32 (w % 4) + l: keys 64 (w / 4) .. + 63 of the
-// float32 state (registers) and positions 32 (w / 4) .. + 31 of every chunk's output.
-//   warps 0-7: per chunk c, read N (own column, own keys) and Gamma_C while the product runs, then
+// float32 state (registers) and positions 32 (w / 4) .. + 31 of every chunk's output. The workspace
+// holds N and P U transposed (row = value column), so each thread reads its own row with 16-byte
+// loads.
+//   warps 0-7: per chunk c, read its N^T row and Gamma_C while the product runs, then
 //              S = Gamma_C S + upV N + sc D (D from tensor memory), write S_h = S / sc' into the A
-//              operand for the next product, then the output rows o = sc D_o + upV P U of chunk c,
-//              staged in shared memory and written by two TMA tensor stores (clipped at L).
+//              operand for the next product, then its output values o = sc D_o + upV P U of chunk
+//              c, stored straight to global memory (positions < L only).
 //   warp 8:   issues the 8 MMAs of each chunk into D[c % 2] (two accumulators, so that the output
 //              rows of chunk c are read while the product of chunk c + 1 runs).
 //   warp 9:   loads [M'; Q'], N and the chunk's scale block into a 2-stage ring.
@@ -961,18 +1014,18 @@ constexpr uint32_t kCAtom = 24576;                        // one 192-row K atom 
 constexpr uint32_t kCNOff = kCBBytes;                     // N slices
 constexpr uint32_t kCPUOff = kCNOff + kNBytes;            // P U slices
 constexpr uint32_t kCStageBytes = kCPUOff + kPUBytes;     // 98304
-constexpr uint32_t kCOStage = kChainStages * kCStageBytes;   // o staging: two [64 pos][64 values] bf16 boxes
-constexpr uint32_t kChainSmem = kCOStage + 16384 + 1024;
+constexpr uint32_t kChainSmem = kChainStages * kCStageBytes + 1024;
 constexpr uint32_t kTmemChain = 512;                      // D[0] at 0, D[1] at 192 (192 columns each), S_h at 384
 constexpr uint32_t kTA = 384;
 constexpr uint32_t kStateBar = 1, kStateCount = 256;      // named barrier of the eight state warps
+constexpr int kChainPrefetch = 6;                         // ring loads prefetch the chunk this far ahead into L2
 static_assert(kCStageBytes % 1024 == 0 && kChainSmem <= 227 * 1024, "chain kernel shared memory");
 
 // 1 / x for a power of two x (exact)
 __device__ __forceinline__ float pow2_inverse(float x) { return __uint_as_float((254u << 23) - __float_as_uint(x)); }
 
 __global__ void __launch_bounds__(kChainThreads, 1)
-chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChunkArgs a) {
+chunk_chain_kernel(const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t fullB[kChainStages], fullN[kChainStages], fullP[kChainStages];
@@ -1038,6 +1091,19 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChunkArgs a) 
         if (!ok || *(volatile int*)&abort_flag) break;
         const uint8_t* ub = unit_base(a, b, h, c);
         uint8_t* st = sm + s * kCStageBytes;
+        // the chunk kChainPrefetch further on into L2, so that the ring's loads hit L2
+        if (c == 0) {
+          for (int cf = 0; cf < kChainPrefetch && cf < NC; ++cf) {
+            const uint8_t* uf = unit_base(a, b, h, cf);
+            if (bn) bulk_prefetch_l2(uf, kUnitPU);
+            else bulk_prefetch_l2(uf + kUnitPU, kPUBytes);
+          }
+        }
+        if (c + kChainPrefetch < NC) {
+          const uint8_t* uf = unit_base(a, b, h, c + kChainPrefetch);
+          if (bn) bulk_prefetch_l2(uf, kUnitPU);   // M', Q', N (contiguous)
+          else bulk_prefetch_l2(uf + kUnitPU, kPUBytes);
+        }
         if (bn) {
           mbar_arrive_expect_tx(&fullB[s], kCBBytes);
           bulk_load(st, ub, 16384, &fullB[s]);                               // M' atom 0
@@ -1127,26 +1193,25 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChunkArgs a) 
       if (lane == 0) mbar_arrive(&opReady);
     };
     write_state_operand(inv);
+    __nv_bfloat16* orow = a.o + (((size_t)b * a.L) * a.Hv + h) * kD + v;   // o[b][pos][h][v] = orow[pos Hv D]
+    const size_t ostride = (size_t)a.Hv * kD;
     for (int c = 0; c < NC; ++c) {
       const int s = c % kChainStages, p = c & 1;
       const uint32_t ph = (uint32_t)(c / kChainStages) & 1u;
       const uint8_t* st = sm + s * kCStageBytes;
       float gc = 0.f, upV = 0.f;
-      __half2 nv[32];
+      uint4 nv[8];   // N^T[v][keys 64 hf .. + 63], fp16
       ok = ok && mbar_wait(&fullN[s], ph, a.wait_budget) && !*(volatile int*)&abort_flag;
       if (ok) {
-        // N[key][v] for this thread's keys (slice v / 32: 128 rows of 32 values, 64-byte swizzle),
-        // read while the product of this chunk runs
+        // this thread's N^T row (value column v, its 64 keys), read while the product of this chunk runs
         const float4 sv = scl[s];
         gc = sv.x;
         upV = sv.y;
-        const uint8_t* nsl = st + kCNOff + (v >> 5) * 8192;
+        const uint8_t* nrow = st + kCNOff + v * 256;
 #pragma unroll
-        for (int e2 = 0; e2 < 32; ++e2) {
-          const int key = 64 * hf + 2 * e2;
-          const __half lo = *reinterpret_cast<const __half*>(nsl + swz64(key * 64 + (v & 31) * 2));
-          const __half hi = *reinterpret_cast<const __half*>(nsl + swz64((key + 1) * 64 + (v & 31) * 2));
-          nv[e2] = __halves2half2(lo, hi);
+        for (int q = 0; q < 8; ++q) {
+          const int j = 8 * hf + q;
+          nv[q] = *reinterpret_cast<const uint4*>(nrow + (((j & 8) | ((j & 7) ^ (v & 7))) << 4));
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&emptyN[s]);
@@ -1155,66 +1220,46 @@ chunk_chain_kernel(const __grid_constant__ CUtensorMap tm_o, const ChunkArgs a) 
       float sc_next = sc;
       if (ok) {
         tc_fence_after();
+        uint32_t d[64];
+        tmem_ld32_nowait(tb + lane_base + 192 * p + 64 * hf, d);
+        tmem_ld32_nowait(tb + lane_base + 192 * p + 64 * hf + 32, d + 32);
+        tmem_wait_ld32x2(d);
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-          float d[16];
-          tmem_ld16(tb + lane_base + 192 * p + 64 * hf + 16 * part, d);
+        for (int q = 0; q < 8; ++q) {
+          float n[8];
+          unpack8_f16(nv[q], n);
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const float2 n2 = __half22float2(nv[8 * part + e / 2]);
-            S[16 * part + e] = fmaf(gc, S[16 * part + e], fmaf(sc, d[e], upV * n2.x));
-            S[16 * part + e + 1] = fmaf(gc, S[16 * part + e + 1], fmaf(sc, d[e + 1], upV * n2.y));
-          }
+          for (int e = 0; e < 8; ++e)
+            S[8 * q + e] = fmaf(gc, S[8 * q + e], fmaf(sc, __uint_as_float(d[8 * q + e]), upV * n[e]));
         }
         sc_next = fmaxf(sc, upV);
         if (c + 1 < NC) write_state_operand(pow2_inverse(sc_next));   // the next product may start
       }
-      // the output rows of chunk c (overlapping the next product)
+      // the output rows of chunk c (overlapping the next product): o = sc D_o + upV (P U)^T, written
+      // straight to global memory (a warp's store covers 64 contiguous bytes of one position's row)
       ok = ok && mbar_wait(&fullP[s], ph, a.wait_budget);
-      uint32_t ob[16];   // the 32 output values, bf16 pairs
-      const uint8_t* psl = st + kCPUOff + (v >> 5) * 4096;
       if (ok) {
+        float ov[32], pu[32];
+        tmem_ld32(tb + lane_base + 192 * p + 128 + 32 * hf, ov);
+        const uint8_t* prow = st + kCPUOff + v * 128;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          float ov[16];
-          tmem_ld16(tb + lane_base + 192 * p + 128 + 32 * hf + 16 * part, ov);
-#pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const int pos = 32 * hf + 16 * part + e;
-            const float pu0 = __half2float(*reinterpret_cast<const __half*>(psl + swz64(pos * 64 + (v & 31) * 2)));
-            const float pu1 = __half2float(*reinterpret_cast<const __half*>(psl + swz64((pos + 1) * 64 + (v & 31) * 2)));
-            ob[8 * part + e / 2] = pack_bf16x2(fmaf(sc, ov[e], upV * pu0), fmaf(sc, ov[e + 1], upV * pu1));
-          }
-        }
+        for (int q = 0; q < 4; ++q)
+          unpack8_f16(*reinterpret_cast<const uint4*>(prow + (((4 * hf + q) ^ (v & 7)) << 4)), pu + 8 * q);
         __syncwarp();
         if (lane == 0) mbar_arrive(&emptyP[s]);
-      }
-      if (tid == 0) bulk_wait_read();   // the previous chunk's o stores have read the staging
-      if (!named_bar_and(kStateBar, kStateCount, ok)) {
-        ok = false;
-        break;
-      }
-      uint8_t* ost = sm + kCOStage + (v >> 6) * 8192 + (v & 63) * 2;
+        const int p0 = c * kChunk + 32 * hf;
 #pragma unroll
-      for (int e2 = 0; e2 < 16; ++e2) {
-        *reinterpret_cast<uint16_t*>(ost + (32 * hf + 2 * e2) * 128) = (uint16_t)(ob[e2] & 0xFFFFu);
-        *reinterpret_cast<uint16_t*>(ost + (32 * hf + 2 * e2 + 1) * 128) = (uint16_t)(ob[e2] >> 16);
-      }
-      fence_async_smem();
-      named_bar_and(kStateBar, kStateCount, true);
-      if (tid == 0) {
-        tma_store_4d(&tm_o, sm + kCOStage, 0, h, c * kChunk, b);
-        tma_store_4d(&tm_o, sm + kCOStage + 8192, 64, h, c * kChunk, b);
-        bulk_commit();
+        for (int e = 0; e < 32; ++e)
+          if (p0 + e < a.L) orow[(size_t)(p0 + e) * ostride] = __float2bfloat16_rn(fmaf(sc, ov[e], upV * pu[e]));
       }
       sc = sc_next;
+      if (!ok) break;
     }
     if (ok && a.S_T) {
       float* so = a.S_T + ((size_t)b * a.Hv + h) * kD * kD;
 #pragma unroll
       for (int e = 0; e < 64; ++e) so[(size_t)(64 * hf + e) * kD + v] = S[e];
     }
-    if (tid == 0) bulk_wait_all();   // the o stores are complete before the CTA exits
   }
   if (!ok) {
     atomicExch(&abort_flag, 1);
@@ -1245,9 +1290,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [B, L, H, 128] bf16 tensor, box {64 columns, 1 head, 64 positions, 1 row}, 128-byte swizzle
-// (the operand tiles of the prep kernel) or none (the o rows the state kernel stores).
-bool make_map(CUtensorMap* m, const void* base, int B, int L, int H, bool swizzle = true) {
+// [B, L, H, 128] bf16 tensor, box {64 columns, 1 head, 64 positions, 1 row}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int B, int L, int H) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
@@ -1255,8 +1299,7 @@ bool make_map(CUtensorMap* m, const void* base, int B, int L, int H, bool swizzl
   cuuint32_t box[4] = {64, 1, 64, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1328,8 +1371,6 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   slot = stage_timer_begin(s, kKernChunkState);
   // launched as a programmatic dependent of the prep kernel: its set-up (barriers, tensor memory,
   // the initial state) overlaps the prep kernel's tail; its loads of the workspace wait for it
-  CUtensorMap mo;
-  if (!make_map(&mo, p.o, p.B, p.L, p.Hv, false)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.Hv, p.B, 1);
   cfg.blockDim = dim3(kChainThreads, 1, 1);
@@ -1340,7 +1381,7 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, chunk_chain_kernel, mo, a);
+  e = cudaLaunchKernelEx(&cfg, chunk_chain_kernel, a);
   stage_timer_end(slot, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
