@@ -531,10 +531,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   auto unit_scales = [&](float& upK, float& dnK, float& upV, float& dnV) {
     const uint32_t mk = max(tile_max[0], max(tile_max[1], tile_max[2]));
     const uint32_t mv = max(tile_max[3], max(tile_max[4], tile_max[5]));
-    // k is scaled only when its tile would leave fp16's comfortable range (largest |k| >= 2^15 or
-    // below 2^-8); v always, so that U, N and P U are formed in v's own scale
+    // k is scaled when its largest |k| is outside [2^-6, 2^6): within it, both k and the inverse
+    // norms that the A1 and sk scalings fold in (>= 2^-6 / sqrt(128)) are normal fp16 numbers;
+    // v always, so that U, N and P U are formed in v's own scale
     upK = dnK = 1.f;
-    if (mk >= 0x4700u || mk < 0x3B80u) pow2_scales(__uint_as_float(mk << 16), upK, dnK);
+    if (mk >= 0x4280u || mk < 0x3C80u) pow2_scales(__uint_as_float(mk << 16), upK, dnK);
     pow2_scales(__uint_as_float(mv << 16), upV, dnV);
   };
   if (tid < 64) {
