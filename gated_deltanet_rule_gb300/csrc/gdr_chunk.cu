@@ -990,49 +990,66 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 //
 // Thread (warp w < 8, lane l) owns value column v = 32 (w % 4) + l: keys 64 (w / 4) .. + 63 of the
 // float32 state (registers) and positions 32 (w / 4) .. + 31 of every chunk's output. The workspace
-// holds N and P U transposed (row = value column), so each thread reads its own row with 16-byte
-// loads.
-//   warps 0-7: per chunk c, read its N^T row and Gamma_C while the product runs, then
-//              S = Gamma_C S + upV N + sc D (D from tensor memory), write S_h = S / sc' into the A
-//              operand for the next product, then its output values o = sc D_o + upV P U of chunk
-//              c, stored straight to global memory (positions < L only).
+// holds N and P U transposed (row = value column), so each thread loads its own rows (and the chunk's
+// scale block) straight from L2 into registers, one chunk ahead; only [M'; Q'] passes through shared
+// memory, for the MMAs.
+//   warps 0-7: per chunk c, S = Gamma_C S + upV N + sc D (D from tensor memory), write
+//              S_h = S / sc' into the A operand for the next product, load the next chunk's rows,
+//              then the output values o = sc D_o + upV P U of chunk c: transposed through a 2 KB
+//              shared-memory tile per warp and stored as 16-byte pieces of the rows of o.
 //   warp 8:   issues the 8 MMAs of each chunk into D[c % 2] (two accumulators, so that the output
-//              rows of chunk c are read while the product of chunk c + 1 runs).
-//   warp 9:   loads [M'; Q'], N and the chunk's scale block into a 2-stage ring.
-//   warp 10:  loads P U into the same ring stages.
+//              of chunk c is read while the product of chunk c + 1 runs).
+//   warp 9:   loads [M'; Q'] into a 3-stage ring, and prefetches the units further ahead into L2.
 // Scales: N and P U arrive in their chunk's v scale (upV, a power of two, in the scale block); the
 // fp16 copy of S is S / sc with sc a running power of two: the initial state's own scale, raised to
 // upV of every chunk already applied. Power-of-two scales keep every fp16 operand in range and make
 // the whole path exactly linear under power-of-two scaling of (v, S0).
-// Barriers: fullB/fullN/fullP[s] (loads landed), emptyB[s] (the products of the stage's chunk are
-// done: an MMA commit), emptyN/emptyP[s] (each state warp has read N / P U), opReady (each state
-// warp has written S_h), bar_d[p] (the products into D[p] are done). Every wait is bounded; a wait
-// that runs out raises the CTA's abort flag and GDR_ERR_TIMEOUT, and the CTA drains and exits.
+// Barriers: fullB[s] (the stage's operand landed), emptyB[s] (the products that read it are done:
+// an MMA commit), opReady (each state warp has written its part of S_h), bar_d[p] (the products into
+// D[p] are done). Every wait is bounded; a wait that runs out raises the CTA's abort flag and
+// GDR_ERR_TIMEOUT, and the CTA drains and exits.
 constexpr int kChainThreads = 384;
-constexpr int kChainStages = 2;
+constexpr int kChainStages = 3;
 constexpr uint32_t kCBBytes = 49152;                      // [M' atom 0 | Q' atom 0 | M' atom 1 | Q' atom 1]
 constexpr uint32_t kCAtom = 24576;                        // one 192-row K atom of the B operand
-constexpr uint32_t kCNOff = kCBBytes;                     // N slices
-constexpr uint32_t kCPUOff = kCNOff + kNBytes;            // P U slices
-constexpr uint32_t kCStageBytes = kCPUOff + kPUBytes;     // 98304
-constexpr uint32_t kChainSmem = kChainStages * kCStageBytes + 1024;
+constexpr uint32_t kCOTile = kChainStages * kCBBytes;     // 8 warp tiles [32 positions][32 values] bf16
+constexpr uint32_t kChainSmem = kCOTile + 8 * 2048 + 1024;
 constexpr uint32_t kTmemChain = 512;                      // D[0] at 0, D[1] at 192 (192 columns each), S_h at 384
 constexpr uint32_t kTA = 384;
 constexpr uint32_t kStateBar = 1, kStateCount = 256;      // named barrier of the eight state warps
-constexpr int kChainPrefetch = 6;                         // ring loads prefetch the chunk this far ahead into L2
-static_assert(kCStageBytes % 1024 == 0 && kChainSmem <= 227 * 1024, "chain kernel shared memory");
+constexpr int kChainPrefetch = 6;                         // units prefetched into L2 this far ahead
+static_assert(kCBBytes % 1024 == 0 && kChainSmem <= 227 * 1024, "chain kernel shared memory");
 
 // 1 / x for a power of two x (exact)
 __device__ __forceinline__ float pow2_inverse(float x) { return __uint_as_float((254u << 23) - __float_as_uint(x)); }
+
+// This thread's rows of a unit: N^T row v, keys 64 hf .. + 63 (its half of the 256-byte row, chunk j
+// at (j & 8) | ((j & 7) ^ (v % 8))), (P U)^T row v, positions 32 hf .. + 31 (chunk j at j ^ (v % 8)),
+// and the scale block; plain loads through L1 (the workspace is read-only for this kernel).
+struct ChainRows {
+  uint4 n[8];
+  uint4 pu[4];
+  float4 sv;
+};
+__device__ __forceinline__ void load_chain_rows(ChainRows& r, const uint8_t* ub, int v, int hf) {
+  const uint8_t* nrow = ub + kUnitN + v * 256;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int j = 8 * hf + q;
+    r.n[q] = __ldg(reinterpret_cast<const uint4*>(nrow + (((j & 8) | ((j & 7) ^ (v & 7))) << 4)));
+  }
+  const uint8_t* prow = ub + kUnitPU + v * 128;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) r.pu[q] = __ldg(reinterpret_cast<const uint4*>(prow + (((4 * hf + q) ^ (v & 7)) << 4)));
+  r.sv = __ldg(reinterpret_cast<const float4*>(ub + kUnitS));
+}
 
 __global__ void __launch_bounds__(kChainThreads, 1)
 chunk_chain_kernel(const ChunkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t fullB[kChainStages], fullN[kChainStages], fullP[kChainStages];
-  __shared__ uint64_t emptyB[kChainStages], emptyN[kChainStages], emptyP[kChainStages];
+  __shared__ uint64_t fullB[kChainStages], emptyB[kChainStages];
   __shared__ uint64_t bar_d[2], opReady;
-  __shared__ __align__(16) float4 scl[kChainStages];   // Gamma_C, upV of the chunk in each stage
   __shared__ uint32_t s0max[8];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -1044,11 +1061,7 @@ chunk_chain_kernel(const ChunkArgs a) {
   if (tid == 0) {
     for (int s = 0; s < kChainStages; ++s) {
       mbar_init(&fullB[s], 1);
-      mbar_init(&fullN[s], 1);
-      mbar_init(&fullP[s], 1);
       mbar_init(&emptyB[s], 1);
-      mbar_init(&emptyN[s], 8);
-      mbar_init(&emptyP[s], 8);
     }
     mbar_init(&bar_d[0], 1);
     mbar_init(&bar_d[1], 1);
@@ -1076,62 +1089,31 @@ chunk_chain_kernel(const ChunkArgs a) {
 
   if (skip) {
     // every thread of the CTA read the same index
-  } else if (warp == 9 || warp == 10) {
-    // ---------------- producers (lane 0): [M'; Q'] + N + scales (warp 9), P U (warp 10) ----------
+  } else if (warp == 9) {
+    // ---------------- producer (lane 0): the [M'; Q'] ring and the L2 prefetch ----------------
     if (lane == 0) {
       wait_prerequisite();   // the workspace is complete once the prep kernel has finished
-      const bool bn = warp == 9;
+      for (int cf = 0; cf < kChainPrefetch && cf < NC; ++cf) bulk_prefetch_l2(unit_base(a, b, h, cf), kUnitS + 16);
       int last = -1;
       for (int c = 0; c < NC; ++c) {
         const int s = c % kChainStages;
-        if (c >= kChainStages) {
-          const uint32_t ph = (uint32_t)((c / kChainStages) - 1) & 1u;
-          ok = bn ? (mbar_wait(&emptyB[s], ph, a.wait_budget) && mbar_wait(&emptyN[s], ph, a.wait_budget))
-                  : mbar_wait(&emptyP[s], ph, a.wait_budget);
-        }
+        if (c >= kChainStages)
+          ok = mbar_wait(&emptyB[s], (uint32_t)((c / kChainStages) - 1) & 1u, a.wait_budget);
         if (!ok || *(volatile int*)&abort_flag) break;
+        if (c + kChainPrefetch < NC) bulk_prefetch_l2(unit_base(a, b, h, c + kChainPrefetch), kUnitS + 16);
         const uint8_t* ub = unit_base(a, b, h, c);
-        uint8_t* st = sm + s * kCStageBytes;
-        // the chunk kChainPrefetch further on into L2, so that the ring's loads hit L2
-        if (c == 0) {
-          for (int cf = 0; cf < kChainPrefetch && cf < NC; ++cf) {
-            const uint8_t* uf = unit_base(a, b, h, cf);
-            if (bn) bulk_prefetch_l2(uf, kUnitPU);
-            else bulk_prefetch_l2(uf + kUnitPU, kPUBytes);
-          }
-        }
-        if (c + kChainPrefetch < NC) {
-          const uint8_t* uf = unit_base(a, b, h, c + kChainPrefetch);
-          if (bn) bulk_prefetch_l2(uf, kUnitPU);   // M', Q', N (contiguous)
-          else bulk_prefetch_l2(uf + kUnitPU, kPUBytes);
-        }
-        if (bn) {
-          mbar_arrive_expect_tx(&fullB[s], kCBBytes);
-          bulk_load(st, ub, 16384, &fullB[s]);                               // M' atom 0
-          bulk_load(st + 16384, ub + kUnitQ, 8192, &fullB[s]);               // Q' atom 0
-          bulk_load(st + kCAtom, ub + 16384, 16384, &fullB[s]);              // M' atom 1
-          bulk_load(st + kCAtom + 16384, ub + kUnitQ + 8192, 8192, &fullB[s]);   // Q' atom 1
-          mbar_arrive_expect_tx(&fullN[s], kNBytes + kSCopy);
-          bulk_load(st + kCNOff, ub + kUnitN, kNBytes, &fullN[s]);
-          bulk_load(&scl[s], ub + kUnitS, kSCopy, &fullN[s]);
-        } else {
-          mbar_arrive_expect_tx(&fullP[s], kPUBytes);
-          bulk_load(st + kCPUOff, ub + kUnitPU, kPUBytes, &fullP[s]);
-        }
+        uint8_t* st = sm + s * kCBBytes;
+        mbar_arrive_expect_tx(&fullB[s], kCBBytes);
+        bulk_load(st, ub, 16384, &fullB[s]);                               // M' atom 0
+        bulk_load(st + 16384, ub + kUnitQ, 8192, &fullB[s]);               // Q' atom 0
+        bulk_load(st + kCAtom, ub + 16384, 16384, &fullB[s]);              // M' atom 1
+        bulk_load(st + kCAtom + 16384, ub + kUnitQ + 8192, 8192, &fullB[s]);   // Q' atom 1
         last = c;
       }
       if (!ok) {
         // drain: the copies of the last issued chunks land before the CTA's memory is released
-        for (int c = (last - kChainStages + 1 > 0 ? last - kChainStages + 1 : 0); c <= last; ++c) {
-          const int s = c % kChainStages;
-          const uint32_t ph = (uint32_t)(c / kChainStages) & 1u;
-          if (bn) {
-            mbar_wait(&fullB[s], ph, kDrainBudget);
-            mbar_wait(&fullN[s], ph, kDrainBudget);
-          } else {
-            mbar_wait(&fullP[s], ph, kDrainBudget);
-          }
-        }
+        for (int c = (last - kChainStages + 1 > 0 ? last - kChainStages + 1 : 0); c <= last; ++c)
+          mbar_wait(&fullB[c % kChainStages], (uint32_t)(c / kChainStages) & 1u, kDrainBudget);
       }
     }
   } else if (warp == 8) {
@@ -1145,7 +1127,7 @@ chunk_chain_kernel(const ChunkArgs a) {
              mbar_wait(&opReady, (uint32_t)c & 1u, a.wait_budget);
         if (!ok || *(volatile int*)&abort_flag) break;
         tc_fence_after();
-        const uint32_t bb = smem_u32(sm + s * kCStageBytes);
+        const uint32_t bb = smem_u32(sm + s * kCBBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_f16_tmem_a(tb + 192 * p, tb + kTA + kk * 8, smem_desc(bb + (kk >> 2) * kCAtom + (kk & 3) * 32, 16, 1024),
@@ -1194,33 +1176,19 @@ chunk_chain_kernel(const ChunkArgs a) {
       if (lane == 0) mbar_arrive(&opReady);
     };
     write_state_operand(inv);
-    __nv_bfloat16* orow = a.o + (((size_t)b * a.L) * a.Hv + h) * kD + v;   // o[b][pos][h][v] = orow[pos Hv D]
-    const size_t ostride = (size_t)a.Hv * kD;
+    wait_prerequisite();   // the workspace is complete once the prep kernel has finished
+    ChainRows rows;
+    load_chain_rows(rows, unit_base(a, b, h, 0), v, hf);
+    uint8_t* otile = sm + kCOTile + warp * 2048;                 // [32 positions][32 values] bf16
+    const size_t ostride = (size_t)a.Hv * kD;                    // elements between positions of o
+    __nv_bfloat16* obase = a.o + ((size_t)b * a.L * a.Hv + h) * kD + 32 * (warp & 3) + 8 * (lane & 3);
     for (int c = 0; c < NC; ++c) {
-      const int s = c % kChainStages, p = c & 1;
-      const uint32_t ph = (uint32_t)(c / kChainStages) & 1u;
-      const uint8_t* st = sm + s * kCStageBytes;
-      float gc = 0.f, upV = 0.f;
-      uint4 nv[8];   // N^T[v][keys 64 hf .. + 63], fp16
-      ok = ok && mbar_wait(&fullN[s], ph, a.wait_budget) && !*(volatile int*)&abort_flag;
-      if (ok) {
-        // this thread's N^T row (value column v, its 64 keys), read while the product of this chunk runs
-        const float4 sv = scl[s];
-        gc = sv.x;
-        upV = sv.y;
-        const uint8_t* nrow = st + kCNOff + v * 256;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int j = 8 * hf + q;
-          nv[q] = *reinterpret_cast<const uint4*>(nrow + (((j & 8) | ((j & 7) ^ (v & 7))) << 4));
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&emptyN[s]);
-      }
-      ok = ok && mbar_wait(&bar_d[p], (uint32_t)(c >> 1) & 1u, a.wait_budget);
-      float sc_next = sc;
-      if (ok) {
-        tc_fence_after();
+      const int p = c & 1;
+      const float gc = rows.sv.x, upV = rows.sv.y;
+      ok = ok && mbar_wait(&bar_d[p], (uint32_t)(c >> 1) & 1u, a.wait_budget) && !*(volatile int*)&abort_flag;
+      if (!ok) break;
+      tc_fence_after();
+      {
         uint32_t d[64];
         tmem_ld32_nowait(tb + lane_base + 192 * p + 64 * hf, d);
         tmem_ld32_nowait(tb + lane_base + 192 * p + 64 * hf + 32, d + 32);
@@ -1228,33 +1196,46 @@ chunk_chain_kernel(const ChunkArgs a) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           float n[8];
-          unpack8_f16(nv[q], n);
+          unpack8_f16(rows.n[q], n);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             S[8 * q + e] = fmaf(gc, S[8 * q + e], fmaf(sc, __uint_as_float(d[8 * q + e]), upV * n[e]));
         }
-        sc_next = fmaxf(sc, upV);
-        if (c + 1 < NC) write_state_operand(pow2_inverse(sc_next));   // the next product may start
       }
-      // the output rows of chunk c (overlapping the next product): o = sc D_o + upV (P U)^T, written
-      // straight to global memory (a warp's store covers 64 contiguous bytes of one position's row)
-      ok = ok && mbar_wait(&fullP[s], ph, a.wait_budget);
-      if (ok) {
+      const float sc_next = fmaxf(sc, upV);
+      if (c + 1 < NC) {
+        write_state_operand(pow2_inverse(sc_next));   // the next product may start
+#pragma unroll
+        for (int q = 0; q < 8; ++q) rows.n[q] = __ldg(reinterpret_cast<const uint4*>(
+            unit_base(a, b, h, c + 1) + kUnitN + v * 256 + ((((8 * hf + q) & 8) | (((8 * hf + q) & 7) ^ (v & 7))) << 4)));
+      }
+      // the output of chunk c (overlapping the next product): o = sc D_o + upV (P U)^T
+      {
         float ov[32], pu[32];
         tmem_ld32(tb + lane_base + 192 * p + 128 + 32 * hf, ov);
-        const uint8_t* prow = st + kCPUOff + v * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          unpack8_f16(*reinterpret_cast<const uint4*>(prow + (((4 * hf + q) ^ (v & 7)) << 4)), pu + 8 * q);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&emptyP[s]);
-        const int p0 = c * kChunk + 32 * hf;
+        for (int q = 0; q < 4; ++q) unpack8_f16(rows.pu[q], pu + 8 * q);
+        __syncwarp();   // the previous chunk's tile has been read by every lane
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          if (p0 + e < a.L) orow[(size_t)(p0 + e) * ostride] = __float2bfloat16_rn(fmaf(sc, ov[e], upV * pu[e]));
+          *reinterpret_cast<__nv_bfloat16*>(otile + e * 64 + lane * 2) = __float2bfloat16_rn(fmaf(sc, ov[e], upV * pu[e]));
+        __syncwarp();
+        const int p0 = c * kChunk + 32 * hf;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int r = 8 * m + (lane >> 2);
+          const uint4 w = *reinterpret_cast<const uint4*>(otile + r * 64 + (lane & 3) * 16);
+          if (p0 + r < a.L) *reinterpret_cast<uint4*>(obase + (size_t)(p0 + r) * ostride) = w;
+        }
+      }
+      if (c + 1 < NC) {
+        const uint8_t* un = unit_base(a, b, h, c + 1);
+        const uint8_t* prow = un + kUnitPU + v * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) rows.pu[q] = __ldg(reinterpret_cast<const uint4*>(prow + (((4 * hf + q) ^ (v & 7)) << 4)));
+        rows.sv = __ldg(reinterpret_cast<const float4*>(un + kUnitS));
       }
       sc = sc_next;
-      if (!ok) break;
     }
     if (ok && a.S_T) {
       float* so = a.S_T + ((size_t)b * a.Hv + h) * kD * kD;
