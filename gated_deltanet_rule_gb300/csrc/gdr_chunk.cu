@@ -55,6 +55,8 @@ namespace {
 constexpr float kScale = 0.08838834764831845f;   // 128^-0.5
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kDrainBudget = 2000000000ll;  // cycles (~1 s) an aborting CTA waits for its own copies
+constexpr int kSlices = 4;                        // value-column slices (state CTAs) per value head
+constexpr int kN = kD / kSlices;                  // 32 value columns per state CTA
 
 // Workspace. Per (row, value head, chunk) unit:
 constexpr uint32_t kMBytes = 32768;     // M': 128 x 128 fp16, two 64-column 128B-swizzled K-atoms
@@ -116,6 +118,8 @@ __device__ __forceinline__ void pow2_scales(float m, float& up, float& dn) {
   up = __uint_as_float((uint32_t)(127 + e) << 23);
   dn = __uint_as_float((uint32_t)(127 - e) << 23);
 }
+// 1 / x for a power of two x (exact)
+__device__ __forceinline__ float pow2_inverse(float x) { return __uint_as_float((254u << 23) - __float_as_uint(x)); }
 // Largest |x| over the 8 bf16 values of a 16-byte chunk, as bf16 magnitude bits (|x| orders like
 // its bits with the sign cleared).
 __device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 w) {
@@ -210,8 +214,7 @@ __device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, 
   } else {
     // warps 2-7 meanwhile: the k and v tiles to fp16 in place, for the fp16 products (the Gram MMA
     // that read k as bf16 has completed); 2048 chunks of 16 B, k atoms then v atoms, each tile
-    // scaled by its power of two (dnK, dnV: the tile's largest magnitude lands in [0.5, 1), so
-    // every finite bf16 input fits fp16's range)
+    // times its power of two (dnK, dnV; dnK is 1 unless k's tile needs scaling)
     for (int chunk16 = tid - 64; chunk16 < 2048; chunk16 += kPrepThreads - 64) {
       const int which = chunk16 >> 9, off = (chunk16 & 511) * 16;
       const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPVt + (which - 2) * 16384);
@@ -524,10 +527,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   }
   __syncthreads();
-  // the unit's power-of-two scales: k and v enter the fp16 products as k dnK and v dnV; 2^eK = upK
-  // is folded into the scalings that multiply K (A1 and sk), so W, M' and the rest come out as
-  // before, while U, N and P U stay in v's scale (upV is carried to the state kernel)
-  // (recomputed from tile_max where they are used, so that no register holds them across the unit)
+  // The unit's power-of-two scales: k and v enter the fp16 products as k dnK and v dnV; upK = 1 / dnK
+  // is folded into the scalings that multiply K (A1 and sk), so W, M' and the rest come out as before,
+  // while U, N and P U are formed in v's scale (upV goes to the state kernel with Gamma_C). They are
+  // recomputed from tile_max where they are used, so that no register holds them across the unit.
   auto unit_scales = [&](float& upK, float& dnK, float& upV, float& dnV) {
     const uint32_t mk = max(tile_max[0], max(tile_max[1], tile_max[2]));
     const uint32_t mv = max(tile_max[3], max(tile_max[4], tile_max[5]));
@@ -696,20 +699,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_before();
   __syncthreads();
 
-  // P W into columns 0-127 of TMEM lanes 0-63 (M = 128: operand rows 64-127 run past P into rows
-  // that nobody reads), and (P U)^T = U^T P^T into columns 128-191 of all 128 lanes (lane = value
-  // column: U as the MN-major A operand, P as the K-major B operand, N = 64 positions)
+  // P W into columns 0-127 of TMEM lanes 0-63 and P U into columns 128-255 of lanes 64-127
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t id_pw = idesc_f16(128, 128, false, true), id_pu = idesc_f16(128, 64, true, false);
+    const uint32_t idesc = idesc_f16(128, 128, false, true);
     const uint32_t pa = smem_u32(sm + kPP), wu = smem_u32(sm + kPV);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_bf16(tb, smem_desc(pa + kk * 32, 16, 1024), smem_desc(wu + kk * 2048, 8192, 1024), id_pw, kk > 0);
+      mma_bf16(tb, smem_desc(pa + kk * 32, 16, 1024), smem_desc(wu + kk * 2048, 8192, 1024), idesc, kk > 0);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_bf16(tb + 128, smem_desc(wu + 16384 + kk * 2048, 8192, 1024), smem_desc(pa + kk * 32, 16, 1024), id_pu,
-               kk > 0);
+      mma_bf16(tb + 128, smem_desc(pa - 8192 + kk * 32, 16, 1024), smem_desc(wu + 16384 + kk * 2048, 8192, 1024),
+               idesc, kk > 0);
     mma_commit(&bar_mma);
   }
   ok = wait_mma();
@@ -717,13 +718,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_after();
 
   {
-    // warps 0, 1, 4, 5 (lanes 0-63): Q'_i = sq_i q_i - (P W)_i, the fp16 image, on columns cb .. cb + 63,
-    // staged over the consumed W operand. Every warp: (P U)^T row v = TMEM lane (value column),
-    // positions 32 (w / 4) .. + 31, staged over the consumed U operand as [128 values][64 positions]
-    // fp16 rows of 128 bytes, 16-byte chunk j of row v at chunk j ^ (v % 8). Gamma_C over P.
+    // warps 0, 1, 4, 5 (lanes 0-63): Q'_i = sq_i q_i - (P W)_i, the fp16 image, on columns cb .. cb + 63;
+    // warps 2, 3, 6, 7 (lanes 64-127): (P U)_i, the fp16 slices, on columns cb .. cb + 63. Both are
+    // staged over the consumed [W | U] operand, Gamma_C over P.
     const int row = 32 * (warp & 3) + lane, i = row & 63, cb = (warp >> 2) * 64;
+    float w[64];
     if (row < 64) {
-      float w[64];
       const float sq = Gam[i] * qinv[i] * kScale;
       tmem_ld64(tb + lane_base + cb, w);
 #pragma unroll
@@ -741,14 +741,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         *reinterpret_cast<uint4*>(sm + kPV + off) = pack8_f16(v);
       }
-    }
-    {
-      float pu[32];
-      const int hp = warp >> 2;
-      tmem_ld32(tb + lane_base + 128 + 32 * hp, pu);
+    } else {
+      tmem_ld64(tb + lane_base + 128 + cb, w);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(sm + kPV + 16384 + row * 128 + (((4 * hp + q) ^ (row & 7)) << 4)) = pack8_f16(pu + 8 * q);
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const int col = cb + q8 * 8;
+        *reinterpret_cast<uint4*>(sm + kPV + 16384 + (col >> 5) * 4096 + swz64(i * 64 + (q8 & 3) * 16)) =
+            pack8_f16(w + q8 * 8);
+      }
     }
     if (tid == 0) {
       float upK, dnK, upV, dnV;
@@ -760,22 +760,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_before();
   __syncthreads();
 
-  // K^T (sk W) = -M' and (sk U)^T K = N^T into columns 0-255 (the P W and (P U)^T results have been
-  // read); Q', (P U)^T and Gamma_C leave for the workspace meanwhile
+  // K^T [sk W | sk U] = [-M' | N] into columns 0-255 (the P [W | U] results have been read); Q',
+  // P U and Gamma_C leave for the workspace meanwhile
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t idesc = idesc_f16(128, 128, true, true);
-    const uint32_t kt = smem_u32(sm + kPK0);    // k atoms (M / N blocks) at +8192 and +24576: stride 16384
+    const uint32_t idesc = idesc_f16(128, 256, true, true);
+    const uint32_t kt = smem_u32(sm + kPK0);    // k atoms (M blocks) at +8192 and +24576: stride 16384
     const uint32_t wsu = smem_u32(sm + kPWS);
-    // -M' = K^T (sk W): lane = key (columns 0-127)
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16(tb, smem_desc(kt + kk * 2048, 16384, 1024), smem_desc(wsu + kk * 2048, 8192, 1024), idesc, kk > 0);
-    // N^T = (sk U)^T K: lane = value column (columns 128-255)
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      mma_bf16(tb + 128, smem_desc(wsu + 16384 + kk * 2048, 8192, 1024), smem_desc(kt + kk * 2048, 16384, 1024), idesc,
-               kk > 0);
     mma_commit(&bar_mma);
     if (!kFused) {
       bulk_store(ub + kUnitQ, sm + kPV, kQBytes);
@@ -789,9 +783,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_after();
 
   {
-    // every warp: lane i, columns cb .. cb + 63: of M' = -D[:, 0:128] (key row i; the fp16 K-major
-    // image over q and k, consumed) and of N^T = D[:, 128:256] (value row i), staged for bulk stores
-    // (per-thread 16-byte global stores of these row layouts are far slower)
+    // every warp: key row i = TMEM lane, columns cb .. cb + 63 of M' = -D[:, 0:128] (fp16 K-major
+    // image over q and k, consumed) and of N = D[:, 128:256] (fp16 slices over [sk W | sk U]),
+    // staged for bulk stores (per-thread 16-byte global stores of these row layouts are far slower)
     const int i = 32 * (warp & 3) + lane, cb = (warp >> 2) * 64;
     {
       float w[64];
@@ -806,15 +800,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
     {
-      // N^T row i (a value column), keys cb .. cb + 63, staged over the consumed [sk W | sk U] as
-      // [128 values][128 keys] fp16 rows of 256 bytes, 16-byte chunk j of row v at chunk
-      // (j & 8) | ((j & 7) ^ (v % 8))
       float n[64];
       tmem_ld64(tb + lane_base + 128 + cb, n);
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
-        const int j = (cb >> 3) + q8;
-        *reinterpret_cast<uint4*>(sm + kPWS + i * 256 + (((j & 8) | ((j & 7) ^ (i & 7))) << 4)) = pack8_f16(n + q8 * 8);
+        const int col = cb + q8 * 8;
+        *reinterpret_cast<uint4*>(sm + kPWS + (col >> 5) * 8192 + swz64(i * 64 + (q8 & 3) * 16)) =
+            pack8_f16(n + q8 * 8);
       }
     }
   }
@@ -900,39 +892,31 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       // S_T[i][v] for keys i = 64 hb .. + 63; N[i][v] from its staged fp16 slice
       float* so = a.S_T + (((size_t)b * a.Hv + h) * kD) * kD;
       const float gc = Gam[63];
-      const uint8_t* nrow = sm + kPWS + v * 256;   // N^T row v
+      const uint8_t* nsl = sm + kPWS + (v >> 5) * 8192;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         float d[32];
         tmem_ld32(tb + lane_base + 64 + 64 * hb + 32 * part, d);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int j = 8 * hb + 4 * part + q;
-          float n[8];
-          unpack8_f16(*reinterpret_cast<const uint4*>(nrow + (((j & 8) | ((j & 7) ^ (v & 7))) << 4)), n);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int i = 64 * hb + 32 * part + 8 * q + e;
-            so[(size_t)i * kD + v] = fmaf(gc, x0[32 * part + 8 * q + e], fmaf(upS, d[8 * q + e], upV * n[e]));
-          }
+        for (int e = 0; e < 32; ++e) {
+          const int i = 64 * hb + 32 * part + e;
+          const float n = __half2float(*reinterpret_cast<const __half*>(nsl + swz64(i * 64 + (v & 31) * 2)));
+          so[(size_t)i * kD + v] = fmaf(gc, x0[32 * part + e], fmaf(upS, d[e], upV * n));
         }
       }
     }
     if (write) {
-      // o at positions 32 hb .. + 31 of this chunk; (P U)^T[v][pos] from its staged row. The bf16
-      // rows are staged over the consumed Q' image and leave by one bulk store per position.
+      // o at positions 32 hb .. + 31 of this chunk; (P U)[pos][v] from its staged fp16 slice. The
+      // bf16 rows are staged over the consumed Q' image and leave by one bulk store per position.
       float ov[32];
       tmem_ld32(tb + lane_base + 192 + 32 * hb, ov);
-      const uint8_t* prow = sm + kPV + 16384 + v * 128;   // (P U)^T row v
-      float pu[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        unpack8_f16(*reinterpret_cast<const uint4*>(prow + (((4 * hb + q) ^ (v & 7)) << 4)), pu + 8 * q);
+      const uint8_t* psl = sm + kPV + 16384 + (v >> 5) * 4096;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int pos = 32 * hb + e;
+        const float pu = __half2float(*reinterpret_cast<const __half*>(psl + swz64(pos * 64 + (v & 31) * 2)));
         *reinterpret_cast<__nv_bfloat16*>(sm + kPV + pos * 256 + v * 2) =
-            __float2bfloat16_rn(fmaf(upS, ov[e], upV * pu[e]));
+            __float2bfloat16_rn(fmaf(upS, ov[e], upV * pu));
       }
     }
     fence_async_smem();
@@ -978,98 +962,91 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 }
 
 // -------------------------------------------------------------------------------------------
-// Kernel 2: sequential state recurrence over chunks; one CTA per (row, value head)
+// Kernel 2: sequential state recurrence over chunks; four CTAs per (row, value head)
 // -------------------------------------------------------------------------------------------
-// The chunk step S' = Gamma_C S + M' S + N and the chunk output o = Q' S + P U are formed
-// transposed: D = S_h^T [M'^T | Q'^T] with M = 128 (value columns), N = 192 (128 keys, then the
-// 64 positions of the chunk) and K = 128 (keys). The A operand is the fp16 copy S_h of the state,
-// kept in tensor memory (lane = value column, 32-bit column c = keys 2c and 2c + 1); the B operand
-// is the workspace's K-major images of M' (128 rows) and Q' (64 rows), loaded as one 192-row
-// operand. So the state product and the output product are one group of 8 MMAs per chunk, and a
-// thread's state update reads and writes only its own tensor-memory lane.
-//
-// Thread (warp w < 8, lane l) owns value column v = 32 (w % 4) + l: keys 64 (w / 4) .. + 63 of the
-// float32 state (registers) and positions 32 (w / 4) .. + 31 of every chunk's output. The workspace
-// holds N and P U transposed (row = value column), so each thread loads its own rows (and the chunk's
-// scale block) straight from L2 into registers, one chunk ahead; only [M'; Q'] passes through shared
-// memory, for the MMAs.
-//   warps 0-7: per chunk c, S = Gamma_C S + upV N + sc D (D from tensor memory), write
-//              S_h = S / sc' into the A operand for the next product, load the next chunk's rows,
-//              then the output values o = sc D_o + upV P U of chunk c: transposed through a 2 KB
-//              shared-memory tile per warp and stored as 16-byte pieces of the rows of o.
-//   warp 8:   issues the 8 MMAs of each chunk into D[c % 2] (two accumulators, so that the output
-//              of chunk c is read while the product of chunk c + 1 runs).
-//   warp 9:   loads [M'; Q'] into a 3-stage ring, and prefetches the units further ahead into L2.
-// Scales: N and P U arrive in their chunk's v scale (upV, a power of two, in the scale block); the
-// fp16 copy of S is S / sc with sc a running power of two: the initial state's own scale, raised to
-// upV of every chunk already applied. Power-of-two scales keep every fp16 operand in range and make
-// the whole path exactly linear under power-of-two scaling of (v, S0).
-// Barriers: fullB[s] (the stage's operand landed), emptyB[s] (the products that read it are done:
-// an MMA commit), opReady (each state warp has written its part of S_h), bar_d[p] (the products into
-// D[p] are done). Every wait is bounded; a wait that runs out raises the CTA's abort flag and
-// GDR_ERR_TIMEOUT, and the CTA drains and exits.
-constexpr int kChainThreads = 384;
-constexpr int kChainStages = 3;
-constexpr uint32_t kCBBytes = 49152;                      // [M' atom 0 | Q' atom 0 | M' atom 1 | Q' atom 1]
-constexpr uint32_t kCAtom = 24576;                        // one 192-row K atom of the B operand
-constexpr uint32_t kCOTile = kChainStages * kCBBytes;     // 8 warp tiles [32 positions][32 values] bf16
-constexpr uint32_t kChainSmem = kCOTile + 8 * 2048 + 1024;
-constexpr uint32_t kTmemChain = 512;                      // D[0] at 0, D[1] at 192 (192 columns each), S_h at 384
-constexpr uint32_t kTA = 384;
-constexpr uint32_t kStateBar = 1, kStateCount = 256;      // named barrier of the eight state warps
-constexpr int kChainPrefetch = 6;                         // units prefetched into L2 this far ahead
-static_assert(kCBBytes % 1024 == 0 && kChainSmem <= 227 * 1024, "chain kernel shared memory");
+// CTA s (blockIdx.x) owns value columns [32 s, 32 s + 32) of one value head. The four CTAs of a
+// head are independent: each reads the head's M' and Q' tiles itself (the other three read the
+// same lines, so they come from L2) and its own slices of N and P U. No CTA waits on another.
+// Warp roles (warp w reads TMEM lanes 32 (w % 4) .. + 31):
+//   warps 0-3: own the state rows (key row = tid, 32 value columns, float32 registers), form
+//              S = Gamma_C S + D + N and write its fp16 copy, the operand of the next products.
+//   warps 4, 5: output rows o = O' + P U for positions 0-63 (TMEM lanes 0-63); named barrier 2.
+//   warp 6: loads the chain ring (M', this CTA's N slice, Gamma_C) up to CS chunks ahead, and
+//           prefetches the chunk kPrefetchAhead beyond each load into L2.
+//   warp 7: issues the output product O' = Q' S, so that its issue time stays off the chain.
+//   warp 8: loads the output ring (Q', this CTA's P U slice) up to OS chunks ahead (with the
+//           same L2 prefetch).
+//   warp 9: issues the state product D = M' S (in a warp of its own, so that its issue is not
+//           serialised with the state update of a diverged state warp).
+// Per chunk c: chain stage c % CS (chFull / chFree: each state warp releases it after its
+// update), output stage c % OS (outFull / outFree: released by the output warps), state operand
+// q = c % kSb (opReady: the state warps have written S_c; sReady: the state product was issued, so
+// the output product may read it too; sFree: the output product has read it), TMEM buffers
+// p = c % 2 (D[p] with bar_d; O'[p] with bar_o: product done, oFree: the output warps have read
+// it). Every barrier completes once per CS, OS, kSb, 2 chunks or per chunk, and none can run two
+// phases ahead of its waiters.
+constexpr int kStateThreads = 320;
+constexpr uint32_t kOutBar = 2, kOutCount = 64;
+constexpr uint32_t kStateBar = 3;      // named barrier of the four state warps (S0 scale only)
+constexpr uint32_t kCStage = 40960;    // M' (two 16 KB K-atoms), then this CTA's N slice (8 KB)
+constexpr uint32_t kCN = 32768;
+constexpr uint32_t kOStage = 20480;    // Q' (two 8 KB K-atoms), then this CTA's P U slice (4 KB)
+constexpr uint32_t kOPU = 16384;
+constexpr uint32_t kTmemState = 128;   // D[2] at 0, 32; O'[2] at 64, 96
+// Rings: 3 chain and 3 output stages. After the rings: kSb fp16 state operands (MN-major, 128 rows
+// of 64 B). The M = 128 output product reads 8 KB past each Q' tile
+// (operand rows 64-127, whose products land in TMEM lanes nobody reads), which stays inside the
+// buffer because the state operands follow the output ring.
+constexpr int kPrefetchAhead = 3;      // ring loads also prefetch the chunk this far beyond them into L2
+constexpr int kSb = 5;                 // fp16 state operands: the output path may trail the chain by 4 chunks
+constexpr uint32_t state_smem(int cs, int os) { return cs * kCStage + os * kOStage + kSb * 8192 + 1024; }
+static_assert(kCN == kMBytes && kOPU == kQBytes, "stage layout");
 
-// 1 / x for a power of two x (exact)
-__device__ __forceinline__ float pow2_inverse(float x) { return __uint_as_float((254u << 23) - __float_as_uint(x)); }
-
-// This thread's rows of a unit: N^T row v, keys 64 hf .. + 63 (its half of the 256-byte row, chunk j
-// at (j & 8) | ((j & 7) ^ (v % 8))), (P U)^T row v, positions 32 hf .. + 31 (chunk j at j ^ (v % 8)),
-// and the scale block; plain loads through L1 (the workspace is read-only for this kernel).
-struct ChainRows {
-  uint4 n[8];
-  uint4 pu[4];
-  float4 sv;
-};
-__device__ __forceinline__ void load_chain_rows(ChainRows& r, const uint8_t* ub, int v, int hf) {
-  const uint8_t* nrow = ub + kUnitN + v * 256;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int j = 8 * hf + q;
-    r.n[q] = __ldg(reinterpret_cast<const uint4*>(nrow + (((j & 8) | ((j & 7) ^ (v & 7))) << 4)));
-  }
-  const uint8_t* prow = ub + kUnitPU + v * 128;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) r.pu[q] = __ldg(reinterpret_cast<const uint4*>(prow + (((4 * hf + q) ^ (v & 7)) << 4)));
-  r.sv = __ldg(reinterpret_cast<const float4*>(ub + kUnitS));
-}
-
-__global__ void __launch_bounds__(kChainThreads, 1)
-chunk_chain_kernel(const ChunkArgs a) {
+template <int CS, int OS>
+__global__ void __launch_bounds__(kStateThreads, 1)
+chunk_state_kernel(const ChunkArgs a) {
+  constexpr uint32_t kOffO = CS * kCStage;
+  constexpr uint32_t kOffSb = kOffO + OS * kOStage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t fullB[kChainStages], emptyB[kChainStages];
-  __shared__ uint64_t bar_d[2], opReady;
-  __shared__ uint32_t s0max[8];
+  __shared__ uint64_t chFull[CS], chFree[CS], outFull[OS], outFree[OS], bar_d, opReady, bar_o[2], oFree[2], sReady[kSb],
+      sFree[kSb];
+  __shared__ __align__(16) float4 gam_ring[CS];   // Gamma_C, upV of the chunk in each chain stage
+  __shared__ __align__(16) float4 out_scl[OS];    // Gamma_C, upV of the chunk in each output stage
+  __shared__ uint64_t vReady;                      // the row's largest v scale is in v_scale
+  __shared__ float v_scale;
+  __shared__ uint32_t s0max[6];                    // per warp 0-5: largest |S0| of its rows of the slice
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
-  const int h = blockIdx.x, b = blockIdx.y;
+  const int sl = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NC = a.NC;
 
   if (tid == 0) {
-    for (int s = 0; s < kChainStages; ++s) {
-      mbar_init(&fullB[s], 1);
-      mbar_init(&emptyB[s], 1);
+    for (int s = 0; s < CS; ++s) {
+      mbar_init(&chFull[s], 1);
+      mbar_init(&chFree[s], 4);
     }
-    mbar_init(&bar_d[0], 1);
-    mbar_init(&bar_d[1], 1);
-    mbar_init(&opReady, 8);
+    for (int s = 0; s < OS; ++s) {
+      mbar_init(&outFull[s], 1);
+      mbar_init(&outFree[s], 1);
+    }
+    mbar_init(&bar_d, 1);
+    mbar_init(&opReady, 4);
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(&bar_o[p], 1);
+      mbar_init(&oFree[p], 1);
+    }
+    for (int q = 0; q < kSb; ++q) {
+      mbar_init(&sReady[q], 1);
+      mbar_init(&sFree[q], 1);
+    }
+    mbar_init(&vReady, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(&tmem_base, kTmemChain);
+  if (warp == 0) tmem_alloc(&tmem_base, kTmemState);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1087,172 +1064,266 @@ chunk_chain_kernel(const ChunkArgs a) {
     if (skip && tid == 0) set_error(a.err, kErrDeviceIndex);
   }
 
+  // The scale sc of the fp16 copy of the state: the power of two of the largest of |S0| over this
+  // CTA's slice and of the v scales (upV) of every chunk of the row, constant over the row. The
+  // state warps (one key row per thread) and the output warps (two key rows per thread) each take
+  // the S0 part themselves; warp 6 takes the v part from the workspace's scale blocks.
+  auto state_scale = [&](float m, uint32_t bar, uint32_t count, int w0, int nw) -> float {
+    const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+    if (lane == 0) s0max[warp] = mw;
+    named_bar_and(bar, count, true);
+    uint32_t mall = 0;
+    for (int w = w0; w < w0 + nw; ++w) mall = max(mall, s0max[w]);
+    float up, dn;
+    pow2_scales(__uint_as_float(mall), up, dn);
+    return up;
+  };
+
   if (skip) {
-    // every thread of the CTA read the same index
-  } else if (warp == 9) {
-    // ---------------- producer (lane 0): the [M'; Q'] ring and the L2 prefetch ----------------
+    // every CTA of the row reads the same index and skips
+  } else if (warp == 6 || warp == 8) {
+    // ---------------- producers (lane 0): the chain ring (warp 6) and the output ring (warp 8) ----
+    if (warp == 6) {
+      // the row's largest v scale (the scale blocks' second word), for the state scale
+      wait_prerequisite();
+      float mv = 0.f;
+      for (int c = lane; c < NC; c += 32) mv = fmaxf(mv, __ldg(reinterpret_cast<const float*>(unit_base(a, b, h, c) + kUnitS) + 1));
+      mv = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mv)));
+      if (lane == 0) {
+        v_scale = mv;
+        mbar_arrive(&vReady);
+      }
+    }
     if (lane == 0) {
       wait_prerequisite();   // the workspace is complete once the prep kernel has finished
-      for (int cf = 0; cf < kChainPrefetch && cf < NC; ++cf) bulk_prefetch_l2(unit_base(a, b, h, cf), kUnitS + 16);
-      int last = -1;
+      const bool chain = warp == 6;
+      const int S = chain ? CS : OS;
+      int last = -1;   // last chunk whose tiles were issued
       for (int c = 0; c < NC; ++c) {
-        const int s = c % kChainStages;
-        if (c >= kChainStages)
-          ok = mbar_wait(&emptyB[s], (uint32_t)((c / kChainStages) - 1) & 1u, a.wait_budget);
+        const int s = c % S;
+        if (c >= S) ok = mbar_wait(chain ? &chFree[s] : &outFree[s], ((c - S) / S) & 1, a.wait_budget);
         if (!ok || *(volatile int*)&abort_flag) break;
-        if (c + kChainPrefetch < NC) bulk_prefetch_l2(unit_base(a, b, h, c + kChainPrefetch), kUnitS + 16);
         const uint8_t* ub = unit_base(a, b, h, c);
-        uint8_t* st = sm + s * kCBBytes;
-        mbar_arrive_expect_tx(&fullB[s], kCBBytes);
-        bulk_load(st, ub, 16384, &fullB[s]);                               // M' atom 0
-        bulk_load(st + 16384, ub + kUnitQ, 8192, &fullB[s]);               // Q' atom 0
-        bulk_load(st + kCAtom, ub + 16384, 16384, &fullB[s]);              // M' atom 1
-        bulk_load(st + kCAtom + 16384, ub + kUnitQ + 8192, 8192, &fullB[s]);   // Q' atom 1
+        if (chain) {
+          uint8_t* st = sm + s * kCStage;
+          mbar_arrive_expect_tx(&chFull[s], kMBytes + 8192 + kSCopy);
+          bulk_load(st, ub, 16384, &chFull[s]);
+          bulk_load(st + 16384, ub + 16384, 16384, &chFull[s]);
+          bulk_load(st + kCN, ub + kUnitN + sl * 8192, 8192, &chFull[s]);
+          bulk_load(&gam_ring[s], ub + kUnitS, kSCopy, &chFull[s]);
+          if (c + kPrefetchAhead < NC) {   // the chunk kPrefetchAhead further on into L2
+            const uint8_t* uf = unit_base(a, b, h, c + kPrefetchAhead);
+            bulk_prefetch_l2(uf, kMBytes);
+            bulk_prefetch_l2(uf + kUnitN + sl * 8192, 8192);
+          }
+        } else {
+          uint8_t* st = sm + kOffO + s * kOStage;
+          mbar_arrive_expect_tx(&outFull[s], kQBytes + 4096 + kSCopy);
+          bulk_load(st, ub + kUnitQ, kQBytes, &outFull[s]);
+          bulk_load(st + kOPU, ub + kUnitPU + sl * 4096, 4096, &outFull[s]);
+          bulk_load(&out_scl[s], ub + kUnitS, kSCopy, &outFull[s]);
+          if (c + kPrefetchAhead < NC) {
+            const uint8_t* uf = unit_base(a, b, h, c + kPrefetchAhead);
+            bulk_prefetch_l2(uf + kUnitQ, kQBytes);
+            bulk_prefetch_l2(uf + kUnitPU + sl * 4096, 4096);
+          }
+        }
         last = c;
       }
       if (!ok) {
-        // drain: the copies of the last issued chunks land before the CTA's memory is released
-        for (int c = (last - kChainStages + 1 > 0 ? last - kChainStages + 1 : 0); c <= last; ++c)
-          mbar_wait(&fullB[c % kChainStages], (uint32_t)(c / kChainStages) & 1u, kDrainBudget);
+        // drain: the tiles of the last S issued chunks land before the CTA's memory is released
+        for (int c = (last - S + 1 > 0 ? last - S + 1 : 0); c <= last; ++c)
+          mbar_wait(chain ? &chFull[c % S] : &outFull[c % S], (c / S) & 1, kDrainBudget);
       }
     }
-  } else if (warp == 8) {
-    // ---------------- MMA issuer (lane 0) ----------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16(128, 192, false, false);
-      int last = -1;
-      for (int c = 0; c < NC; ++c) {
-        const int s = c % kChainStages, p = c & 1;
-        ok = mbar_wait(&fullB[s], (uint32_t)(c / kChainStages) & 1u, a.wait_budget) &&
-             mbar_wait(&opReady, (uint32_t)c & 1u, a.wait_budget);
-        if (!ok || *(volatile int*)&abort_flag) break;
-        tc_fence_after();
-        const uint32_t bb = smem_u32(sm + s * kCBBytes);
+  } else if (warp < 4) {
+    // ---------------- state warps ----------------
+    const int kr = tid;
+    float Sm[kN];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16_tmem_a(tb + 192 * p, tb + kTA + kk * 8, smem_desc(bb + (kk >> 2) * kCAtom + (kk & 3) * 32, 16, 1024),
-                         idesc, kk > 0);
-        mma_commit(&bar_d[p]);
-        mma_commit(&emptyB[s]);
-        last = c;
+    for (int n = 0; n < kN; ++n) Sm[n] = 0.f;
+    if (a.S0) {
+      const float* s0 = a.S0 + ((s0row * a.Hv + h) * kD + kr) * kD + sl * kN;
+#pragma unroll
+      for (int n = 0; n < kN; n += 4) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(s0 + n));
+        Sm[n] = x.x; Sm[n + 1] = x.y; Sm[n + 2] = x.z; Sm[n + 3] = x.w;
       }
-      if (!ok && last >= 0) mbar_wait(&bar_d[last & 1], (uint32_t)(last >> 1) & 1u, kDrainBudget);   // drain
     }
-  } else if (warp < 8) {
-    // ---------------- state and output warps ----------------
-    const int v = 32 * (warp & 3) + lane, hf = warp >> 2;
-    float S[64];
-    {
-      const float* s0 = a.S0 ? a.S0 + (s0row * a.Hv + h) * kD * kD : nullptr;
+    float m0 = 0.f;
 #pragma unroll
-      for (int e = 0; e < 64; ++e) S[e] = s0 ? __ldg(s0 + (size_t)(64 * hf + e) * kD + v) : 0.f;
-    }
-    // sc: the power of two of the head's largest |S0|
-    float sc, inv;
-    {
-      float m = 0.f;
+    for (int n = 0; n < kN; ++n) m0 = fmaxf(m0, fabsf(Sm[n]));
+    const float up0 = state_scale(m0, kStateBar, 128, 0, 4);
+    ok = mbar_wait(&vReady, 0, a.wait_budget);
+    const float sc = fmaxf(up0, v_scale), inv = pow2_inverse(sc);
+    // fp16 state operand q: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle, S / sc
+    auto write_state_operand = [&](int q) {
 #pragma unroll
-      for (int e = 0; e < 64; ++e) m = fmaxf(m, fabsf(S[e]));
-      const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
-      if (lane == 0) s0max[warp] = mw;
-      named_bar_and(kStateBar, kStateCount, true);
-      uint32_t mall = 0;
+      for (int ch = 0; ch < 4; ++ch) {
+        float t[8];
 #pragma unroll
-      for (int w8 = 0; w8 < 8; ++w8) mall = max(mall, s0max[w8]);
-      pow2_scales(__uint_as_float(mall), sc, inv);
-    }
-    // S_h = S / sc into this thread's 32 columns of the A operand, then signal the issuer
-    auto write_state_operand = [&](float iv) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t r16[16];
-#pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) r16[c2] = pack_f16x2(S[32 * hh + 2 * c2] * iv, S[32 * hh + 2 * c2 + 1] * iv);
-        tmem_st16_nowait(tb + lane_base + kTA + 32 * hf + 16 * hh, r16);
+        for (int e = 0; e < 8; ++e) t[e] = Sm[8 * ch + e] * inv;
+        *reinterpret_cast<uint4*>(sm + kOffSb + q * 8192 + swz64(kr * 64 + ch * 16)) = pack8_f16(t);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&opReady);
     };
-    write_state_operand(inv);
-    wait_prerequisite();   // the workspace is complete once the prep kernel has finished
-    ChainRows rows;
-    load_chain_rows(rows, unit_base(a, b, h, 0), v, hf);
-    uint8_t* otile = sm + kCOTile + warp * 2048;                 // [32 positions][32 values] bf16
-    const size_t ostride = (size_t)a.Hv * kD;                    // elements between positions of o
-    __nv_bfloat16* obase = a.o + ((size_t)b * a.L * a.Hv + h) * kD + 32 * (warp & 3) + 8 * (lane & 3);
-    for (int c = 0; c < NC; ++c) {
-      const int p = c & 1;
-      const float gc = rows.sv.x, upV = rows.sv.y;
-      ok = ok && mbar_wait(&bar_d[p], (uint32_t)(c >> 1) & 1u, a.wait_budget) && !*(volatile int*)&abort_flag;
+    write_state_operand(0);
+    fence_async_smem();
+    __syncwarp();
+    if (ok && lane == 0) mbar_arrive(&opReady);   // S_0 is in Sb[0]
+    for (int c = 0; c < NC && ok; ++c) {
+      const int cs = c % CS, p = c & 1, qn = (c + 1) % kSb;
+      const uint8_t* st = sm + cs * kCStage;
+      ok = mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
+      if (!ok) break;
+      // while the product D = M' S_c runs: S <- Gamma_C S + upV N (S_c is already in the fp16
+      // operand; N is in its chunk's v scale upV)
+      const float gc = gam_ring[cs].x, upV = gam_ring[cs].y;
+      const uint8_t* nrow = st + kCN;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        float nv[8];
+        unpack8_f16(*reinterpret_cast<const uint4*>(nrow + swz64(kr * 64 + ch * 16)), nv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], upV * nv[e]);
+      }
+      // Sb[qn] is rewritten below: the output product of chunk c + 1 - kSb must have read it
+      ok = mbar_wait(&bar_d, c & 1, a.wait_budget) &&
+           (c + 1 < kSb || mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget));
       if (!ok) break;
       tc_fence_after();
-      {
-        uint32_t d[64];
-        tmem_ld32_nowait(tb + lane_base + 192 * p + 64 * hf, d);
-        tmem_ld32_nowait(tb + lane_base + 192 * p + 64 * hf + 32, d + 32);
-        tmem_wait_ld32x2(d);
+      float d[kN];
+      tmem_ld32(tb + lane_base + 32 * p, d);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float n[8];
-          unpack8_f16(rows.n[q], n);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            S[8 * q + e] = fmaf(gc, S[8 * q + e], fmaf(sc, __uint_as_float(d[8 * q + e]), upV * n[e]));
-        }
+      for (int n = 0; n < kN; ++n) Sm[n] = fmaf(sc, d[n], Sm[n]);   // D = M' (S_c / sc)
+      write_state_operand(qn);
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&opReady);                        // S_{c+1} is in Sb[qn]
+        if (c + CS < NC) mbar_arrive(&chFree[cs]);   // this warp is done with N and Gamma_C
       }
-      const float sc_next = fmaxf(sc, upV);
-      if (c + 1 < NC) {
-        write_state_operand(pow2_inverse(sc_next));   // the next product may start
-#pragma unroll
-        for (int q = 0; q < 8; ++q) rows.n[q] = __ldg(reinterpret_cast<const uint4*>(
-            unit_base(a, b, h, c + 1) + kUnitN + v * 256 + ((((8 * hf + q) & 8) | (((8 * hf + q) & 7) ^ (v & 7))) << 4)));
-      }
-      // the output of chunk c (overlapping the next product): o = sc D_o + upV (P U)^T
-      {
-        float ov[32], pu[32];
-        tmem_ld32(tb + lane_base + 192 * p + 128 + 32 * hf, ov);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) unpack8_f16(rows.pu[q], pu + 8 * q);
-        __syncwarp();   // the previous chunk's tile has been read by every lane
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          *reinterpret_cast<__nv_bfloat16*>(otile + e * 64 + lane * 2) = __float2bfloat16_rn(fmaf(sc, ov[e], upV * pu[e]));
-        __syncwarp();
-        const int p0 = c * kChunk + 32 * hf;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int r = 8 * m + (lane >> 2);
-          const uint4 w = *reinterpret_cast<const uint4*>(otile + r * 64 + (lane & 3) * 16);
-          if (p0 + r < a.L) *reinterpret_cast<uint4*>(obase + (size_t)(p0 + r) * ostride) = w;
-        }
-      }
-      if (c + 1 < NC) {
-        const uint8_t* un = unit_base(a, b, h, c + 1);
-        const uint8_t* prow = un + kUnitPU + v * 128;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) rows.pu[q] = __ldg(reinterpret_cast<const uint4*>(prow + (((4 * hf + q) ^ (v & 7)) << 4)));
-        rows.sv = __ldg(reinterpret_cast<const float4*>(un + kUnitS));
-      }
-      sc = sc_next;
     }
     if (ok && a.S_T) {
-      float* so = a.S_T + ((size_t)b * a.Hv + h) * kD * kD;
+      float* dst = a.S_T + (((size_t)b * a.Hv + h) * kD + kr) * kD + sl * kN;
 #pragma unroll
-      for (int e = 0; e < 64; ++e) so[(size_t)(64 * hf + e) * kD + v] = S[e];
+      for (int n = 0; n < kN; n += 4)
+        *reinterpret_cast<float4*>(dst + n) = make_float4(Sm[n], Sm[n + 1], Sm[n + 2], Sm[n + 3]);
+    }
+  } else if (warp == 9) {
+    // ---------------- state-product issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(128, kN, false, true);
+      int last = -1;   // last chunk whose state product was issued
+      for (int c = 0; c < NC; ++c) {
+        const int cs = c % CS, p = c & 1, q = c % kSb;
+        ok = mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && mbar_wait(&opReady, c & 1, a.wait_budget);
+        if (!ok || *(volatile int*)&abort_flag) break;
+        tc_fence_after();
+        const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
+        const uint32_t sm_m = smem_u32(sm + cs * kCStage);
+        // D[p] = M' S_c: the product on the chain
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tb + 32 * p, smem_desc(sm_m + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                   smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
+        mma_commit(&bar_d);
+        mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
+        last = c;
+      }
+      if (!ok && last >= 0) mbar_wait(&bar_d, last & 1, kDrainBudget);   // drain
+    }
+  } else if (warp == 7) {
+    // ---------------- output-product issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(128, kN, false, true);
+      int last = -1;   // last chunk whose output product was issued
+      for (int c = 0; c < NC; ++c) {
+        const int os = c % OS, p = c & 1, q = c % kSb;
+        ok = mbar_wait(&outFull[os], (c / OS) & 1, a.wait_budget) &&
+             mbar_wait(&sReady[q], (c / kSb) & 1, a.wait_budget) &&
+             (c < 2 || mbar_wait(&oFree[p], ((c - 2) >> 1) & 1, a.wait_budget));
+        if (!ok || *(volatile int*)&abort_flag) break;
+        tc_fence_after();
+        const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
+        const uint32_t sm_q = smem_u32(sm + kOffO + os * kOStage);
+        // O'[p] = Q' S  (M = 128; operand rows 64-127 run past the tile and are not read)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tb + 64 + 32 * p, smem_desc(sm_q + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                   smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
+        mma_commit(&bar_o[p]);
+        mma_commit(&sFree[q]);
+        last = c;
+      }
+      if (!ok && last >= 0) mbar_wait(&bar_o[last & 1], (last >> 1) & 1, kDrainBudget);   // drain
+    }
+  } else {
+    // ---------------- output warps 4, 5 ----------------
+    const int i = tid - 128;   // position in the chunk = TMEM lane
+    float sc = 1.f;
+    {
+      // the state scale, as the state warps take it: S0 rows i and i + 64 of the slice here
+      float m0 = 0.f;
+      if (a.S0) {
+        for (int rr = i; rr < kD; rr += 64) {
+          const float* s0 = a.S0 + ((s0row * a.Hv + h) * kD + rr) * kD + sl * kN;
+#pragma unroll
+          for (int n = 0; n < kN; n += 4) {
+            const float4 x = __ldg(reinterpret_cast<const float4*>(s0 + n));
+            m0 = fmaxf(m0, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+          }
+        }
+      }
+      const float up0 = state_scale(m0, kOutBar, kOutCount, 4, 2);
+      ok = mbar_wait(&vReady, 0, a.wait_budget);
+      sc = fmaxf(up0, v_scale);
+    }
+    for (int c = 0; c < NC && ok; ++c) {
+      const int os = c % OS, p = c & 1;
+      const uint8_t* st = sm + kOffO + os * kOStage;
+      ok = mbar_wait(&outFull[os], (c / OS) & 1, a.wait_budget) &&
+           mbar_wait(&bar_o[p], (c >> 1) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
+      if (ok) {
+        tc_fence_after();
+        float qs[kN];
+        tmem_ld32(tb + lane_base + 64 + 32 * p, qs);
+        const int pos = c * 64 + i;
+        if (pos < a.L) {
+          float pu[kN];
+          const uint8_t* purow = st + kOPU;
+          const float upV = out_scl[os].y;   // P U is in its chunk's v scale
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+            unpack8_f16(*reinterpret_cast<const uint4*>(purow + swz64(i * 64 + ch * 16)), pu + 8 * ch);
+          __nv_bfloat16* orow_p = a.o + (((size_t)b * a.L + pos) * a.Hv + h) * kD + sl * kN;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = fmaf(sc, qs[8 * ch + e], upV * pu[8 * ch + e]);   // O' = Q' (S_c / sc)
+            *reinterpret_cast<uint4*>(orow_p + 8 * ch) = pack8_bf16(v);
+          }
+        }
+      }
+      tc_fence_before();
+      if (!named_bar_and(kOutBar, kOutCount, ok)) break;
+      if (tid == 128) {
+        mbar_arrive(&oFree[p]);
+        if (c + OS < NC) mbar_arrive(&outFree[os]);   // the Q' product complete, P U read
+      }
     }
   }
   if (!ok) {
     atomicExch(&abort_flag, 1);
     set_error(a.err, kErrTimeout);
   }
-  __syncwarp();
+  __syncwarp();         // the producer and issuer warps' lanes reconverge before the block barrier
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tb, kTmemChain);
+    tmem_dealloc(tb, kTmemState);
   }
 }
 
@@ -1337,7 +1408,7 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem);
+    e = cudaFuncSetAttribute(chunk_state_kernel<3, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(3, 3));
   if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkPrep);
   const long long units = (long long)a.B * a.Hv * a.NC;
@@ -1354,16 +1425,16 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   // launched as a programmatic dependent of the prep kernel: its set-up (barriers, tensor memory,
   // the initial state) overlaps the prep kernel's tail; its loads of the workspace wait for it
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.Hv, p.B, 1);
-  cfg.blockDim = dim3(kChainThreads, 1, 1);
-  cfg.dynamicSmemBytes = kChainSmem;
+  cfg.gridDim = dim3(kSlices, p.Hv, p.B);
+  cfg.blockDim = dim3(kStateThreads, 1, 1);
+  cfg.dynamicSmemBytes = state_smem(3, 3);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, chunk_chain_kernel, a);
+  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3>, a);
   stage_timer_end(slot, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
