@@ -987,7 +987,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // phases ahead of its waiters.
 constexpr int kStateThreads = 320;
 constexpr uint32_t kOutBar = 2, kOutCount = 64;
-constexpr uint32_t kStateBar = 3;      // named barrier of the four state warps (S0 scale only)
+constexpr uint32_t kStateBar = 3;      // named barrier of the four state warps (the state scale)
 constexpr uint32_t kCStage = 40960;    // M' (two 16 KB K-atoms), then this CTA's N slice (8 KB)
 constexpr uint32_t kCN = 32768;
 constexpr uint32_t kOStage = 20480;    // Q' (two 8 KB K-atoms), then this CTA's P U slice (4 KB)
@@ -1013,9 +1013,9 @@ chunk_state_kernel(const ChunkArgs a) {
       sFree[kSb];
   __shared__ __align__(16) float4 gam_ring[CS];   // Gamma_C, upV of the chunk in each chain stage
   __shared__ __align__(16) float4 out_scl[OS];    // Gamma_C, upV of the chunk in each output stage
-  __shared__ uint64_t vReady;                      // the row's largest v scale is in v_scale
-  __shared__ float v_scale;
-  __shared__ uint32_t s0max[6];                    // per warp 0-5: largest |S0| of its rows of the slice
+  __shared__ uint64_t scRdy[8];                    // the state scale of chunk c is in sc_ring[c % 8]
+  __shared__ float sc_ring[8];
+  __shared__ uint32_t smax[2][4];                  // per state warp: largest |S| of its rows of the slice
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -1042,7 +1042,7 @@ chunk_state_kernel(const ChunkArgs a) {
       mbar_init(&sReady[q], 1);
       mbar_init(&sFree[q], 1);
     }
-    mbar_init(&vReady, 1);
+    for (int r = 0; r < 8; ++r) mbar_init(&scRdy[r], 4);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -1064,36 +1064,10 @@ chunk_state_kernel(const ChunkArgs a) {
     if (skip && tid == 0) set_error(a.err, kErrDeviceIndex);
   }
 
-  // The scale sc of the fp16 copy of the state: the power of two of the largest of |S0| over this
-  // CTA's slice and of the v scales (upV) of every chunk of the row, constant over the row. The
-  // state warps (one key row per thread) and the output warps (two key rows per thread) each take
-  // the S0 part themselves; warp 6 takes the v part from the workspace's scale blocks.
-  auto state_scale = [&](float m, uint32_t bar, uint32_t count, int w0, int nw) -> float {
-    const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
-    if (lane == 0) s0max[warp] = mw;
-    named_bar_and(bar, count, true);
-    uint32_t mall = 0;
-    for (int w = w0; w < w0 + nw; ++w) mall = max(mall, s0max[w]);
-    float up, dn;
-    pow2_scales(__uint_as_float(mall), up, dn);
-    return up;
-  };
-
   if (skip) {
     // every CTA of the row reads the same index and skips
   } else if (warp == 6 || warp == 8) {
     // ---------------- producers (lane 0): the chain ring (warp 6) and the output ring (warp 8) ----
-    if (warp == 6) {
-      // the row's largest v scale (the scale blocks' second word), for the state scale
-      wait_prerequisite();
-      float mv = 0.f;
-      for (int c = lane; c < NC; c += 32) mv = fmaxf(mv, __ldg(reinterpret_cast<const float*>(unit_base(a, b, h, c) + kUnitS) + 1));
-      mv = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mv)));
-      if (lane == 0) {
-        v_scale = mv;
-        mbar_arrive(&vReady);
-      }
-    }
     if (lane == 0) {
       wait_prerequisite();   // the workspace is complete once the prep kernel has finished
       const bool chain = warp == 6;
@@ -1150,57 +1124,82 @@ chunk_state_kernel(const ChunkArgs a) {
         Sm[n] = x.x; Sm[n + 1] = x.y; Sm[n + 2] = x.z; Sm[n + 3] = x.w;
       }
     }
-    float m0 = 0.f;
+    // The fp16 copy of S_c is S_c / sc_c with sc_c the power of two of max |S_c| over this CTA's
+    // slice (a function of the state alone: results do not depend on where a sequence is split, and
+    // scaling (v, S0) by 2^k scales every sc_c by 2^k). The four state warps take the maximum
+    // together (one named barrier per chunk); sc_c goes to the output warps through sc_ring.
+    int mpar = 0;   // which half of smax the next maximum uses (a warp may start the next chunk's
+                    // maximum while another still reads this one)
+    auto slice_scale = [&](bool ok_in, float& up, float& dn) -> bool {
+      float m = 0.f;
 #pragma unroll
-    for (int n = 0; n < kN; ++n) m0 = fmaxf(m0, fabsf(Sm[n]));
-    const float up0 = state_scale(m0, kStateBar, 128, 0, 4);
-    ok = mbar_wait(&vReady, 0, a.wait_budget);
-    const float sc = fmaxf(up0, v_scale), inv = pow2_inverse(sc);
-    // fp16 state operand q: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle, S / sc
-    auto write_state_operand = [&](int q) {
+      for (int n = 0; n < kN; ++n) m = fmaxf(m, fabsf(Sm[n]));
+      const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+      if (lane == 0) smax[mpar][warp] = mw;
+      const bool all = named_bar_and(kStateBar, 128, ok_in);
+      const uint32_t mall = max(max(smax[mpar][0], smax[mpar][1]), max(smax[mpar][2], smax[mpar][3]));
+      mpar ^= 1;
+      pow2_scales(__uint_as_float(mall), up, dn);
+      return all;
+    };
+    // fp16 state operand q: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle
+    auto write_state_operand = [&](int q, float dn) {
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         float t[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t[e] = Sm[8 * ch + e] * inv;
+        for (int e = 0; e < 8; ++e) t[e] = Sm[8 * ch + e] * dn;
         *reinterpret_cast<uint4*>(sm + kOffSb + q * 8192 + swz64(kr * 64 + ch * 16)) = pack8_f16(t);
       }
     };
-    write_state_operand(0);
+    float sc, dn;
+    slice_scale(true, sc, dn);
+    write_state_operand(0, dn);
+    if (tid == 0) sc_ring[0] = sc;
     fence_async_smem();
     __syncwarp();
-    if (ok && lane == 0) mbar_arrive(&opReady);   // S_0 is in Sb[0]
-    for (int c = 0; c < NC && ok; ++c) {
+    if (lane == 0) {
+      mbar_arrive(&opReady);     // S_0 is in Sb[0]
+      mbar_arrive(&scRdy[0]);    // and its scale in sc_ring[0]
+    }
+    for (int c = 0; c < NC; ++c) {
       const int cs = c % CS, p = c & 1, qn = (c + 1) % kSb;
       const uint8_t* st = sm + cs * kCStage;
-      ok = mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
-      if (!ok) break;
-      // while the product D = M' S_c runs: S <- Gamma_C S + upV N (S_c is already in the fp16
-      // operand; N is in its chunk's v scale upV)
-      const float gc = gam_ring[cs].x, upV = gam_ring[cs].y;
-      const uint8_t* nrow = st + kCN;
+      ok = ok && mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
+      if (ok) {
+        // while the product D = M' S_c runs: S <- Gamma_C S + upV N (S_c is already in the fp16
+        // operand; N is in its chunk's v scale upV)
+        const float gc = gam_ring[cs].x, upV = gam_ring[cs].y;
+        const uint8_t* nrow = st + kCN;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        float nv[8];
-        unpack8_f16(*reinterpret_cast<const uint4*>(nrow + swz64(kr * 64 + ch * 16)), nv);
+        for (int ch = 0; ch < 4; ++ch) {
+          float nv[8];
+          unpack8_f16(*reinterpret_cast<const uint4*>(nrow + swz64(kr * 64 + ch * 16)), nv);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], upV * nv[e]);
+          for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], upV * nv[e]);
+        }
+        // Sb[qn] is rewritten below: the output product of chunk c + 1 - kSb must have read it
+        ok = mbar_wait(&bar_d, c & 1, a.wait_budget) &&
+             (c + 1 < kSb || mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget));
       }
-      // Sb[qn] is rewritten below: the output product of chunk c + 1 - kSb must have read it
-      ok = mbar_wait(&bar_d, c & 1, a.wait_budget) &&
-           (c + 1 < kSb || mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget));
-      if (!ok) break;
-      tc_fence_after();
-      float d[kN];
-      tmem_ld32(tb + lane_base + 32 * p, d);
+      if (ok) {
+        tc_fence_after();
+        float d[kN];
+        tmem_ld32(tb + lane_base + 32 * p, d);
 #pragma unroll
-      for (int n = 0; n < kN; ++n) Sm[n] = fmaf(sc, d[n], Sm[n]);   // D = M' (S_c / sc)
-      write_state_operand(qn);
+        for (int n = 0; n < kN; ++n) Sm[n] = fmaf(sc, d[n], Sm[n]);   // D = M' (S_c / sc_c)
+      }
+      // every state warp reaches this barrier once per chunk, so a warp that gave up stops them all
+      ok = slice_scale(ok, sc, dn);
+      if (!ok) break;
+      write_state_operand(qn, dn);
+      if (tid == 0) sc_ring[(c + 1) & 7] = sc;
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&opReady);                        // S_{c+1} is in Sb[qn]
+        mbar_arrive(&scRdy[(c + 1) & 7]);             // and its scale in sc_ring
         if (c + CS < NC) mbar_arrive(&chFree[cs]);   // this warp is done with N and Gamma_C
       }
     }
@@ -1261,29 +1260,12 @@ chunk_state_kernel(const ChunkArgs a) {
   } else {
     // ---------------- output warps 4, 5 ----------------
     const int i = tid - 128;   // position in the chunk = TMEM lane
-    float sc = 1.f;
-    {
-      // the state scale, as the state warps take it: S0 rows i and i + 64 of the slice here
-      float m0 = 0.f;
-      if (a.S0) {
-        for (int rr = i; rr < kD; rr += 64) {
-          const float* s0 = a.S0 + ((s0row * a.Hv + h) * kD + rr) * kD + sl * kN;
-#pragma unroll
-          for (int n = 0; n < kN; n += 4) {
-            const float4 x = __ldg(reinterpret_cast<const float4*>(s0 + n));
-            m0 = fmaxf(m0, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
-          }
-        }
-      }
-      const float up0 = state_scale(m0, kOutBar, kOutCount, 4, 2);
-      ok = mbar_wait(&vReady, 0, a.wait_budget);
-      sc = fmaxf(up0, v_scale);
-    }
     for (int c = 0; c < NC && ok; ++c) {
       const int os = c % OS, p = c & 1;
       const uint8_t* st = sm + kOffO + os * kOStage;
       ok = mbar_wait(&outFull[os], (c / OS) & 1, a.wait_budget) &&
-           mbar_wait(&bar_o[p], (c >> 1) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
+           mbar_wait(&bar_o[p], (c >> 1) & 1, a.wait_budget) &&
+           mbar_wait(&scRdy[c & 7], (c >> 3) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
       if (ok) {
         tc_fence_after();
         float qs[kN];
@@ -1293,6 +1275,7 @@ chunk_state_kernel(const ChunkArgs a) {
           float pu[kN];
           const uint8_t* purow = st + kOPU;
           const float upV = out_scl[os].y;   // P U is in its chunk's v scale
+          const float sc = sc_ring[c & 7];     // O' = Q' (S_c / sc_c)
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch)
             unpack8_f16(*reinterpret_cast<const uint4*>(purow + swz64(i * 64 + ch * 16)), pu + 8 * ch);
