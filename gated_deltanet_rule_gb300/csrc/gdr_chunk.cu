@@ -120,15 +120,6 @@ __device__ __forceinline__ void pow2_scales(float m, float& up, float& dn) {
 }
 // 1 / x for a power of two x (exact)
 __device__ __forceinline__ float pow2_inverse(float x) { return __uint_as_float((254u << 23) - __float_as_uint(x)); }
-// Largest |x| over the 8 bf16 values of a 16-byte chunk, as bf16 magnitude bits (|x| orders like
-// its bits with the sign cleared).
-__device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 w) {
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-  uint32_t m = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) m = max(m, max(u[e] & 0x7FFFu, (u[e] >> 16) & 0x7FFFu));
-  return m;
-}
 // bf16x2 word -> fp16x2 word of the values times s (a power of two)
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float s) {
   return pack_f16x2(__uint_as_float(w << 16) * s, __uint_as_float(w & 0xFFFF0000u) * s);
@@ -335,7 +326,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_base;
   __shared__ float gbuf[2][128];   // gates of the current and the next unit: g[64] | beta[64]
-  __shared__ uint32_t tile_max[6];   // per warp 4-6: largest |k| (0-2) and |v| (3-5) of the unit, bf16 bits
+  __shared__ uint32_t tile_max[5];   // largest |k_row|^2 (warps 2, 3: float bits), |v| (warps 4-6: bf16 bits)
+  __shared__ float unit_scl[4];      // upK, dnK, upV, dnV of the current unit
   __shared__ uint32_t s0max[kPrepThreads / 32];   // per-warp largest |S0| (float bits), fused apply
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -494,6 +486,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
     (tid < 64 ? qinv : kinv)[rr] = rsqrtf(s0 + s1 + 1e-6f);
+    // the largest squared row norm of k (for k's scale, which only guards fp16's range)
+    const uint32_t kn = __reduce_max_sync(0xffffffffu, __float_as_uint(s0 + s1));
+    if (warp >= 2 && lane == 0) tile_max[warp - 2] = kn;
   } else {
     // decay factors through the 16-block anchors: for j < 16 I <= i,
     // exp(gamma_i - gamma_j) = exp(gamma_i - gamma_16I) * exp(gamma_16I - gamma_j), both factors
@@ -508,39 +503,40 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         E2[I * 68 + j] = (j < 16 * I) ? ex2_approx(gam2[16 * I] - gam2[j]) : 0.f;
       }
     }
-    // the largest |k| and |v| of the tiles (two 8 KB atoms each), for their power-of-two scales:
-    // warp 4 + t, t < 3, takes 16-byte chunks t, t + 3, ... of the 2048
-    uint32_t mk = 0, mv = 0;
+    // the largest |v| of the tile (two 8 KB atoms), for its power-of-two scale: warp 4 + t, t < 3,
+    // takes 16-byte chunks t, t + 3, ... of the 1024, as per-halfword maxima of the bf16 magnitude
+    // bits (|x| orders like its bits with the sign cleared)
+    uint32_t mv2 = 0;
 #pragma unroll 4
-    for (int c16 = tid - 128; c16 < 2048; c16 += 96) {
-      const int which = c16 >> 9;
-      const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPVt + (which - 2) * 16384);
-      const uint32_t m = bf16x8_absmax_bits(*reinterpret_cast<const uint4*>(sm + base + (c16 & 511) * 16));
-      if (which < 2) mk = max(mk, m);
-      else mv = max(mv, m);
+    for (int c16 = tid - 128; c16 < 1024; c16 += 96) {
+      const uint4 w = *reinterpret_cast<const uint4*>(sm + kPVt + (c16 >> 9) * 16384 + (c16 & 511) * 16);
+      mv2 = __vmaxu2(mv2, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu), __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
     }
-    mk = __reduce_max_sync(0xffffffffu, mk);
-    mv = __reduce_max_sync(0xffffffffu, mv);
-    if (lane == 0) {
-      tile_max[warp - 4] = mk;
-      tile_max[warp - 1] = mv;
-    }
+    const uint32_t mv = __reduce_max_sync(0xffffffffu, max(mv2 & 0xFFFFu, mv2 >> 16));
+    if (lane == 0) tile_max[warp - 2] = mv;
   }
   __syncthreads();
   // The unit's power-of-two scales: k and v enter the fp16 products as k dnK and v dnV; upK = 1 / dnK
   // is folded into the scalings that multiply K (A1 and sk), so W, M' and the rest come out as before,
-  // while U, N and P U are formed in v's scale (upV goes to the state kernel with Gamma_C). They are
-  // recomputed from tile_max where they are used, so that no register holds them across the unit.
+  // while U, N and P U are formed in v's scale (upV goes to the state kernel with Gamma_C). v is
+  // always scaled (exactness under power-of-two scaling of v); k only when its largest row norm is
+  // outside [2^-6, 2^6), where k or the inverse norms folded into A1 and sk would leave fp16's
+  // normal range. Thread 0 publishes them in unit_scl for the uses after the next barrier.
   auto unit_scales = [&](float& upK, float& dnK, float& upV, float& dnV) {
-    const uint32_t mk = max(tile_max[0], max(tile_max[1], tile_max[2]));
-    const uint32_t mv = max(tile_max[3], max(tile_max[4], tile_max[5]));
-    // k is scaled when its largest |k| is outside [2^-6, 2^6): within it, both k and the inverse
-    // norms that the A1 and sk scalings fold in (>= 2^-6 / sqrt(128)) are normal fp16 numbers;
-    // v always, so that U, N and P U are formed in v's own scale
+    const float kn = sqrtf(__uint_as_float(max(tile_max[0], tile_max[1])));
+    const uint32_t mv = max(tile_max[2], max(tile_max[3], tile_max[4]));
     upK = dnK = 1.f;
-    if (mk >= 0x4280u || mk < 0x3C80u) pow2_scales(__uint_as_float(mk << 16), upK, dnK);
+    if (kn >= 64.f || (kn > 0.f && kn < 0.015625f)) pow2_scales(kn, upK, dnK);
     pow2_scales(__uint_as_float(mv << 16), upV, dnV);
   };
+  if (tid == 0) {
+    float upK, dnK, upV, dnV;
+    unit_scales(upK, dnK, upV, dnV);
+    unit_scl[0] = upK;
+    unit_scl[1] = dnK;
+    unit_scl[2] = upV;
+    unit_scl[3] = dnV;
+  }
   if (tid < 64) {
     float upK, dnK, upV, dnV;
     unit_scales(upK, dnK, upV, dnV);
@@ -629,18 +625,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   __syncthreads();
 
-  {
-    float upK, dnK, upV, dnV;
-    unit_scales(upK, dnK, upV, dnV);
-    invert_unit_lower(AT, Tm, Xs, sm, tid, dnK, dnV);
-  }
+  invert_unit_lower(AT, Tm, Xs, sm, tid, unit_scl[1], unit_scl[3]);
 
   // operand [A1; A2] = [T diag(beta Gamma ki); T diag(beta)], MN-major: K-row j holds column j of T
   {
     const int j = tid & 63, blk = (tid >> 6) & 1, hf = tid >> 7;
-    float upK, dnK, upV, dnV;
-    unit_scales(upK, dnK, upV, dnV);
-    const float s = blk ? bet[j] : bet[j] * Gam[j] * kinv[j] * upK;
+    const float s = blk ? bet[j] : bet[j] * Gam[j] * kinv[j] * unit_scl[0];
     const float4* trow = reinterpret_cast<const float4*>(AT + j * 68);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -750,11 +740,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             pack8_f16(w + q8 * 8);
       }
     }
-    if (tid == 0) {
-      float upK, dnK, upV, dnV;
-      unit_scales(upK, dnK, upV, dnV);
-      *reinterpret_cast<float4*>(sm + kPP) = make_float4(Gam[63], upV, 0.f, 0.f);
-    }
+    if (tid == 0) *reinterpret_cast<float4*>(sm + kPP) = make_float4(Gam[63], unit_scl[2], 0.f, 0.f);
   }
   fence_async_smem();
   tc_fence_before();
@@ -821,11 +807,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // (warp w, lane l) owns value v = 32 (w % 4) + l and keys / positions of half w / 4.
     tc_fence_after();
     const int v = 32 * (warp & 3) + lane, hb = warp >> 2;
-    float upV;
-    {
-      float upK, dnK, dnV;
-      unit_scales(upK, dnK, upV, dnV);
-    }
+    const float upV = unit_scl[2];
     const float* s0 = nullptr;
     bool write = true;
     if (a.S0) {
