@@ -129,6 +129,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float s) 
 // Kernel 1: per-chunk factors
 // -------------------------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
+constexpr uint32_t kVBar = 4;   // named barrier of warps 4-7 (v's scale)
 constexpr uint32_t kPQ0 = 0, kPK0 = 8192, kPQ1 = 16384, kPK1 = 24576;   // [q|k] K-atoms (Gram operand)
 constexpr uint32_t kPV = 32768;       // the v atoms' region; then the MN-major operand [W0 | W1 | U0 | U1];
                                       // then the staged Q' image and P U slices
@@ -163,7 +164,7 @@ static_assert(kPVt == kPK1 + 16384 && kPXs + 36 * 32 * 4 <= kPVt + 16384 && kPVt
 // zeroed once consumed, so that a row of AT restricted to a finished diagonal block is exactly a
 // column of T. Block products read rows of the left factor and columns of the right factor as
 // contiguous float4 runs, and skip the blocks that are zero by triangularity.
-__device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, int tid, float dnK, float dnV) {
+__device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, int tid, float dnK) {
   const int warp = tid >> 5, lane = tid & 31;
   // 1. diagonal 16-blocks (warps 0, 1): thread = (block, column c), computing column c of the
   //    block's inverse in registers, left-looking: x_i = -sum_{j < i} A_ij x_j for rows i > c (x_c = 1,
@@ -203,13 +204,13 @@ __device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, 
     for (int m4 = 0; m4 < 4; ++m4)
       trow[m4] = make_float4(x[4 * m4], x[4 * m4 + 1], x[4 * m4 + 2], x[4 * m4 + 3]);
   } else {
-    // warps 2-7 meanwhile: the k and v tiles to fp16 in place, for the fp16 products (the Gram MMA
-    // that read k as bf16 has completed); 2048 chunks of 16 B, k atoms then v atoms, each tile
-    // times its power of two (dnK, dnV; dnK is 1 unless k's tile needs scaling)
-    for (int chunk16 = tid - 64; chunk16 < 2048; chunk16 += kPrepThreads - 64) {
+    // warps 2-7 meanwhile: the k tile to fp16 in place, for the fp16 products (the Gram MMA that
+    // read k as bf16 has completed); 1024 chunks of 16 B, times dnK (1 unless k needs scaling).
+    // (v was converted, times its own power of two, while the Gram product ran.)
+    for (int chunk16 = tid - 64; chunk16 < 1024; chunk16 += kPrepThreads - 64) {
       const int which = chunk16 >> 9, off = (chunk16 & 511) * 16;
-      const uint32_t base = which == 0 ? kPK0 : (which == 1 ? kPK1 : kPVt + (which - 2) * 16384);
-      const float sc = which < 2 ? dnK : dnV;
+      const uint32_t base = which == 0 ? kPK0 : kPK1;
+      const float sc = dnK;
       uint4* p = reinterpret_cast<uint4*>(sm + base + off);
       uint4 w = *p;
       if (sc == 1.f)
@@ -326,7 +327,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_base;
   __shared__ float gbuf[2][128];   // gates of the current and the next unit: g[64] | beta[64]
-  __shared__ uint32_t tile_max[5];   // largest |k_row|^2 (warps 2, 3: float bits), |v| (warps 4-6: bf16 bits)
+  __shared__ uint32_t tile_max[6];   // largest |k_row|^2 (warps 2, 3: float bits), |v| (warps 4-7: bf16 bits)
   __shared__ float unit_scl[4];      // upK, dnK, upV, dnV of the current unit
   __shared__ uint32_t s0max[kPrepThreads / 32];   // per-warp largest |S0| (float bits), fused apply
 
@@ -503,17 +504,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         E2[I * 68 + j] = (j < 16 * I) ? ex2_approx(gam2[16 * I] - gam2[j]) : 0.f;
       }
     }
-    // the largest |v| of the tile (two 8 KB atoms), for its power-of-two scale: warp 4 + t, t < 3,
-    // takes 16-byte chunks t, t + 3, ... of the 1024, as per-halfword maxima of the bf16 magnitude
-    // bits (|x| orders like its bits with the sign cleared)
-    uint32_t mv2 = 0;
-#pragma unroll 4
-    for (int c16 = tid - 128; c16 < 1024; c16 += 96) {
-      const uint4 w = *reinterpret_cast<const uint4*>(sm + kPVt + (c16 >> 9) * 16384 + (c16 & 511) * 16);
-      mv2 = __vmaxu2(mv2, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu), __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
-    }
-    const uint32_t mv = __reduce_max_sync(0xffffffffu, max(mv2 & 0xFFFFu, mv2 >> 16));
-    if (lane == 0) tile_max[warp - 2] = mv;
   }
   __syncthreads();
   // The unit's power-of-two scales: k and v enter the fp16 products as k dnK and v dnV; upK = 1 / dnK
@@ -521,29 +511,52 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // while U, N and P U are formed in v's scale (upV goes to the state kernel with Gamma_C). v is
   // always scaled (exactness under power-of-two scaling of v); k only when its largest row norm is
   // outside [2^-6, 2^6), where k or the inverse norms folded into A1 and sk would leave fp16's
-  // normal range. Thread 0 publishes them in unit_scl for the uses after the next barrier.
-  auto unit_scales = [&](float& upK, float& dnK, float& upV, float& dnV) {
+  // normal range. They are published in unit_scl for the uses after the next barrier: k's by thread 0
+  // now, v's by warps 4-7, which take v's maximum and convert v while the Gram product completes.
+  auto k_scales = [&](float& upK, float& dnK) {
     const float kn = sqrtf(__uint_as_float(max(tile_max[0], tile_max[1])));
-    const uint32_t mv = max(tile_max[2], max(tile_max[3], tile_max[4]));
     upK = dnK = 1.f;
     if (kn >= 64.f || (kn > 0.f && kn < 0.015625f)) pow2_scales(kn, upK, dnK);
-    pow2_scales(__uint_as_float(mv << 16), upV, dnV);
   };
-  if (tid == 0) {
-    float upK, dnK, upV, dnV;
-    unit_scales(upK, dnK, upV, dnV);
-    unit_scl[0] = upK;
-    unit_scl[1] = dnK;
-    unit_scl[2] = upV;
-    unit_scl[3] = dnV;
-  }
   if (tid < 64) {
-    float upK, dnK, upV, dnV;
-    unit_scales(upK, dnK, upV, dnV);
+    float upK, dnK;
+    k_scales(upK, dnK);
     skv[tid] *= kinv[tid] * upK;
+    if (tid == 0) {
+      unit_scl[0] = upK;
+      unit_scl[1] = dnK;
+    }
   } else {
     const int I = 1 + ((tid - 64) >> 6), j = tid & 63;
     E2[I * 68 + j] *= kinv[j];
+  }
+  if (tid >= 128) {
+    // while the Gram product completes: the largest |v| of the tile (two 8 KB atoms), for its
+    // power-of-two scale; warp 4 + t takes 16-byte chunks t, t + 4, ... of the 1024, as per-halfword
+    // maxima of the bf16 magnitude bits (|x| orders like its bits with the sign cleared)
+    uint32_t mv2 = 0;
+#pragma unroll 4
+    for (int c16 = tid - 128; c16 < 1024; c16 += 128) {
+      const uint4 w = *reinterpret_cast<const uint4*>(sm + kPVt + (c16 >> 9) * 16384 + (c16 & 511) * 16);
+      mv2 = __vmaxu2(mv2, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu), __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
+    }
+    const uint32_t mv = __reduce_max_sync(0xffffffffu, max(mv2 & 0xFFFFu, mv2 >> 16));
+    if (lane == 0) tile_max[warp - 2] = mv;
+    named_bar_and(kVBar, 128, true);
+    // v's power of two, and v to fp16 in place times dnV (the Gram product does not read v)
+    float upV, dnV;
+    pow2_scales(__uint_as_float(max(max(tile_max[2], tile_max[3]), max(tile_max[4], tile_max[5])) << 16), upV, dnV);
+    if (tid == 128) {
+      unit_scl[2] = upV;
+      unit_scl[3] = dnV;
+    }
+#pragma unroll 4
+    for (int c16 = tid - 128; c16 < 1024; c16 += 128) {
+      uint4* p = reinterpret_cast<uint4*>(sm + kPVt + (c16 >> 9) * 16384 + (c16 & 511) * 16);
+      const uint4 w = *p;
+      *p = make_uint4(bf16x2_to_f16x2_scaled(w.x, dnV), bf16x2_to_f16x2_scaled(w.y, dnV),
+                      bf16x2_to_f16x2_scaled(w.z, dnV), bf16x2_to_f16x2_scaled(w.w, dnV));
+    }
   }
   if (tid == 0) bulk_wait_read();   // the previous unit's N store has read the AT / Tm region
   ok = wait_mma();
@@ -625,7 +638,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   __syncthreads();
 
-  invert_unit_lower(AT, Tm, Xs, sm, tid, unit_scl[1], unit_scl[3]);
+  invert_unit_lower(AT, Tm, Xs, sm, tid, unit_scl[1]);
 
   // operand [A1; A2] = [T diag(beta Gamma ki); T diag(beta)], MN-major: K-row j holds column j of T
   {
