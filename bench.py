@@ -357,6 +357,7 @@ def run_gb300(args) -> dict | None:
         line["rows"]["next_f2_gated_rmsnorm"] = run_epilogue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
         line["rows"]["next_f4_backward"] = run_backward(reps=max(3, min(args.steps, 10)), warmup=args.warmup)
         line["rows"]["configs"] = run_configs(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
+        line["rows"]["next_f3_varlen"] = run_varlen(reps=max(3, min(args.steps, 20)), warmup=args.warmup)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
     return line
@@ -598,6 +599,34 @@ def _time_calls(fn, reps: int, warmup: int, stream) -> tuple[float, dict]:
     gdr.stage_timer_enable(False, 0)
     gdr.gdr_sync_status()
     return us, {kname: {"launches": c, "avg_us": round(t / c * 1e3, 2)} for kname, (t, c) in stages.items() if c}
+
+
+def run_varlen(reps: int, warmup: int) -> dict:
+    """Times the variable-length prefill (next row f3): 4 right-padded rows of 4096 positions with
+    4096, 1000, 1 and 2048 valid tokens at the prefill shapes (16 -> 32 heads, bf16, S0), once with
+    their lengths (gdr_chunk_fwd_varlen: chunks past a row's length are skipped) and once as plain
+    rows whose pads carry beta = g = 0 (every chunk run). tokens_per_s counts valid tokens."""
+    import torch
+    from gated_deltanet_rule_gb300 import gdr, inputs
+    lens = [4096, 1000, 1, 2048]
+    B, L, Hk, Hv = len(lens), 4096, 16, 32
+    x = inputs.regime("R1", L, 5, Hk=Hk, Hv=Hv, B=B, init_state=True, dtype=torch.bfloat16)
+    for r, n in enumerate(lens):
+        x.g[r, n:] = 0.0
+        x.beta[r, n:] = 0.0
+    q, k, v, g, beta, S0 = (t.cuda().contiguous() for t in (x.q, x.k, x.v, x.g, x.beta, x.S0))
+    lengths = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    o = torch.empty_like(v)
+    S_T = torch.empty_like(S0)
+    ws = torch.empty(gdr.workspace_bytes(B, L, Hk, Hv), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    out = {"workload": f"{B} rows of {L} positions, lengths {lens}, Hk={Hk} Hv={Hv} D={D}, bf16, S0"}
+    for name, ln in (("with_lengths", lengths), ("all_positions", None)):
+        def call(i, ln=ln):
+            gdr.gdr_chunk_fwd(q, k, v, g, beta, S0, o=o, S_T=S_T, ws=ws, stream=stream, lengths=ln)
+        us, kern = _time_calls(call, reps, warmup, stream)
+        out[name] = {"us_per_call": round(us, 2), "tokens_per_s": round(sum(lens) / (us * 1e-6), 1), "kernels": kern}
+    return out
 
 
 def run_configs(reps: int, warmup: int) -> dict:

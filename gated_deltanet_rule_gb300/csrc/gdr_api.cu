@@ -159,15 +159,20 @@ size_t gdr_chunk_workspace_bytes(int B, int L, int Hk, int Hv, int D, gdr_dtype 
   return chunk_workspace_bytes(B, Hk, L, Hv);
 }
 
-gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
-                         const float* beta, const float* S0, void* o, float* S_T, int B, int L,
-                         int Hk, int Hv, int D, gdr_dtype dt, void* ws, size_t ws_bytes,
-                         gdr_stream_t stream) {
-  const char* who = "gdr_chunk_fwd";
+}  // extern "C"
+
+namespace {
+
+// gdr_chunk_fwd and gdr_chunk_fwd_varlen (lengths NULL = every row has L tokens)
+gdr_status chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                     const float* S0, const int32_t* lengths, void* o, float* S_T, int B, int L, int Hk, int Hv,
+                     int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream, const char* who) {
   gdr_status st = check_common(q, k, v, g, beta, o, B, L, Hk, Hv, D, dt, who);
   if (st != GDR_OK) return st;
   if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T)))
     return fail(GDR_ERR_INVALID_ARG, "%s: S0 and S_T must be 16-byte aligned", who);
+  if (lengths && (reinterpret_cast<uintptr_t>(lengths) & 3u))
+    return fail(GDR_ERR_INVALID_ARG, "%s: lengths must be 4-byte aligned", who);
   const size_t need = gdr_chunk_workspace_bytes(B, L, Hk, Hv, D, dt);
   if (need > 0 && (ws == nullptr || ws_bytes < need))
     return fail(GDR_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", who, need,
@@ -180,13 +185,36 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
     if (B > 65535 || Hk > 65535)
       return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d or Hk=%d exceeds 65535", who, B, Hk);
     ChunkLaunch c{q, k, v, g, beta, S0, o, S_T, ws, B, L, Hk, Hv, err};
+    c.lengths = lengths;
     return launch_status(launch_chunk_bf16(c, s), who);
   }
   RecurrentArgs a{q, k, v, g, beta, S0, nullptr, B, o, S_T, B, L, Hk, Hv, false, err};
+  a.lengths = lengths;
   const int slot = stage_timer_begin(s, kKernRecurrent);
   cudaError_t e = launch_recurrent(a, s);
   stage_timer_end(slot, s);
   return launch_status(e, who);
+}
+
+}  // namespace
+
+extern "C" {
+
+gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* S0, void* o, float* S_T, int B, int L,
+                         int Hk, int Hv, int D, gdr_dtype dt, void* ws, size_t ws_bytes,
+                         gdr_stream_t stream) {
+  return chunk_fwd(q, k, v, g, beta, S0, nullptr, o, S_T, B, L, Hk, Hv, D, dt, ws, ws_bytes, stream,
+                   "gdr_chunk_fwd");
+}
+
+gdr_status gdr_chunk_fwd_varlen(const void* q, const void* k, const void* v, const float* g,
+                                const float* beta, const float* S0, const int32_t* lengths, void* o,
+                                float* S_T, int B, int L, int Hk, int Hv, int D, gdr_dtype dt, void* ws,
+                                size_t ws_bytes, gdr_stream_t stream) {
+  if (!lengths) return fail(GDR_ERR_INVALID_ARG, "gdr_chunk_fwd_varlen: lengths must be non-NULL");
+  return chunk_fwd(q, k, v, g, beta, S0, lengths, o, S_T, B, L, Hk, Hv, D, dt, ws, ws_bytes, stream,
+                   "gdr_chunk_fwd_varlen");
 }
 
 size_t gdr_fork_workspace_bytes(int F, int L_pad, int Hk, int Hv, int D, gdr_dtype dt) {

@@ -82,6 +82,7 @@ struct ChunkArgs {
   uint8_t* ws;       // 1024-aligned
   int B, L, Hk, Hv, NC;
   int* err;
+  const int32_t* lengths;  // valid tokens per row (NULL = L); positions at or past it are pads
 };
 
 __device__ __forceinline__ uint8_t* unit_base(const ChunkArgs& a, int b, int h, int c) {
@@ -353,14 +354,35 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     c = a.NC - 1 - rest % a.NC;
     b = rest / a.NC;
   };
+  // valid tokens of row b (its length when lengths are given)
+  auto row_len = [&](int b) -> int { return a.lengths ? a.lengths[b] : a.L; };
+  // a unit is skipped when its row's length is invalid (outside [0, L]) or, for rows of several
+  // chunks, when the unit lies wholly at or past the length (the state kernel stops there); a
+  // single-chunk row's unit always runs, since it also writes the row's final state
+  auto valid = [&](int u) -> bool {
+    if (!a.lengths) return true;
+    int c, h, b;
+    unit_of(u, c, h, b);
+    const int lb = a.lengths[b];
+    if (lb < 0 || lb > a.L) {
+      if (tid == 0) set_error(a.err, kErrDeviceIndex);
+      return false;
+    }
+    return kFused || c * 64 < lb;
+  };
+  auto next_valid = [&](int u) -> int {
+    while (u < total && !valid(u)) u += (int)gridDim.x;
+    return u;
+  };
   // gates of a unit into gbuf[buf] (threads 0-63, one position each, asynchronous copies);
-  // positions past L read as beta = g = 0. Every thread commits one group per call.
+  // positions past L or past the row's length read as beta = g = 0 (pads). Every thread commits one
+  // group per call.
   auto copy_gates = [&](int u, int buf) {
     if (tid < 64) {
       int c, h, b;
       unit_of(u, c, h, b);
       const int p = c * 64 + tid;
-      if (p < a.L) {
+      if (p < a.L && p < row_len(b)) {
         cp_async4(&gbuf[buf][tid], a.g + ((size_t)b * a.L + p) * a.Hv + h);
         cp_async4(&gbuf[buf][64 + tid], a.beta + ((size_t)b * a.L + p) * a.Hv + h);
       } else {
@@ -391,15 +413,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   };
 
-  int u = blockIdx.x;
-  copy_gates(u, 0);
+  int u = next_valid(blockIdx.x);
+  if (u < total) copy_gates(u, 0);
   if (tid == 0) {
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
   }
   __syncthreads();
-  tiles(u, true);
+  if (u < total) tiles(u, true);
   if (warp == 1) tmem_alloc(&tmem_base, 256);
   tc_fence_before();
   __syncthreads();
@@ -418,11 +440,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     return r;
   };
 
-  for (int it = 0;; ++it) {
+  for (int it = 0; u < total; ++it) {
   int c, h, b;
   unit_of(u, c, h, b);
   uint8_t* ub = unit_base(a, b, h, c);
-  const int un = u + (int)gridDim.x;
+  const int un = next_valid(u + (int)gridDim.x);
   if (un < total) {
     copy_gates(un, (it + 1) & 1);
   } else {
@@ -916,7 +938,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     fence_async_smem();
     __syncthreads();
-    if (write && tid < 64 && c * 64 + tid < a.L) {
+    if (write && tid < 64 && c * 64 + tid < a.L && c * 64 + tid < row_len(b)) {
       bulk_store(a.o + (((size_t)b * a.L + c * 64 + tid) * a.Hv + h) * kD, sm + kPV + tid * 256, 256);
       bulk_commit();
       bulk_wait_read();   // the next unit's tiles overwrite the staging
@@ -934,8 +956,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
-  if (un >= total) break;
   u = un;
+  if (u >= total) break;
   tiles(u, true);
   }   // units
 
@@ -1016,7 +1038,11 @@ chunk_state_kernel(const ChunkArgs a) {
 
   const int sl = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int NC = a.NC;
+  // the row's valid tokens: chunks wholly past them are not run (the state there is final) and
+  // output positions past them are not written; a length outside [0, L] skips the row
+  const int len = a.lengths ? a.lengths[b] : a.L;
+  const bool bad_len = len < 0 || len > a.L;
+  const int NC = bad_len ? 0 : (len + kChunk - 1) / kChunk;
 
   if (tid == 0) {
     for (int s = 0; s < CS; ++s) {
@@ -1051,12 +1077,13 @@ chunk_state_kernel(const ChunkArgs a) {
   // the row's initial state: S0[b], or for forks the trunk state S0[S0_idx[b]]; an index out of
   // range skips the row entirely (nothing of it is written) and records the error
   size_t s0row = b;
-  bool skip = false;
+  bool skip = bad_len;
+  if (skip && tid == 0) set_error(a.err, kErrDeviceIndex);
   if (a.S0_idx) {
     const long long ix = a.S0_idx[b];
-    skip = ix < 0 || ix >= a.n_S0;
-    s0row = skip ? 0 : (size_t)ix;
-    if (skip && tid == 0) set_error(a.err, kErrDeviceIndex);
+    skip = skip || ix < 0 || ix >= a.n_S0;
+    s0row = (ix < 0 || ix >= a.n_S0) ? 0 : (size_t)ix;
+    if ((ix < 0 || ix >= a.n_S0) && tid == 0) set_error(a.err, kErrDeviceIndex);
   }
 
   if (skip) {
@@ -1266,7 +1293,7 @@ chunk_state_kernel(const ChunkArgs a) {
         float qs[kN];
         tmem_ld32(tb + lane_base + 64 + 32 * p, qs);
         const int pos = c * 64 + i;
-        if (pos < a.L) {
+        if (pos < len) {
           float pu[kN];
           const uint8_t* purow = st + kOPU;
           const float upV = out_scl[os].y;   // P U is in its chunk's v scale
@@ -1381,6 +1408,7 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   a.Hv = p.Hv;
   a.NC = (p.L + kChunk - 1) / kChunk;
   a.err = p.err;
+  a.lengths = p.lengths;
 
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)

@@ -40,6 +40,8 @@ struct RecurrentArgs {
   int B, L, Hk, Hv;
   bool bf16;
   int* err;            // device error word
+  const int32_t* lengths = nullptr;   // valid tokens per row (NULL = L): later tokens are not run,
+                                      // their o is not written; a length outside [0, L] skips the row
 };
 cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t s);
 
@@ -61,6 +63,7 @@ struct ChunkLaunch {
   int* err;
   const int64_t* S0_idx = nullptr;
   int n_S0 = 0;
+  const int32_t* lengths = nullptr;   // valid tokens per row (NULL = L), as for RecurrentArgs
 };
 size_t chunk_workspace_bytes(int B, int Hk, int L, int Hv);
 cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s);

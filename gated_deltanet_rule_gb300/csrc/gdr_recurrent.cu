@@ -37,7 +37,15 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(RecurrentArgs a) {
   const int rg = tid >> 3;
   const int warp = tid >> 5, lane = tid & 31;
   const int hk = h / (a.Hv / a.Hk);
-  const int L = a.L;
+  // tokens of this row: L, or the row's length (later tokens are not run, their o is not written)
+  int L = a.L;
+  if (a.lengths) {
+    L = a.lengths[b];
+    if (L < 0 || L > a.L) {
+      if (tid == 0) atomicCAS(a.err, 0, kErrDeviceIndex);
+      return;   // this row's outputs stay untouched
+    }
+  }
 
   __shared__ float qs[2][kD], ks[2][kD], vs[2][kCols];
   __shared__ float nred[2][4][3];        // per-warp partials of q.q, k.k, q.k
@@ -68,7 +76,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(RecurrentArgs a) {
   const T* k = static_cast<const T*>(a.k);
   const T* v = static_cast<const T*>(a.v);
   T* o = static_cast<T*>(a.o);
-  const size_t row_tok = (size_t)b * L;
+  const size_t row_tok = (size_t)b * a.L;
 
   float qn = 0.f, kn = 0.f, vn = 0.f, gn = 0.f, bn = 0.f;
   auto fetch = [&](int t) {

@@ -20,7 +20,8 @@ GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_CUDA, GDR_ERR_DEVICE_I
 GDR_F32, GDR_BF16 = 0, 1
 D = 128
 
-EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_noalloc", "gdr_fork_workspace_bytes",
+EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_varlen", "gdr_chunk_fwd_noalloc",
+           "gdr_fork_workspace_bytes",
            "gdr_fork_fwd", "gdr_decode_step", "gdr_prologue", "gdr_gated_rmsnorm",
            "gdr_backward_workspace_bytes", "gdr_backward",
            "gdr_sync_status", "gdr_status_string", "gdr_last_error_message",
@@ -50,6 +51,8 @@ def lib() -> ctypes.CDLL:
     L.gdr_chunk_workspace_bytes.restype = sz
     L.gdr_chunk_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, vp, sz, vp]
     L.gdr_chunk_fwd.restype = i
+    L.gdr_chunk_fwd_varlen.argtypes = [vp, vp, vp, fp, fp, fp, vp, vp, fp, i, i, i, i, i, i, vp, sz, vp]
+    L.gdr_chunk_fwd_varlen.restype = i
     L.gdr_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, vp]
     L.gdr_chunk_fwd_noalloc.restype = i
     L.gdr_fork_workspace_bytes.argtypes = [i, i, i, i, i, i]
@@ -136,8 +139,11 @@ def workspace_bytes(B: int, L: int, Hk: int, Hv: int, D: int = D, dtype=torch.bf
 
 
 def gdr_chunk_fwd(q, k, v, g, beta, S0=None, o=None, S_T=None, ws=None, stream=None,
-                  final_state: bool = True):
-    """Prefill of B rows: returns (o [B,L,Hv,D] in v's dtype, S_T [B,Hv,D,D] float32 or None)."""
+                  final_state: bool = True, lengths=None):
+    """Prefill of B rows: returns (o [B,L,Hv,D] in v's dtype, S_T [B,Hv,D,D] float32 or None).
+
+    lengths: optional CUDA int32 [B], each row's valid tokens (gdr_chunk_fwd_varlen): positions past
+    a row's length are pads, not run, and their o is left as it was (pass o to control it)."""
     B, L, Hk, Hv, Dk = _check_inputs(q, k, v, g, beta)
     dt = _dtype_code(q)
     if o is None:
@@ -151,8 +157,14 @@ def gdr_chunk_fwd(q, k, v, g, beta, S0=None, o=None, S_T=None, ws=None, stream=N
     if need and ws is None:
         ws = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
-    _check(lib().gdr_chunk_fwd(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o), _p(S_T),
-                               B, L, Hk, Hv, Dk, dt, _p(ws), ws_bytes, _stream(stream)))
+    if lengths is None:
+        _check(lib().gdr_chunk_fwd(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o), _p(S_T),
+                                   B, L, Hk, Hv, Dk, dt, _p(ws), ws_bytes, _stream(stream)))
+    else:
+        _need(lengths.is_cuda and lengths.dtype == torch.int32 and lengths.shape == (B,) and lengths.is_contiguous(),
+              "lengths must be a contiguous CUDA int32 tensor of shape [B]")
+        _check(lib().gdr_chunk_fwd_varlen(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(lengths), _p(o),
+                                          _p(S_T), B, L, Hk, Hv, Dk, dt, _p(ws), ws_bytes, _stream(stream)))
     return o, S_T
 
 

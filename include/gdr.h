@@ -76,6 +76,22 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
                          int Hk, int Hv, int D, gdr_dtype dt, void* ws, size_t ws_bytes,
                          gdr_stream_t stream);
 
+/*
+ * Prefill of B right-padded rows of different lengths (DEG "model.py": Backbone.forward over a batch
+ * whose State.lengths give each row's real tokens; _dn_gates makes the padding exact no-ops).
+ * Same arguments, layouts, workspace and results as gdr_chunk_fwd, plus
+ *   lengths [B] int32 (device)   valid tokens of each row, in [0, L]
+ * Row b runs only its first lengths[b] tokens: positions at or past lengths[b] are pads whatever
+ * their g and beta hold, the 64-token chunks wholly past it are skipped (no work), o is not written
+ * there (it keeps what the caller left), and S_T[b] is the state after the row's last valid token
+ * (S0[b] when the length is 0). A length outside [0, L] leaves that row's o and S_T untouched and
+ * records GDR_ERR_DEVICE_INDEX in the device error word.
+ */
+gdr_status gdr_chunk_fwd_varlen(const void* q, const void* k, const void* v, const float* g,
+                                const float* beta, const float* S0, const int32_t* lengths, void* o,
+                                float* S_T, int B, int L, int Hk, int Hv, int D, gdr_dtype dt, void* ws,
+                                size_t ws_bytes, gdr_stream_t stream);
+
 /* Bytes of caller workspace gdr_fork_fwd needs for these sizes (0 for float32, and 0 for
  * single-chunk forks, L_pad <= 64, which the tensor-core path finishes in one kernel). */
 size_t gdr_fork_workspace_bytes(int F, int L_pad, int Hk, int Hv, int D, gdr_dtype dt);
