@@ -166,7 +166,8 @@ namespace {
 // gdr_chunk_fwd and gdr_chunk_fwd_varlen (lengths NULL = every row has L tokens)
 gdr_status chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                      const float* S0, const int32_t* lengths, void* o, float* S_T, int B, int L, int Hk, int Hv,
-                     int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream, const char* who) {
+                     int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream, const char* who,
+                     const void* z = nullptr, const float* w = nullptr, float eps = 0.f) {
   gdr_status st = check_common(q, k, v, g, beta, o, B, L, Hk, Hv, D, dt, who);
   if (st != GDR_OK) return st;
   if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T)))
@@ -186,6 +187,9 @@ gdr_status chunk_fwd(const void* q, const void* k, const void* v, const float* g
       return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d or Hk=%d exceeds 65535", who, B, Hk);
     ChunkLaunch c{q, k, v, g, beta, S0, o, S_T, ws, B, L, Hk, Hv, err};
     c.lengths = lengths;
+    c.z = z;
+    c.w = w;
+    c.eps = eps;
     return launch_status(launch_chunk_bf16(c, s), who);
   }
   RecurrentArgs a{q, k, v, g, beta, S0, nullptr, B, o, S_T, B, L, Hk, Hv, false, err};
@@ -206,6 +210,24 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
                          gdr_stream_t stream) {
   return chunk_fwd(q, k, v, g, beta, S0, nullptr, o, S_T, B, L, Hk, Hv, D, dt, ws, ws_bytes, stream,
                    "gdr_chunk_fwd");
+}
+
+gdr_status gdr_chunk_fwd_gated(const void* q, const void* k, const void* v, const float* g,
+                               const float* beta, const float* S0, const void* z, const float* w, float eps,
+                               void* out, float* S_T, int B, int L, int Hk, int Hv, int D, gdr_dtype dt, void* ws,
+                               size_t ws_bytes, gdr_stream_t stream) {
+  const char* who = "gdr_chunk_fwd_gated";
+  if (!z || !w) return fail(GDR_ERR_INVALID_ARG, "%s: z and w must be non-NULL", who);
+  if (dt != GDR_BF16) return fail(GDR_ERR_UNSUPPORTED, "%s: the gated epilogue takes bfloat16 q, k, v, z (dt=%d)", who, (int)dt);
+  if (!(eps >= 0.f)) return fail(GDR_ERR_INVALID_ARG, "%s: eps must be >= 0", who);
+  if (!aligned16(z) || !aligned16(w)) return fail(GDR_ERR_INVALID_ARG, "%s: z and w must be 16-byte aligned", who);
+  if (out) {
+    // out is written while z is read: they must not overlap
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(out), z0 = reinterpret_cast<uintptr_t>(z);
+    const uintptr_t n = (uintptr_t)B * L * Hv * kD * 2;
+    if (o0 < z0 + n && z0 < o0 + n) return fail(GDR_ERR_INVALID_ARG, "%s: out overlaps z", who);
+  }
+  return chunk_fwd(q, k, v, g, beta, S0, nullptr, out, S_T, B, L, Hk, Hv, D, dt, ws, ws_bytes, stream, who, z, w, eps);
 }
 
 gdr_status gdr_chunk_fwd_varlen(const void* q, const void* k, const void* v, const float* g,

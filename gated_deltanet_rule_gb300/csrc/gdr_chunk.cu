@@ -43,6 +43,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include "gdr_epilogue.h"
 #include "gdr_internal.h"
 #include "ptx.cuh"
 
@@ -83,6 +84,11 @@ struct ChunkArgs {
   int B, L, Hk, Hv, NC;
   int* err;
   const int32_t* lengths;  // valid tokens per row (NULL = L); positions at or past it are pads
+  // gated RMSNorm epilogue (state kernel, clusters of the four column CTAs of a head): o is replaced
+  // by w * o / sqrt(mean(o^2) + eps) * silu(z) over the 128 values of each position and value head
+  const __nv_bfloat16* z;
+  const float* w;
+  float eps;
 };
 
 __device__ __forceinline__ uint8_t* unit_base(const ChunkArgs& a, int b, int h, int c) {
@@ -1019,7 +1025,7 @@ constexpr int kSb = 5;                 // fp16 state operands: the output path m
 constexpr uint32_t state_smem(int cs, int os) { return cs * kCStage + os * kOStage + kSb * 8192 + 1024; }
 static_assert(kCN == kMBytes && kOPU == kQBytes, "stage layout");
 
-template <int CS, int OS>
+template <int CS, int OS, bool kGated>
 __global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const ChunkArgs a) {
   constexpr uint32_t kOffO = CS * kCStage;
@@ -1033,6 +1039,12 @@ chunk_state_kernel(const ChunkArgs a) {
   __shared__ uint64_t scRdy[8];                    // the state scale of chunk c is in sc_ring[c % 8]
   __shared__ float sc_ring[8];
   __shared__ uint32_t smax[2][4];                  // per state warp: largest |S| of its rows of the slice
+  // gated epilogue: red[p][r][i] = the sum of o^2 over CTA r's 32 values at position i of a chunk of
+  // parity p (written by CTA r into every CTA of the cluster); fullR[p]: all 4 x 64 partials of the
+  // chunk are here; freeR[p]: every CTA of the cluster has read its red[p] (so it may be rewritten)
+  __shared__ float red[2][4][64];
+  __shared__ uint64_t fullR[2], freeR[2];
+  __shared__ float w_s[kN];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -1064,13 +1076,21 @@ chunk_state_kernel(const ChunkArgs a) {
       mbar_init(&sFree[q], 1);
     }
     for (int r = 0; r < 8; ++r) mbar_init(&scRdy[r], 4);
+    if (kGated) {
+      for (int q = 0; q < 2; ++q) {
+        mbar_init(&fullR[q], 4 * kOutCount);
+        mbar_init(&freeR[q], 4 * kOutCount);
+      }
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
+  if (kGated && tid < kN) w_s[tid] = a.w[sl * kN + tid];
   if (warp == 0) tmem_alloc(&tmem_base, kTmemState);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (kGated) cluster_sync_all();   // every CTA's barriers are initialised before any remote arrive
   const uint32_t tb = tmem_base;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   bool ok = true;
@@ -1293,7 +1313,58 @@ chunk_state_kernel(const ChunkArgs a) {
         float qs[kN];
         tmem_ld32(tb + lane_base + 64 + 32 * p, qs);
         const int pos = c * 64 + i;
-        if (pos < len) {
+        if (kGated) {
+          // o (float32) for this CTA's 32 values, its sum of squares to every CTA of the cluster,
+          // then w * o / rms(o) * silu(z) once all four partials of the position are in
+          float pu[kN];
+          const uint8_t* purow = st + kOPU;
+          const float upV = out_scl[os].y, sc = sc_ring[c & 7];
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+            unpack8_f16(*reinterpret_cast<const uint4*>(purow + swz64(i * 64 + ch * 16)), pu + 8 * ch);
+          float ss = 0.f;
+#pragma unroll
+          for (int n = 0; n < kN; ++n) {
+            qs[n] = fmaf(sc, qs[n], upV * pu[n]);
+            ss = fmaf(qs[n], qs[n], ss);
+          }
+          // red[p] of every CTA may be rewritten once every CTA has read it for chunk c - 2
+          ok = c < 2 || mbar_wait_cluster(&freeR[p], ((c >> 1) - 1) & 1, a.wait_budget);
+          if (ok) {
+#pragma unroll
+            for (uint32_t r = 0; r < 4; ++r) st_cluster_f32(dsmem_addr(&red[p][sl][i], r), ss);
+#pragma unroll
+            for (uint32_t r = 0; r < 4; ++r) remote_arrive(&fullR[p], r);
+            ok = mbar_wait_cluster(&fullR[p], (c >> 1) & 1, a.wait_budget);
+          }
+          if (ok) {
+            const float tot = red[p][0][i] + red[p][1][i] + red[p][2][i] + red[p][3][i];
+#pragma unroll
+            for (uint32_t r = 0; r < 4; ++r) remote_arrive(&freeR[p], r);
+            const float rs = rsqrtf(tot * (1.f / kD) + a.eps);
+            if (pos < len) {
+              const size_t off = (((size_t)b * a.L + pos) * a.Hv + h) * kD + sl * kN;
+              __nv_bfloat16* orow_p = a.o + off;
+              const uint4* zrow = reinterpret_cast<const uint4*>(a.z + off);
+#pragma unroll
+              for (int ch = 0; ch < 4; ++ch) {
+                const uint4 zv = __ldg(zrow + ch);
+                const uint32_t zu[4] = {zv.x, zv.y, zv.z, zv.w};
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+#pragma unroll
+                  for (int u = 0; u < 2; ++u) {
+                    const float zz = __uint_as_float(u ? (zu[e] & 0xFFFF0000u) : (zu[e] << 16));
+                    const int n = 8 * ch + 2 * e + u;
+                    y[2 * e + u] = w_s[n] * (qs[n] * rs) * __fdividef(zz, 1.f + __expf(-zz));
+                  }
+                }
+                *reinterpret_cast<uint4*>(orow_p + 8 * ch) = pack8_bf16(y);
+              }
+            }
+          }
+        } else if (pos < len) {
           float pu[kN];
           const uint8_t* purow = st + kOPU;
           const float upV = out_scl[os].y;   // P U is in its chunk's v scale
@@ -1330,6 +1401,9 @@ chunk_state_kernel(const ChunkArgs a) {
     tc_fence_after();
     tmem_dealloc(tb, kTmemState);
   }
+  // no CTA of the cluster leaves while another may still write its shared memory (every thread of
+  // every CTA reaches this point: all loops above are bounded)
+  if (kGated) cluster_sync_all();
 }
 
 // -------------------------------------------------------------------------------------------
@@ -1409,12 +1483,16 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   a.NC = (p.L + kChunk - 1) / kChunk;
   a.err = p.err;
   a.lengths = p.lengths;
+  a.z = static_cast<const __nv_bfloat16*>(p.z);
+  a.w = p.w;
+  a.eps = p.eps;
 
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(chunk_state_kernel<3, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(3, 3));
+    e = cudaFuncSetAttribute(p.z ? chunk_state_kernel<3, 3, true> : chunk_state_kernel<3, 3, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(3, 3));
   if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkPrep);
   const long long units = (long long)a.B * a.Hv * a.NC;
@@ -1426,7 +1504,12 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   stage_timer_end(slot, s);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (a.fused) return cudaSuccess;   // single-chunk rows are complete after kernel 1
+  if (a.fused) {
+    // single-chunk rows are complete after kernel 1; the gated epilogue then runs over o in place
+    if (!p.z) return cudaSuccess;
+    EpilogueArgs ea{p.o, p.z, p.w, p.eps, p.o, (long long)p.B * p.L * p.Hv};
+    return launch_gated_rmsnorm(ea, s);
+  }
   slot = stage_timer_begin(s, kKernChunkState);
   // launched as a programmatic dependent of the prep kernel: its set-up (barriers, tensor memory,
   // the initial state) overlaps the prep kernel's tail; its loads of the workspace wait for it
@@ -1435,12 +1518,18 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   cfg.blockDim = dim3(kStateThreads, 1, 1);
   cfg.dynamicSmemBytes = state_smem(3, 3);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // the gated epilogue reduces over a head's 128 values: its four column CTAs form a cluster
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kSlices;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3>, a);
+  cfg.numAttrs = p.z ? 2 : 1;
+  e = p.z ? cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, true>, a)
+          : cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false>, a);
   stage_timer_end(slot, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -64,6 +64,10 @@ struct ChunkLaunch {
   const int64_t* S0_idx = nullptr;
   int n_S0 = 0;
   const int32_t* lengths = nullptr;   // valid tokens per row (NULL = L), as for RecurrentArgs
+  // gated RMSNorm epilogue (NULL z = none): o is written as w * o / sqrt(mean(o^2) + eps) * silu(z)
+  const void* z = nullptr;            // [B, L, Hv, 128] bf16
+  const float* w = nullptr;           // [128]
+  float eps = 0.f;
 };
 size_t chunk_workspace_bytes(int B, int Hk, int L, int Hv);
 cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s);

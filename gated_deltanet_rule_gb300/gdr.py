@@ -20,7 +20,8 @@ GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_CUDA, GDR_ERR_DEVICE_I
 GDR_F32, GDR_BF16 = 0, 1
 D = 128
 
-EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_varlen", "gdr_chunk_fwd_noalloc",
+EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_varlen", "gdr_chunk_fwd_gated",
+           "gdr_chunk_fwd_noalloc",
            "gdr_fork_workspace_bytes",
            "gdr_fork_fwd", "gdr_decode_step", "gdr_prologue", "gdr_gated_rmsnorm",
            "gdr_backward_workspace_bytes", "gdr_backward",
@@ -53,6 +54,8 @@ def lib() -> ctypes.CDLL:
     L.gdr_chunk_fwd.restype = i
     L.gdr_chunk_fwd_varlen.argtypes = [vp, vp, vp, fp, fp, fp, vp, vp, fp, i, i, i, i, i, i, vp, sz, vp]
     L.gdr_chunk_fwd_varlen.restype = i
+    L.gdr_chunk_fwd_gated.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, ctypes.c_float, vp, fp, i, i, i, i, i, i, vp, sz, vp]
+    L.gdr_chunk_fwd_gated.restype = i
     L.gdr_chunk_fwd_noalloc.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, vp]
     L.gdr_chunk_fwd_noalloc.restype = i
     L.gdr_fork_workspace_bytes.argtypes = [i, i, i, i, i, i]
@@ -166,6 +169,27 @@ def gdr_chunk_fwd(q, k, v, g, beta, S0=None, o=None, S_T=None, ws=None, stream=N
         _check(lib().gdr_chunk_fwd_varlen(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(lengths), _p(o),
                                           _p(S_T), B, L, Hk, Hv, Dk, dt, _p(ws), ws_bytes, _stream(stream)))
     return o, S_T
+
+
+def gdr_chunk_fwd_gated(q, k, v, g, beta, S0, z, w, eps: float, out=None, S_T=None, ws=None, stream=None,
+                        final_state: bool = True):
+    """Prefill with the gated RMSNorm fused into its output: returns (out [B,L,Hv,D] bf16 =
+    w * o / rms(o) * silu(z), S_T [B,Hv,D,D] float32 or None)."""
+    B, L, Hk, Hv, Dk = _check_inputs(q, k, v, g, beta)
+    dt = _dtype_code(q)
+    _need(z.is_cuda and z.dtype == torch.bfloat16 and z.shape == v.shape and z.is_contiguous(), "z: contiguous CUDA bf16 like v")
+    _need(w.is_cuda and w.dtype == torch.float32 and w.shape == (Dk,) and w.is_contiguous(), "w: contiguous CUDA float32 [D]")
+    if out is None:
+        out = torch.empty_like(v)
+    if S_T is None and final_state:
+        S_T = torch.empty(B, Hv, Dk, v.shape[3], device=v.device, dtype=torch.float32)
+    need = workspace_bytes(B, L, Hk, Hv, Dk, q.dtype)
+    if need and ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().gdr_chunk_fwd_gated(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(z), _p(w), float(eps), _p(out),
+                                     _p(S_T), B, L, Hk, Hv, Dk, dt, _p(ws), ws_bytes, _stream(stream)))
+    return out, S_T
 
 
 def fork_workspace_bytes(F: int, L_pad: int, Hk: int, Hv: int, D: int = D, dtype=torch.bfloat16) -> int:

@@ -92,6 +92,25 @@ gdr_status gdr_chunk_fwd_varlen(const void* q, const void* k, const void* v, con
                                 float* S_T, int B, int L, int Hk, int Hv, int D, gdr_dtype dt, void* ws,
                                 size_t ws_bytes, gdr_stream_t stream);
 
+/*
+ * Prefill followed by the layer's gated RMSNorm, fused into the output of the recurrence (DEG
+ * "model.py": _linear_layer applies _gated_rms with the in_proj_z gate to _delta_rule's output). Same
+ * arguments, workspace and final state as gdr_chunk_fwd, but instead of o it writes
+ *   out[b, t, h, :] = w * o / sqrt(mean(o^2) + eps) * silu(z[b, t, h, :]),  silu(x) = x / (1 + exp(-x))
+ * over the 128 values of each position and value head, from the float32 o (o itself is not stored):
+ *   z    [B, L, Hv, D] bfloat16   the gate; 16-byte aligned
+ *   w    [D] float32              the norm weight; 16-byte aligned
+ *   eps  >= 0
+ *   out  [B, L, Hv, D] bfloat16   must not overlap z
+ * bfloat16 only (GDR_ERR_UNSUPPORTED for float32). Rows of several chunks reduce over the four
+ * column blocks of a head in the state kernel (a cluster of four CTAs); rows of one chunk (L <= 64)
+ * run gdr_gated_rmsnorm over the bf16 o in place.
+ */
+gdr_status gdr_chunk_fwd_gated(const void* q, const void* k, const void* v, const float* g,
+                               const float* beta, const float* S0, const void* z, const float* w, float eps,
+                               void* out, float* S_T, int B, int L, int Hk, int Hv, int D, gdr_dtype dt, void* ws,
+                               size_t ws_bytes, gdr_stream_t stream);
+
 /* Bytes of caller workspace gdr_fork_fwd needs for these sizes (0 for float32, and 0 for
  * single-chunk forks, L_pad <= 64, which the tensor-core path finishes in one kernel). */
 size_t gdr_fork_workspace_bytes(int F, int L_pad, int Hk, int Hv, int D, gdr_dtype dt);

@@ -217,3 +217,24 @@ def test_backward_rejects_overlapping_outputs(L):
     for over in cases:
         assert call(**over) == gdr.GDR_ERR_INVALID_ARG, over
         assert b"overlaps" in L.gdr_last_error_message(), over
+
+
+def test_varlen_and_gated_reject_bad_arguments(L):
+    """The variable-length and gated prefill calls check their extra arguments on the host."""
+    B, Lt, Hk, Hv = 1, 64, 2, 4
+    # gdr_chunk_fwd_varlen(q, k, v, g, beta, S0, lengths, o, S_T, B, L, Hk, Hv, D, dt, ws, ws_bytes, stream)
+    f = L.gdr_chunk_fwd_varlen
+    assert f(P, P, P, P, P, None, None, P, None, B, Lt, Hk, Hv, 128, 1, None, 0, None) == gdr.GDR_ERR_INVALID_ARG
+    assert b"lengths" in L.gdr_last_error_message()
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    assert f(P, P, P, P, P, None, odd, P, None, B, Lt, Hk, Hv, 128, 1, None, 0, None) == gdr.GDR_ERR_INVALID_ARG
+    assert b"aligned" in L.gdr_last_error_message()
+    # gdr_chunk_fwd_gated(q, k, v, g, beta, S0, z, w, eps, out, S_T, B, L, Hk, Hv, D, dt, ws, ws_bytes, stream)
+    f = L.gdr_chunk_fwd_gated
+    Z = ctypes.c_void_p(1 << 32)
+    assert f(P, P, P, P, P, None, None, P, 1e-6, P, None, B, Lt, Hk, Hv, 128, 1, None, 0, None) == gdr.GDR_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, None, Z, P, 1e-6, P, None, B, Lt, Hk, Hv, 128, 0, None, 0, None) == gdr.GDR_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, None, Z, P, -1.0, P, None, B, Lt, Hk, Hv, 128, 1, None, 0, None) == gdr.GDR_ERR_INVALID_ARG
+    assert f(P, P, P, P, P, None, Z, P, 1e-6, ctypes.c_void_p((1 << 32) + 4096), None, B, Lt, Hk, Hv, 128, 1, None, 0,
+             None) == gdr.GDR_ERR_INVALID_ARG
+    assert b"overlaps" in L.gdr_last_error_message()

@@ -1,7 +1,7 @@
 """GPU parity of the gated RMSNorm epilogue (gdr_gated_rmsnorm through the C ABI) against the
 float64 oracle: element by element within 2^-8 |ref| + 1e-6 (one rounding to bf16 of an fp32
-result); in place equals out of place bit for bit; the composition gdr_chunk_fwd -> epilogue
-matches the oracle recurrence -> oracle epilogue at the path's bf16 tolerance."""
+result); in place equals out of place bit for bit; the composition gdr_chunk_fwd -> epilogue, and the
+fused gdr_chunk_fwd_gated, match the oracle recurrence -> oracle epilogue at the path's bf16 tolerance."""
 import numpy as np
 import pytest
 import torch
@@ -61,3 +61,30 @@ def test_chunked_path_then_epilogue_matches_oracle_composition():
     gdr.gdr_sync_status()
     ro, _ = oracle.forward(x.q, x.k, x.v, x.g, x.beta, x.S0)
     assert_close(out, oe.gated_rms(ro, z, w, 1e-6), TOL_BF16, "normalised output")
+
+
+@pytest.mark.parametrize("L,B", [(200, 1), (300, 2), (50, 2)])
+def test_fused_gated_prefill_matches_oracle_composition(L, B):
+    """gdr_chunk_fwd_gated: the gated RMSNorm fused into the recurrence's output (rows of several
+    chunks: the four column CTAs of a head reduce the sum of squares in a cluster; rows of one chunk:
+    the epilogue over o in place) matches oracle recurrence -> oracle epilogue, and its final state
+    equals gdr_chunk_fwd's bit for bit."""
+    x = inputs.regime("R1", L, 73 + L, Hk=2, Hv=4, B=B, init_state=True, dtype=torch.bfloat16)
+    _, z, w = _xzw(tuple(x.v.shape), 74 + L)
+    args = [t.cuda() for t in (x.q, x.k, x.v, x.g, x.beta, x.S0)]
+    out, S = gdr.gdr_chunk_fwd_gated(*args, z.cuda(), w.cuda(), 1e-6)
+    _, S_plain = gdr.gdr_chunk_fwd(*args)
+    gdr.gdr_sync_status()
+    ro, rS = oracle.forward(x.q, x.k, x.v, x.g, x.beta, x.S0)
+    assert_close(out, oe.gated_rms(ro, z, w, 1e-6), TOL_BF16, "fused normalised output")
+    assert torch.equal(S, S_plain)
+
+
+def test_fused_gated_prefill_full_size_4096():
+    x = inputs.config3()
+    _, z, w = _xzw(tuple(x.v.shape), 75)
+    args = [t.cuda() for t in (x.q, x.k, x.v, x.g, x.beta, x.S0)]
+    out, _ = gdr.gdr_chunk_fwd_gated(*args, z.cuda(), w.cuda(), 1e-6)
+    gdr.gdr_sync_status()
+    ro, _ = oracle.forward(x.q, x.k, x.v, x.g, x.beta, x.S0)
+    assert_close(out, oe.gated_rms(ro, z, w, 1e-6), TOL_BF16, "fused normalised output (L = 4096)")
