@@ -355,6 +355,8 @@ def run_gb300(args) -> dict | None:
         line["rows"] = run_fork_decode(reps=max(3, min(args.steps, 20)), warmup=args.warmup)
         line["rows"]["next_f1_prologue"] = run_prologue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
         line["rows"]["next_f2_gated_rmsnorm"] = run_epilogue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
+        line["rows"]["next_f2_gated_rmsnorm"]["fused_into_prefill"] = run_gated_prefill(
+            reps=max(3, min(args.steps, 20)), warmup=args.warmup)
         line["rows"]["next_f4_backward"] = run_backward(reps=max(3, min(args.steps, 10)), warmup=args.warmup)
         line["rows"]["configs"] = run_configs(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
         line["rows"]["next_f3_varlen"] = run_varlen(reps=max(3, min(args.steps, 20)), warmup=args.warmup)
@@ -599,6 +601,38 @@ def _time_calls(fn, reps: int, warmup: int, stream) -> tuple[float, dict]:
     gdr.stage_timer_enable(False, 0)
     gdr.gdr_sync_status()
     return us, {kname: {"launches": c, "avg_us": round(t / c * 1e3, 2)} for kname, (t, c) in stages.items() if c}
+
+
+def run_gated_prefill(reps: int, warmup: int) -> dict:
+    """Times the gated RMSNorm fused into the prefill's output (gdr_chunk_fwd_gated) on the prefill
+    row (L = 4096, 16 -> 32 heads, bf16, S0) against the same prefill followed by the separate
+    gdr_gated_rmsnorm pass over its o."""
+    import torch
+    from gated_deltanet_rule_gb300 import gdr, inputs
+    x = inputs.config3()
+    q, k, v, g, beta, S0 = (t.cuda().contiguous() for t in (x.q, x.k, x.v, x.g, x.beta, x.S0))
+    gen = torch.Generator().manual_seed(9)
+    z = torch.randn(v.shape, generator=gen).bfloat16().cuda()
+    w = (0.5 + torch.rand(D, generator=gen)).cuda()
+    L, Hk, Hv = q.shape[1], q.shape[2], v.shape[2]
+    o = torch.empty_like(v)
+    out = torch.empty_like(v)
+    S_T = torch.empty_like(S0)
+    ws = torch.empty(gdr.workspace_bytes(1, L, Hk, Hv), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def fused(i):
+        gdr.gdr_chunk_fwd_gated(q, k, v, g, beta, S0, z, w, 1e-6, out=out, S_T=S_T, ws=ws, stream=stream)
+
+    def separate(i):
+        gdr.gdr_chunk_fwd(q, k, v, g, beta, S0, o=o, S_T=S_T, ws=ws, stream=stream)
+        gdr.gdr_gated_rmsnorm(o, z, w, 1e-6, out=out, stream=stream)
+
+    res = {"workload": f"prefill L={L} Hk={Hk} Hv={Hv} D={D} bf16 with S0, then the gated RMSNorm of its output"}
+    for name, fn in (("fused", fused), ("separate_pass", separate)):
+        us, kern = _time_calls(fn, reps, warmup, stream)
+        res[name] = {"us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1), "kernels": kern}
+    return res
 
 
 def run_varlen(reps: int, warmup: int) -> dict:
