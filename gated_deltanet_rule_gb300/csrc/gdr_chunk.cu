@@ -125,8 +125,6 @@ __device__ __forceinline__ void pow2_scales(float m, float& up, float& dn) {
   up = __uint_as_float((uint32_t)(127 + e) << 23);
   dn = __uint_as_float((uint32_t)(127 - e) << 23);
 }
-// 1 / x for a power of two x (exact)
-__device__ __forceinline__ float pow2_inverse(float x) { return __uint_as_float((254u << 23) - __float_as_uint(x)); }
 // bf16x2 word -> fp16x2 word of the values times s (a power of two)
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float s) {
   return pack_f16x2(__uint_as_float(w << 16) * s, __uint_as_float(w & 0xFFFF0000u) * s);
@@ -993,13 +991,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // Warp roles (warp w reads TMEM lanes 32 (w % 4) .. + 31):
 //   warps 0-3: own the state rows (key row = tid, 32 value columns, float32 registers), form
 //              S = Gamma_C S + D + N and write its fp16 copy, the operand of the next products.
-//   warps 4, 5: output rows o = O' + P U for positions 0-63 (TMEM lanes 0-63); named barrier 2.
+//   warps 4, 5 and 8, 9: output rows o = O' + P U for positions 0-63 (TMEM lanes 0-63), columns
+//              0-15 (warps 4, 5) and 16-31 (warps 8, 9) of the slice; named barrier 2. Four
+//              warps, so that the gated epilogue's per-position work is spread over two warps on
+//              each of the two SMSPs that may read those TMEM lanes.
 //   warp 6: loads the chain ring (M', this CTA's N slice, Gamma_C) up to CS chunks ahead, and
 //           prefetches the chunk kPrefetchAhead beyond each load into L2.
 //   warp 7: issues the output product O' = Q' S, so that its issue time stays off the chain.
-//   warp 8: loads the output ring (Q', this CTA's P U slice) up to OS chunks ahead (with the
+//   warp 10: loads the output ring (Q', this CTA's P U slice) up to OS chunks ahead (with the
 //           same L2 prefetch).
-//   warp 9: issues the state product D = M' S (in a warp of its own, so that its issue is not
+//   warp 11: issues the state product D = M' S (in a warp of its own, so that its issue is not
 //           serialised with the state update of a diverged state warp).
 // Per chunk c: chain stage c % CS (chFull / chFree: each state warp releases it after its
 // update), output stage c % OS (outFull / outFree: released by the output warps), state operand
@@ -1008,8 +1009,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // p = c % 2 (D[p] with bar_d; O'[p] with bar_o: product done, oFree: the output warps have read
 // it). Every barrier completes once per CS, OS, kSb, 2 chunks or per chunk, and none can run two
 // phases ahead of its waiters.
-constexpr int kStateThreads = 320;
-constexpr uint32_t kOutBar = 2, kOutCount = 64;
+constexpr int kStateThreads = 384;
+constexpr uint32_t kOutBar = 2, kOutCount = 128;
+constexpr int kOutCols = kN / 2;       // value columns per output warp
 constexpr uint32_t kStateBar = 3;      // named barrier of the four state warps (the state scale)
 constexpr uint32_t kCStage = 40960;    // M' (two 16 KB K-atoms), then this CTA's N slice (8 KB)
 constexpr uint32_t kCN = 32768;
@@ -1039,12 +1041,14 @@ chunk_state_kernel(const ChunkArgs a) {
   __shared__ uint64_t scRdy[8];                    // the state scale of chunk c is in sc_ring[c % 8]
   __shared__ float sc_ring[8];
   __shared__ uint32_t smax[2][4];                  // per state warp: largest |S| of its rows of the slice
-  // gated epilogue: red[p][r][i] = the sum of o^2 over CTA r's 32 values at position i of a chunk of
-  // parity p (written by CTA r into every CTA of the cluster); fullR[p]: all 4 x 64 partials of the
-  // chunk are here; freeR[p]: every CTA of the cluster has read its red[p] (so it may be rewritten)
-  __shared__ float red[2][4][64];
+  // gated epilogue: red[p][2 r + hc][i] = the sum of o^2 over the 16 values of column half hc of
+  // CTA r at position i of a chunk of parity p (written by CTA r into every CTA of the cluster as
+  // asynchronous stores that complete transaction bytes on the receiver's fullR[p]); fullR[p]: all
+  // 8 x 64 partials of the chunk are here (one local arrival posts the 2048 bytes); freeR[p]: every
+  // CTA of the cluster has read its red[p], so it may be rewritten (one arrival per CTA)
+  __shared__ float red[kGated ? 2 : 1][2 * kSlices][64];
   __shared__ uint64_t fullR[2], freeR[2];
-  __shared__ float w_s[kN];
+  __shared__ __align__(16) float w_s[kN];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -1078,8 +1082,8 @@ chunk_state_kernel(const ChunkArgs a) {
     for (int r = 0; r < 8; ++r) mbar_init(&scRdy[r], 4);
     if (kGated) {
       for (int q = 0; q < 2; ++q) {
-        mbar_init(&fullR[q], 4 * kOutCount);
-        mbar_init(&freeR[q], 4 * kOutCount);
+        mbar_init(&fullR[q], 1);
+        mbar_init(&freeR[q], kSlices);
       }
     }
     abort_flag = 0;
@@ -1108,8 +1112,8 @@ chunk_state_kernel(const ChunkArgs a) {
 
   if (skip) {
     // every CTA of the row reads the same index and skips
-  } else if (warp == 6 || warp == 8) {
-    // ---------------- producers (lane 0): the chain ring (warp 6) and the output ring (warp 8) ----
+  } else if (warp == 6 || warp == 10) {
+    // ---------------- producers (lane 0): the chain ring (warp 6) and the output ring (warp 10) ---
     if (lane == 0) {
       wait_prerequisite();   // the workspace is complete once the prep kernel has finished
       const bool chain = warp == 6;
@@ -1224,6 +1228,7 @@ chunk_state_kernel(const ChunkArgs a) {
         ok = mbar_wait(&bar_d, c & 1, a.wait_budget) &&
              (c + 1 < kSb || mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget));
       }
+      ok = __all_sync(0xffffffffu, ok);   // the TMEM load below is warp-collective
       if (ok) {
         tc_fence_after();
         float d[kN];
@@ -1251,7 +1256,7 @@ chunk_state_kernel(const ChunkArgs a) {
       for (int n = 0; n < kN; n += 4)
         *reinterpret_cast<float4*>(dst + n) = make_float4(Sm[n], Sm[n + 1], Sm[n + 2], Sm[n + 3]);
     }
-  } else if (warp == 9) {
+  } else if (warp == 11) {
     // ---------------- state-product issuer ----------------
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, kN, false, true);
@@ -1300,86 +1305,92 @@ chunk_state_kernel(const ChunkArgs a) {
       if (!ok && last >= 0) mbar_wait(&bar_o[last & 1], (last >> 1) & 1, kDrainBudget);   // drain
     }
   } else {
-    // ---------------- output warps 4, 5 ----------------
-    const int i = tid - 128;   // position in the chunk = TMEM lane
+    // ---------------- output warps 4, 5, 8, 9 ----------------
+    const int i = 32 * (warp & 1) + lane;   // position in the chunk = TMEM lane
+    const int hc = warp >> 3;               // column half: slice columns 16 hc .. 16 hc + 15
+    const int col0 = sl * kN + kOutCols * hc;
+    // gated: this thread's 16 gate values z of the chunk, loaded one chunk ahead
+    uint4 zc[2] = {};
+    auto load_z = [&](int c) {
+      const int pos = c * 64 + i;
+      if (kGated && c < NC && pos < len) {
+        const uint4* zrow = reinterpret_cast<const uint4*>(a.z + (((size_t)b * a.L + pos) * a.Hv + h) * kD + col0);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) zc[ch] = __ldg(zrow + ch);
+      }
+    };
+    load_z(0);
     for (int c = 0; c < NC && ok; ++c) {
       const int os = c % OS, p = c & 1;
       const uint8_t* st = sm + kOffO + os * kOStage;
       ok = mbar_wait(&outFull[os], (c / OS) & 1, a.wait_budget) &&
            mbar_wait(&bar_o[p], (c >> 1) & 1, a.wait_budget) &&
            mbar_wait(&scRdy[c & 7], (c >> 3) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
+      ok = __all_sync(0xffffffffu, ok);   // the TMEM load below is warp-collective
       if (ok) {
         tc_fence_after();
-        float qs[kN];
-        tmem_ld32(tb + lane_base + 64 + 32 * p, qs);
+        float qs[kOutCols];
+        tmem_ld16(tb + lane_base + 64 + 32 * p + kOutCols * hc, qs);
         const int pos = c * 64 + i;
-        if (kGated) {
-          // o (float32) for this CTA's 32 values, its sum of squares to every CTA of the cluster,
-          // then w * o / rms(o) * silu(z) once all four partials of the position are in
-          float pu[kN];
-          const uint8_t* purow = st + kOPU;
-          const float upV = out_scl[os].y, sc = sc_ring[c & 7];
+        float pu[kOutCols];
+        const uint8_t* purow = st + kOPU;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch)
-            unpack8_f16(*reinterpret_cast<const uint4*>(purow + swz64(i * 64 + ch * 16)), pu + 8 * ch);
+        for (int ch = 0; ch < 2; ++ch)
+          unpack8_f16(*reinterpret_cast<const uint4*>(purow + swz64(i * 64 + (2 * hc + ch) * 16)), pu + 8 * ch);
+        const float upV = out_scl[os].y;   // P U is in its chunk's v scale
+        const float sc = sc_ring[c & 7];     // O' = Q' (S_c / sc_c)
+#pragma unroll
+        for (int n = 0; n < kOutCols; ++n) qs[n] = fmaf(sc, qs[n], upV * pu[n]);
+        if (kGated) {
+          // o (float32) for these 16 values, its sum of squares to every CTA of the cluster, then
+          // w * o / rms(o) * silu(z) once all eight partials of the position are in
           float ss = 0.f;
 #pragma unroll
-          for (int n = 0; n < kN; ++n) {
-            qs[n] = fmaf(sc, qs[n], upV * pu[n]);
-            ss = fmaf(qs[n], qs[n], ss);
-          }
+          for (int n = 0; n < kOutCols; ++n) ss = fmaf(qs[n], qs[n], ss);
           // red[p] of every CTA may be rewritten once every CTA has read it for chunk c - 2
-          ok = c < 2 || mbar_wait_cluster(&freeR[p], ((c >> 1) - 1) & 1, a.wait_budget);
+          ok = c < 2 || mbar_wait(&freeR[p], ((c >> 1) - 1) & 1, a.wait_budget);
           if (ok) {
+            if (tid == 128) mbar_arrive_expect_tx(&fullR[p], 2 * kSlices * 64 * 4);
 #pragma unroll
-            for (uint32_t r = 0; r < 4; ++r) st_cluster_f32(dsmem_addr(&red[p][sl][i], r), ss);
+            for (uint32_t r = 0; r < kSlices; ++r)
+              st_async_f32(dsmem_addr(&red[p][2 * sl + hc][i], r), ss, dsmem_addr(&fullR[p], r));
+            // while the partials travel: w silu(z), which does not depend on o
+            float gz[kOutCols];
 #pragma unroll
-            for (uint32_t r = 0; r < 4; ++r) remote_arrive(&fullR[p], r);
-            ok = mbar_wait_cluster(&fullR[p], (c >> 1) & 1, a.wait_budget);
-          }
-          if (ok) {
-            const float tot = red[p][0][i] + red[p][1][i] + red[p][2][i] + red[p][3][i];
+            for (int ch = 0; ch < 2; ++ch) {
+              const uint32_t zu[4] = {zc[ch].x, zc[ch].y, zc[ch].z, zc[ch].w};
+              const float4 w0 = reinterpret_cast<const float4*>(w_s + kOutCols * hc)[2 * ch];
+              const float4 w1 = reinterpret_cast<const float4*>(w_s + kOutCols * hc)[2 * ch + 1];
+              const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-            for (uint32_t r = 0; r < 4; ++r) remote_arrive(&freeR[p], r);
-            const float rs = rsqrtf(tot * (1.f / kD) + a.eps);
-            if (pos < len) {
-              const size_t off = (((size_t)b * a.L + pos) * a.Hv + h) * kD + sl * kN;
-              __nv_bfloat16* orow_p = a.o + off;
-              const uint4* zrow = reinterpret_cast<const uint4*>(a.z + off);
-#pragma unroll
-              for (int ch = 0; ch < 4; ++ch) {
-                const uint4 zv = __ldg(zrow + ch);
-                const uint32_t zu[4] = {zv.x, zv.y, zv.z, zv.w};
-                float y[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-#pragma unroll
-                  for (int u = 0; u < 2; ++u) {
-                    const float zz = __uint_as_float(u ? (zu[e] & 0xFFFF0000u) : (zu[e] << 16));
-                    const int n = 8 * ch + 2 * e + u;
-                    y[2 * e + u] = w_s[n] * (qs[n] * rs) * __fdividef(zz, 1.f + __expf(-zz));
-                  }
-                }
-                *reinterpret_cast<uint4*>(orow_p + 8 * ch) = pack8_bf16(y);
+              for (int e = 0; e < 8; ++e) {
+                const float zz = __uint_as_float((e & 1) ? (zu[e >> 1] & 0xFFFF0000u) : (zu[e >> 1] << 16));
+                gz[8 * ch + e] = wv[e] * __fdividef(zz, 1.f + __expf(-zz));
               }
+            }
+            ok = mbar_wait(&fullR[p], (c >> 1) & 1, a.wait_budget);
+            if (ok) {
+              float tot = 0.f;
+#pragma unroll
+              for (int r = 0; r < 2 * kSlices; ++r) tot += red[p][r][i];
+              const float rs = rsqrtf(tot * (1.f / kD) + a.eps);
+              if (pos < len) {
+                __nv_bfloat16* orow_p = a.o + (((size_t)b * a.L + pos) * a.Hv + h) * kD + col0;
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                  float y[8];
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) y[e] = (qs[8 * ch + e] * rs) * gz[8 * ch + e];
+                  *reinterpret_cast<uint4*>(orow_p + 8 * ch) = pack8_bf16(y);
+                }
+              }
+              load_z(c + 1);
             }
           }
         } else if (pos < len) {
-          float pu[kN];
-          const uint8_t* purow = st + kOPU;
-          const float upV = out_scl[os].y;   // P U is in its chunk's v scale
-          const float sc = sc_ring[c & 7];     // O' = Q' (S_c / sc_c)
+          __nv_bfloat16* orow_p = a.o + (((size_t)b * a.L + pos) * a.Hv + h) * kD + col0;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch)
-            unpack8_f16(*reinterpret_cast<const uint4*>(purow + swz64(i * 64 + ch * 16)), pu + 8 * ch);
-          __nv_bfloat16* orow_p = a.o + (((size_t)b * a.L + pos) * a.Hv + h) * kD + sl * kN;
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            float v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = fmaf(sc, qs[8 * ch + e], upV * pu[8 * ch + e]);   // O' = Q' (S_c / sc)
-            *reinterpret_cast<uint4*>(orow_p + 8 * ch) = pack8_bf16(v);
-          }
+          for (int ch = 0; ch < 2; ++ch) *reinterpret_cast<uint4*>(orow_p + 8 * ch) = pack8_bf16(qs + 8 * ch);
         }
       }
       tc_fence_before();
@@ -1387,6 +1398,11 @@ chunk_state_kernel(const ChunkArgs a) {
       if (tid == 128) {
         mbar_arrive(&oFree[p]);
         if (c + OS < NC) mbar_arrive(&outFree[os]);   // the Q' product complete, P U read
+        if (kGated) {
+          // both output warps of each column half have read red[p]: every CTA may rewrite it
+#pragma unroll
+          for (uint32_t r = 0; r < kSlices; ++r) remote_arrive_relaxed(&freeR[p], r);
+        }
       }
     }
   }

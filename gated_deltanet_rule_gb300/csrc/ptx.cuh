@@ -167,36 +167,20 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(p)), "r"(rank));
   return addr;
 }
-// Store a float to a distributed-shared-memory address (from dsmem_addr).
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+// Store a 32-bit value to a distributed-shared-memory address (from dsmem_addr) as an asynchronous
+// store that completes 4 bytes of transaction on the mbarrier at `bar_addr` in the same CTA as the
+// destination: the receiver's wait on that mbarrier makes the value visible, no release needed.
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar_addr) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+               "r"(__float_as_uint(v)), "r"(bar_addr)
+               : "memory");
 }
-// As mbar_wait, with acquire at cluster scope (the phase was completed by arrivals from other CTAs
-// of the cluster whose earlier distributed-shared-memory stores must be visible).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, long long budget) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait_cluster(bar, parity)) {
-    if (clock64() - t0 > budget) return false;
-  }
-  return true;
-}
-// Arrive (release, cluster scope) on the mbarrier at the same offset as `bar` in CTA `rank`.
-__device__ __forceinline__ void remote_arrive(uint64_t* bar, uint32_t rank) {
+// Arrive (relaxed, cluster scope) on the mbarrier at the same offset as `bar` in CTA `rank`: a
+// signal that publishes no data (the arriving side's reads have completed).
+__device__ __forceinline__ void remote_arrive_relaxed(uint64_t* bar, uint32_t rank) {
   uint32_t addr;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(bar)), "r"(rank));
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 
 // ---------------------------------------------------------------------------------------------
