@@ -533,8 +533,10 @@ def run_epilogue(reps: int, warmup: int) -> dict:
 
 
 def run_backward(reps: int, warmup: int) -> dict:
-    """Times the backward (gdr_backward: the checkpointed token-loop kernel and its reducer) on the
-    prefill workload, L = 4096, Hk = 16, Hv = 32, bf16 q, k, v, dO, with dS_T. Its HBM roofline
+    """Times the backward on the prefill workload, L = 4096, Hk = 16, Hv = 32, bf16 q, k, v, dO,
+    with dS_T: gdr_backward_chunked (the chunked tensor-core form: forward factors, chunk-entry
+    states, Nb = Q'^T dO, the adjoint chain, the chunk-local gradients, the key-head reduction) as
+    the row, and gdr_backward (the checkpointed float32 token loop) beside it. The HBM roofline
     counts the algorithmic bytes: q, k, v, dO, g, beta, dS_T read once, every gradient written once."""
     import torch
     from gated_deltanet_rule_gb300 import gdr, inputs
@@ -542,40 +544,36 @@ def run_backward(reps: int, warmup: int) -> dict:
     x = inputs.regime("R1", L, 3, Hk=Hk, Hv=Hv, B=1, dtype=torch.bfloat16)
     dO, dS_T = inputs.upstream_grads(1, L, Hv, 4, dtype=torch.bfloat16)
     q, k, v, g, beta, dO, dS_T = (t.cuda() for t in (x.q, x.k, x.v, x.g, x.beta, dO, dS_T))
-    ws = torch.empty(gdr.backward_workspace_bytes(1, L, Hk, Hv), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     nbytes = (2 * L * Hk * D * 2 + 2 * L * Hv * D * 2 + 2 * L * Hv * 4 + Hv * D * D * 4       # inputs
               + 2 * L * Hk * D * 4 + L * Hv * D * 4 + 2 * L * Hv * 4 + Hv * D * D * 4)       # gradients
-
-    def call():
-        return gdr.gdr_backward(q, k, v, g, beta, None, dO, dS_T, ws=ws, stream=stream)
-
-    for _ in range(warmup):
-        call()
-    gdr.gdr_sync_status()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        out = call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / reps
-    gdr.stage_timer_enable(True, 4 * reps + 16)
-    for _ in range(reps):
-        call()
-    torch.cuda.synchronize()
-    stages = gdr.stage_timer_collect()
-    gdr.stage_timer_enable(False, 0)
-    gdr.gdr_sync_status()
-    gbs = nbytes / (us * 1e-6) / 1e9
     peaks = measured_peaks()
-    assert all(torch.isfinite(t).all() for t in out if t is not None)
-    return {"us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1),
-            "workload": f"backward of the prefill row [1, {L}], Hk={Hk}, Hv={Hv}, D={D}, bf16 q/k/v/dO, float32 gradients",
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes,
-                         "note": "a sequential token loop on CUDA cores: latency-bound, far from this roofline"},
-            "kernels": {kname: {"launches": c, "avg_us": round(t / c * 1e3, 2)} for kname, (t, c) in stages.items() if c}}
+    workload = f"backward of the prefill row [1, {L}], Hk={Hk}, Hv={Hv}, D={D}, bf16 q/k/v/dO, float32 gradients"
+
+    def timed(fn, ws_bytes):
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        out = []
+
+        def call(_i):
+            out[:] = fn(q, k, v, g, beta, None, dO, dS_T, ws=ws, stream=stream)
+        us, stages = _time_calls(call, reps, warmup, stream)
+        gdr.gdr_sync_status()
+        assert all(torch.isfinite(t).all() for t in out if t is not None)
+        del ws
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1),
+                "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes},
+                "kernels": stages}
+
+    row = timed(gdr.gdr_backward_chunked, gdr.backward_chunked_workspace_bytes(1, L, Hk, Hv))
+    row["workload"] = workload
+    row["roofline"]["note"] = ("latency of the sequential passes (the forward's chunk chain again and the adjoint "
+                               "chain, 64 steps each) and of the chunk-local products; far from this roofline")
+    loop = timed(gdr.gdr_backward, gdr.backward_workspace_bytes(1, L, Hk, Hv))
+    loop["roofline"]["note"] = "a sequential token loop on CUDA cores: latency-bound, far from this roofline"
+    row["token_loop_float32"] = loop
+    return row
 
 
 def _time_calls(fn, reps: int, warmup: int, stream) -> tuple[float, dict]:
@@ -593,7 +591,7 @@ def _time_calls(fn, reps: int, warmup: int, stream) -> tuple[float, dict]:
     e1.record(stream)
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / reps
-    gdr.stage_timer_enable(True, 4 * reps + 16)
+    gdr.stage_timer_enable(True, 8 * reps + 16)
     for i in range(reps):
         fn(i)
     torch.cuda.synchronize()

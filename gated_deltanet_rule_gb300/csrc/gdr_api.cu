@@ -365,6 +365,42 @@ gdr_status gdr_gated_rmsnorm(const void* x, const void* z, const float* w, float
   return launch_status(launch_gated_rmsnorm(ea, reinterpret_cast<cudaStream_t>(stream)), who);
 }
 
+// The backward's outputs (and the workspace) must not overlap one another or any input: half-open
+// byte ranges, checked pairwise.
+static gdr_status check_backward_buffers(const void* q, const void* k, const void* v, const float* g,
+                                         const float* beta, const float* S0, const void* dO, const float* dS_T,
+                                         const float* dq, const float* dk, const float* dv, const float* dg,
+                                         const float* dbeta, const float* dS0, const void* ws, size_t need, int B,
+                                         int L, int Hk, int Hv, size_t es, const char* who) {
+  const size_t nq = (size_t)B * L * Hk * kD, nv = (size_t)B * L * Hv * kD, ng = (size_t)B * L * Hv;
+  const size_t ns = (size_t)B * Hv * kD * kD;
+  struct Range {
+    const void* p;
+    size_t bytes;
+    const char* name;
+  };
+  const Range outs[] = {{dq, nq * 4, "dq"},       {dk, nq * 4, "dk"},     {dv, nv * 4, "dv"},
+                        {dg, ng * 4, "dg"},       {dbeta, ng * 4, "dbeta"}, {dS0, ns * 4, "dS0"},
+                        {ws, need, "ws"}};
+  const Range ins[] = {{q, nq * es, "q"}, {k, nq * es, "k"},     {v, nv * es, "v"},   {g, ng * 4, "g"},
+                       {beta, ng * 4, "beta"}, {S0, ns * 4, "S0"}, {dO, nv * es, "dO"}, {dS_T, ns * 4, "dS_T"}};
+  auto overlap = [](const Range& a, const Range& b) {
+    if (!a.p || !b.p) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+  };
+  const int n_out = sizeof(outs) / sizeof(outs[0]);
+  for (int i = 0; i < n_out; ++i) {
+    for (int j = i + 1; j < n_out; ++j)
+      if (overlap(outs[i], outs[j]))
+        return fail(GDR_ERR_INVALID_ARG, "%s: %s overlaps %s", who, outs[i].name, outs[j].name);
+    for (const Range& in : ins)
+      if (overlap(outs[i], in))
+        return fail(GDR_ERR_INVALID_ARG, "%s: %s overlaps the input %s", who, outs[i].name, in.name);
+  }
+  return GDR_OK;
+}
+
 size_t gdr_backward_workspace_bytes(int B, int L, int Hk, int Hv, int D) {
   if (B < 1 || L < 1 || Hk < 1 || Hv < 1 || D != kD || Hv % Hk != 0) return 0;
   return backward_workspace_bytes(B, L, Hk, Hv);
@@ -393,39 +429,48 @@ gdr_status gdr_backward(const void* q, const void* k, const void* v, const float
   if (ws == nullptr || ws_bytes < need)
     return fail(GDR_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", who, need,
                 ws == nullptr ? (size_t)0 : ws_bytes);
-  {
-    // the outputs (and the workspace) must not overlap one another or any input: half-open byte
-    // ranges, checked pairwise
-    const size_t es = dt == GDR_BF16 ? 2 : 4;
-    const size_t nq = (size_t)B * L * Hk * kD, nv = (size_t)B * L * Hv * kD, ng = (size_t)B * L * Hv;
-    const size_t ns = (size_t)B * Hv * kD * kD;
-    struct Range {
-      const void* p;
-      size_t bytes;
-      const char* name;
-    };
-    const Range outs[] = {{dq, nq * 4, "dq"},       {dk, nq * 4, "dk"},     {dv, nv * 4, "dv"},
-                          {dg, ng * 4, "dg"},       {dbeta, ng * 4, "dbeta"}, {dS0, ns * 4, "dS0"},
-                          {ws, need, "ws"}};
-    const Range ins[] = {{q, nq * es, "q"}, {k, nq * es, "k"},     {v, nv * es, "v"},   {g, ng * 4, "g"},
-                         {beta, ng * 4, "beta"}, {S0, ns * 4, "S0"}, {dO, nv * es, "dO"}, {dS_T, ns * 4, "dS_T"}};
-    auto overlap = [](const Range& a, const Range& b) {
-      if (!a.p || !b.p) return false;
-      const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
-      return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
-    };
-    const int n_out = sizeof(outs) / sizeof(outs[0]);
-    for (int i = 0; i < n_out; ++i) {
-      for (int j = i + 1; j < n_out; ++j)
-        if (overlap(outs[i], outs[j]))
-          return fail(GDR_ERR_INVALID_ARG, "%s: %s overlaps %s", who, outs[i].name, outs[j].name);
-      for (const Range& in : ins)
-        if (overlap(outs[i], in))
-          return fail(GDR_ERR_INVALID_ARG, "%s: %s overlaps the input %s", who, outs[i].name, in.name);
-    }
-  }
+  st = check_backward_buffers(q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, ws, need, B, L, Hk, Hv,
+                              dt == GDR_BF16 ? 2 : 4, who);
+  if (st != GDR_OK) return st;
   BackwardArgs a{q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, ws, B, L, Hk, Hv, dt == GDR_BF16};
   return launch_status(launch_backward(a, reinterpret_cast<cudaStream_t>(stream)), who);
+}
+
+size_t gdr_backward_chunked_workspace_bytes(int B, int L, int Hk, int Hv, int D) {
+  if (B < 1 || L < 1 || Hk < 1 || Hv < 1 || D != kD || Hv % Hk != 0) return 0;
+  return chunk_bwd_workspace_bytes(B, L, Hk, Hv);
+}
+
+gdr_status gdr_backward_chunked(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                const float* S0, const void* dO, const float* dS_T, float* dq, float* dk,
+                                float* dv, float* dg, float* dbeta, float* dS0, int B, int L, int Hk, int Hv,
+                                int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream) {
+  const char* who = "gdr_backward_chunked";
+  if (!dO) return fail(GDR_ERR_INVALID_ARG, "%s: dO must be non-NULL", who);
+  gdr_status st = check_common(q, k, v, g, beta, dO, B, L, Hk, Hv, D, dt, who);
+  if (st != GDR_OK) return st;
+  if (dt != GDR_BF16) return fail(GDR_ERR_UNSUPPORTED, "%s: bf16 q, k, v, dO only (float32: gdr_backward)", who);
+  if (!dq || !dk || !dv || !dg || !dbeta)
+    return fail(GDR_ERR_INVALID_ARG, "%s: dq, dk, dv, dg and dbeta must be non-NULL", who);
+  const void* ptrs16[] = {dq, dk, dv, dg, dbeta, S0, dS_T, dS0, ws};
+  for (const void* p : ptrs16)
+    if (p && !aligned16(p))
+      return fail(GDR_ERR_INVALID_ARG, "%s: every array and the workspace must be 16-byte aligned", who);
+  // launch limits: B Hv NC units on the grid's x dimension, B L positions on the reducer's
+  const long long units = (long long)B * Hv * ((L + kChunk - 1) / kChunk);
+  if (units > 0x7fffffffLL || (long long)B * L > 0x7fffffffLL || Hk > 65535 || Hv > 65535 || B > 65535)
+    return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d, L=%d, Hv=%d too large", who, B, L, Hv);
+  const size_t need = chunk_bwd_workspace_bytes(B, L, Hk, Hv);
+  if (ws == nullptr || ws_bytes < need)
+    return fail(GDR_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", who, need,
+                ws == nullptr ? (size_t)0 : ws_bytes);
+  st = check_backward_buffers(q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, ws, need, B, L, Hk, Hv, 2,
+                              who);
+  if (st != GDR_OK) return st;
+  int* err = device_error_word();
+  if (!err) return fail(GDR_ERR_CUDA, "%s: no device error word", who);
+  ChunkBackwardArgs a{q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, ws, B, L, Hk, Hv, err};
+  return launch_status(launch_chunk_backward(a, reinterpret_cast<cudaStream_t>(stream)), who);
 }
 
 gdr_status gdr_sync_status(gdr_stream_t stream) {
@@ -516,6 +561,10 @@ const char* gdr_kernel_name(int id) {
     case kKernEpilogue: return "gdr_gated_rmsnorm";
     case kKernBackward: return "gdr_backward";
     case kKernBackwardReduce: return "gdr_backward_reduce";
+    case kKernChunkNb: return "gdr_chunk_nb";
+    case kKernChunkAdjoint: return "gdr_chunk_adjoint";
+    case kKernChunkBwdLocal: return "gdr_chunk_bwd_local";
+    case kKernChunkBwdReduce: return "gdr_chunk_bwd_reduce";
   }
   return nullptr;
 }

@@ -44,6 +44,7 @@
 #include <cudaTypedefs.h>
 
 #include "gdr_epilogue.h"
+#include "gdr_backward.h"
 #include "gdr_internal.h"
 #include "ptx.cuh"
 
@@ -89,6 +90,10 @@ struct ChunkArgs {
   const __nv_bfloat16* z;
   const float* w;
   float eps;
+  // state kernel modes 1 and 2 (the backward's passes): the state at the top of each chunk's step,
+  // float32 [B, Hv, NC, D, D] (mode 1: the chunk's entering state; mode 2: the adjoint of its
+  // exiting state)
+  float* st_save;
 };
 
 __device__ __forceinline__ uint8_t* unit_base(const ChunkArgs& a, int b, int h, int c) {
@@ -124,10 +129,6 @@ __device__ __forceinline__ void pow2_scales(float m, float& up, float& dn) {
   e = e < -125 ? -125 : (e > 125 ? 125 : e);
   up = __uint_as_float((uint32_t)(127 + e) << 23);
   dn = __uint_as_float((uint32_t)(127 - e) << 23);
-}
-// bf16x2 word -> fp16x2 word of the values times s (a power of two)
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float s) {
-  return pack_f16x2(__uint_as_float(w << 16) * s, __uint_as_float(w & 0xFFFF0000u) * s);
 }
 
 // -------------------------------------------------------------------------------------------
@@ -1027,9 +1028,16 @@ constexpr int kSb = 5;                 // fp16 state operands: the output path m
 constexpr uint32_t state_smem(int cs, int os) { return cs * kCStage + os * kOStage + kSb * 8192 + 1024; }
 static_assert(kCN == kMBytes && kOPU == kQBytes, "stage layout");
 
-template <int CS, int OS, bool kGated>
+// kMode 0: the forward (o and S_T). kMode 1: the forward recomputed for the backward: no output
+// side; the entering state of every chunk is saved to st_save. kMode 2: the backward's adjoint
+// chain dS <- Gamma_C dS + M'^T dS + Nb, chunks from the last to the first: the unit's N slot holds
+// Nb = Q'^T dO (in the scale block's second word's scale), the chain product reads the M' image
+// transposed (an MN-major A operand), the initial state is dS_T (a.S0), the final one dS0 (a.S_T),
+// and the adjoint entering each chunk's step (that of its exiting state) is saved to st_save.
+template <int CS, int OS, bool kGated, int kMode>
 __global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const ChunkArgs a) {
+  constexpr bool kOut = kMode == 0;   // the output side (output ring, product and warps) runs
   constexpr uint32_t kOffO = CS * kCStage;
   constexpr uint32_t kOffSb = kOffO + OS * kOStage;
   extern __shared__ uint8_t smem_raw[];
@@ -1114,7 +1122,7 @@ chunk_state_kernel(const ChunkArgs a) {
     // every CTA of the row reads the same index and skips
   } else if (warp == 6 || warp == 10) {
     // ---------------- producers (lane 0): the chain ring (warp 6) and the output ring (warp 10) ---
-    if (lane == 0) {
+    if (lane == 0 && (warp == 6 || kOut)) {
       wait_prerequisite();   // the workspace is complete once the prep kernel has finished
       const bool chain = warp == 6;
       const int S = chain ? CS : OS;
@@ -1123,7 +1131,8 @@ chunk_state_kernel(const ChunkArgs a) {
         const int s = c % S;
         if (c >= S) ok = mbar_wait(chain ? &chFree[s] : &outFree[s], ((c - S) / S) & 1, a.wait_budget);
         if (!ok || *(volatile int*)&abort_flag) break;
-        const uint8_t* ub = unit_base(a, b, h, c);
+        const int cu = kMode == 2 ? NC - 1 - c : c;   // the chunk of step c
+        const uint8_t* ub = unit_base(a, b, h, cu);
         if (chain) {
           uint8_t* st = sm + s * kCStage;
           mbar_arrive_expect_tx(&chFull[s], kMBytes + 8192 + kSCopy);
@@ -1131,8 +1140,8 @@ chunk_state_kernel(const ChunkArgs a) {
           bulk_load(st + 16384, ub + 16384, 16384, &chFull[s]);
           bulk_load(st + kCN, ub + kUnitN + sl * 8192, 8192, &chFull[s]);
           bulk_load(&gam_ring[s], ub + kUnitS, kSCopy, &chFull[s]);
-          if (c + kPrefetchAhead < NC) {   // the chunk kPrefetchAhead further on into L2
-            const uint8_t* uf = unit_base(a, b, h, c + kPrefetchAhead);
+          if (c + kPrefetchAhead < NC) {   // the chunk kPrefetchAhead steps further on into L2
+            const uint8_t* uf = unit_base(a, b, h, kMode == 2 ? cu - kPrefetchAhead : cu + kPrefetchAhead);
             bulk_prefetch_l2(uf, kMBytes);
             bulk_prefetch_l2(uf + kUnitN + sl * 8192, 8192);
           }
@@ -1211,6 +1220,14 @@ chunk_state_kernel(const ChunkArgs a) {
     for (int c = 0; c < NC; ++c) {
       const int cs = c % CS, p = c & 1, qn = (c + 1) % kSb;
       const uint8_t* st = sm + cs * kCStage;
+      if (kMode != 0) {
+        // the state at the top of the step: this thread's key row, the CTA's 32 value columns
+        const int cu = kMode == 2 ? NC - 1 - c : c;
+        float* dst = a.st_save + ((((size_t)b * a.Hv + h) * NC + cu) * kD + kr) * kD + sl * kN;
+#pragma unroll
+        for (int n = 0; n < kN; n += 4)
+          *reinterpret_cast<float4*>(dst + n) = make_float4(Sm[n], Sm[n + 1], Sm[n + 2], Sm[n + 3]);
+      }
       ok = ok && mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
       if (ok) {
         // while the product D = M' S_c runs: S <- Gamma_C S + upV N (S_c is already in the fp16
@@ -1226,7 +1243,7 @@ chunk_state_kernel(const ChunkArgs a) {
         }
         // Sb[qn] is rewritten below: the output product of chunk c + 1 - kSb must have read it
         ok = mbar_wait(&bar_d, c & 1, a.wait_budget) &&
-             (c + 1 < kSb || mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget));
+             (c + 1 < kSb || !kOut || mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget));
       }
       ok = __all_sync(0xffffffffu, ok);   // the TMEM load below is warp-collective
       if (ok) {
@@ -1259,7 +1276,7 @@ chunk_state_kernel(const ChunkArgs a) {
   } else if (warp == 11) {
     // ---------------- state-product issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(128, kN, false, true);
+      const uint32_t idesc = idesc_f16(128, kN, kMode == 2, true);
       int last = -1;   // last chunk whose state product was issued
       for (int c = 0; c < NC; ++c) {
         const int cs = c % CS, p = c & 1, q = c % kSb;
@@ -1268,11 +1285,14 @@ chunk_state_kernel(const ChunkArgs a) {
         tc_fence_after();
         const uint32_t sb = smem_u32(sm + kOffSb + q * 8192);
         const uint32_t sm_m = smem_u32(sm + cs * kCStage);
-        // D[p] = M' S_c: the product on the chain
+        // D[p] = M' S_c: the product on the chain (kMode 2: M'^T dS, the K-major M' image read as an
+        // MN-major operand: K-row j is row j of M', the two 64-row M blocks its two column atoms)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tb + 32 * p, smem_desc(sm_m + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                   smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t adesc = kMode == 2 ? smem_desc(sm_m + kk * 2048, 16384, 1024)
+                                            : smem_desc(sm_m + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+          mma_bf16(tb + 32 * p, adesc, smem_desc(sb + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
+        }
         mma_commit(&bar_d);
         mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
         last = c;
@@ -1281,7 +1301,7 @@ chunk_state_kernel(const ChunkArgs a) {
     }
   } else if (warp == 7) {
     // ---------------- output-product issuer ----------------
-    if (lane == 0) {
+    if (lane == 0 && kOut) {
       const uint32_t idesc = idesc_f16(128, kN, false, true);
       int last = -1;   // last chunk whose output product was issued
       for (int c = 0; c < NC; ++c) {
@@ -1304,7 +1324,7 @@ chunk_state_kernel(const ChunkArgs a) {
       }
       if (!ok && last >= 0) mbar_wait(&bar_o[last & 1], (last >> 1) & 1, kDrainBudget);   // drain
     }
-  } else {
+  } else if (kOut) {
     // ---------------- output warps 4, 5, 8, 9 ----------------
     const int i = 32 * (warp & 1) + lane;   // position in the chunk = TMEM lane
     const int hc = warp >> 3;               // column half: slice columns 16 hc .. 16 hc + 15
@@ -1423,6 +1443,124 @@ chunk_state_kernel(const ChunkArgs a) {
 }
 
 // -------------------------------------------------------------------------------------------
+// Backward: Nb = Q'^T dO per unit, the adjoint chain's inhomogeneous term
+// -------------------------------------------------------------------------------------------
+// One CTA per (row, value head, chunk) unit. Q' (the unit's fp16 image, positions x keys, K-major)
+// read transposed is an MN-major A operand (keys = M in its two 64-column atoms, positions = K);
+// the dO tile (positions x values, TMA with 128-byte swizzle) is an MN-major B operand once
+// converted to fp16, divided by the power of two of its largest magnitude. Nb (keys x values) is
+// written over the unit's N slot, which the forward state pass has consumed, in N's four 32-column
+// slices, and the scale (that power of two) into the scale block's second word, where the state
+// kernel takes N's scale from. Gamma_C in the first word stays.
+constexpr int kNbThreads = 128;
+constexpr uint32_t kNbSmem = 16384 + 16384 + 32768 + 1024;   // Q', dO, Nb staging, alignment
+
+__global__ void __launch_bounds__(kNbThreads)
+chunk_nb_kernel(const __grid_constant__ CUtensorMap tm_do, const ChunkArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint32_t tmem_base;
+  __shared__ uint32_t wmax[kNbThreads / 32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int u = blockIdx.x;
+  const int c = u % a.NC, h = (u / a.NC) % a.Hv, b = u / (a.NC * a.Hv);
+  uint8_t* ub = unit_base(a, b, h, c);
+  uint8_t* sq = sm;              // Q' image: atoms (keys 0-63, 64-127) of 64 positions x 128 B
+  uint8_t* sd = sm + 16384;      // dO: two 64 x 64 boxes (values 0-63, 64-127)
+  uint8_t* sn = sm + 32768;      // Nb staging: four 32-column slices of 128 rows x 64 B
+  if (tid == 0) {
+    mbar_init(&bar_ld, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar_ld, 2 * 16384);
+    bulk_load(sq, ub + kUnitQ, kQBytes, &bar_ld);
+    tma_load_4d(sd, &tm_do, &bar_ld, 0, h, c * kChunk, b);
+    tma_load_4d(sd + 8192, &tm_do, &bar_ld, 64, h, c * kChunk, b);
+  }
+  const bool ld_ok = mbar_wait(&bar_ld, 0, a.wait_budget);
+  bool ok = __syncthreads_and(ld_ok);
+  float up = 1.f, dn = 1.f;
+  if (ok) {
+    // dO's largest magnitude (bf16 magnitude bits order like the values), then dO / 2^e as fp16
+    uint32_t m2 = 0;
+    for (int c16 = tid; c16 < 1024; c16 += kNbThreads) {
+      const uint4 w = reinterpret_cast<const uint4*>(sd)[c16];
+      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu), __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
+    }
+    const uint32_t mw = __reduce_max_sync(0xffffffffu, max(m2 & 0xFFFFu, m2 >> 16));
+    if (lane == 0) wmax[warp] = mw;
+    __syncthreads();
+    pow2_scales(__uint_as_float(max(max(wmax[0], wmax[1]), max(wmax[2], wmax[3])) << 16), up, dn);
+    for (int c16 = tid; c16 < 1024; c16 += kNbThreads) {
+      uint4* pw = reinterpret_cast<uint4*>(sd) + c16;
+      const uint4 w = *pw;
+      *pw = make_uint4(bf16x2_to_f16x2_scaled(w.x, dn), bf16x2_to_f16x2_scaled(w.y, dn),
+                       bf16x2_to_f16x2_scaled(w.z, dn), bf16x2_to_f16x2_scaled(w.w, dn));
+    }
+    fence_async_smem();
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (ok && tid == 0) {
+    // D[keys, values] = Q'^T dO: M = 128 (two 64-key blocks 8 KB apart), N = 128 (two 64-value
+    // blocks 8 KB apart), K = 64 positions in steps of 16 rows (2 KB)
+    tc_fence_after();
+    const uint32_t idesc = idesc_f16(128, 128, true, true);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16(tb, smem_desc(smem_u32(sq) + kk * 2048, 8192, 1024), smem_desc(smem_u32(sd) + kk * 2048, 8192, 1024),
+               idesc, kk > 0);
+    mma_commit(&bar_mma);
+  }
+  const bool issued = ok;   // the product was committed (tid 0 issues it exactly when ok)
+  ok = __syncthreads_and(ok && mbar_wait(&bar_mma, 0, a.wait_budget));
+  if (ok) {
+    tc_fence_after();
+    // key row i = tid = TMEM lane; its 128 values into the four slices
+    const int i = tid;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float w[64];
+      tmem_ld64(tb + lane_base + 64 * half, w);
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const int col = 64 * half + 8 * q8;
+        *reinterpret_cast<uint4*>(sn + (col >> 5) * 8192 + swz64(i * 64 + (q8 & 3) * 16)) = pack8_f16(w + 8 * q8);
+      }
+    }
+    fence_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (ok && tid == 0) {
+    bulk_store(ub + kUnitN, sn, kNBytes);
+    bulk_commit();
+    *reinterpret_cast<float*>(ub + kUnitS + 4) = up;   // N's scale for the adjoint chain
+    bulk_wait_all();
+  }
+  if (!ok && tid == 0) {
+    // drain what is still in flight before the CTA's memory is released
+    set_error(a.err, kErrTimeout);
+    if (!ld_ok) mbar_wait(&bar_ld, 0, kDrainBudget);
+    if (issued) mbar_wait(&bar_mma, 0, kDrainBudget);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tb, 128);
+  }
+}
+
+// -------------------------------------------------------------------------------------------
 // Host side
 // -------------------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1507,7 +1645,7 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(p.z ? chunk_state_kernel<3, 3, true> : chunk_state_kernel<3, 3, false>,
+    e = cudaFuncSetAttribute(p.z ? chunk_state_kernel<3, 3, true, 0> : chunk_state_kernel<3, 3, false, 0>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem(3, 3));
   if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkPrep);
@@ -1544,8 +1682,76 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.z ? 2 : 1;
-  e = p.z ? cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, true>, a)
-          : cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false>, a);
+  e = p.z ? cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, true, 0>, a)
+          : cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 0>, a);
+  stage_timer_end(slot, s);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+size_t chunk_bwd_units_bytes(int B, int L, int Hv) { return units_bytes(B, L, Hv) + 1024; }
+
+cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s) {
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_map(&mq, p.q, p.B, p.L, p.Hk) || !make_map(&mk, p.k, p.B, p.L, p.Hk) ||
+      !make_map(&mv, p.v, p.B, p.L, p.Hv) || !make_map(&mo, p.dO, p.B, p.L, p.Hv))
+    return cudaErrorInvalidValue;
+  ChunkArgs a{};
+  a.g = p.g;
+  a.beta = p.beta;
+  a.S0 = p.S0;
+  a.fused = 0;   // rows of one chunk also go through the workspace: the backward needs their factors
+  a.wait_budget = wait_budget_cycles();
+  a.ws = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p.ws) + 1023) & ~uintptr_t(1023));
+  a.B = p.B;
+  a.L = p.L;
+  a.Hk = p.Hk;
+  a.Hv = p.Hv;
+  a.NC = (p.L + kChunk - 1) / kChunk;
+  a.err = p.err;
+  cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(chunk_state_kernel<3, 3, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             state_smem(3, 3));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(chunk_state_kernel<3, 3, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             state_smem(3, 3));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(chunk_nb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kNbSmem);
+  if (e != cudaSuccess) return e;
+  // 1. the forward's chunk factors
+  const long long units = (long long)a.B * a.Hv * a.NC;
+  int slot = stage_timer_begin(s, kKernChunkPrep);
+  chunk_prep_kernel<false><<<(int)std::min<long long>(units, 2ll * num_sms()), kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
+  stage_timer_end(slot, s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // 2. the chunk-entry states (a programmatic dependent of the prep kernel, as in the forward)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kSlices, p.Hv, p.B);
+  cfg.blockDim = dim3(kStateThreads, 1, 1);
+  cfg.dynamicSmemBytes = state_smem(3, 3);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  a.st_save = p.S_save;
+  a.S_T = nullptr;
+  slot = stage_timer_begin(s, kKernChunkState);
+  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 1>, a);
+  stage_timer_end(slot, s);
+  if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
+  // 3. Nb = Q'^T dO over the N slots the state pass has read
+  slot = stage_timer_begin(s, kKernChunkNb);
+  chunk_nb_kernel<<<(unsigned)units, kNbThreads, kNbSmem, s>>>(mo, a);
+  stage_timer_end(slot, s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // 4. the adjoint chain: dS_T in, dS0 out, the adjoint entering each chunk's step saved
+  a.S0 = p.dS_T;
+  a.S_T = p.dS0;
+  a.st_save = p.dS_save;
+  slot = stage_timer_begin(s, kKernChunkAdjoint);
+  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 2>, a);
   stage_timer_end(slot, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -1,0 +1,760 @@
+// Chunked backward of the gated delta rule, bf16 rows: the chunk-local gradients and the key-head
+// reduction. The sequential passes (the forward's chunk factors, the chunk-entry states S_c, Nb =
+// Q'^T dO and the adjoint chain) run in gdr_chunk.cu (launch_chunk_bwd_chain); what is left is
+// local to each (row, value head, chunk) unit once S_c and the adjoint dS' of the chunk's exiting
+// state are known.
+//
+// The pages train through the recurrence but print no backward. With the chunk algebra of the
+// forward (per 64-token chunk, entering state S: A_ij = beta_i (k^_i . k^_j) E_ij for j < i with
+// E_ij = e^{gamma_i - gamma_j}, T = (I + A)^-1, W = T diag(beta Gamma) K^, U = T diag(beta) V,
+// Delta = U - W S, P_ij = (q~_i . k^_j) E_ij for j <= i, O = diag(Gamma) Q~ S + P Delta,
+// S' = Gamma_C S + K^T diag(e) Delta with e_i = e^{gamma_C - gamma_i}), the reverse given dO and
+// dS' is, per chunk:
+//   dDelta = P^T dO + diag(e) K^ dS',  dW = -dDelta S^T,  dP = dO Delta^T (j <= i)
+//   dQ~ = diag(Gamma) dO S^T + (dP o E) K^
+//   dK^ = (dP o E)^T Q~ + diag(e) Delta dS'^T + diag(beta Gamma) T^T dW + (dA~ + dA~^T) K^
+//   dT = dDelta (diag(beta) V)^T + dW (diag(beta Gamma) K^)^T,  dA = -T^T dT T^T (j < i),
+//   dA~ = dA o beta_i E,  dV = diag(beta) T^T dDelta
+//   dbeta_i = V_i . (T^T dDelta)_i + Gamma_i K^_i . (T^T dW)_i + sum_j dA_ij (k^_i . k^_j) E_ij
+//   dgamma_i = Gamma_i q~_i . (dO S^T)_i + rows - columns of (dP o P) and (dA o A)
+//              + beta_i Gamma_i K^_i . (T^T dW)_i - e_i k^_i . (dS' Delta_i)
+//              (+ Gamma_C <S, dS'> + sum_j e_j k^_j . (dS' Delta_j) at the chunk's last position)
+//   dg_j = sum_{i >= j} dgamma_i within the chunk
+// then the normalisations' backward and the sum over the value heads of a key head.
+//
+// Products run on warp-level tensor-core instructions (mma.sync m16n8k16, fp32 accumulation):
+// they are 64-row products of K = 64 or 128, a dozen per unit, each feeding an elementwise
+// epilogue, with both operands already in shared memory. The raw bf16 q, k enter the Gram
+// products exactly (bf16 operands); every other operand is fp16, divided by the power of two of its
+// tile's largest magnitude where that magnitude is not bounded (v, dO, S, dS', Delta and the
+// gradients), the scales applied back in fp32.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "gdr_backward.h"
+#include "gdr_internal.h"
+#include "ptx.cuh"
+
+namespace gdr {
+namespace {
+using namespace ptx;
+
+constexpr int kLT = 256;                         // threads of the chunk-local kernel (8 warps)
+constexpr int kLd = 136;                         // row stride (halves) of 128-column fp16 tiles
+constexpr int kLs = 72;                          // row stride (halves) of 64-column fp16 tiles
+constexpr int kLf = 68;                          // row stride (floats) of the fp32 64 x 64 tile
+constexpr float kQs = 0.08838834764831845f;      // 128^-0.5
+constexpr float kL2e = 1.4426950408889634f;
+
+constexpr uint32_t kT128 = 64 * kLd * 2;         // a 64 x 128 fp16 tile
+constexpr uint32_t kT128x = 128 * kLd * 2;       // a 128 x 128 fp16 tile
+constexpr uint32_t kT64 = 64 * kLs * 2;          // a 64 x 64 fp16 tile
+constexpr uint32_t kOQ = 0;                      // q (bf16, then the fp16 unit rows q^)
+constexpr uint32_t kOK = kOQ + kT128;            // k (bf16, then k^)
+constexpr uint32_t kOV = kOK + kT128;            // v / 2^eV
+constexpr uint32_t kOO = kOV + kT128;            // dO / 2^eO
+constexpr uint32_t kOS = kOO + kT128;            // S / 2^eS [key][value]; later dPE, dT, Z
+constexpr uint32_t kODS = kOS + kT128x;          // dS' / 2^eD; later dW, dA~
+constexpr uint32_t kOX1 = kODS + kT128x;         // beta Gamma K^, beta V, then Delta
+constexpr uint32_t kOX2 = kOX1 + kT128;          // W, then dDelta
+constexpr uint32_t kOTf = kOX2 + kT128;          // fp32 A (strictly lower)
+constexpr uint32_t kOT16 = kOTf + 64 * kLf * 4;  // T (fp16)
+constexpr uint32_t kOP16 = kOT16 + kT64;         // P (fp16)
+constexpr uint32_t kOG16 = kOP16 + kT64;         // K^ K^T (fp16)
+constexpr uint32_t kOVec = kOG16 + kT64;         // per-position vectors and reduction scratch
+constexpr int kNVec = 24;
+constexpr uint32_t kLocalSmem = kOVec + kNVec * 64 * 4;
+// vectors (64 floats each)
+enum : int { vG2 = 0, vGam, vE, vBet, vSq, vSk, vRowG0, vRowG1, vRowB0, vRowB1, vRowD0, vRowD1,
+             vColG0, vColG1, vColG2, vColG3, vMax, vDot, vScan };
+
+__device__ __forceinline__ void pow2_up_dn(float m, float& up, float& dn) {
+  // up = 2^e with m / up in [0.5, 1) (1 for m = 0), dn = 1 / up, e clamped to keep both normal
+  const int eb = (int)((__float_as_uint(m) >> 23) & 0xFFu);
+  int e = eb == 0 ? 0 : eb - 126;
+  e = e < -125 ? -125 : (e > 125 ? 125 : e);
+  up = __uint_as_float((uint32_t)(127 + e) << 23);
+  dn = __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+template <bool kBf>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if (kBf)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// acc (16 rows from m0, 8 NT columns from n0) += A B over K. A: 64 x K, stored [row][K] (AT false)
+// or [K][row] (AT true: the product uses the transpose of the stored tile). B: K x N, stored
+// [K][N] (BT false) or [N][K] (BT true). Strides in 16-bit elements. The fragment this thread
+// holds: rows m0 + g and m0 + g + 8, columns n0 + 8 nt + 2 t and + 1 (g = lane / 4, t = lane % 4).
+template <int NT, bool AT, bool BT, bool kBf = false>
+__device__ __forceinline__ void tile_mma(float (&acc)[NT][4], const uint8_t* A, int lda, int m0, const uint8_t* B,
+                                         int ldb, int n0, int K, int lane) {
+  const uint16_t* a16 = reinterpret_cast<const uint16_t*>(A);
+  const uint16_t* b16 = reinterpret_cast<const uint16_t*>(B);
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t af[4];
+    if (!AT)
+      ldsm_x4(af, a16 + (m0 + (lane & 15)) * lda + k0 + 8 * (lane >> 4));
+    else
+      ldsm_x4_t(af, a16 + (k0 + (lane & 7) + 8 * (lane >> 4)) * lda + m0 + 8 * ((lane >> 3) & 1));
+#pragma unroll
+    for (int nt = 0; nt < NT; nt += 2) {
+      uint32_t bf[4];
+      if (!BT)
+        ldsm_x4_t(bf, b16 + (k0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * ldb + n0 + 8 * nt + 8 * (lane >> 4));
+      else
+        ldsm_x4(bf, b16 + (n0 + 8 * nt + (lane & 7) + 8 * (lane >> 4)) * ldb + k0 + 8 * ((lane >> 3) & 1));
+      mma16816<kBf>(acc[nt], af, bf[0], bf[1]);
+      mma16816<kBf>(acc[nt + 1], af, bf[2], bf[3]);
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void zero(float (&acc)[NT][4]) {
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+}
+template <int NT>
+__device__ __forceinline__ float absmax(const float (&acc)[NT][4]) {
+  float m = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(acc[nt][e]));
+  return m;
+}
+__device__ __forceinline__ float h2f(const uint8_t* tile, int ld, int r, int c) {
+  return __half2float(reinterpret_cast<const __half*>(tile)[r * ld + c]);
+}
+// fragment element (row, column) of acc[nt][e]
+__device__ __forceinline__ int frow(int m0, int lane, int e) { return m0 + (lane >> 2) + 8 * (e >> 1); }
+__device__ __forceinline__ int fcol(int n0, int lane, int nt, int e) { return n0 + 8 * nt + 2 * (lane & 3) + (e & 1); }
+
+// store a fragment as fp16 (times s) into a tile with stride ld
+template <int NT>
+__device__ __forceinline__ void store_h(uint8_t* tile, int ld, int m0, int n0, const float (&acc)[NT][4], float s,
+                                        int lane) {
+  __half* t = reinterpret_cast<__half*>(tile);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = frow(m0, lane, 2 * hh), c = fcol(n0, lane, nt, 0);
+      *reinterpret_cast<__half2*>(t + r * ld + c) = __floats2half2_rn(acc[nt][2 * hh] * s, acc[nt][2 * hh + 1] * s);
+    }
+}
+
+// CTA-wide max of a per-thread value (every thread gets it); uses vec[vMax][0..7]
+__device__ __forceinline__ float cta_max(float m, float* vmax, int warp, int lane) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __syncthreads();   // earlier readers of vmax are done
+  if (lane == 0) vmax[warp] = m;
+  __syncthreads();
+  float r = vmax[0];
+#pragma unroll
+  for (int w = 1; w < kLT / 32; ++w) r = fmaxf(r, vmax[w]);
+  return r;
+}
+
+struct LocalArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const float* g;
+  const float* beta;
+  const __nv_bfloat16* dO;
+  const float* S_save;    // [B, Hv, NC, D, D]
+  const float* dS_save;   // [B, Hv, NC, D, D]
+  float* dqt;             // [B, L, Hv, D]: gradient of q~ per value head
+  float* dkh;             // [B, L, Hv, D]: gradient of k^ per value head
+  float* dv;
+  float* dg;
+  float* dbeta;
+  int B, L, Hk, Hv, NC;
+};
+
+// One CTA per (row, value head, chunk) unit. Warp w owns rows 16 (w % 4) .. + 15 of every 64-row
+// product and the column half w / 4 (64 columns of a 128-column product, 32 of a 64-column one).
+__global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  float* vec = reinterpret_cast<float*>(sm + kOVec);
+  auto V = [&](int i) { return vec + i * 64; };
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int u = blockIdx.x;
+  const int c = u % a.NC, h = (u / a.NC) % a.Hv, b = u / (a.NC * a.Hv);
+  const int hk = h / (a.Hv / a.Hk);
+  const int m0 = 16 * (warp & 3), half = warp >> 2;
+  const int n128 = 64 * half, n64 = 32 * half;
+  const int p0 = c * kChunk;   // first position of the chunk
+  uint8_t* tQ = sm + kOQ;
+  uint8_t* tK = sm + kOK;
+  uint8_t* tV = sm + kOV;
+  uint8_t* tO = sm + kOO;
+  uint8_t* tS = sm + kOS;
+  uint8_t* tD = sm + kODS;
+  uint8_t* tX1 = sm + kOX1;
+  uint8_t* tX2 = sm + kOX2;
+  float* Af = reinterpret_cast<float*>(sm + kOTf);
+  uint8_t* tT = sm + kOT16;
+  uint8_t* tP = sm + kOP16;
+  uint8_t* tG = sm + kOG16;
+
+  // ---- 0. inputs: gates, raw q k v dO rows (zero past L), S and dS' (fp32 -> fp16 scaled) ----
+  if (tid < 64) {
+    const int pos = p0 + tid;
+    const size_t gi = ((size_t)b * a.L + pos) * a.Hv + h;
+    const float gg = pos < a.L ? a.g[gi] : 0.f;
+    V(vBet)[tid] = pos < a.L ? a.beta[gi] : 0.f;
+    float x = gg;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    V(vScan)[tid] = x;
+  }
+  {
+    // 64 rows x 16 chunks of 16 bytes for each of q, k (key head hk) and v, dO (value head h)
+    for (int idx = tid; idx < 4 * 1024; idx += kLT) {
+      const int which = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
+      const int pos = p0 + row;
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (pos < a.L) {
+        const __nv_bfloat16* src = which == 0 ? a.q : which == 1 ? a.k : which == 2 ? a.v : a.dO;
+        const int H = which < 2 ? a.Hk : a.Hv, hh = which < 2 ? hk : h;
+        w = __ldg(reinterpret_cast<const uint4*>(src + (((size_t)b * a.L + pos) * H + hh) * kD) + ch);
+      }
+      uint8_t* dst = which == 0 ? tQ : which == 1 ? tK : which == 2 ? tV : tO;
+      *reinterpret_cast<uint4*>(dst + row * kLd * 2 + ch * 16) = w;
+    }
+  }
+  // S and dS': thread tid holds float4 number tid + 256 m (m < 16) of each, in registers
+  const size_t sbase = (((size_t)b * a.Hv + h) * a.NC + c) * kD * kD;
+  float4 s4[16], d4[16];
+  float mS = 0.f, mD = 0.f, dot = 0.f;
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    s4[m] = __ldg(reinterpret_cast<const float4*>(a.S_save + sbase) + tid + 256 * m);
+    d4[m] = __ldg(reinterpret_cast<const float4*>(a.dS_save + sbase) + tid + 256 * m);
+    mS = fmaxf(mS, fmaxf(fmaxf(fabsf(s4[m].x), fabsf(s4[m].y)), fmaxf(fabsf(s4[m].z), fabsf(s4[m].w))));
+    mD = fmaxf(mD, fmaxf(fmaxf(fabsf(d4[m].x), fabsf(d4[m].y)), fmaxf(fabsf(d4[m].z), fabsf(d4[m].w))));
+    dot += s4[m].x * d4[m].x + s4[m].y * d4[m].y + s4[m].z * d4[m].z + s4[m].w * d4[m].w;
+  }
+  __syncthreads();
+  if (tid < 64) {
+    const float gam = V(vScan)[tid] + (tid >= 32 ? V(vScan)[31] : 0.f);
+    V(vG2)[tid] = gam * kL2e;
+  }
+  __syncthreads();
+  if (tid < 64) {
+    V(vGam)[tid] = exp2f(V(vG2)[tid]);
+    V(vE)[tid] = exp2f(V(vG2)[63] - V(vG2)[tid]);
+  } else if (tid < 192) {
+    // inverse norms of the raw q, k rows (threads 64-127: q, 128-191: k)
+    const int row = tid & 63;
+    const uint8_t* src = (tid < 128 ? tQ : tK) + row * kLd * 2;
+    float s0 = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < 16; ++ch) {
+      const uint4 w = *reinterpret_cast<const uint4*>(src + ch * 16);
+      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xFFFF0000u);
+        s0 = fmaf(lo, lo, fmaf(hi, hi, s0));
+      }
+    }
+    V(tid < 128 ? vSq : vSk)[row] = rsqrtf(s0 + 1e-6f);
+  }
+  // largest |v|, |dO| (bf16 magnitude bits order like the values)
+  uint32_t mv = 0, mo = 0;
+  for (int idx = tid; idx < 1024; idx += kLT) {
+    const int row = idx >> 4, ch = idx & 15;
+    const uint4 wv = *reinterpret_cast<const uint4*>(tV + row * kLd * 2 + ch * 16);
+    const uint4 wo = *reinterpret_cast<const uint4*>(tO + row * kLd * 2 + ch * 16);
+    mv = __vmaxu2(mv, __vmaxu2(__vmaxu2(wv.x & 0x7FFF7FFFu, wv.y & 0x7FFF7FFFu), __vmaxu2(wv.z & 0x7FFF7FFFu, wv.w & 0x7FFF7FFFu)));
+    mo = __vmaxu2(mo, __vmaxu2(__vmaxu2(wo.x & 0x7FFF7FFFu, wo.y & 0x7FFF7FFFu), __vmaxu2(wo.z & 0x7FFF7FFFu, wo.w & 0x7FFF7FFFu)));
+  }
+  const float fmv = __uint_as_float(max(mv & 0xFFFFu, mv >> 16) << 16);
+  const float fmo = __uint_as_float(max(mo & 0xFFFFu, mo >> 16) << 16);
+  float upV, dnV, upO, dnO, upS, dnS, upD, dnD;
+  pow2_up_dn(cta_max(fmv, V(vMax), warp, lane), upV, dnV);
+  pow2_up_dn(cta_max(fmo, V(vMax), warp, lane), upO, dnO);
+  pow2_up_dn(cta_max(mS, V(vMax), warp, lane), upS, dnS);
+  pow2_up_dn(cta_max(mD, V(vMax), warp, lane), upD, dnD);
+  {
+    // <S, dS'> over the whole 128 x 128 state (fixed order: warp sums, then warps in order)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if (lane == 0) V(vDot)[warp] = dot;
+  }
+  // v, dO -> fp16 scaled, in place; S, dS' -> fp16 scaled tiles [key][value]
+  for (int idx = tid; idx < 1024; idx += kLT) {
+    const int row = idx >> 4, ch = idx & 15;
+    uint4* pv = reinterpret_cast<uint4*>(tV + row * kLd * 2 + ch * 16);
+    uint4* po = reinterpret_cast<uint4*>(tO + row * kLd * 2 + ch * 16);
+    const uint4 wv = *pv, wo = *po;
+    *pv = make_uint4(bf16x2_to_f16x2_scaled(wv.x, dnV), bf16x2_to_f16x2_scaled(wv.y, dnV),
+                     bf16x2_to_f16x2_scaled(wv.z, dnV), bf16x2_to_f16x2_scaled(wv.w, dnV));
+    *po = make_uint4(bf16x2_to_f16x2_scaled(wo.x, dnO), bf16x2_to_f16x2_scaled(wo.y, dnO),
+                     bf16x2_to_f16x2_scaled(wo.z, dnO), bf16x2_to_f16x2_scaled(wo.w, dnO));
+  }
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const int e = 4 * (tid + 256 * m), row = e >> 7, col = e & 127;
+    __half* ps = reinterpret_cast<__half*>(tS) + row * kLd + col;
+    __half* pd = reinterpret_cast<__half*>(tD) + row * kLd + col;
+    *reinterpret_cast<__half2*>(ps) = __floats2half2_rn(s4[m].x * dnS, s4[m].y * dnS);
+    *reinterpret_cast<__half2*>(ps + 2) = __floats2half2_rn(s4[m].z * dnS, s4[m].w * dnS);
+    *reinterpret_cast<__half2*>(pd) = __floats2half2_rn(d4[m].x * dnD, d4[m].y * dnD);
+    *reinterpret_cast<__half2*>(pd + 2) = __floats2half2_rn(d4[m].z * dnD, d4[m].w * dnD);
+  }
+  __syncthreads();
+
+  // per-thread partial sums: rows (this warp's column half, unshuffled) and columns of the 64 x 64
+  // products (this thread's two rows)
+  float rg[2] = {0.f, 0.f}, rb[2] = {0.f, 0.f}, rd[2] = {0.f, 0.f}, cg[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) cg[i] = 0.f;
+  const float* gam2 = V(vG2);
+  const float* Gam = V(vGam);
+  const float* ev = V(vE);
+  const float* bet = V(vBet);
+  auto Eij = [&](int i, int j) { return exp2f(gam2[i] - gam2[j]); };   // j <= i only
+
+  // ---- 1. Gram products from the raw bf16 rows: A (fp32), K^ K^T and P (fp16) ----
+  {
+    float G[4][4], Gq[4][4];
+    zero(G);
+    zero(Gq);
+    tile_mma<4, false, true, true>(G, tK, kLd, m0, tK, kLd, n64, 128, lane);
+    tile_mma<4, false, true, true>(Gq, tQ, kLd, m0, tK, kLd, n64, 128, lane);
+    const float* sq = V(vSq);
+    const float* sk = V(vSk);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = frow(m0, lane, e), j = fcol(n64, lane, nt, e);
+        const float kk = sk[i] * sk[j] * G[nt][e];
+        const float E = j <= i ? Eij(i, j) : 0.f;
+        Af[i * kLf + j] = j < i ? bet[i] * kk * E : 0.f;
+        reinterpret_cast<__half*>(tG)[i * kLs + j] = __float2half_rn(kk);
+        reinterpret_cast<__half*>(tP)[i * kLs + j] = __float2half_rn(kQs * sq[i] * sk[j] * Gq[nt][e] * E);
+      }
+  }
+  __syncthreads();
+  // raw rows -> fp16 unit rows q^ = q / |q|, k^ = k / |k| (q~ = q^ 128^-0.5)
+  for (int idx = tid; idx < 2 * 1024; idx += kLT) {
+    const int which = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
+    uint4* p = reinterpret_cast<uint4*>((which ? tK : tQ) + row * kLd * 2 + ch * 16);
+    const float s = V(which ? vSk : vSq)[row];
+    const uint4 w = *p;
+    *p = make_uint4(bf16x2_to_f16x2_scaled(w.x, s), bf16x2_to_f16x2_scaled(w.y, s),
+                    bf16x2_to_f16x2_scaled(w.z, s), bf16x2_to_f16x2_scaled(w.w, s));
+  }
+  __syncthreads();
+
+  // ---- 2. T = (I + A)^-1 (threads 0-63: column j by forward substitution); meanwhile the operand
+  //         diag(beta Gamma) K^ ----
+  if (tid < 64) {
+    const int j = tid;
+    float x[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) x[i] = (i == j) ? 1.f : 0.f;
+#pragma unroll
+    for (int i = 1; i < 64; ++i) {
+      const float* arow = Af + i * kLf;
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int m = 0; m < i; m += 2) {
+        s0 = fmaf(arow[m], x[m], s0);
+        if (m + 1 < i) s1 = fmaf(arow[m + 1], x[m + 1], s1);
+      }
+      if (i > j) x[i] = -(s0 + s1);
+    }
+#pragma unroll
+    for (int i = 0; i < 64; ++i) reinterpret_cast<__half*>(tT)[i * kLs + j] = __float2half_rn(x[i]);
+  } else {
+    for (int idx = tid - 64; idx < 64 * 64; idx += kLT - 64) {
+      const int row = idx >> 6, c2 = idx & 63;
+      const float s = bet[row] * Gam[row];
+      __half2* p = reinterpret_cast<__half2*>(tK + row * kLd * 2) + c2;
+      const float2 f = __half22float2(*p);
+      reinterpret_cast<__half2*>(tX1 + row * kLd * 2)[c2] = __floats2half2_rn(f.x * s, f.y * s);
+    }
+  }
+  __syncthreads();
+
+  // ---- 3. W = T diag(beta Gamma) K^, U = T diag(beta) V, Delta = U - W S ----
+  float acc[8][4], acc2[8][4];
+  zero(acc);
+  tile_mma<8, false, false>(acc, tT, kLs, m0, tX1, kLd, n128, 64, lane);   // W
+  store_h(tX2, kLd, m0, n128, acc, 1.f, lane);
+  __syncthreads();
+  for (int idx = tid; idx < 64 * 64; idx += kLT) {
+    const int row = idx >> 6, c2 = idx & 63;
+    const float2 f = __half22float2(reinterpret_cast<const __half2*>(tV + row * kLd * 2)[c2]);
+    reinterpret_cast<__half2*>(tX1 + row * kLd * 2)[c2] = __floats2half2_rn(f.x * bet[row], f.y * bet[row]);
+  }
+  __syncthreads();
+  zero(acc);
+  tile_mma<8, false, false>(acc, tT, kLs, m0, tX1, kLd, n128, 64, lane);    // U / 2^eV
+  zero(acc2);
+  tile_mma<8, false, false>(acc2, tX2, kLd, m0, tS, kLd, n128, 128, lane);  // W S / 2^eS
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = upV * acc[nt][e] - upS * acc2[nt][e];   // Delta
+  float upDl, dnDl;
+  pow2_up_dn(cta_max(absmax(acc), V(vMax), warp, lane), upDl, dnDl);   // (its barriers: X1 is free)
+  store_h(tX1, kLd, m0, n128, acc, dnDl, lane);                         // Delta / 2^eDl
+  __syncthreads();
+
+  // ---- 4. dDelta = P^T dO + diag(e) K^ dS'; the rows e_i k^_i . (dS' Delta_i) ----
+  zero(acc);
+  tile_mma<8, true, false>(acc, tP, kLs, m0, tO, kLd, n128, 64, lane);     // P^T dO / 2^eO
+  zero(acc2);
+  tile_mma<8, false, false>(acc2, tK, kLd, m0, tD, kLd, n128, 128, lane);  // K^ dS' / 2^eD
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = frow(m0, lane, e), col = fcol(n128, lane, nt, e);
+      const float kd = upD * acc2[nt][e];
+      rd[e >> 1] += ev[i] * kd * (upDl * h2f(tX1, kLd, i, col));
+      acc[nt][e] = upO * acc[nt][e] + ev[i] * kd;
+    }
+  float updD, dndD;
+  pow2_up_dn(cta_max(absmax(acc), V(vMax), warp, lane), updD, dndD);
+  store_h(tX2, kLd, m0, n128, acc, dndD, lane);                          // dDelta / 2^edD (W is spent)
+
+  // ---- 5. dK^ = diag(e) Delta dS'^T (the first of its terms) ----
+  float dK[8][4], dQ[8][4];
+  zero(dK);
+  tile_mma<8, false, true>(dK, tX1, kLd, m0, tD, kLd, n128, 128, lane);
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dK[nt][e] *= ev[frow(m0, lane, e)] * upDl * upD;
+  __syncthreads();   // dDelta is stored; dS' is read by every warp (its tile is reused below)
+
+  // ---- 6. dW = -dDelta S^T; dQ~ = diag(Gamma) dO S^T; the rows Gamma_i q~_i . (dO S^T)_i ----
+  zero(acc);
+  tile_mma<8, false, true>(acc, tX2, kLd, m0, tS, kLd, n128, 128, lane);
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] *= -updD * upS;
+  float updW, dndW;
+  pow2_up_dn(cta_max(absmax(acc), V(vMax), warp, lane), updW, dndW);
+  uint8_t* tdW = tD;   // dS' is spent
+  store_h(tdW, kLd, m0, n128, acc, dndW, lane);
+  zero(dQ);
+  tile_mma<8, false, true>(dQ, tO, kLd, m0, tS, kLd, n128, 128, lane);
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = frow(m0, lane, e), col = fcol(n128, lane, nt, e);
+      const float x = upO * upS * dQ[nt][e];
+      rg[e >> 1] += Gam[i] * kQs * h2f(tQ, kLd, i, col) * x;
+      dQ[nt][e] = Gam[i] * x;
+    }
+  __syncthreads();   // S is spent (its tile holds dPE, dT and Z below)
+
+  // ---- 7. dP = dO Delta^T (j <= i); dQ~ += (dP o E) K^, dK^ += (dP o E)^T q~ ----
+  uint8_t* tPE = tS;
+  uint8_t* tdT = tS + kT64;
+  uint8_t* tZ = tS + 2 * kT64;
+  uint8_t* tdA = tD + kT128;
+  {
+    float dp[4][4];
+    zero(dp);
+    tile_mma<4, false, true>(dp, tO, kLd, m0, tX1, kLd, n64, 128, lane);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = frow(m0, lane, e), j = fcol(n64, lane, nt, e);
+        const float d = j <= i ? upO * upDl * dp[nt][e] : 0.f;
+        const float pp = d * h2f(tP, kLs, i, j);
+        rg[e >> 1] += pp;
+        cg[2 * nt + (e & 1)] -= pp;
+        dp[nt][e] = j <= i ? d * Eij(i, j) : 0.f;
+      }
+    float up, dn;
+    pow2_up_dn(cta_max(absmax(dp), V(vMax), warp, lane), up, dn);
+    store_h(tPE, kLs, m0, n64, dp, dn, lane);
+    __syncthreads();
+    float t2[8][4];
+    zero(t2);
+    tile_mma<8, false, false>(t2, tPE, kLs, m0, tK, kLd, n128, 64, lane);
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dQ[nt][e] += up * t2[nt][e];
+    zero(t2);
+    tile_mma<8, true, false>(t2, tPE, kLs, m0, tQ, kLd, n128, 64, lane);
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dK[nt][e] += up * kQs * t2[nt][e];
+  }
+
+  // ---- 8. T^T dDelta -> dV, dbeta; T^T dW -> dK^, dbeta, dgamma ----
+  zero(acc);
+  tile_mma<8, true, false>(acc, tT, kLs, m0, tX2, kLd, n128, 64, lane);
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int i = frow(m0, lane, 2 * hh), col = fcol(n128, lane, nt, 0);
+      const float x0 = updD * acc[nt][2 * hh], x1 = updD * acc[nt][2 * hh + 1];
+      rb[hh] += upV * (x0 * h2f(tV, kLd, i, col) + x1 * h2f(tV, kLd, i, col + 1));
+      if (p0 + i < a.L)
+        *reinterpret_cast<float2*>(a.dv + (((size_t)b * a.L + p0 + i) * a.Hv + h) * kD + col) =
+            make_float2(bet[i] * x0, bet[i] * x1);
+    }
+  zero(acc);
+  tile_mma<8, true, false>(acc, tT, kLs, m0, tdW, kLd, n128, 64, lane);
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = frow(m0, lane, e), col = fcol(n128, lane, nt, e);
+      const float x = updW * acc[nt][e];
+      const float r = x * h2f(tK, kLd, i, col);
+      rb[e >> 1] += Gam[i] * r;
+      rg[e >> 1] += bet[i] * Gam[i] * r;
+      dK[nt][e] += bet[i] * Gam[i] * x;
+    }
+
+  // ---- 9. dT = dDelta (beta V)^T + dW (beta Gamma K^)^T; dA = -T^T dT T^T (j < i) ----
+  {
+    float t1[4][4], t2[4][4];
+    zero(t1);
+    tile_mma<4, false, true>(t1, tX2, kLd, m0, tV, kLd, n64, 128, lane);
+    zero(t2);
+    tile_mma<4, false, true>(t2, tdW, kLd, m0, tK, kLd, n64, 128, lane);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = fcol(n64, lane, nt, e);
+        t1[nt][e] = bet[j] * (updD * upV * t1[nt][e] + Gam[j] * updW * t2[nt][e]);
+      }
+    float upT, dnT;
+    pow2_up_dn(cta_max(absmax(t1), V(vMax), warp, lane), upT, dnT);
+    store_h(tdT, kLs, m0, n64, t1, dnT, lane);
+    __syncthreads();
+    zero(t2);
+    tile_mma<4, false, true>(t2, tdT, kLs, m0, tT, kLs, n64, 64, lane);   // dT T^T
+    float upZ, dnZ;
+    pow2_up_dn(cta_max(absmax(t2), V(vMax), warp, lane), upZ, dnZ);
+    store_h(tZ, kLs, m0, n64, t2, dnZ, lane);
+    __syncthreads();
+    zero(t1);
+    tile_mma<4, true, false>(t1, tT, kLs, m0, tZ, kLs, n64, 64, lane);    // T^T (dT T^T)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = frow(m0, lane, e), j = fcol(n64, lane, nt, e);
+        float dAt = 0.f;   // dA~ = dA beta_i E_ij
+        if (j < i) {
+          const float dA = -upT * upZ * t1[nt][e];
+          const float E = Eij(i, j), gk = h2f(tG, kLs, i, j);   // k^_i . k^_j
+          rb[e >> 1] += dA * gk * E;
+          const float aa = dA * bet[i] * gk * E;                  // dA o A
+          rg[e >> 1] += aa;
+          cg[2 * nt + (e & 1)] -= aa;
+          dAt = dA * bet[i] * E;
+        }
+        t1[nt][e] = dAt;
+      }
+    float upA, dnA;
+    pow2_up_dn(cta_max(absmax(t1), V(vMax), warp, lane), upA, dnA);
+    store_h(tdA, kLs, m0, n64, t1, dnA, lane);
+    __syncthreads();
+    float t3[8][4];
+    zero(t3);
+    tile_mma<8, false, false>(t3, tdA, kLs, m0, tK, kLd, n128, 64, lane);
+    tile_mma<8, true, false>(t3, tdA, kLs, m0, tK, kLd, n128, 64, lane);
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dK[nt][e] += upA * t3[nt][e];
+  }
+
+  // ---- 10. reductions: dgamma -> dg, dbeta; outputs ----
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      rg[hh] += __shfl_xor_sync(0xffffffffu, rg[hh], o);
+      rb[hh] += __shfl_xor_sync(0xffffffffu, rb[hh], o);
+      rd[hh] += __shfl_xor_sync(0xffffffffu, rd[hh], o);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) cg[i] += __shfl_xor_sync(0xffffffffu, cg[i], o);
+  if ((lane & 3) == 0) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int i = m0 + (lane >> 2) + 8 * hh;
+      V(vRowG0 + half)[i] = rg[hh];
+      V(vRowB0 + half)[i] = rb[hh];
+      V(vRowD0 + half)[i] = rd[hh];
+    }
+  }
+  if (lane < 4) {
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int x = 0; x < 2; ++x) V(vColG0 + (warp & 3))[n64 + 8 * nt + 2 * lane + x] = cg[2 * nt + x];
+  }
+  __syncthreads();
+  if (warp == 0 || warp == 1) {
+    // dgamma_i, then dg_j = sum_{i >= j} dgamma_i (a reversed inclusive scan over two warps)
+    const int i = 63 - tid;   // warp 0: positions 63..32, warp 1: 31..0
+    const float de = V(vRowD0)[i] + V(vRowD1)[i];
+    float dga = V(vRowG0)[i] + V(vRowG1)[i] + V(vColG0)[i] + V(vColG1)[i] + V(vColG2)[i] + V(vColG3)[i] - de;
+    if (i == 63) {
+      float tot_de = 0.f, dotS = 0.f;
+      for (int r = 0; r < 64; ++r) tot_de += V(vRowD0)[r] + V(vRowD1)[r];
+      for (int w = 0; w < kLT / 32; ++w) dotS += V(vDot)[w];
+      dga += Gam[63] * dotS + tot_de;
+    }
+    float x = dga;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    V(vScan)[tid] = x;
+  }
+  __syncthreads();
+  if (tid < 64) {
+    const int i = 63 - tid;
+    const float dgi = V(vScan)[tid] + (tid >= 32 ? V(vScan)[31] : 0.f);
+    if (p0 + i < a.L) {
+      const size_t gi = ((size_t)b * a.L + p0 + i) * a.Hv + h;
+      a.dg[gi] = dgi;
+      a.dbeta[gi] = V(vRowB0)[i] + V(vRowB1)[i];
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int i = frow(m0, lane, 2 * hh), col = fcol(n128, lane, nt, 0);
+      if (p0 + i < a.L) {
+        const size_t o = (((size_t)b * a.L + p0 + i) * a.Hv + h) * kD + col;
+        *reinterpret_cast<float2*>(a.dqt + o) = make_float2(dQ[nt][2 * hh], dQ[nt][2 * hh + 1]);
+        *reinterpret_cast<float2*>(a.dkh + o) = make_float2(dK[nt][2 * hh], dK[nt][2 * hh + 1]);
+      }
+    }
+}
+
+// One (row, position, key head) per CTA, one key dimension per thread: the sums over the value
+// heads of the key head, then the normalisations' backward (q~ = q s_q 128^-0.5, k^ = k s_k).
+__global__ void __launch_bounds__(kD) chunk_bwd_reduce_kernel(const LocalArgs a, float* dq, float* dk) {
+  __shared__ float red[4][4];
+  const size_t bt = blockIdx.x;   // b L + position
+  const int hk = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = a.Hv / a.Hk;
+  float dqt = 0.f, dkh = 0.f;
+  for (int j = 0; j < r; ++j) {
+    const size_t o = (bt * a.Hv + (size_t)hk * r + j) * kD + tid;
+    dqt += a.dqt[o];
+    dkh += a.dkh[o];
+  }
+  const size_t off = (bt * a.Hk + hk) * kD + tid;
+  const float qv = __bfloat162float(a.q[off]), kv = __bfloat162float(a.k[off]);
+  float s[4] = {qv * qv, qv * dqt, kv * kv, kv * dkh};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s[j] += __shfl_xor_sync(0xffffffffu, s[j], o);
+    if (lane == 0) red[warp][j] = s[j];
+  }
+  __syncthreads();
+  float tot[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) tot[j] = red[0][j] + red[1][j] + red[2][j] + red[3][j];
+  const float sq = rsqrtf(tot[0] + 1e-6f), sk = rsqrtf(tot[2] + 1e-6f);
+  dq[off] = kQs * (sq * dqt - sq * sq * sq * tot[1] * qv);
+  dk[off] = sk * dkh - sk * sk * sk * tot[3] * kv;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t chunk_bwd_workspace_bytes(int B, int L, int Hk, int Hv) {
+  (void)Hk;
+  const size_t NC = ((size_t)L + kChunk - 1) / kChunk;
+  const size_t states = (size_t)B * Hv * NC * kD * kD * sizeof(float);
+  const size_t parts = (size_t)B * L * Hv * kD * sizeof(float);
+  return align256(chunk_bwd_units_bytes(B, L, Hv)) + 2 * align256(states) + 2 * align256(parts);
+}
+
+cudaError_t launch_chunk_backward(const ChunkBackwardArgs& p, cudaStream_t s) {
+  const size_t NC = ((size_t)p.L + kChunk - 1) / kChunk;
+  const size_t states = (size_t)p.B * p.Hv * NC * kD * kD * sizeof(float);
+  const size_t parts = (size_t)p.B * p.L * p.Hv * kD * sizeof(float);
+  uint8_t* w = static_cast<uint8_t*>(p.ws);
+  uint8_t* units = w;
+  float* S_save = reinterpret_cast<float*>(w + align256(chunk_bwd_units_bytes(p.B, p.L, p.Hv)));
+  float* dS_save = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(S_save) + align256(states));
+  float* dqt = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dS_save) + align256(states));
+  float* dkh = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dqt) + align256(parts));
+  ChunkBwdChainLaunch cl{p.q, p.k, p.v, p.g, p.beta, p.S0, p.dO, p.dS_T, p.dS0, S_save, dS_save, units,
+                         p.B, p.L, p.Hk, p.Hv, p.err};
+  cudaError_t e = launch_chunk_bwd_chain(cl, s);
+  if (e != cudaSuccess) return e;
+  LocalArgs la{static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k),
+               static_cast<const __nv_bfloat16*>(p.v), p.g, p.beta, static_cast<const __nv_bfloat16*>(p.dO),
+               S_save, dS_save, dqt, dkh, p.dv, p.dg, p.dbeta, p.B, p.L, p.Hk, p.Hv, (int)NC};
+  e = cudaFuncSetAttribute(chunk_bwd_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalSmem + 128);
+  if (e != cudaSuccess) return e;
+  int slot = stage_timer_begin(s, kKernChunkBwdLocal);
+  chunk_bwd_local_kernel<<<(unsigned)((size_t)p.B * p.Hv * NC), kLT, kLocalSmem + 128, s>>>(la);
+  stage_timer_end(slot, s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  slot = stage_timer_begin(s, kKernChunkBwdReduce);
+  chunk_bwd_reduce_kernel<<<dim3((unsigned)((size_t)p.B * p.L), (unsigned)p.Hk), kD, 0, s>>>(la, p.dq, p.dk);
+  stage_timer_end(slot, s);
+  return cudaGetLastError();
+}
+
+}  // namespace gdr

@@ -397,6 +397,10 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
+// bf16x2 word -> fp16x2 word of the values times s (a power of two)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float s) {
+  return pack_f16x2(__uint_as_float(w << 16) * s, __uint_as_float(w & 0xFFFF0000u) * s);
+}
 // Warp-level tensor-core product for small fp32 tiles kept at fp32 accuracy: each operand x is split
 // into hi = x with its 13 low mantissa bits cleared (a tf32 value) and lo = x - hi (exact in fp32;
 // the product reads its tf32 part), and D += A B is formed as lo*hi + hi*lo + hi*hi (the dropped

@@ -25,6 +25,7 @@ EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_varlen",
            "gdr_fork_workspace_bytes",
            "gdr_fork_fwd", "gdr_decode_step", "gdr_prologue", "gdr_gated_rmsnorm",
            "gdr_backward_workspace_bytes", "gdr_backward",
+           "gdr_backward_chunked_workspace_bytes", "gdr_backward_chunked",
            "gdr_sync_status", "gdr_status_string", "gdr_last_error_message",
            "gdr_stage_timer_enable", "gdr_stage_timer_collect", "gdr_kernel_name", "gdr_debug_set_wait_budget"]
 
@@ -72,6 +73,11 @@ def lib() -> ctypes.CDLL:
     L.gdr_backward_workspace_bytes.restype = sz
     L.gdr_backward.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp, sz, vp]
     L.gdr_backward.restype = i
+    L.gdr_backward_chunked_workspace_bytes.argtypes = [i, i, i, i, i]
+    L.gdr_backward_chunked_workspace_bytes.restype = sz
+    L.gdr_backward_chunked.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp, sz,
+                                       vp]
+    L.gdr_backward_chunked.restype = i
     L.gdr_sync_status.argtypes = [vp]
     L.gdr_sync_status.restype = i
     L.gdr_status_string.argtypes = [i]
@@ -314,6 +320,38 @@ def gdr_backward(q, k, v, g, beta, S0, dO, dS_T=None, ws=None, stream=None, want
     _check(lib().gdr_backward(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(dO), _p(dS_T), _p(dq), _p(dk),
                               _p(dv), _p(dg), _p(dbeta), _p(dS0), B, L, Hk, Hv, Dk, dt, _p(ws), ws_bytes,
                               _stream(stream)))
+    return dq, dk, dv, dg, dbeta, dS0
+
+
+def backward_chunked_workspace_bytes(B: int, L: int, Hk: int, Hv: int, D: int = 128) -> int:
+    return int(lib().gdr_backward_chunked_workspace_bytes(B, L, Hk, Hv, D))
+
+
+def gdr_backward_chunked(q, k, v, g, beta, S0, dO, dS_T=None, ws=None, stream=None, want_dS0: bool = True):
+    """gdr_backward's gradients for bf16 q, k, v, dO, computed chunk by chunk on the tensor cores
+    (bf16-path accuracy); same arguments and results."""
+    B, L, Hk, Hv, Dk = _check_inputs(q, k, v, g, beta)
+    _need(q.dtype == torch.bfloat16, "gdr_backward_chunked takes bf16 q, k, v, dO (float32: gdr_backward)")
+    _need(isinstance(dO, torch.Tensor) and dO.is_cuda and dO.is_contiguous() and dO.dtype == q.dtype
+          and dO.shape == v.shape, "dO must be a contiguous CUDA tensor of v's shape and q's dtype")
+    for name, t in (("S0", S0), ("dS_T", dS_T)):
+        if t is not None:
+            _need(t.dtype == torch.float32 and t.is_contiguous() and t.is_cuda and t.shape == (B, Hv, Dk, v.shape[3]),
+                  f"{name} must be contiguous CUDA float32 [B, Hv, D, D]")
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq = torch.empty(q.shape, **f32)
+    dk = torch.empty(k.shape, **f32)
+    dv = torch.empty(v.shape, **f32)
+    dg = torch.empty(g.shape, **f32)
+    dbeta = torch.empty(beta.shape, **f32)
+    dS0 = torch.empty(B, Hv, Dk, v.shape[3], **f32) if want_dS0 else None
+    need = backward_chunked_workspace_bytes(B, L, Hk, Hv, Dk)
+    if ws is None:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    ws_bytes = ws.numel() * ws.element_size()
+    _check(lib().gdr_backward_chunked(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(dO), _p(dS_T), _p(dq),
+                                      _p(dk), _p(dv), _p(dg), _p(dbeta), _p(dS0), B, L, Hk, Hv, Dk, _dtype_code(q),
+                                      _p(ws), ws_bytes, _stream(stream)))
     return dq, dk, dv, dg, dbeta, dS0
 
 

@@ -251,6 +251,28 @@ gdr_status gdr_backward(const void* q, const void* k, const void* v, const float
                         float* dv, float* dg, float* dbeta, float* dS0, int B, int L, int Hk, int Hv,
                         int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream);
 
+/*
+ * gdr_backward_chunked: the same gradients as gdr_backward for bf16 q, k, v, dO, computed chunk by
+ * chunk on the tensor cores. The pages print no backward; this is the reverse of the chunked
+ * forward (the chunk algebra of gdr_chunk_fwd, 64-token chunks): the sequential part is the
+ * adjoint chain, the forward chain transposed,
+ *   dS_c = Gamma_C dS_{c+1} + M'^T dS_{c+1} + Q'^T dO_c    (dS_NC = dS_T, dS0 = dS_0),
+ * and the rest is local to each chunk once its entering state S_c and dS_{c+1} are known (the
+ * gradients through Delta = U - W S, P, T = (I + A)^-1, the decays and the normalisations).
+ * Arguments, shapes, ownership and the no-overlap rule as for gdr_backward; dt must be GDR_BF16
+ * (GDR_ERR_UNSUPPORTED otherwise). ws holds at least gdr_backward_chunked_workspace_bytes(...)
+ * bytes: the forward's per-chunk factors, the chunk-entry states and adjoints (float32, 64 KiB
+ * per row, value head and chunk each) and the per-value-head gradients of q~ and k^. The products
+ * take fp16 (bf16 for the raw q, k Gram products) operands with float32 accumulation, like the
+ * bf16 forward, so the result matches the float64 backward to the bf16 path's tolerance, not
+ * gdr_backward's float32 one; the sums run in a fixed order (deterministic).
+ */
+size_t gdr_backward_chunked_workspace_bytes(int B, int L, int Hk, int Hv, int D);
+gdr_status gdr_backward_chunked(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                const float* S0, const void* dO, const float* dS_T, float* dq, float* dk,
+                                float* dv, float* dg, float* dbeta, float* dS0, int B, int L, int Hk, int Hv,
+                                int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream);
+
 /* Synchronise `stream`, then read and clear the sticky device error word of the current device. */
 gdr_status gdr_sync_status(gdr_stream_t stream);
 

@@ -238,3 +238,26 @@ def test_varlen_and_gated_reject_bad_arguments(L):
     assert f(P, P, P, P, P, None, Z, P, 1e-6, ctypes.c_void_p((1 << 32) + 4096), None, B, Lt, Hk, Hv, 128, 1, None, 0,
              None) == gdr.GDR_ERR_INVALID_ARG
     assert b"overlaps" in L.gdr_last_error_message()
+
+
+def test_chunked_backward_rejects_bad_arguments_and_sizes_its_workspace(L):
+    """gdr_backward_chunked: bf16 only, the backward's host checks, and a workspace of the forward's
+    chunk factors plus float32 chunk-entry states and adjoints and the per-value-head q~, k^
+    gradients."""
+    f = L.gdr_backward_chunked
+    need = L.gdr_backward_chunked_workspace_bytes(1, 64, 2, 4, 128)
+    args = lambda dt=1, dO=P, ws_bytes=need, dq=P: (P, P, P, P, P, None, dO, None, dq, P, P, P, P, None, 1, 64, 2,
+                                                     4, 128, dt, P, ws_bytes, None)
+    assert f(*args(dt=0)) == gdr.GDR_ERR_UNSUPPORTED
+    assert b"bf16" in L.gdr_last_error_message()
+    assert f(*args(dO=None)) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(dq=None)) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(ws_bytes=need - 1)) == gdr.GDR_ERR_INVALID_ARG
+    assert b"workspace" in L.gdr_last_error_message()
+    assert L.gdr_backward_chunked_workspace_bytes(1, 64, 3, 4, 128) == 0
+    for B, Lt, Hv in ((1, 64, 4), (2, 130, 8), (1, 4096, 32)):
+        NC = -(-Lt // 64)
+        units = B * Hv * NC * 98816 + 1024
+        a256 = lambda x: -(-x // 256) * 256
+        want = a256(units) + 2 * a256(B * Hv * NC * 128 * 128 * 4) + 2 * a256(B * Lt * Hv * 128 * 4)
+        assert L.gdr_backward_chunked_workspace_bytes(B, Lt, 2, Hv, 128) == want
