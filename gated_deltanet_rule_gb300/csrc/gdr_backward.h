@@ -1,6 +1,7 @@
 // Internal declarations of the backward (not part of the ABI).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "gdr_epilogue.h"
@@ -48,7 +49,8 @@ cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
 // The chunked backward's sequential passes over bf16 rows (any L >= 1): the forward's chunk factors
 // (prep kernel, into ws), the chunk-entry states (state kernel, mode 1: S_save), Nb = Q'^T dO over
 // the spent N slots, and the adjoint chain (state kernel, mode 2: dS0 and, per chunk, the adjoint
-// of its exiting state, dS_save). S_save and dS_save are float32 [B, Hv, NC, D, D]; ws holds
+// of its exiting state, dS_save). S_save and dS_save are fp16 [B, Hv, NC, D, D], each 32-column slice
+// of a state divided by the power of two in S_scale / dS_scale [B, Hv, NC, 4]; ws holds
 // chunk_bwd_units_bytes(B, L, Hv) bytes. dS_T may be NULL (zeros), dS0 NULL (not written).
 struct ChunkBwdChainLaunch {
   const void* q;
@@ -60,8 +62,10 @@ struct ChunkBwdChainLaunch {
   const void* dO;
   const float* dS_T;
   float* dS0;
-  float* S_save;
-  float* dS_save;
+  __half* S_save;
+  float* S_scale;
+  __half* dS_save;
+  float* dS_scale;
   void* ws;
   int B, L, Hk, Hv;
   int* err;

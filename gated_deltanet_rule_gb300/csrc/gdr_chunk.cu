@@ -45,6 +45,7 @@
 
 #include "gdr_epilogue.h"
 #include "gdr_backward.h"
+#include "gdr_inverse.cuh"
 #include "gdr_internal.h"
 #include "ptx.cuh"
 
@@ -90,10 +91,12 @@ struct ChunkArgs {
   const __nv_bfloat16* z;
   const float* w;
   float eps;
-  // state kernel modes 1 and 2 (the backward's passes): the state at the top of each chunk's step,
-  // float32 [B, Hv, NC, D, D] (mode 1: the chunk's entering state; mode 2: the adjoint of its
-  // exiting state)
-  float* st_save;
+  // state kernel modes 1 and 2 (the backward's passes): the state at the top of each chunk's step
+  // (mode 1: the chunk's entering state; mode 2: the adjoint of its exiting state) as the fp16
+  // operand the step's product reads, [B, Hv, NC, D, D] with key rows and value columns, each 32-
+  // column slice divided by its own power of two, kept in st_scale [B, Hv, NC, 4]
+  __half* st_save;
+  float* st_scale;
 };
 
 __device__ __forceinline__ uint8_t* unit_base(const ChunkArgs& a, int b, int h, int c) {
@@ -161,163 +164,6 @@ static_assert(kPP + 16384 <= kPrepSmem - 1024 && kPAop + 16384 <= kPVec, "M = 12
 static_assert(kPWS % 1024 == 0 && kPWS + 32768 <= kPVec, "the [sk W | sk U] operand fits over AT and T");
 static_assert(kPVt == kPK1 + 16384 && kPXs + 36 * 32 * 4 <= kPVt + 16384 && kPVt + 16384 + 8192 <= kPP,
               "v atoms continue the k atoms' stride; the inverse scratch fits between them");
-
-// T = (I + A)^-1 for the strictly lower 64 x 64 A in AT (row stride 68, 1 on the diagonal), by
-// recursive doubling: 16 x 16 diagonal blocks by forward substitution, then the merges
-// T_BL = -T_BR (A_BL T_TL) for the 16-blocks (1,0), (3,2) and for the 32-block (1,0). T is written
-// twice: transposed into AT's strictly upper part (T(i, j) = AT[j][i], a column of T is a row of
-// AT) and row-major into Tm, whose diagonal is 1 and upper part 0 on entry. Entries of A are
-// zeroed once consumed, so that a row of AT restricted to a finished diagonal block is exactly a
-// column of T. Block products read rows of the left factor and columns of the right factor as
-// contiguous float4 runs, and skip the blocks that are zero by triangularity.
-__device__ void invert_unit_lower(float* AT, float* Tm, float* Xs, uint8_t* sm, int tid, float dnK) {
-  const int warp = tid >> 5, lane = tid & 31;
-  // 1. diagonal 16-blocks (warps 0, 1): thread = (block, column c), computing column c of the
-  //    block's inverse in registers, left-looking: x_i = -sum_{j < i} A_ij x_j for rows i > c (x_c = 1,
-  //    x_j = 0 above it). Each row of A is read as four float4 broadcasts; no shuffles.
-  if (warp < 2) {
-    const int r0 = (tid >> 4) * 16, c = tid & 15;
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (i == c) ? 1.f : 0.f;
-#pragma unroll
-    for (int i = 1; i < 16; ++i) {
-      const float4* arow = reinterpret_cast<const float4*>(AT + (r0 + i) * 68 + r0);
-      float av[16];
-#pragma unroll
-      for (int m4 = 0; m4 < 4; ++m4) {
-        if (4 * m4 < i) {
-          const float4 t = arow[m4];
-          av[4 * m4] = t.x; av[4 * m4 + 1] = t.y; av[4 * m4 + 2] = t.z; av[4 * m4 + 3] = t.w;
-        }
-      }
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int j = 0; j < i; ++j) {
-        if (j & 1) s1 = fmaf(av[j], x[j], s1);
-        else s0 = fmaf(av[j], x[j], s0);
-      }
-      x[i] = (i > c) ? -(s0 + s1) : x[i];
-    }
-    __syncwarp();   // every lane of the block has read A's rows before row c of AT is overwritten
-    // column c of T: Tm rows below the diagonal (its diagonal 1 and upper zeros are in place), and
-    // AT row c over the block's columns: 0 above the diagonal of T (the consumed A), 1 on it, T below
-#pragma unroll
-    for (int i = 1; i < 16; ++i)
-      if (i > c) Tm[(r0 + i) * 68 + r0 + c] = x[i];
-    float4* trow = reinterpret_cast<float4*>(AT + (r0 + c) * 68 + r0);
-#pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4)
-      trow[m4] = make_float4(x[4 * m4], x[4 * m4 + 1], x[4 * m4 + 2], x[4 * m4 + 3]);
-  } else {
-    // warps 2-7 meanwhile: the k tile to fp16 in place, for the fp16 products (the Gram MMA that
-    // read k as bf16 has completed); 1024 chunks of 16 B, times dnK (1 unless k needs scaling).
-    // (v was converted, times its own power of two, while the Gram product ran.)
-    for (int chunk16 = tid - 64; chunk16 < 1024; chunk16 += kPrepThreads - 64) {
-      const int which = chunk16 >> 9, off = (chunk16 & 511) * 16;
-      const uint32_t base = which == 0 ? kPK0 : kPK1;
-      const float sc = dnK;
-      uint4* p = reinterpret_cast<uint4*>(sm + base + off);
-      uint4 w = *p;
-      if (sc == 1.f)
-        w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
-      else
-        w = make_uint4(bf16x2_to_f16x2_scaled(w.x, sc), bf16x2_to_f16x2_scaled(w.y, sc),
-                       bf16x2_to_f16x2_scaled(w.z, sc), bf16x2_to_f16x2_scaled(w.w, sc));
-      *p = w;
-    }
-  }
-  __syncthreads();
-  // 2. 16-block merges p = 0, 1 (TL = [32p, 32p+16), BR = [32p+16, 32p+32)) with the same warp-level
-  //    products: warp w < 4 forms the 16 x 8 tile (merge p = w >> 1, columns 8 (w & 1)) of
-  //    X = A_BL T_TL (stored transposed, Xs[p][j][i]) and then of T_BL = -T_BR X (into Tm and AT).
-  if (warp < 4) {
-    const int g = lane >> 2, t = lane & 3, p = warp >> 1, n = warp & 1, base = 32 * p;
-    float dh[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      if (kk < n) continue;
-      const float* ar = AT + (base + 16 + g) * 68 + base + 8 * kk + t;   // A_BL(i, k)
-      const float* br = AT + (base + 8 * n + g) * 68 + base + 8 * kk + t;   // T_TL(k, j) = AT[j][k]
-      const float a4[4] = {ar[0], ar[8 * 68], ar[4], ar[8 * 68 + 4]};
-      const float b2[2] = {br[0], br[4]};
-      mma_3xtf32(dh, dc, a4, b2);
-    }
-    const int j0 = 8 * n + 2 * t;
-    Xs[(p * 16 + j0) * 20 + g] = dh[0] + dc[0];
-    Xs[(p * 16 + j0 + 1) * 20 + g] = dh[1] + dc[1];
-    Xs[(p * 16 + j0) * 20 + g + 8] = dh[2] + dc[2];
-    Xs[(p * 16 + j0 + 1) * 20 + g + 8] = dh[3] + dc[3];
-  }
-  __syncthreads();
-  if (warp < 4) {
-    {   // A_BL consumed: a row of AT restricted to a finished 32-block is then exactly a column of T
-      const int p = lane >> 4, i = lane & 15, base = 32 * p;
-      reinterpret_cast<float4*>(AT + (base + 16 + i) * 68 + base)[warp] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    const int g = lane >> 2, t = lane & 3, p = warp >> 1, n = warp & 1, base = 32 * p;
-    float dh[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const float* ar = Tm + (base + 16 + g) * 68 + base + 16 + 8 * kk + t;   // T_BR(i, k), row-major
-      const float* br = Xs + (p * 16 + 8 * n + g) * 20 + 8 * kk + t;         // X(k, j) = Xs[p][j][k]
-      const float a4[4] = {ar[0], ar[8 * 68], ar[4], ar[8 * 68 + 4]};
-      const float b2[2] = {br[0], br[4]};
-      mma_3xtf32(dh, dc, a4, b2);
-    }
-    const int j0 = 8 * n + 2 * t;
-    const float r[4] = {-(dh[0] + dc[0]), -(dh[1] + dc[1]), -(dh[2] + dc[2]), -(dh[3] + dc[3])};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = base + 16 + g + 8 * (e >> 1), j = base + j0 + (e & 1);
-      Tm[i * 68 + j] = r[e];
-      AT[j * 68 + i] = r[e];
-    }
-  }
-  __syncthreads();
-  // 3. 32-block merge on the tensor cores with warp-level products at fp32 accuracy (3xTF32): warp w
-  //    forms the 16 x 8 tile (rows 16 (w & 1), columns 8 (w >> 1)) of X = A_BL T_TL, stored
-  //    transposed (Xs[j][i]), then of T_BL = -T_BR X into AT's upper part. Zero blocks of the
-  //    triangular factors are skipped (T_TL: k-blocks below the column block; T_BR: above the row block).
-  {
-    const int g = lane >> 2, t = lane & 3, m = warp & 1, n = warp >> 1;
-    float dh[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      if (kk < n) continue;
-      const float* ar = AT + (32 + 16 * m + g) * 68 + 8 * kk + t;   // A_BL(i, k) = A(32 + i, k)
-      const float* br = AT + (8 * n + g) * 68 + 8 * kk + t;          // T_TL(k, j) = AT[j][k]
-      const float a4[4] = {ar[0], ar[8 * 68], ar[4], ar[8 * 68 + 4]};
-      const float b2[2] = {br[0], br[4]};
-      mma_3xtf32(dh, dc, a4, b2);
-    }
-    const int i0 = 16 * m + g, j0 = 8 * n + 2 * t;
-    Xs[j0 * 36 + i0] = dh[0] + dc[0];
-    Xs[(j0 + 1) * 36 + i0] = dh[1] + dc[1];
-    Xs[j0 * 36 + i0 + 8] = dh[2] + dc[2];
-    Xs[(j0 + 1) * 36 + i0 + 8] = dh[3] + dc[3];
-  }
-  __syncthreads();
-  {
-    const int g = lane >> 2, t = lane & 3, m = warp & 1, n = warp >> 1;
-    float dh[4] = {0.f, 0.f, 0.f, 0.f}, dc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      if (kk > 2 * m + 1) continue;
-      const float* ar = Tm + (32 + 16 * m + g) * 68 + 32 + 8 * kk + t;   // T_BR(i, k), row-major
-      const float* br = Xs + (8 * n + g) * 36 + 8 * kk + t;              // X(k, j) = Xs[j][k]
-      const float a4[4] = {ar[0], ar[8 * 68], ar[4], ar[8 * 68 + 4]};
-      const float b2[2] = {br[0], br[4]};
-      mma_3xtf32(dh, dc, a4, b2);
-    }
-    const int i0 = 16 * m + g, j0 = 8 * n + 2 * t;   // T(32 + i, j) = AT[j][32 + i]
-    AT[j0 * 68 + 32 + i0] = -(dh[0] + dc[0]);
-    AT[(j0 + 1) * 68 + 32 + i0] = -(dh[1] + dc[1]);
-    AT[j0 * 68 + 32 + i0 + 8] = -(dh[2] + dc[2]);
-    AT[(j0 + 1) * 68 + 32 + i0 + 8] = -(dh[3] + dc[3]);
-  }
-  __syncthreads();
-}
 
 // Persistent: CTA i takes units i, i + gridDim.x, ... in the order value head fastest, then chunks
 // from the last to the first (so the units the state kernel reads first were written last and are
@@ -665,7 +511,23 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   __syncthreads();
 
-  invert_unit_lower(AT, Tm, Xs, sm, tid, unit_scl[1]);
+  invert_unit_lower(AT, Tm, Xs, tid, [&](int t) {
+    // the k tile to fp16 in place, for the fp16 products (the Gram MMA that read k as bf16 has
+    // completed); 1024 chunks of 16 B, times k's scale (1 unless k needs scaling). (v was converted,
+    // times its own power of two, while the Gram product ran.)
+    const float sc = unit_scl[1];
+    for (int chunk16 = t - 64; chunk16 < 1024; chunk16 += kPrepThreads - 64) {
+      const int which = chunk16 >> 9, off = (chunk16 & 511) * 16;
+      uint4* p = reinterpret_cast<uint4*>(sm + (which == 0 ? kPK0 : kPK1) + off);
+      uint4 w = *p;
+      if (sc == 1.f)
+        w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+      else
+        w = make_uint4(bf16x2_to_f16x2_scaled(w.x, sc), bf16x2_to_f16x2_scaled(w.y, sc),
+                       bf16x2_to_f16x2_scaled(w.z, sc), bf16x2_to_f16x2_scaled(w.w, sc));
+      *p = w;
+    }
+  });
 
   // operand [A1; A2] = [T diag(beta Gamma ki); T diag(beta)], MN-major: K-row j holds column j of T
   {
@@ -1029,11 +891,11 @@ constexpr uint32_t state_smem(int cs, int os) { return cs * kCStage + os * kOSta
 static_assert(kCN == kMBytes && kOPU == kQBytes, "stage layout");
 
 // kMode 0: the forward (o and S_T). kMode 1: the forward recomputed for the backward: no output
-// side; the entering state of every chunk is saved to st_save. kMode 2: the backward's adjoint
+// side; the entering state of every chunk is saved (st_save, st_scale). kMode 2: the backward's adjoint
 // chain dS <- Gamma_C dS + M'^T dS + Nb, chunks from the last to the first: the unit's N slot holds
 // Nb = Q'^T dO (in the scale block's second word's scale), the chain product reads the M' image
 // transposed (an MN-major A operand), the initial state is dS_T (a.S0), the final one dS0 (a.S_T),
-// and the adjoint entering each chunk's step (that of its exiting state) is saved to st_save.
+// and the adjoint entering each chunk's step (that of its exiting state) is saved likewise.
 template <int CS, int OS, bool kGated, int kMode>
 __global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const ChunkArgs a) {
@@ -1197,19 +1059,26 @@ chunk_state_kernel(const ChunkArgs a) {
       pow2_scales(__uint_as_float(mall), up, dn);
       return all;
     };
-    // fp16 state operand q: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle
-    auto write_state_operand = [&](int q, float dn) {
+    // fp16 state operand q: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle. Modes 1
+    // and 2 also save it, with its scale up, as the state at the top of step `step` (if < NC).
+    auto write_state_operand = [&](int q, float dn, int step, float up) {
+      const int cu = kMode == 2 ? NC - 1 - step : step;
+      const size_t unit = ((size_t)b * a.Hv + h) * NC + cu;
+      uint4* dst = kMode != 0 ? reinterpret_cast<uint4*>(a.st_save + (unit * kD + kr) * kD + sl * kN) : nullptr;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         float t[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) t[e] = Sm[8 * ch + e] * dn;
-        *reinterpret_cast<uint4*>(sm + kOffSb + q * 8192 + swz64(kr * 64 + ch * 16)) = pack8_f16(t);
+        const uint4 w = pack8_f16(t);
+        *reinterpret_cast<uint4*>(sm + kOffSb + q * 8192 + swz64(kr * 64 + ch * 16)) = w;
+        if (kMode != 0 && step < NC) dst[ch] = w;
       }
+      if (kMode != 0 && step < NC && kr == 0) a.st_scale[unit * kSlices + sl] = up;
     };
     float sc, dn;
     slice_scale(true, sc, dn);
-    write_state_operand(0, dn);
+    write_state_operand(0, dn, 0, sc);
     if (tid == 0) sc_ring[0] = sc;
     fence_async_smem();
     __syncwarp();
@@ -1220,14 +1089,6 @@ chunk_state_kernel(const ChunkArgs a) {
     for (int c = 0; c < NC; ++c) {
       const int cs = c % CS, p = c & 1, qn = (c + 1) % kSb;
       const uint8_t* st = sm + cs * kCStage;
-      if (kMode != 0) {
-        // the state at the top of the step: this thread's key row, the CTA's 32 value columns
-        const int cu = kMode == 2 ? NC - 1 - c : c;
-        float* dst = a.st_save + ((((size_t)b * a.Hv + h) * NC + cu) * kD + kr) * kD + sl * kN;
-#pragma unroll
-        for (int n = 0; n < kN; n += 4)
-          *reinterpret_cast<float4*>(dst + n) = make_float4(Sm[n], Sm[n + 1], Sm[n + 2], Sm[n + 3]);
-      }
       ok = ok && mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
       if (ok) {
         // while the product D = M' S_c runs: S <- Gamma_C S + upV N (S_c is already in the fp16
@@ -1256,7 +1117,7 @@ chunk_state_kernel(const ChunkArgs a) {
       // every state warp reaches this barrier once per chunk, so a warp that gave up stops them all
       ok = slice_scale(ok, sc, dn);
       if (!ok) break;
-      write_state_operand(qn, dn);
+      write_state_operand(qn, dn, c + 1, sc);
       if (tid == 0) sc_ring[(c + 1) & 7] = sc;
       fence_async_smem();
       tc_fence_before();
@@ -1736,6 +1597,7 @@ cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s)
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   a.st_save = p.S_save;
+  a.st_scale = p.S_scale;
   a.S_T = nullptr;
   slot = stage_timer_begin(s, kKernChunkState);
   e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 1>, a);
@@ -1750,6 +1612,7 @@ cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s)
   a.S0 = p.dS_T;
   a.S_T = p.dS0;
   a.st_save = p.dS_save;
+  a.st_scale = p.dS_scale;
   slot = stage_timer_begin(s, kKernChunkAdjoint);
   e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 2>, a);
   stage_timer_end(slot, s);

@@ -34,18 +34,20 @@
 
 #include "gdr_backward.h"
 #include "gdr_internal.h"
+#include "gdr_inverse.cuh"
 #include "ptx.cuh"
 
 namespace gdr {
 namespace {
 using namespace ptx;
 
-constexpr int kLT = 256;                         // threads of the chunk-local kernel (8 warps)
+constexpr int kLT = 512;                         // threads of the chunk-local kernel (16 warps)
 constexpr int kLd = 136;                         // row stride (halves) of 128-column fp16 tiles
 constexpr int kLs = 72;                          // row stride (halves) of 64-column fp16 tiles
 constexpr int kLf = 68;                          // row stride (floats) of the fp32 64 x 64 tile
 constexpr float kQs = 0.08838834764831845f;      // 128^-0.5
 constexpr float kL2e = 1.4426950408889634f;
+constexpr int kStateSlices = 4;                  // 32-column slices of a saved state, one scale each
 
 constexpr uint32_t kT128 = 64 * kLd * 2;         // a 64 x 128 fp16 tile
 constexpr uint32_t kT128x = 128 * kLd * 2;       // a 128 x 128 fp16 tile
@@ -63,11 +65,11 @@ constexpr uint32_t kOT16 = kOTf + 64 * kLf * 4;  // T (fp16)
 constexpr uint32_t kOP16 = kOT16 + kT64;         // P (fp16)
 constexpr uint32_t kOG16 = kOP16 + kT64;         // K^ K^T (fp16)
 constexpr uint32_t kOVec = kOG16 + kT64;         // per-position vectors and reduction scratch
-constexpr int kNVec = 24;
+constexpr int kNVec = 26;
 constexpr uint32_t kLocalSmem = kOVec + kNVec * 64 * 4;
 // vectors (64 floats each)
-enum : int { vG2 = 0, vGam, vE, vBet, vSq, vSk, vRowG0, vRowG1, vRowB0, vRowB1, vRowD0, vRowD1,
-             vColG0, vColG1, vColG2, vColG3, vMax, vDot, vScan };
+enum : int { vG2 = 0, vGam, vE, vBet, vSq, vSk, vRowG0, vRowB0 = vRowG0 + 4, vRowD0 = vRowB0 + 4,
+             vColG0 = vRowD0 + 4, vMax = vColG0 + 4, vDot, vScan };
 
 __device__ __forceinline__ void pow2_up_dn(float m, float& up, float& dn) {
   // up = 2^e with m / up in [0.5, 1) (1 for m = 0), dn = 1 / up, e clamped to keep both normal
@@ -180,6 +182,24 @@ __device__ __forceinline__ float cta_max(float m, float* vmax, int warp, int lan
   return r;
 }
 
+// CTA-wide maxima of four per-thread values at once (every thread gets them); uses vmax[0..63]
+__device__ __forceinline__ void cta_max4(float (&m)[4], float* vmax, int warp, int lane) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], o));
+  __syncthreads();
+  if (lane < 4) vmax[4 * warp + lane] = lane == 0 ? m[0] : lane == 1 ? m[1] : lane == 2 ? m[2] : m[3];
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float r = vmax[j];
+#pragma unroll
+    for (int w = 1; w < kLT / 32; ++w) r = fmaxf(r, vmax[4 * w + j]);
+    m[j] = r;
+  }
+}
+
 struct LocalArgs {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
@@ -187,8 +207,10 @@ struct LocalArgs {
   const float* g;
   const float* beta;
   const __nv_bfloat16* dO;
-  const float* S_save;    // [B, Hv, NC, D, D]
-  const float* dS_save;   // [B, Hv, NC, D, D]
+  const __half* S_save;   // [B, Hv, NC, D, D] fp16, 32-column slices divided by S_scale [B, Hv, NC, 4]
+  const float* S_scale;
+  const __half* dS_save;  // likewise for the adjoints
+  const float* dS_scale;
   float* dqt;             // [B, L, Hv, D]: gradient of q~ per value head
   float* dkh;             // [B, L, Hv, D]: gradient of k^ per value head
   float* dv;
@@ -198,18 +220,15 @@ struct LocalArgs {
 };
 
 // One CTA per (row, value head, chunk) unit. Warp w owns rows 16 (w % 4) .. + 15 of every 64-row
-// product and the column half w / 4 (64 columns of a 128-column product, 32 of a 64-column one).
-__global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+// product and the column quarter w / 4 (32 columns of a 128-column product, 16 of a 64-column one).
+__device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, const int u) {
   float* vec = reinterpret_cast<float*>(sm + kOVec);
   auto V = [&](int i) { return vec + i * 64; };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int u = blockIdx.x;
   const int c = u % a.NC, h = (u / a.NC) % a.Hv, b = u / (a.NC * a.Hv);
   const int hk = h / (a.Hv / a.Hk);
-  const int m0 = 16 * (warp & 3), half = warp >> 2;
-  const int n128 = 64 * half, n64 = 32 * half;
+  const int m0 = 16 * (warp & 3), quarter = warp >> 2;
+  const int n128 = 32 * quarter, n64 = 16 * quarter;
   const int p0 = c * kChunk;   // first position of the chunk
   uint8_t* tQ = sm + kOQ;
   uint8_t* tK = sm + kOK;
@@ -239,32 +258,31 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
     V(vScan)[tid] = x;
   }
   {
-    // 64 rows x 16 chunks of 16 bytes for each of q, k (key head hk) and v, dO (value head h)
-    for (int idx = tid; idx < 4 * 1024; idx += kLT) {
+    // 64 rows x 16 chunks of 16 bytes for each of q, k (key head hk) and v, dO (value head h), as
+    // asynchronous copies (rows past L are zero-filled)
+#pragma unroll
+    for (int it = 0; it < 4 * 1024 / kLT; ++it) {
+      const int idx = tid + kLT * it;
       const int which = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
       const int pos = p0 + row;
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if (pos < a.L) {
-        const __nv_bfloat16* src = which == 0 ? a.q : which == 1 ? a.k : which == 2 ? a.v : a.dO;
-        const int H = which < 2 ? a.Hk : a.Hv, hh = which < 2 ? hk : h;
-        w = __ldg(reinterpret_cast<const uint4*>(src + (((size_t)b * a.L + pos) * H + hh) * kD) + ch);
-      }
+      const __nv_bfloat16* src = which == 0 ? a.q : which == 1 ? a.k : which == 2 ? a.v : a.dO;
+      const int H = which < 2 ? a.Hk : a.Hv, hh = which < 2 ? hk : h;
+      const size_t r = pos < a.L ? (((size_t)b * a.L + pos) * H + hh) * kD : 0;
       uint8_t* dst = which == 0 ? tQ : which == 1 ? tK : which == 2 ? tV : tO;
-      *reinterpret_cast<uint4*>(dst + row * kLd * 2 + ch * 16) = w;
+      cp_async16_zfill(dst + row * kLd * 2 + ch * 16, reinterpret_cast<const uint4*>(src + r) + ch, pos < a.L ? 16 : 0);
     }
-  }
-  // S and dS': thread tid holds float4 number tid + 256 m (m < 16) of each, in registers
-  const size_t sbase = (((size_t)b * a.Hv + h) * a.NC + c) * kD * kD;
-  float4 s4[16], d4[16];
-  float mS = 0.f, mD = 0.f, dot = 0.f;
+    // S and dS' (fp16 key rows of 256 bytes) straight into their tiles
+    const size_t unit = ((size_t)b * a.Hv + h) * a.NC + c;
 #pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    s4[m] = __ldg(reinterpret_cast<const float4*>(a.S_save + sbase) + tid + 256 * m);
-    d4[m] = __ldg(reinterpret_cast<const float4*>(a.dS_save + sbase) + tid + 256 * m);
-    mS = fmaxf(mS, fmaxf(fmaxf(fabsf(s4[m].x), fabsf(s4[m].y)), fmaxf(fabsf(s4[m].z), fabsf(s4[m].w))));
-    mD = fmaxf(mD, fmaxf(fmaxf(fabsf(d4[m].x), fabsf(d4[m].y)), fmaxf(fabsf(d4[m].z), fabsf(d4[m].w))));
-    dot += s4[m].x * d4[m].x + s4[m].y * d4[m].y + s4[m].z * d4[m].z + s4[m].w * d4[m].w;
+    for (int it = 0; it < 2 * 2048 / kLT; ++it) {
+      const int idx = tid + kLT * it;
+      const int which = idx >> 11, row = (idx >> 4) & 127, ch = idx & 15;
+      const __half* src = (which ? a.dS_save : a.S_save) + (unit * kD + row) * kD;
+      cp_async16_zfill((which ? tD : tS) + row * kLd * 2 + ch * 16, reinterpret_cast<const uint4*>(src) + ch, 16);
+    }
+    cp_async_commit();
   }
+  cp_async_wait<0>();
   __syncthreads();
   if (tid < 64) {
     const float gam = V(vScan)[tid] + (tid >= 32 ? V(vScan)[31] : 0.f);
@@ -291,22 +309,81 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
     }
     V(tid < 128 ? vSq : vSk)[row] = rsqrtf(s0 + 1e-6f);
   }
-  // largest |v|, |dO| (bf16 magnitude bits order like the values)
-  uint32_t mv = 0, mo = 0;
-  for (int idx = tid; idx < 1024; idx += kLT) {
-    const int row = idx >> 4, ch = idx & 15;
-    const uint4 wv = *reinterpret_cast<const uint4*>(tV + row * kLd * 2 + ch * 16);
-    const uint4 wo = *reinterpret_cast<const uint4*>(tO + row * kLd * 2 + ch * 16);
-    mv = __vmaxu2(mv, __vmaxu2(__vmaxu2(wv.x & 0x7FFF7FFFu, wv.y & 0x7FFF7FFFu), __vmaxu2(wv.z & 0x7FFF7FFFu, wv.w & 0x7FFF7FFFu)));
-    mo = __vmaxu2(mo, __vmaxu2(__vmaxu2(wo.x & 0x7FFF7FFFu, wo.y & 0x7FFF7FFFu), __vmaxu2(wo.z & 0x7FFF7FFFu, wo.w & 0x7FFF7FFFu)));
+  __syncthreads();   // the norms and decays are in
+
+  // per-thread partial sums: rows (this warp's column quarter, unshuffled) and columns of the 64 x 64
+  // products (this thread's two rows)
+  float rg[2] = {0.f, 0.f}, rb[2] = {0.f, 0.f}, rd[2] = {0.f, 0.f}, cg[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) cg[i] = 0.f;
+  const float* gam2 = V(vG2);
+  const float* Gam = V(vGam);
+  const float* ev = V(vE);
+  const float* bet = V(vBet);
+  auto Eij = [&](int i, int j) { return exp2f(gam2[i] - gam2[j]); };   // j <= i only
+
+  // ---- 1. Gram products from the raw bf16 rows: A (fp32), K^ K^T and P (fp16) ----
+  {
+    float G[2][4], Gq[2][4];
+    zero(G);
+    zero(Gq);
+    tile_mma<2, false, true, true>(G, tK, kLd, m0, tK, kLd, n64, 128, lane);
+    tile_mma<2, false, true, true>(Gq, tQ, kLd, m0, tK, kLd, n64, 128, lane);
+    const float* sq = V(vSq);
+    const float* sk = V(vSk);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = frow(m0, lane, e), j = fcol(n64, lane, nt, e);
+        const float kk = sk[i] * sk[j] * G[nt][e];
+        const float E = j <= i ? Eij(i, j) : 0.f;
+        Af[i * kLf + j] = j < i ? bet[i] * kk * E : (j == i ? 1.f : 0.f);   // 1 on the diagonal
+        reinterpret_cast<__half*>(tG)[i * kLs + j] = __float2half_rn(kk);
+        reinterpret_cast<__half*>(tP)[i * kLs + j] = __float2half_rn(kQs * sq[i] * sk[j] * Gq[nt][e] * E);
+      }
   }
-  const float fmv = __uint_as_float(max(mv & 0xFFFFu, mv >> 16) << 16);
-  const float fmo = __uint_as_float(max(mo & 0xFFFFu, mo >> 16) << 16);
-  float upV, dnV, upO, dnO, upS, dnS, upD, dnD;
-  pow2_up_dn(cta_max(fmv, V(vMax), warp, lane), upV, dnV);
-  pow2_up_dn(cta_max(fmo, V(vMax), warp, lane), upO, dnO);
-  pow2_up_dn(cta_max(mS, V(vMax), warp, lane), upS, dnS);
-  pow2_up_dn(cta_max(mD, V(vMax), warp, lane), upD, dnD);
+  // the largest |v|, |dO| (bf16 magnitude bits order like the values); S and dS' to one power of
+  // two per tile (their slices' largest), <S, dS'>
+  float mx[4] = {0.f, 0.f, 0.f, 0.f}, dot = 0.f;
+  {
+    uint32_t mv = 0, mo = 0;
+    for (int idx = tid; idx < 1024; idx += kLT) {
+      const int row = idx >> 4, ch = idx & 15;
+      const uint4 wv = *reinterpret_cast<const uint4*>(tV + row * kLd * 2 + ch * 16);
+      const uint4 wo = *reinterpret_cast<const uint4*>(tO + row * kLd * 2 + ch * 16);
+      mv = __vmaxu2(mv, __vmaxu2(__vmaxu2(wv.x & 0x7FFF7FFFu, wv.y & 0x7FFF7FFFu), __vmaxu2(wv.z & 0x7FFF7FFFu, wv.w & 0x7FFF7FFFu)));
+      mo = __vmaxu2(mo, __vmaxu2(__vmaxu2(wo.x & 0x7FFF7FFFu, wo.y & 0x7FFF7FFFu), __vmaxu2(wo.z & 0x7FFF7FFFu, wo.w & 0x7FFF7FFFu)));
+    }
+    mx[0] = __uint_as_float(max(mv & 0xFFFFu, mv >> 16) << 16);
+    mx[1] = __uint_as_float(max(mo & 0xFFFFu, mo >> 16) << 16);
+  }
+  cta_max4(mx, V(vMax), warp, lane);
+  float upV, dnV, upO, dnO;
+  pow2_up_dn(mx[0], upV, dnV);
+  pow2_up_dn(mx[1], upO, dnO);
+  const size_t unit = ((size_t)b * a.Hv + h) * a.NC + c;
+  const float4 scS = *reinterpret_cast<const float4*>(a.S_scale + unit * 4);
+  const float4 scD = *reinterpret_cast<const float4*>(a.dS_scale + unit * 4);
+  const float upS = fmaxf(fmaxf(scS.x, scS.y), fmaxf(scS.z, scS.w));
+  const float upD = fmaxf(fmaxf(scD.x, scD.y), fmaxf(scD.z, scD.w));
+  for (int idx = tid; idx < 2048; idx += kLT) {
+    const int row = idx >> 4, ch = idx & 15, j = ch >> 2;   // slice j: columns 32 j .. + 31
+    const float sj = j == 0 ? scS.x : j == 1 ? scS.y : j == 2 ? scS.z : scS.w;
+    const float dj = j == 0 ? scD.x : j == 1 ? scD.y : j == 2 ? scD.z : scD.w;
+    __half2* ps = reinterpret_cast<__half2*>(tS + row * kLd * 2 + ch * 16);
+    __half2* pd = reinterpret_cast<__half2*>(tD + row * kLd * 2 + ch * 16);
+    const float fs = sj / upS, fd = dj / upD;   // powers of two <= 1
+    float part = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __half22float2(ps[e]), y = __half22float2(pd[e]);
+      part = fmaf(x.x, y.x, fmaf(x.y, y.y, part));
+      if (fs != 1.f) ps[e] = __floats2half2_rn(x.x * fs, x.y * fs);
+      if (fd != 1.f) pd[e] = __floats2half2_rn(y.x * fd, y.y * fd);
+    }
+    dot = fmaf(part, sj * dj, dot);
+  }
   {
     // <S, dS'> over the whole 128 x 128 state (fixed order: warp sums, then warps in order)
 #pragma unroll
@@ -324,50 +401,6 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
     *po = make_uint4(bf16x2_to_f16x2_scaled(wo.x, dnO), bf16x2_to_f16x2_scaled(wo.y, dnO),
                      bf16x2_to_f16x2_scaled(wo.z, dnO), bf16x2_to_f16x2_scaled(wo.w, dnO));
   }
-#pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const int e = 4 * (tid + 256 * m), row = e >> 7, col = e & 127;
-    __half* ps = reinterpret_cast<__half*>(tS) + row * kLd + col;
-    __half* pd = reinterpret_cast<__half*>(tD) + row * kLd + col;
-    *reinterpret_cast<__half2*>(ps) = __floats2half2_rn(s4[m].x * dnS, s4[m].y * dnS);
-    *reinterpret_cast<__half2*>(ps + 2) = __floats2half2_rn(s4[m].z * dnS, s4[m].w * dnS);
-    *reinterpret_cast<__half2*>(pd) = __floats2half2_rn(d4[m].x * dnD, d4[m].y * dnD);
-    *reinterpret_cast<__half2*>(pd + 2) = __floats2half2_rn(d4[m].z * dnD, d4[m].w * dnD);
-  }
-  __syncthreads();
-
-  // per-thread partial sums: rows (this warp's column half, unshuffled) and columns of the 64 x 64
-  // products (this thread's two rows)
-  float rg[2] = {0.f, 0.f}, rb[2] = {0.f, 0.f}, rd[2] = {0.f, 0.f}, cg[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) cg[i] = 0.f;
-  const float* gam2 = V(vG2);
-  const float* Gam = V(vGam);
-  const float* ev = V(vE);
-  const float* bet = V(vBet);
-  auto Eij = [&](int i, int j) { return exp2f(gam2[i] - gam2[j]); };   // j <= i only
-
-  // ---- 1. Gram products from the raw bf16 rows: A (fp32), K^ K^T and P (fp16) ----
-  {
-    float G[4][4], Gq[4][4];
-    zero(G);
-    zero(Gq);
-    tile_mma<4, false, true, true>(G, tK, kLd, m0, tK, kLd, n64, 128, lane);
-    tile_mma<4, false, true, true>(Gq, tQ, kLd, m0, tK, kLd, n64, 128, lane);
-    const float* sq = V(vSq);
-    const float* sk = V(vSk);
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = frow(m0, lane, e), j = fcol(n64, lane, nt, e);
-        const float kk = sk[i] * sk[j] * G[nt][e];
-        const float E = j <= i ? Eij(i, j) : 0.f;
-        Af[i * kLf + j] = j < i ? bet[i] * kk * E : 0.f;
-        reinterpret_cast<__half*>(tG)[i * kLs + j] = __float2half_rn(kk);
-        reinterpret_cast<__half*>(tP)[i * kLs + j] = __float2half_rn(kQs * sq[i] * sk[j] * Gq[nt][e] * E);
-      }
-  }
   __syncthreads();
   // raw rows -> fp16 unit rows q^ = q / |q|, k^ = k / |k| (q~ = q^ 128^-0.5)
   for (int idx = tid; idx < 2 * 1024; idx += kLT) {
@@ -380,41 +413,39 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
   }
   __syncthreads();
 
-  // ---- 2. T = (I + A)^-1 (threads 0-63: column j by forward substitution); meanwhile the operand
-  //         diag(beta Gamma) K^ ----
-  if (tid < 64) {
-    const int j = tid;
-    float x[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) x[i] = (i == j) ? 1.f : 0.f;
-#pragma unroll
-    for (int i = 1; i < 64; ++i) {
-      const float* arow = Af + i * kLf;
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int m = 0; m < i; m += 2) {
-        s0 = fmaf(arow[m], x[m], s0);
-        if (m + 1 < i) s1 = fmaf(arow[m + 1], x[m + 1], s1);
-      }
-      if (i > j) x[i] = -(s0 + s1);
+  // ---- 2. T = (I + A)^-1 by recursive doubling (the forward's inverse: fp32-accurate merges), T
+  //         row-major in fp32 over X2 with its scratch over T's fp16 tile; meanwhile the operand
+  //         diag(beta Gamma) K^ into X1 ----
+  {
+    float* Tm = reinterpret_cast<float*>(tX2);
+    for (int e = tid; e < 64 * 17; e += kLT) {   // Tm starts as the identity
+      const int rr = e / 17, c4 = e - rr * 17;
+      const int d = ((rr >> 2) == c4) ? (rr & 3) : -1;
+      reinterpret_cast<float4*>(Tm + rr * kLf)[c4] =
+          make_float4(d == 0 ? 1.f : 0.f, d == 1 ? 1.f : 0.f, d == 2 ? 1.f : 0.f, d == 3 ? 1.f : 0.f);
     }
-#pragma unroll
-    for (int i = 0; i < 64; ++i) reinterpret_cast<__half*>(tT)[i * kLs + j] = __float2half_rn(x[i]);
-  } else {
-    for (int idx = tid - 64; idx < 64 * 64; idx += kLT - 64) {
-      const int row = idx >> 6, c2 = idx & 63;
-      const float s = bet[row] * Gam[row];
-      __half2* p = reinterpret_cast<__half2*>(tK + row * kLd * 2) + c2;
-      const float2 f = __half22float2(*p);
-      reinterpret_cast<__half2*>(tX1 + row * kLd * 2)[c2] = __floats2half2_rn(f.x * s, f.y * s);
+    __syncthreads();
+    invert_unit_lower(Af, Tm, reinterpret_cast<float*>(tT), tid, [&](int t) {
+      for (int idx = t - 64; idx < 64 * 64; idx += kLT - 64) {
+        const int row = idx >> 6, c2 = idx & 63;
+        const float sc = bet[row] * Gam[row];
+        const float2 f = __half22float2(reinterpret_cast<const __half2*>(tK + row * kLd * 2)[c2]);
+        reinterpret_cast<__half2*>(tX1 + row * kLd * 2)[c2] = __floats2half2_rn(f.x * sc, f.y * sc);
+      }
+    });
+    // T as fp16, row-major (over the inverse's scratch), from its transposed copy in A's upper part:
+    // T(i, j) = Af[j][i] below the diagonal, 1 on it
+    for (int e = tid; e < 64 * 64; e += kLT) {
+      const int i = e >> 6, j = e & 63;
+      reinterpret_cast<__half*>(tT)[i * kLs + j] = __float2half_rn(i > j ? Af[j * kLf + i] : (i == j ? 1.f : 0.f));
     }
   }
   __syncthreads();
 
   // ---- 3. W = T diag(beta Gamma) K^, U = T diag(beta) V, Delta = U - W S ----
-  float acc[8][4], acc2[8][4];
+  float acc[4][4], acc2[4][4];
   zero(acc);
-  tile_mma<8, false, false>(acc, tT, kLs, m0, tX1, kLd, n128, 64, lane);   // W
+  tile_mma<4, false, false>(acc, tT, kLs, m0, tX1, kLd, n128, 64, lane);   // W
   store_h(tX2, kLd, m0, n128, acc, 1.f, lane);
   __syncthreads();
   for (int idx = tid; idx < 64 * 64; idx += kLT) {
@@ -424,11 +455,11 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
   }
   __syncthreads();
   zero(acc);
-  tile_mma<8, false, false>(acc, tT, kLs, m0, tX1, kLd, n128, 64, lane);    // U / 2^eV
+  tile_mma<4, false, false>(acc, tT, kLs, m0, tX1, kLd, n128, 64, lane);    // U / 2^eV
   zero(acc2);
-  tile_mma<8, false, false>(acc2, tX2, kLd, m0, tS, kLd, n128, 128, lane);  // W S / 2^eS
+  tile_mma<4, false, false>(acc2, tX2, kLd, m0, tS, kLd, n128, 128, lane);  // W S / 2^eS
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[nt][e] = upV * acc[nt][e] - upS * acc2[nt][e];   // Delta
   float upDl, dnDl;
@@ -438,11 +469,11 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
 
   // ---- 4. dDelta = P^T dO + diag(e) K^ dS'; the rows e_i k^_i . (dS' Delta_i) ----
   zero(acc);
-  tile_mma<8, true, false>(acc, tP, kLs, m0, tO, kLd, n128, 64, lane);     // P^T dO / 2^eO
+  tile_mma<4, true, false>(acc, tP, kLs, m0, tO, kLd, n128, 64, lane);     // P^T dO / 2^eO
   zero(acc2);
-  tile_mma<8, false, false>(acc2, tK, kLd, m0, tD, kLd, n128, 128, lane);  // K^ dS' / 2^eD
+  tile_mma<4, false, false>(acc2, tK, kLd, m0, tD, kLd, n128, 128, lane);  // K^ dS' / 2^eD
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int i = frow(m0, lane, e), col = fcol(n128, lane, nt, e);
@@ -455,20 +486,20 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
   store_h(tX2, kLd, m0, n128, acc, dndD, lane);                          // dDelta / 2^edD (W is spent)
 
   // ---- 5. dK^ = diag(e) Delta dS'^T (the first of its terms) ----
-  float dK[8][4], dQ[8][4];
+  float dK[4][4], dQ[4][4];
   zero(dK);
-  tile_mma<8, false, true>(dK, tX1, kLd, m0, tD, kLd, n128, 128, lane);
+  tile_mma<4, false, true>(dK, tX1, kLd, m0, tD, kLd, n128, 128, lane);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) dK[nt][e] *= ev[frow(m0, lane, e)] * upDl * upD;
   __syncthreads();   // dDelta is stored; dS' is read by every warp (its tile is reused below)
 
   // ---- 6. dW = -dDelta S^T; dQ~ = diag(Gamma) dO S^T; the rows Gamma_i q~_i . (dO S^T)_i ----
   zero(acc);
-  tile_mma<8, false, true>(acc, tX2, kLd, m0, tS, kLd, n128, 128, lane);
+  tile_mma<4, false, true>(acc, tX2, kLd, m0, tS, kLd, n128, 128, lane);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[nt][e] *= -updD * upS;
   float updW, dndW;
@@ -476,9 +507,9 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
   uint8_t* tdW = tD;   // dS' is spent
   store_h(tdW, kLd, m0, n128, acc, dndW, lane);
   zero(dQ);
-  tile_mma<8, false, true>(dQ, tO, kLd, m0, tS, kLd, n128, 128, lane);
+  tile_mma<4, false, true>(dQ, tO, kLd, m0, tS, kLd, n128, 128, lane);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int i = frow(m0, lane, e), col = fcol(n128, lane, nt, e);
@@ -494,11 +525,11 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
   uint8_t* tZ = tS + 2 * kT64;
   uint8_t* tdA = tD + kT128;
   {
-    float dp[4][4];
+    float dp[2][4];
     zero(dp);
-    tile_mma<4, false, true>(dp, tO, kLd, m0, tX1, kLd, n64, 128, lane);
+    tile_mma<2, false, true>(dp, tO, kLd, m0, tX1, kLd, n64, 128, lane);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = frow(m0, lane, e), j = fcol(n64, lane, nt, e);
@@ -512,26 +543,26 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
     pow2_up_dn(cta_max(absmax(dp), V(vMax), warp, lane), up, dn);
     store_h(tPE, kLs, m0, n64, dp, dn, lane);
     __syncthreads();
-    float t2[8][4];
+    float t2[4][4];
     zero(t2);
-    tile_mma<8, false, false>(t2, tPE, kLs, m0, tK, kLd, n128, 64, lane);
+    tile_mma<4, false, false>(t2, tPE, kLs, m0, tK, kLd, n128, 64, lane);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) dQ[nt][e] += up * t2[nt][e];
     zero(t2);
-    tile_mma<8, true, false>(t2, tPE, kLs, m0, tQ, kLd, n128, 64, lane);
+    tile_mma<4, true, false>(t2, tPE, kLs, m0, tQ, kLd, n128, 64, lane);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) dK[nt][e] += up * kQs * t2[nt][e];
   }
 
   // ---- 8. T^T dDelta -> dV, dbeta; T^T dW -> dK^, dbeta, dgamma ----
   zero(acc);
-  tile_mma<8, true, false>(acc, tT, kLs, m0, tX2, kLd, n128, 64, lane);
+  tile_mma<4, true, false>(acc, tT, kLs, m0, tX2, kLd, n128, 64, lane);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int i = frow(m0, lane, 2 * hh), col = fcol(n128, lane, nt, 0);
@@ -542,9 +573,9 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
             make_float2(bet[i] * x0, bet[i] * x1);
     }
   zero(acc);
-  tile_mma<8, true, false>(acc, tT, kLs, m0, tdW, kLd, n128, 64, lane);
+  tile_mma<4, true, false>(acc, tT, kLs, m0, tdW, kLd, n128, 64, lane);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int i = frow(m0, lane, e), col = fcol(n128, lane, nt, e);
@@ -557,13 +588,13 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
 
   // ---- 9. dT = dDelta (beta V)^T + dW (beta Gamma K^)^T; dA = -T^T dT T^T (j < i) ----
   {
-    float t1[4][4], t2[4][4];
+    float t1[2][4], t2[2][4];
     zero(t1);
-    tile_mma<4, false, true>(t1, tX2, kLd, m0, tV, kLd, n64, 128, lane);
+    tile_mma<2, false, true>(t1, tX2, kLd, m0, tV, kLd, n64, 128, lane);
     zero(t2);
-    tile_mma<4, false, true>(t2, tdW, kLd, m0, tK, kLd, n64, 128, lane);
+    tile_mma<2, false, true>(t2, tdW, kLd, m0, tK, kLd, n64, 128, lane);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = fcol(n64, lane, nt, e);
@@ -574,15 +605,15 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
     store_h(tdT, kLs, m0, n64, t1, dnT, lane);
     __syncthreads();
     zero(t2);
-    tile_mma<4, false, true>(t2, tdT, kLs, m0, tT, kLs, n64, 64, lane);   // dT T^T
+    tile_mma<2, false, true>(t2, tdT, kLs, m0, tT, kLs, n64, 64, lane);   // dT T^T
     float upZ, dnZ;
     pow2_up_dn(cta_max(absmax(t2), V(vMax), warp, lane), upZ, dnZ);
     store_h(tZ, kLs, m0, n64, t2, dnZ, lane);
     __syncthreads();
     zero(t1);
-    tile_mma<4, true, false>(t1, tT, kLs, m0, tZ, kLs, n64, 64, lane);    // T^T (dT T^T)
+    tile_mma<2, true, false>(t1, tT, kLs, m0, tZ, kLs, n64, 64, lane);    // T^T (dT T^T)
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = frow(m0, lane, e), j = fcol(n64, lane, nt, e);
@@ -602,12 +633,12 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
     pow2_up_dn(cta_max(absmax(t1), V(vMax), warp, lane), upA, dnA);
     store_h(tdA, kLs, m0, n64, t1, dnA, lane);
     __syncthreads();
-    float t3[8][4];
+    float t3[4][4];
     zero(t3);
-    tile_mma<8, false, false>(t3, tdA, kLs, m0, tK, kLd, n128, 64, lane);
-    tile_mma<8, true, false>(t3, tdA, kLs, m0, tK, kLd, n128, 64, lane);
+    tile_mma<4, false, false>(t3, tdA, kLs, m0, tK, kLd, n128, 64, lane);
+    tile_mma<4, true, false>(t3, tdA, kLs, m0, tK, kLd, n128, 64, lane);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) dK[nt][e] += upA * t3[nt][e];
   }
@@ -623,33 +654,42 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
     }
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) cg[i] += __shfl_xor_sync(0xffffffffu, cg[i], o);
   if ((lane & 3) == 0) {
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int i = m0 + (lane >> 2) + 8 * hh;
-      V(vRowG0 + half)[i] = rg[hh];
-      V(vRowB0 + half)[i] = rb[hh];
-      V(vRowD0 + half)[i] = rd[hh];
+      V(vRowG0 + quarter)[i] = rg[hh];
+      V(vRowB0 + quarter)[i] = rb[hh];
+      V(vRowD0 + quarter)[i] = rd[hh];
     }
   }
   if (lane < 4) {
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int x = 0; x < 2; ++x) V(vColG0 + (warp & 3))[n64 + 8 * nt + 2 * lane + x] = cg[2 * nt + x];
+  }
+  __syncthreads();
+  auto sum4 = [&](int v0, int r) { return (V(v0)[r] + V(v0 + 1)[r]) + (V(v0 + 2)[r] + V(v0 + 3)[r]); };
+  if (warp < 2) {
+    // sum_j e_j k^_j . (dS' Delta_j) over the chunk (two warp sums)
+    float t = sum4(vRowD0, tid);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) V(vMax)[warp] = t;
   }
   __syncthreads();
   if (warp == 0 || warp == 1) {
     // dgamma_i, then dg_j = sum_{i >= j} dgamma_i (a reversed inclusive scan over two warps)
     const int i = 63 - tid;   // warp 0: positions 63..32, warp 1: 31..0
-    const float de = V(vRowD0)[i] + V(vRowD1)[i];
-    float dga = V(vRowG0)[i] + V(vRowG1)[i] + V(vColG0)[i] + V(vColG1)[i] + V(vColG2)[i] + V(vColG3)[i] - de;
+    const float de = sum4(vRowD0, i);
+    float dga = sum4(vRowG0, i) + sum4(vColG0, i) - de;
     if (i == 63) {
-      float tot_de = 0.f, dotS = 0.f;
-      for (int r = 0; r < 64; ++r) tot_de += V(vRowD0)[r] + V(vRowD1)[r];
+      const float tot_de = V(vMax)[0] + V(vMax)[1];
+      float dotS = 0.f;
       for (int w = 0; w < kLT / 32; ++w) dotS += V(vDot)[w];
       dga += Gam[63] * dotS + tot_de;
     }
@@ -668,11 +708,11 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
     if (p0 + i < a.L) {
       const size_t gi = ((size_t)b * a.L + p0 + i) * a.Hv + h;
       a.dg[gi] = dgi;
-      a.dbeta[gi] = V(vRowB0)[i] + V(vRowB1)[i];
+      a.dbeta[gi] = (V(vRowB0)[i] + V(vRowB0 + 1)[i]) + (V(vRowB0 + 2)[i] + V(vRowB0 + 3)[i]);
     }
   }
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int i = frow(m0, lane, 2 * hh), col = fcol(n128, lane, nt, 0);
@@ -684,36 +724,62 @@ __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs
     }
 }
 
-// One (row, position, key head) per CTA, one key dimension per thread: the sums over the value
-// heads of the key head, then the normalisations' backward (q~ = q s_q 128^-0.5, k^ = k s_k).
-__global__ void __launch_bounds__(kD) chunk_bwd_reduce_kernel(const LocalArgs a, float* dq, float* dk) {
-  __shared__ float red[4][4];
-  const size_t bt = blockIdx.x;   // b L + position
-  const int hk = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// One CTA per unit (the unit's tiles take most of an SM's shared memory).
+__global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs a) {
+  static_assert(kLT == 512, "the warp tiling assumes 16 warps");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  local_unit(a, sm, blockIdx.x);
+}
+
+// One (row, position, key head) per warp, four key dimensions per lane: the sums over the value
+// heads of the key head, then the normalisations' backward (q~ = q s_q 128^-0.5, k^ = k s_k); the
+// row sums by warp shuffles in a fixed order.
+constexpr int kRedWarps = 8;
+__global__ void __launch_bounds__(kRedWarps * 32) chunk_bwd_reduce_kernel(const LocalArgs a, float* dq, float* dk) {
+  const int lane = threadIdx.x & 31;
+  const size_t item = (size_t)blockIdx.x * kRedWarps + (threadIdx.x >> 5);   // (b L + position) Hk + hk
+  if (item >= (size_t)a.B * a.L * a.Hk) return;
+  const size_t bt = item / a.Hk;
+  const int hk = (int)(item - bt * a.Hk);
   const int r = a.Hv / a.Hk;
-  float dqt = 0.f, dkh = 0.f;
+  float4 dq4 = make_float4(0.f, 0.f, 0.f, 0.f), dk4 = dq4;
   for (int j = 0; j < r; ++j) {
-    const size_t o = (bt * a.Hv + (size_t)hk * r + j) * kD + tid;
-    dqt += a.dqt[o];
-    dkh += a.dkh[o];
+    const size_t o = (bt * a.Hv + (size_t)hk * r + j) * kD + 4 * lane;
+    const float4 x = __ldg(reinterpret_cast<const float4*>(a.dqt + o));
+    const float4 y = __ldg(reinterpret_cast<const float4*>(a.dkh + o));
+    dq4.x += x.x; dq4.y += x.y; dq4.z += x.z; dq4.w += x.w;
+    dk4.x += y.x; dk4.y += y.y; dk4.z += y.z; dk4.w += y.w;
   }
-  const size_t off = (bt * a.Hk + hk) * kD + tid;
-  const float qv = __bfloat162float(a.q[off]), kv = __bfloat162float(a.k[off]);
-  float s[4] = {qv * qv, qv * dqt, kv * kv, kv * dkh};
+  const size_t off = item * kD + 4 * lane;
+  const uint2 qw = __ldg(reinterpret_cast<const uint2*>(a.q + off));
+  const uint2 kw = __ldg(reinterpret_cast<const uint2*>(a.k + off));
+  const float qv[4] = {__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xFFFF0000u), __uint_as_float(qw.y << 16),
+                       __uint_as_float(qw.y & 0xFFFF0000u)};
+  const float kv[4] = {__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u), __uint_as_float(kw.y << 16),
+                       __uint_as_float(kw.y & 0xFFFF0000u)};
+  const float dqv[4] = {dq4.x, dq4.y, dq4.z, dq4.w}, dkv[4] = {dk4.x, dk4.y, dk4.z, dk4.w};
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int e = 0; e < 4; ++e) {
+    s[0] = fmaf(qv[e], qv[e], s[0]);
+    s[1] = fmaf(qv[e], dqv[e], s[1]);
+    s[2] = fmaf(kv[e], kv[e], s[2]);
+    s[3] = fmaf(kv[e], dkv[e], s[3]);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s[j] += __shfl_xor_sync(0xffffffffu, s[j], o);
-    if (lane == 0) red[warp][j] = s[j];
-  }
-  __syncthreads();
-  float tot[4];
+  const float sq = rsqrtf(s[0] + 1e-6f), sk = rsqrtf(s[2] + 1e-6f);
+  float oq[4], ok[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) tot[j] = red[0][j] + red[1][j] + red[2][j] + red[3][j];
-  const float sq = rsqrtf(tot[0] + 1e-6f), sk = rsqrtf(tot[2] + 1e-6f);
-  dq[off] = kQs * (sq * dqt - sq * sq * sq * tot[1] * qv);
-  dk[off] = sk * dkh - sk * sk * sk * tot[3] * kv;
+  for (int e = 0; e < 4; ++e) {
+    oq[e] = kQs * (sq * dqv[e] - sq * sq * sq * s[1] * qv[e]);
+    ok[e] = sk * dkv[e] - sk * sk * sk * s[3] * kv[e];
+  }
+  *reinterpret_cast<float4*>(dq + off) = make_float4(oq[0], oq[1], oq[2], oq[3]);
+  *reinterpret_cast<float4*>(dk + off) = make_float4(ok[0], ok[1], ok[2], ok[3]);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -723,28 +789,37 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 size_t chunk_bwd_workspace_bytes(int B, int L, int Hk, int Hv) {
   (void)Hk;
   const size_t NC = ((size_t)L + kChunk - 1) / kChunk;
-  const size_t states = (size_t)B * Hv * NC * kD * kD * sizeof(float);
+  const size_t states = (size_t)B * Hv * NC * kD * kD * sizeof(__half);
+  const size_t scales = (size_t)B * Hv * NC * kStateSlices * sizeof(float);
   const size_t parts = (size_t)B * L * Hv * kD * sizeof(float);
-  return align256(chunk_bwd_units_bytes(B, L, Hv)) + 2 * align256(states) + 2 * align256(parts);
+  return align256(chunk_bwd_units_bytes(B, L, Hv)) + 2 * align256(states) + 2 * align256(scales) + 2 * align256(parts);
 }
 
 cudaError_t launch_chunk_backward(const ChunkBackwardArgs& p, cudaStream_t s) {
   const size_t NC = ((size_t)p.L + kChunk - 1) / kChunk;
-  const size_t states = (size_t)p.B * p.Hv * NC * kD * kD * sizeof(float);
+  const size_t states = (size_t)p.B * p.Hv * NC * kD * kD * sizeof(__half);
+  const size_t scales = (size_t)p.B * p.Hv * NC * kStateSlices * sizeof(float);
   const size_t parts = (size_t)p.B * p.L * p.Hv * kD * sizeof(float);
   uint8_t* w = static_cast<uint8_t*>(p.ws);
-  uint8_t* units = w;
-  float* S_save = reinterpret_cast<float*>(w + align256(chunk_bwd_units_bytes(p.B, p.L, p.Hv)));
-  float* dS_save = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(S_save) + align256(states));
-  float* dqt = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dS_save) + align256(states));
-  float* dkh = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dqt) + align256(parts));
-  ChunkBwdChainLaunch cl{p.q, p.k, p.v, p.g, p.beta, p.S0, p.dO, p.dS_T, p.dS0, S_save, dS_save, units,
-                         p.B, p.L, p.Hk, p.Hv, p.err};
+  uint8_t* unit_ws = w;
+  w += align256(chunk_bwd_units_bytes(p.B, p.L, p.Hv));
+  __half* S_save = reinterpret_cast<__half*>(w);
+  w += align256(states);
+  __half* dS_save = reinterpret_cast<__half*>(w);
+  w += align256(states);
+  float* S_scale = reinterpret_cast<float*>(w);
+  w += align256(scales);
+  float* dS_scale = reinterpret_cast<float*>(w);
+  w += align256(scales);
+  float* dqt = reinterpret_cast<float*>(w);
+  float* dkh = reinterpret_cast<float*>(w + align256(parts));
+  ChunkBwdChainLaunch cl{p.q, p.k, p.v, p.g, p.beta, p.S0, p.dO, p.dS_T, p.dS0, S_save, S_scale, dS_save, dS_scale,
+                         unit_ws, p.B, p.L, p.Hk, p.Hv, p.err};
   cudaError_t e = launch_chunk_bwd_chain(cl, s);
   if (e != cudaSuccess) return e;
   LocalArgs la{static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k),
                static_cast<const __nv_bfloat16*>(p.v), p.g, p.beta, static_cast<const __nv_bfloat16*>(p.dO),
-               S_save, dS_save, dqt, dkh, p.dv, p.dg, p.dbeta, p.B, p.L, p.Hk, p.Hv, (int)NC};
+               S_save, S_scale, dS_save, dS_scale, dqt, dkh, p.dv, p.dg, p.dbeta, p.B, p.L, p.Hk, p.Hv, (int)NC};
   e = cudaFuncSetAttribute(chunk_bwd_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalSmem + 128);
   if (e != cudaSuccess) return e;
   int slot = stage_timer_begin(s, kKernChunkBwdLocal);
@@ -752,7 +827,8 @@ cudaError_t launch_chunk_backward(const ChunkBackwardArgs& p, cudaStream_t s) {
   stage_timer_end(slot, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   slot = stage_timer_begin(s, kKernChunkBwdReduce);
-  chunk_bwd_reduce_kernel<<<dim3((unsigned)((size_t)p.B * p.L), (unsigned)p.Hk), kD, 0, s>>>(la, p.dq, p.dk);
+  const size_t items = (size_t)p.B * p.L * p.Hk;
+  chunk_bwd_reduce_kernel<<<(unsigned)((items + kRedWarps - 1) / kRedWarps), kRedWarps * 32, 0, s>>>(la, p.dq, p.dk);
   stage_timer_end(slot, s);
   return cudaGetLastError();
 }
