@@ -561,10 +561,8 @@ const char* gdr_kernel_name(int id) {
     case kKernEpilogue: return "gdr_gated_rmsnorm";
     case kKernBackward: return "gdr_backward";
     case kKernBackwardReduce: return "gdr_backward_reduce";
-    case kKernChunkNb: return "gdr_chunk_nb";
     case kKernChunkAdjoint: return "gdr_chunk_adjoint";
     case kKernChunkBwdLocal: return "gdr_chunk_bwd_local";
-    case kKernChunkBwdReduce: return "gdr_chunk_bwd_reduce";
   }
   return nullptr;
 }

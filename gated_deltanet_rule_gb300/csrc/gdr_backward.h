@@ -11,12 +11,10 @@ namespace gdr {
 // Stage-timer ids, after the epilogue's.
 constexpr int kKernBackward = kKernEpilogue + 1;
 constexpr int kKernBackwardReduce = kKernEpilogue + 2;
-// the chunked backward (bf16): Nb = Q'^T dO, the adjoint chain, the chunk-local gradients, the
-// key-head reduction with the normalisations' backward
-constexpr int kKernChunkNb = kKernEpilogue + 3;
-constexpr int kKernChunkAdjoint = kKernEpilogue + 4;
-constexpr int kKernChunkBwdLocal = kKernEpilogue + 5;
-constexpr int kKernChunkBwdReduce = kKernEpilogue + 6;
+// the chunked backward (bf16): the adjoint chain, the chunk-local gradients (with the key-head sums
+// and the normalisations' backward)
+constexpr int kKernChunkAdjoint = kKernEpilogue + 3;
+constexpr int kKernChunkBwdLocal = kKernEpilogue + 4;
 
 constexpr int kBwdSeg = 32;        // tokens per recomputed segment
 constexpr int kBwdColBlocks = 8;   // CTAs per (row, value head), each owning D / 8 value columns
@@ -47,9 +45,9 @@ size_t backward_workspace_bytes(int B, int L, int Hk, int Hv);
 cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
 
 // The chunked backward's sequential passes over bf16 rows (any L >= 1): the forward's chunk factors
-// (prep kernel, into ws), the chunk-entry states (state kernel, mode 1: S_save), Nb = Q'^T dO over
-// the spent N slots, and the adjoint chain (state kernel, mode 2: dS0 and, per chunk, the adjoint
-// of its exiting state, dS_save). S_save and dS_save are fp16 [B, Hv, NC, D, D], each 32-column slice
+// (prep kernel, into ws), the chunk-entry states (state kernel, mode 1: S_save), and the adjoint
+// chain with Nb = Q'^T dO formed on its output side (state kernel, mode 2: dS0 and, per chunk, the
+// adjoint of its exiting state, dS_save). S_save and dS_save are fp16 [B, Hv, NC, D, D], each 32-column slice
 // of a state divided by the power of two in S_scale / dS_scale [B, Hv, NC, 4]; ws holds
 // chunk_bwd_units_bytes(B, L, Hv) bytes. dS_T may be NULL (zeros), dS0 NULL (not written).
 struct ChunkBwdChainLaunch {
@@ -74,7 +72,8 @@ size_t chunk_bwd_units_bytes(int B, int L, int Hv);
 cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s);
 
 // The chunked backward of bf16 rows (q, k, v, dO bf16; g, beta, S0, dS_T and every gradient
-// float32): the sequential passes above, then the chunk-local gradients and the key-head reduction.
+// float32): the sequential passes above, then the chunk-local gradients, one CTA per (row, key head,
+// chunk) taking the key head's value heads in turn and finishing dq, dk itself.
 // ws holds chunk_bwd_workspace_bytes(B, L, Hk, Hv) bytes.
 struct ChunkBackwardArgs {
   const void* q;

@@ -892,14 +892,18 @@ static_assert(kCN == kMBytes && kOPU == kQBytes, "stage layout");
 
 // kMode 0: the forward (o and S_T). kMode 1: the forward recomputed for the backward: no output
 // side; the entering state of every chunk is saved (st_save, st_scale). kMode 2: the backward's adjoint
-// chain dS <- Gamma_C dS + M'^T dS + Nb, chunks from the last to the first: the unit's N slot holds
-// Nb = Q'^T dO (in the scale block's second word's scale), the chain product reads the M' image
-// transposed (an MN-major A operand), the initial state is dS_T (a.S0), the final one dS0 (a.S_T),
-// and the adjoint entering each chunk's step (that of its exiting state) is saved likewise.
+// chain dS <- Gamma_C dS + M'^T dS + Nb, chunks from the last to the first: the chain product reads
+// the M' image transposed (an MN-major A operand); the output side forms Nb = Q'^T dO for the CTA's
+// 32 columns a step or more ahead (the output ring brings Q' and a box of dO, tm_do; the output
+// warps turn dO into fp16 divided by its power of two; warp 7 issues the product into the TMEM
+// slots the forward's O' uses) and the state warps read it from TMEM; the initial state is dS_T
+// (a.S0), the final one dS0 (a.S_T), and the adjoint entering each chunk's step (that of its
+// exiting state) is saved likewise.
 template <int CS, int OS, bool kGated, int kMode>
 __global__ void __launch_bounds__(kStateThreads, 1)
-chunk_state_kernel(const ChunkArgs a) {
-  constexpr bool kOut = kMode == 0;   // the output side (output ring, product and warps) runs
+chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do) {
+  constexpr bool kOut = kMode == 0;   // the output side forms o
+  constexpr bool kNb = kMode == 2;    // the output side forms Nb = Q'^T dO
   constexpr uint32_t kOffO = CS * kCStage;
   constexpr uint32_t kOffSb = kOffO + OS * kOStage;
   extern __shared__ uint8_t smem_raw[];
@@ -921,6 +925,12 @@ chunk_state_kernel(const ChunkArgs a) {
   __shared__ __align__(16) float w_s[kN];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  // kMode 2: doRdy[s]: the dO box of output stage s is fp16 (for the product's issuer); nbRdy[c % 8]:
+  // its scale is in nb_scl[c % 8] (for the state warps, which the output warps may lead by up to five
+  // chunks: an eight-deep ring never runs two phases ahead of them, a three-deep one would)
+  __shared__ uint64_t doRdy[OS], nbRdy[8];
+  __shared__ float nb_scl[8];
+  __shared__ uint32_t nbmax[4];
 
   const int sl = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -950,6 +960,8 @@ chunk_state_kernel(const ChunkArgs a) {
       mbar_init(&sFree[q], 1);
     }
     for (int r = 0; r < 8; ++r) mbar_init(&scRdy[r], 4);
+    for (int s2 = 0; s2 < OS; ++s2) mbar_init(&doRdy[s2], 1);
+    for (int r = 0; r < 8; ++r) mbar_init(&nbRdy[r], 1);
     if (kGated) {
       for (int q = 0; q < 2; ++q) {
         mbar_init(&fullR[q], 1);
@@ -984,7 +996,7 @@ chunk_state_kernel(const ChunkArgs a) {
     // every CTA of the row reads the same index and skips
   } else if (warp == 6 || warp == 10) {
     // ---------------- producers (lane 0): the chain ring (warp 6) and the output ring (warp 10) ---
-    if (lane == 0 && (warp == 6 || kOut)) {
+    if (lane == 0 && (warp == 6 || kOut || kNb)) {
       wait_prerequisite();   // the workspace is complete once the prep kernel has finished
       const bool chain = warp == 6;
       const int S = chain ? CS : OS;
@@ -997,15 +1009,25 @@ chunk_state_kernel(const ChunkArgs a) {
         const uint8_t* ub = unit_base(a, b, h, cu);
         if (chain) {
           uint8_t* st = sm + s * kCStage;
-          mbar_arrive_expect_tx(&chFull[s], kMBytes + 8192 + kSCopy);
+          mbar_arrive_expect_tx(&chFull[s], kMBytes + (kNb ? 0 : 8192) + kSCopy);
           bulk_load(st, ub, 16384, &chFull[s]);
           bulk_load(st + 16384, ub + 16384, 16384, &chFull[s]);
-          bulk_load(st + kCN, ub + kUnitN + sl * 8192, 8192, &chFull[s]);
+          if (!kNb) bulk_load(st + kCN, ub + kUnitN + sl * 8192, 8192, &chFull[s]);   // (Nb comes from TMEM)
           bulk_load(&gam_ring[s], ub + kUnitS, kSCopy, &chFull[s]);
           if (c + kPrefetchAhead < NC) {   // the chunk kPrefetchAhead steps further on into L2
             const uint8_t* uf = unit_base(a, b, h, kMode == 2 ? cu - kPrefetchAhead : cu + kPrefetchAhead);
             bulk_prefetch_l2(uf, kMBytes);
-            bulk_prefetch_l2(uf + kUnitN + sl * 8192, 8192);
+            if (!kNb) bulk_prefetch_l2(uf + kUnitN + sl * 8192, 8192);
+          }
+        } else if (kNb) {
+          // Q' and this CTA's 32 columns of dO (a 64 x 32 box, 64-byte swizzle) over the P U slot
+          uint8_t* st = sm + kOffO + s * kOStage;
+          mbar_arrive_expect_tx(&outFull[s], kQBytes + 4096);
+          bulk_load(st, ub + kUnitQ, kQBytes, &outFull[s]);
+          tma_load_4d(st + kOPU, &tm_do, &outFull[s], sl * kN, h, cu * kChunk, b);
+          if (c + kPrefetchAhead < NC) {
+            bulk_prefetch_l2(unit_base(a, b, h, cu - kPrefetchAhead) + kUnitQ, kQBytes);
+            tma_prefetch_4d(&tm_do, sl * kN, h, (cu - kPrefetchAhead) * kChunk, b);
           }
         } else {
           uint8_t* st = sm + kOffO + s * kOStage;
@@ -1090,17 +1112,34 @@ chunk_state_kernel(const ChunkArgs a) {
       const int cs = c % CS, p = c & 1, qn = (c + 1) % kSb;
       const uint8_t* st = sm + cs * kCStage;
       ok = ok && mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
+      if (kNb) {
+        // Nb_c = Q'_c^T dO_c in TMEM slot p (and its scale in nb_scl)
+        ok = ok && mbar_wait(&nbRdy[c & 7], (c >> 3) & 1, a.wait_budget) &&
+             mbar_wait(&bar_o[p], (c >> 1) & 1, a.wait_budget);
+        ok = __all_sync(0xffffffffu, ok);   // the TMEM load below is warp-collective
+      }
       if (ok) {
         // while the product D = M' S_c runs: S <- Gamma_C S + upV N (S_c is already in the fp16
-        // operand; N is in its chunk's v scale upV)
-        const float gc = gam_ring[cs].x, upV = gam_ring[cs].y;
-        const uint8_t* nrow = st + kCN;
+        // operand; N is in its chunk's v scale upV), or S <- Gamma_C S + Nb in the adjoint chain
+        const float gc = gam_ring[cs].x;
+        if (kNb) {
+          tc_fence_after();
+          float nb[kN];
+          tmem_ld32(tb + lane_base + 64 + 32 * p, nb);
+          const float up = nb_scl[c & 7];
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float nv[8];
-          unpack8_f16(*reinterpret_cast<const uint4*>(nrow + swz64(kr * 64 + ch * 16)), nv);
+          for (int n = 0; n < kN; ++n) Sm[n] = fmaf(gc, Sm[n], up * nb[n]);
+          tc_fence_before();
+        } else {
+          const float upV = gam_ring[cs].y;
+          const uint8_t* nrow = st + kCN;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], upV * nv[e]);
+          for (int ch = 0; ch < 4; ++ch) {
+            float nv[8];
+            unpack8_f16(*reinterpret_cast<const uint4*>(nrow + swz64(kr * 64 + ch * 16)), nv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], upV * nv[e]);
+          }
         }
         // Sb[qn] is rewritten below: the output product of chunk c + 1 - kSb must have read it
         ok = mbar_wait(&bar_d, c & 1, a.wait_budget) &&
@@ -1117,6 +1156,7 @@ chunk_state_kernel(const ChunkArgs a) {
       // every state warp reaches this barrier once per chunk, so a warp that gave up stops them all
       ok = slice_scale(ok, sc, dn);
       if (!ok) break;
+      if (kNb && tid == 0) mbar_arrive(&oFree[p]);   // the four state warps have read Nb's slot
       write_state_operand(qn, dn, c + 1, sc);
       if (tid == 0) sc_ring[(c + 1) & 7] = sc;
       fence_async_smem();
@@ -1162,7 +1202,29 @@ chunk_state_kernel(const ChunkArgs a) {
     }
   } else if (warp == 7) {
     // ---------------- output-product issuer ----------------
-    if (lane == 0 && kOut) {
+    if (lane == 0 && kNb) {
+      // Nb[p] = Q'^T dO: A = the Q' image read as an MN-major operand (keys = M in its two 64-column
+      // atoms 8 KB apart, positions = K in rows of 128 B), B = the fp16 dO box (positions = K in rows
+      // of 64 B, 64-byte swizzle, N = 32)
+      const uint32_t idesc = idesc_f16(128, kN, true, true);
+      int last = -1;
+      for (int c = 0; c < NC; ++c) {
+        const int os = c % OS, p = c & 1;
+        ok = mbar_wait(&doRdy[os], (c / OS) & 1, a.wait_budget) &&
+             (c < 2 || mbar_wait(&oFree[p], ((c - 2) >> 1) & 1, a.wait_budget));
+        if (!ok || *(volatile int*)&abort_flag) break;
+        tc_fence_after();
+        const uint32_t sq = smem_u32(sm + kOffO + os * kOStage), sd = sq + kOPU;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(tb + 64 + 32 * p, smem_desc(sq + kk * 2048, 8192, 1024),
+                   smem_desc(sd + kk * 1024, 4096, 512, kSwizzle64B), idesc, kk > 0);
+        mma_commit(&bar_o[p]);
+        mma_commit(&outFree[os]);   // the stage is read once the product completes
+        last = c;
+      }
+      if (!ok && last >= 0) mbar_wait(&bar_o[last & 1], (last >> 1) & 1, kDrainBudget);   // drain
+    } else if (lane == 0 && kOut) {
       const uint32_t idesc = idesc_f16(128, kN, false, true);
       int last = -1;   // last chunk whose output product was issued
       for (int c = 0; c < NC; ++c) {
@@ -1184,6 +1246,39 @@ chunk_state_kernel(const ChunkArgs a) {
         last = c;
       }
       if (!ok && last >= 0) mbar_wait(&bar_o[last & 1], (last >> 1) & 1, kDrainBudget);   // drain
+    }
+  } else if (kNb) {
+    // ---------------- output warps 4, 5, 8, 9 (adjoint chain): the dO box to fp16 ----------------
+    const int ot = (warp < 8 ? tid - 128 : tid - 192);   // 0 .. 127
+    const int wi = ot >> 5;
+    for (int c = 0; c < NC; ++c) {
+      const int os = c % OS;
+      ok = ok && mbar_wait(&outFull[os], (c / OS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
+      uint4* box = reinterpret_cast<uint4*>(sm + kOffO + os * kOStage + kOPU);   // 256 chunks of 16 B
+      uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+      uint32_t m2 = 0;
+      if (ok) {
+        w0 = box[ot];
+        w1 = box[ot + 128];
+        m2 = __vmaxu2(__vmaxu2(__vmaxu2(w0.x & 0x7FFF7FFFu, w0.y & 0x7FFF7FFFu), __vmaxu2(w0.z & 0x7FFF7FFFu, w0.w & 0x7FFF7FFFu)),
+                      __vmaxu2(__vmaxu2(w1.x & 0x7FFF7FFFu, w1.y & 0x7FFF7FFFu), __vmaxu2(w1.z & 0x7FFF7FFFu, w1.w & 0x7FFF7FFFu)));
+      }
+      const uint32_t mw = __reduce_max_sync(0xffffffffu, max(m2 & 0xFFFFu, m2 >> 16));
+      if (lane == 0) nbmax[wi] = mw;
+      if (!named_bar_and(kOutBar, kOutCount, ok)) break;
+      float up, dn;
+      pow2_scales(__uint_as_float(max(max(nbmax[0], nbmax[1]), max(nbmax[2], nbmax[3])) << 16), up, dn);
+      box[ot] = make_uint4(bf16x2_to_f16x2_scaled(w0.x, dn), bf16x2_to_f16x2_scaled(w0.y, dn),
+                           bf16x2_to_f16x2_scaled(w0.z, dn), bf16x2_to_f16x2_scaled(w0.w, dn));
+      box[ot + 128] = make_uint4(bf16x2_to_f16x2_scaled(w1.x, dn), bf16x2_to_f16x2_scaled(w1.y, dn),
+                                 bf16x2_to_f16x2_scaled(w1.z, dn), bf16x2_to_f16x2_scaled(w1.w, dn));
+      fence_async_smem();   // generic writes, then the product (async proxy) reads them
+      if (!named_bar_and(kOutBar, kOutCount, true)) break;
+      if (ot == 0) {
+        nb_scl[c & 7] = up;
+        mbar_arrive(&nbRdy[c & 7]);
+        mbar_arrive(&doRdy[os]);
+      }
     }
   } else if (kOut) {
     // ---------------- output warps 4, 5, 8, 9 ----------------
@@ -1304,124 +1399,6 @@ chunk_state_kernel(const ChunkArgs a) {
 }
 
 // -------------------------------------------------------------------------------------------
-// Backward: Nb = Q'^T dO per unit, the adjoint chain's inhomogeneous term
-// -------------------------------------------------------------------------------------------
-// One CTA per (row, value head, chunk) unit. Q' (the unit's fp16 image, positions x keys, K-major)
-// read transposed is an MN-major A operand (keys = M in its two 64-column atoms, positions = K);
-// the dO tile (positions x values, TMA with 128-byte swizzle) is an MN-major B operand once
-// converted to fp16, divided by the power of two of its largest magnitude. Nb (keys x values) is
-// written over the unit's N slot, which the forward state pass has consumed, in N's four 32-column
-// slices, and the scale (that power of two) into the scale block's second word, where the state
-// kernel takes N's scale from. Gamma_C in the first word stays.
-constexpr int kNbThreads = 128;
-constexpr uint32_t kNbSmem = 16384 + 16384 + 32768 + 1024;   // Q', dO, Nb staging, alignment
-
-__global__ void __launch_bounds__(kNbThreads)
-chunk_nb_kernel(const __grid_constant__ CUtensorMap tm_do, const ChunkArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_ld, bar_mma;
-  __shared__ uint32_t tmem_base;
-  __shared__ uint32_t wmax[kNbThreads / 32];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int u = blockIdx.x;
-  const int c = u % a.NC, h = (u / a.NC) % a.Hv, b = u / (a.NC * a.Hv);
-  uint8_t* ub = unit_base(a, b, h, c);
-  uint8_t* sq = sm;              // Q' image: atoms (keys 0-63, 64-127) of 64 positions x 128 B
-  uint8_t* sd = sm + 16384;      // dO: two 64 x 64 boxes (values 0-63, 64-127)
-  uint8_t* sn = sm + 32768;      // Nb staging: four 32-column slices of 128 rows x 64 B
-  if (tid == 0) {
-    mbar_init(&bar_ld, 1);
-    mbar_init(&bar_mma, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(&tmem_base, 128);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = tmem_base;
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bar_ld, 2 * 16384);
-    bulk_load(sq, ub + kUnitQ, kQBytes, &bar_ld);
-    tma_load_4d(sd, &tm_do, &bar_ld, 0, h, c * kChunk, b);
-    tma_load_4d(sd + 8192, &tm_do, &bar_ld, 64, h, c * kChunk, b);
-  }
-  const bool ld_ok = mbar_wait(&bar_ld, 0, a.wait_budget);
-  bool ok = __syncthreads_and(ld_ok);
-  float up = 1.f, dn = 1.f;
-  if (ok) {
-    // dO's largest magnitude (bf16 magnitude bits order like the values), then dO / 2^e as fp16
-    uint32_t m2 = 0;
-    for (int c16 = tid; c16 < 1024; c16 += kNbThreads) {
-      const uint4 w = reinterpret_cast<const uint4*>(sd)[c16];
-      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu), __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
-    }
-    const uint32_t mw = __reduce_max_sync(0xffffffffu, max(m2 & 0xFFFFu, m2 >> 16));
-    if (lane == 0) wmax[warp] = mw;
-    __syncthreads();
-    pow2_scales(__uint_as_float(max(max(wmax[0], wmax[1]), max(wmax[2], wmax[3])) << 16), up, dn);
-    for (int c16 = tid; c16 < 1024; c16 += kNbThreads) {
-      uint4* pw = reinterpret_cast<uint4*>(sd) + c16;
-      const uint4 w = *pw;
-      *pw = make_uint4(bf16x2_to_f16x2_scaled(w.x, dn), bf16x2_to_f16x2_scaled(w.y, dn),
-                       bf16x2_to_f16x2_scaled(w.z, dn), bf16x2_to_f16x2_scaled(w.w, dn));
-    }
-    fence_async_smem();
-    tc_fence_before();
-  }
-  __syncthreads();
-  if (ok && tid == 0) {
-    // D[keys, values] = Q'^T dO: M = 128 (two 64-key blocks 8 KB apart), N = 128 (two 64-value
-    // blocks 8 KB apart), K = 64 positions in steps of 16 rows (2 KB)
-    tc_fence_after();
-    const uint32_t idesc = idesc_f16(128, 128, true, true);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      mma_bf16(tb, smem_desc(smem_u32(sq) + kk * 2048, 8192, 1024), smem_desc(smem_u32(sd) + kk * 2048, 8192, 1024),
-               idesc, kk > 0);
-    mma_commit(&bar_mma);
-  }
-  const bool issued = ok;   // the product was committed (tid 0 issues it exactly when ok)
-  ok = __syncthreads_and(ok && mbar_wait(&bar_mma, 0, a.wait_budget));
-  if (ok) {
-    tc_fence_after();
-    // key row i = tid = TMEM lane; its 128 values into the four slices
-    const int i = tid;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float w[64];
-      tmem_ld64(tb + lane_base + 64 * half, w);
-#pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        const int col = 64 * half + 8 * q8;
-        *reinterpret_cast<uint4*>(sn + (col >> 5) * 8192 + swz64(i * 64 + (q8 & 3) * 16)) = pack8_f16(w + 8 * q8);
-      }
-    }
-    fence_async_smem();
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (ok && tid == 0) {
-    bulk_store(ub + kUnitN, sn, kNBytes);
-    bulk_commit();
-    *reinterpret_cast<float*>(ub + kUnitS + 4) = up;   // N's scale for the adjoint chain
-    bulk_wait_all();
-  }
-  if (!ok && tid == 0) {
-    // drain what is still in flight before the CTA's memory is released
-    set_error(a.err, kErrTimeout);
-    if (!ld_ok) mbar_wait(&bar_ld, 0, kDrainBudget);
-    if (issued) mbar_wait(&bar_mma, 0, kDrainBudget);
-  }
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tb, 128);
-  }
-}
-
-// -------------------------------------------------------------------------------------------
 // Host side
 // -------------------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1437,17 +1414,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [B, L, H, 128] bf16 tensor, box {64 columns, 1 head, 64 positions, 1 row}, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int B, int L, int H) {
+// [B, L, H, 128] bf16 tensor, box {width columns, 1 head, 64 positions, 1 row}: 64 columns with
+// 128-byte swizzle (the prep kernel's tiles) or 32 with 64-byte swizzle (the adjoint chain's dO box).
+bool make_map(CUtensorMap* m, const void* base, int B, int L, int H, int width = 64) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2, (cuuint64_t)L * H * kD * 2};
-  cuuint32_t box[4] = {64, 1, 64, 1};
+  cuuint32_t box[4] = {(cuuint32_t)width, 1, 64, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_INTERLEAVE_NONE, width == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // SMs of the current device (cached per device ordinal)
@@ -1543,8 +1521,9 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.z ? 2 : 1;
-  e = p.z ? cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, true, 0>, a)
-          : cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 0>, a);
+  const CUtensorMap no_map{};   // (the forward's state kernel reads no dO)
+  e = p.z ? cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, true, 0>, a, no_map)
+          : cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 0>, a, no_map);
   stage_timer_end(slot, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1555,7 +1534,7 @@ size_t chunk_bwd_units_bytes(int B, int L, int Hv) { return units_bytes(B, L, Hv
 cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s) {
   CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, p.q, p.B, p.L, p.Hk) || !make_map(&mk, p.k, p.B, p.L, p.Hk) ||
-      !make_map(&mv, p.v, p.B, p.L, p.Hv) || !make_map(&mo, p.dO, p.B, p.L, p.Hv))
+      !make_map(&mv, p.v, p.B, p.L, p.Hv) || !make_map(&mo, p.dO, p.B, p.L, p.Hv, kN))
     return cudaErrorInvalidValue;
   ChunkArgs a{};
   a.g = p.g;
@@ -1577,7 +1556,6 @@ cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s)
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(chunk_state_kernel<3, 3, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              state_smem(3, 3));
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(chunk_nb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kNbSmem);
   if (e != cudaSuccess) return e;
   // 1. the forward's chunk factors
   const long long units = (long long)a.B * a.Hv * a.NC;
@@ -1599,22 +1577,19 @@ cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s)
   a.st_save = p.S_save;
   a.st_scale = p.S_scale;
   a.S_T = nullptr;
+  const CUtensorMap no_map{};   // (the forward pass reads no dO)
   slot = stage_timer_begin(s, kKernChunkState);
-  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 1>, a);
+  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 1>, a, no_map);
   stage_timer_end(slot, s);
   if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
-  // 3. Nb = Q'^T dO over the N slots the state pass has read
-  slot = stage_timer_begin(s, kKernChunkNb);
-  chunk_nb_kernel<<<(unsigned)units, kNbThreads, kNbSmem, s>>>(mo, a);
-  stage_timer_end(slot, s);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // 4. the adjoint chain: dS_T in, dS0 out, the adjoint entering each chunk's step saved
+  // 3. the adjoint chain (Nb = Q'^T dO formed on its output side): dS_T in, dS0 out, the adjoint
+  //    entering each chunk's step saved
   a.S0 = p.dS_T;
   a.S_T = p.dS0;
   a.st_save = p.dS_save;
   a.st_scale = p.dS_scale;
   slot = stage_timer_begin(s, kKernChunkAdjoint);
-  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 2>, a);
+  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 2>, a, mo);
   stage_timer_end(slot, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

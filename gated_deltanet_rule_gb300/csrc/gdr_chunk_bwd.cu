@@ -63,8 +63,7 @@ constexpr uint32_t kOX2 = kOX1 + kT128;          // W, then dDelta
 constexpr uint32_t kOTf = kOX2 + kT128;          // fp32 A (strictly lower)
 constexpr uint32_t kOT16 = kOTf + 64 * kLf * 4;  // T (fp16)
 constexpr uint32_t kOP16 = kOT16 + kT64;         // P (fp16)
-constexpr uint32_t kOG16 = kOP16 + kT64;         // K^ K^T (fp16)
-constexpr uint32_t kOVec = kOG16 + kT64;         // per-position vectors and reduction scratch
+constexpr uint32_t kOVec = kOP16 + kT64;         // per-position vectors and reduction scratch
 constexpr int kNVec = 26;
 constexpr uint32_t kLocalSmem = kOVec + kNVec * 64 * 4;
 // vectors (64 floats each)
@@ -211,8 +210,8 @@ struct LocalArgs {
   const float* S_scale;
   const __half* dS_save;  // likewise for the adjoints
   const float* dS_scale;
-  float* dqt;             // [B, L, Hv, D]: gradient of q~ per value head
-  float* dkh;             // [B, L, Hv, D]: gradient of k^ per value head
+  float* dq;              // [B, L, Hk, D]
+  float* dk;
   float* dv;
   float* dg;
   float* dbeta;
@@ -225,8 +224,8 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
   float* vec = reinterpret_cast<float*>(sm + kOVec);
   auto V = [&](int i) { return vec + i * 64; };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = u % a.NC, h = (u / a.NC) % a.Hv, b = u / (a.NC * a.Hv);
-  const int hk = h / (a.Hv / a.Hk);
+  const int c = u % a.NC, hk = (u / a.NC) % a.Hk, b = u / (a.NC * a.Hk);
+  const int r = a.Hv / a.Hk;
   const int m0 = 16 * (warp & 3), quarter = warp >> 2;
   const int n128 = 32 * quarter, n64 = 16 * quarter;
   const int p0 = c * kChunk;   // first position of the chunk
@@ -241,9 +240,72 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
   float* Af = reinterpret_cast<float*>(sm + kOTf);
   uint8_t* tT = sm + kOT16;
   uint8_t* tP = sm + kOP16;
-  uint8_t* tG = sm + kOG16;
 
-  // ---- 0. inputs: gates, raw q k v dO rows (zero past L), S and dS' (fp32 -> fp16 scaled) ----
+  // ---- prologue (once per key head): raw q, k rows, their inverse norms, the Gram products
+  //      K K^T and Q K^T from the raw bf16 rows (kept in registers: every value head's A and P are
+  //      elementwise in them), then q^ = q / |q|, k^ = k / |k| as fp16 (q~ = q^ 128^-0.5) ----
+#pragma unroll
+  for (int it = 0; it < 2 * 1024 / kLT; ++it) {
+    const int idx = tid + kLT * it;
+    const int which = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
+    const int pos = p0 + row;
+    const size_t ro = pos < a.L ? (((size_t)b * a.L + pos) * a.Hk + hk) * kD : 0;
+    cp_async16_zfill((which ? tK : tQ) + row * kLd * 2 + ch * 16,
+                     reinterpret_cast<const uint4*>((which ? a.k : a.q) + ro) + ch, pos < a.L ? 16 : 0);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  if (tid < 128) {
+    // inverse norms of the raw q, k rows (threads 0-63: q, 64-127: k)
+    const int row = tid & 63;
+    const uint8_t* src = (tid < 64 ? tQ : tK) + row * kLd * 2;
+    float s0 = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < 16; ++ch) {
+      const uint4 w = *reinterpret_cast<const uint4*>(src + ch * 16);
+      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xFFFF0000u);
+        s0 = fmaf(lo, lo, fmaf(hi, hi, s0));
+      }
+    }
+    V(tid < 64 ? vSq : vSk)[row] = rsqrtf(s0 + 1e-6f);
+  }
+  float G[2][4], Gq[2][4];
+  zero(G);
+  zero(Gq);
+  tile_mma<2, false, true, true>(G, tK, kLd, m0, tK, kLd, n64, 128, lane);
+  tile_mma<2, false, true, true>(Gq, tQ, kLd, m0, tK, kLd, n64, 128, lane);
+  __syncthreads();   // the norms are in; the raw rows are read
+  const float* sq = V(vSq);
+  const float* sk = V(vSk);
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = frow(m0, lane, e), j = fcol(n64, lane, nt, e);
+      G[nt][e] *= sk[i] * sk[j];                 // k^_i . k^_j
+      Gq[nt][e] *= kQs * sq[i] * sk[j];          // q~_i . k^_j
+    }
+  for (int idx = tid; idx < 2 * 1024; idx += kLT) {
+    const int which = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
+    uint4* p = reinterpret_cast<uint4*>((which ? tK : tQ) + row * kLd * 2 + ch * 16);
+    const float sc = V(which ? vSk : vSq)[row];
+    const uint4 w = *p;
+    *p = make_uint4(bf16x2_to_f16x2_scaled(w.x, sc), bf16x2_to_f16x2_scaled(w.y, sc),
+                    bf16x2_to_f16x2_scaled(w.z, sc), bf16x2_to_f16x2_scaled(w.w, sc));
+  }
+  float dK[4][4], dQ[4][4];   // summed over the key head's value heads
+  zero(dK);
+  zero(dQ);
+
+  for (int jh = 0; jh < r; ++jh) {
+  const int h = hk * r + jh;
+  __syncthreads();   // the previous value head's tiles are spent (and q^, k^ are in)
+
+  // ---- 0. the value head's inputs: gates, v and dO rows (zero past L), S and dS' (fp16) ----
   if (tid < 64) {
     const int pos = p0 + tid;
     const size_t gi = ((size_t)b * a.L + pos) * a.Hv + h;
@@ -258,20 +320,15 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
     V(vScan)[tid] = x;
   }
   {
-    // 64 rows x 16 chunks of 16 bytes for each of q, k (key head hk) and v, dO (value head h), as
-    // asynchronous copies (rows past L are zero-filled)
 #pragma unroll
-    for (int it = 0; it < 4 * 1024 / kLT; ++it) {
+    for (int it = 0; it < 2 * 1024 / kLT; ++it) {
       const int idx = tid + kLT * it;
       const int which = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
       const int pos = p0 + row;
-      const __nv_bfloat16* src = which == 0 ? a.q : which == 1 ? a.k : which == 2 ? a.v : a.dO;
-      const int H = which < 2 ? a.Hk : a.Hv, hh = which < 2 ? hk : h;
-      const size_t r = pos < a.L ? (((size_t)b * a.L + pos) * H + hh) * kD : 0;
-      uint8_t* dst = which == 0 ? tQ : which == 1 ? tK : which == 2 ? tV : tO;
-      cp_async16_zfill(dst + row * kLd * 2 + ch * 16, reinterpret_cast<const uint4*>(src + r) + ch, pos < a.L ? 16 : 0);
+      const size_t ro = pos < a.L ? (((size_t)b * a.L + pos) * a.Hv + h) * kD : 0;
+      cp_async16_zfill((which ? tO : tV) + row * kLd * 2 + ch * 16,
+                       reinterpret_cast<const uint4*>((which ? a.dO : a.v) + ro) + ch, pos < a.L ? 16 : 0);
     }
-    // S and dS' (fp16 key rows of 256 bytes) straight into their tiles
     const size_t unit = ((size_t)b * a.Hv + h) * a.NC + c;
 #pragma unroll
     for (int it = 0; it < 2 * 2048 / kLT; ++it) {
@@ -292,24 +349,8 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
   if (tid < 64) {
     V(vGam)[tid] = exp2f(V(vG2)[tid]);
     V(vE)[tid] = exp2f(V(vG2)[63] - V(vG2)[tid]);
-  } else if (tid < 192) {
-    // inverse norms of the raw q, k rows (threads 64-127: q, 128-191: k)
-    const int row = tid & 63;
-    const uint8_t* src = (tid < 128 ? tQ : tK) + row * kLd * 2;
-    float s0 = 0.f;
-#pragma unroll
-    for (int ch = 0; ch < 16; ++ch) {
-      const uint4 w = *reinterpret_cast<const uint4*>(src + ch * 16);
-      const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xFFFF0000u);
-        s0 = fmaf(lo, lo, fmaf(hi, hi, s0));
-      }
-    }
-    V(tid < 128 ? vSq : vSk)[row] = rsqrtf(s0 + 1e-6f);
   }
-  __syncthreads();   // the norms and decays are in
+  __syncthreads();   // the decays are in
 
   // per-thread partial sums: rows (this warp's column quarter, unshuffled) and columns of the 64 x 64
   // products (this thread's two rows)
@@ -322,27 +363,16 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
   const float* bet = V(vBet);
   auto Eij = [&](int i, int j) { return exp2f(gam2[i] - gam2[j]); };   // j <= i only
 
-  // ---- 1. Gram products from the raw bf16 rows: A (fp32), K^ K^T and P (fp16) ----
-  {
-    float G[2][4], Gq[2][4];
-    zero(G);
-    zero(Gq);
-    tile_mma<2, false, true, true>(G, tK, kLd, m0, tK, kLd, n64, 128, lane);
-    tile_mma<2, false, true, true>(Gq, tQ, kLd, m0, tK, kLd, n64, 128, lane);
-    const float* sq = V(vSq);
-    const float* sk = V(vSk);
+  // ---- 1. A (fp32, 1 on the diagonal) and P (fp16) from the Gram products ----
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+  for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = frow(m0, lane, e), j = fcol(n64, lane, nt, e);
-        const float kk = sk[i] * sk[j] * G[nt][e];
-        const float E = j <= i ? Eij(i, j) : 0.f;
-        Af[i * kLf + j] = j < i ? bet[i] * kk * E : (j == i ? 1.f : 0.f);   // 1 on the diagonal
-        reinterpret_cast<__half*>(tG)[i * kLs + j] = __float2half_rn(kk);
-        reinterpret_cast<__half*>(tP)[i * kLs + j] = __float2half_rn(kQs * sq[i] * sk[j] * Gq[nt][e] * E);
-      }
-  }
+    for (int e = 0; e < 4; ++e) {
+      const int i = frow(m0, lane, e), j = fcol(n64, lane, nt, e);
+      const float E = j <= i ? Eij(i, j) : 0.f;
+      Af[i * kLf + j] = j < i ? bet[i] * G[nt][e] * E : (j == i ? 1.f : 0.f);
+      reinterpret_cast<__half*>(tP)[i * kLs + j] = __float2half_rn(Gq[nt][e] * E);
+    }
   // the largest |v|, |dO| (bf16 magnitude bits order like the values); S and dS' to one power of
   // two per tile (their slices' largest), <S, dS'>
   float mx[4] = {0.f, 0.f, 0.f, 0.f}, dot = 0.f;
@@ -400,16 +430,6 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
                      bf16x2_to_f16x2_scaled(wv.z, dnV), bf16x2_to_f16x2_scaled(wv.w, dnV));
     *po = make_uint4(bf16x2_to_f16x2_scaled(wo.x, dnO), bf16x2_to_f16x2_scaled(wo.y, dnO),
                      bf16x2_to_f16x2_scaled(wo.z, dnO), bf16x2_to_f16x2_scaled(wo.w, dnO));
-  }
-  __syncthreads();
-  // raw rows -> fp16 unit rows q^ = q / |q|, k^ = k / |k| (q~ = q^ 128^-0.5)
-  for (int idx = tid; idx < 2 * 1024; idx += kLT) {
-    const int which = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
-    uint4* p = reinterpret_cast<uint4*>((which ? tK : tQ) + row * kLd * 2 + ch * 16);
-    const float s = V(which ? vSk : vSq)[row];
-    const uint4 w = *p;
-    *p = make_uint4(bf16x2_to_f16x2_scaled(w.x, s), bf16x2_to_f16x2_scaled(w.y, s),
-                    bf16x2_to_f16x2_scaled(w.z, s), bf16x2_to_f16x2_scaled(w.w, s));
   }
   __syncthreads();
 
@@ -485,17 +505,16 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
   pow2_up_dn(cta_max(absmax(acc), V(vMax), warp, lane), updD, dndD);
   store_h(tX2, kLd, m0, n128, acc, dndD, lane);                          // dDelta / 2^edD (W is spent)
 
-  // ---- 5. dK^ = diag(e) Delta dS'^T (the first of its terms) ----
-  float dK[4][4], dQ[4][4];
-  zero(dK);
-  tile_mma<4, false, true>(dK, tX1, kLd, m0, tD, kLd, n128, 128, lane);
+  // ---- 5. dK^ += diag(e) Delta dS'^T ----
+  zero(acc2);
+  tile_mma<4, false, true>(acc2, tX1, kLd, m0, tD, kLd, n128, 128, lane);
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) dK[nt][e] *= ev[frow(m0, lane, e)] * upDl * upD;
+    for (int e = 0; e < 4; ++e) dK[nt][e] += acc2[nt][e] * ev[frow(m0, lane, e)] * upDl * upD;
   __syncthreads();   // dDelta is stored; dS' is read by every warp (its tile is reused below)
 
-  // ---- 6. dW = -dDelta S^T; dQ~ = diag(Gamma) dO S^T; the rows Gamma_i q~_i . (dO S^T)_i ----
+  // ---- 6. dW = -dDelta S^T; dQ~ += diag(Gamma) dO S^T; the rows Gamma_i q~_i . (dO S^T)_i ----
   zero(acc);
   tile_mma<4, false, true>(acc, tX2, kLd, m0, tS, kLd, n128, 128, lane);
 #pragma unroll
@@ -506,16 +525,16 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
   pow2_up_dn(cta_max(absmax(acc), V(vMax), warp, lane), updW, dndW);
   uint8_t* tdW = tD;   // dS' is spent
   store_h(tdW, kLd, m0, n128, acc, dndW, lane);
-  zero(dQ);
-  tile_mma<4, false, true>(dQ, tO, kLd, m0, tS, kLd, n128, 128, lane);
+  zero(acc2);
+  tile_mma<4, false, true>(acc2, tO, kLd, m0, tS, kLd, n128, 128, lane);
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int i = frow(m0, lane, e), col = fcol(n128, lane, nt, e);
-      const float x = upO * upS * dQ[nt][e];
+      const float x = upO * upS * acc2[nt][e];
       rg[e >> 1] += Gam[i] * kQs * h2f(tQ, kLd, i, col) * x;
-      dQ[nt][e] = Gam[i] * x;
+      dQ[nt][e] += Gam[i] * x;
     }
   __syncthreads();   // S is spent (its tile holds dPE, dT and Z below)
 
@@ -620,7 +639,7 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
         float dAt = 0.f;   // dA~ = dA beta_i E_ij
         if (j < i) {
           const float dA = -upT * upZ * t1[nt][e];
-          const float E = Eij(i, j), gk = h2f(tG, kLs, i, j);   // k^_i . k^_j
+          const float E = Eij(i, j), gk = G[nt][e];   // k^_i . k^_j (the Gram fragment has this tiling)
           rb[e >> 1] += dA * gk * E;
           const float aa = dA * bet[i] * gk * E;                  // dA o A
           rg[e >> 1] += aa;
@@ -711,75 +730,74 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
       a.dbeta[gi] = (V(vRowB0)[i] + V(vRowB0 + 1)[i]) + (V(vRowB0 + 2)[i] + V(vRowB0 + 3)[i]);
     }
   }
+  }   // value heads
+
+  // ---- the normalisations' backward: q~ = q s_q 128^-0.5, k^ = k s_k, from the raw bf16 rows:
+  //      dq = 128^-0.5 (s_q dq~ - s_q^3 (q . dq~) q), dk = s_k dk^ - s_k^3 (k . dk^) k ----
+  {
+    float xq[4][4], xk[4][4];
+    float rq[2] = {0.f, 0.f}, rk[2] = {0.f, 0.f};
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int i = frow(m0, lane, 2 * hh), col = fcol(n128, lane, nt, 0);
-      if (p0 + i < a.L) {
-        const size_t o = (((size_t)b * a.L + p0 + i) * a.Hv + h) * kD + col;
-        *reinterpret_cast<float2*>(a.dqt + o) = make_float2(dQ[nt][2 * hh], dQ[nt][2 * hh + 1]);
-        *reinterpret_cast<float2*>(a.dkh + o) = make_float2(dK[nt][2 * hh], dK[nt][2 * hh + 1]);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i = frow(m0, lane, 2 * hh), col = fcol(n128, lane, nt, 0);
+        float2 qv = make_float2(0.f, 0.f), kv = qv;
+        if (p0 + i < a.L) {
+          const size_t o = (((size_t)b * a.L + p0 + i) * a.Hk + hk) * kD + col;
+          qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(a.q + o));
+          kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(a.k + o));
+        }
+        xq[nt][2 * hh] = qv.x;
+        xq[nt][2 * hh + 1] = qv.y;
+        xk[nt][2 * hh] = kv.x;
+        xk[nt][2 * hh + 1] = kv.y;
+        rq[hh] += qv.x * dQ[nt][2 * hh] + qv.y * dQ[nt][2 * hh + 1];
+        rk[hh] += kv.x * dK[nt][2 * hh] + kv.y * dK[nt][2 * hh + 1];
+      }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        rq[hh] += __shfl_xor_sync(0xffffffffu, rq[hh], o);
+        rk[hh] += __shfl_xor_sync(0xffffffffu, rk[hh], o);
+      }
+    __syncthreads();   // the last value head's reads of the vectors are done
+    if ((lane & 3) == 0) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i = m0 + (lane >> 2) + 8 * hh;
+        V(vRowG0 + quarter)[i] = rq[hh];
+        V(vRowB0 + quarter)[i] = rk[hh];
       }
     }
+    __syncthreads();
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i = frow(m0, lane, 2 * hh), col = fcol(n128, lane, nt, 0);
+        if (p0 + i >= a.L) continue;
+        const float tq = (V(vRowG0)[i] + V(vRowG0 + 1)[i]) + (V(vRowG0 + 2)[i] + V(vRowG0 + 3)[i]);
+        const float tk = (V(vRowB0)[i] + V(vRowB0 + 1)[i]) + (V(vRowB0 + 2)[i] + V(vRowB0 + 3)[i]);
+        const float s_q = sq[i], s_k = sk[i];
+        const size_t o = (((size_t)b * a.L + p0 + i) * a.Hk + hk) * kD + col;
+        *reinterpret_cast<float2*>(a.dq + o) =
+            make_float2(kQs * (s_q * dQ[nt][2 * hh] - s_q * s_q * s_q * tq * xq[nt][2 * hh]),
+                        kQs * (s_q * dQ[nt][2 * hh + 1] - s_q * s_q * s_q * tq * xq[nt][2 * hh + 1]));
+        *reinterpret_cast<float2*>(a.dk + o) =
+            make_float2(s_k * dK[nt][2 * hh] - s_k * s_k * s_k * tk * xk[nt][2 * hh],
+                        s_k * dK[nt][2 * hh + 1] - s_k * s_k * s_k * tk * xk[nt][2 * hh + 1]);
+      }
+  }
 }
 
-// One CTA per unit (the unit's tiles take most of an SM's shared memory).
+// One CTA per (row, key head, chunk) (its tiles take most of an SM's shared memory).
 __global__ void __launch_bounds__(kLT, 1) chunk_bwd_local_kernel(const LocalArgs a) {
   static_assert(kLT == 512, "the warp tiling assumes 16 warps");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   local_unit(a, sm, blockIdx.x);
-}
-
-// One (row, position, key head) per warp, four key dimensions per lane: the sums over the value
-// heads of the key head, then the normalisations' backward (q~ = q s_q 128^-0.5, k^ = k s_k); the
-// row sums by warp shuffles in a fixed order.
-constexpr int kRedWarps = 8;
-__global__ void __launch_bounds__(kRedWarps * 32) chunk_bwd_reduce_kernel(const LocalArgs a, float* dq, float* dk) {
-  const int lane = threadIdx.x & 31;
-  const size_t item = (size_t)blockIdx.x * kRedWarps + (threadIdx.x >> 5);   // (b L + position) Hk + hk
-  if (item >= (size_t)a.B * a.L * a.Hk) return;
-  const size_t bt = item / a.Hk;
-  const int hk = (int)(item - bt * a.Hk);
-  const int r = a.Hv / a.Hk;
-  float4 dq4 = make_float4(0.f, 0.f, 0.f, 0.f), dk4 = dq4;
-  for (int j = 0; j < r; ++j) {
-    const size_t o = (bt * a.Hv + (size_t)hk * r + j) * kD + 4 * lane;
-    const float4 x = __ldg(reinterpret_cast<const float4*>(a.dqt + o));
-    const float4 y = __ldg(reinterpret_cast<const float4*>(a.dkh + o));
-    dq4.x += x.x; dq4.y += x.y; dq4.z += x.z; dq4.w += x.w;
-    dk4.x += y.x; dk4.y += y.y; dk4.z += y.z; dk4.w += y.w;
-  }
-  const size_t off = item * kD + 4 * lane;
-  const uint2 qw = __ldg(reinterpret_cast<const uint2*>(a.q + off));
-  const uint2 kw = __ldg(reinterpret_cast<const uint2*>(a.k + off));
-  const float qv[4] = {__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xFFFF0000u), __uint_as_float(qw.y << 16),
-                       __uint_as_float(qw.y & 0xFFFF0000u)};
-  const float kv[4] = {__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u), __uint_as_float(kw.y << 16),
-                       __uint_as_float(kw.y & 0xFFFF0000u)};
-  const float dqv[4] = {dq4.x, dq4.y, dq4.z, dq4.w}, dkv[4] = {dk4.x, dk4.y, dk4.z, dk4.w};
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    s[0] = fmaf(qv[e], qv[e], s[0]);
-    s[1] = fmaf(qv[e], dqv[e], s[1]);
-    s[2] = fmaf(kv[e], kv[e], s[2]);
-    s[3] = fmaf(kv[e], dkv[e], s[3]);
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s[j] += __shfl_xor_sync(0xffffffffu, s[j], o);
-  const float sq = rsqrtf(s[0] + 1e-6f), sk = rsqrtf(s[2] + 1e-6f);
-  float oq[4], ok[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    oq[e] = kQs * (sq * dqv[e] - sq * sq * sq * s[1] * qv[e]);
-    ok[e] = sk * dkv[e] - sk * sk * sk * s[3] * kv[e];
-  }
-  *reinterpret_cast<float4*>(dq + off) = make_float4(oq[0], oq[1], oq[2], oq[3]);
-  *reinterpret_cast<float4*>(dk + off) = make_float4(ok[0], ok[1], ok[2], ok[3]);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -791,15 +809,13 @@ size_t chunk_bwd_workspace_bytes(int B, int L, int Hk, int Hv) {
   const size_t NC = ((size_t)L + kChunk - 1) / kChunk;
   const size_t states = (size_t)B * Hv * NC * kD * kD * sizeof(__half);
   const size_t scales = (size_t)B * Hv * NC * kStateSlices * sizeof(float);
-  const size_t parts = (size_t)B * L * Hv * kD * sizeof(float);
-  return align256(chunk_bwd_units_bytes(B, L, Hv)) + 2 * align256(states) + 2 * align256(scales) + 2 * align256(parts);
+  return align256(chunk_bwd_units_bytes(B, L, Hv)) + 2 * align256(states) + 2 * align256(scales);
 }
 
 cudaError_t launch_chunk_backward(const ChunkBackwardArgs& p, cudaStream_t s) {
   const size_t NC = ((size_t)p.L + kChunk - 1) / kChunk;
   const size_t states = (size_t)p.B * p.Hv * NC * kD * kD * sizeof(__half);
   const size_t scales = (size_t)p.B * p.Hv * NC * kStateSlices * sizeof(float);
-  const size_t parts = (size_t)p.B * p.L * p.Hv * kD * sizeof(float);
   uint8_t* w = static_cast<uint8_t*>(p.ws);
   uint8_t* unit_ws = w;
   w += align256(chunk_bwd_units_bytes(p.B, p.L, p.Hv));
@@ -810,25 +826,18 @@ cudaError_t launch_chunk_backward(const ChunkBackwardArgs& p, cudaStream_t s) {
   float* S_scale = reinterpret_cast<float*>(w);
   w += align256(scales);
   float* dS_scale = reinterpret_cast<float*>(w);
-  w += align256(scales);
-  float* dqt = reinterpret_cast<float*>(w);
-  float* dkh = reinterpret_cast<float*>(w + align256(parts));
   ChunkBwdChainLaunch cl{p.q, p.k, p.v, p.g, p.beta, p.S0, p.dO, p.dS_T, p.dS0, S_save, S_scale, dS_save, dS_scale,
                          unit_ws, p.B, p.L, p.Hk, p.Hv, p.err};
   cudaError_t e = launch_chunk_bwd_chain(cl, s);
   if (e != cudaSuccess) return e;
   LocalArgs la{static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k),
                static_cast<const __nv_bfloat16*>(p.v), p.g, p.beta, static_cast<const __nv_bfloat16*>(p.dO),
-               S_save, S_scale, dS_save, dS_scale, dqt, dkh, p.dv, p.dg, p.dbeta, p.B, p.L, p.Hk, p.Hv, (int)NC};
+               S_save, S_scale, dS_save, dS_scale, p.dq, p.dk, p.dv, p.dg, p.dbeta, p.B, p.L, p.Hk, p.Hv, (int)NC};
   e = cudaFuncSetAttribute(chunk_bwd_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalSmem + 128);
   if (e != cudaSuccess) return e;
+  // one CTA per (row, key head, chunk): the key head's value heads one after the other
   int slot = stage_timer_begin(s, kKernChunkBwdLocal);
-  chunk_bwd_local_kernel<<<(unsigned)((size_t)p.B * p.Hv * NC), kLT, kLocalSmem + 128, s>>>(la);
-  stage_timer_end(slot, s);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  slot = stage_timer_begin(s, kKernChunkBwdReduce);
-  const size_t items = (size_t)p.B * p.L * p.Hk;
-  chunk_bwd_reduce_kernel<<<(unsigned)((items + kRedWarps - 1) / kRedWarps), kRedWarps * 32, 0, s>>>(la, p.dq, p.dk);
+  chunk_bwd_local_kernel<<<(unsigned)((size_t)p.B * p.Hk * NC), kLT, kLocalSmem + 128, s>>>(la);
   stage_timer_end(slot, s);
   return cudaGetLastError();
 }

@@ -261,8 +261,8 @@ gdr_status gdr_backward(const void* q, const void* k, const void* v, const float
  * gradients through Delta = U - W S, P, T = (I + A)^-1, the decays and the normalisations).
  * Arguments, shapes, ownership and the no-overlap rule as for gdr_backward; dt must be GDR_BF16
  * (GDR_ERR_UNSUPPORTED otherwise). ws holds at least gdr_backward_chunked_workspace_bytes(...)
- * bytes: the forward's per-chunk factors, the chunk-entry states and adjoints (float32, 64 KiB
- * per row, value head and chunk each) and the per-value-head gradients of q~ and k^. The products
+ * bytes: the forward's per-chunk factors and the chunk-entry states and adjoints (fp16 with a power
+ * of two per 32-column slice, 32 KiB per row, value head and chunk each). The products
  * take fp16 (bf16 for the raw q, k Gram products) operands with float32 accumulation, like the
  * bf16 forward, so the result matches the float64 backward to the bf16 path's tolerance, not
  * gdr_backward's float32 one; the sums run in a fixed order (deterministic).

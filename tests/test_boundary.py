@@ -242,8 +242,7 @@ def test_varlen_and_gated_reject_bad_arguments(L):
 
 def test_chunked_backward_rejects_bad_arguments_and_sizes_its_workspace(L):
     """gdr_backward_chunked: bf16 only, the backward's host checks, and a workspace of the forward's
-    chunk factors plus the chunk-entry states and adjoints (fp16 with one scale per 32-column slice)
-    and the per-value-head q~, k^ gradients."""
+    chunk factors plus the chunk-entry states and adjoints (fp16 with one scale per 32-column slice)."""
     f = L.gdr_backward_chunked
     need = L.gdr_backward_chunked_workspace_bytes(1, 64, 2, 4, 128)
     args = lambda dt=1, dO=P, ws_bytes=need, dq=P: (P, P, P, P, P, None, dO, None, dq, P, P, P, P, None, 1, 64, 2,
@@ -259,6 +258,5 @@ def test_chunked_backward_rejects_bad_arguments_and_sizes_its_workspace(L):
         NC = -(-Lt // 64)
         units = B * Hv * NC * 98816 + 1024
         a256 = lambda x: -(-x // 256) * 256
-        want = (a256(units) + 2 * a256(B * Hv * NC * 128 * 128 * 2) + 2 * a256(B * Hv * NC * 4 * 4)
-                + 2 * a256(B * Lt * Hv * 128 * 4))
+        want = a256(units) + 2 * a256(B * Hv * NC * 128 * 128 * 2) + 2 * a256(B * Hv * NC * 4 * 4)
         assert L.gdr_backward_chunked_workspace_bytes(B, Lt, 2, Hv, 128) == want
