@@ -47,8 +47,9 @@ cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
 // The chunked backward's sequential passes over bf16 rows (any L >= 1): the forward's chunk factors
 // (prep kernel, into ws), the chunk-entry states (state kernel, mode 1: S_save), and the adjoint
 // chain with Nb = Q'^T dO formed on its output side (state kernel, mode 2: dS0 and, per chunk, the
-// adjoint of its exiting state, dS_save). S_save and dS_save are fp16 [B, Hv, NC, D, D], each 32-column slice
-// of a state divided by the power of two in S_scale / dS_scale [B, Hv, NC, 4]; ws holds
+// adjoint of its exiting state, dS_save). S_save and dS_save hold per (row, value head, chunk) four
+// fp16 images of 8 KiB, one per 32-column slice (128 key rows of 64 bytes, 64-byte swizzle), each
+// divided by its power of two in S_scale / dS_scale [B, Hv, NC, 4]; ws holds
 // chunk_bwd_units_bytes(B, L, Hv) bytes. dS_T may be NULL (zeros), dS0 NULL (not written).
 struct ChunkBwdChainLaunch {
   const void* q;
@@ -64,6 +65,7 @@ struct ChunkBwdChainLaunch {
   float* S_scale;
   __half* dS_save;
   float* dS_scale;
+  float* unit_scale;   // [B, Hv, NC, 8]: dO's four slice powers of two, then v's
   void* ws;
   int B, L, Hk, Hv;
   int* err;

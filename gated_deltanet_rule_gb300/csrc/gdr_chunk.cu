@@ -93,10 +93,14 @@ struct ChunkArgs {
   float eps;
   // state kernel modes 1 and 2 (the backward's passes): the state at the top of each chunk's step
   // (mode 1: the chunk's entering state; mode 2: the adjoint of its exiting state) as the fp16
-  // operand the step's product reads, [B, Hv, NC, D, D] with key rows and value columns, each 32-
-  // column slice divided by its own power of two, kept in st_scale [B, Hv, NC, 4]
+  // operand the step's product reads: per (row, value head, chunk) four 8 KiB images, one per
+  // 32-column slice (128 key rows of 64 bytes, 64-byte swizzle), each divided by its own power of
+  // two, kept in st_scale [B, Hv, NC, 4]
   __half* st_save;
   float* st_scale;
+  // per unit [B, Hv, NC, 8]: the powers of two of dO's four 32-column slices (kMode 2) and of v
+  // (word 4, kMode 1), for the backward's chunk-local kernel
+  float* unit_scale;
 };
 
 __device__ __forceinline__ uint8_t* unit_base(const ChunkArgs& a, int b, int h, int c) {
@@ -1082,21 +1086,20 @@ chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do)
       return all;
     };
     // fp16 state operand q: MN-major, row kr = 32 value columns (64 bytes), 64-byte swizzle. Modes 1
-    // and 2 also save it, with its scale up, as the state at the top of step `step` (if < NC).
+    // and 2 save its scale up as that of the state at the top of step `step` (if < NC); the operand
+    // itself leaves by the state-product issuer's bulk store.
     auto write_state_operand = [&](int q, float dn, int step, float up) {
-      const int cu = kMode == 2 ? NC - 1 - step : step;
-      const size_t unit = ((size_t)b * a.Hv + h) * NC + cu;
-      uint4* dst = kMode != 0 ? reinterpret_cast<uint4*>(a.st_save + (unit * kD + kr) * kD + sl * kN) : nullptr;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         float t[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) t[e] = Sm[8 * ch + e] * dn;
-        const uint4 w = pack8_f16(t);
-        *reinterpret_cast<uint4*>(sm + kOffSb + q * 8192 + swz64(kr * 64 + ch * 16)) = w;
-        if (kMode != 0 && step < NC) dst[ch] = w;
+        *reinterpret_cast<uint4*>(sm + kOffSb + q * 8192 + swz64(kr * 64 + ch * 16)) = pack8_f16(t);
       }
-      if (kMode != 0 && step < NC && kr == 0) a.st_scale[unit * kSlices + sl] = up;
+      if (kMode != 0 && step < NC && kr == 0) {
+        const int cu = kMode == 2 ? NC - 1 - step : step;
+        a.st_scale[(((size_t)b * a.Hv + h) * NC + cu) * kSlices + sl] = up;
+      }
     };
     float sc, dn;
     slice_scale(true, sc, dn);
@@ -1112,6 +1115,8 @@ chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do)
       const int cs = c % CS, p = c & 1, qn = (c + 1) % kSb;
       const uint8_t* st = sm + cs * kCStage;
       ok = ok && mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
+      if (kMode == 1 && sl == 0 && tid == 0 && ok)
+        a.unit_scale[(((size_t)b * a.Hv + h) * NC + c) * 8 + 4] = gam_ring[cs].y;   // v's power of two
       if (kNb) {
         // Nb_c = Q'_c^T dO_c in TMEM slot p (and its scale in nb_scl)
         ok = ok && mbar_wait(&nbRdy[c & 7], (c >> 3) & 1, a.wait_budget) &&
@@ -1141,9 +1146,10 @@ chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do)
             for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], upV * nv[e]);
           }
         }
-        // Sb[qn] is rewritten below: the output product of chunk c + 1 - kSb must have read it
+        // Sb[qn] is rewritten below: the output product (modes 1, 2: the bulk store) of chunk
+        // c + 1 - kSb must have read it
         ok = mbar_wait(&bar_d, c & 1, a.wait_budget) &&
-             (c + 1 < kSb || !kOut || mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget));
+             (c + 1 < kSb || mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget));
       }
       ok = __all_sync(0xffffffffu, ok);   // the TMEM load below is warp-collective
       if (ok) {
@@ -1196,9 +1202,22 @@ chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do)
         }
         mma_commit(&bar_d);
         mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
+        if (kMode != 0) {
+          // modes 1, 2: the step's operand (the state at its top, over its slice's power of two)
+          // to st_save; the previous step's buffer is free once its store has read it
+          const int cu = kMode == 2 ? NC - 1 - c : c;
+          bulk_store(a.st_save + (((size_t)b * a.Hv + h) * NC + cu) * kD * kD + sl * kD * kN, sm + kOffSb + q * 8192,
+                     8192);
+          bulk_commit();
+          if (c > 0) {
+            bulk_wait_read_but_last();
+            mbar_arrive(&sFree[(c - 1) % kSb]);
+          }
+        }
         last = c;
       }
       if (!ok && last >= 0) mbar_wait(&bar_d, last & 1, kDrainBudget);   // drain
+      if (kMode != 0) bulk_wait_all();   // the saved states are complete before the kernel ends
     }
   } else if (warp == 7) {
     // ---------------- output-product issuer ----------------
@@ -1278,6 +1297,7 @@ chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do)
         nb_scl[c & 7] = up;
         mbar_arrive(&nbRdy[c & 7]);
         mbar_arrive(&doRdy[os]);
+        a.unit_scale[(((size_t)b * a.Hv + h) * NC + (NC - 1 - c)) * 8 + sl] = up;   // dO's power of two
       }
     }
   } else if (kOut) {
@@ -1576,6 +1596,7 @@ cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s)
   cfg.numAttrs = 1;
   a.st_save = p.S_save;
   a.st_scale = p.S_scale;
+  a.unit_scale = p.unit_scale;
   a.S_T = nullptr;
   const CUtensorMap no_map{};   // (the forward pass reads no dO)
   slot = stage_timer_begin(s, kKernChunkState);

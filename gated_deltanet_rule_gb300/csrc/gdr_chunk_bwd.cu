@@ -181,24 +181,6 @@ __device__ __forceinline__ float cta_max(float m, float* vmax, int warp, int lan
   return r;
 }
 
-// CTA-wide maxima of four per-thread values at once (every thread gets them); uses vmax[0..63]
-__device__ __forceinline__ void cta_max4(float (&m)[4], float* vmax, int warp, int lane) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], o));
-  __syncthreads();
-  if (lane < 4) vmax[4 * warp + lane] = lane == 0 ? m[0] : lane == 1 ? m[1] : lane == 2 ? m[2] : m[3];
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float r = vmax[j];
-#pragma unroll
-    for (int w = 1; w < kLT / 32; ++w) r = fmaxf(r, vmax[4 * w + j]);
-    m[j] = r;
-  }
-}
-
 struct LocalArgs {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
@@ -206,10 +188,11 @@ struct LocalArgs {
   const float* g;
   const float* beta;
   const __nv_bfloat16* dO;
-  const __half* S_save;   // [B, Hv, NC, D, D] fp16, 32-column slices divided by S_scale [B, Hv, NC, 4]
+  const __half* S_save;   // per unit four 32-column slice images (fp16, each over its S_scale [B, Hv, NC, 4])
   const float* S_scale;
   const __half* dS_save;  // likewise for the adjoints
   const float* dS_scale;
+  const float* unit_scale;   // [B, Hv, NC, 8]: the powers of two of dO's four slices, then of v
   float* dq;              // [B, L, Hk, D]
   float* dk;
   float* dv;
@@ -329,13 +312,15 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
       cp_async16_zfill((which ? tO : tV) + row * kLd * 2 + ch * 16,
                        reinterpret_cast<const uint4*>((which ? a.dO : a.v) + ro) + ch, pos < a.L ? 16 : 0);
     }
+    // S and dS': four 32-column slice images of 128 key rows x 64 bytes (64-byte swizzle) each
     const size_t unit = ((size_t)b * a.Hv + h) * a.NC + c;
 #pragma unroll
     for (int it = 0; it < 2 * 2048 / kLT; ++it) {
       const int idx = tid + kLT * it;
       const int which = idx >> 11, row = (idx >> 4) & 127, ch = idx & 15;
-      const __half* src = (which ? a.dS_save : a.S_save) + (unit * kD + row) * kD;
-      cp_async16_zfill((which ? tD : tS) + row * kLd * 2 + ch * 16, reinterpret_cast<const uint4*>(src) + ch, 16);
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(which ? a.dS_save : a.S_save) + unit * (kD * kD * 2) +
+                           (ch >> 2) * 8192 + swz64(row * 64 + (ch & 3) * 16);
+      cp_async16_zfill((which ? tD : tS) + row * kLd * 2 + ch * 16, src, 16);
     }
     cp_async_commit();
   }
@@ -373,25 +358,18 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
       Af[i * kLf + j] = j < i ? bet[i] * G[nt][e] * E : (j == i ? 1.f : 0.f);
       reinterpret_cast<__half*>(tP)[i * kLs + j] = __float2half_rn(Gq[nt][e] * E);
     }
-  // the largest |v|, |dO| (bf16 magnitude bits order like the values); S and dS' to one power of
-  // two per tile (their slices' largest), <S, dS'>
-  float mx[4] = {0.f, 0.f, 0.f, 0.f}, dot = 0.f;
-  {
-    uint32_t mv = 0, mo = 0;
-    for (int idx = tid; idx < 1024; idx += kLT) {
-      const int row = idx >> 4, ch = idx & 15;
-      const uint4 wv = *reinterpret_cast<const uint4*>(tV + row * kLd * 2 + ch * 16);
-      const uint4 wo = *reinterpret_cast<const uint4*>(tO + row * kLd * 2 + ch * 16);
-      mv = __vmaxu2(mv, __vmaxu2(__vmaxu2(wv.x & 0x7FFF7FFFu, wv.y & 0x7FFF7FFFu), __vmaxu2(wv.z & 0x7FFF7FFFu, wv.w & 0x7FFF7FFFu)));
-      mo = __vmaxu2(mo, __vmaxu2(__vmaxu2(wo.x & 0x7FFF7FFFu, wo.y & 0x7FFF7FFFu), __vmaxu2(wo.z & 0x7FFF7FFFu, wo.w & 0x7FFF7FFFu)));
-    }
-    mx[0] = __uint_as_float(max(mv & 0xFFFFu, mv >> 16) << 16);
-    mx[1] = __uint_as_float(max(mo & 0xFFFFu, mo >> 16) << 16);
-  }
-  cta_max4(mx, V(vMax), warp, lane);
+  // v's and dO's powers of two (taken by the prep and adjoint-chain kernels over the same tiles: dO's
+  // is the largest of its four slices'); S and dS' to one power of two per tile (their slices'
+  // largest), <S, dS'>
+  float dot = 0.f;
   float upV, dnV, upO, dnO;
-  pow2_up_dn(mx[0], upV, dnV);
-  pow2_up_dn(mx[1], upO, dnO);
+  {
+    const float* us = a.unit_scale + (((size_t)b * a.Hv + h) * a.NC + c) * 8;
+    upV = us[4];
+    upO = fmaxf(fmaxf(us[0], us[1]), fmaxf(us[2], us[3]));
+    dnV = __uint_as_float((254u << 23) - __float_as_uint(upV));   // 1 / 2^e, exact
+    dnO = __uint_as_float((254u << 23) - __float_as_uint(upO));
+  }
   const size_t unit = ((size_t)b * a.Hv + h) * a.NC + c;
   const float4 scS = *reinterpret_cast<const float4*>(a.S_scale + unit * 4);
   const float4 scD = *reinterpret_cast<const float4*>(a.dS_scale + unit * 4);
@@ -809,7 +787,8 @@ size_t chunk_bwd_workspace_bytes(int B, int L, int Hk, int Hv) {
   const size_t NC = ((size_t)L + kChunk - 1) / kChunk;
   const size_t states = (size_t)B * Hv * NC * kD * kD * sizeof(__half);
   const size_t scales = (size_t)B * Hv * NC * kStateSlices * sizeof(float);
-  return align256(chunk_bwd_units_bytes(B, L, Hv)) + 2 * align256(states) + 2 * align256(scales);
+  const size_t uscales = (size_t)B * Hv * NC * 8 * sizeof(float);
+  return align256(chunk_bwd_units_bytes(B, L, Hv)) + 2 * align256(states) + 2 * align256(scales) + align256(uscales);
 }
 
 cudaError_t launch_chunk_backward(const ChunkBackwardArgs& p, cudaStream_t s) {
@@ -826,13 +805,15 @@ cudaError_t launch_chunk_backward(const ChunkBackwardArgs& p, cudaStream_t s) {
   float* S_scale = reinterpret_cast<float*>(w);
   w += align256(scales);
   float* dS_scale = reinterpret_cast<float*>(w);
+  w += align256(scales);
+  float* unit_scale = reinterpret_cast<float*>(w);
   ChunkBwdChainLaunch cl{p.q, p.k, p.v, p.g, p.beta, p.S0, p.dO, p.dS_T, p.dS0, S_save, S_scale, dS_save, dS_scale,
-                         unit_ws, p.B, p.L, p.Hk, p.Hv, p.err};
+                         unit_scale, unit_ws, p.B, p.L, p.Hk, p.Hv, p.err};
   cudaError_t e = launch_chunk_bwd_chain(cl, s);
   if (e != cudaSuccess) return e;
   LocalArgs la{static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k),
                static_cast<const __nv_bfloat16*>(p.v), p.g, p.beta, static_cast<const __nv_bfloat16*>(p.dO),
-               S_save, S_scale, dS_save, dS_scale, p.dq, p.dk, p.dv, p.dg, p.dbeta, p.B, p.L, p.Hk, p.Hv, (int)NC};
+               S_save, S_scale, dS_save, dS_scale, unit_scale, p.dq, p.dk, p.dv, p.dg, p.dbeta, p.B, p.L, p.Hk, p.Hv, (int)NC};
   e = cudaFuncSetAttribute(chunk_bwd_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalSmem + 128);
   if (e != cudaSuccess) return e;
   // one CTA per (row, key head, chunk): the key head's value heads one after the other

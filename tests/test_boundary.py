@@ -258,5 +258,6 @@ def test_chunked_backward_rejects_bad_arguments_and_sizes_its_workspace(L):
         NC = -(-Lt // 64)
         units = B * Hv * NC * 98816 + 1024
         a256 = lambda x: -(-x // 256) * 256
-        want = a256(units) + 2 * a256(B * Hv * NC * 128 * 128 * 2) + 2 * a256(B * Hv * NC * 4 * 4)
+        want = (a256(units) + 2 * a256(B * Hv * NC * 128 * 128 * 2) + 2 * a256(B * Hv * NC * 4 * 4)
+                + a256(B * Hv * NC * 8 * 4))
         assert L.gdr_backward_chunked_workspace_bytes(B, Lt, 2, Hv, 128) == want
