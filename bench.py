@@ -354,6 +354,8 @@ def run_gb300(args) -> dict | None:
     if world == 1 and not args.no_rows:
         line["rows"] = run_fork_decode(reps=max(3, min(args.steps, 20)), warmup=args.warmup)
         line["rows"]["next_f1_prologue"] = run_prologue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
+        line["rows"]["next_f1_prologue"]["fused_into_prefill"] = run_fused_prologue(
+            reps=max(3, min(args.steps, 20)), warmup=args.warmup)
         line["rows"]["next_f2_gated_rmsnorm"] = run_epilogue(reps=max(3, min(args.steps, 50)), warmup=args.warmup)
         line["rows"]["next_f2_gated_rmsnorm"]["fused_into_prefill"] = run_gated_prefill(
             reps=max(3, min(args.steps, 20)), warmup=args.warmup)
@@ -627,6 +629,43 @@ def run_gated_prefill(reps: int, warmup: int) -> dict:
         gdr.gdr_gated_rmsnorm(o, z, w, 1e-6, out=out, stream=stream)
 
     res = {"workload": f"prefill L={L} Hk={Hk} Hv={Hv} D={D} bf16 with S0, then the gated RMSNorm of its output"}
+    for name, fn in (("fused", fused), ("separate_pass", separate)):
+        us, kern = _time_calls(fn, reps, warmup, stream)
+        res[name] = {"us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1), "kernels": kern}
+    return res
+
+
+def run_fused_prologue(reps: int, warmup: int) -> dict:
+    """Times the GDN prologue fused into the prefill (gdr_chunk_fwd_prologue: q, k, v, g, beta formed
+    inside the chunk kernel) on the prefill row (L = 4096, 16 -> 32 heads, K = 4, with a carry and
+    S0) against gdr_prologue followed by gdr_chunk_fwd on its outputs."""
+    import torch
+    from gated_deltanet_rule_gb300 import gdr, inputs
+    K, L, Hk, Hv = 4, 4096, 16, 32
+    x = inputs.prologue_inputs(1, L, 3, Hk=Hk, Hv=Hv, K=K)
+    d = lambda t: t.cuda().contiguous()
+    mixed, w, a, b, A_log, dt_bias, tail = (d(t) for t in (x.mixed, x.conv_w, x.a, x.b, x.A_log, x.dt_bias, x.tail))
+    gen = torch.Generator().manual_seed(8)
+    S0 = (0.1 * torch.randn(1, Hv, D, D, generator=gen)).cuda()
+    pro = gdr.gdr_prologue(mixed, w, a, b, A_log, dt_bias, Hk, Hv, tail=tail)
+    o = torch.empty(1, L, Hv, D, dtype=torch.bfloat16, device="cuda")
+    S_T = torch.empty_like(S0)
+    new_tail = torch.empty_like(tail)
+    ws = torch.empty(max(gdr.workspace_bytes(1, L, Hk, Hv), gdr.prologue_workspace_bytes(1, L, Hk, Hv, K)),
+                     dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def fused(i):
+        gdr.gdr_chunk_fwd_prologue(mixed, w, a, b, A_log, dt_bias, Hk, Hv, S0=S0, tail=tail, o=o, S_T=S_T,
+                                   new_tail=new_tail, ws=ws, stream=stream)
+
+    def separate(i):
+        gdr.gdr_prologue(mixed, w, a, b, A_log, dt_bias, Hk, Hv, tail=tail, q=pro[0], k=pro[1], v=pro[2], g=pro[3],
+                         beta=pro[4], new_tail=new_tail, stream=stream)
+        gdr.gdr_chunk_fwd(pro[0], pro[1], pro[2], pro[3], pro[4], S0, o=o, S_T=S_T, ws=ws, stream=stream)
+
+    res = {"workload": f"GDN prologue (conv + SiLU, gates, carry) L={L} Hk={Hk} Hv={Hv} D={D} K={K}, then the "
+                       f"prefill with S0, bf16"}
     for name, fn in (("fused", fused), ("separate_pass", separate)):
         us, kern = _time_calls(fn, reps, warmup, stream)
         res[name] = {"us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1), "kernels": kern}

@@ -239,6 +239,65 @@ gdr_status gdr_chunk_fwd_varlen(const void* q, const void* k, const void* v, con
                    "gdr_chunk_fwd_varlen");
 }
 
+size_t gdr_chunk_fwd_prologue_workspace_bytes(int B, int L, int Hk, int Hv, int D, int K) {
+  if (B < 1 || L < 1 || Hk < 1 || Hv < 1 || D != kD || Hv % Hk != 0 || K != 4) return 0;
+  return chunk_prologue_workspace_bytes(B, L, Hv);
+}
+
+gdr_status gdr_chunk_fwd_prologue(const void* mixed, const void* tail, const float* conv_w, const float* a,
+                                  const float* b, const float* A_log, const float* dt_bias, const float* S0,
+                                  void* o, float* S_T, void* new_tail, int B, int L, int Hk, int Hv, int D,
+                                  int K, void* ws, size_t ws_bytes, gdr_stream_t stream) {
+  const char* who = "gdr_chunk_fwd_prologue";
+  if (!mixed || !conv_w || !a || !b || !A_log || !dt_bias || !o)
+    return fail(GDR_ERR_INVALID_ARG, "%s: mixed, conv_w, a, b, A_log, dt_bias and o must be non-NULL", who);
+  if (B < 1 || L < 1 || Hk < 1 || Hv < 1)
+    return fail(GDR_ERR_INVALID_ARG, "%s: sizes must be >= 1 (B=%d L=%d Hk=%d Hv=%d)", who, B, L, Hk, Hv);
+  if (Hv % Hk != 0) return fail(GDR_ERR_INVALID_ARG, "%s: Hv=%d is not a multiple of Hk=%d", who, Hv, Hk);
+  if (K < 1 || K > 8) return fail(GDR_ERR_INVALID_ARG, "%s: conv width K=%d is outside [1, 8]", who, K);
+  if (K != 4) return fail(GDR_ERR_UNSUPPORTED, "%s: the fused prologue takes a 4-tap conv (K=%d)", who, K);
+  if (D != kD) return fail(GDR_ERR_UNSUPPORTED, "%s: head dimension D=%d is not implemented (only 128)", who, D);
+  if (B > 65535 || Hv > 65535)
+    return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d or Hv=%d exceeds 65535", who, B, Hv);
+  const void* ptrs16[] = {mixed, tail, conv_w, S0, o, S_T, new_tail};
+  for (const void* p : ptrs16)
+    if (p && !aligned16(p))
+      return fail(GDR_ERR_INVALID_ARG, "%s: mixed, tail, conv_w, S0, o, S_T and new_tail must be 16-byte aligned", who);
+  const void* ptrs4[] = {a, b, A_log, dt_bias};
+  for (const void* p : ptrs4)
+    if (reinterpret_cast<uintptr_t>(p) & 3u)
+      return fail(GDR_ERR_INVALID_ARG, "%s: a, b, A_log and dt_bias must be 4-byte aligned", who);
+  // o is written while mixed and tail may still be read (the carry is gathered after the path), and
+  // new_tail is gathered from both: half-open byte ranges, checked pairwise
+  const uintptr_t C = (uintptr_t)(2 * Hk + Hv) * kD;
+  struct Range { const void* p; uintptr_t n; };
+  const Range in_mixed{mixed, (uintptr_t)B * L * C * 2}, in_tail{tail, (uintptr_t)B * 3 * C * 2};
+  const Range out_o{o, (uintptr_t)B * L * Hv * kD * 2}, out_tail{new_tail, (uintptr_t)B * 3 * C * 2};
+  auto overlap = [](const Range& x, const Range& y) {
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(x.p), y0 = reinterpret_cast<uintptr_t>(y.p);
+    return x.p && y.p && x0 < y0 + y.n && y0 < x0 + x.n;
+  };
+  if (overlap(out_o, in_mixed) || overlap(out_o, in_tail) || overlap(out_tail, in_mixed) ||
+      overlap(out_tail, in_tail) || overlap(out_tail, out_o))
+    return fail(GDR_ERR_INVALID_ARG, "%s: o and new_tail must overlap neither mixed, tail nor each other", who);
+  const size_t need = gdr_chunk_fwd_prologue_workspace_bytes(B, L, Hk, Hv, D, K);
+  if (ws == nullptr || ws_bytes < need)
+    return fail(GDR_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", who, need,
+                ws == nullptr ? (size_t)0 : ws_bytes);
+  int* err = device_error_word();
+  if (!err) return fail(GDR_ERR_CUDA, "%s: no CUDA device available", who);
+  ChunkLaunch c{nullptr, nullptr, nullptr, nullptr, nullptr, S0, o, S_T, ws, B, L, Hk, Hv, err};
+  c.mixed = mixed;
+  c.tail = tail;
+  c.conv_w = conv_w;
+  c.proj_a = a;
+  c.proj_b = b;
+  c.A_log = A_log;
+  c.dt_bias = dt_bias;
+  c.new_tail = new_tail;
+  return launch_status(launch_chunk_bf16(c, reinterpret_cast<cudaStream_t>(stream)), who);
+}
+
 size_t gdr_fork_workspace_bytes(int F, int L_pad, int Hk, int Hv, int D, gdr_dtype dt) {
   return gdr_chunk_workspace_bytes(F, L_pad, Hk, Hv, D, dt);
 }

@@ -101,6 +101,17 @@ struct ChunkArgs {
   // per unit [B, Hv, NC, 8]: the powers of two of dO's four 32-column slices (kMode 2) and of v
   // (word 4, kMode 1), for the backward's chunk-local kernel
   float* unit_scale;
+  // the GDN prologue fused into the prep kernel (kPro): the q|k|v projection [B, L, C] and its carry
+  // [B, 3, C] (bf16), the depthwise conv weights [C, 4], the gate projections a, b [B, L, Hv] and
+  // A_log, dt_bias [Hv]; q, k, v tiles and the gates are formed from them in place of the loads
+  const __nv_bfloat16* mixed;
+  const __nv_bfloat16* tail;
+  const float* conv_w;
+  const float* proj_a;
+  const float* proj_b;
+  const float* A_log;
+  const float* dt_bias;
+  int C;
 };
 
 __device__ __forceinline__ uint8_t* unit_base(const ChunkArgs& a, int b, int h, int c) {
@@ -174,7 +185,11 @@ static_assert(kPVt == kPK1 + 16384 && kPXs + 36 * 32 * 4 <= kPVt + 16384 && kPVt
 // the likeliest to still sit in L2), then rows. While one unit computes, the next unit's gates are
 // loaded into registers and its tiles prefetched into L2. kFused (rows of one chunk, a.fused) is a
 // template parameter, so that the multi-chunk kernel carries none of the in-place apply's code.
-template <bool kFused>
+// kPro: the GDN prologue runs here (DEG "model.py", _linear_layer: _conv_silu over [carry, mixed],
+// _dn_gates): each unit forms its q, k, v tiles as the causal depthwise conv (4 taps) + SiLU of the
+// projection's rows, rounded to bf16, in the prologue kernel's order of operations (so the tiles
+// equal the separate prologue's output bit for bit), and its gates from a, b.
+template <bool kFused, bool kPro = false>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const ChunkArgs a) {
@@ -238,8 +253,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       unit_of(u, c, h, b);
       const int p = c * 64 + tid;
       if (p < a.L && p < row_len(b)) {
-        cp_async4(&gbuf[buf][tid], a.g + ((size_t)b * a.L + p) * a.Hv + h);
-        cp_async4(&gbuf[buf][64 + tid], a.beta + ((size_t)b * a.L + p) * a.Hv + h);
+        cp_async4(&gbuf[buf][tid], (kPro ? a.proj_a : a.g) + ((size_t)b * a.L + p) * a.Hv + h);
+        cp_async4(&gbuf[buf][64 + tid], (kPro ? a.proj_b : a.beta) + ((size_t)b * a.L + p) * a.Hv + h);
       } else {
         gbuf[buf][tid] = 0.f;
         gbuf[buf][64 + tid] = 0.f;
@@ -250,7 +265,83 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // raw q, k, v tiles of a unit (six 64 x 64 boxes) into shared memory, or only into L2; called
   // by every thread: lane 0 of warp t < 6 issues box t, so the six issues proceed in parallel
   // (warp 0 also posts the byte count; the order of count and bytes does not matter)
+  // kPro: the unit's q, k, v tiles as conv + SiLU of the projection, stored like the TMA boxes (rows
+  // past L zero). Thread = (8-channel group cg, 4-row group rg) per tile; ext rows p - 3 .. p + 3
+  // (the carry for positions before 0, zeros past L); s = sum_j w_j x_{t-3+j} in tap order, then
+  // s / (1 + e^-s), one rounding to bf16.
+  auto pro_tiles = [&](int u) {
+    int c, h, b;
+    unit_of(u, c, h, b);
+    const int hk = h / r, cg = tid & 15, rg = tid >> 4, p0 = c * 64;
+    const int HkD = a.Hk * kD;
+#pragma unroll 1
+    for (int tsr = 0; tsr < 3; ++tsr) {
+      const int chan0 = (tsr == 0 ? hk * kD : tsr == 1 ? HkD + hk * kD : 2 * HkD + h * kD) + cg * 8;
+      float w[4][8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(a.conv_w) + chan0 + e);
+        w[0][e] = f.x;
+        w[1][e] = f.y;
+        w[2][e] = f.z;
+        w[3][e] = f.w;
+      }
+      uint4 raw[7];
+#pragma unroll
+      for (int j = 0; j < 7; ++j) {
+        const int pos = p0 + 4 * rg - 3 + j;
+        raw[j] = make_uint4(0, 0, 0, 0);
+        if (pos < 0) {
+          if (a.tail) raw[j] = __ldg(reinterpret_cast<const uint4*>(a.tail + ((size_t)b * 3 + pos + 3) * a.C + chan0));
+        } else if (pos < a.L) {
+          raw[j] = __ldg(reinterpret_cast<const uint4*>(a.mixed + ((size_t)b * a.L + pos) * a.C + chan0));
+        }
+      }
+      float win[7][8];
+#pragma unroll
+      for (int j = 0; j < 7; ++j) {
+        const uint32_t wv[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          win[j][2 * e] = __uint_as_float(wv[e] << 16);
+          win[j][2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
+        }
+      }
+      uint8_t* base = sm + (tsr == 0 ? kPQ0 : tsr == 1 ? kPK0 : kPVt);   // (the 64-column atoms are 16 KB apart)
+      constexpr uint32_t atom_stride = 16384;
+      const int col = cg * 8, atom = col >> 6, ch = (col & 63) >> 3;
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int row = 4 * rg + rr;
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float sacc = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sacc = fmaf(w[j][e], win[rr + j][e], sacc);
+          y[e] = __fdividef(sacc, 1.f + __expf(-sacc));
+        }
+        const uint4 out = p0 + row < a.L ? pack8_bf16(y) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(base + atom * atom_stride + row * 128 + ((ch ^ (row & 7)) << 4)) = out;
+      }
+    }
+  };
+  // kPro: the next unit's projection rows into L2 (67 positions x 256 bytes for each of q, k, v)
+  auto pro_prefetch = [&](int u) {
+    if (tid >= 3 * 67) return;
+    int c, h, b;
+    unit_of(u, c, h, b);
+    const int tsr = tid / 67, pos = c * 64 - 3 + tid % 67;
+    if (pos < 0 || pos >= a.L) return;
+    const int HkD = a.Hk * kD, hk = h / r;
+    const int chan = tsr == 0 ? hk * kD : tsr == 1 ? HkD + hk * kD : 2 * HkD + h * kD;
+    bulk_prefetch_l2(a.mixed + ((size_t)b * a.L + pos) * a.C + chan, kD * 2);
+  };
   auto tiles = [&](int u, bool to_smem) {
+    if (kPro) {
+      if (!to_smem) pro_prefetch(u);
+      return;
+    }
     if (warp >= 6 || lane != 0) return;
     const int t = warp;
     int c, h, b;
@@ -308,7 +399,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   cp_async_wait<1>();   // this unit's gates have landed (the next unit's may still be in flight)
   // inclusive scan of g over the chunk (warps 0 and 1, then warp 1 adds warp 0's total)
   if (tid < 64) {
-    const float gg = gbuf[it & 1][tid], bb = gbuf[it & 1][64 + tid];
+    float gg = gbuf[it & 1][tid], bb = gbuf[it & 1][64 + tid];
+    if (kPro) {
+      // the prologue's gates from the projections: beta = sigmoid(b), g = -exp(A_log) softplus(a +
+      // dt_bias) at valid positions, 0 at pads (as the prologue kernel computes them)
+      float beta = 0.f, g = 0.f;
+      if (c * 64 + tid < a.L) {
+        beta = 1.f / (1.f + expf(-bb));
+        const float xa = gg + a.dt_bias[h];
+        const float sp = xa > 20.f ? xa : log1pf(expf(xa));
+        g = -expf(a.A_log[h]) * sp;
+      }
+      gg = g;
+      bb = beta;
+    }
     float x = gg;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -325,7 +429,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     Gam[tid] = exp2f(gam * kLog2e);
   }
 
-  ok = mbar_wait(&bar_ld, it & 1, a.wait_budget);
+  if (kPro) {
+    // the previous unit's stores staged over q, k, v have been read (the end of its loop)
+    pro_tiles(u);
+    fence_async_smem();   // generic writes, then the Gram product reads them
+    ok = true;
+  } else {
+    ok = mbar_wait(&bar_ld, it & 1, a.wait_budget);
+  }
   if (!ok) ld_fail = it & 1;
   if (!__syncthreads_and(ok)) break;
 
@@ -1474,17 +1585,18 @@ size_t chunk_workspace_bytes(int B, int Hk, int L, int Hv) {
 }
 
 cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, p.B, p.L, p.Hk) || !make_map(&mk, p.k, p.B, p.L, p.Hk) ||
-      !make_map(&mv, p.v, p.B, p.L, p.Hv))
+  CUtensorMap mq{}, mk{}, mv{};   // (the fused prologue forms its tiles without them)
+  if (!p.mixed && (!make_map(&mq, p.q, p.B, p.L, p.Hk) || !make_map(&mk, p.k, p.B, p.L, p.Hk) ||
+                   !make_map(&mv, p.v, p.B, p.L, p.Hv)))
     return cudaErrorInvalidValue;
-  ChunkArgs a;
+  ChunkArgs a{};
   a.g = p.g;
   a.beta = p.beta;
   a.S0 = p.S0;
   a.S0_idx = p.S0_idx;
   a.n_S0 = p.n_S0;
-  a.fused = (p.L <= kChunk) ? 1 : 0;
+  // (with the fused prologue, rows of one chunk also take the two-kernel path through the workspace)
+  a.fused = (p.L <= kChunk && !p.mixed) ? 1 : 0;
   a.wait_budget = wait_budget_cycles();
   a.o = static_cast<__nv_bfloat16*>(p.o);
   a.S_T = p.S_T;
@@ -1499,8 +1611,19 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   a.z = static_cast<const __nv_bfloat16*>(p.z);
   a.w = p.w;
   a.eps = p.eps;
+  a.mixed = static_cast<const __nv_bfloat16*>(p.mixed);
+  a.tail = static_cast<const __nv_bfloat16*>(p.tail);
+  a.conv_w = p.conv_w;
+  a.proj_a = p.proj_a;
+  a.proj_b = p.proj_b;
+  a.A_log = p.A_log;
+  a.dt_bias = p.dt_bias;
+  a.C = (2 * p.Hk + p.Hv) * kD;
+  const bool pro = p.mixed != nullptr;   // the prologue fused into the prep kernel
 
   cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+  if (e == cudaSuccess && pro)
+    e = cudaFuncSetAttribute(chunk_prep_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
   if (e == cudaSuccess)
@@ -1510,7 +1633,9 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
   int slot = stage_timer_begin(s, kKernChunkPrep);
   const long long units = (long long)a.B * a.Hv * a.NC;
   const int grid = (int)std::min<long long>(units, 2ll * num_sms());
-  if (a.fused)
+  if (pro)
+    chunk_prep_kernel<false, true><<<grid, kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
+  else if (a.fused)
     chunk_prep_kernel<true><<<grid, kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
   else
     chunk_prep_kernel<false><<<grid, kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
@@ -1546,8 +1671,26 @@ cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s) {
           : cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 0>, a, no_map);
   stage_timer_end(slot, s);
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (pro && p.new_tail) {
+    // the carry for the next call: ext positions L .. L + 2 of every row, ext = [tail; mixed], i.e.
+    // tail rows L .. 2 (zeros without a tail) when L < 3, then mixed rows max(L - 3, 0) .. L - 1
+    const size_t row = (size_t)a.C * 2;
+    const int nt = std::max(0, 3 - p.L), nm = 3 - nt;
+    uint8_t* dst = static_cast<uint8_t*>(p.new_tail);
+    if (nt > 0)
+      e = p.tail ? cudaMemcpy2DAsync(dst, 3 * row, static_cast<const uint8_t*>(p.tail) + (size_t)p.L * row, 3 * row,
+                                     nt * row, (size_t)p.B, cudaMemcpyDeviceToDevice, s)
+                 : cudaMemset2DAsync(dst, 3 * row, 0, nt * row, (size_t)p.B, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(dst + nt * row, 3 * row,
+                            static_cast<const uint8_t*>(p.mixed) + (size_t)(p.L - nm) * row, (size_t)p.L * row,
+                            nm * row, (size_t)p.B, cudaMemcpyDeviceToDevice, s);
+  }
+  return e;
 }
+
+size_t chunk_prologue_workspace_bytes(int B, int L, int Hv) { return units_bytes(B, L, Hv) + 1024; }
 
 size_t chunk_bwd_units_bytes(int B, int L, int Hv) { return units_bytes(B, L, Hv) + 1024; }
 

@@ -68,8 +68,22 @@ struct ChunkLaunch {
   const void* z = nullptr;            // [B, L, Hv, 128] bf16
   const float* w = nullptr;           // [128]
   float eps = 0.f;
+  // the GDN prologue fused into the prep kernel (NULL mixed = none; otherwise q, k, v, g, beta are
+  // unused and the conv has 4 taps): mixed [B, L, C] bf16 with C = (2 Hk + Hv) 128, its carry tail [B, 3, C] bf16 (NULL
+  // = zeros), conv_w [C, 4], proj_a, proj_b [B, L, Hv], A_log, dt_bias [Hv]; new_tail [B, 3, C]
+  // receives the carry for the next call (NULL = not written)
+  const void* mixed = nullptr;
+  const void* tail = nullptr;
+  const float* conv_w = nullptr;
+  const float* proj_a = nullptr;
+  const float* proj_b = nullptr;
+  const float* A_log = nullptr;
+  const float* dt_bias = nullptr;
+  void* new_tail = nullptr;
 };
 size_t chunk_workspace_bytes(int B, int Hk, int L, int Hv);
+// the workspace of launch_chunk_bf16 with the fused prologue (any L: rows of one chunk included)
+size_t chunk_prologue_workspace_bytes(int B, int L, int Hv);
 cudaError_t launch_chunk_bf16(const ChunkLaunch& p, cudaStream_t s);
 
 // GDN prologue (causal depthwise conv + SiLU over [tail, mixed], the gates, the conv carry).

@@ -21,7 +21,7 @@ GDR_F32, GDR_BF16 = 0, 1
 D = 128
 
 EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_varlen", "gdr_chunk_fwd_gated",
-           "gdr_chunk_fwd_noalloc",
+           "gdr_chunk_fwd_noalloc", "gdr_chunk_fwd_prologue_workspace_bytes", "gdr_chunk_fwd_prologue",
            "gdr_fork_workspace_bytes",
            "gdr_fork_fwd", "gdr_decode_step", "gdr_prologue", "gdr_gated_rmsnorm",
            "gdr_backward_workspace_bytes", "gdr_backward",
@@ -67,6 +67,10 @@ def lib() -> ctypes.CDLL:
     L.gdr_decode_step.restype = i
     L.gdr_prologue.argtypes = [vp, vp, fp, fp, fp, fp, fp, vp, vp, vp, vp, fp, fp, vp, i, i, i, i, i, i, vp]
     L.gdr_prologue.restype = i
+    L.gdr_chunk_fwd_prologue_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    L.gdr_chunk_fwd_prologue_workspace_bytes.restype = sz
+    L.gdr_chunk_fwd_prologue.argtypes = [vp, vp, fp, fp, fp, fp, fp, fp, vp, fp, vp, i, i, i, i, i, i, vp, sz, vp]
+    L.gdr_chunk_fwd_prologue.restype = i
     L.gdr_gated_rmsnorm.argtypes = [vp, vp, fp, ctypes.c_float, vp, ctypes.c_longlong, i, vp]
     L.gdr_gated_rmsnorm.restype = i
     L.gdr_backward_workspace_bytes.argtypes = [i, i, i, i, i]
@@ -275,6 +279,51 @@ def gdr_prologue(mixed, conv_w, a, b, A_log, dt_bias, Hk: int, Hv: int, tail=Non
                               _p(q), _p(k), _p(v), _p(g), _p(beta), _p(new_tail), B, L, Hk, Hv, D, K,
                               _stream(stream)))
     return q, k, v, g, beta, new_tail
+
+
+def prologue_workspace_bytes(B: int, L: int, Hk: int, Hv: int, K: int = 4, D: int = D) -> int:
+    return int(lib().gdr_chunk_fwd_prologue_workspace_bytes(B, L, Hk, Hv, D, K))
+
+
+def gdr_chunk_fwd_prologue(mixed, conv_w, a, b, A_log, dt_bias, Hk: int, Hv: int, S0=None, tail=None,
+                           o=None, S_T=None, new_tail=None, ws=None, stream=None, final_state: bool = True,
+                           keep_tail: bool = True):
+    """The GDN prologue fused into the bf16 prefill: gdr_prologue(mixed, ...) then gdr_chunk_fwd on its
+    outputs, in one pass. Returns (o [B,L,Hv,D] bf16, S_T [B,Hv,D,D] float32 or None, new_tail
+    [B,3,C] bf16 or None)."""
+    for name, t in (("mixed", mixed), ("conv_w", conv_w), ("a", a), ("b", b), ("A_log", A_log), ("dt_bias", dt_bias)):
+        _need(isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _need(mixed.dtype == torch.bfloat16 and mixed.dim() == 3, "mixed must be bfloat16 [B, L, C]")
+    B, L, C = mixed.shape
+    _need(C == (2 * Hk + Hv) * D, f"mixed has {C} channels, expected (2 Hk + Hv) D = {(2 * Hk + Hv) * D}")
+    _need(conv_w.dtype == torch.float32 and conv_w.dim() == 2 and conv_w.shape[0] == C, "conv_w must be float32 [C, K]")
+    K = conv_w.shape[1]
+    for name, t in (("a", a), ("b", b)):
+        _need(t.dtype == torch.float32 and t.shape == (B, L, Hv), f"{name} must be float32 [B, L, Hv]")
+    for name, t in (("A_log", A_log), ("dt_bias", dt_bias)):
+        _need(t.dtype == torch.float32 and t.shape == (Hv,), f"{name} must be float32 [Hv]")
+    if tail is not None:
+        _need(tail.is_cuda and tail.is_contiguous() and tail.dtype == torch.bfloat16 and tail.shape == (B, K - 1, C),
+              "tail must be contiguous CUDA bfloat16 [B, K-1, C]")
+    for name, t in (("S0", S0), ("S_T", S_T)):
+        if t is not None:
+            _need(t.dtype == torch.float32 and t.is_contiguous() and t.is_cuda and t.shape == (B, Hv, D, D),
+                  f"{name} must be contiguous CUDA float32 [B, Hv, D, D]")
+    dev = mixed.device
+    if o is None:
+        o = torch.empty(B, L, Hv, D, device=dev, dtype=torch.bfloat16)
+    if S_T is None and final_state:
+        S_T = torch.empty(B, Hv, D, D, device=dev, dtype=torch.float32)
+    if new_tail is None and keep_tail and K > 1:
+        new_tail = torch.empty(B, K - 1, C, device=dev, dtype=torch.bfloat16)
+    need = prologue_workspace_bytes(B, L, Hk, Hv, K)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().gdr_chunk_fwd_prologue(_p(mixed), _p(tail), _p(conv_w), _p(a), _p(b), _p(A_log), _p(dt_bias),
+                                        _p(S0), _p(o), _p(S_T), _p(new_tail), B, L, Hk, Hv, D, K, _p(ws), ws_bytes,
+                                        _stream(stream)))
+    return o, S_T, new_tail
 
 
 def gdr_gated_rmsnorm(x, z, w, eps: float = 1e-6, out=None, stream=None):

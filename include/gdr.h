@@ -208,6 +208,29 @@ gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w
                         int Hk, int Hv, int D, int K, gdr_stream_t stream);
 
 /*
+ * The GDN prologue fused into the bfloat16 prefill: gdr_prologue (K = 4, lengths NULL) followed by
+ * gdr_chunk_fwd on its q, k, v, g and beta, without q, k, v, g and beta ever reaching memory
+ * (DEG "model.py": _linear_layer, where _conv_silu and _dn_gates feed _delta_rule). The chunk
+ * kernel forms each 64-token tile of q, k and v as the conv + SiLU of the projection rows (and the
+ * carry) in gdr_prologue's own order of operations, one rounding to bfloat16, and each chunk's g and
+ * beta from a and b the same way: o, S_T and new_tail equal those of the two separate calls bit for
+ * bit.
+ *   mixed, tail, conv_w, a, b, A_log, dt_bias, new_tail   as for gdr_prologue (conv_w [C, 4]; tail
+ *                                   NULL = zeros, new_tail NULL = not written)
+ *   S0, o, S_T                      as for gdr_chunk_fwd with dt = GDR_BF16 (o [B, L, Hv, D] bf16)
+ *   ws    workspace of at least gdr_chunk_fwd_prologue_workspace_bytes(...) bytes (never NULL,
+ *         every L included), owned by the caller: the per-chunk factors
+ * o and new_tail must overlap neither mixed, tail nor each other. K must be 4 and D 128
+ * (GDR_ERR_UNSUPPORTED otherwise); B, Hv <= 65535. Every row has L valid tokens (for rows with their
+ * own lengths, call gdr_prologue with lengths and then gdr_chunk_fwd_varlen).
+ */
+size_t gdr_chunk_fwd_prologue_workspace_bytes(int B, int L, int Hk, int Hv, int D, int K);
+gdr_status gdr_chunk_fwd_prologue(const void* mixed, const void* tail, const float* conv_w, const float* a,
+                                  const float* b, const float* A_log, const float* dt_bias, const float* S0,
+                                  void* o, float* S_T, void* new_tail, int B, int L, int Hk, int Hv, int D,
+                                  int K, void* ws, size_t ws_bytes, gdr_stream_t stream);
+
+/*
  * Gated RMSNorm epilogue: per row of D values (a position and value head of the recurrence
  * output o [B, L, Hv, D], so rows = B L Hv), with the gate z of the same shape,
  *   out = w * (x / sqrt(mean(x^2) + eps)) * silu(z),   silu(z) = z / (1 + exp(-z))

@@ -261,3 +261,47 @@ def test_chunked_backward_rejects_bad_arguments_and_sizes_its_workspace(L):
         want = (a256(units) + 2 * a256(B * Hv * NC * 128 * 128 * 2) + 2 * a256(B * Hv * NC * 4 * 4)
                 + a256(B * Hv * NC * 8 * 4))
         assert L.gdr_backward_chunked_workspace_bytes(B, Lt, 2, Hv, 128) == want
+
+
+def test_fused_prologue_rejects_bad_arguments_and_sizes_its_workspace(L):
+    """gdr_chunk_fwd_prologue: the prologue's and the prefill's host checks, a 4-tap conv only, o and
+    new_tail clear of the inputs, and a workspace of the per-chunk factors for every L (rows of one
+    chunk included: with the prologue fused they go through the two-kernel path)."""
+    f = L.gdr_chunk_fwd_prologue
+    need = L.gdr_chunk_fwd_prologue_workspace_bytes(1, 64, 2, 4, 128, 4)
+    assert need == 1 * 4 * 1 * 98816 + 1024
+    O = ctypes.c_void_p(1 << 30)   # an output far from P's inputs
+
+    def args(mixed=P, conv_w=P, a=P, o=O, new_tail=None, tail=None, B=1, Lt=64, Hk=2, Hv=4, D=128, K=4,
+             ws=P, ws_bytes=need):
+        return (mixed, tail, conv_w, a, P, P, P, None, o, None, new_tail, B, Lt, Hk, Hv, D, K, ws, ws_bytes, None)
+
+    assert f(*args(mixed=None)) == gdr.GDR_ERR_INVALID_ARG
+    assert b"non-NULL" in L.gdr_last_error_message()
+    assert f(*args(o=None)) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(Lt=0)) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(Hk=3)) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(K=9)) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(K=3)) == gdr.GDR_ERR_UNSUPPORTED
+    assert b"4-tap" in L.gdr_last_error_message()
+    assert f(*args(D=64)) == gdr.GDR_ERR_UNSUPPORTED
+    assert f(*args(B=65536)) == gdr.GDR_ERR_UNSUPPORTED
+    assert f(*args(mixed=BAD)) == gdr.GDR_ERR_INVALID_ARG
+    assert b"aligned" in L.gdr_last_error_message()
+    assert f(*args(conv_w=BAD)) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(a=ctypes.c_void_p((1 << 20) + 2))) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(o=P)) == gdr.GDR_ERR_INVALID_ARG
+    assert b"overlap" in L.gdr_last_error_message()
+    assert f(*args(new_tail=ctypes.c_void_p((1 << 20) + 4096))) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(tail=ctypes.c_void_p(1 << 31), new_tail=ctypes.c_void_p((1 << 31) + 1024))) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(ws_bytes=need - 1)) == gdr.GDR_ERR_INVALID_ARG
+    assert b"workspace" in L.gdr_last_error_message()
+    assert f(*args(ws=None)) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_chunk_fwd_prologue_workspace_bytes(1, 64, 2, 4, 128, 3) == 0
+    assert L.gdr_chunk_fwd_prologue_workspace_bytes(1, 64, 3, 4, 128, 4) == 0
+    for B, Lt, Hv in ((1, 1, 4), (2, 130, 8), (1, 4096, 32)):
+        NC = -(-Lt // 64)
+        assert L.gdr_chunk_fwd_prologue_workspace_bytes(B, Lt, 2, Hv, 128, 4) == B * Hv * NC * 98816 + 1024
+    # rows longer than one chunk take the prefill's own workspace
+    assert L.gdr_chunk_fwd_prologue_workspace_bytes(1, 4096, 16, 32, 128, 4) == \
+        L.gdr_chunk_workspace_bytes(1, 4096, 16, 32, 128, 1)
