@@ -179,6 +179,16 @@ static_assert(kPP + 16384 <= kPrepSmem - 1024 && kPAop + 16384 <= kPVec, "M = 12
 static_assert(kPWS % 1024 == 0 && kPWS + 32768 <= kPVec, "the [sk W | sk U] operand fits over AT and T");
 static_assert(kPVt == kPK1 + 16384 && kPXs + 36 * 32 * 4 <= kPVt + 16384 && kPVt + 16384 + 8192 <= kPP,
               "v atoms continue the k atoms' stride; the inverse scratch fits between them");
+// The fused prologue's staging, free from the end of the previous unit until the tiles are formed:
+// the raw projection rows p0 - 3 .. p0 + 63 of q, k and v (67 rows of 256 bytes each, unswizzled)
+// and the unit's conv weights as float4s in [tensor][channel % 8][channel / 8] order (a quarter-warp
+// reads 128 contiguous bytes). q's rows lie under the q and k tiles, v's under the first v atom,
+// k's under the second v atom and P: each tile is written only once the rows beneath it are read.
+constexpr uint32_t kRawRow = 256, kRawRows = 67;
+constexpr uint32_t kRawQ = 0, kRawV = 32768, kRawK = kRawV + kRawRows * kRawRow, kRawW = kRawK + kRawRows * kRawRow;
+static_assert(kRawQ + kRawRows * kRawRow <= kRawV && kRawV >= kPK1 + 8192 && kRawW % 16 == 0 &&
+              kRawW + 3 * 128 * 16 <= kPAT,
+              "v's and k's rows clear of the q and k tiles, everything clear of the draining N store");
 
 // Persistent: CTA i takes units i, i + gridDim.x, ... in the order value head fastest, then chunks
 // from the last to the first (so the units the state kernel reads first were written last and are
@@ -266,64 +276,82 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // by every thread: lane 0 of warp t < 6 issues box t, so the six issues proceed in parallel
   // (warp 0 also posts the byte count; the order of count and bytes does not matter)
   // kPro: the unit's q, k, v tiles as conv + SiLU of the projection, stored like the TMA boxes (rows
-  // past L zero). Thread = (8-channel group cg, 4-row group rg) per tile; ext rows p - 3 .. p + 3
-  // (the carry for positions before 0, zeros past L); s = sum_j w_j x_{t-3+j} in tap order, then
-  // s / (1 + e^-s), one rounding to bf16.
-  auto pro_tiles = [&](int u) {
-    int c, h, b;
-    unit_of(u, c, h, b);
-    const int hk = h / r, cg = tid & 15, rg = tid >> 4, p0 = c * 64;
+  // past L zero). The raw rows (the carry for positions before 0, zeros past L) and the weights are
+  // copied into shared memory at the top of the unit (pro_issue) and land during the gate scan.
+  // Thread = (8-channel group cg, 4-row group rg) per tile, window ext rows p - 3 .. p + 3;
+  // s = sum_j w_j x_{t-3+j} in tap order, then s / (1 + e^-s), one rounding to bf16.
+  auto pro_chan = [&](int tsr, int h) {
     const int HkD = a.Hk * kD;
+    return tsr == 0 ? (h / r) * kD : tsr == 1 ? HkD + (h / r) * kD : 2 * HkD + h * kD;
+  };
+  auto pro_issue = [&](int c, int h, int b) {
+    const int p0 = c * 64 - 3;
 #pragma unroll 1
-    for (int tsr = 0; tsr < 3; ++tsr) {
-      const int chan0 = (tsr == 0 ? hk * kD : tsr == 1 ? HkD + hk * kD : 2 * HkD + h * kD) + cg * 8;
-      float w[4][8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float4 f = __ldg(reinterpret_cast<const float4*>(a.conv_w) + chan0 + e);
-        w[0][e] = f.x;
-        w[1][e] = f.y;
-        w[2][e] = f.z;
-        w[3][e] = f.w;
+    for (int i = tid; i < 3 * (int)kRawRows * 16; i += kPrepThreads) {
+      const int tsr = i / ((int)kRawRows * 16), rem = i - tsr * (int)kRawRows * 16, row = rem >> 4, ch = rem & 15;
+      const int pos = p0 + row, chan = pro_chan(tsr, h) + ch * 8;
+      const __nv_bfloat16* src = a.mixed;   // (a valid address; nothing is read when n = 0)
+      uint32_t n = 0;
+      if (pos < 0) {
+        if (a.tail) {
+          src = a.tail + ((size_t)b * 3 + pos + 3) * a.C + chan;
+          n = 16;
+        }
+      } else if (pos < a.L) {
+        src = a.mixed + ((size_t)b * a.L + pos) * a.C + chan;
+        n = 16;
       }
-      uint4 raw[7];
+      const uint32_t base = tsr == 0 ? kRawQ : tsr == 1 ? kRawK : kRawV;
+      cp_async16_zfill(sm + base + row * kRawRow + ch * 16, src, n);
+    }
+    for (int i = tid; i < 3 * 128; i += kPrepThreads) {
+      const int tsr = i >> 7, cc = i & 127;
+      cp_async16_zfill(sm + kRawW + ((tsr * 8 + (cc & 7)) * 16 + (cc >> 3)) * 16,
+                       a.conv_w + (size_t)(pro_chan(tsr, h) + cc) * 4, 16);
+    }
+  };
+  auto pro_window = [&](int tsr, uint4 (&raw)[7]) {
+    const uint8_t* src = sm + (tsr == 0 ? kRawQ : tsr == 1 ? kRawK : kRawV) + 4 * (tid >> 4) * kRawRow + (tid & 15) * 16;
+#pragma unroll
+    for (int j = 0; j < 7; ++j) raw[j] = *reinterpret_cast<const uint4*>(src + j * kRawRow);
+  };
+  auto pro_conv = [&](int tsr, int c, const uint4 (&raw)[7]) {
+    const int cg = tid & 15, rg = tid >> 4, col = cg * 8;
+    const float4* wsm = reinterpret_cast<const float4*>(sm + kRawW) + tsr * 128 + cg;
+    uint32_t out[4][4];   // [row][channel pair], bf16x2
+#pragma unroll
+    for (int ep = 0; ep < 4; ++ep) {
+      // channels 2 ep (the low half of each raw word ep) and 2 ep + 1 (the high half)
+      const float4 wa = wsm[(2 * ep) * 16], wb = wsm[(2 * ep + 1) * 16];
+      float xa[7], xb[7];
 #pragma unroll
       for (int j = 0; j < 7; ++j) {
-        const int pos = p0 + 4 * rg - 3 + j;
-        raw[j] = make_uint4(0, 0, 0, 0);
-        if (pos < 0) {
-          if (a.tail) raw[j] = __ldg(reinterpret_cast<const uint4*>(a.tail + ((size_t)b * 3 + pos + 3) * a.C + chan0));
-        } else if (pos < a.L) {
-          raw[j] = __ldg(reinterpret_cast<const uint4*>(a.mixed + ((size_t)b * a.L + pos) * a.C + chan0));
-        }
+        const uint32_t wv = ep == 0 ? raw[j].x : ep == 1 ? raw[j].y : ep == 2 ? raw[j].z : raw[j].w;
+        xa[j] = __uint_as_float(wv << 16);
+        xb[j] = __uint_as_float(wv & 0xFFFF0000u);
       }
-      float win[7][8];
-#pragma unroll
-      for (int j = 0; j < 7; ++j) {
-        const uint32_t wv[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          win[j][2 * e] = __uint_as_float(wv[e] << 16);
-          win[j][2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
-        }
-      }
-      uint8_t* base = sm + (tsr == 0 ? kPQ0 : tsr == 1 ? kPK0 : kPVt);   // (the 64-column atoms are 16 KB apart)
-      constexpr uint32_t atom_stride = 16384;
-      const int col = cg * 8, atom = col >> 6, ch = (col & 63) >> 3;
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
-        const int row = 4 * rg + rr;
-        float y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float sacc = 0.f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) sacc = fmaf(w[j][e], win[rr + j][e], sacc);
-          y[e] = __fdividef(sacc, 1.f + __expf(-sacc));
-        }
-        const uint4 out = p0 + row < a.L ? pack8_bf16(y) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(base + atom * atom_stride + row * 128 + ((ch ^ (row & 7)) << 4)) = out;
+        float sa = 0.f, sb = 0.f;
+        sa = fmaf(wa.x, xa[rr], sa);
+        sb = fmaf(wb.x, xb[rr], sb);
+        sa = fmaf(wa.y, xa[rr + 1], sa);
+        sb = fmaf(wb.y, xb[rr + 1], sb);
+        sa = fmaf(wa.z, xa[rr + 2], sa);
+        sb = fmaf(wb.z, xb[rr + 2], sb);
+        sa = fmaf(wa.w, xa[rr + 3], sa);
+        sb = fmaf(wb.w, xb[rr + 3], sb);
+        out[rr][ep] = pack_bf16x2(__fdividef(sa, 1.f + __expf(-sa)), __fdividef(sb, 1.f + __expf(-sb)));
       }
+    }
+    uint8_t* base = sm + (tsr == 0 ? kPQ0 : tsr == 1 ? kPK0 : kPVt) + (col >> 6) * 16384;   // atoms 16 KB apart
+    const int ch = (col & 63) >> 3;
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int row = 4 * rg + rr;
+      const uint4 v = c * 64 + row < a.L ? make_uint4(out[rr][0], out[rr][1], out[rr][2], out[rr][3])
+                                         : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(base + row * 128 + ((ch ^ (row & 7)) << 4)) = v;
     }
   };
   // kPro: the next unit's projection rows into L2 (67 positions x 256 bytes for each of q, k, v)
@@ -390,13 +418,27 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   int c, h, b;
   unit_of(u, c, h, b);
   uint8_t* ub = unit_base(a, b, h, c);
+  float pro_dtb = 0.f, pro_alog = 0.f;
+  if (kPro) {
+    // the previous unit's stores staged over this region have been read (the end of its loop)
+    pro_issue(c, h, b);   // its own group, between this unit's gates and the next unit's
+    cp_async_commit();
+    if (tid < 64) {
+      pro_dtb = __ldg(a.dt_bias + h);
+      pro_alog = __ldg(a.A_log + h);
+    }
+  }
   const int un = next_valid(u + (int)gridDim.x);
   if (un < total) {
     copy_gates(un, (it + 1) & 1);
   } else {
     cp_async_commit();
   }
-  cp_async_wait<1>();   // this unit's gates have landed (the next unit's may still be in flight)
+  // this unit's gates have landed (the next unit's, and with kPro the staged rows, may still be in flight)
+  if (kPro)
+    cp_async_wait<2>();
+  else
+    cp_async_wait<1>();
   // inclusive scan of g over the chunk (warps 0 and 1, then warp 1 adds warp 0's total)
   if (tid < 64) {
     float gg = gbuf[it & 1][tid], bb = gbuf[it & 1][64 + tid];
@@ -406,9 +448,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       float beta = 0.f, g = 0.f;
       if (c * 64 + tid < a.L) {
         beta = 1.f / (1.f + expf(-bb));
-        const float xa = gg + a.dt_bias[h];
+        const float xa = gg + pro_dtb;
         const float sp = xa > 20.f ? xa : log1pf(expf(xa));
-        g = -expf(a.A_log[h]) * sp;
+        g = -expf(pro_alog) * sp;
       }
       gg = g;
       bb = beta;
@@ -430,8 +472,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
 
   if (kPro) {
-    // the previous unit's stores staged over q, k, v have been read (the end of its loop)
-    pro_tiles(u);
+    cp_async_wait<1>();   // the staged rows and weights (the next unit's gates may still be in flight)
+    __syncthreads();
+    uint4 raw[7];
+    pro_window(0, raw);
+    __syncthreads();   // q's rows are read before the q tiles overwrite them
+    pro_conv(0, c, raw);
+    pro_window(1, raw);
+    pro_conv(1, c, raw);
+    pro_window(2, raw);
+    __syncthreads();   // k's and v's rows are read before the v tiles overwrite them
+    pro_conv(2, c, raw);
     fence_async_smem();   // generic writes, then the Gram product reads them
     ok = true;
   } else {
