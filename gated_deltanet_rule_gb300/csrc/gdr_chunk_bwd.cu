@@ -168,16 +168,21 @@ __device__ __forceinline__ void store_h(uint8_t* tile, int ld, int m0, int n0, c
     }
 }
 
-// CTA-wide max of a per-thread value (every thread gets it); uses vec[vMax][0..7]
-__device__ __forceinline__ float cta_max(float m, float* vmax, int warp, int lane) {
+// CTA-wide max of a per-thread value (every thread gets it), with one block barrier (which also
+// orders everything before the call against everything after it). The per-warp maxima alternate
+// between vec[vMax][0..15] and [32..47] from one call to the next (par, the same in every thread):
+// a buffer is rewritten two calls later, after the intervening call's barrier has passed every
+// reader of it.
+__device__ __forceinline__ float cta_max(float m, float* vmax, int warp, int lane, int& par) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  __syncthreads();   // earlier readers of vmax are done
-  if (lane == 0) vmax[warp] = m;
+  float* buf = vmax + 32 * par;
+  par ^= 1;
+  if (lane == 0) buf[warp] = m;
   __syncthreads();
-  float r = vmax[0];
+  float r = buf[0];
 #pragma unroll
-  for (int w = 1; w < kLT / 32; ++w) r = fmaxf(r, vmax[w]);
+  for (int w = 1; w < kLT / 32; ++w) r = fmaxf(r, buf[w]);
   return r;
 }
 
@@ -212,6 +217,7 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
   const int m0 = 16 * (warp & 3), quarter = warp >> 2;
   const int n128 = 32 * quarter, n64 = 16 * quarter;
   const int p0 = c * kChunk;   // first position of the chunk
+  int mpar = 0;                // cta_max's buffer parity
   uint8_t* tQ = sm + kOQ;
   uint8_t* tK = sm + kOK;
   uint8_t* tV = sm + kOV;
@@ -223,6 +229,43 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
   float* Af = reinterpret_cast<float*>(sm + kOTf);
   uint8_t* tT = sm + kOT16;
   uint8_t* tP = sm + kOP16;
+
+  // a value head's v and dO rows (zero past L) and its S and dS' (four 32-column slice images of 128
+  // key rows x 64 bytes, 64-byte swizzle, each) into their tiles, as one group of asynchronous copies
+  auto issue_head = [&](int h) {
+#pragma unroll
+    for (int it = 0; it < 2 * 1024 / kLT; ++it) {
+      const int idx = tid + kLT * it;
+      const int which = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
+      const int pos = p0 + row;
+      const size_t ro = pos < a.L ? (((size_t)b * a.L + pos) * a.Hv + h) * kD : 0;
+      cp_async16_zfill((which ? tO : tV) + row * kLd * 2 + ch * 16,
+                       reinterpret_cast<const uint4*>((which ? a.dO : a.v) + ro) + ch, pos < a.L ? 16 : 0);
+    }
+    const size_t unit = ((size_t)b * a.Hv + h) * a.NC + c;
+#pragma unroll
+    for (int it = 0; it < 2 * 2048 / kLT; ++it) {
+      const int idx = tid + kLT * it;
+      const int which = idx >> 11, row = (idx >> 4) & 127, ch = idx & 15;
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(which ? a.dS_save : a.S_save) + unit * (kD * kD * 2) +
+                           (ch >> 2) * 8192 + swz64(row * 64 + (ch & 3) * 16);
+      cp_async16_zfill((which ? tD : tS) + row * kLd * 2 + ch * 16, src, 16);
+    }
+    cp_async_commit();
+  };
+  // the same inputs of a later value head into L2 only (the tiles are still in use)
+  auto prefetch_head = [&](int h) {
+    if (tid < 128) {
+      const int pos = p0 + (tid & 63);
+      if (pos < a.L)
+        bulk_prefetch_l2(((tid < 64 ? a.v : a.dO) + (((size_t)b * a.L + pos) * a.Hv + h) * kD), kD * 2);
+    } else if (tid < 136) {
+      const size_t unit = ((size_t)b * a.Hv + h) * a.NC + c;
+      const int piece = tid - 128;   // 8 KB pieces: S's four slices, then dS''s
+      bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(piece < 4 ? a.S_save : a.dS_save) + unit * (kD * kD * 2) +
+                       (piece & 3) * 8192, 8192);
+    }
+  };
 
   // ---- prologue (once per key head): raw q, k rows, their inverse norms, the Gram products
   //      K K^T and Q K^T from the raw bf16 rows (kept in registers: every value head's A and P are
@@ -237,7 +280,8 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
                      reinterpret_cast<const uint4*>((which ? a.k : a.q) + ro) + ch, pos < a.L ? 16 : 0);
   }
   cp_async_commit();
-  cp_async_wait<0>();
+  issue_head(hk * r);   // the first value head's inputs load while q and k are prepared
+  cp_async_wait<1>();   // q and k have landed
   __syncthreads();
   if (tid < 128) {
     // inverse norms of the raw q, k rows (threads 0-63: q, 64-127: k)
@@ -287,6 +331,7 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
   for (int jh = 0; jh < r; ++jh) {
   const int h = hk * r + jh;
   __syncthreads();   // the previous value head's tiles are spent (and q^, k^ are in)
+  if (jh + 1 < r) prefetch_head(h + 1);
 
   // ---- 0. the value head's inputs: gates, v and dO rows (zero past L), S and dS' (fp16) ----
   if (tid < 64) {
@@ -302,28 +347,7 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
     }
     V(vScan)[tid] = x;
   }
-  {
-#pragma unroll
-    for (int it = 0; it < 2 * 1024 / kLT; ++it) {
-      const int idx = tid + kLT * it;
-      const int which = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
-      const int pos = p0 + row;
-      const size_t ro = pos < a.L ? (((size_t)b * a.L + pos) * a.Hv + h) * kD : 0;
-      cp_async16_zfill((which ? tO : tV) + row * kLd * 2 + ch * 16,
-                       reinterpret_cast<const uint4*>((which ? a.dO : a.v) + ro) + ch, pos < a.L ? 16 : 0);
-    }
-    // S and dS': four 32-column slice images of 128 key rows x 64 bytes (64-byte swizzle) each
-    const size_t unit = ((size_t)b * a.Hv + h) * a.NC + c;
-#pragma unroll
-    for (int it = 0; it < 2 * 2048 / kLT; ++it) {
-      const int idx = tid + kLT * it;
-      const int which = idx >> 11, row = (idx >> 4) & 127, ch = idx & 15;
-      const uint8_t* src = reinterpret_cast<const uint8_t*>(which ? a.dS_save : a.S_save) + unit * (kD * kD * 2) +
-                           (ch >> 2) * 8192 + swz64(row * 64 + (ch & 3) * 16);
-      cp_async16_zfill((which ? tD : tS) + row * kLd * 2 + ch * 16, src, 16);
-    }
-    cp_async_commit();
-  }
+  if (jh > 0) issue_head(h);   // (the first value head's inputs were issued with q and k)
   cp_async_wait<0>();
   __syncthreads();
   if (tid < 64) {
@@ -461,7 +485,7 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[nt][e] = upV * acc[nt][e] - upS * acc2[nt][e];   // Delta
   float upDl, dnDl;
-  pow2_up_dn(cta_max(absmax(acc), V(vMax), warp, lane), upDl, dnDl);   // (its barriers: X1 is free)
+  pow2_up_dn(cta_max(absmax(acc), V(vMax), warp, lane, mpar), upDl, dnDl);   // (its barriers: X1 is free)
   store_h(tX1, kLd, m0, n128, acc, dnDl, lane);                         // Delta / 2^eDl
   __syncthreads();
 
@@ -480,7 +504,7 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
       acc[nt][e] = upO * acc[nt][e] + ev[i] * kd;
     }
   float updD, dndD;
-  pow2_up_dn(cta_max(absmax(acc), V(vMax), warp, lane), updD, dndD);
+  pow2_up_dn(cta_max(absmax(acc), V(vMax), warp, lane, mpar), updD, dndD);
   store_h(tX2, kLd, m0, n128, acc, dndD, lane);                          // dDelta / 2^edD (W is spent)
 
   // ---- 5. dK^ += diag(e) Delta dS'^T ----
@@ -500,7 +524,7 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[nt][e] *= -updD * upS;
   float updW, dndW;
-  pow2_up_dn(cta_max(absmax(acc), V(vMax), warp, lane), updW, dndW);
+  pow2_up_dn(cta_max(absmax(acc), V(vMax), warp, lane, mpar), updW, dndW);
   uint8_t* tdW = tD;   // dS' is spent
   store_h(tdW, kLd, m0, n128, acc, dndW, lane);
   zero(acc2);
@@ -537,7 +561,7 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
         dp[nt][e] = j <= i ? d * Eij(i, j) : 0.f;
       }
     float up, dn;
-    pow2_up_dn(cta_max(absmax(dp), V(vMax), warp, lane), up, dn);
+    pow2_up_dn(cta_max(absmax(dp), V(vMax), warp, lane, mpar), up, dn);
     store_h(tPE, kLs, m0, n64, dp, dn, lane);
     __syncthreads();
     float t2[4][4];
@@ -598,13 +622,13 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
         t1[nt][e] = bet[j] * (updD * upV * t1[nt][e] + Gam[j] * updW * t2[nt][e]);
       }
     float upT, dnT;
-    pow2_up_dn(cta_max(absmax(t1), V(vMax), warp, lane), upT, dnT);
+    pow2_up_dn(cta_max(absmax(t1), V(vMax), warp, lane, mpar), upT, dnT);
     store_h(tdT, kLs, m0, n64, t1, dnT, lane);
     __syncthreads();
     zero(t2);
     tile_mma<2, false, true>(t2, tdT, kLs, m0, tT, kLs, n64, 64, lane);   // dT T^T
     float upZ, dnZ;
-    pow2_up_dn(cta_max(absmax(t2), V(vMax), warp, lane), upZ, dnZ);
+    pow2_up_dn(cta_max(absmax(t2), V(vMax), warp, lane, mpar), upZ, dnZ);
     store_h(tZ, kLs, m0, n64, t2, dnZ, lane);
     __syncthreads();
     zero(t1);
@@ -627,7 +651,7 @@ __device__ __forceinline__ void local_unit(const LocalArgs& a, uint8_t* sm, cons
         t1[nt][e] = dAt;
       }
     float upA, dnA;
-    pow2_up_dn(cta_max(absmax(t1), V(vMax), warp, lane), upA, dnA);
+    pow2_up_dn(cta_max(absmax(t1), V(vMax), warp, lane, mpar), upA, dnA);
     store_h(tdA, kLs, m0, n64, t1, dnA, lane);
     __syncthreads();
     float t3[4][4];
