@@ -58,6 +58,18 @@ def test_fused_prologue_equals_the_separate_calls_bit_for_bit(B, L, with_tail, w
         assert torch.equal(a, b), name
 
 
+@pytest.mark.parametrize("Hk,Hv", [(2, 2), (1, 4), (3, 6)])
+def test_fused_prologue_head_ratios_equal_the_separate_calls(Hk, Hv):
+    """One, four and two value heads per key head: the channel split of the projection (q at key
+    head h / r, k after all of q, v after all of k) and the gates' head index, bit for bit."""
+    x = inputs.prologue_inputs(2, 150, 101 + Hv, Hk=Hk, Hv=Hv, K=4)
+    S0 = initial_state(2, Hv, 102 + Hv)
+    got = fused(x, S0)
+    want = separate(x, S0)
+    for name, a, b in zip(("o", "S_T", "new_tail"), got, want):
+        assert torch.equal(a, b), name
+
+
 @pytest.mark.parametrize("B,L,with_tail", [(2, 200, True), (1, 1, True), (2, 2, True), (1, 3, False), (2, 64, True),
                                            (1, 100, False)])
 def test_fused_prologue_matches_the_oracle_composition(B, L, with_tail):
