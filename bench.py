@@ -484,6 +484,33 @@ def run_fork_decode(reps: int, warmup: int) -> dict:
     return out
 
 
+def _graph_us(call, reps: int, per_graph: int = 24) -> float:
+    """GPU microseconds per call of call(stream), from CUDA-graph replays of per_graph calls (no
+    Python or launch overhead between the kernels: a 15-35 us kernel launched from a Python loop is
+    bound by the loop)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(per_graph):
+            call(s)
+    cur = torch.cuda.current_stream()
+    g.replay()
+    cur.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(1, reps // per_graph + 1)
+    e0.record(cur)
+    for _ in range(n):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (n * per_graph)
+
+
 def run_prologue(reps: int, warmup: int) -> dict:
     """Times the GDN prologue (the first adjacent row: conv + SiLU, gates, carry) on the prefill
     row's shapes, L = 4096, 16 -> 32 heads, K = 4, with its HBM roofline."""
@@ -494,12 +521,17 @@ def run_prologue(reps: int, warmup: int) -> dict:
     d = lambda t: t.cuda().contiguous()
     mixed, w, a, b, A_log, dt_bias, tail = (d(t) for t in (x.mixed, x.conv_w, x.a, x.b, x.A_log, x.dt_bias, x.tail))
     C = mixed.shape[2]
-    outs = gdr.gdr_prologue(mixed, w, a, b, A_log, dt_bias, Hk, Hv, tail=tail)
+    # two input and output sets (272 MB, over twice the L2), used in turn
+    sets = [(mixed, a, b, tail), tuple(t.clone() for t in (mixed, a, b, tail))]
+    outs = [gdr.gdr_prologue(m_, w, a_, b_, A_log, dt_bias, Hk, Hv, tail=t_) for m_, a_, b_, t_ in sets]
     stream = torch.cuda.current_stream()
+    turn = [0]
 
-    def call():
-        gdr.gdr_prologue(mixed, w, a, b, A_log, dt_bias, Hk, Hv, tail=tail, q=outs[0], k=outs[1], v=outs[2],
-                         g=outs[3], beta=outs[4], new_tail=outs[5], stream=stream)
+    def call(st=stream):
+        j = turn[0] = turn[0] ^ 1
+        (m_, a_, b_, t_), o_ = sets[j], outs[j]
+        gdr.gdr_prologue(m_, w, a_, b_, A_log, dt_bias, Hk, Hv, tail=t_, q=o_[0], k=o_[1], v=o_[2], g=o_[3],
+                         beta=o_[4], new_tail=o_[5], stream=st)
 
     # algorithmic bytes: mixed and tail read, q, k, v and the carry written (bf16); a, b read and
     # g, beta written (float32); the weights
@@ -513,7 +545,8 @@ def run_prologue(reps: int, warmup: int) -> dict:
         call()
     e1.record(stream)
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / reps
+    us_eager = e0.elapsed_time(e1) * 1e3 / reps
+    us = _graph_us(call, reps)
     # the kernel's own time from a second pass with the stage timer (its events add a little)
     gdr.stage_timer_enable(True, 4 * reps + 16)
     for _ in range(reps):
@@ -524,8 +557,11 @@ def run_prologue(reps: int, warmup: int) -> dict:
     gdr.gdr_sync_status()
     gbs = nbytes / (us * 1e-6) / 1e9
     peaks = measured_peaks()
-    assert torch.isfinite(outs[3]).all() and torch.isfinite(outs[0].float()).all()
+    assert all(torch.isfinite(o_[3]).all() and torch.isfinite(o_[0].float()).all() for o_ in outs)
     return {"us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1),
+            "timing": "CUDA-graph replays of 24 calls over input sets larger than L2 in turn; us_per_call_eager: "
+                      "the same calls from a Python loop",
+            "us_per_call_eager": round(us_eager, 2),
             "workload": f"GDN prologue L={L} Hk={Hk} Hv={Hv} D={D} K={K} (conv + SiLU, gates, carry), bf16",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes},
@@ -542,12 +578,17 @@ def run_epilogue(reps: int, warmup: int) -> dict:
     x = torch.randn(1, L, Hv, D, generator=gen).bfloat16().cuda()
     z = torch.randn(1, L, Hv, D, generator=gen).bfloat16().cuda()
     w = (0.5 + torch.rand(D, generator=gen)).cuda()
-    out = torch.empty_like(x)
+    # three (x, z, out) sets (302 MB, over twice the L2), used in turn
+    sets = [(x, z, torch.empty_like(x))] + [(x.clone(), z.clone(), torch.empty_like(x)) for _ in range(2)]
+    out = sets[0][2]
     stream = torch.cuda.current_stream()
     nbytes = 3 * x.numel() * 2 + D * 4   # x and z read, out written (bf16), the weight
+    turn = [0]
 
-    def call():
-        gdr.gdr_gated_rmsnorm(x, z, w, 1e-6, out=out, stream=stream)
+    def call(st=stream):
+        turn[0] = (turn[0] + 1) % 3
+        x_, z_, o_ = sets[turn[0]]
+        gdr.gdr_gated_rmsnorm(x_, z_, w, 1e-6, out=o_, stream=st)
 
     for _ in range(warmup):
         call()
@@ -558,7 +599,8 @@ def run_epilogue(reps: int, warmup: int) -> dict:
         call()
     e1.record(stream)
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / reps
+    us_eager = e0.elapsed_time(e1) * 1e3 / reps
+    us = _graph_us(call, reps)
     gdr.stage_timer_enable(True, 4 * reps + 16)
     for _ in range(reps):
         call()
@@ -570,6 +612,9 @@ def run_epilogue(reps: int, warmup: int) -> dict:
     peaks = measured_peaks()
     assert torch.isfinite(out.float()).all()
     return {"us_per_call": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1),
+            "timing": "CUDA-graph replays of 24 calls over input sets larger than L2 in turn; us_per_call_eager: "
+                      "the same calls from a Python loop",
+            "us_per_call_eager": round(us_eager, 2),
             "workload": f"gated RMSNorm over o [1, {L}, {Hv}, {D}] bf16 with gate z",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes},

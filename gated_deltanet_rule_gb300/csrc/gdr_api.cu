@@ -372,9 +372,9 @@ gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w
   if (Hv % Hk != 0) return fail(GDR_ERR_INVALID_ARG, "%s: Hv=%d is not a multiple of Hk=%d", who, Hv, Hk);
   if (K < 1 || K > 8) return fail(GDR_ERR_INVALID_ARG, "%s: conv width K=%d is outside [1, 8]", who, K);
   if (D != kD) return fail(GDR_ERR_UNSUPPORTED, "%s: head dimension D=%d is not implemented (only 128)", who, D);
-  // launch limits: rows are the grid's z dimension, runs of 32 positions its y dimension
-  if ((long long)B > 65535 || (long long)L > 32LL * 65535)
-    return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d or L=%d too large (B <= 65535, L <= 2097120)", who, B, L);
+  // launch limits: rows are the grid's z dimension, tiles of 16 positions its y dimension
+  if ((long long)B > 65535 || (long long)L > 16LL * 65535)
+    return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d or L=%d too large (B <= 65535, L <= 1048560)", who, B, L);
   const void* ptrs16[] = {mixed, q, k, v, tail, new_tail};
   for (const void* p : ptrs16)
     if (p && !aligned16(p)) return fail(GDR_ERR_INVALID_ARG, "%s: mixed, tail, q, k, v and new_tail must be 16-byte aligned", who);
@@ -398,6 +398,7 @@ gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w
   if (!err) return fail(GDR_ERR_CUDA, "%s: no CUDA device available", who);
   PrologueArgs pa{mixed, tail, conv_w, a, b, A_log, dt_bias, lengths, q, k, v, g, beta, new_tail,
                   B, L, Hk, Hv, (int)C, K, err};
+  pa.wait_budget = wait_budget_cycles();
   return launch_status(launch_prologue(pa, reinterpret_cast<cudaStream_t>(stream)), who);
 }
 

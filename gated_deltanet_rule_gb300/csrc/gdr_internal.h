@@ -106,6 +106,7 @@ struct PrologueArgs {
   void* new_tail;
   int B, L, Hk, Hv, C, K;
   int* err;
+  long long wait_budget = 0;   // cycles a wait for the staged tile may take (wait_budget_cycles())
 };
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);
 

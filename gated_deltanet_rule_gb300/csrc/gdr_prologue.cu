@@ -3,24 +3,35 @@
 // (DEG "model.py": _linear_layer, with _conv_silu over ext = [tail, mixed] and _dn_gates.)
 //
 // One streaming kernel, bound by HBM: every input element is read once and every output written
-// once. Each thread runs its part of the convolution: 4 consecutive channels (one 8-byte vector)
-// of one row over a run of positions, with the last K inputs in registers (a sliding window) and
-// eight loads in flight, so a warp reads and writes 256 contiguous bytes per position; fp32
-// arithmetic, one rounding to bf16 at the end. Then it takes a grid-stride share of
+// once. A block takes a tile of 16 positions x 512 channels of one row: one warp copies the tile's
+// ext rows (the 16 positions and the K - 1 before them, 1 KB each) into shared memory by bulk
+// asynchronous copies completing on one mbarrier, so that many kilobytes per SM are in flight
+// without registers; then each thread convolves 4 channels down the 16 positions with the last K
+// inputs in registers (a sliding window), fp32 arithmetic and one rounding to bf16, a warp writing
+// 256 contiguous bytes per position. Then every thread takes a grid-stride share of
 //  - the gates: one (row, position, value head) per element, and
 //  - the carry: 8 channels of one of the K-1 carried positions per element.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "gdr_internal.h"
+#include "ptx.cuh"
 
 namespace gdr {
 namespace {
 
-constexpr int kConvThreads = 128;   // threads per block (8 channels each)
-constexpr int kConvRun = 32;        // positions one thread walks
+using namespace ptx;
+
+constexpr int kConvThreads = 128;                // threads per block (4 channels each)
+constexpr int kConvRun = 16;                     // positions per tile
+constexpr int kTileCh = 4 * kConvThreads;        // channels per tile
+constexpr uint32_t kRowBytes = kTileCh * 2;      // shared-memory row: one ext position of the tile
+constexpr long long kDrainBudget = 2000000000ll; // cycles (~1 s) a block that gave up waits for its copies
+template <int K>
+constexpr uint32_t conv_smem() { return (kConvRun + K - 1) * kRowBytes; }
 
 __device__ __forceinline__ void set_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
@@ -36,17 +47,6 @@ __device__ __forceinline__ uint4 ext_load(const PrologueArgs& a, int b, int e, i
   return __ldg(reinterpret_cast<const uint4*>(a.mixed) + ((size_t)b * a.L + (e - (K - 1))) * (C / 8) + c8);
 }
 
-// 4-channel (8-byte) vectors for the convolution: half the registers of 8-channel vectors, so
-// twice the warps, and twice the loads in flight, per SM
-__device__ __forceinline__ uint2 ext_load4(const PrologueArgs& a, int b, int e, int c4, int K) {
-  const size_t C = a.C;
-  if (e < K - 1) {
-    if (!a.tail) return make_uint2(0, 0);
-    return __ldg(reinterpret_cast<const uint2*>(a.tail) + ((size_t)b * (K - 1) + e) * (C / 4) + c4);
-  }
-  return __ldg(reinterpret_cast<const uint2*>(a.mixed) + ((size_t)b * a.L + (e - (K - 1))) * (C / 4) + c4);
-}
-
 __device__ __forceinline__ void bf16x4_to_f32(uint2 w, float* x) {
   x[0] = __uint_as_float(w.x << 16);
   x[1] = __uint_as_float(w.x & 0xFFFF0000u);
@@ -59,15 +59,42 @@ __device__ __forceinline__ uint2 f32x4_to_bf16(const float* x) {
   return make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
 }
 
-// out[t] = sum_{j < K} w[c][j] ext[t + j]; y = out sigmoid(out), written to q, k or v by channel
+// out[t] = sum_{j < K} w[c][j] ext[t + j]; y = out sigmoid(out), written to q, k or v by channel.
+// The tile's ext rows t0 .. t0 + K + 14 land in stage (row i = ext position t0 + i, kRowBytes
+// apart); rows past the last one that feeds an output (ext position >= L + K - 1) are not loaded.
 template <int K>
-__device__ __forceinline__ void conv_run(const PrologueArgs& a) {
-  const int c4 = blockIdx.x * kConvThreads + threadIdx.x;   // 4-channel vector index
-  const int b = blockIdx.z;
-  const int t0 = blockIdx.y * kConvRun;
-  if (c4 * 4 >= a.C) return;
+__device__ __forceinline__ void conv_run(const PrologueArgs& a, uint8_t* stage, uint64_t* bar) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int c_base = blockIdx.x * kTileCh, b = blockIdx.z, t0 = blockIdx.y * kConvRun;
+  const int nch = min(kTileCh, a.C - c_base);               // a multiple of 128
+  const int rows = min(kConvRun + K - 1, a.L - t0 + K - 1);  // ext rows that feed this tile's outputs
+  const uint32_t row_bytes = (uint32_t)nch * 2;
+  if (!a.tail) {
+    // carried positions without a carry read as zeros
+    for (int i = 0; i < rows && t0 + i < K - 1; ++i)
+      if (4 * tid < nch) *reinterpret_cast<uint2*>(stage + i * kRowBytes + tid * 8) = make_uint2(0, 0);
+  }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int first = a.tail ? 0 : max(0, K - 1 - t0);   // the rows before it are zeros, not copies
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(rows - first) * row_bytes);
+    __syncwarp();
+    for (int i = first + lane; i < rows; i += 32) {
+      const int e = t0 + i;
+      const uint8_t* src = e < K - 1
+          ? static_cast<const uint8_t*>(a.tail) + (((size_t)b * (K - 1) + e) * a.C + c_base) * 2
+          : static_cast<const uint8_t*>(a.mixed) + (((size_t)b * a.L + (e - (K - 1))) * a.C + c_base) * 2;
+      bulk_load(stage + i * kRowBytes, src, row_bytes, bar);
+    }
+  }
+  const int c4 = c_base / 4 + tid;   // this thread's 4-channel vector
+  const bool mine = 4 * tid < nch;
   float w[K][4];   // this thread's 4 x K weights are 4 K contiguous floats (16-byte aligned: 16 K bytes)
-  {
+  if (mine) {
     const float4* w4 = reinterpret_cast<const float4*>(a.conv_w + (size_t)c4 * 4 * K);
 #pragma unroll
     for (int i = 0; i < K; ++i) {
@@ -77,6 +104,18 @@ __device__ __forceinline__ void conv_run(const PrologueArgs& a) {
       for (int u = 0; u < 4; ++u) w[(4 * i + u) % K][(4 * i + u) / K] = fv[u];
     }
   }
+  // every thread waits for the copies (bounded); a block that gives up records the timeout and waits
+  // once more for its copies before it leaves
+  const bool ok = mbar_wait(bar, 0, a.wait_budget);
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) {
+      set_error(a.err, kErrTimeout);
+      mbar_wait(bar, 0, kDrainBudget);
+    }
+    __syncthreads();
+    return;
+  }
+  if (!mine) return;
   // destination: channels [0, HkD) -> q, [HkD, 2 HkD) -> k, the rest -> v (4-channel vectors never
   // straddle a boundary, since the boundaries are multiples of 128)
   const int HkD = a.Hk * kD, c0 = c4 * 4;
@@ -92,36 +131,27 @@ __device__ __forceinline__ void conv_run(const PrologueArgs& a) {
     dst = reinterpret_cast<uint2*>(a.v) + (c0 - 2 * HkD) / 4;
     stride4 = (size_t)a.Hv * kD / 4;
   }
-  float win[K][4];   // ext positions t .. t + K - 1 (the last one is loaded in the loop)
+  const uint8_t* col = stage + tid * 8;
+  float win[K][4];   // ext positions t .. t + K - 1
 #pragma unroll
-  for (int j = 0; j < K - 1; ++j) bf16x4_to_f32(ext_load4(a, b, t0 + j, c4, K), win[j]);
-  const int tend = min(t0 + kConvRun, a.L);
-  // ext position t + K - 1 is the new input t: eight of them are loaded before any is used
-  const uint2* src = reinterpret_cast<const uint2*>(a.mixed) + (size_t)b * a.L * (a.C / 4) + c4;
-  for (int tg = t0; tg < tend; tg += 8) {
-    uint2 xr[8];
+  for (int j = 0; j < K - 1; ++j) bf16x4_to_f32(*reinterpret_cast<const uint2*>(col + j * kRowBytes), win[j]);
+  const int n = min(kConvRun, a.L - t0);
+#pragma unroll 4
+  for (int u = 0; u < n; ++u) {
+    bf16x4_to_f32(*reinterpret_cast<const uint2*>(col + (u + K - 1) * kRowBytes), win[K - 1]);
+    float y[4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      xr[u] = tg + u < tend ? __ldcs(src + (size_t)(tg + u) * (a.C / 4)) : make_uint2(0, 0);   // read once
+    for (int e = 0; e < 4; ++e) {
+      float sacc = 0.f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (tg + u < tend) {
-        bf16x4_to_f32(xr[u], win[K - 1]);
-        float y[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float s = 0.f;
-#pragma unroll
-          for (int j = 0; j < K; ++j) s = fmaf(w[j][e], win[j][e], s);
-          y[e] = __fdividef(s, 1.f + __expf(-s));   // one rounding to bf16 follows
-        }
-        dst[((size_t)b * a.L + tg + u) * stride4] = f32x4_to_bf16(y);
-#pragma unroll
-        for (int j = 0; j < K - 1; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) win[j][e] = win[j + 1][e];
-      }
+      for (int j = 0; j < K; ++j) sacc = fmaf(w[j][e], win[j][e], sacc);
+      y[e] = __fdividef(sacc, 1.f + __expf(-sacc));   // one rounding to bf16 follows
     }
+    dst[((size_t)b * a.L + t0 + u) * stride4] = f32x4_to_bf16(y);
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) win[j][e] = win[j + 1][e];
   }
 }
 
@@ -165,10 +195,12 @@ __device__ __forceinline__ void carry_element(const PrologueArgs& a, long long i
 // share of the gates and of the carry (grid-stride over their elements).
 template <int K>
 __global__ void __launch_bounds__(kConvThreads) prologue_kernel(const PrologueArgs a) {
+  extern __shared__ __align__(16) uint8_t stage[];
+  __shared__ uint64_t bar;
   const long long nthreads = (long long)gridDim.x * gridDim.y * gridDim.z * kConvThreads;
   const long long gtid =
       (((long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * kConvThreads + threadIdx.x;
-  conv_run<K>(a);
+  conv_run<K>(a, stage, &bar);
   const long long ngates = (long long)a.B * a.L * a.Hv;
   for (long long i = gtid; i < ngates; i += nthreads) gate_element(a, i);
   if (K > 1 && a.new_tail) {
@@ -179,9 +211,22 @@ __global__ void __launch_bounds__(kConvThreads) prologue_kernel(const PrologueAr
 
 template <int K>
 cudaError_t launch_conv(const PrologueArgs& a, cudaStream_t s) {
-  const dim3 grid((unsigned)((a.C / 4 + kConvThreads - 1) / kConvThreads), (unsigned)((a.L + kConvRun - 1) / kConvRun),
+  const dim3 grid((unsigned)((a.C + kTileCh - 1) / kTileCh), (unsigned)((a.L + kConvRun - 1) / kConvRun),
                   (unsigned)a.B);
-  prologue_kernel<K><<<grid, kConvThreads, 0, s>>>(a);
+  // (below the default 48 KB; the largest carveout lets ten or more blocks share an SM. Set once per
+  // device ordinal: it is a hint, and a call per launch costs host time a 30 us kernel notices)
+  static std::atomic<unsigned long long> set_on{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (!bit || !(set_on.load() & bit)) {
+    e = cudaFuncSetAttribute(prologue_kernel<K>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    set_on.fetch_or(bit);
+  }
+  prologue_kernel<K><<<grid, kConvThreads, conv_smem<K>(), s>>>(a);
   return cudaGetLastError();
 }
 

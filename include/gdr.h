@@ -198,7 +198,7 @@ gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
  *   q, k     [B, L, Hk, D] bfloat16;  v [B, L, Hv, D] bfloat16
  *   g, beta  [B, L, Hv] float32
  *   new_tail [B, K-1, C] bfloat16         NULL = not written; must not overlap tail or mixed
- * K is the convolution width, 1 <= K <= 8 (the pages use 4); B <= 65535 and L <= 2097120
+ * K is the convolution width, 1 <= K <= 8 (the pages use 4); B <= 65535 and L <= 1048560
  * (GDR_ERR_UNSUPPORTED otherwise). Arithmetic is float32 from the
  * bfloat16 inputs, with one rounding of q, k, v to bfloat16.
  */

@@ -137,7 +137,7 @@ def test_prologue_rejects_bad_arguments(L):
     assert _prologue(L, tail=P, new_tail=P) == gdr.GDR_ERR_INVALID_ARG
     assert b"overlap" in L.gdr_last_error_message()
     assert _prologue(L, new_tail=ctypes.c_void_p((1 << 20) + 4096)) == gdr.GDR_ERR_INVALID_ARG
-    assert _prologue(L, Lt=32 * 65535 + 1) == gdr.GDR_ERR_UNSUPPORTED
+    assert _prologue(L, Lt=16 * 65535 + 1) == gdr.GDR_ERR_UNSUPPORTED
     assert _prologue(L, B=65536) == gdr.GDR_ERR_UNSUPPORTED
 
 
