@@ -662,6 +662,29 @@ def run_backward(reps: int, warmup: int) -> dict:
     loop = timed(gdr.gdr_backward, gdr.backward_workspace_bytes(1, L, Hk, Hv))
     loop["roofline"]["note"] = "a sequential token loop on CUDA cores: latency-bound, far from this roofline"
     row["token_loop_float32"] = loop
+    # a training step's forward + backward: checkpointed (gdr_chunk_fwd, then the backward recomputes
+    # the forward's passes) against kept intermediates (gdr_chunk_fwd_save, gdr_backward_chunked_saved)
+    wsb = gdr.backward_chunked_workspace_bytes(1, L, Hk, Hv)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    fws = torch.empty(max(1, gdr.workspace_bytes(1, L, Hk, Hv)), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(v)
+    S_T = torch.empty(1, Hv, D, D, dtype=torch.float32, device="cuda")
+
+    def recompute(_i):
+        gdr.gdr_chunk_fwd(q, k, v, g, beta, None, o=o, S_T=S_T, ws=fws, stream=stream)
+        gdr.gdr_backward_chunked(q, k, v, g, beta, None, dO, dS_T, ws=ws, stream=stream)
+
+    def keep(_i):
+        gdr.gdr_chunk_fwd_save(q, k, v, g, beta, None, saved=ws, o=o, S_T=S_T, stream=stream)
+        gdr.gdr_backward_chunked(q, k, v, g, beta, None, dO, dS_T, saved=ws, stream=stream)
+
+    step = {"workload": f"forward + backward of the prefill row [1, {L}], Hk={Hk}, Hv={Hv}, D={D}, bf16",
+            "saved_bytes": wsb}
+    for name, fn in (("checkpointed", recompute), ("kept_intermediates", keep)):
+        us, stages = _time_calls(fn, reps, warmup, stream)
+        step[name] = {"us_per_step": round(us, 2), "tokens_per_s": round(L / (us * 1e-6), 1), "kernels": stages}
+    gdr.gdr_sync_status()
+    row["training_step"] = step
     return row
 
 

@@ -501,11 +501,14 @@ size_t gdr_backward_chunked_workspace_bytes(int B, int L, int Hk, int Hv, int D)
   return chunk_bwd_workspace_bytes(B, L, Hk, Hv);
 }
 
-gdr_status gdr_backward_chunked(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                                const float* S0, const void* dO, const float* dS_T, float* dq, float* dk,
-                                float* dv, float* dg, float* dbeta, float* dS0, int B, int L, int Hk, int Hv,
-                                int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream) {
-  const char* who = "gdr_backward_chunked";
+}  // extern "C"
+
+// gdr_backward_chunked and gdr_backward_chunked_saved (saved: ws holds what gdr_chunk_fwd_save left)
+static gdr_status backward_chunked(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                   const float* S0, const void* dO, const float* dS_T, float* dq, float* dk,
+                                   float* dv, float* dg, float* dbeta, float* dS0, int B, int L, int Hk, int Hv,
+                                   int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream, bool saved,
+                                   const char* who) {
   if (!dO) return fail(GDR_ERR_INVALID_ARG, "%s: dO must be non-NULL", who);
   gdr_status st = check_common(q, k, v, g, beta, dO, B, L, Hk, Hv, D, dt, who);
   if (st != GDR_OK) return st;
@@ -530,7 +533,61 @@ gdr_status gdr_backward_chunked(const void* q, const void* k, const void* v, con
   int* err = device_error_word();
   if (!err) return fail(GDR_ERR_CUDA, "%s: no device error word", who);
   ChunkBackwardArgs a{q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, ws, B, L, Hk, Hv, err};
+  a.saved = saved;
   return launch_status(launch_chunk_backward(a, reinterpret_cast<cudaStream_t>(stream)), who);
+}
+
+extern "C" {
+
+gdr_status gdr_backward_chunked(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                const float* S0, const void* dO, const float* dS_T, float* dq, float* dk,
+                                float* dv, float* dg, float* dbeta, float* dS0, int B, int L, int Hk, int Hv,
+                                int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream) {
+  return backward_chunked(q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, B, L, Hk, Hv, D, dt, ws,
+                          ws_bytes, stream, false, "gdr_backward_chunked");
+}
+
+gdr_status gdr_backward_chunked_saved(const void* q, const void* k, const void* v, const float* g,
+                                      const float* beta, const float* S0, const void* dO, const float* dS_T,
+                                      float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dS0, int B,
+                                      int L, int Hk, int Hv, int D, gdr_dtype dt, void* saved, size_t saved_bytes,
+                                      gdr_stream_t stream) {
+  return backward_chunked(q, k, v, g, beta, S0, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, B, L, Hk, Hv, D, dt, saved,
+                          saved_bytes, stream, true, "gdr_backward_chunked_saved");
+}
+
+gdr_status gdr_chunk_fwd_save(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              const float* S0, void* o, float* S_T, int B, int L, int Hk, int Hv, int D,
+                              gdr_dtype dt, void* saved, size_t saved_bytes, gdr_stream_t stream) {
+  const char* who = "gdr_chunk_fwd_save";
+  gdr_status st = check_common(q, k, v, g, beta, o, B, L, Hk, Hv, D, dt, who);
+  if (st != GDR_OK) return st;
+  if (dt != GDR_BF16) return fail(GDR_ERR_UNSUPPORTED, "%s: bf16 q, k, v only (the chunked backward's forward)", who);
+  if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T)) || (saved && !aligned16(saved)))
+    return fail(GDR_ERR_INVALID_ARG, "%s: S0, S_T and saved must be 16-byte aligned", who);
+  const long long units = (long long)B * Hv * ((L + kChunk - 1) / kChunk);
+  if (units > 0x7fffffffLL || Hk > 65535 || Hv > 65535 || B > 65535)
+    return fail(GDR_ERR_UNSUPPORTED, "%s: B=%d, L=%d, Hv=%d too large", who, B, L, Hv);
+  const size_t need = chunk_bwd_workspace_bytes(B, L, Hk, Hv);
+  if (saved == nullptr || saved_bytes < need)
+    return fail(GDR_ERR_INVALID_ARG, "%s: saved buffer of %zu bytes needed, %zu given", who, need,
+                saved == nullptr ? (size_t)0 : saved_bytes);
+  // the saved buffer is written while every input is read and the outputs are written
+  const size_t nq = (size_t)B * L * Hk * kD * 2, nv = (size_t)B * L * Hv * kD * 2, ng = (size_t)B * L * Hv * 4;
+  const size_t ns = (size_t)B * Hv * kD * kD * 4;
+  const struct { const void* p; size_t n; } others[] = {{q, nq}, {k, nq}, {v, nv}, {g, ng}, {beta, ng},
+                                                        {S0, ns}, {o, nv}, {S_T, ns}};
+  const uintptr_t w0 = reinterpret_cast<uintptr_t>(saved), w1 = w0 + need;
+  for (const auto& r : others) {
+    const uintptr_t p0 = reinterpret_cast<uintptr_t>(r.p);
+    if (r.p && p0 < w1 && w0 < p0 + r.n)
+      return fail(GDR_ERR_INVALID_ARG, "%s: saved overlaps an input or an output", who);
+  }
+  int* err = device_error_word();
+  if (!err) return fail(GDR_ERR_CUDA, "%s: no CUDA device available", who);
+  return launch_status(launch_chunk_forward_saving(q, k, v, g, beta, S0, o, S_T, saved, B, L, Hk, Hv, err,
+                                                   reinterpret_cast<cudaStream_t>(stream)),
+                       who);
 }
 
 gdr_status gdr_sync_status(gdr_stream_t stream) {

@@ -69,9 +69,32 @@ struct ChunkBwdChainLaunch {
   void* ws;
   int B, L, Hk, Hv;
   int* err;
+  bool saved = false;  // the factors, S_save, S_scale and v's scales are in place: adjoint chain only
 };
 size_t chunk_bwd_units_bytes(int B, int L, int Hv);
 cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s);
+
+// The forward (o, S_T, as the bf16 prefill computes them) that also leaves what the chunked
+// backward's sequential passes would recompute: the chunk factors in ws, the chunk-entry states in
+// S_save / S_scale and v's powers of two in unit_scale (word 4), in the layout of
+// ChunkBwdChainLaunch (rows of one chunk included).
+struct ChunkFwdSaveLaunch {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const float* S0;
+  void* o;
+  float* S_T;
+  __half* S_save;
+  float* S_scale;
+  float* unit_scale;
+  void* ws;
+  int B, L, Hk, Hv;
+  int* err;
+};
+cudaError_t launch_chunk_fwd_save(const ChunkFwdSaveLaunch& p, cudaStream_t s);
 
 // The chunked backward of bf16 rows (q, k, v, dO bf16; g, beta, S0, dS_T and every gradient
 // float32): the sequential passes above, then the chunk-local gradients, one CTA per (row, key head,
@@ -95,8 +118,14 @@ struct ChunkBackwardArgs {
   void* ws;
   int B, L, Hk, Hv;
   int* err;
+  bool saved = false;  // ws holds what launch_chunk_forward_saving left: skip the forward passes
 };
 size_t chunk_bwd_workspace_bytes(int B, int L, int Hk, int Hv);
 cudaError_t launch_chunk_backward(const ChunkBackwardArgs& p, cudaStream_t s);
+// The bf16 prefill (o, S_T) leaving in ws (chunk_bwd_workspace_bytes) the forward passes'
+// results for launch_chunk_backward with saved = true.
+cudaError_t launch_chunk_forward_saving(const void* q, const void* k, const void* v, const float* g,
+                                        const float* beta, const float* S0, void* o, float* S_T, void* ws,
+                                        int B, int L, int Hk, int Hv, int* err, cudaStream_t s);
 
 }  // namespace gdr

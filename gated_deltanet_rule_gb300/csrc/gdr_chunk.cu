@@ -1064,11 +1064,13 @@ static_assert(kCN == kMBytes && kOPU == kQBytes, "stage layout");
 // warps turn dO into fp16 divided by its power of two; warp 7 issues the product into the TMEM
 // slots the forward's O' uses) and the state warps read it from TMEM; the initial state is dS_T
 // (a.S0), the final one dS0 (a.S_T), and the adjoint entering each chunk's step (that of its
-// exiting state) is saved likewise.
+// exiting state) is saved likewise. kMode 3: the forward of kMode 0 that also saves what kMode 1
+// saves (for a backward that then skips its forward passes); a state operand buffer is free once
+// both the output product and its store have read it.
 template <int CS, int OS, bool kGated, int kMode>
 __global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do) {
-  constexpr bool kOut = kMode == 0;   // the output side forms o
+  constexpr bool kOut = kMode == 0 || kMode == 3;   // the output side forms o
   constexpr bool kNb = kMode == 2;    // the output side forms Nb = Q'^T dO
   constexpr uint32_t kOffO = CS * kCStage;
   constexpr uint32_t kOffSb = kOffO + OS * kOStage;
@@ -1123,7 +1125,7 @@ chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do)
     }
     for (int q = 0; q < kSb; ++q) {
       mbar_init(&sReady[q], 1);
-      mbar_init(&sFree[q], 1);
+      mbar_init(&sFree[q], kMode == 3 ? 2 : 1);
     }
     for (int r = 0; r < 8; ++r) mbar_init(&scRdy[r], 4);
     for (int s2 = 0; s2 < OS; ++s2) mbar_init(&doRdy[s2], 1);
@@ -1277,7 +1279,7 @@ chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do)
       const int cs = c % CS, p = c & 1, qn = (c + 1) % kSb;
       const uint8_t* st = sm + cs * kCStage;
       ok = ok && mbar_wait(&chFull[cs], (c / CS) & 1, a.wait_budget) && !*(volatile int*)&abort_flag;
-      if (kMode == 1 && sl == 0 && tid == 0 && ok)
+      if ((kMode == 1 || kMode == 3) && sl == 0 && tid == 0 && ok)
         a.unit_scale[(((size_t)b * a.Hv + h) * NC + c) * 8 + 4] = gam_ring[cs].y;   // v's power of two
       if (kNb) {
         // Nb_c = Q'_c^T dO_c in TMEM slot p (and its scale in nb_scl)
@@ -1308,8 +1310,8 @@ chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do)
             for (int e = 0; e < 8; ++e) Sm[8 * ch + e] = fmaf(gc, Sm[8 * ch + e], upV * nv[e]);
           }
         }
-        // Sb[qn] is rewritten below: the output product (modes 1, 2: the bulk store) of chunk
-        // c + 1 - kSb must have read it
+        // Sb[qn] is rewritten below: the output product (modes 1, 2: the bulk store; mode 3: both)
+        // of chunk c + 1 - kSb must have read it
         ok = mbar_wait(&bar_d, c & 1, a.wait_budget) &&
              (c + 1 < kSb || mbar_wait(&sFree[qn], ((c + 1 - kSb) / kSb) & 1, a.wait_budget));
       }
@@ -1365,8 +1367,9 @@ chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do)
         mma_commit(&bar_d);
         mbar_arrive(&sReady[q]);   // Sb[q] holds S_c: warp 7 may issue the output product
         if (kMode != 0) {
-          // modes 1, 2: the step's operand (the state at its top, over its slice's power of two)
-          // to st_save; the previous step's buffer is free once its store has read it
+          // modes 1, 2, 3: the step's operand (the state at its top, over its slice's power of two)
+          // to st_save; the previous step's buffer is free once its store has read it (mode 3:
+          // and once the output product has read it, the barrier's other arrival)
           const int cu = kMode == 2 ? NC - 1 - c : c;
           bulk_store(a.st_save + (((size_t)b * a.Hv + h) * NC + cu) * kD * kD + sl * kD * kN, sm + kOffSb + q * 8192,
                      8192);
@@ -1771,12 +1774,15 @@ cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s)
     e = cudaFuncSetAttribute(chunk_state_kernel<3, 3, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              state_smem(3, 3));
   if (e != cudaSuccess) return e;
-  // 1. the forward's chunk factors
   const long long units = (long long)a.B * a.Hv * a.NC;
-  int slot = stage_timer_begin(s, kKernChunkPrep);
-  chunk_prep_kernel<false><<<(int)std::min<long long>(units, 2ll * num_sms()), kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
-  stage_timer_end(slot, s);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  int slot = -1;
+  if (!p.saved) {
+    // 1. the forward's chunk factors
+    slot = stage_timer_begin(s, kKernChunkPrep);
+    chunk_prep_kernel<false><<<(int)std::min<long long>(units, 2ll * num_sms()), kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
+    stage_timer_end(slot, s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   // 2. the chunk-entry states (a programmatic dependent of the prep kernel, as in the forward)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kSlices, p.Hv, p.B);
@@ -1792,11 +1798,13 @@ cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s)
   a.st_scale = p.S_scale;
   a.unit_scale = p.unit_scale;
   a.S_T = nullptr;
-  const CUtensorMap no_map{};   // (the forward pass reads no dO)
-  slot = stage_timer_begin(s, kKernChunkState);
-  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 1>, a, no_map);
-  stage_timer_end(slot, s);
-  if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!p.saved) {
+    const CUtensorMap no_map{};   // (the forward pass reads no dO)
+    slot = stage_timer_begin(s, kKernChunkState);
+    e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 1>, a, no_map);
+    stage_timer_end(slot, s);
+    if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   // 3. the adjoint chain (Nb = Q'^T dO formed on its output side): dS_T in, dS0 out, the adjoint
   //    entering each chunk's step saved
   a.S0 = p.dS_T;
@@ -1805,6 +1813,57 @@ cudaError_t launch_chunk_bwd_chain(const ChunkBwdChainLaunch& p, cudaStream_t s)
   a.st_scale = p.dS_scale;
   slot = stage_timer_begin(s, kKernChunkAdjoint);
   e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 2>, a, mo);
+  stage_timer_end(slot, s);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_fwd_save(const ChunkFwdSaveLaunch& p, cudaStream_t s) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, p.q, p.B, p.L, p.Hk) || !make_map(&mk, p.k, p.B, p.L, p.Hk) ||
+      !make_map(&mv, p.v, p.B, p.L, p.Hv))
+    return cudaErrorInvalidValue;
+  ChunkArgs a{};
+  a.g = p.g;
+  a.beta = p.beta;
+  a.S0 = p.S0;
+  a.fused = 0;   // rows of one chunk also go through the workspace: the backward reads their factors
+  a.wait_budget = wait_budget_cycles();
+  a.o = static_cast<__nv_bfloat16*>(p.o);
+  a.S_T = p.S_T;
+  a.ws = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p.ws) + 1023) & ~uintptr_t(1023));
+  a.B = p.B;
+  a.L = p.L;
+  a.Hk = p.Hk;
+  a.Hv = p.Hv;
+  a.NC = (p.L + kChunk - 1) / kChunk;
+  a.err = p.err;
+  a.st_save = p.S_save;
+  a.st_scale = p.S_scale;
+  a.unit_scale = p.unit_scale;
+  cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(chunk_state_kernel<3, 3, false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             state_smem(3, 3));
+  if (e != cudaSuccess) return e;
+  const long long units = (long long)a.B * a.Hv * a.NC;
+  int slot = stage_timer_begin(s, kKernChunkPrep);
+  chunk_prep_kernel<false><<<(int)std::min<long long>(units, 2ll * num_sms()), kPrepThreads, kPrepSmem, s>>>(mq, mk, mv, a);
+  stage_timer_end(slot, s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kSlices, p.Hv, p.B);
+  cfg.blockDim = dim3(kStateThreads, 1, 1);
+  cfg.dynamicSmemBytes = state_smem(3, 3);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const CUtensorMap no_map{};
+  slot = stage_timer_begin(s, kKernChunkState);
+  e = cudaLaunchKernelEx(&cfg, chunk_state_kernel<3, 3, false, 3>, a, no_map);
   stage_timer_end(slot, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

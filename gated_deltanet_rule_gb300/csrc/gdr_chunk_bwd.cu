@@ -815,24 +815,55 @@ size_t chunk_bwd_workspace_bytes(int B, int L, int Hk, int Hv) {
   return align256(chunk_bwd_units_bytes(B, L, Hv)) + 2 * align256(states) + 2 * align256(scales) + align256(uscales);
 }
 
+// the chunked backward's workspace: the chunk factors, then S_save, dS_save, S_scale, dS_scale and
+// the per-unit scales
+struct BwdWorkspace {
+  uint8_t* units;
+  __half* S_save;
+  __half* dS_save;
+  float* S_scale;
+  float* dS_scale;
+  float* unit_scale;
+};
+static BwdWorkspace split_workspace(void* ws, int B, int L, int Hv) {
+  const size_t NC = ((size_t)L + kChunk - 1) / kChunk;
+  const size_t states = (size_t)B * Hv * NC * kD * kD * sizeof(__half);
+  const size_t scales = (size_t)B * Hv * NC * kStateSlices * sizeof(float);
+  BwdWorkspace r;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  r.units = w;
+  w += align256(chunk_bwd_units_bytes(B, L, Hv));
+  r.S_save = reinterpret_cast<__half*>(w);
+  w += align256(states);
+  r.dS_save = reinterpret_cast<__half*>(w);
+  w += align256(states);
+  r.S_scale = reinterpret_cast<float*>(w);
+  w += align256(scales);
+  r.dS_scale = reinterpret_cast<float*>(w);
+  w += align256(scales);
+  r.unit_scale = reinterpret_cast<float*>(w);
+  return r;
+}
+
+cudaError_t launch_chunk_forward_saving(const void* q, const void* k, const void* v, const float* g,
+                                        const float* beta, const float* S0, void* o, float* S_T, void* ws,
+                                        int B, int L, int Hk, int Hv, int* err, cudaStream_t s) {
+  const BwdWorkspace w = split_workspace(ws, B, L, Hv);
+  ChunkFwdSaveLaunch fl{q, k, v, g, beta, S0, o, S_T, w.S_save, w.S_scale, w.unit_scale, w.units, B, L, Hk, Hv, err};
+  return launch_chunk_fwd_save(fl, s);
+}
+
 cudaError_t launch_chunk_backward(const ChunkBackwardArgs& p, cudaStream_t s) {
   const size_t NC = ((size_t)p.L + kChunk - 1) / kChunk;
-  const size_t states = (size_t)p.B * p.Hv * NC * kD * kD * sizeof(__half);
-  const size_t scales = (size_t)p.B * p.Hv * NC * kStateSlices * sizeof(float);
-  uint8_t* w = static_cast<uint8_t*>(p.ws);
-  uint8_t* unit_ws = w;
-  w += align256(chunk_bwd_units_bytes(p.B, p.L, p.Hv));
-  __half* S_save = reinterpret_cast<__half*>(w);
-  w += align256(states);
-  __half* dS_save = reinterpret_cast<__half*>(w);
-  w += align256(states);
-  float* S_scale = reinterpret_cast<float*>(w);
-  w += align256(scales);
-  float* dS_scale = reinterpret_cast<float*>(w);
-  w += align256(scales);
-  float* unit_scale = reinterpret_cast<float*>(w);
+  const BwdWorkspace w = split_workspace(p.ws, p.B, p.L, p.Hv);
+  __half* S_save = w.S_save;
+  __half* dS_save = w.dS_save;
+  float* S_scale = w.S_scale;
+  float* dS_scale = w.dS_scale;
+  float* unit_scale = w.unit_scale;
   ChunkBwdChainLaunch cl{p.q, p.k, p.v, p.g, p.beta, p.S0, p.dO, p.dS_T, p.dS0, S_save, S_scale, dS_save, dS_scale,
-                         unit_scale, unit_ws, p.B, p.L, p.Hk, p.Hv, p.err};
+                         unit_scale, w.units, p.B, p.L, p.Hk, p.Hv, p.err};
+  cl.saved = p.saved;
   cudaError_t e = launch_chunk_bwd_chain(cl, s);
   if (e != cudaSuccess) return e;
   LocalArgs la{static_cast<const __nv_bfloat16*>(p.q), static_cast<const __nv_bfloat16*>(p.k),

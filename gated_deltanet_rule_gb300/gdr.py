@@ -26,6 +26,7 @@ EXPORTS = ["gdr_chunk_workspace_bytes", "gdr_chunk_fwd", "gdr_chunk_fwd_varlen",
            "gdr_fork_fwd", "gdr_decode_step", "gdr_prologue", "gdr_gated_rmsnorm",
            "gdr_backward_workspace_bytes", "gdr_backward",
            "gdr_backward_chunked_workspace_bytes", "gdr_backward_chunked",
+           "gdr_chunk_fwd_save", "gdr_backward_chunked_saved",
            "gdr_sync_status", "gdr_status_string", "gdr_last_error_message",
            "gdr_stage_timer_enable", "gdr_stage_timer_collect", "gdr_kernel_name", "gdr_debug_set_wait_budget"]
 
@@ -82,6 +83,10 @@ def lib() -> ctypes.CDLL:
     L.gdr_backward_chunked.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp, sz,
                                        vp]
     L.gdr_backward_chunked.restype = i
+    L.gdr_backward_chunked_saved.argtypes = L.gdr_backward_chunked.argtypes
+    L.gdr_backward_chunked_saved.restype = i
+    L.gdr_chunk_fwd_save.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, i, i, i, i, i, i, vp, sz, vp]
+    L.gdr_chunk_fwd_save.restype = i
     L.gdr_sync_status.argtypes = [vp]
     L.gdr_sync_status.restype = i
     L.gdr_status_string.argtypes = [i]
@@ -376,9 +381,34 @@ def backward_chunked_workspace_bytes(B: int, L: int, Hk: int, Hv: int, D: int = 
     return int(lib().gdr_backward_chunked_workspace_bytes(B, L, Hk, Hv, D))
 
 
-def gdr_backward_chunked(q, k, v, g, beta, S0, dO, dS_T=None, ws=None, stream=None, want_dS0: bool = True):
+def gdr_chunk_fwd_save(q, k, v, g, beta, S0=None, saved=None, o=None, S_T=None, stream=None,
+                       final_state: bool = True):
+    """gdr_chunk_fwd for bf16 rows that also keeps, in ``saved`` (a uint8 CUDA buffer of
+    backward_chunked_workspace_bytes; allocated if None), what gdr_backward_chunked would recompute.
+    Returns (o, S_T or None, saved); pass saved to gdr_backward_chunked(..., saved=saved)."""
+    B, L, Hk, Hv, Dk = _check_inputs(q, k, v, g, beta)
+    _need(q.dtype == torch.bfloat16, "gdr_chunk_fwd_save takes bf16 q, k, v")
+    if o is None:
+        o = torch.empty_like(v)
+    if S_T is None and final_state:
+        S_T = torch.empty(B, Hv, Dk, v.shape[3], device=v.device, dtype=torch.float32)
+    for name, t in (("S0", S0), ("S_T", S_T)):
+        if t is not None:
+            _need(t.dtype == torch.float32 and t.is_contiguous() and t.is_cuda, f"{name} must be contiguous CUDA float32")
+    need = backward_chunked_workspace_bytes(B, L, Hk, Hv, Dk)
+    if saved is None:
+        saved = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(lib().gdr_chunk_fwd_save(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(o), _p(S_T), B, L, Hk, Hv, Dk,
+                                    _dtype_code(q), _p(saved), saved.numel() * saved.element_size(), _stream(stream)))
+    return o, S_T, saved
+
+
+def gdr_backward_chunked(q, k, v, g, beta, S0, dO, dS_T=None, ws=None, stream=None, want_dS0: bool = True,
+                         saved=None):
     """gdr_backward's gradients for bf16 q, k, v, dO, computed chunk by chunk on the tensor cores
-    (bf16-path accuracy); same arguments and results."""
+    (bf16-path accuracy); same arguments and results. With ``saved`` (the buffer gdr_chunk_fwd_save
+    filled on the same q, k, v, g, beta, S0) the forward passes are not run again
+    (gdr_backward_chunked_saved)."""
     B, L, Hk, Hv, Dk = _check_inputs(q, k, v, g, beta)
     _need(q.dtype == torch.bfloat16, "gdr_backward_chunked takes bf16 q, k, v, dO (float32: gdr_backward)")
     _need(isinstance(dO, torch.Tensor) and dO.is_cuda and dO.is_contiguous() and dO.dtype == q.dtype
@@ -395,12 +425,15 @@ def gdr_backward_chunked(q, k, v, g, beta, S0, dO, dS_T=None, ws=None, stream=No
     dbeta = torch.empty(beta.shape, **f32)
     dS0 = torch.empty(B, Hv, Dk, v.shape[3], **f32) if want_dS0 else None
     need = backward_chunked_workspace_bytes(B, L, Hk, Hv, Dk)
+    if saved is not None:
+        _need(ws is None, "pass either ws or saved")
+        ws = saved
     if ws is None:
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     ws_bytes = ws.numel() * ws.element_size()
-    _check(lib().gdr_backward_chunked(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(dO), _p(dS_T), _p(dq),
-                                      _p(dk), _p(dv), _p(dg), _p(dbeta), _p(dS0), B, L, Hk, Hv, Dk, _dtype_code(q),
-                                      _p(ws), ws_bytes, _stream(stream)))
+    fn = lib().gdr_backward_chunked_saved if saved is not None else lib().gdr_backward_chunked
+    _check(fn(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(S0), _p(dO), _p(dS_T), _p(dq), _p(dk), _p(dv), _p(dg),
+              _p(dbeta), _p(dS0), B, L, Hk, Hv, Dk, _dtype_code(q), _p(ws), ws_bytes, _stream(stream)))
     return dq, dk, dv, dg, dbeta, dS0
 
 

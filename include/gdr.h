@@ -296,6 +296,30 @@ gdr_status gdr_backward_chunked(const void* q, const void* k, const void* v, con
                                 float* dv, float* dg, float* dbeta, float* dS0, int B, int L, int Hk, int Hv,
                                 int D, gdr_dtype dt, void* ws, size_t ws_bytes, gdr_stream_t stream);
 
+/*
+ * The chunked backward without its recomputation, for callers that keep the forward's
+ * intermediates instead of checkpointing (the DEG model recomputes them; both give the same
+ * gradients). gdr_chunk_fwd_save is gdr_chunk_fwd for bf16 rows (o and S_T as gdr_chunk_fwd
+ * computes them for rows longer than one chunk, bit for bit; rows of one chunk take the two-kernel
+ * path, equal within the bf16 tolerance) that also leaves in `saved` what gdr_backward_chunked's
+ * sequential forward passes would recompute: the per-chunk factors, the fp16 chunk-entry states
+ * with their powers of two, and v's powers of two. gdr_backward_chunked_saved then runs only the
+ * adjoint chain and the chunk-local gradients; its results equal gdr_backward_chunked's bit for bit.
+ *   saved  at least gdr_backward_chunked_workspace_bytes(B, L, Hk, Hv, D) bytes, 16-byte aligned,
+ *          owned by the caller, overlapping no input or output. Between the two calls it must stay
+ *          untouched and the backward must be given the same q, k, v, g, beta and S0 (nothing
+ *          checks this: other inputs give wrong gradients, not an error).
+ * Arguments, sizes and checks otherwise as gdr_chunk_fwd (dt = GDR_BF16) and gdr_backward_chunked.
+ */
+gdr_status gdr_chunk_fwd_save(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              const float* S0, void* o, float* S_T, int B, int L, int Hk, int Hv, int D,
+                              gdr_dtype dt, void* saved, size_t saved_bytes, gdr_stream_t stream);
+gdr_status gdr_backward_chunked_saved(const void* q, const void* k, const void* v, const float* g,
+                                      const float* beta, const float* S0, const void* dO, const float* dS_T,
+                                      float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dS0, int B,
+                                      int L, int Hk, int Hv, int D, gdr_dtype dt, void* saved, size_t saved_bytes,
+                                      gdr_stream_t stream);
+
 /* Synchronise `stream`, then read and clear the sticky device error word of the current device. */
 gdr_status gdr_sync_status(gdr_stream_t stream);
 

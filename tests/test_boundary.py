@@ -305,3 +305,29 @@ def test_fused_prologue_rejects_bad_arguments_and_sizes_its_workspace(L):
     # rows longer than one chunk take the prefill's own workspace
     assert L.gdr_chunk_fwd_prologue_workspace_bytes(1, 4096, 16, 32, 128, 4) == \
         L.gdr_chunk_workspace_bytes(1, 4096, 16, 32, 128, 1)
+
+
+def test_saving_forward_and_saved_backward_reject_bad_arguments(L):
+    """gdr_chunk_fwd_save: bf16 only, a saved buffer of the chunked backward's workspace size clear of
+    every input and output; gdr_backward_chunked_saved: the chunked backward's checks."""
+    f = L.gdr_chunk_fwd_save
+    need = L.gdr_backward_chunked_workspace_bytes(1, 130, 2, 4, 128)
+    W = ctypes.c_void_p(1 << 32)   # far from P
+    args = lambda dt=1, saved=W, nbytes=need, o=P, q=P: (q, P, P, P, P, None, o, None, 1, 130, 2, 4, 128, dt, saved,
+                                                        nbytes, None)
+    assert f(*args(dt=0)) == gdr.GDR_ERR_UNSUPPORTED
+    assert f(*args(q=None)) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(saved=None)) == gdr.GDR_ERR_INVALID_ARG
+    assert f(*args(nbytes=need - 1)) == gdr.GDR_ERR_INVALID_ARG
+    assert b"saved" in L.gdr_last_error_message()
+    assert f(*args(saved=P)) == gdr.GDR_ERR_INVALID_ARG
+    assert b"overlaps" in L.gdr_last_error_message()
+    assert f(*args(saved=BAD)) == gdr.GDR_ERR_INVALID_ARG
+    b = L.gdr_backward_chunked_saved
+    bargs = lambda dt=1, dO=P, nbytes=need: (P, P, P, P, P, None, dO, None, W, ctypes.c_void_p((1 << 32) + (1 << 28)),
+                                             ctypes.c_void_p((1 << 32) + (2 << 28)), ctypes.c_void_p((1 << 32) + (3 << 28)),
+                                             ctypes.c_void_p((1 << 32) + (4 << 28)), None, 1, 130, 2, 4, 128, dt,
+                                             ctypes.c_void_p(1 << 34), nbytes, None)
+    assert b(*bargs(dt=0)) == gdr.GDR_ERR_UNSUPPORTED
+    assert b(*bargs(dO=None)) == gdr.GDR_ERR_INVALID_ARG
+    assert b(*bargs(nbytes=need - 1)) == gdr.GDR_ERR_INVALID_ARG
