@@ -114,6 +114,7 @@ __device__ __forceinline__ void tile_mma(float (&acc)[NT][4], const uint8_t* A, 
                                          int ldb, int n0, int K, int lane) {
   const uint16_t* a16 = reinterpret_cast<const uint16_t*>(A);
   const uint16_t* b16 = reinterpret_cast<const uint16_t*>(B);
+#pragma unroll 2   // (K is a multiple of 32: two steps' fragment loads overlap, and fewer registers spill)
   for (int k0 = 0; k0 < K; k0 += 16) {
     uint32_t af[4];
     if (!AT)
