@@ -1100,8 +1100,33 @@ chunk_state_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tm_do)
   __shared__ float nb_scl[8];
   __shared__ uint32_t nbmax[4];
 
-  const int sl = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int sl = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // With row lengths (up to 64 rows), the grid's z index is a rank: z runs the row with the z-th
+  // most chunks (ties by row index), so that CTAs, which launch in z order, start the longest chains
+  // first and the shorter rows fill the SMs around them. Every warp ranks the rows itself (a lane per
+  // row, a scan of the lengths); a length outside [0, L] counts as no chunks.
+  int b = blockIdx.z;
+  if (a.lengths && gridDim.z > 1 && gridDim.z <= 64) {
+    const int nrows = (int)gridDim.z;
+    auto nchunks = [&](int r) {
+      const int l = a.lengths[r];
+      return (l < 0 || l > a.L) ? 0 : (l + kChunk - 1) / kChunk;
+    };
+    int found = -1;
+    for (int r = lane; r < nrows; r += 32) {
+      const int nr = nchunks(r);
+      int rank = 0;
+      for (int q = 0; q < nrows; ++q) {
+        const int nq = nchunks(q);
+        rank += (nq > nr || (nq == nr && q < r)) ? 1 : 0;
+      }
+      if (rank == (int)blockIdx.z) found = r;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) found = max(found, __shfl_xor_sync(0xffffffffu, found, o));
+    b = found;   // (the ranks are a permutation of 0 .. nrows - 1: exactly one row has this one)
+  }
   // the row's valid tokens: chunks wholly past them are not run (the state there is final) and
   // output positions past them are not written; a length outside [0, L] skips the row
   const int len = a.lengths ? a.lengths[b] : a.L;
