@@ -89,7 +89,7 @@ def source_digest() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_deltanet_rule_gb300", "csrc")
-    for name in ("gdr_chunk.cu", "gdr_internal.h", "ptx.cuh"):
+    for name in ("gdr_chunk.cu", "gdr_internal.h", "gdr_inverse.cuh", "ptx.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
