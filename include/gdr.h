@@ -213,8 +213,9 @@ gdr_status gdr_prologue(const void* mixed, const void* tail, const float* conv_w
  * (DEG "model.py": _linear_layer, where _conv_silu and _dn_gates feed _delta_rule). The chunk
  * kernel forms each 64-token tile of q, k and v as the conv + SiLU of the projection rows (and the
  * carry) in gdr_prologue's own order of operations, one rounding to bfloat16, and each chunk's g and
- * beta from a and b the same way: o, S_T and new_tail equal those of the two separate calls bit for
- * bit.
+ * beta from a and b the same way: for rows longer than one chunk (L > 64) o, S_T and new_tail equal
+ * those of the two separate calls bit for bit; rows of one chunk take the two-kernel path (which
+ * gdr_chunk_fwd replaces by one kernel), equal within the bf16 tolerance, new_tail bit for bit.
  *   mixed, tail, conv_w, a, b, A_log, dt_bias, new_tail   as for gdr_prologue (conv_w [C, 4]; tail
  *                                   NULL = zeros, new_tail NULL = not written)
  *   S0, o, S_T                      as for gdr_chunk_fwd with dt = GDR_BF16 (o [B, L, Hv, D] bf16)
